@@ -1,0 +1,496 @@
+/*
+ * CPU oracle for the fused Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, call or
+ * load this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.  It shares no code, header, table or helper with the CUDA
+ * library; the two meet only through the seeded inputs.
+ *
+ * What it computes is the plain definition of the layer described on the
+ * fused-MoE pages ("AITER" walk-through, section 3 "Fused MoE": gating ->
+ * token reorder -> expert GEMMs -> weighted combine; the talk on group-GEMM
+ * MoE kernels for Mixtral with a SwiGLU activation):
+ *
+ *   per token t:  l_e  = x_t . W_router[e] (+ bias_e)           (router)
+ *                 ids  = the k largest l_e (ties -> lower e)     (top-k)
+ *                 w_j  = softmax over the k selected logits      (renormalised)
+ *                 for j: g = W_gate[e_j] x_t, u = W_up[e_j] x_t
+ *                        a = silu(g) * u,  y_j = W_down[e_j] a   (SwiGLU expert)
+ *                 out_t = sum_j w_j y_j   (j ascending)          (combine)
+ *
+ * plus the integer reorder ("moe_sorting" in section 3.1: tokens grouped by
+ * expert, each expert padded to whole blocks, buffer of T*k + E*B - k
+ * entries) and the per-128 block-scaled FP8 quantisation ("per_1x128").
+ *
+ * Precision: inputs are bf16 (or e4m3 codes with fp32 scales) taken exactly;
+ * every dot product of the expert GEMMs accumulates in fp64.  The router
+ * logits are the one place where floating point decides an integer (the
+ * expert ids), so they are taken in fp32 in one fixed summation order, the
+ * same order the GPU router uses (see oracle_router_logit).
+ *
+ * Every routine is a straight loop over the definition; the only parallelism
+ * is independent tokens split across POSIX threads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 */
+
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* ---------------------------------------------------------------- e4m3 */
+/*
+ * OCP 8-bit floating point, E4M3 ("fn" variant): 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 holds subnormals m/8 * 2^-6;
+ * the pattern S.1111.111 is NaN and there is no infinity, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int E = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (E == 15 && m == 7)
+        return NAN;
+    if (E == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* Round to nearest, ties to even, saturating to +-448 (no overflow to NaN). */
+uint8_t oracle_e4m3_encode(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest normal */
+        double q = nearbyint(a * 512.0); /* default mode: nearest, ties to even */
+        return sign | (uint8_t)q;
+    }
+    int e2;
+    double m = frexp(a, &e2); /* a = m * 2^e2, m in [0.5, 1) */
+    int E = e2 - 1;           /* a = (2m) * 2^E, 2m in [1, 2) */
+    double frac = nearbyint((2.0 * m - 1.0) * 8.0);
+    if (frac == 8.0) {
+        frac = 0.0;
+        E += 1;
+    }
+    if (E > 8)
+        return sign | 0x7E;
+    return sign | (uint8_t)(((E + 7) << 3) | (int)frac);
+}
+
+/* scale = amax / 448 in fp32 (1 when the group is all zero). */
+static float group_scale(float amax)
+{
+    if (!(amax > 0.0f))
+        return 1.0f;
+    return amax / 448.0f;
+}
+
+/*
+ * "per_1x128" activation quantisation: each row of X [R, C] is cut into
+ * groups of 128 columns; each group gets scale = amax/448 and codes
+ * e4m3(x / scale).  q [R, C] codes, s [R, C/128] fp32.
+ */
+void oracle_quant_1x128(const uint16_t *X, int R, int C, uint8_t *q, float *s)
+{
+    int G = C / 128;
+    for (int r = 0; r < R; ++r) {
+        for (int g = 0; g < G; ++g) {
+            float amax = 0.0f;
+            for (int c = g * 128; c < g * 128 + 128; ++c) {
+                float v = fabsf(bf16_to_float(X[(size_t)r * C + c]));
+                if (v > amax)
+                    amax = v;
+            }
+            float sc = group_scale(amax);
+            s[(size_t)r * G + g] = sc;
+            for (int c = g * 128; c < g * 128 + 128; ++c)
+                q[(size_t)r * C + c] = oracle_e4m3_encode(bf16_to_float(X[(size_t)r * C + c]) / sc);
+        }
+    }
+}
+
+/*
+ * Weight quantisation with one fp32 scale per 128x128 block of W [R, C]
+ * (rows = output features, columns = the reduction dim).  s [R/128, C/128].
+ */
+void oracle_quant_128x128(const uint16_t *W, long R, int C, uint8_t *q, float *s)
+{
+    int GC = C / 128;
+    long GR = R / 128;
+    for (long br = 0; br < GR; ++br) {
+        for (int bc = 0; bc < GC; ++bc) {
+            float amax = 0.0f;
+            for (long r = br * 128; r < br * 128 + 128; ++r)
+                for (int c = bc * 128; c < bc * 128 + 128; ++c) {
+                    float v = fabsf(bf16_to_float(W[r * C + c]));
+                    if (v > amax)
+                        amax = v;
+                }
+            float sc = group_scale(amax);
+            s[br * GC + bc] = sc;
+            for (long r = br * 128; r < br * 128 + 128; ++r)
+                for (int c = bc * 128; c < bc * 128 + 128; ++c)
+                    q[r * C + c] = oracle_e4m3_encode(bf16_to_float(W[r * C + c]) / sc);
+        }
+    }
+}
+
+/* -------------------------------------------------------------- router */
+/*
+ * Router logit in fp32, in one fixed order: the H products are dealt to 32
+ * partial sums in chunks of 8 consecutive elements (element h goes to
+ * partial (h / 8) mod 32), each partial adds its elements in ascending h,
+ * then the 32 partials are combined pairwise by a butterfly with strides
+ * 16, 8, 4, 2, 1 (partial i takes partial i + partial (i xor stride)).  A
+ * bf16 x bf16 product is exact in fp32, so only this order matters.  The
+ * bias (if any) is added last.
+ */
+float oracle_router_logit(const uint16_t *x, const uint16_t *w, int H, const float *bias, int e)
+{
+    float part[32];
+    for (int i = 0; i < 32; ++i)
+        part[i] = 0.0f;
+    for (int h = 0; h < H; ++h) {
+        float p = bf16_to_float(x[h]) * bf16_to_float(w[h]);
+        part[(h / 8) % 32] = part[(h / 8) % 32] + p;
+    }
+    for (int stride = 16; stride >= 1; stride /= 2) {
+        float nxt[32];
+        for (int i = 0; i < 32; ++i)
+            nxt[i] = part[i] + part[i ^ stride];
+        for (int i = 0; i < 32; ++i)
+            part[i] = nxt[i];
+    }
+    float l = part[0];
+    if (bias)
+        l = l + bias[e];
+    return l;
+}
+
+/*
+ * Top-k on the logits (largest first; an equal logit goes to the lower
+ * expert index), then softmax over the k selected logits, which is the same
+ * as softmax over all E followed by top-k and renormalisation.
+ */
+static void route_token(const float *logit, int E, int k, int32_t *ids, double *w)
+{
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            int taken = 0;
+            for (int i = 0; i < j; ++i)
+                if (ids[i] == e)
+                    taken = 1;
+            if (taken)
+                continue;
+            if (best < 0 || logit[e] > logit[best])
+                best = e;
+        }
+        ids[j] = best;
+    }
+    double lmax = logit[ids[0]];
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) {
+        w[j] = exp((double)logit[ids[j]] - lmax);
+        sum += w[j];
+    }
+    for (int j = 0; j < k; ++j)
+        w[j] /= sum;
+}
+
+typedef struct {
+    const uint16_t *x, *Wr;
+    const float *bias;
+    int T, H, E, k;
+    int32_t *ids;
+    double *w;
+    float *logits;
+    int t0, t1;
+} route_job;
+
+static void *route_worker(void *arg)
+{
+    route_job *J = (route_job *)arg;
+    float *l = (float *)malloc(sizeof(float) * J->E);
+    for (int t = J->t0; t < J->t1; ++t) {
+        for (int e = 0; e < J->E; ++e)
+            l[e] = oracle_router_logit(J->x + (size_t)t * J->H, J->Wr + (size_t)e * J->H, J->H, J->bias, e);
+        if (J->logits)
+            memcpy(J->logits + (size_t)t * J->E, l, sizeof(float) * J->E);
+        route_token(l, J->E, J->k, J->ids + (size_t)t * J->k, J->w + (size_t)t * J->k);
+    }
+    free(l);
+    return NULL;
+}
+
+static int clamp_threads(int nthreads, int work)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > work)
+        nthreads = work;
+    if (nthreads > 256)
+        nthreads = 256;
+    return nthreads < 1 ? 1 : nthreads;
+}
+
+/* ids [T,k] int32, w [T,k] fp64, logits [T,E] fp32 (nullable). */
+int oracle_route(const uint16_t *x, const uint16_t *Wr, const float *bias, int T, int H, int E, int k,
+                 int32_t *ids, double *w, float *logits, int nthreads)
+{
+    if (T <= 0)
+        return 0;
+    nthreads = clamp_threads(nthreads, T);
+    pthread_t th[256];
+    route_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        route_job J = {x, Wr, bias, T, H, E, k, ids, w, logits,
+                       (int)((long)T * i / nthreads), (int)((long)T * (i + 1) / nthreads)};
+        jobs[i] = J;
+        pthread_create(&th[i], NULL, route_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+    return 0;
+}
+
+/* ---------------------------------------------------------- align-sort */
+/*
+ * Reorder the T*k slots (slot s = t*k + j) by expert.  Expert e's segment
+ * holds its slots in ascending s, padded with the sentinel S = T*k up to a
+ * whole number of blocks of B rows; segments follow in ascending e; experts
+ * without slots get no block.  Buffers are sized as on the page:
+ * P_max = T*k + E*B - k entries and ceil(P_max / B) blocks.  Unused entries
+ * of sorted_ids hold S and unused block entries hold -1.
+ */
+int oracle_align_sort(const int32_t *ids, int T, int k, int E, int B, int32_t *sorted_ids,
+                      int32_t *sorted_expert_ids, int32_t *num_post_padded, int32_t *counts)
+{
+    long S = (long)T * k;
+    long P_max = S + (long)E * B - k;
+    long NB_max = (P_max + B - 1) / B;
+    for (long i = 0; i < P_max; ++i)
+        sorted_ids[i] = (int32_t)S;
+    for (long b = 0; b < NB_max; ++b)
+        sorted_expert_ids[b] = -1;
+    long pos = 0;
+    for (int e = 0; e < E; ++e) {
+        long cnt = 0;
+        for (long s = 0; s < S; ++s)
+            if (ids[s] == e)
+                sorted_ids[pos + cnt++] = (int32_t)s;
+        counts[e] = (int32_t)cnt;
+        long padded = (cnt + B - 1) / B * B;
+        for (long b = pos / B; b < (pos + padded) / B; ++b)
+            sorted_expert_ids[b] = e;
+        pos += padded;
+    }
+    *num_post_padded = (int32_t)pos;
+    return 0;
+}
+
+/* ------------------------------------------------------------ forward */
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+typedef struct {
+    int mode; /* 0 bf16, 1 fp8 */
+    const uint16_t *x, *Wr;
+    const float *bias;
+    const uint16_t *Wgu, *Wd;                /* bf16 weights */
+    const uint8_t *Wgu_q, *Wd_q;             /* e4m3 codes */
+    const float *w1s, *w2s;                  /* 128x128 block scales */
+    int T, H, I, E, k;
+    const int64_t *tokens;
+    int n0, n1;
+    double *out; /* [n, H] */
+} fwd_job;
+
+static void *fwd_worker(void *arg)
+{
+    fwd_job *J = (fwd_job *)arg;
+    int H = J->H, I = J->I, E = J->E, k = J->k;
+    float *l = (float *)malloc(sizeof(float) * E);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * k);
+    double *w = (double *)malloc(sizeof(double) * k);
+    double *xt = (double *)malloc(sizeof(double) * H);
+    double *a = (double *)malloc(sizeof(double) * I);
+    uint8_t *xq = (uint8_t *)malloc(H);
+    float *xs = (float *)malloc(sizeof(float) * (H / 128 + 1));
+    uint8_t *aq = (uint8_t *)malloc(I);
+    for (int n = J->n0; n < J->n1; ++n) {
+        long t = (long)J->tokens[n];
+        const uint16_t *xrow = J->x + t * H;
+        for (int e = 0; e < E; ++e)
+            l[e] = oracle_router_logit(xrow, J->Wr + (size_t)e * H, H, J->bias, e);
+        route_token(l, E, k, ids, w);
+        if (J->mode == 0) {
+            for (int h = 0; h < H; ++h)
+                xt[h] = bf16_to_float(xrow[h]);
+        } else {
+            oracle_quant_1x128(xrow, 1, H, xq, xs);
+            for (int h = 0; h < H; ++h)
+                xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[h / 128];
+        }
+        double *o = J->out + (size_t)n * H;
+        for (int h = 0; h < H; ++h)
+            o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[j];
+            for (int i = 0; i < I; ++i) {
+                double g = 0.0, u = 0.0;
+                size_t rg = ((size_t)e * 2 * I + i) * H;
+                size_t ru = ((size_t)e * 2 * I + I + i) * H;
+                if (J->mode == 0) {
+                    for (int h = 0; h < H; ++h) {
+                        g += (double)bf16_to_float(J->Wgu[rg + h]) * xt[h];
+                        u += (double)bf16_to_float(J->Wgu[ru + h]) * xt[h];
+                    }
+                } else {
+                    /* block (row/128, col/128) of the [E*2I, H] matrix */
+                    const float *sg = J->w1s + ((size_t)e * 2 * I + i) / 128 * (H / 128);
+                    const float *su = J->w1s + ((size_t)e * 2 * I + I + i) / 128 * (H / 128);
+                    for (int h = 0; h < H; ++h) {
+                        g += oracle_e4m3_decode(J->Wgu_q[rg + h]) * (double)sg[h / 128] * xt[h];
+                        u += oracle_e4m3_decode(J->Wgu_q[ru + h]) * (double)su[h / 128] * xt[h];
+                    }
+                }
+                a[i] = silu(g) * u;
+            }
+            if (J->mode == 1) {
+                /* the intermediate is re-quantised per 1x128 group before the
+                 * down projection (two-stage path, quantised between stages) */
+                for (int gi = 0; gi < I / 128; ++gi) {
+                    float amax = 0.0f;
+                    for (int i = gi * 128; i < gi * 128 + 128; ++i) {
+                        float v = fabsf((float)a[i]);
+                        if (v > amax)
+                            amax = v;
+                    }
+                    float sc = group_scale(amax);
+                    for (int i = gi * 128; i < gi * 128 + 128; ++i) {
+                        aq[i] = oracle_e4m3_encode((float)a[i] / sc);
+                        a[i] = oracle_e4m3_decode(aq[i]) * (double)sc;
+                    }
+                }
+            }
+            for (int h = 0; h < H; ++h) {
+                double y = 0.0;
+                size_t rd = ((size_t)e * H + h) * I;
+                if (J->mode == 0) {
+                    for (int i = 0; i < I; ++i)
+                        y += (double)bf16_to_float(J->Wd[rd + i]) * a[i];
+                } else {
+                    const float *sd = J->w2s + ((size_t)e * H + h) / 128 * (I / 128);
+                    for (int i = 0; i < I; ++i)
+                        y += oracle_e4m3_decode(J->Wd_q[rd + i]) * (double)sd[i / 128] * a[i];
+                }
+                o[h] += w[j] * y;
+            }
+        }
+    }
+    free(l);
+    free(ids);
+    free(w);
+    free(xt);
+    free(a);
+    free(xq);
+    free(xs);
+    free(aq);
+    return NULL;
+}
+
+static int run_forward(fwd_job proto, int n_tokens, int nthreads)
+{
+    if (n_tokens <= 0)
+        return 0;
+    nthreads = clamp_threads(nthreads, n_tokens);
+    pthread_t th[256];
+    fwd_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = proto;
+        jobs[i].n0 = (int)((long)n_tokens * i / nthreads);
+        jobs[i].n1 = (int)((long)n_tokens * (i + 1) / nthreads);
+        pthread_create(&th[i], NULL, fwd_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+    return 0;
+}
+
+/*
+ * bf16 layer: x [T,H], W_router [E,H], bias [E] (nullable),
+ * W_gate_up [E,2I,H] (gate rows first), W_down [E,H,I], all bf16 bits.
+ * Computes out[n,:] (fp64) for the tokens listed in tokens[0..n_tokens).
+ */
+int oracle_moe_forward_bf16(const uint16_t *x, const uint16_t *Wr, const float *bias, const uint16_t *Wgu,
+                            const uint16_t *Wd, int T, int H, int I, int E, int k, const int64_t *tokens,
+                            int n_tokens, double *out, int nthreads)
+{
+    fwd_job J;
+    memset(&J, 0, sizeof J);
+    J.mode = 0;
+    J.x = x;
+    J.Wr = Wr;
+    J.bias = bias;
+    J.Wgu = Wgu;
+    J.Wd = Wd;
+    J.T = T;
+    J.H = H;
+    J.I = I;
+    J.E = E;
+    J.k = k;
+    J.tokens = tokens;
+    J.out = out;
+    return run_forward(J, n_tokens, nthreads);
+}
+
+/*
+ * Block-scaled FP8 layer: the router runs on the bf16 activations; the
+ * expert GEMMs see x quantised per 1x128 group, weights as e4m3 codes with
+ * one fp32 scale per 128x128 block (w1s [E*2I/128, H/128], w2s [E*H/128,
+ * I/128]) and the SwiGLU output re-quantised per 1x128 group.  Products are
+ * of the dequantised values (code * scale), accumulated in fp64.
+ */
+int oracle_moe_forward_fp8(const uint16_t *x, const uint16_t *Wr, const float *bias, const uint8_t *Wgu_q,
+                           const float *w1s, const uint8_t *Wd_q, const float *w2s, int T, int H, int I, int E,
+                           int k, const int64_t *tokens, int n_tokens, double *out, int nthreads)
+{
+    fwd_job J;
+    memset(&J, 0, sizeof J);
+    J.mode = 1;
+    J.x = x;
+    J.Wr = Wr;
+    J.bias = bias;
+    J.Wgu_q = Wgu_q;
+    J.w1s = w1s;
+    J.Wd_q = Wd_q;
+    J.w2s = w2s;
+    J.T = T;
+    J.H = H;
+    J.I = I;
+    J.E = E;
+    J.k = k;
+    J.tokens = tokens;
+    J.out = out;
+    return run_forward(J, n_tokens, nthreads);
+}

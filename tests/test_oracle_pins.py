@@ -1,0 +1,397 @@
+"""Pins for the CPU oracle: each test ties the oracle to something other than
+itself -- values worked by hand from the pages' formulas, brute-force
+enumeration, an independent formulation (masked dense MoE), closed cases
+(E=1/k=1 is a plain SwiGLU MLP; k=E is a softmax mixture) evaluated with
+library routines, and PyTorch's own E4M3 encoder.  CPU only.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import heuristics
+from mixture_experts_grouped_moe_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _bf16_bits_of(values):
+    t = torch.tensor(values, dtype=torch.float32).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _f(bits):
+    """bf16 bits -> float64 values."""
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------------------ e4m3
+
+def test_e4m3_decode_known_values():
+    # OCP FP8 E4M3: bias 7, max finite 448, min normal 2^-6, min subnormal 2^-9, S.1111.111 = NaN
+    d = oracle.e4m3_decode(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x40, 0x7E, 0xFE, 0x80], np.uint8))
+    assert list(d) == [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 2.0, 448.0, -448.0, 0.0]
+    assert math.isnan(oracle.e4m3_decode(np.array([0x7F], np.uint8))[0])
+    assert math.isnan(oracle.e4m3_decode(np.array([0xFF], np.uint8))[0])
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_table()
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), ~finite)
+    assert np.array_equal(ours[finite], ref[finite])
+
+
+def test_e4m3_encode_roundtrip_and_midpoints():
+    tab = oracle.e4m3_table()
+    finite = [c for c in range(256) if not math.isnan(tab[c])]
+    enc = oracle.e4m3_encode(np.array([tab[c] for c in finite], np.float32))
+    assert list(enc) == finite  # includes -0 -> 0x80
+    # exact midpoints between neighbouring positive codes go to the even code
+    pos = [c for c in range(0x00, 0x7F)]
+    for a, b in zip(pos[:-1], pos[1:]):
+        mid = np.float32((tab[a] + tab[b]) / 2)
+        assert float(mid) == (tab[a] + tab[b]) / 2
+        got = int(oracle.e4m3_encode(np.array([mid], np.float32))[0])
+        assert got == (a if a % 2 == 0 else b), (a, b, got)
+    # saturation instead of NaN above 448
+    assert list(oracle.e4m3_encode(np.array([448, 460, 1e4, -1e30, np.inf], np.float32))) == \
+        [0x7E, 0x7E, 0x7E, 0xFE, 0x7E]
+
+
+def test_e4m3_encode_matches_torch_random():
+    rng = np.random.default_rng(0)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-12, 6, 20000))).astype(np.float32)
+    v = v[np.abs(v) < 448]
+    ours = oracle.e4m3_encode(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_quant_1x128_against_torch_encoder():
+    g = torch.Generator().manual_seed(3)
+    X = (torch.randn(7, 512, generator=g) * torch.exp(torch.randn(7, 1, generator=g) * 3)).to(torch.bfloat16)
+    X[2, 128:256] = 0  # an all-zero group takes scale 1
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    q, s = oracle.quant_1x128(bits)
+    xf = X.float().reshape(7, 4, 128)
+    amax = xf.abs().amax(-1)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert np.array_equal(s, sc.numpy())
+    ref = (xf / sc[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(7, 512).numpy()
+    assert np.array_equal(q, ref)
+    tab = oracle.e4m3_table()
+    for r in range(7):
+        for gi in range(4):
+            vals = np.abs(tab[q[r, gi * 128:(gi + 1) * 128]])
+            assert vals.max() == (0.0 if (r, gi) == (2, 1) else 448.0)
+
+
+def test_quant_128x128_block_scales():
+    g = torch.Generator().manual_seed(4)
+    W = (torch.randn(256, 384, generator=g) / 16).to(torch.bfloat16)
+    W[128:, 256:] *= 64
+    bits = W.view(torch.int16).numpy().view(np.uint16)
+    q, s = oracle.quant_128x128(bits)
+    assert s.shape == (2, 3)
+    Wf = W.float().reshape(2, 128, 3, 128).permute(0, 2, 1, 3)
+    amax = Wf.abs().amax((-1, -2))
+    assert np.array_equal(s, (amax / 448.0).numpy())
+    ref = (Wf / (amax / 448.0)[..., None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    ref = ref.permute(0, 2, 1, 3).reshape(256, 384).numpy()
+    assert np.array_equal(q, ref)
+
+
+# ---------------------------------------------------------------- router
+
+def test_router_order_hand_worked_cases():
+    for case, H, bias, expected, triples in _golden_rows("router_order.txt"):
+        H = int(H)
+        x = np.zeros(H, np.float32)
+        w = np.zeros(H, np.float32)
+        for t in triples.split(","):
+            h, xv, wv = t.split(":")
+            x[int(h)] = float(xv)
+            w[int(h)] = float(wv)
+        b = None if bias == "none" else np.array([float(bias)], np.float32)
+        got = oracle.router_logit(_bf16_bits_of(x), _bf16_bits_of(w), b, 0)
+        assert got == np.float32(float(expected)), (case, got, expected)
+
+
+def test_router_logit_within_fp32_bound_of_exact():
+    g = torch.Generator().manual_seed(5)
+    for H in (8, 128, 1000, 4096, 7168):
+        x = torch.randn(H, generator=g).to(torch.bfloat16)
+        w = (torch.randn(H, generator=g) / math.sqrt(H)).to(torch.bfloat16)
+        xb, wb = x.view(torch.int16).numpy().view(np.uint16), w.view(torch.int16).numpy().view(np.uint16)
+        got = float(oracle.router_logit(xb, wb))
+        prod = _f(xb) * _f(wb)
+        exact = prod.sum()
+        # each partial adds at most ceil(H/256)*8 terms, then 5 butterfly levels
+        depth = 8 * -(-H // 256) + 5
+        bound = depth * 2.0 ** -24 * np.abs(prod).sum() * 1.01
+        assert abs(got - exact) <= bound
+
+
+def test_route_topk_against_fp64_softmax_topk_renorm():
+    cfg = synth.CONFIGS["tiny"].with_(T=64, E=6, k=3)
+    inp = synth.make_inputs(cfg, seed=1, weights=False)
+    xb, wb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    ids, w, logits = oracle.route(xb, wb, None, cfg.k)
+    # independent formulation: exact logits, softmax over all E, top-k, renormalise
+    L = _f(xb) @ _f(wb).T
+    P = np.exp(L - L.max(1, keepdims=True))
+    P /= P.sum(1, keepdims=True)
+    for t in range(cfg.T):
+        order = sorted(range(cfg.E), key=lambda e: (-L[t, e], e))
+        gaps = np.abs(np.diff(np.sort(L[t])[::-1][:cfg.k + 1]))
+        if gaps.min() < 1e-5:
+            continue  # near-tie: fp32 vs exact may legitimately differ
+        assert list(ids[t]) == order[:cfg.k]
+        ref = P[t, ids[t]] / P[t, ids[t]].sum()
+        np.testing.assert_allclose(w[t], ref, rtol=1e-6)
+        assert abs(w[t].sum() - 1.0) < 1e-12
+        assert np.all(np.diff(w[t]) <= 0)
+    # returned logits are the fixed-order fp32 values
+    for t in (0, 7):
+        for e in range(cfg.E):
+            assert logits[t, e] == oracle.router_logit(xb[t], wb[e])
+
+
+def test_route_ties_go_to_lower_expert():
+    H = 64
+    x = np.ones((2, H), np.float32)
+    W = np.zeros((4, H), np.float32)
+    W[1] = W[2] = 0.5   # experts 1 and 2 tie for the top logit
+    W[3] = 0.25
+    ids, w, _ = oracle.route(_bf16_bits_of(x), _bf16_bits_of(W), None, 3)
+    assert list(ids[0]) == [1, 2, 3]
+    assert w[0, 0] == w[0, 1]
+    # a bias breaks the tie and changes the weights too
+    ids, w, _ = oracle.route(_bf16_bits_of(x), _bf16_bits_of(W), np.array([0, 0, 1, 0], np.float32), 2)
+    assert list(ids[0]) == [2, 1]
+    np.testing.assert_allclose(w[0], [1 / (1 + math.exp(-1)), math.exp(-1) / (1 + math.exp(-1))], rtol=1e-12)
+
+
+# ------------------------------------------------------------ align-sort
+
+def test_align_sort_sizes_golden():
+    for T, k, E, B, P, NB in _golden_rows("align_sort_sizes.txt"):
+        assert oracle.align_sort_sizes(int(T), int(k), int(E), int(B)) == (int(P), int(NB))
+
+
+def _sort_by_definition(ids, E, B):
+    """Stable grouping of slots by expert with per-expert padding, from Python's sorted()."""
+    T, k = ids.shape
+    S = T * k
+    slots = sorted(range(S), key=lambda s: (ids.flat[s], s))
+    P, NB = oracle.align_sort_sizes(T, k, E, B)
+    out, eids = [], []
+    for e in range(E):
+        seg = [s for s in slots if ids.flat[s] == e]
+        pad = -(-len(seg) // B) * B
+        out += seg + [S] * (pad - len(seg))
+        eids += [e] * (pad // B)
+    n = len(out)
+    return np.array(out + [S] * (P - n), np.int32), np.array(eids + [-1] * (NB - len(eids)), np.int32), n
+
+
+def test_align_sort_brute_force_all_small_routings():
+    n_cases = 0
+    for E in (1, 2, 3):
+        for k in range(1, E + 1):
+            choices = list(itertools.permutations(range(E), k))
+            for T in (1, 2, 3):
+                for routing in itertools.product(choices, repeat=T):
+                    ids = np.array(routing, np.int32).reshape(T, k)
+                    for B in (1, 2, 3, 4):
+                        si, se, npp, cnt = oracle.align_sort(ids, E, B)
+                        ri, re_, rn = _sort_by_definition(ids, E, B)
+                        assert np.array_equal(si, ri) and np.array_equal(se, re_) and npp == rn
+                        assert list(cnt) == [int((ids == e).sum()) for e in range(E)]
+                        n_cases += 1
+    assert n_cases > 1000
+
+
+def check_sort_invariants(ids, E, B, sorted_ids, sorted_eids, npp, counts):
+    """Properties any correct align-sort output has (used for oracle and GPU)."""
+    T, k = ids.shape
+    S = T * k
+    P, NB = oracle.align_sort_sizes(T, k, E, B)
+    assert sorted_ids.shape == (P,) and sorted_eids.shape == (NB,)
+    assert counts.sum() == S
+    assert npp % B == 0 and npp <= P
+    real = sorted_ids[sorted_ids != S]
+    assert np.array_equal(np.sort(real), np.arange(S))
+    assert np.all(sorted_ids[npp:] == S)
+    used = sorted_eids[: npp // B]
+    assert np.all(np.diff(used) >= 0)
+    assert np.all(sorted_eids[npp // B:] == -1)
+    pos = 0
+    for e in range(E):
+        c = int(counts[e])
+        pad = -(-c // B) * B
+        seg = sorted_ids[pos:pos + pad]
+        assert np.all(ids.flat[seg[:c]] == e)
+        assert np.all(np.diff(seg[:c]) > 0)
+        assert np.all(seg[c:] == S)
+        assert np.all(sorted_eids[pos // B:(pos + pad) // B] == e)
+        pos += pad
+    assert pos == npp
+
+
+def test_align_sort_invariants_random():
+    rng = np.random.default_rng(7)
+    for T, k, E, B in [(100, 2, 8, 16), (33, 8, 256, 128), (4096, 8, 64, 64), (5, 1, 1, 128)]:
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+        si, se, npp, cnt = oracle.align_sort(ids, E, B)
+        check_sort_invariants(ids, E, B, si, se, npp, cnt)
+
+
+# --------------------------------------------------------------- forward
+
+def _dense_masked_reference(inp, k):
+    """Masked dense MoE (every expert evaluated, weighted by the routing mask): the
+    formulation the group-GEMM talk says grouped GEMMs replace.  fp64 numpy."""
+    x = _f(synth.bf16_bits(inp["x"]))
+    Wr = _f(synth.bf16_bits(inp["W_router"]))
+    Wgu = _f(synth.bf16_bits(inp["W_gate_up"]))
+    Wd = _f(synth.bf16_bits(inp["W_down"]))
+    E, twoI, H = Wgu.shape
+    I = twoI // 2
+    ids, w, _ = oracle.route(synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"]),
+                             None if inp["bias"] is None else inp["bias"].numpy(), k)
+    mask = np.zeros((x.shape[0], E))
+    for t in range(x.shape[0]):
+        mask[t, ids[t]] = w[t]
+    out = np.zeros_like(x)
+    for e in range(E):
+        g = x @ Wgu[e, :I].T
+        u = x @ Wgu[e, I:].T
+        a = g / (1 + np.exp(-g)) * u
+        out += mask[:, e:e + 1] * (a @ Wd[e].T)
+    return out
+
+
+def _oracle_bf16(inp, k, tokens=None):
+    b = None if inp["bias"] is None else inp["bias"].numpy()
+    return oracle.moe_forward_bf16(synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"]), b,
+                                   synth.bf16_bits(inp["W_gate_up"]), synth.bf16_bits(inp["W_down"]), k, tokens)
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+@pytest.mark.parametrize("T,E,k,bias", [(16, 4, 2, None), (1, 1, 1, None), (3, 2, 2, "normal"),
+                                        (17, 5, 2, "normal"), (9, 5, 5, None)])
+def test_forward_equals_masked_dense(T, E, k, bias):
+    cfg = synth.CONFIGS["tiny"].with_(T=T, E=E, k=k, bias=bias, bias_param=0.5)
+    inp = synth.make_inputs(cfg, seed=2)
+    assert _rel(_oracle_bf16(inp, k), _dense_masked_reference(inp, k)) < 1e-12
+
+
+def test_forward_e1_k1_is_plain_swiglu_mlp():
+    cfg = synth.CONFIGS["tiny"].with_(T=12, E=1, k=1)
+    inp = synth.make_inputs(cfg, seed=3)
+    x = inp["x"].double()
+    Wg, Wu = inp["W_gate_up"][0, :cfg.I].double(), inp["W_gate_up"][0, cfg.I:].double()
+    Wd = inp["W_down"][0].double()
+    ref = torch.nn.functional.linear(torch.nn.functional.silu(x @ Wg.T) * (x @ Wu.T), Wd)
+    assert _rel(_oracle_bf16(inp, 1), ref.numpy()) < 1e-12
+
+
+def test_forward_k_equals_e_is_softmax_mixture():
+    cfg = synth.CONFIGS["tiny"].with_(T=10, E=3, k=3)
+    inp = synth.make_inputs(cfg, seed=4)
+    x = inp["x"].double()
+    logits = x @ inp["W_router"].double().T
+    p = torch.softmax(logits, -1)
+    ref = torch.zeros_like(x)
+    for e in range(3):
+        Wg, Wu = inp["W_gate_up"][e, :cfg.I].double(), inp["W_gate_up"][e, cfg.I:].double()
+        ref += p[:, e:e + 1] * (torch.nn.functional.silu(x @ Wg.T) * (x @ Wu.T)) @ inp["W_down"][e].double().T
+    assert _rel(_oracle_bf16(inp, 3), ref.numpy()) < 1e-6  # logits fp32 vs fp64 only
+
+
+def test_forward_unused_expert_weights_never_read():
+    cfg = synth.CONFIGS["tiny"].with_(T=8, E=6, k=2)
+    inp = synth.make_inputs(cfg, seed=5)
+    ids, _, _ = oracle.route(synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"]), None, 2)
+    unused = sorted(set(range(6)) - set(ids.ravel().tolist()))
+    assert unused, "seed should leave an expert without tokens"
+    ref = _oracle_bf16(inp, 2)
+    for e in unused:
+        inp["W_gate_up"][e] = float("nan")
+        inp["W_down"][e] = float("nan")
+    got = _oracle_bf16(inp, 2)
+    assert np.array_equal(got, ref)
+
+
+def test_forward_token_permutation_and_subset():
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_inputs(cfg, seed=6)
+    full = _oracle_bf16(inp, 2)
+    perm = torch.randperm(cfg.T, generator=torch.Generator().manual_seed(0))
+    inp2 = dict(inp, x=inp["x"][perm].contiguous())
+    assert np.array_equal(_oracle_bf16(inp2, 2), full[perm.numpy()])
+    sub = np.array([0, 5, 15], np.int64)
+    assert np.array_equal(_oracle_bf16(inp, 2, sub), full[sub])
+
+
+def test_forward_fp8_against_dense_dequantised_reference():
+    """FP8 path vs an independent dense formulation: torch's e4m3 encoder for
+    the 1x128 re-quantisation of the SwiGLU output, numpy matmuls."""
+    cfg = synth.CONFIGS["tiny"].with_(T=6, H=256, I=256, E=3, k=2)
+    inp = synth.make_inputs(cfg, seed=7)
+    xb, wrb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    qgu, s1 = oracle.quant_128x128(synth.bf16_bits(inp["W_gate_up"]))
+    qd, s2 = oracle.quant_128x128(synth.bf16_bits(inp["W_down"]))
+    got = oracle.moe_forward_fp8(xb, wrb, None, qgu, s1, qd, s2, cfg.k)
+
+    tab = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    Wgu = tab[qgu] * np.repeat(np.repeat(s1, 128, 0), 128, 1).reshape(qgu.shape)
+    Wd = tab[qd] * np.repeat(np.repeat(s2, 128, 0), 128, 1).reshape(qd.shape)
+    xq, xs = oracle.quant_1x128(xb)
+    x = tab[xq] * np.repeat(xs, 128, 1)
+    ids, w, _ = oracle.route(xb, wrb, None, cfg.k)
+    ref = np.zeros((cfg.T, cfg.H))
+    I = cfg.I
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            e = ids[t, j]
+            g, u = Wgu[e, :I] @ x[t], Wgu[e, I:] @ x[t]
+            a = torch.from_numpy(g / (1 + np.exp(-g)) * u).float().reshape(-1, 128)
+            amax = a.abs().amax(-1, keepdim=True)
+            sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+            aq = (a / sc).clamp(-448, 448).to(torch.float8_e4m3fn).double() * sc.double()
+            ref[t] += w[t, j] * (Wd[e] @ aq.reshape(-1).numpy())
+    assert _rel(got, ref) < 1e-12
+
+
+# ------------------------------------------------------------ heuristics
+
+def test_heuristics_golden():
+    for kind, token, topk, expert, inter, model, units, bm, expected in _golden_rows("heuristics.txt"):
+        token, topk, expert, inter, model, units, bm, expected = map(
+            int, (token, topk, expert, inter, model, units, bm, expected))
+        if kind == "bsm":
+            assert heuristics.block_size_m(token, topk, expert, inter, units) == expected
+        else:
+            assert heuristics.ksplit(token, topk, expert, inter, model, units, bm) == expected
