@@ -1,0 +1,415 @@
+"""Benchmark of the fused MoE layer on GB300 (one JSON line on stdout).
+
+Default workload: Mixtral-8x7B MoE decode (T=32 tokens, H=4096, I=14336,
+E=8 experts, top-2, bf16 weights/activations, fp32 accumulation).  A step is
+one whole forward of the layer (route, sort, gather, stage-1 and stage-2
+group GEMMs, combine) through the C ABI on device-resident inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the layer is independent per token: weak scaling, no collective on the data
+path); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE TFLOP/s & HBM GB/s per shape on 1 GB300; % of roofline; tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["route", "sort", "gather", "stage1", "stage2", "combine"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_grouped_moe_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d.get(workload, {}).get(kernel)
+        if not ent or ent.get("source_hash") != kernel_source_hash():
+            return None
+        return ent["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def algorithmic_counts(cfg, counts, dtype_bytes):
+    """FLOPs and bytes of the layer from the actual routing (counts per expert)."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    S = T * k
+    flops = 2.0 * S * 3 * H * I + 2.0 * T * H * E
+    active = int(sum(1 for c in counts if c > 0))
+    scale_bytes = 0
+    if dtype_bytes == 1:
+        scale_bytes = active * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+    bytes_ = active * 3 * H * I * dtype_bytes + scale_bytes + T * H * 2 + T * H * 2 + E * H * 2
+    s1_bytes = active * 2 * I * H * dtype_bytes
+    s2_bytes = active * H * I * dtype_bytes
+    return flops, bytes_, active, s1_bytes, s2_bytes
+
+
+def run_cuda(args, cfg, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from mixture_experts_grouped_moe_gb300 import build as moe_build
+    from mixture_experts_grouped_moe_gb300 import moe, synth
+
+    moe_build.build()
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_kind = load_peaks()
+    fp8 = cfg.dtype == "fp8"
+    dtype = moe.MOE_FP8_BLOCK128 if fp8 else moe.MOE_BF16
+
+    inp = synth.make_inputs(cfg, seed=0, device=dev)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"]}
+    if fp8:
+        E, I, H = cfg.E, cfg.I, cfg.H
+        q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        s1 = torch.empty(E * 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        q2 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        s2 = torch.empty(E * H // 128, I // 128, dtype=torch.float32, device=dev)
+        moe.moe_quantize_fp8_weights(inp["W_gate_up"], E * 2 * I, H, q1, s1)
+        moe.moe_quantize_fp8_weights(inp["W_down"], E * H, I, q2, s2)
+        w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
+    else:
+        w.update(W_gate_up=inp["W_gate_up"], W_down=inp["W_down"])
+    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, host_staging=True)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    # per-step events: 7 stage marks per step
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        layer(inp["x"], w, out)
+    torch.cuda.synchronize()
+    if layer.status() != moe.MOE_OK:
+        raise RuntimeError("device wait timed out during warm-up")
+    counts = layer.view("expert_counts", torch.int32, (cfg.E,)).cpu().numpy().tolist()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.15)
+    start.record(stream)
+    for i in range(K):
+        moe.moe_set_stage_events(ev[i])
+        layer(inp["x"], w, out)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms_total = start.elapsed_time(stop)
+    stage_ms = {s: 0.0 for s in STAGES}
+    for i in range(K):
+        for j, s in enumerate(STAGES):
+            stage_ms[s] += ev[i][j].elapsed_time(ev[i][j + 1])
+    stage_ms = {s: v / K for s, v in stage_ms.items()}
+
+    # end to end: host (pinned) x in, host out back, through the C-ABI host entry
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(3, W // 4)):
+        layer.forward_host(x_host, w, out_host)
+    torch.cuda.synchronize()
+    K2 = max(1, K // 2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        layer.forward_host(x_host, w, out_host)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K2
+    assert np.isfinite(out_host.float().numpy()).all()
+
+    ms = ms_total / K
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    return dict(ms=ms, e2e_ms=e2e_ms, stage_ms=stage_ms, counts=counts, clocks=clocks, peaks=peaks,
+                peak_kind=peak_kind, plan=layer.plan, K=K, W=W)
+
+
+def cpu_baseline(cfg, host, budget_s=20.0):
+    """The oracle as it stands on this host's cores, on a bounded token sample."""
+    import numpy as np
+
+    import oracle
+    from mixture_experts_grouped_moe_gb300 import synth
+
+    n = max(1, min(cfg.T, oracle.default_threads()))
+    toks = synth.token_sample(cfg.T, n).numpy()
+    t0 = time.perf_counter()
+    run_oracle(cfg, host, toks)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while time.perf_counter() - t0 < min(budget_s, 3 * dt + 1e-9) and n * (reps + 1) <= 4 * cfg.T and dt * (reps + 1) < budget_s:
+        run_oracle(cfg, host, toks)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{n} of the {cfg.T} tokens, full layer per token (fp64 CPU oracle), {reps} run(s)"}
+
+
+def run_oracle(cfg, host, toks):
+    import oracle
+    if cfg.dtype == "fp8":
+        return oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
+                                      host["q2"], host["s2"], cfg.k, toks)
+    return oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
+                                   cfg.k, toks)
+
+
+def host_inputs(cfg, device):
+    import torch
+
+    import oracle
+    from mixture_experts_grouped_moe_gb300 import synth
+    inp = synth.make_inputs(cfg, seed=0, device=device)
+    host = {k: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+            for k, v in inp.items()}
+    if cfg.dtype == "fp8":
+        host["q1"], host["s1"] = oracle.quant_128x128(host["W_gate_up"])
+        host["q2"], host["s2"] = oracle.quant_128x128(host["W_down"])
+    return host
+
+
+def workload_desc(cfg):
+    d = {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k} SwiGLU"
+                     + (" block-scaled FP8 e4m3" if cfg.dtype == "fp8" else " bf16")
+                     + ("" if cfg.bias is None else f" router bias {cfg.bias}({cfg.bias_param})"),
+         "tokens_per_step": cfg.T, "seq_len": 1 if cfg.T <= 128 else cfg.T}
+    return d
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default="mixtral_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from mixture_experts_grouped_moe_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, cfg)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    r = run_cuda(args, cfg, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], 1 if cfg.dtype == "fp8" else 2)
+    peaks = r["peaks"]
+    ms = r["ms"]
+    tokens_s = world * cfg.T / (ms * 1e-3)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = bytes_ / (ms * 1e-3) / 1e9
+    peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    if cfg.dtype == "fp8":
+        peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)
+    t_roof = max(flops / (peak_t * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9))
+    memory_bound = bytes_ / (peaks["hbm_gbs"] * 1e9) >= flops / (peak_t * 1e12)
+    # dominant kernel: stage 1 (gate/up group GEMM)
+    s1_ms = r["stage_ms"]["stage1"]
+    T, H, I = cfg.T, cfg.H, cfg.I
+    npp_rows = sum(-(-c // r["plan"].block_m) * r["plan"].block_m for c in r["counts"])
+    eb = 1 if cfg.dtype == "fp8" else 2
+    if memory_bound:
+        s1_alg = s1_bytes + npp_rows * H * eb + npp_rows * I * eb
+        achieved = s1_alg / (s1_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": "stage1 gate/up group GEMM (swap-AB)",
+                "alg_bytes_per_launch": s1_alg}
+    else:
+        s1_flops = 2.0 * cfg.S * 2 * H * I
+        achieved = s1_flops / (s1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_t, "unit": "TFLOP/s",
+                "frac": round(achieved / peak_t, 4), "kernel": "stage1 gate/up group GEMM",
+                "alg_flops_per_launch": s1_flops}
+    roof["peak_source"] = r["peak_kind"]
+    roof["traffic"] = profiled_traffic(cfg.name, "stage1")
+    roof["kernel_ms"] = round(s1_ms, 5)
+    line = {
+        "metric": METRIC, "value": round(tokens_s, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": r["K"], "warmup": r["W"], "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3/fp32-acc" if cfg.dtype == "fp8" else "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights; random init, no checkpoint)",
+        "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}",
+                       l2="inputs larger than L2 (expert weights streamed every step)"),
+        "tflops": round(tflops, 2), "hbm_gbs": round(gbs, 1),
+        "layer_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof / (ms * 1e-3), 4),
+                           "bound": "hbm" if memory_bound else "tensor", "alg_bytes": bytes_, "alg_flops": flops,
+                           "active_experts": active},
+        "stage_ms": {k: round(v, 5) for k, v in r["stage_ms"].items()},
+        "roofline": roof,
+        "gpu_launches": 8 * r["K"],
+        "clocks": r["clocks"],
+        "e2e": {"value": round(world * cfg.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+                "ms_per_step": round(r["e2e_ms"], 5)},
+        "plan": {"mode": "swap" if r["plan"].mode == 1 else "grouped", "block_m": r["plan"].block_m,
+                 "split_k2": r["plan"].split_k2},
+    }
+    if not args.no_cpu_baseline and world == 1 or (world > 1 and rank == 0 and not args.no_cpu_baseline):
+        import torch
+        host = host_inputs(cfg, torch.device("cuda", local_rank))
+        line["cpu_baseline"] = cpu_baseline(cfg, host)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, cfg):
+    """The CPU oracle as the reference arm: each step runs the layer on a bounded token sample."""
+    import torch
+
+    import oracle
+    from mixture_experts_grouped_moe_gb300 import synth
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    host = host_inputs(cfg, dev)
+    nthr = oracle.default_threads()
+    n = max(1, min(cfg.T, nthr))
+    toks = synth.token_sample(cfg.T, n).numpy()
+    t0 = time.perf_counter()
+    run_oracle(cfg, host, toks)
+    t_step = time.perf_counter() - t0
+    budget = 150.0
+    if (args.steps + args.warmup) * t_step > budget:
+        n = 1  # smallest sample: one token per step
+        toks = toks[:1]
+    for _ in range(args.warmup):
+        run_oracle(cfg, host, toks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle(cfg, host, toks)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+            "data": "synthetic", "config": dict(workload_desc(cfg), parallelism="host cores"),
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": nthr, "kind": "oracle",
+                             "sample": f"{n} token(s) of the {cfg.T}-token batch per step"},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

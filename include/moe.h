@@ -1,0 +1,255 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer.
+ *
+ * The layer is the fused MoE of the AITER walk-through (section 3, "Fused
+ * MoE": gating -> token reorder by expert -> expert GEMMs -> weighted
+ * combine) built as the two-stage group-GEMM path of the FlyDSL/Mixtral talk
+ * (group GEMMs in place of masked dense GEMMs, SwiGLU activation):
+ *
+ *   route:   logits = x W_router^T (+ bias), top-k per token, softmax over
+ *            the k selected logits (the weights sum to 1)
+ *   sort:    the T*k (token, slot) pairs grouped by expert, each expert
+ *            padded to whole blocks of block_m rows (section 3.1)
+ *   stage 1: per block, gathered rows of x times W_gate_up[e]^T, then
+ *            h = silu(gate) * up                              (section 3.2)
+ *   stage 2: h times W_down[e]^T, each row scaled by its top-k weight
+ *   combine: out[t] = sum over j of the weighted rows of token t
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked (device) are CUDA device pointers, (host) are host
+ *    pointers.  All matrices are row-major and contiguous.  bf16 is IEEE
+ *    bfloat16 bits in a uint16; e4m3 is the OCP FP8 E4M3 byte.
+ *  - Weight layouts: W_router [E][H]; W_gate_up [E][2I][H] with rows 0..I-1
+ *    the gate projection and rows I..2I-1 the up projection; W_down [E][H][I]
+ *    (each expert matrix is N x K with K contiguous).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on it: no host synchronisation, no
+ *    allocation, no exceptions; results are ready when the stream is.
+ *  - The caller owns every buffer.  The library keeps only per-device
+ *    constants (SM count, kernel attributes).
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns a negative status and launches nothing.  A CUDA
+ *    launch error returns MOE_ERR_CUDA.  Kernels that wait on barriers give
+ *    up after a bounded time and record MOE_ERR_TIMEOUT in the workspace
+ *    status word (read it with moe_workspace_status).
+ *
+ * Limits: 1 <= k <= min(E, 32); E <= 1024; H and I multiples of 128;
+ * T >= 0 (T = 0 is a no-op that returns MOE_OK).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)
+#define MOE_ERR_UNSUPPORTED (-2)
+#define MOE_ERR_WORKSPACE (-3)
+#define MOE_ERR_CUDA (-4)
+#define MOE_ERR_TIMEOUT (-5)
+
+#define MOE_BF16 0          /* bf16 weights and activations, fp32 accumulation */
+#define MOE_FP8_BLOCK128 1  /* e4m3 weights (fp32 scale per 128x128 block) and
+                               activations (fp32 scale per 1x128 group) */
+
+#define MOE_MODE_GROUPED 0  /* tokens on the MMA M side, 128-row blocks */
+#define MOE_MODE_SWAP 1     /* weights on the MMA M side, tokens on N (small T) */
+
+/* Text for a status code.  Never NULL. */
+const char *moe_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+/*
+ * Sizes of the align-sort outputs (AITER page, section 3.1):
+ * max_padded = T*k + E*block_m - k entries of sorted_ids / sorted_weights,
+ * max_blocks = ceil(max_padded / block_m) entries of sorted_expert_ids.
+ * Host only.  Returns MOE_OK or MOE_ERR_INVALID_ARG.
+ */
+int moe_align_sort_sizes(int T, int k, int E, int block_m, int64_t *max_padded, int64_t *max_blocks);
+
+/*
+ * The block-size rule of the AITER page (section 3.3, get_block_size_M):
+ * among `candidates` (n entries), the block size with the fewest rounds of
+ * ceil(inter_dim/128) * ceil(max_padded/BM) tiles over `units` compute
+ * units, then the fewest idle units in the last round.  Host only; returns
+ * the chosen block size or a negative status.
+ */
+int moe_block_size_m_heuristic(int token, int topk, int expert, int inter_dim, int units,
+                               const int *candidates, int n);
+
+/*
+ * The K-split rule of the AITER page (section 3.4, get_ksplit), with the
+ * page's undefined tgN/tgM read as ceil(inter_dim/128) and
+ * ceil(token*topk/block_m).  Returns the split (0 = none) or a negative
+ * status.  Host only.
+ */
+int moe_ksplit_heuristic(int token, int topk, int expert, int inter_dim, int model_dim, int units,
+                         int block_m);
+
+/* The plan moe_fused_forward follows for a shape. */
+typedef struct moe_plan {
+    int mode;           /* MOE_MODE_GROUPED or MOE_MODE_SWAP */
+    int block_m;        /* sort block size (rows per padded expert block) */
+    int split_k1;       /* K splits of stage 1 (1 = none) */
+    int split_k2;       /* K splits of stage 2 (1 = none) */
+    int64_t max_padded; /* T*k + E*block_m - k */
+    int64_t max_blocks; /* ceil(max_padded / block_m) */
+    size_t workspace_bytes;
+} moe_plan_t;
+
+/*
+ * Choose mode, block size and K splits for a layer shape.  block_m = 0 and
+ * split_k = 0 mean automatic; otherwise they are used as given (block_m
+ * must be 128 in grouped mode and a multiple of 16 up to 128 in swap mode;
+ * split_k splits stage 2's K = I and must divide I/64).  num_sms = 0 asks
+ * the current CUDA device; a positive value plans for that many SMs without
+ * touching CUDA.  Returns MOE_OK or a negative status.  Host only.
+ */
+int moe_plan(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k, int num_sms,
+             moe_plan_t *plan);
+
+/*
+ * Workspace bytes moe_fused_forward needs for this shape (the plan's
+ * workspace_bytes, planned for the current device).  0 on invalid input.
+ */
+size_t moe_fused_workspace_size(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k);
+
+/*
+ * Byte offsets of the intermediate buffers inside the workspace of
+ * moe_fused_forward (for inspection and tests; -1 = not present).
+ */
+typedef struct moe_ws_layout {
+    int64_t status;          /* int32 status word (MOE_OK or MOE_ERR_TIMEOUT) */
+    int64_t topk_ids;        /* int32 [T][k] */
+    int64_t topk_weights;    /* fp32 [T][k] */
+    int64_t sorted_ids;      /* int32 [max_padded] */
+    int64_t sorted_weights;  /* fp32 [max_padded] */
+    int64_t sorted_expert_ids; /* int32 [max_blocks] */
+    int64_t num_tokens_post_padded; /* int32 [1] */
+    int64_t expert_counts;   /* int32 [E] */
+    int64_t x_sorted;        /* bf16 [max_padded][H] or e4m3 [max_padded][H] */
+    int64_t x_scales;        /* fp32 [H/128][max_padded] (FP8 only) */
+    int64_t inter;           /* bf16 [max_padded][I] or e4m3 [max_padded][I] */
+    int64_t inter_scales;    /* fp32 [I/128][max_padded] (FP8 only) */
+    int64_t y;               /* fp32 [T*k][H], weighted rows in slot order */
+    int64_t total;
+} moe_ws_layout_t;
+
+int moe_workspace_layout(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k,
+                         moe_ws_layout_t *layout);
+
+/*
+ * Read the workspace status word (device) into *status (host).  Synchronises
+ * `stream`.  Returns MOE_OK or MOE_ERR_CUDA.
+ */
+int moe_workspace_status(const void *ws, int *status, void *stream);
+
+/*
+ * Router (gating + top-k; AITER page section 3, FlyDSL talk "Mixtral"):
+ *   logit[t][e] = sum_h x[t][h] * W_router[e][h]  (+ bias[e])
+ * in fp32 in one fixed order -- the H products are dealt to 32 partial sums
+ * in chunks of 8 elements (element h to partial (h/8) mod 32), each partial
+ * adds in ascending h, then the partials are combined by a butterfly with
+ * strides 16, 8, 4, 2, 1 -- so the ids are a deterministic function of the
+ * bytes.  topk_ids[t] = the k largest logits, largest first, an equal logit
+ * going to the lower expert; topk_weights[t][j] = exp(l_j - l_0) / sum.
+ *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H];
+ *   bias (device) fp32 [E] or NULL; topk_ids (device) int32 [T][k];
+ *   topk_weights (device) fp32 [T][k]; logits (device) fp32 [T][E] or NULL.
+ */
+int moe_route_topk(const void *x, const void *W_router, const float *bias, int T, int H, int E, int k,
+                   int32_t *topk_ids, float *topk_weights, float *logits, void *stream);
+
+/* Scratch bytes moe_align_sort needs (device memory passed as ws). */
+size_t moe_align_sort_workspace_size(int T, int k, int E);
+
+/*
+ * Token sort and alignment by expert (AITER page section 3.1, moe_sorting):
+ * slot s = t*k + j.  Expert e's segment lists its slots in ascending s and
+ * is padded with the sentinel T*k up to a multiple of block_m; segments
+ * follow in ascending e; experts without slots take no block.
+ *   topk_ids (device) int32 [T][k]; topk_weights (device) fp32 [T][k];
+ *   sorted_ids (device) int32 [max_padded]: slot or T*k (padding / unused);
+ *   sorted_weights (device) fp32 [max_padded]: topk weight of the slot, 0 on padding;
+ *   sorted_expert_ids (device) int32 [max_blocks]: expert of each block, -1 if unused;
+ *   num_tokens_post_padded (device) int32 [1]: sum of the padded segment lengths;
+ *   expert_counts (device) int32 [E] or NULL: slots per expert;
+ *   ws (device) scratch of moe_align_sort_workspace_size bytes.
+ * Ids outside [0, E) are a caller error and are not checked on the device.
+ */
+int moe_align_sort(const int32_t *topk_ids, const float *topk_weights, int T, int k, int E, int block_m,
+                   int32_t *sorted_ids, float *sorted_weights, int32_t *sorted_expert_ids,
+                   int32_t *num_tokens_post_padded, int32_t *expert_counts, void *ws, size_t ws_bytes,
+                   void *stream);
+
+/*
+ * Block-scaled FP8 quantisation ("per_1x128" on the AITER page):
+ * activations per 1x128 group of a row, weights per 128x128 block; each
+ * group takes scale = amax / 448 (1 for an all-zero group) and codes
+ * e4m3(v / scale), rounded to nearest even and saturated to +-448.
+ *   moe_quantize_fp8_act: X (device) bf16 [R][C], C % 128 == 0 ->
+ *     q (device) e4m3 [R][C], s (device) fp32 [R][C/128].
+ *   moe_quantize_fp8_weights: W (device) bf16 [R][C], R and C % 128 == 0
+ *     (an expert stack [E][N][K] is R = E*N, C = K) ->
+ *     q (device) e4m3 [R][C], s (device) fp32 [R/128][C/128].
+ */
+int moe_quantize_fp8_act(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream);
+int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float *s, void *stream);
+
+/*
+ * The whole layer: route, align-sort, stage 1 (gate/up group GEMM with the
+ * SwiGLU epilogue), stage 2 (down group GEMM scaled by the top-k weights),
+ * combine.  out (device) bf16 [T][H].
+ *   dtype MOE_BF16: W_gate_up / W_down (device) bf16; w1_scale, w2_scale NULL.
+ *   dtype MOE_FP8_BLOCK128: W_gate_up / W_down (device) e4m3 with
+ *     w1_scale (device) fp32 [E*2I/128][H/128] and w2_scale (device) fp32
+ *     [E*H/128][I/128] (as produced by moe_quantize_fp8_weights); x is
+ *     quantised per 1x128 group inside the call, the router runs on bf16 x,
+ *     and the SwiGLU output is re-quantised per 1x128 group between stages.
+ *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H]; router_bias
+ *   (device) fp32 [E] or NULL; block_m / split_k as in moe_plan;
+ *   ws (device) of at least moe_fused_workspace_size bytes, 1024-byte aligned.
+ * The result is deterministic: no atomics touch floating-point data.
+ */
+int moe_fused_forward(int dtype, const void *x, const void *W_router, const float *router_bias,
+                      const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                      int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/*
+ * moe_fused_forward with the activations in host memory: x_host (host) bf16
+ * [T][H] is copied to the device inside the call and the result is copied
+ * back to out_host (host) bf16 [T][H], all on `stream` (pinned host memory
+ * keeps the copies asynchronous).  Device staging lives in ws, which must
+ * hold moe_fused_workspace_size(...) + moe_host_staging_bytes(T, H) bytes.
+ * out_host is valid once the stream has completed.
+ */
+size_t moe_host_staging_bytes(int T, int H);
+int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, const float *router_bias,
+                           const void *W_gate_up, const float *w1_scale, const void *W_down,
+                           const float *w2_scale, int T, int H, int I, int E, int k, int block_m,
+                           int split_k, void *out_host, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Optional per-stage timing for the next moe_fused_forward (or _host) call
+ * made by the calling host thread: `events` (host array of n >= 7 CUDA
+ * events, cudaEvent_t cast to void*, created by the caller) are recorded on
+ * the call's stream at [0] entry, [1] after routing, [2] after the sort,
+ * [3] after the gather (FP8: gather + quantise), [4] after stage 1, [5]
+ * after stage 2, [6] after the combine.  One call consumes the setting;
+ * events = NULL clears it.  Returns MOE_OK or MOE_ERR_INVALID_ARG.
+ */
+int moe_set_stage_events(void *const *events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,616 @@
+// C ABI of the fused MoE layer (declared in include/moe.h): argument
+// validation, the host planner (mode, block size, K split, workspace
+// carve-up), TMA descriptor encoding, and the launch sequence
+//   route -> align-sort -> gather (FP8: gather + 1x128 quantise) ->
+//   stage-1 group GEMM -> stage-2 group GEMM -> combine
+// on the caller's stream.  Nothing here allocates device memory or
+// synchronises (except moe_workspace_status, which reads one word back).
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int64_t kAlign = 1024;
+
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows)
+{
+    auto fn = get_encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms_current_device()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Workspace carve-up (byte offsets from ws).
+struct Layout {
+    int64_t status, topk_ids, topk_w, sort_scratch, counts, offsets, active, num_active, npp;
+    int64_t sorted_ids, sorted_w, sorted_eids, slot_pos;
+    int64_t x_sorted, x_scales, inter, inter_scales, y, partials;
+    int64_t total;
+};
+
+static int validate_shape(int dtype, int T, int H, int I, int E, int k)
+{
+    if (dtype != MOE_BF16 && dtype != MOE_FP8_BLOCK128)
+        return MOE_ERR_INVALID_ARG;
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > E || k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (H % 128 != 0 || I % 128 != 0)
+        return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)E * 2 * I > (int64_t)1 << 30 ||
+        (int64_t)E * H > (int64_t)1 << 30 || H > (1 << 20) || I > (1 << 20))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const moe_plan_t &p)
+{
+    Layout L;
+    const int64_t S = (int64_t)T * k;
+    const int64_t P = p.max_padded, NB = p.max_blocks;
+    const int64_t eb = (dtype == MOE_BF16) ? 2 : 1;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t o = off;
+        off = align_up(off + (bytes > 0 ? bytes : 0), kAlign);
+        return o;
+    };
+    L.status = take(16);
+    L.topk_ids = take(S * 4);
+    L.topk_w = take(S * 4);
+    L.sort_scratch = take((int64_t)sort_scratch_bytes(T, k, E));
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.active = take(E * 4);
+    L.num_active = take(4);
+    L.npp = take(4);
+    L.sorted_ids = take(P * 4);
+    L.sorted_w = take(P * 4);
+    L.sorted_eids = take(NB * 4);
+    L.slot_pos = take(S * 4);
+    L.x_sorted = take(P * H * eb);
+    L.x_scales = (dtype == MOE_FP8_BLOCK128) ? take((H / 128) * P * 4) : -1;
+    L.inter = take(P * I * eb);
+    L.inter_scales = (dtype == MOE_FP8_BLOCK128) ? take((I / 128) * P * 4) : -1;
+    if (p.split_k2 > 1) {
+        L.y = -1;
+        L.partials = take((int64_t)p.split_k2 * P * H * 4);
+    } else {
+        L.y = take(S * H * 4);
+        L.partials = -1;
+    }
+    L.total = off;
+    return L;
+}
+
+static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k, int num_sms,
+                     moe_plan_t *plan)
+{
+    int st = validate_shape(dtype, T, H, I, E, k);
+    if (st != MOE_OK)
+        return st;
+    if (!plan || block_m < 0 || split_k < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        num_sms = num_sms_current_device();
+        if (num_sms <= 0)
+            return MOE_ERR_CUDA;
+    }
+    moe_plan_t p;
+    memset(&p, 0, sizeof p);
+    // Swap (weights on the MMA M side) while every expert segment fits one
+    // N <= 128 tile, i.e. T <= 128; FP8 always runs the grouped kernel.
+    p.mode = (dtype == MOE_BF16 && T <= 128) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
+    if (block_m == 0)
+        block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
+    if (p.mode == MOE_MODE_GROUPED && block_m != 128)
+        return MOE_ERR_UNSUPPORTED;
+    if (p.mode == MOE_MODE_SWAP && (block_m % 16 != 0 || block_m > 128))
+        return MOE_ERR_UNSUPPORTED;
+    p.block_m = block_m;
+    p.split_k1 = 1;
+    const int kblocks2 = I / 64;
+    if (p.mode == MOE_MODE_SWAP) {
+        if (split_k == 0) {
+            // Enough stage-2 tiles for ~4 per SM: the smallest divisor of I/64 that reaches it.
+            const int64_t e_act = (int64_t)((T * k < E) ? T * k : E);
+            const int64_t tiles = e_act * ((H + 255) / 256);
+            split_k = 1;
+            if (tiles < 4LL * num_sms) {
+                for (int d = 2; d <= 16 && d <= kblocks2; ++d)
+                    if (kblocks2 % d == 0) {
+                        split_k = d;
+                        if (tiles * d >= 4LL * num_sms)
+                            break;
+                    }
+            }
+        } else if (kblocks2 % split_k != 0) {
+            return MOE_ERR_UNSUPPORTED;
+        }
+        p.split_k2 = split_k;
+    } else {
+        if (split_k > 1)
+            return MOE_ERR_UNSUPPORTED;
+        p.split_k2 = 1;
+    }
+    p.max_padded = (int64_t)T * k + (int64_t)E * block_m - k;
+    p.max_blocks = (p.max_padded + block_m - 1) / block_m;
+    p.workspace_bytes = (size_t)make_layout(dtype, T, H, I, E, k, p).total;
+    *plan = p;
+    return MOE_OK;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Per-stage timing events of the next forward call on this host thread.
+static thread_local cudaEvent_t t_stage_events[7];
+static thread_local bool t_stage_armed = false;
+
+static void mark(int i, cudaStream_t st)
+{
+    if (t_stage_armed)
+        cudaEventRecord(t_stage_events[i], st);
+}
+
+static int forward_impl(int dtype, const void *x, const void *W_router, const float *router_bias,
+                        const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                        int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
+                        size_t ws_bytes, cudaStream_t st)
+{
+    int rc = validate_shape(dtype, T, H, I, E, k);
+    if (rc != MOE_OK)
+        return rc;
+    if (!x || !W_router || !W_gate_up || !W_down || !out || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (dtype == MOE_FP8_BLOCK128 && (!w1_scale || !w2_scale))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W_router, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) ||
+        !aligned(out, 16) || !aligned(ws, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return MOE_OK;
+    moe_plan_t p;
+    rc = plan_impl(dtype, T, H, I, E, k, block_m, split_k, 0, &p);
+    if (rc != MOE_OK)
+        return rc;
+    if (ws_bytes < p.workspace_bytes)
+        return MOE_ERR_WORKSPACE;
+    const Layout L = make_layout(dtype, T, H, I, E, k, p);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    auto at = [&](int64_t off) -> void * { return off < 0 ? nullptr : (void *)(w + off); };
+    const int S = T * k;
+    const int nsm = num_sms_current_device();
+
+    int *status = static_cast<int *>(at(L.status));
+    mark(0, st);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    int32_t *topk_ids = static_cast<int32_t *>(at(L.topk_ids));
+    float *topk_w = static_cast<float *>(at(L.topk_w));
+    launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router), router_bias,
+                  T, H, E, k, topk_ids, topk_w, nullptr, st);
+    mark(1, st);
+
+    SortOut so;
+    so.sorted_ids = static_cast<int32_t *>(at(L.sorted_ids));
+    so.sorted_weights = static_cast<float *>(at(L.sorted_w));
+    so.sorted_expert_ids = static_cast<int32_t *>(at(L.sorted_eids));
+    so.num_post_padded = static_cast<int32_t *>(at(L.npp));
+    so.expert_counts = static_cast<int32_t *>(at(L.counts));
+    so.expert_offsets = static_cast<int32_t *>(at(L.offsets));
+    so.active_experts = static_cast<int32_t *>(at(L.active));
+    so.num_active = static_cast<int32_t *>(at(L.num_active));
+    so.slot_pos = static_cast<int32_t *>(at(L.slot_pos));
+    launch_align_sort(topk_ids, topk_w, T, k, E, p.block_m, so, at(L.sort_scratch), st);
+    mark(2, st);
+
+    const int64_t P = p.max_padded;
+    const int eb = (dtype == MOE_BF16) ? 2 : 1;
+    if (dtype == MOE_BF16)
+        launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
+                           static_cast<__nv_bfloat16 *>(at(L.x_sorted)), st);
+    else
+        launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k,
+                                 H, P, static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
+                                 st);
+    if (cudaGetLastError() != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(3, st);
+
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    g.sorted_ids = so.sorted_ids;
+    g.sorted_weights = so.sorted_weights;
+    g.sorted_expert_ids = so.sorted_expert_ids;
+    g.num_post_padded = so.num_post_padded;
+    g.expert_offsets = so.expert_offsets;
+    g.active_experts = so.active_experts;
+    g.num_active = so.num_active;
+    g.expert_counts = so.expert_counts;
+    g.S = S;
+    g.E = E;
+    g.P_max = P;
+    g.status = status;
+    const uint32_t box_inner = (uint32_t)(128 / eb);  // one 128-byte swizzle row
+    const uint32_t box_x_rows = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
+
+    // ---------------------------------------------------------- stage 1
+    GemmArgs g1 = g;
+    if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H, P, box_inner, box_x_rows) ||
+        !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H, (uint64_t)E * 2 * I, box_inner, 128))
+        return MOE_ERR_CUDA;
+    g1.K = H;
+    g1.N = I;
+    g1.rows_per_expert = 2 * I;
+    g1.split_k = 1;
+    g1.inter = at(L.inter);
+    g1.x_scales = static_cast<float *>(at(L.x_scales));
+    g1.w_scales = w1_scale;
+    g1.inter_scales = static_cast<float *>(at(L.inter_scales));
+    cudaError_t ce;
+    if (p.mode == MOE_MODE_SWAP) {
+        const int64_t ub = (int64_t)((S < E) ? S : E) * (I / 128);
+        ce = launch_gemm_swap_bf16(1, g1, (int)(ub < nsm ? ub : nsm), st);
+    } else {
+        const int64_t ub = p.max_blocks * (I / 128);
+        ce = (dtype == MOE_BF16) ? launch_gemm_grouped_bf16(1, g1, (int)(ub < nsm ? ub : nsm), st)
+                                 : launch_gemm_grouped_fp8(1, g1, (int)(ub < nsm ? ub : nsm), st);
+    }
+    if (ce != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(4, st);
+
+    // ---------------------------------------------------------- stage 2
+    GemmArgs g2 = g;
+    if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I, P, box_inner, box_x_rows) ||
+        !encode_tmap_2d(&g2.tm_w, W_down, eb, I, (uint64_t)E * H, box_inner, 128))
+        return MOE_ERR_CUDA;
+    g2.K = I;
+    g2.N = H;
+    g2.rows_per_expert = H;
+    g2.split_k = p.split_k2;
+    g2.x_scales = static_cast<float *>(at(L.inter_scales));
+    g2.w_scales = w2_scale;
+    g2.y = static_cast<float *>(at(L.y));
+    g2.partials = static_cast<float *>(at(L.partials));
+    const int nt2 = (H + 255) / 256;
+    if (p.mode == MOE_MODE_SWAP) {
+        const int64_t ub = (int64_t)((S < E) ? S : E) * nt2 * p.split_k2;
+        ce = launch_gemm_swap_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st);
+    } else {
+        const int64_t ub = p.max_blocks * nt2;
+        ce = (dtype == MOE_BF16) ? launch_gemm_grouped_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st)
+                                 : launch_gemm_grouped_fp8(2, g2, (int)(ub < nsm ? ub : nsm), st);
+    }
+    if (ce != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(5, st);
+
+    // ----------------------------------------------------------- combine
+    if (p.split_k2 > 1)
+        launch_splitk_combine(g2.partials, p.split_k2, P, so.slot_pos, topk_w, T, k, H,
+                              static_cast<__nv_bfloat16 *>(out), st);
+    else
+        launch_combine(g2.y, T, k, H, static_cast<__nv_bfloat16 *>(out), st);
+    mark(6, st);
+    t_stage_armed = false;
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_set_stage_events(void *const *events, int n)
+{
+    if (!events) {
+        t_stage_armed = false;
+        return MOE_OK;
+    }
+    if (n < 7)
+        return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 7; ++i) {
+        if (!events[i])
+            return MOE_ERR_INVALID_ARG;
+        t_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    t_stage_armed = true;
+    return MOE_OK;
+}
+
+int moe_align_sort_sizes(int T, int k, int E, int block_m, int64_t *max_padded, int64_t *max_blocks)
+{
+    if (T < 0 || k <= 0 || E <= 0 || block_m <= 0 || !max_padded || !max_blocks)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t p = (int64_t)T * k + (int64_t)E * block_m - k;
+    *max_padded = p;
+    *max_blocks = (p + block_m - 1) / block_m;
+    return MOE_OK;
+}
+
+int moe_block_size_m_heuristic(int token, int topk, int expert, int inter_dim, int units, const int *candidates,
+                               int n)
+{
+    if (token < 0 || topk <= 0 || expert <= 0 || inter_dim <= 0 || units <= 0 || !candidates || n <= 0)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t tgN = (inter_dim + 127) / 128;
+    int best = -1;
+    int64_t best_r = 0, best_idle = 0;
+    for (int i = 0; i < n; ++i) {
+        const int bm = candidates[i];
+        if (bm <= 0)
+            return MOE_ERR_INVALID_ARG;
+        const int64_t padded = (int64_t)token * topk + (int64_t)expert * bm - topk;
+        const int64_t tiles = tgN * ((padded + bm - 1) / bm);
+        const int64_t rounds = (tiles + units - 1) / units;
+        const int64_t idle = units - tiles % units;
+        if (best < 0 || rounds < best_r || (rounds == best_r && idle < best_idle) ||
+            (rounds == best_r && idle == best_idle && bm < best)) {
+            best = bm;
+            best_r = rounds;
+            best_idle = idle;
+        }
+    }
+    return best;
+}
+
+int moe_ksplit_heuristic(int token, int topk, int expert, int inter_dim, int model_dim, int units, int block_m)
+{
+    if (token < 0 || topk <= 0 || expert <= 0 || inter_dim <= 0 || model_dim <= 0 || units <= 0 || block_m <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if ((int64_t)token * topk > expert)
+        return 0;
+    const int64_t tgN = (inter_dim + 127) / 128;
+    const int64_t tgM = ((int64_t)token * topk + block_m - 1) / block_m;
+    const int64_t tiles = tgN * tgM;
+    if (tiles >= units || tiles == 0)
+        return 0;
+    const int64_t split_max = (units + tiles - 1) / tiles;
+    for (int64_t i = split_max; i >= 2; --i)
+        if (model_dim % i == 0 && (model_dim / i) % 256 == 0)
+            return (int)i;
+    return 0;
+}
+
+int moe_plan(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k, int num_sms, moe_plan_t *plan)
+{
+    return plan_impl(dtype, T, H, I, E, k, block_m, split_k, num_sms, plan);
+}
+
+size_t moe_fused_workspace_size(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k)
+{
+    moe_plan_t p;
+    if (plan_impl(dtype, T, H, I, E, k, block_m, split_k, 0, &p) != MOE_OK)
+        return 0;
+    return p.workspace_bytes;
+}
+
+int moe_workspace_layout(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k,
+                         moe_ws_layout_t *out)
+{
+    if (!out)
+        return MOE_ERR_INVALID_ARG;
+    moe_plan_t p;
+    int rc = plan_impl(dtype, T, H, I, E, k, block_m, split_k, 0, &p);
+    if (rc != MOE_OK)
+        return rc;
+    const Layout L = make_layout(dtype, T, H, I, E, k, p);
+    out->status = L.status;
+    out->topk_ids = L.topk_ids;
+    out->topk_weights = L.topk_w;
+    out->sorted_ids = L.sorted_ids;
+    out->sorted_weights = L.sorted_w;
+    out->sorted_expert_ids = L.sorted_eids;
+    out->num_tokens_post_padded = L.npp;
+    out->expert_counts = L.counts;
+    out->x_sorted = L.x_sorted;
+    out->x_scales = L.x_scales;
+    out->inter = L.inter;
+    out->inter_scales = L.inter_scales;
+    out->y = L.y;
+    out->total = L.total;
+    return MOE_OK;
+}
+
+int moe_workspace_status(const void *ws, int *status, void *stream)
+{
+    if (!ws || !status)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *status = v;
+    return MOE_OK;
+}
+
+int moe_route_topk(const void *x, const void *W_router, const float *bias, int T, int H, int E, int k,
+                   int32_t *topk_ids, float *topk_weights, float *logits, void *stream)
+{
+    if (T < 0 || H <= 0 || H % 8 != 0 || E <= 0 || k <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > E || k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !W_router || !topk_ids || !topk_weights || !aligned(x, 16) || !aligned(W_router, 16))
+        return MOE_ERR_INVALID_ARG;
+    launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router), bias, T, H,
+                  E, k, topk_ids, topk_weights, logits, static_cast<cudaStream_t>(stream));
+    return cuda_status(cudaGetLastError());
+}
+
+size_t moe_align_sort_workspace_size(int T, int k, int E)
+{
+    if (T < 0 || k <= 0 || E <= 0)
+        return 0;
+    return (size_t)align_up((int64_t)sort_scratch_bytes(T, k, E), kAlign) + (size_t)(E + 1) * 4;
+}
+
+int moe_align_sort(const int32_t *topk_ids, const float *topk_weights, int T, int k, int E, int block_m,
+                   int32_t *sorted_ids, float *sorted_weights, int32_t *sorted_expert_ids,
+                   int32_t *num_tokens_post_padded, int32_t *expert_counts, void *ws, size_t ws_bytes, void *stream)
+{
+    if (T < 0 || k <= 0 || E <= 0 || block_m <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > E)
+        return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)T * k > (int64_t)1 << 30)
+        return MOE_ERR_UNSUPPORTED;
+    if (!topk_ids || !topk_weights || !sorted_ids || !sorted_weights || !sorted_expert_ids ||
+        !num_tokens_post_padded || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_align_sort_workspace_size(T, k, E))
+        return MOE_ERR_WORKSPACE;
+    SortOut so;
+    memset(&so, 0, sizeof so);
+    so.sorted_ids = sorted_ids;
+    so.sorted_weights = sorted_weights;
+    so.sorted_expert_ids = sorted_expert_ids;
+    so.num_post_padded = num_tokens_post_padded;
+    so.expert_counts = expert_counts;
+    so.expert_offsets = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) +
+                                                    align_up((int64_t)sort_scratch_bytes(T, k, E), kAlign));
+    launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, ws, static_cast<cudaStream_t>(stream));
+    return cuda_status(cudaGetLastError());
+}
+
+int moe_quantize_fp8_act(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream)
+{
+    if (R < 0 || C <= 0 || C % 128 != 0 || !X || !q || !s || !aligned(X, 16) || !aligned(q, 8))
+        return MOE_ERR_INVALID_ARG;
+    launch_quant_act(static_cast<const __nv_bfloat16 *>(X), R, C, q, s, static_cast<cudaStream_t>(stream));
+    return cuda_status(cudaGetLastError());
+}
+
+int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float *s, void *stream)
+{
+    if (R < 0 || R % 128 != 0 || C <= 0 || C % 128 != 0 || R / 128 > 65535 || !W || !q || !s || !aligned(W, 16) ||
+        !aligned(q, 8))
+        return MOE_ERR_INVALID_ARG;
+    launch_quant_weights(static_cast<const __nv_bfloat16 *>(W), R, C, q, s, static_cast<cudaStream_t>(stream));
+    return cuda_status(cudaGetLastError());
+}
+
+int moe_fused_forward(int dtype, const void *x, const void *W_router, const float *router_bias,
+                      const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale, int T,
+                      int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws, size_t ws_bytes,
+                      void *stream)
+{
+    return forward_impl(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
+                        block_m, split_k, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_host_staging_bytes(int T, int H)
+{
+    if (T < 0 || H <= 0)
+        return 0;
+    return (size_t)align_up((int64_t)T * H * 2, kAlign) * 2;
+}
+
+int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, const float *router_bias,
+                           const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                           int T, int H, int I, int E, int k, int block_m, int split_k, void *out_host, void *ws,
+                           size_t ws_bytes, void *stream)
+{
+    int rc = validate_shape(dtype, T, H, I, E, k);
+    if (rc != MOE_OK)
+        return rc;
+    if (!x_host || !out_host || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return MOE_OK;
+    const size_t need = moe_fused_workspace_size(dtype, T, H, I, E, k, block_m, split_k);
+    if (need == 0)
+        return MOE_ERR_INVALID_ARG;
+    const size_t stage = moe_host_staging_bytes(T, H);
+    if (ws_bytes < need + stage)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws) + need;
+    void *x_dev = base;
+    void *out_dev = base + stage / 2;
+    const size_t bytes = (size_t)T * H * 2;
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    rc = forward_impl(dtype, x_dev, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
+                      block_m, split_k, out_dev, ws, need, st);
+    if (rc != MOE_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // extern "C"

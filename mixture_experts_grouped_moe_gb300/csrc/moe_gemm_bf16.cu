@@ -1,0 +1,441 @@
+// Stage-1 and stage-2 group GEMMs of the fused MoE layer, bf16 inputs with
+// fp32 accumulation in tensor memory, on the sm_100-family tensor core
+// (tcgen05) fed by TMA.
+//
+// The two stages are the "2-stage" path of the AITER walk-through
+// (section 3.2: stage 1 = gate/up projection + activation, stage 2 = down
+// projection) run as group GEMMs over the blocks produced by the token sort
+// (section 3.1), as in the Mixtral group-GEMM talk (group GEMMs in place of
+// masked dense GEMMs; SwiGLU).  Each block of sorted rows belongs to one
+// expert, so a tile is a dense GEMM against that expert's weights.
+//
+// Design (one CTA per SM, persistent, warp-specialised):
+//   warp 0      TMA producer: weight tile (256 rows x 64 K) and token tile
+//               (up to 128 rows x 64 K) per pipeline stage, 128-byte swizzle
+//   warp 1      TMEM allocator and MMA issuer (one thread); tcgen05.commit
+//               frees a stage when its MMAs finish, and signals a finished
+//               accumulator to the epilogue
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31), fused SwiGLU (stage 1) or top-k weight
+//               scaling (stage 2), stores to global memory
+// Two 256-column fp32 accumulators in TMEM let the epilogue of one tile
+// overlap the main loop of the next.
+//
+// Two tile shapes:
+//   grouped (large T): M = 128 sorted token rows, N = 256 weight rows.
+//     Stage 1's 256 weight rows are 128 gate rows and the matching 128 up
+//     rows, so accumulator columns j and 128+j pair up for SwiGLU inside one
+//     thread.  Stage 2's are 256 rows of W_down (256 output features).
+//   swap (small T, decode): the weights take the MMA's M side.  A tile is
+//     one expert's whole padded token segment (N = 16..128 tokens) against
+//     256 weight rows issued as two M = 128 MMAs (stage 1: gate rows and the
+//     matching up rows; stage 2: two halves of 256 output features), so
+//     every weight byte of an active expert is streamed exactly once.
+//     Stage 2 may split K (= I) across CTAs; the partial sums then go to a
+//     workspace and a separate pass reduces them in a fixed order.
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace bf16gemm {
+
+constexpr int kBK = 64;                     // K elements per stage (128 bytes)
+constexpr int kStages = 4;
+constexpr int kWRows = 256;
+constexpr int kXRows = 128;
+constexpr int kWBytes = kWRows * 128;       // 32 KiB
+constexpr int kXBytes = kXRows * 128;       // 16 KiB
+constexpr int kStageBytes = kWBytes + kXBytes;
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 16;                 // raster: 16 M-blocks share each weight tile in turn
+
+struct __align__(1024) Smem {
+    uint8_t stage[kStages][kStageBytes];    // [W tile | X tile] per stage, 1024-byte aligned
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct Tile {
+    int valid;
+    int e;          // expert
+    int xrow;       // first token row (sorted position)
+    int nx;         // token rows (grouped: 128; swap: padded segment length)
+    int wrow0;      // first weight row of W-tile half 0
+    int wrow1;      // first weight row of W-tile half 1
+    int ncol0;      // output column base (stage 1: h column; stage 2: output feature)
+    int kb0, kb1;   // K-block range
+    int ks;         // K split index (swap stage 2)
+};
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int MODE, int STAGE>
+__device__ __forceinline__ int num_tiles(const GemmArgs &a)
+{
+    if (MODE == MOE_MODE_GROUPED) {
+        const int nmb = *a.num_post_padded / 128;
+        const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+        return nmb * nnt;
+    } else {
+        const int nact = *a.num_active;
+        const int nwt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+        return nact * nwt * a.split_k;
+    }
+}
+
+template <int MODE, int STAGE>
+__device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t)
+{
+    Tile tl;
+    tl.valid = 1;
+    const int nkb = a.K / kBK;
+    if (MODE == MOE_MODE_GROUPED) {
+        const int nmb = *a.num_post_padded / 128;
+        const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+        const int group = t / (kGroupM * nnt);
+        const int within = t - group * kGroupM * nnt;
+        const int gsize = min(kGroupM, nmb - group * kGroupM);
+        const int nt = within / gsize;
+        const int mb = group * kGroupM + within % gsize;
+        tl.e = a.sorted_expert_ids[mb];
+        tl.xrow = mb * 128;
+        tl.nx = 128;
+        if (STAGE == 1) {
+            tl.wrow0 = tl.e * a.rows_per_expert + nt * 128;          // gate rows
+            tl.wrow1 = tl.e * a.rows_per_expert + a.N + nt * 128;    // matching up rows
+            tl.ncol0 = nt * 128;
+        } else {
+            tl.wrow0 = tl.e * a.rows_per_expert + nt * 256;
+            tl.wrow1 = tl.wrow0 + 128;
+            tl.ncol0 = nt * 256;
+        }
+        tl.kb0 = 0;
+        tl.kb1 = nkb;
+        tl.ks = 0;
+    } else {
+        const int nact = *a.num_active;
+        const int nwt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+        const int ai = t % nact;
+        const int r = t / nact;
+        const int wt = r % nwt;
+        const int ks = r / nwt;
+        tl.e = a.active_experts[ai];
+        tl.xrow = a.expert_offsets[tl.e];
+        tl.nx = a.expert_offsets[tl.e + 1] - tl.xrow;
+        if (STAGE == 1) {
+            tl.wrow0 = tl.e * a.rows_per_expert + wt * 128;
+            tl.wrow1 = tl.e * a.rows_per_expert + a.N + wt * 128;
+            tl.ncol0 = wt * 128;
+        } else {
+            tl.wrow0 = tl.e * a.rows_per_expert + wt * 256;
+            tl.wrow1 = tl.wrow0 + 128;
+            tl.ncol0 = wt * 256;
+        }
+        const int per = nkb / a.split_k;
+        tl.kb0 = ks * per;
+        tl.kb1 = tl.kb0 + per;
+        tl.ks = ks;
+    }
+    return tl;
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&h)[32])
+{
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 p = __floats2bfloat162_rn(h[q * 8 + 2 * i], h[q * 8 + 2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&p);
+        }
+        d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int MODE, int STAGE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 4);
+        }
+        mbar_init(&sm.drain, 1);
+        sm.abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&a.tm_x);
+        tma_prefetch_desc(&a.tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    const int ntiles = num_tiles<MODE, STAGE>(a);
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            int issued[kStages];
+            uint32_t issued_ph[kStages];
+            for (int i = 0; i < kStages; ++i)
+                issued[i] = 0, issued_ph[i] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const Tile tl = get_tile<MODE, STAGE>(a, t);
+                const uint32_t bytes = kWBytes + tl.nx * 128;
+                for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+                    if (!mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *wdst = sm.stage[s];
+                    uint8_t *xdst = sm.stage[s] + kWBytes;
+                    mbar_arrive_expect_tx(&sm.full[s], bytes);
+                    tma_load_2d(wdst, &a.tm_w, kb * kBK, tl.wrow0, &sm.full[s], pol_w);
+                    tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * kBK, tl.wrow1, &sm.full[s], pol_w);
+                    if (MODE == MOE_MODE_GROUPED) {
+                        tma_load_2d(xdst, &a.tm_x, kb * kBK, tl.xrow, &sm.full[s], pol_x);
+                    } else {
+                        for (int c = 0; c < tl.nx; c += 16)
+                            tma_load_2d(xdst + c * 128, &a.tm_x, kb * kBK, tl.xrow + c, &sm.full[s], pol_x);
+                    }
+                    issued[s] = 1;
+                    issued_ph[s] = ph;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already in flight land before the CTA exits
+                for (int i = 0; i < kStages; ++i)
+                    if (issued[i]) {
+                        const unsigned long long t0 = global_timer_ns();
+                        while (!mbar_try_wait(&sm.full[i], issued_ph[i]) && global_timer_ns() - t0 < 100000000ull) {
+                        }
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            bool any = false;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const Tile tl = get_tile<MODE, STAGE>(a, t);
+                if (!mbar_wait(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * kAccCols;
+                const uint32_t idesc = (MODE == MOE_MODE_GROUPED) ? make_idesc(1, 1, 128, 256)
+                                                                  : make_idesc(1, 1, 128, (uint32_t)tl.nx);
+                for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+                    if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *w = sm.stage[s];
+                    const uint8_t *xs = sm.stage[s] + kWBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t accum = (kb > tl.kb0 || kk > 0) ? 1u : 0u;
+                        if (MODE == MOE_MODE_GROUPED) {
+                            mma_bf16(d, smem_desc_sw128(xs + kk * 32), smem_desc_sw128(w + kk * 32), idesc, accum);
+                        } else {
+                            mma_bf16(d, smem_desc_sw128(w + kk * 32), smem_desc_sw128(xs + kk * 32), idesc, accum);
+                            mma_bf16(d + 128, smem_desc_sw128(w + kWBytes / 2 + kk * 32),
+                                     smem_desc_sw128(xs + kk * 32), idesc, accum);
+                        }
+                    }
+                    any = true;
+                    mma_commit(&sm.empty[s]);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(&sm.tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok && any) {
+                // drain: wait (bounded) until every MMA issued so far has finished
+                mma_commit(&sm.drain);
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&sm.drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;           // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;    // accumulator row (TMEM lane)
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const Tile tl = get_tile<MODE, STAGE>(a, t);
+            bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+
+            if (MODE == MOE_MODE_GROUPED && STAGE == 1) {
+                // row = sorted position; columns j (gate) and 128+j (up) of h column ncol0+j
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)(tl.xrow + row) * a.N + tl.ncol0;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    float g[32], u[32], h[32];
+                    tmem_ld32(tacc + c0, g);
+                    tmem_ld32(tacc + 128 + c0, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        h[i] = silu(g[i]) * u[i];
+                    store_bf16x32(dst + c0, h);
+                }
+            } else if (MODE == MOE_MODE_GROUPED && STAGE == 2) {
+                const int pos = tl.xrow + row;
+                const int slot = a.sorted_ids[pos];
+                const float wgt = a.sorted_weights[pos];
+                const bool live = slot < a.S;
+                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + tl.ncol0;
+                const int ncols = min(256, a.N - tl.ncol0);
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    if (live) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
+                                                wgt * v[4 * i + 3]);
+                    }
+                }
+            } else if (MODE == MOE_MODE_SWAP && STAGE == 1) {
+                // row = h column within the 128-wide tile; TMEM columns = tokens of the segment
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)tl.xrow * a.N + tl.ncol0 + row;
+#pragma unroll 1
+                for (int c0 = 0; c0 < tl.nx; c0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(tacc + c0, g);
+                    tmem_ld16(tacc + 128 + c0, u);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        dst[(size_t)(c0 + j) * a.N] = __float2bfloat16_rn(silu(g[j]) * u[j]);
+                }
+            } else {
+                // swap, stage 2: rows = output features ncol0 + half*128 + row; columns = tokens
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int n = tl.ncol0 + half * 128 + row;
+                    const bool nok = n < a.N;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < tl.nx; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(tacc + half * 128 + c0, v);
+                        if (!nok)
+                            continue;
+                        if (a.split_k > 1) {
+                            float *dst = a.partials + ((size_t)tl.ks * a.P_max + tl.xrow + c0) * a.N + n;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                dst[(size_t)j * a.N] = v[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int pos = tl.xrow + c0 + j;
+                                const int slot = a.sorted_ids[pos];
+                                if (slot < a.S)
+                                    a.y[(size_t)slot * a.N + n] = a.sorted_weights[pos] * v[j];
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int MODE, int STAGE>
+cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
+{
+    auto kern = gemm_kernel<MODE, STAGE>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    kern<<<grid, kThreads, kSmemBytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace bf16gemm
+
+cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_GROUPED, 1>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_GROUPED, 2>(a, grid, st);
+}
+
+cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_SWAP, 1>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_SWAP, 2>(a, grid, st);
+}
+
+}  // namespace moe

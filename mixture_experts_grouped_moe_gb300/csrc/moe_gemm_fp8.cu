@@ -1,0 +1,353 @@
+// Block-scaled FP8 (e4m3) group GEMMs of the fused MoE layer ("per_1x128"
+// quantisation of the AITER walk-through; two-stage path with the
+// intermediate re-quantised between the stages, section 3.2).
+//
+// Scales are fp32 per 128x128 weight block and per 1x128 activation group,
+// so they are not the power-of-two 32-element scales the tensor core applies
+// in hardware.  Each 128-wide K block is therefore accumulated on its own
+// by tcgen05.mma kind::f8f6f4 into one of two TMEM buffers, and eight
+// promotion warps fold it into fp32 registers:
+//     acc[row][col] += D_kb[row][col] * s_x[row][kb] * s_w[col_block][kb]
+// while the tensor core fills the other buffer with the next K block.
+// After the last K block the same warps run the epilogue from registers:
+// stage 1 computes h = silu(gate) * up and re-quantises each 1x128 group of
+// h (scale = amax / 448); stage 2 scales rows by their top-k weight.
+//
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9
+// promotion/epilogue (warp w reads TMEM lanes 32*(w%4)..+31 and one half
+// of the 256 accumulator columns).  Tiles: M = 128 sorted token rows,
+// N = 256 weight rows (stage 1: 128 gate + the matching 128 up rows;
+// stage 2: 256 output features).  Each thread owns two 64-column chunks:
+// stage 1 gate columns [64h, 64h+64) and up columns [128+64h, ...) so the
+// SwiGLU pairs stay inside the thread; stage 2 columns [128h, 128h+128).
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace fp8gemm {
+
+constexpr int kBK = 128;                    // one 128-wide K block (128 bytes) per stage
+constexpr int kStages = 4;
+constexpr int kWBytes = 256 * 128;          // 32 KiB
+constexpr int kXBytes = 128 * 128;          // 16 KiB
+constexpr int kStageBytes = kWBytes + kXBytes;
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kPromoWarps = 8;
+constexpr int kThreads = 64 + 32 * kPromoWarps;
+constexpr int kGroupM = 16;
+
+struct __align__(1024) Smem {
+    uint8_t stage[kStages][kStageBytes];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    float amax[2][128];
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void named_bar(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+struct Tile {
+    int e, xrow, wrow0, wrow1, ncol0;
+};
+
+template <int STAGE>
+__device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t, int nmb, int nnt)
+{
+    const int group = t / (kGroupM * nnt);
+    const int within = t - group * kGroupM * nnt;
+    const int gsize = min(kGroupM, nmb - group * kGroupM);
+    const int nt = within / gsize;
+    const int mb = group * kGroupM + within % gsize;
+    Tile tl;
+    tl.e = a.sorted_expert_ids[mb];
+    tl.xrow = mb * 128;
+    if (STAGE == 1) {
+        tl.wrow0 = tl.e * a.rows_per_expert + nt * 128;
+        tl.wrow1 = tl.e * a.rows_per_expert + a.N + nt * 128;
+        tl.ncol0 = nt * 128;
+    } else {
+        tl.wrow0 = tl.e * a.rows_per_expert + nt * 256;
+        tl.wrow1 = tl.wrow0 + 128;
+        tl.ncol0 = nt * 256;
+    }
+    return tl;
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_constant__ GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], kPromoWarps);
+        }
+        mbar_init(&sm.drain, 1);
+        sm.abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&a.tm_x);
+        tma_prefetch_desc(&a.tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    const int nmb = *a.num_post_padded / 128;
+    const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+    const int ntiles = nmb * nnt;
+    const int nkb = a.K / kBK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            int issued[kStages];
+            uint32_t issued_ph[kStages];
+            for (int i = 0; i < kStages; ++i)
+                issued[i] = 0, issued_ph[i] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *wdst = sm.stage[s];
+                    mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+                    tma_load_2d(wdst, &a.tm_w, kb * kBK, tl.wrow0, &sm.full[s], pol_w);
+                    tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * kBK, tl.wrow1, &sm.full[s], pol_w);
+                    tma_load_2d(wdst + kWBytes, &a.tm_x, kb * kBK, tl.xrow, &sm.full[s], pol_x);
+                    issued[s] = 1;
+                    issued_ph[s] = ph;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int i = 0; i < kStages; ++i)
+                    if (issued[i]) {
+                        const unsigned long long t0 = global_timer_ns();
+                        while (!mbar_try_wait(&sm.full[i], issued_ph[i]) && global_timer_ns() - t0 < 100000000ull) {
+                        }
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int buf = 0;
+            uint32_t bph = 0;
+            bool ok = true, any = false;
+            const uint32_t idesc = make_idesc(0, 0, 128, 256);
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&sm.tempty[buf], bph ^ 1, a.status, abort_flag) ||
+                        !mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + buf * kAccCols;
+                    const uint8_t *w = sm.stage[s];
+                    const uint8_t *xs = sm.stage[s] + kWBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk)
+                        mma_fp8(d, smem_desc_sw128(xs + kk * 32), smem_desc_sw128(w + kk * 32), idesc,
+                                kk > 0 ? 1u : 0u);
+                    any = true;
+                    mma_commit(&sm.empty[s]);
+                    mma_commit(&sm.tfull[buf]);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    if (++buf == 2) {
+                        buf = 0;
+                        bph ^= 1;
+                    }
+                }
+            }
+            if (!ok && any) {
+                mma_commit(&sm.drain);
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&sm.drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------- promotion + epilogue
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;      // 0 or 1
+        const int row = q * 32 + lane;
+        const int c0 = (STAGE == 1) ? half * 64 : half * 128;          // first chunk
+        const int c1 = (STAGE == 1) ? 128 + half * 64 : half * 128 + 64;  // second chunk
+        const int KB128 = a.K / 128;
+        int buf = 0;
+        uint32_t bph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
+            const int pos = tl.xrow + row;
+            // weight-scale rows of this thread's two column chunks; a stage-2 half past the last
+            // output feature (H % 256 == 128) reads a valid row and is never stored
+            const int nrb = a.E * a.rows_per_expert / 128;
+            int rb0 = (tl.wrow0 + (STAGE == 1 ? half * 64 : half * 128)) / 128;
+            int rb1 = (STAGE == 1 ? tl.wrow1 + half * 64 : tl.wrow0 + half * 128 + 64) / 128;
+            rb0 = rb0 < nrb ? rb0 : nrb - 1;
+            rb1 = rb1 < nrb ? rb1 : nrb - 1;
+            const float *sw0 = a.w_scales + (size_t)rb0 * KB128;
+            const float *sw1 = a.w_scales + (size_t)rb1 * KB128;
+            float acc0[64], acc1[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                acc0[i] = 0.0f, acc1[i] = 0.0f;
+            for (int kb = 0; kb < nkb; ++kb) {
+                bool w_ok = mbar_wait(&sm.tfull[buf], bph, a.status, abort_flag);
+                w_ok = __all_sync(0xffffffffu, w_ok);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sx = a.x_scales[(size_t)kb * a.P_max + pos];
+                const float f0 = sx * sw0[kb];
+                const float f1 = sx * sw1[kb];
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
+#pragma unroll
+                for (int c = 0; c < 64; c += 32) {
+                    float v[32];
+                    tmem_ld32(tb + c0 + c, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc0[c + i] = fmaf(v[i], f0, acc0[c + i]);
+                }
+#pragma unroll
+                for (int c = 0; c < 64; c += 32) {
+                    float v[32];
+                    tmem_ld32(tb + c1 + c, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc1[c + i] = fmaf(v[i], f1, acc1[c + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.tempty[buf]);
+                if (++buf == 2) {
+                    buf = 0;
+                    bph ^= 1;
+                }
+            }
+            if (!ok)
+                break;
+            if (STAGE == 1) {
+                // h for columns ncol0 + half*64 + i; one 1x128 group spans both halves of the row
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    acc0[i] = silu(acc0[i]) * acc1[i];
+                    amax = fmaxf(amax, fabsf(acc0[i]));
+                }
+                sm.amax[half][row] = amax;
+                named_bar(1 + q, 64);
+                amax = fmaxf(amax, sm.amax[half ^ 1][row]);
+                named_bar(1 + q, 64);
+                const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)pos * a.N + tl.ncol0 + half * 64;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t pk = 0;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            pk |= (uint32_t)__nv_cvt_float_to_fp8(acc0[v * 16 + j * 4 + b] / sc, __NV_SATFINITE,
+                                                                  __NV_E4M3)
+                                  << (8 * b);
+                        w[j] = pk;
+                    }
+                    reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                if (half == 0)
+                    a.inter_scales[(size_t)(tl.ncol0 / 128) * a.P_max + pos] = sc;
+            } else {
+                const int slot = a.sorted_ids[pos];
+                if (slot < a.S) {
+                    const float wgt = a.sorted_weights[pos];
+                    const int n0 = tl.ncol0 + half * 128;
+                    float *dst = a.y + (size_t)slot * a.N + n0;
+                    if (n0 < a.N) {
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(wgt * acc0[i], wgt * acc0[i + 1], wgt * acc0[i + 2], wgt * acc0[i + 3]);
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4)
+                            *reinterpret_cast<float4 *>(dst + 64 + i) =
+                                make_float4(wgt * acc1[i], wgt * acc1[i + 1], wgt * acc1[i + 2], wgt * acc1[i + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int STAGE>
+cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
+{
+    auto kern = gemm_fp8_kernel<STAGE>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    kern<<<grid, kThreads, kSmemBytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8gemm
+
+cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? fp8gemm::launch<1>(a, grid, st) : fp8gemm::launch<2>(a, grid, st);
+}
+
+}  // namespace moe

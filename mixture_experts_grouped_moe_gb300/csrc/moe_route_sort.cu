@@ -1,0 +1,609 @@
+// Router (gating + warp-shuffle top-k), align-sort by expert, row gathers,
+// block-scaled FP8 quantisation and the weighted combine of the fused MoE
+// layer.  These are the memory-bound steps around the two group GEMMs.
+//
+// Sources (fused-MoE pages): AITER walk-through section 3 ("Fused MoE":
+// gating -> token reorder -> expert GEMMs -> weighted combine), section 3.1
+// (moe_sorting: slots grouped by expert, per-expert padding to the block
+// size, buffers of T*k + E*B - k entries), the "per_1x128" quantisation type
+// of that page, and the Mixtral group-GEMM talk (top-2 routing, SwiGLU).
+#include <cuda_fp8.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float (&f)[8])
+{
+    const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(p[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// ================================================================ router
+//
+// logit[t][e] in fp32, fixed order: lane L of a warp accumulates (with one
+// rounding per element; a bf16 x bf16 product is exact in fp32) the
+// elements h with (h / 8) mod 32 == L in ascending h, then a xor butterfly
+// with strides 16, 8, 4, 2, 1 combines the 32 partials; the bias is added
+// last.  A CTA takes TT tokens; each warp takes groups of EG experts.  The
+// logits of the CTA's tokens go to shared memory; then one warp per token
+// selects the top k by repeated warp arg-max (larger logit first, lower
+// expert on ties) and takes the softmax over the selected logits.
+
+template <int TT, int EG>
+__global__ void __launch_bounds__(256) router_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                     const __nv_bfloat16 *__restrict__ Wr,
+                                                     const float *__restrict__ bias, int T, int H, int E, int k,
+                                                     int32_t *__restrict__ ids, float *__restrict__ wts,
+                                                     float *__restrict__ logits_out)
+{
+    extern __shared__ float s_logit[];  // [TT][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * TT;
+    const int ngroups = (E + EG - 1) / EG;
+
+    for (int g = warp; g < ngroups; g += 8) {
+        float acc[TT][EG];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int j = 0; j < EG; ++j)
+                acc[t][j] = 0.0f;
+#pragma unroll 2
+        for (int h0 = lane * 8; h0 < H; h0 += 256) {
+            float wf[EG][8];
+#pragma unroll
+            for (int j = 0; j < EG; ++j) {
+                const int e = g * EG + j;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (e < E)
+                    v = __ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0));
+                bf16x8_to_float(v, wf[j]);
+            }
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                const int tok = t0 + t;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (tok < T)
+                    v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)tok * H + h0));
+                float xf[8];
+                bf16x8_to_float(v, xf);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+#pragma unroll
+                    for (int j = 0; j < EG; ++j)
+                        acc[t][j] = __fmaf_rn(xf[c], wf[j][c], acc[t][j]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int j = 0; j < EG; ++j) {
+                float v = acc[t][j];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1)
+                    v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+                const int e = g * EG + j;
+                if (lane == 0 && e < E) {
+                    if (bias)
+                        v = __fadd_rn(v, bias[e]);
+                    s_logit[t * E + e] = v;
+                }
+            }
+    }
+    __syncthreads();
+
+    for (int t = warp; t < TT; t += 8) {
+        const int tok = t0 + t;
+        if (tok >= T)
+            continue;
+        const float *lg = s_logit + t * E;
+        if (logits_out)
+            for (int e = lane; e < E; e += 32)
+                logits_out[(size_t)tok * E + e] = lg[e];
+        uint32_t taken = 0;  // bit m: expert lane + 32m already selected
+        float my_v = 0.0f;
+        int my_e = 0;
+        for (int j = 0; j < k; ++j) {
+            float bv = -FLT_MAX;
+            int be = INT_MAX;
+            for (int m = 0, e = lane; e < E; ++m, e += 32) {
+                if (taken & (1u << m))
+                    continue;
+                const float v = lg[e];
+                if (be == INT_MAX || v > bv) {  // ascending e: ties keep the lower expert
+                    bv = v;
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane)
+                taken |= 1u << (be >> 5);
+            if (lane == j) {
+                my_v = bv;
+                my_e = be;
+            }
+        }
+        const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+        const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
+        float sum = 0.0f;
+        for (int j = 0; j < k; ++j)
+            sum += __shfl_sync(0xffffffffu, ex, j);
+        if (lane < k) {
+            ids[(size_t)tok * k + lane] = my_e;
+            wts[(size_t)tok * k + lane] = ex / sum;
+        }
+    }
+}
+
+void launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
+                   int k, int32_t *ids, float *wts, float *logits, cudaStream_t st)
+{
+    if (T <= 0)
+        return;
+    if ((long)T * E <= 256L * 64) {
+        constexpr int TT = 2;
+        const size_t sm = sizeof(float) * TT * E;
+        router_kernel<TT, 1><<<(T + TT - 1) / TT, 256, sm, st>>>(x, Wr, bias, T, H, E, k, ids, wts, logits);
+    } else {
+        constexpr int TT = 8;
+        const size_t sm = sizeof(float) * TT * E;
+        router_kernel<TT, 4><<<(T + TT - 1) / TT, 256, sm, st>>>(x, Wr, bias, T, H, E, k, ids, wts, logits);
+    }
+}
+
+// ============================================================ align-sort
+//
+// Three launches over chunks of kSortChunk consecutive slots:
+//  1. count:   per-chunk histogram of expert ids -> cc[chunk][e]; also
+//              pre-fills sorted_ids with the sentinel S and sorted_weights
+//              with 0 (grid-stride over all max_padded entries).
+//  2. scan:    one CTA.  For each expert the chunk histograms become
+//              exclusive prefixes (chunk order), the totals are the expert
+//              counts, padded segment lengths ceil(cnt/B)*B are scanned over
+//              experts (ascending e), block -> expert ids are written, the
+//              compact list of experts with slots is built.
+//  3. scatter: each chunk ranks its slots stably (warp match + per-warp
+//              counts, ascending slot) and writes slot s to
+//              offset[e] + prefix[chunk][e] + rank.
+
+size_t sort_scratch_bytes(int T, int k, int E)
+{
+    const long S = (long)T * k;
+    const long nchunks = (S + kSortChunk - 1) / kSortChunk;
+    return (size_t)(nchunks > 0 ? nchunks : 1) * E * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restrict__ ids, int S, int E,
+                                                         int32_t *__restrict__ cc,
+                                                         int32_t *__restrict__ sorted_ids,
+                                                         float *__restrict__ sorted_w, int64_t P_max)
+{
+    extern __shared__ int32_t s_hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        s_hist[e] = 0;
+    __syncthreads();
+    const int s = blockIdx.x * kSortChunk + threadIdx.x;
+    if (s < S)
+        atomicAdd(&s_hist[ids[s]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cc[(size_t)blockIdx.x * E + e] = s_hist[e];
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < P_max; i += (int64_t)gridDim.x * blockDim.x) {
+        sorted_ids[i] = S;
+        sorted_w[i] = 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ cc, int nchunks, int E, int B,
+                                                        int64_t NB_max, int32_t *__restrict__ counts,
+                                                        int32_t *__restrict__ offsets,
+                                                        int32_t *__restrict__ sorted_eids,
+                                                        int32_t *__restrict__ npp, int32_t *__restrict__ active,
+                                                        int32_t *__restrict__ num_active)
+{
+    __shared__ int32_t s_pad[1024];
+    __shared__ int32_t s_act[1024];
+    __shared__ int32_t s_cnt[1024];
+    const int e = threadIdx.x;
+    int cnt = 0;
+    if (e < E) {
+        for (int c = 0; c < nchunks; ++c) {
+            const int v = cc[(size_t)c * E + e];
+            cc[(size_t)c * E + e] = cnt;
+            cnt += v;
+        }
+    }
+    s_cnt[e] = cnt;
+    s_pad[e] = (e < E) ? (cnt + B - 1) / B * B : 0;
+    s_act[e] = (e < E && cnt > 0) ? 1 : 0;
+    __syncthreads();
+    // inclusive Hillis-Steele scans over the (at most 1024) experts
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int a = (e >= off) ? s_pad[e - off] : 0;
+        const int b = (e >= off) ? s_act[e - off] : 0;
+        __syncthreads();
+        s_pad[e] += a;
+        s_act[e] += b;
+        __syncthreads();
+    }
+    const int pad_incl = s_pad[e];
+    const int pad_excl = pad_incl - ((e < E) ? (s_cnt[e] + B - 1) / B * B : 0);
+    if (e < E) {
+        if (counts)
+            counts[e] = cnt;
+        if (offsets)
+            offsets[e] = pad_excl;
+        if (active && cnt > 0)
+            active[s_act[e] - 1] = e;
+        for (int b = pad_excl / B; b < pad_incl / B; ++b)
+            sorted_eids[b] = e;
+    }
+    const int total = s_pad[1023];
+    if (e == 0) {
+        *npp = total;
+        if (offsets)
+            offsets[E] = total;
+        if (num_active)
+            *num_active = s_act[1023];
+    }
+    for (int64_t b = total / B + e; b < NB_max; b += blockDim.x)
+        sorted_eids[b] = -1;
+}
+
+__global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t *__restrict__ ids,
+                                                           const float *__restrict__ wts, int S, int E,
+                                                           const int32_t *__restrict__ cc,
+                                                           const int32_t *__restrict__ offsets_scan, int B,
+                                                           int32_t *__restrict__ sorted_ids,
+                                                           float *__restrict__ sorted_w,
+                                                           int32_t *__restrict__ slot_pos)
+{
+    extern __shared__ int32_t s_wc[];  // [32 warps][E] per-warp counts -> exclusive prefixes over warps
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x)
+        s_wc[i] = 0;
+    __syncthreads();
+    const int s = blockIdx.x * kSortChunk + threadIdx.x;
+    const bool valid = s < S;
+    const int e = valid ? ids[s] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0)
+        s_wc[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int v = s_wc[w * E + ex];
+            s_wc[w * E + ex] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (valid) {
+        const int pos = offsets_scan[e] + cc[(size_t)blockIdx.x * E + e] + s_wc[warp * E + e] + rank;
+        sorted_ids[pos] = s;
+        sorted_w[pos] = wts[s];
+        if (slot_pos)
+            slot_pos[s] = pos;
+    }
+}
+
+void launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
+                       const SortOut &o, void *scratch, cudaStream_t st)
+{
+    const int S = T * k;
+    const int nchunks = (S + kSortChunk - 1) / kSortChunk;
+    const int64_t P_max = (int64_t)S + (int64_t)E * block_m - k;
+    const int64_t NB_max = (P_max + block_m - 1) / block_m;
+    int32_t *cc = static_cast<int32_t *>(scratch);  // o.expert_offsets must be non-null (the scatter reads it)
+    const int count_grid = nchunks > 0 ? nchunks : 1;
+    sort_count_kernel<<<count_grid, 1024, sizeof(int32_t) * E, st>>>(ids, S, E, cc, o.sorted_ids,
+                                                                    o.sorted_weights, P_max);
+    sort_scan_kernel<<<1, 1024, 0, st>>>(cc, nchunks, E, block_m, NB_max, o.expert_counts, o.expert_offsets,
+                                         o.sorted_expert_ids, o.num_post_padded, o.active_experts,
+                                         o.num_active);
+    if (32 * E * sizeof(int32_t) > 48 * 1024)
+        cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(32 * E * sizeof(int32_t)));
+    if (nchunks > 0)
+        sort_scatter_kernel<<<nchunks, 1024, sizeof(int32_t) * 32 * E, st>>>(
+            ids, wts, S, E, cc, o.expert_offsets, block_m, o.sorted_ids, o.sorted_weights, o.slot_pos);
+}
+
+// ================================================================ gather
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                         const int32_t *__restrict__ sorted_ids,
+                                                         const int32_t *__restrict__ npp, int S, int k, int H,
+                                                         __nv_bfloat16 *__restrict__ xs)
+{
+    const int rows = *npp;
+    const int nvec = H / 8;
+    for (int i = blockIdx.x; i < rows; i += gridDim.x) {
+        const int s = sorted_ids[i];
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)i * H);
+        if (s < S) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s / k) * H);
+            for (int c = threadIdx.x; c < nvec; c += blockDim.x)
+                dst[c] = __ldg(src + c);
+        } else {
+            for (int c = threadIdx.x; c < nvec; c += blockDim.x)
+                dst[c] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+void launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
+                        int H, int64_t P_max, __nv_bfloat16 *xs, cudaStream_t st)
+{
+    int grid = (int)(P_max < 8192 ? P_max : 8192);
+    if (grid < 1)
+        grid = 1;
+    gather_rows_kernel<<<grid, 256, 0, st>>>(x, sorted_ids, npp, S, k, H, xs);
+}
+
+// ---------------------------------------------------- FP8 quantisation
+//
+// Group quantisation with scale = amax / 448 (1 if amax is 0) and codes
+// e4m3(v / scale), round-to-nearest-even, saturating (satfinite).  The
+// division is IEEE (the library is built without fast-math).
+
+__device__ __forceinline__ float group_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+__device__ __forceinline__ uint2 encode8(const float (&f)[8], float scale)
+{
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = __nv_cvt_float_to_fp8(f[i] / scale, __NV_SATFINITE, __NV_E4M3);
+        lo |= c << (8 * i);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = __nv_cvt_float_to_fp8(f[4 + i] / scale, __NV_SATFINITE, __NV_E4M3);
+        hi |= c << (8 * i);
+    }
+    return make_uint2(lo, hi);
+}
+
+// One 16-lane segment handles one 128-column group (8 columns per lane).
+__device__ __forceinline__ float seg16_max(float v)
+{
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float absmax8(const float (&f)[8])
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m = fmaxf(m, fabsf(f[i]));
+    return m;
+}
+
+// Rows of X [R][C] quantised per 1x128: codes q [R][C], scales s [R][C/128].
+__global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16 *__restrict__ X, int64_t R, int C,
+                                                       uint8_t *__restrict__ q, float *__restrict__ s)
+{
+    const int nvec = C / 8;
+    const int64_t total = R * nvec;
+    // 256 threads cover 16 groups; every 16 consecutive vectors form one group
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v - threadIdx.x < total;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const bool ok = v < total;
+        float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ok)
+            bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(X) + v), f);
+        const float sc = group_scale(seg16_max(absmax8(f)));
+        if (ok) {
+            reinterpret_cast<uint2 *>(q)[v] = encode8(f, sc);
+            if ((v & 15) == 0)
+                s[v / 16] = sc;
+        }
+    }
+}
+
+void launch_quant_act(const __nv_bfloat16 *X, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st)
+{
+    const int64_t total = R * (C / 8);
+    int64_t grid = (total + 255) / 256;
+    if (grid > 65535)
+        grid = 65535;
+    if (grid < 1)
+        return;
+    quant_act_kernel<<<(int)grid, 256, 0, st>>>(X, R, C, q, s);
+}
+
+// Gathered rows quantised per 1x128: q [P_max][H] in sorted order, scales
+// transposed sT [H/128][P_max] so that a GEMM tile reads them coalesced.
+__global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                          const int32_t *__restrict__ sorted_ids,
+                                                          const int32_t *__restrict__ npp, int S, int k, int H,
+                                                          int64_t P_max, uint8_t *__restrict__ q,
+                                                          float *__restrict__ sT)
+{
+    const int rows = *npp;
+    const int nvec = H / 8;
+    for (int i = blockIdx.x; i < rows; i += gridDim.x) {
+        const int s = sorted_ids[i];
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s < S ? s / k : 0) * H);
+        for (int c0 = 0; c0 < nvec; c0 += blockDim.x) {
+            const int c = c0 + threadIdx.x;
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (c < nvec && s < S)
+                bf16x8_to_float(__ldg(src + c), f);
+            const float sc = group_scale(seg16_max(absmax8(f)));
+            if (c < nvec) {
+                reinterpret_cast<uint2 *>(q + (size_t)i * H)[c] = encode8(f, sc);
+                if ((c & 15) == 0)
+                    sT[(size_t)(c / 16) * P_max + i] = sc;
+            }
+        }
+    }
+}
+
+void launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
+                              int k, int H, int64_t P_max, uint8_t *q, float *sT, cudaStream_t st)
+{
+    int grid = (int)(P_max < 8192 ? P_max : 8192);
+    if (grid < 1)
+        grid = 1;
+    gather_quant_kernel<<<grid, 256, 0, st>>>(x, sorted_ids, npp, S, k, H, P_max, q, sT);
+}
+
+// One CTA per 128x128 block of W [R][C]: amax over the block, then codes.
+__global__ void __launch_bounds__(256) quant_weight_kernel(const __nv_bfloat16 *__restrict__ W, int C,
+                                                          uint8_t *__restrict__ q, float *__restrict__ s)
+{
+    __shared__ float s_red[8];
+    const int64_t br = blockIdx.y;
+    const int bc = blockIdx.x;
+    const int GC = C / 128;
+    // thread -> 16 columns-vectors: row r = tid / 2 (0..127), half = tid % 2 (64 columns)
+    const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const __nv_bfloat16 *row = W + (br * 128 + r) * (int64_t)C + bc * 128 + half * 64;
+    float f[8][8];
+    float m = 0.0f;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(row) + v), f[v]);
+        m = fmaxf(m, absmax8(f[v]));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0)
+        s_red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, s_red[i]);
+    const float sc = group_scale(amax);
+    uint8_t *qrow = q + (br * 128 + r) * (int64_t)C + bc * 128 + half * 64;
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        reinterpret_cast<uint2 *>(qrow)[v] = encode8(f[v], sc);
+    if (threadIdx.x == 0)
+        s[br * GC + bc] = sc;
+}
+
+void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st)
+{
+    if (R <= 0)
+        return;
+    dim3 grid(C / 128, (unsigned)(R / 128));
+    quant_weight_kernel<<<grid, 256, 0, st>>>(W, C, q, s);
+}
+
+// =============================================================== combine
+
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ Y, int T, int k, int H,
+                                                     __nv_bfloat16 *__restrict__ out)
+{
+    const int nv = H / 4;
+    const int64_t total = (int64_t)T * nv;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / nv;
+        const int c = (int)(i % nv);
+        const float4 *src = reinterpret_cast<const float4 *>(Y) + (t * k) * nv + c;
+        float4 a = __ldg(src);
+        for (int j = 1; j < k; ++j) {
+            const float4 b = __ldg(src + (int64_t)j * nv);
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(out)[i] = pk;
+    }
+}
+
+void launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st)
+{
+    const int64_t total = (int64_t)T * (H / 4);
+    int64_t grid = (total + 255) / 256;
+    if (grid > 152 * 16)
+        grid = 152 * 16;
+    if (grid < 1)
+        return;
+    combine_kernel<<<(int)grid, 256, 0, st>>>(Y, T, k, H, out);
+}
+
+__global__ void __launch_bounds__(256) splitk_combine_kernel(const float *__restrict__ P, int SK, int64_t P_rows,
+                                                            const int32_t *__restrict__ slot_pos,
+                                                            const float *__restrict__ wts, int T, int k, int H,
+                                                            __nv_bfloat16 *__restrict__ out)
+{
+    const int nv = H / 4;
+    const int64_t total = (int64_t)T * nv;
+    const int64_t split_stride = P_rows * nv;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / nv;
+        const int c = (int)(i % nv);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int64_t s = t * k + j;
+            const float4 *src = reinterpret_cast<const float4 *>(P) + (int64_t)slot_pos[s] * nv + c;
+            float4 p = __ldg(src);
+            for (int ks = 1; ks < SK; ++ks) {
+                const float4 b = __ldg(src + ks * split_stride);
+                p.x += b.x;
+                p.y += b.y;
+                p.z += b.z;
+                p.w += b.w;
+            }
+            const float w = wts[s];
+            a.x += w * p.x;
+            a.y += w * p.y;
+            a.z += w * p.z;
+            a.w += w * p.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(out)[i] = pk;
+    }
+}
+
+void launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
+                           int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st)
+{
+    const int64_t total = (int64_t)T * (H / 4);
+    int64_t grid = (total + 255) / 256;
+    if (grid > 152 * 16)
+        grid = 152 * 16;
+    if (grid < 1)
+        return;
+    splitk_combine_kernel<<<(int)grid, 256, 0, st>>>(P, SK, P_rows, slot_pos, wts, T, k, H, out);
+}
+
+}  // namespace moe

@@ -1,0 +1,278 @@
+"""Thin ctypes binding of libmoe_gb300 (include/moe.h), same names as the C ABI.
+
+Only argument marshalling lives here: tensors become raw pointers, the
+current torch CUDA stream becomes the `stream` argument, and a negative
+status raises MoEError.  Every step of the layer runs in the CUDA library;
+there is no Python or CPU fallback.  If the library is missing the first
+call raises (build it with `mixture_experts_grouped_moe_gb300.build`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+
+MOE_BF16 = 0
+MOE_FP8_BLOCK128 = 1
+MOE_MODE_GROUPED = 0
+MOE_MODE_SWAP = 1
+
+EXPORTED = [
+    "moe_status_string", "moe_version", "moe_align_sort_sizes", "moe_block_size_m_heuristic",
+    "moe_ksplit_heuristic", "moe_plan", "moe_fused_workspace_size", "moe_workspace_layout",
+    "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
+    "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_fused_forward", "moe_host_staging_bytes",
+    "moe_fused_forward_host", "moe_set_stage_events",
+]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+class moe_plan_t(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("block_m", ctypes.c_int), ("split_k1", ctypes.c_int),
+                ("split_k2", ctypes.c_int), ("max_padded", ctypes.c_int64), ("max_blocks", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class moe_ws_layout_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "status", "topk_ids", "topk_weights", "sorted_ids", "sorted_weights", "sorted_expert_ids",
+        "num_tokens_post_padded", "expert_counts", "x_sorted", "x_scales", "inter", "inter_scales", "y",
+        "total")]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            if not build_if_missing:
+                raise RuntimeError(f"CUDA library not built: {_build.LIB} is missing "
+                                   "(run mixture_experts_grouped_moe_gb300.build.build())")
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "moe_status_string": (ctypes.c_char_p, [I]),
+            "moe_version": (I, []),
+            "moe_align_sort_sizes": (I, [I, I, I, I, P, P]),
+            "moe_block_size_m_heuristic": (I, [I, I, I, I, I, P, I]),
+            "moe_ksplit_heuristic": (I, [I, I, I, I, I, I, I]),
+            "moe_plan": (I, [I, I, I, I, I, I, I, I, I, P]),
+            "moe_fused_workspace_size": (SZ, [I, I, I, I, I, I, I, I]),
+            "moe_workspace_layout": (I, [I, I, I, I, I, I, I, I, P]),
+            "moe_workspace_status": (I, [P, P, P]),
+            "moe_route_topk": (I, [P, P, P, I, I, I, I, P, P, P, P]),
+            "moe_align_sort_workspace_size": (SZ, [I, I, I]),
+            "moe_align_sort": (I, [P, P, I, I, I, I, P, P, P, P, P, P, SZ, P]),
+            "moe_quantize_fp8_act": (I, [P, I64, I, P, P, P]),
+            "moe_quantize_fp8_weights": (I, [P, I64, I, P, P, P]),
+            "moe_fused_forward": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
+            "moe_host_staging_bytes": (SZ, [I, I]),
+            "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
+            "moe_set_stage_events": (I, [P, I]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _p(t):
+    """Raw pointer of a tensor / int / None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoEError(fn, rc)
+    return rc
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def moe_version() -> int:
+    return load().moe_version()
+
+
+def moe_align_sort_sizes(T, k, E, block_m):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check("moe_align_sort_sizes", load().moe_align_sort_sizes(T, k, E, block_m, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def moe_block_size_m_heuristic(token, topk, expert, inter_dim, units, candidates=(32, 64, 128)):
+    arr = (ctypes.c_int * len(candidates))(*candidates)
+    r = load().moe_block_size_m_heuristic(token, topk, expert, inter_dim, units, arr, len(candidates))
+    if r < 0:
+        raise MoEError("moe_block_size_m_heuristic", r)
+    return r
+
+
+def moe_ksplit_heuristic(token, topk, expert, inter_dim, model_dim, units, block_m):
+    r = load().moe_ksplit_heuristic(token, topk, expert, inter_dim, model_dim, units, block_m)
+    if r < 0:
+        raise MoEError("moe_ksplit_heuristic", r)
+    return r
+
+
+def moe_plan(dtype, T, H, I, E, k, block_m=0, split_k=0, num_sms=0) -> moe_plan_t:
+    p = moe_plan_t()
+    _check("moe_plan", load().moe_plan(dtype, T, H, I, E, k, block_m, split_k, num_sms, ctypes.byref(p)))
+    return p
+
+
+def moe_fused_workspace_size(dtype, T, H, I, E, k, block_m=0, split_k=0) -> int:
+    return load().moe_fused_workspace_size(dtype, T, H, I, E, k, block_m, split_k)
+
+
+def moe_workspace_layout(dtype, T, H, I, E, k, block_m=0, split_k=0) -> moe_ws_layout_t:
+    lay = moe_ws_layout_t()
+    _check("moe_workspace_layout",
+           load().moe_workspace_layout(dtype, T, H, I, E, k, block_m, split_k, ctypes.byref(lay)))
+    return lay
+
+
+def moe_workspace_status(ws, stream=None) -> int:
+    v = ctypes.c_int()
+    _check("moe_workspace_status", load().moe_workspace_status(_p(ws), ctypes.byref(v), _stream(stream)))
+    return v.value
+
+
+def moe_route_topk(x, W_router, bias, T, H, E, k, topk_ids, topk_weights, logits=None, stream=None):
+    return _check("moe_route_topk", load().moe_route_topk(
+        _p(x), _p(W_router), _p(bias), T, H, E, k, _p(topk_ids), _p(topk_weights), _p(logits), _stream(stream)))
+
+
+def moe_align_sort_workspace_size(T, k, E) -> int:
+    return load().moe_align_sort_workspace_size(T, k, E)
+
+
+def moe_align_sort(topk_ids, topk_weights, T, k, E, block_m, sorted_ids, sorted_weights, sorted_expert_ids,
+                   num_tokens_post_padded, expert_counts, ws, ws_bytes, stream=None):
+    return _check("moe_align_sort", load().moe_align_sort(
+        _p(topk_ids), _p(topk_weights), T, k, E, block_m, _p(sorted_ids), _p(sorted_weights),
+        _p(sorted_expert_ids), _p(num_tokens_post_padded), _p(expert_counts), _p(ws), ws_bytes,
+        _stream(stream)))
+
+
+def moe_quantize_fp8_act(X, R, C, q, s, stream=None):
+    return _check("moe_quantize_fp8_act", load().moe_quantize_fp8_act(_p(X), R, C, _p(q), _p(s), _stream(stream)))
+
+
+def moe_quantize_fp8_weights(W, R, C, q, s, stream=None):
+    return _check("moe_quantize_fp8_weights",
+                  load().moe_quantize_fp8_weights(_p(W), R, C, _p(q), _p(s), _stream(stream)))
+
+
+def moe_fused_forward(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
+                      block_m, split_k, out, ws, ws_bytes, stream=None):
+    return _check("moe_fused_forward", load().moe_fused_forward(
+        dtype, _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(w1_scale), _p(W_down), _p(w2_scale),
+        T, H, I, E, k, block_m, split_k, _p(out), _p(ws), ws_bytes, _stream(stream)))
+
+
+def moe_host_staging_bytes(T, H) -> int:
+    return load().moe_host_staging_bytes(T, H)
+
+
+def moe_fused_forward_host(dtype, x_host, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I,
+                           E, k, block_m, split_k, out_host, ws, ws_bytes, stream=None):
+    return _check("moe_fused_forward_host", load().moe_fused_forward_host(
+        dtype, _p(x_host), _p(W_router), _p(router_bias), _p(W_gate_up), _p(w1_scale), _p(W_down), _p(w2_scale),
+        T, H, I, E, k, block_m, split_k, _p(out_host), _p(ws), ws_bytes, _stream(stream)))
+
+
+def moe_set_stage_events(events):
+    """Arm per-stage timing events (7 torch.cuda.Event(enable_timing=True)) for the next forward call."""
+    if events is None:
+        return _check("moe_set_stage_events", load().moe_set_stage_events(None, 0))
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return _check("moe_set_stage_events", load().moe_set_stage_events(arr, len(events)))
+
+
+# ------------------------------------------------------------- conveniences
+
+class FusedMoE:
+    """Owns the workspace for one layer shape and calls moe_fused_forward.
+
+    weights: dict with W_router, bias (or None), W_gate_up, W_down (CUDA
+    tensors); for FP8 also w1_scale, w2_scale and e4m3 (uint8) weight stacks.
+    """
+
+    def __init__(self, dtype, T, H, I, E, k, block_m=0, split_k=0, device="cuda", host_staging=False):
+        import torch
+        self.dtype, self.T, self.H, self.I, self.E, self.k = dtype, T, H, I, E, k
+        self.block_m, self.split_k = block_m, split_k
+        self.plan = moe_plan(dtype, T, H, I, E, k, block_m, split_k)
+        self.ws_bytes = moe_fused_workspace_size(dtype, T, H, I, E, k, block_m, split_k)
+        if self.ws_bytes == 0:
+            raise MoEError("moe_fused_workspace_size", MOE_ERR_INVALID_ARG)
+        extra = moe_host_staging_bytes(T, H) if host_staging else 0
+        self.ws = torch.empty(self.ws_bytes + extra, dtype=torch.uint8, device=device)
+        self.layout = moe_workspace_layout(dtype, T, H, I, E, k, block_m, split_k)
+
+    def __call__(self, x, w, out, stream=None):
+        moe_fused_forward(self.dtype, x, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
+                          w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k, self.block_m,
+                          self.split_k, out, self.ws, self.ws_bytes, stream)
+        return out
+
+    def forward_host(self, x_host, w, out_host, stream=None):
+        moe_fused_forward_host(self.dtype, x_host, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
+                               w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k,
+                               self.block_m, self.split_k, out_host, self.ws, self.ws.numel(), stream)
+        return out_host
+
+    def view(self, name, dtype, shape):
+        """A tensor view of one intermediate buffer of the workspace (after a call)."""
+        import torch
+        off = getattr(self.layout, name)
+        if off < 0:
+            return None
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty(0, dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def status(self, stream=None) -> int:
+        return moe_workspace_status(self.ws, stream)

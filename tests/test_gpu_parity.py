@@ -1,0 +1,338 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Integer outputs (expert ids, sort order, padding, FP8 codes) must match
+bit for bit; floating-point outputs must meet relative L2 error <= 5e-3
+(bf16) and <= 3e-2 (block-scaled FP8) against the oracle fed the same
+inputs; top-k weights within 1e-5 relative.  Large workloads compare every
+routing/sort output in full and the layer output on a seeded token sample
+plus the tokens of the least-loaded experts.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_grouped_moe_gb300 import synth
+from moe_checks import check_sort_invariants, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 5e-3
+TOL_FP8 = 3e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_grouped_moe_gb300 import build
+    build.build()
+    from mixture_experts_grouped_moe_gb300 import moe as m
+    m.load()
+    return m
+
+
+_cache = {}
+
+
+def gpu_inputs(cfg, seed=0):
+    key = (cfg, seed)
+    if key not in _cache:
+        if len(_cache) > 1:
+            _cache.clear()
+            torch.cuda.empty_cache()
+        inp = synth.make_inputs(cfg, seed=seed, device="cuda")
+        host = {k: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+                for k, v in inp.items()}
+        _cache[key] = (inp, host)
+    return _cache[key]
+
+
+def bias_np(host):
+    return host["bias"]
+
+
+def run_fused(moe, cfg, inp, dtype=0, block_m=0, split_k=0, fp8w=None):
+    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, block_m, split_k)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"]}
+    if dtype == moe.MOE_BF16:
+        w.update(W_gate_up=inp["W_gate_up"], W_down=inp["W_down"])
+    else:
+        w.update(fp8w)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    layer(inp["x"], w, out)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    return out, layer
+
+
+def quantize_weights_gpu(moe, inp, cfg):
+    E, I, H = cfg.E, cfg.I, cfg.H
+    q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    s1 = torch.empty(E * 2 * I // 128, H // 128, dtype=torch.float32, device="cuda")
+    q2 = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(E * H // 128, I // 128, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_weights(inp["W_gate_up"], E * 2 * I, H, q1, s1)
+    moe.moe_quantize_fp8_weights(inp["W_down"], E * H, I, q2, s2)
+    return {"W_gate_up": q1, "w1_scale": s1, "W_down": q2, "w2_scale": s2}
+
+
+def sample_tokens(cfg, ids, n=64):
+    toks = set(synth.token_sample(cfg.T, n).tolist())
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    nonempty = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:4]
+    extra = [t for t in range(cfg.T) if set(ids[t].tolist()) & set(nonempty)]
+    toks.update(extra[:32])
+    return np.array(sorted(toks), np.int64)
+
+
+# ---------------------------------------------------------------- router
+
+ROUTER_CASES = [
+    synth.CONFIGS["tiny"],
+    synth.CONFIGS["mixtral_decode"],
+    synth.CONFIGS["mixtral_prefill"],
+    synth.CONFIGS["finegrained_zipf"],
+    synth.CONFIGS["tiny"].with_(name="t1", T=1),
+    synth.CONFIGS["tiny"].with_(name="t3_e1", T=3, E=1, k=1),
+    synth.CONFIGS["tiny"].with_(name="t17_k_eq_e", T=17, E=5, k=5),
+    synth.CONFIGS["tiny"].with_(name="e1000_k32", T=40, H=384, E=1000, k=32, bias="normal", bias_param=0.5),
+    synth.CONFIGS["tiny"].with_(name="h_ragged", T=70, H=384, E=40, k=6),
+]
+
+
+@pytest.mark.parametrize("cfg", ROUTER_CASES, ids=lambda c: c.name)
+def test_router_parity(moe, cfg):
+    inp = synth.make_inputs(cfg, seed=0, device="cuda", weights=False)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(inp["x"], inp["W_router"], inp["bias"], T, cfg.H, E, k, ids, w, logits)
+    torch.cuda.synchronize()
+    xb, wb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    b = None if inp["bias"] is None else inp["bias"].cpu().numpy()
+    r_ids, r_w, r_logits = oracle.route(xb, wb, b, k)
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), r_logits.view(np.uint32))
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), r_w, rtol=1e-5, atol=1e-7)
+    assert np.allclose(w.sum(1).cpu().numpy(), 1.0, atol=1e-5)
+    if cfg.name == "finegrained_zipf":
+        counts = np.bincount(r_ids.ravel(), minlength=E)
+        assert (counts == 0).sum() >= 1
+        assert (counts > 0.05 * cfg.S).sum() >= 2
+
+
+# ------------------------------------------------------------ align-sort
+
+SORT_CASES = [(16, 2, 4, 16), (32, 2, 8, 16), (8192, 2, 8, 128), (4096, 8, 256, 128), (1, 1, 1, 1),
+              (3, 2, 3, 4), (700, 3, 1000, 32), (5000, 1, 7, 64), (2049, 4, 16, 128)]
+
+
+@pytest.mark.parametrize("T,k,E,B", SORT_CASES)
+def test_align_sort_parity(moe, T, k, E, B):
+    rng = np.random.default_rng(T * 7 + E)
+    # skewed expert popularity so that some experts get nothing
+    p = rng.dirichlet(np.full(E, 0.3))
+    ids = np.stack([rng.choice(E, k, replace=False, p=p) if E > k else rng.permutation(E)[:k]
+                    for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, k)).astype(np.float32)
+    P, NB = oracle.align_sort_sizes(T, k, E, B)
+    d_ids = torch.from_numpy(ids).cuda()
+    d_w = torch.from_numpy(wts).cuda()
+    s_ids = torch.full((P,), -7, dtype=torch.int32, device="cuda")
+    s_w = torch.full((P,), -7.0, dtype=torch.float32, device="cuda")
+    s_e = torch.full((NB,), -7, dtype=torch.int32, device="cuda")
+    npp = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(E, dtype=torch.int32, device="cuda")
+    wsb = moe.moe_align_sort_workspace_size(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    moe.moe_align_sort(d_ids, d_w, T, k, E, B, s_ids, s_w, s_e, npp, cnt, ws, wsb)
+    torch.cuda.synchronize()
+    r_ids, r_e, r_npp, r_cnt = oracle.align_sort(ids, E, B)
+    g_ids = s_ids.cpu().numpy()
+    assert np.array_equal(g_ids, r_ids)
+    assert np.array_equal(s_e.cpu().numpy(), r_e)
+    assert int(npp.item()) == r_npp
+    assert np.array_equal(cnt.cpu().numpy(), r_cnt)
+    S = T * k
+    ref_w = np.where(r_ids < S, wts.ravel()[np.minimum(r_ids, S - 1)], 0.0).astype(np.float32)
+    assert np.array_equal(s_w.cpu().numpy(), ref_w)
+    check_sort_invariants(ids, E, B, g_ids, s_e.cpu().numpy(), int(npp.item()), cnt.cpu().numpy())
+
+
+# ------------------------------------------------------------ FP8 codes
+
+def test_quant_act_bit_exact(moe):
+    g = torch.Generator(device="cuda").manual_seed(11)
+    X = (torch.randn(300, 1024, generator=g, device="cuda") *
+         torch.exp(torch.randn(300, 1, generator=g, device="cuda") * 3)).to(torch.bfloat16)
+    X[5, 256:384] = 0
+    q = torch.empty(300, 1024, dtype=torch.uint8, device="cuda")
+    s = torch.empty(300, 8, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_act(X, 300, 1024, q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_1x128(synth.bf16_bits(X))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_weights_bit_exact(moe):
+    cfg = synth.CONFIGS["tiny"].with_(E=3, H=256, I=384)
+    inp = synth.make_inputs(cfg, seed=3, device="cuda")
+    inp["W_down"][1, :128, :128] *= 1000.0  # a block with a very different scale
+    w = quantize_weights_gpu(moe, inp, cfg)
+    torch.cuda.synchronize()
+    for name, sname in (("W_gate_up", "w1_scale"), ("W_down", "w2_scale")):
+        rq, rs = oracle.quant_128x128(synth.bf16_bits(inp[name]))
+        assert np.array_equal(w[sname].cpu().numpy().view(np.uint32), rs.view(np.uint32))
+        assert np.array_equal(w[name].cpu().numpy(), rq)
+
+
+# --------------------------------------------------------- fused layer
+
+def _oracle_bf16(host, cfg, tokens):
+    return oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
+                                   cfg.k, tokens)
+
+
+def _check_intermediates(moe, layer, cfg, host):
+    """Routing and sort outputs inside the fused call's workspace are bit-exact."""
+    T, k, E = cfg.T, cfg.k, cfg.E
+    r_ids, r_w, _ = oracle.route(host["x"], host["W_router"], host["bias"], k)
+    ids = layer.view("topk_ids", torch.int32, (T, k)).cpu().numpy()
+    assert np.array_equal(ids, r_ids)
+    B = layer.plan.block_m
+    P, NB = layer.plan.max_padded, layer.plan.max_blocks
+    s_ids = layer.view("sorted_ids", torch.int32, (P,)).cpu().numpy()
+    s_e = layer.view("sorted_expert_ids", torch.int32, (NB,)).cpu().numpy()
+    o_ids, o_e, o_npp, o_cnt = oracle.align_sort(r_ids, E, B)
+    assert np.array_equal(s_ids, o_ids)
+    assert np.array_equal(s_e, o_e)
+    assert int(layer.view("num_tokens_post_padded", torch.int32, (1,)).item()) == o_npp
+    return r_ids
+
+
+FUSED_CASES = ["tiny", "mixtral_decode", "mixtral_prefill", "finegrained_zipf"]
+
+
+@pytest.mark.parametrize("name", FUSED_CASES)
+def test_fused_bf16_parity(moe, name):
+    cfg = synth.CONFIGS[name]
+    inp, host = gpu_inputs(cfg)
+    out, layer = run_fused(moe, cfg, inp)
+    r_ids = _check_intermediates(moe, layer, cfg, host)
+    toks = np.arange(cfg.T) if cfg.T <= 64 else sample_tokens(cfg, r_ids)
+    ref = _oracle_bf16(host, cfg, toks)
+    got = out.float().cpu().numpy()[toks]
+    assert np.isfinite(got).all()
+    err = rel_l2(got, ref)
+    print(f"{name}: relL2 {err:.3e} over {len(toks)} tokens")
+    assert err <= TOL_BF16
+
+
+def test_fused_fp8_parity(moe):
+    cfg = synth.CONFIGS["mixtral_fp8"]
+    inp, host = gpu_inputs(cfg)
+    fp8w = quantize_weights_gpu(moe, inp, cfg)
+    out, layer = run_fused(moe, cfg, inp, dtype=moe.MOE_FP8_BLOCK128, fp8w=fp8w)
+    r_ids = _check_intermediates(moe, layer, cfg, host)
+    # the oracle quantises the weights itself; its codes equal the GPU's (checked on a slice)
+    q1, s1 = oracle.quant_128x128(host["W_gate_up"])
+    q2, s2 = oracle.quant_128x128(host["W_down"])
+    assert np.array_equal(fp8w["W_gate_up"][0, :256].cpu().numpy(), q1[0, :256])
+    toks = sample_tokens(cfg, r_ids, n=48)
+    ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks)
+    got = out.float().cpu().numpy()[toks]
+    err = rel_l2(got, ref)
+    print(f"fp8: relL2 {err:.3e} over {len(toks)} tokens")
+    assert err <= TOL_FP8
+
+
+EDGE_CASES = [
+    # (name, T, H, I, E, k, bias, block_m, split_k)
+    ("t1", 1, 128, 256, 4, 2, None, 0, 0),
+    ("t3_e2", 3, 128, 256, 2, 2, None, 0, 0),
+    ("t17_e5", 17, 256, 384, 5, 2, "normal", 0, 0),
+    ("e1k1", 9, 128, 128, 1, 1, None, 0, 0),
+    ("k_eq_e", 11, 128, 256, 3, 3, None, 0, 0),
+    ("swap_t128", 128, 256, 256, 4, 2, None, 0, 0),
+    ("grouped_t129", 129, 256, 256, 4, 2, None, 0, 0),
+    ("grouped_ragged", 300, 384, 640, 6, 3, "normal", 0, 0),
+    ("swap_b32_sk2", 40, 256, 512, 4, 2, None, 32, 2),
+    ("swap_b128_sk1", 20, 256, 512, 4, 2, None, 128, 1),
+    ("swap_sk8", 8, 512, 1024, 8, 2, None, 0, 8),
+    ("grouped_h_odd", 200, 640, 256, 8, 2, "normal", 0, 0),
+]
+
+
+@pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: c[0])
+def test_fused_bf16_edge_cases(moe, case):
+    name, T, H, I, E, k, bias, bm, sk = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5)
+    inp = synth.make_inputs(cfg, seed=1, device="cuda")
+    host = {kk: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+            for kk, v in inp.items()}
+    out, layer = run_fused(moe, cfg, inp, block_m=bm, split_k=sk)
+    _check_intermediates(moe, layer, cfg, host)
+    ref = _oracle_bf16(host, cfg, np.arange(T))
+    err = rel_l2(out.float().cpu().numpy(), ref)
+    assert err <= TOL_BF16, err
+
+
+@pytest.mark.parametrize("case", [("fp8_small", 40, 256, 384, 4, 2, None), ("fp8_ragged", 257, 384, 256, 6, 3, "normal"),
+                                  ("fp8_t1", 1, 128, 256, 4, 2, None)], ids=lambda c: c[0])
+def test_fused_fp8_edge_cases(moe, case):
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="fp8")
+    inp = synth.make_inputs(cfg, seed=2, device="cuda")
+    host = {kk: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+            for kk, v in inp.items()}
+    fp8w = quantize_weights_gpu(moe, inp, cfg)
+    out, layer = run_fused(moe, cfg, inp, dtype=moe.MOE_FP8_BLOCK128, fp8w=fp8w)
+    _check_intermediates(moe, layer, cfg, host)
+    q1, s1 = oracle.quant_128x128(host["W_gate_up"])
+    q2, s2 = oracle.quant_128x128(host["W_down"])
+    ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, k, np.arange(T))
+    err = rel_l2(out.float().cpu().numpy(), ref)
+    assert err <= TOL_FP8, err
+
+
+def test_fused_deterministic_and_unused_experts_not_read(moe):
+    cfg = synth.MoEConfig("nan_test", T=24, H=256, I=256, E=16, k=2)
+    inp = synth.make_inputs(cfg, seed=5, device="cuda")
+    out1, layer = run_fused(moe, cfg, inp)
+    out2, _ = run_fused(moe, cfg, inp)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    ids = layer.view("topk_ids", torch.int32, (cfg.T, cfg.k)).cpu().numpy()
+    unused = sorted(set(range(cfg.E)) - set(ids.ravel().tolist()))
+    assert unused
+    for e in unused:
+        inp["W_gate_up"][e] = float("nan")
+        inp["W_down"][e] = float("nan")
+    out3, _ = run_fused(moe, cfg, inp)
+    assert torch.equal(out1.view(torch.int16), out3.view(torch.int16))
+    # the grouped kernel too
+    cfg2 = cfg.with_(T=300)
+    inp2 = synth.make_inputs(cfg2, seed=6, device="cuda")
+    o1, lay2 = run_fused(moe, cfg2, inp2)
+    ids2 = lay2.view("topk_ids", torch.int32, (cfg2.T, cfg2.k)).cpu().numpy()
+    unused2 = sorted(set(range(cfg2.E)) - set(ids2.ravel().tolist()))
+    for e in unused2:
+        inp2["W_gate_up"][e] = float("nan")
+        inp2["W_down"][e] = float("nan")
+    o2, _ = run_fused(moe, cfg2, inp2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_fused_host_entry_matches_device_entry(moe):
+    cfg = synth.CONFIGS["tiny"].with_(T=50)
+    inp = synth.make_inputs(cfg, seed=8, device="cuda")
+    out_dev, _ = run_fused(moe, cfg, inp)
+    layer = moe.FusedMoE(0, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, host_staging=True)
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(x_host, {"W_router": inp["W_router"], "bias": None, "W_gate_up": inp["W_gate_up"],
+                                "W_down": inp["W_down"]}, out_host)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))

@@ -15,6 +15,7 @@ import torch
 import oracle
 from oracle import heuristics
 from mixture_experts_grouped_moe_gb300 import synth
+from moe_checks import check_sort_invariants
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -227,33 +228,6 @@ def test_align_sort_brute_force_all_small_routings():
                         assert list(cnt) == [int((ids == e).sum()) for e in range(E)]
                         n_cases += 1
     assert n_cases > 1000
-
-
-def check_sort_invariants(ids, E, B, sorted_ids, sorted_eids, npp, counts):
-    """Properties any correct align-sort output has (used for oracle and GPU)."""
-    T, k = ids.shape
-    S = T * k
-    P, NB = oracle.align_sort_sizes(T, k, E, B)
-    assert sorted_ids.shape == (P,) and sorted_eids.shape == (NB,)
-    assert counts.sum() == S
-    assert npp % B == 0 and npp <= P
-    real = sorted_ids[sorted_ids != S]
-    assert np.array_equal(np.sort(real), np.arange(S))
-    assert np.all(sorted_ids[npp:] == S)
-    used = sorted_eids[: npp // B]
-    assert np.all(np.diff(used) >= 0)
-    assert np.all(sorted_eids[npp // B:] == -1)
-    pos = 0
-    for e in range(E):
-        c = int(counts[e])
-        pad = -(-c // B) * B
-        seg = sorted_ids[pos:pos + pad]
-        assert np.all(ids.flat[seg[:c]] == e)
-        assert np.all(np.diff(seg[:c]) > 0)
-        assert np.all(seg[c:] == S)
-        assert np.all(sorted_eids[pos // B:(pos + pad) // B] == e)
-        pos += pad
-    assert pos == npp
 
 
 def test_align_sort_invariants_random():
