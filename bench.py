@@ -175,6 +175,9 @@ def run_cuda(args, cfg, rank, world, local_rank):
         raise RuntimeError("device wait timed out during warm-up")
     counts = layer.view("expert_counts", torch.int32, (cfg.E,)).cpu().numpy().tolist()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for row in ev:  # torch creates the CUDA event on first record; the handles must exist before use
+        for e in row:
+            e.record(stream)
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
 
@@ -238,11 +241,10 @@ def cpu_baseline(cfg, host, budget_s=20.0):
     toks = synth.token_sample(cfg.T, n).numpy()
     t0 = time.perf_counter()
     run_oracle(cfg, host, toks)
-    dt = time.perf_counter() - t0
-    reps = 1
-    while time.perf_counter() - t0 < min(budget_s, 3 * dt + 1e-9) and n * (reps + 1) <= 4 * cfg.T and dt * (reps + 1) < budget_s:
+    first = time.perf_counter() - t0
+    reps = 1 + max(0, min(9, int(budget_s / max(first, 1e-6)) - 1))
+    for _ in range(reps - 1):
         run_oracle(cfg, host, toks)
-        reps += 1
     dt = (time.perf_counter() - t0) / reps
     return {"value": n / dt, "unit": "tokens/s", "cores": oracle.default_threads(), "kind": "oracle",
             "sample": f"{n} of the {cfg.T} tokens, full layer per token (fp64 CPU oracle), {reps} run(s)"}
@@ -363,7 +365,7 @@ def main():
         "plan": {"mode": "swap" if r["plan"].mode == 1 else "grouped", "block_m": r["plan"].block_m,
                  "split_k2": r["plan"].split_k2},
     }
-    if not args.no_cpu_baseline and world == 1 or (world > 1 and rank == 0 and not args.no_cpu_baseline):
+    if not args.no_cpu_baseline:
         import torch
         host = host_inputs(cfg, torch.device("cuda", local_rank))
         line["cpu_baseline"] = cpu_baseline(cfg, host)
