@@ -238,6 +238,35 @@ int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, 
                            int split_k, void *out_host, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_align_sort without a caller workspace.  (The fused-MoE pages have no
+ * counterpart: this entry exists for callers of this library.)
+ *
+ * For callers that cannot allocate device memory themselves -- code that
+ * must not call cudaMalloc because a host framework owns every device
+ * allocation through its own pool, runs under a fixed memory budget, or
+ * cannot afford the implicit synchronisation of an allocation on its hot
+ * path.  They pass the same inputs and outputs as moe_align_sort, but no ws.
+ *
+ * The scratch is a fixed array of MOE_NOALLOC_SORT_SCRATCH_BYTES in the
+ * library's own device memory; every GPU that loads the library holds it
+ * until the process exits.  The first call on each device looks up the
+ * array's device address (with that device current), so make that first
+ * call before any stream capture.  Nothing is allocated, by this library or
+ * any library it calls.  Shapes whose scratch (one int32 per expert per
+ * 1024 slots, plus E+1 offsets) does not fit return MOE_ERR_UNSUPPORTED;
+ * use moe_align_sort with a workspace for those.  All calls share the one
+ * array and it keeps the last call's contents: calls that overlap on the GPU
+ * (on different streams, or from different host threads without ordering)
+ * race on it and must be serialised by the caller.
+ */
+#define MOE_NOALLOC_SORT_SCRATCH_BYTES (1 << 20)
+
+int moe_align_sort_noalloc(const int32_t *topk_ids, const float *topk_weights, int T, int k, int E,
+                           int block_m, int32_t *sorted_ids, float *sorted_weights,
+                           int32_t *sorted_expert_ids, int32_t *num_tokens_post_padded,
+                           int32_t *expert_counts, void *stream);
+
+/*
  * Optional per-stage timing for the next moe_fused_forward (or _host) call
  * made by the calling host thread: `events` (host array of n >= 7 CUDA
  * events, cudaEvent_t cast to void*, created by the caller) are recorded on

@@ -31,7 +31,7 @@ EXPORTED = [
     "moe_ksplit_heuristic", "moe_plan", "moe_fused_workspace_size", "moe_workspace_layout",
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_fused_forward", "moe_host_staging_bytes",
-    "moe_fused_forward_host", "moe_set_stage_events",
+    "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
 ]
 
 
@@ -94,6 +94,7 @@ def load(build_if_missing: bool = False):
             "moe_host_staging_bytes": (SZ, [I, I]),
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_set_stage_events": (I, [P, I]),
+            "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -192,6 +193,14 @@ def moe_align_sort(topk_ids, topk_weights, T, k, E, block_m, sorted_ids, sorted_
         _p(topk_ids), _p(topk_weights), T, k, E, block_m, _p(sorted_ids), _p(sorted_weights),
         _p(sorted_expert_ids), _p(num_tokens_post_padded), _p(expert_counts), _p(ws), ws_bytes,
         _stream(stream)))
+
+
+def moe_align_sort_noalloc(topk_ids, topk_weights, T, k, E, block_m, sorted_ids, sorted_weights,
+                           sorted_expert_ids, num_tokens_post_padded, expert_counts, stream=None):
+    """moe_align_sort with the library's fixed device scratch instead of a caller workspace."""
+    return _check("moe_align_sort_noalloc", load().moe_align_sort_noalloc(
+        _p(topk_ids), _p(topk_weights), T, k, E, block_m, _p(sorted_ids), _p(sorted_weights),
+        _p(sorted_expert_ids), _p(num_tokens_post_padded), _p(expert_counts), _stream(stream)))
 
 
 def moe_quantize_fp8_act(X, R, C, q, s, stream=None):
