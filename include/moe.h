@@ -163,6 +163,9 @@ int moe_workspace_status(const void *ws, int *status, void *stream);
  *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H];
  *   bias (device) fp32 [E] or NULL; topk_ids (device) int32 [T][k];
  *   topk_weights (device) fp32 [T][k]; logits (device) fp32 [T][E] or NULL.
+ * With logits given and T*E > 4096 the logits are computed by a tiled pass
+ * and the top-k by a second pass (faster for large T*E); otherwise one fused
+ * launch.  Both give the same bits.
  */
 int moe_route_topk(const void *x, const void *W_router, const float *bias, int T, int H, int E, int k,
                    int32_t *topk_ids, float *topk_weights, float *logits, void *stream);

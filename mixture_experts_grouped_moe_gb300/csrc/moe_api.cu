@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -57,6 +58,21 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+bool pdl_enabled(int site, bool grouped)
+{
+    static const int env_mask = [] {
+        const char *off = getenv("MOE_PDL");
+        if (off && off[0] == '0')
+            return 0;
+        const char *m = getenv("MOE_PDL_MASK");
+        return m ? (int)strtol(m, nullptr, 16) : -1;
+    }();
+    int mask = env_mask;
+    if (mask < 0)
+        mask = grouped ? 0x3f & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : 0x3f;
+    return (mask >> site) & 1;
+}
+
 int num_sms_current_device()
 {
     static int cache[64] = {0};
@@ -74,7 +90,7 @@ int num_sms_current_device()
 
 // Workspace carve-up (byte offsets from ws).
 struct Layout {
-    int64_t status, topk_ids, topk_w, sort_scratch, counts, offsets, active, num_active, npp;
+    int64_t status, logits, topk_ids, topk_w, sort_scratch, counts, offsets, active, num_active, npp;
     int64_t sorted_ids, sorted_w, sorted_eids, slot_pos;
     int64_t x_sorted, x_scales, inter, inter_scales, y, partials;
     int64_t total;
@@ -109,6 +125,7 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
         return o;
     };
     L.status = take(16);
+    L.logits = take((int64_t)T * E * 4);
     L.topk_ids = take(S * 4);
     L.topk_w = take(S * 4);
     L.sort_scratch = take((int64_t)sort_scratch_bytes(T, k, E));
@@ -236,12 +253,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     int *status = static_cast<int *>(at(L.status));
     mark(0, st);
-    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess)
-        return MOE_ERR_CUDA;
     int32_t *topk_ids = static_cast<int32_t *>(at(L.topk_ids));
     float *topk_w = static_cast<float *>(at(L.topk_w));
-    launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router), router_bias,
-                  T, H, E, k, topk_ids, topk_w, nullptr, st);
+    // the first kernel follows arbitrary caller work: a normal launch; it also zeroes the status word
+    if (launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
+                      router_bias, T, H, E, k, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status, false,
+                      st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     mark(1, st);
 
     SortOut so;
@@ -254,19 +272,22 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     so.active_experts = static_cast<int32_t *>(at(L.active));
     so.num_active = static_cast<int32_t *>(at(L.num_active));
     so.slot_pos = static_cast<int32_t *>(at(L.slot_pos));
-    launch_align_sort(topk_ids, topk_w, T, k, E, p.block_m, so, at(L.sort_scratch), st);
+    if (launch_align_sort(topk_ids, topk_w, T, k, E, p.block_m, so, at(L.sort_scratch), pdl_enabled(kPdlSort),
+                          st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     mark(2, st);
 
     const int64_t P = p.max_padded;
     const int eb = (dtype == MOE_BF16) ? 2 : 1;
+    cudaError_t ge;
     if (dtype == MOE_BF16)
-        launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
-                           static_cast<__nv_bfloat16 *>(at(L.x_sorted)), st);
+        ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
+                                static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_enabled(kPdlGather), st);
     else
-        launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k,
-                                 H, P, static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
-                                 st);
-    if (cudaGetLastError() != cudaSuccess)
+        ge = launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S,
+                                      k, H, P, static_cast<uint8_t *>(at(L.x_sorted)),
+                                      static_cast<float *>(at(L.x_scales)), pdl_enabled(kPdlGather), st);
+    if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
     mark(3, st);
 
@@ -341,13 +362,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     // ----------------------------------------------------------- combine
     if (p.split_k2 > 1)
-        launch_splitk_combine(g2.partials, p.split_k2, P, so.slot_pos, topk_w, T, k, H,
-                              static_cast<__nv_bfloat16 *>(out), st);
+        ce = launch_splitk_combine(g2.partials, p.split_k2, P, so.slot_pos, topk_w, T, k, H,
+                                   static_cast<__nv_bfloat16 *>(out), pdl_enabled(kPdlCombine), st);
     else
-        launch_combine(g2.y, T, k, H, static_cast<__nv_bfloat16 *>(out), st);
+        ce = launch_combine(g2.y, T, k, H, static_cast<__nv_bfloat16 *>(out), pdl_enabled(kPdlCombine), st);
     mark(6, st);
     t_stage_armed = false;
-    return cuda_status(cudaGetLastError());
+    return cuda_status(ce);
 }
 
 }  // namespace moe
@@ -506,9 +527,9 @@ int moe_route_topk(const void *x, const void *W_router, const float *bias, int T
         return MOE_OK;
     if (!x || !W_router || !topk_ids || !topk_weights || !aligned(x, 16) || !aligned(W_router, 16))
         return MOE_ERR_INVALID_ARG;
-    launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router), bias, T, H,
-                  E, k, topk_ids, topk_weights, logits, static_cast<cudaStream_t>(stream));
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_router(static_cast<const __nv_bfloat16 *>(x),
+                                     static_cast<const __nv_bfloat16 *>(W_router), bias, T, H, E, k, topk_ids,
+                                     topk_weights, logits, nullptr, false, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_align_sort_workspace_size(int T, int k, int E)
@@ -542,8 +563,8 @@ int moe_align_sort(const int32_t *topk_ids, const float *topk_weights, int T, in
     so.expert_counts = expert_counts;
     so.expert_offsets = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) +
                                                     align_up((int64_t)sort_scratch_bytes(T, k, E), kAlign));
-    launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, ws, static_cast<cudaStream_t>(stream));
-    return cuda_status(cudaGetLastError());
+    return cuda_status(
+        launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, ws, false, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_quantize_fp8_act(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream)

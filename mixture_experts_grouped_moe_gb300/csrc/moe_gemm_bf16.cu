@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
+    // everything above is independent of earlier kernels; from here on their outputs are read
+    pdl_wait();
+    pdl_trigger();
     const int ntiles = num_tiles<MODE, STAGE>(a);
 
     if (warp == 0) {
@@ -420,8 +423,8 @@ cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(pdl_enabled(STAGE == 1 ? kPdlStage1 : kPdlStage2, MODE == MOE_MODE_GROUPED), kern,
+                         dim3(grid), dim3(kThreads), kSmemBytes, st, a);
 }
 
 }  // namespace bf16gemm

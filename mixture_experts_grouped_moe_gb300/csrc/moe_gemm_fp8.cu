@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
+    // everything above is independent of earlier kernels; from here on their outputs are read
+    pdl_wait();
+    pdl_trigger();
     const int nmb = *a.num_post_padded / 128;
     const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
     const int ntiles = nmb * nnt;
@@ -234,7 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < 64; ++i)
                 acc0[i] = 0.0f, acc1[i] = 0.0f;
+            // the scales of block kb+1 are fetched while block kb is still on the tensor core
+            float sx_n = a.x_scales[pos], s0_n = sw0[0], s1_n = sw1[0];
             for (int kb = 0; kb < nkb; ++kb) {
+                const float sx = sx_n, s0 = s0_n, s1 = s1_n;
+                if (kb + 1 < nkb) {
+                    sx_n = a.x_scales[(size_t)(kb + 1) * a.P_max + pos];
+                    s0_n = sw0[kb + 1];
+                    s1_n = sw1[kb + 1];
+                }
                 bool w_ok = mbar_wait(&sm.tfull[buf], bph, a.status, abort_flag);
                 w_ok = __all_sync(0xffffffffu, w_ok);
                 if (!w_ok) {
@@ -242,9 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                     break;
                 }
                 tc_fence_after();
-                const float sx = a.x_scales[(size_t)kb * a.P_max + pos];
-                const float f0 = sx * sw0[kb];
-                const float f1 = sx * sw1[kb];
+                const float f0 = sx * s0;
+                const float f1 = sx * s1;
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
 #pragma unroll
                 for (int c = 0; c < 64; c += 32) {
@@ -339,8 +349,8 @@ cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(pdl_enabled(STAGE == 1 ? kPdlStage1 : kPdlStage2, true), kern, dim3(grid),
+                         dim3(kThreads), kSmemBytes, st, a);
 }
 
 }  // namespace fp8gemm

@@ -12,12 +12,66 @@
 
 #include "../../include/moe.h"
 
+#include <utility>
+
 namespace moe {
+
+// ------------------------------------------------ programmatic dependent launch
+//
+// Kernels after the first one of an entry point are launched with
+// programmatic stream serialisation: a kernel may be scheduled while its
+// predecessor drains, runs its prologue, and blocks in pdl_wait() until the
+// predecessor has completed and its writes are visible.  Every kernel calls
+// pdl_wait() before reading anything a previous kernel wrote (and before
+// writing anything a previous kernel reads), and pdl_trigger() to let its
+// own successor be scheduled.  Both are no-ops for a normal launch.
+
+#if defined(__CUDACC__)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
+// Launch boundaries that may overlap (bit i of MOE_PDL_MASK, default all):
+enum PdlSite {
+    kPdlSort = 0,     // router/top-k -> sort, and inside the sort
+    kPdlGather = 1,   // sort -> gather
+    kPdlStage1 = 2,   // gather -> stage 1
+    kPdlStage2 = 3,   // stage 1 -> stage 2
+    kPdlCombine = 4,  // stage 2 -> combine
+    kPdlTopk = 5,     // logit pass -> top-k pass
+};
+// Whether launches at this site use programmatic serialisation: environment
+// MOE_PDL=0 turns it off everywhere, MOE_PDL_MASK (hex) selects sites.
+// Default: every site, except the two GEMM boundaries in grouped mode, where
+// an early-resident persistent GEMM measured slower (Mixtral prefill 3.94 ms
+// without vs 4.38 ms with) while swap mode gains from it.
+bool pdl_enabled(int site, bool grouped = false);
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------ route / sort / aux
 
-void launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
-                   int k, int32_t *ids, float *wts, float *logits, cudaStream_t st);
+// Small T*E: one fused launch.  Large T*E: a tiled logit pass into `logits`
+// (fp32 [T][E], required then) followed by a warp-per-token top-k pass.
+// `status` (nullable) is zeroed by the first kernel.  `pdl` applies to the first launch.
+bool router_needs_logits(int T, int E);
+cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
+                          int k, int32_t *ids, float *wts, float *logits, int *status, bool pdl, cudaStream_t st);
 
 // Chunked stable counting sort; ws holds nchunks*E int32 chunk counters.
 constexpr int kSortChunk = 1024;
@@ -34,24 +88,24 @@ struct SortOut {
     int32_t *num_active;      // [1] (may be null)
     int32_t *slot_pos;        // [S] sorted position of each slot (may be null)
 };
-void launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
-                       const SortOut &o, void *scratch, cudaStream_t st);
+cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
+                              const SortOut &o, void *scratch, bool pdl, cudaStream_t st);
 
 // x rows gathered into sorted order (zero rows for padding), up to *npp rows.
-void launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
-                        int H, int64_t P_max, __nv_bfloat16 *xs, cudaStream_t st);
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
+                               int H, int64_t P_max, __nv_bfloat16 *xs, bool pdl, cudaStream_t st);
 // Same, quantised per 1x128 group: codes [P_max][H], scales transposed [H/128][P_max].
-void launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
-                              int k, int H, int64_t P_max, uint8_t *q, float *sT, cudaStream_t st);
+cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
+                                     int k, int H, int64_t P_max, uint8_t *q, float *sT, bool pdl, cudaStream_t st);
 
 void launch_quant_act(const __nv_bfloat16 *X, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
 void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
 
 // out[t] = sum_j Y[t*k+j] (j ascending), fp32 -> bf16.
-void launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st);
+cudaError_t launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st);
 // out[t] = sum_j w[t*k+j] * sum_ks P[ks][slot_pos[t*k+j]]  (split-K stage-2 partials).
-void launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
-                           int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st);
+cudaError_t launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
+                                  int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st);
 
 // --------------------------------------------------------------- GEMMs
 
@@ -90,6 +144,7 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
 
 int num_sms_current_device();
 
+// The GEMMs are always launched with programmatic serialisation (they follow another kernel).
 cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);

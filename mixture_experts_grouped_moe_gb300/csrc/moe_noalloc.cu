@@ -76,6 +76,7 @@ extern "C" int moe_align_sort_noalloc(const int32_t *topk_ids, const float *topk
     so.num_post_padded = num_tokens_post_padded;
     so.expert_counts = expert_counts;
     so.expert_offsets = scratch + off_at;
-    launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, scratch, static_cast<cudaStream_t>(stream));
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    const cudaError_t err =
+        launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, scratch, false, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

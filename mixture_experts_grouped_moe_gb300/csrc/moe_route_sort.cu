@@ -1,6 +1,7 @@
 // Router (gating + warp-shuffle top-k), align-sort by expert, row gathers,
 // block-scaled FP8 quantisation and the weighted combine of the fused MoE
-// layer.  These are the memory-bound steps around the two group GEMMs.
+// layer.  These are the memory- and latency-bound steps around the two
+// group GEMMs.
 //
 // Sources (fused-MoE pages): AITER walk-through section 3 ("Fused MoE":
 // gating -> token reorder -> expert GEMMs -> weighted combine), section 3.1
@@ -29,23 +30,85 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float (&f)[8])
 
 // ================================================================ router
 //
-// logit[t][e] in fp32, fixed order: lane L of a warp accumulates (with one
+// logit[t][e] in fp32, one fixed order: lane L of a warp accumulates (one
 // rounding per element; a bf16 x bf16 product is exact in fp32) the
 // elements h with (h / 8) mod 32 == L in ascending h, then a xor butterfly
 // with strides 16, 8, 4, 2, 1 combines the 32 partials; the bias is added
-// last.  A CTA takes TT tokens; each warp takes groups of EG experts.  The
-// logits of the CTA's tokens go to shared memory; then one warp per token
-// selects the top k by repeated warp arg-max (larger logit first, lower
-// expert on ties) and takes the softmax over the selected logits.
+// last.  Any tiling that keeps each lane's partial in this order gives the
+// same bits, so the two kernels below agree with each other and with the
+// CPU oracle.
 
-template <int TT, int EG>
-__global__ void __launch_bounds__(256) router_kernel(const __nv_bfloat16 *__restrict__ x,
-                                                     const __nv_bfloat16 *__restrict__ Wr,
-                                                     const float *__restrict__ bias, int T, int H, int E, int k,
-                                                     int32_t *__restrict__ ids, float *__restrict__ wts,
-                                                     float *__restrict__ logits_out)
+__device__ __forceinline__ float butterfly_sum(float v)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// Top k of one token's E logits by one warp (larger logit first, the lower
+// expert on ties), then the softmax over the k selected.  k <= 32, E <= 1024.
+__device__ __forceinline__ void warp_topk_softmax(const float *lg, int E, int k, int lane, int32_t *ids_out,
+                                                  float *w_out)
+{
+    uint32_t taken = 0;  // bit m: expert lane + 32m already selected
+    float my_v = 0.0f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -FLT_MAX;
+        int be = INT_MAX;
+        for (int m = 0, e = lane; e < E; ++m, e += 32) {
+            if (taken & (1u << m))
+                continue;
+            const float v = lg[e];
+            if (be == INT_MAX || v > bv) {  // ascending e: ties keep the lower expert
+                bv = v;
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane)
+            taken |= 1u << (be >> 5);
+        if (lane == j) {
+            my_v = bv;
+            my_e = be;
+        }
+    }
+    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j)
+        sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+        ids_out[lane] = my_e;
+        w_out[lane] = ex / sum;
+    }
+}
+
+// Small T*E (decode): a CTA takes TT tokens, each warp groups of EG experts;
+// each lane keeps UNR 256-element rounds of loads in flight.  The CTA's
+// logits go to shared memory and one warp per token selects the top k.
+template <int TT, int EG, int UNR>
+__global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                           const __nv_bfloat16 *__restrict__ Wr,
+                                                           const float *__restrict__ bias, int T, int H, int E,
+                                                           int k, int32_t *__restrict__ ids,
+                                                           float *__restrict__ wts, float *__restrict__ logits_out,
+                                                           int *status)
 {
     extern __shared__ float s_logit[];  // [TT][E]
+    pdl_wait();
+    pdl_trigger();
+    if (status && blockIdx.x == 0 && threadIdx.x == 0)
+        *status = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TT;
     const int ngroups = (E + EG - 1) / EG;
@@ -57,40 +120,48 @@ __global__ void __launch_bounds__(256) router_kernel(const __nv_bfloat16 *__rest
 #pragma unroll
             for (int j = 0; j < EG; ++j)
                 acc[t][j] = 0.0f;
-#pragma unroll 2
-        for (int h0 = lane * 8; h0 < H; h0 += 256) {
-            float wf[EG][8];
+        for (int hb = 0; hb < H; hb += 256 * UNR) {
+            uint4 wv[UNR][EG], xv[UNR][TT];
 #pragma unroll
-            for (int j = 0; j < EG; ++j) {
-                const int e = g * EG + j;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (e < E)
-                    v = __ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0));
-                bf16x8_to_float(v, wf[j]);
+            for (int u = 0; u < UNR; ++u) {
+                const int h0 = hb + u * 256 + lane * 8;
+#pragma unroll
+                for (int j = 0; j < EG; ++j) {
+                    const int e = g * EG + j;
+                    wv[u][j] = (h0 < H && e < E) ? __ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0))
+                                                 : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    const int tok = t0 + t;
+                    xv[u][t] = (h0 < H && tok < T)
+                                   ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)tok * H + h0))
+                                   : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                const int tok = t0 + t;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (tok < T)
-                    v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)tok * H + h0));
-                float xf[8];
-                bf16x8_to_float(v, xf);
+            for (int u = 0; u < UNR; ++u) {
+                float wf[EG][8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
+                for (int j = 0; j < EG; ++j)
+                    bf16x8_to_float(wv[u][j], wf[j]);
 #pragma unroll
-                    for (int j = 0; j < EG; ++j)
-                        acc[t][j] = __fmaf_rn(xf[c], wf[j][c], acc[t][j]);
+                for (int t = 0; t < TT; ++t) {
+                    float xf[8];
+                    bf16x8_to_float(xv[u][t], xf);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+#pragma unroll
+                        for (int j = 0; j < EG; ++j)
+                            acc[t][j] = __fmaf_rn(xf[c], wf[j][c], acc[t][j]);
+                }
             }
         }
 #pragma unroll
         for (int t = 0; t < TT; ++t)
 #pragma unroll
             for (int j = 0; j < EG; ++j) {
-                float v = acc[t][j];
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1)
-                    v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+                float v = butterfly_sum(acc[t][j]);
                 const int e = g * EG + j;
                 if (lane == 0 && e < E) {
                     if (bias)
@@ -109,68 +180,177 @@ __global__ void __launch_bounds__(256) router_kernel(const __nv_bfloat16 *__rest
         if (logits_out)
             for (int e = lane; e < E; e += 32)
                 logits_out[(size_t)tok * E + e] = lg[e];
-        uint32_t taken = 0;  // bit m: expert lane + 32m already selected
-        float my_v = 0.0f;
-        int my_e = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = -FLT_MAX;
-            int be = INT_MAX;
-            for (int m = 0, e = lane; e < E; ++m, e += 32) {
-                if (taken & (1u << m))
-                    continue;
-                const float v = lg[e];
-                if (be == INT_MAX || v > bv) {  // ascending e: ties keep the lower expert
-                    bv = v;
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane)
-                taken |= 1u << (be >> 5);
-            if (lane == j) {
-                my_v = bv;
-                my_e = be;
-            }
-        }
-        const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-        const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
-        float sum = 0.0f;
-        for (int j = 0; j < k; ++j)
-            sum += __shfl_sync(0xffffffffu, ex, j);
-        if (lane < k) {
-            ids[(size_t)tok * k + lane] = my_e;
-            wts[(size_t)tok * k + lane] = ex / sum;
-        }
+        warp_topk_softmax(lg, E, k, lane, ids + (size_t)tok * k, wts + (size_t)tok * k);
     }
 }
 
-void launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
-                   int k, int32_t *ids, float *wts, float *logits, cudaStream_t st)
+// Large T*E: a CTA computes a (WT*NWT tokens) x (WE*NWE experts) tile of
+// logits.  256-element rounds of x and W_router rows are staged in shared
+// memory (double-buffered cp.async, zero-filled past T, E or H); warp
+// (wt, we) computes WT x WE logits, lane L reading its 16-byte slice of each
+// staged row, so every partial keeps the fixed order above.
+constexpr int kRouterStages = 4;
+
+template <int WT, int WE, int NWT, int NWE>
+constexpr size_t router_tiled_smem()
+{
+    return (size_t)kRouterStages * (WT * NWT + WE * NWE) * 256 * sizeof(__nv_bfloat16);
+}
+
+template <int WT, int WE, int NWT, int NWE>
+__global__ void __launch_bounds__(256) router_tiled_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                           const __nv_bfloat16 *__restrict__ Wr,
+                                                           const float *__restrict__ bias, int T, int H, int E,
+                                                           float *__restrict__ logits, int *status)
+{
+    constexpr int TT = WT * NWT, EC = WE * NWE, ROWS = TT + EC;
+    static_assert(NWT * NWE == 8, "8 warps");
+    extern __shared__ __align__(16) uint8_t s_raw[];
+    auto s_rows = reinterpret_cast<__nv_bfloat16(*)[ROWS][256]>(s_raw);  // [kRouterStages][ROWS][256]
+    pdl_wait();
+    pdl_trigger();
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        *status = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * TT, e0 = blockIdx.y * EC;
+    const int wt = warp / NWE, we = warp % NWE;
+    const int nchunks = (H + 255) / 256;
+
+    auto stage = [&](int c, int b) {
+        for (int v = threadIdx.x; v < ROWS * 32; v += 256) {
+            const int r = v >> 5, col = (v & 31) * 8;
+            const int h = c * 256 + col;
+            const __nv_bfloat16 *src;
+            bool ok;
+            if (r < TT) {
+                ok = (t0 + r < T) && h < H;
+                src = x + (size_t)(ok ? t0 + r : 0) * H + (ok ? h : 0);
+            } else {
+                ok = (e0 + r - TT < E) && h < H;
+                src = Wr + (size_t)(ok ? e0 + r - TT : 0) * H + (ok ? h : 0);
+            }
+            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&s_rows[b][r][col]));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float acc[WT][WE];
+#pragma unroll
+    for (int t = 0; t < WT; ++t)
+#pragma unroll
+        for (int j = 0; j < WE; ++j)
+            acc[t][j] = 0.0f;
+
+    // kRouterStages-deep ring: chunk c lives in buffer c % kRouterStages; one commit group per
+    // chunk (empty past the end) so that "all but the newest kRouterStages-1 groups" = chunk c.
+    for (int c = 0; c < kRouterStages - 1; ++c) {
+        if (c < nchunks)
+            stage(c, c);
+        else
+            asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        const int b = c % kRouterStages;
+        const int cn = c + kRouterStages - 1;
+        if (cn < nchunks)
+            stage(cn, cn % kRouterStages);
+        else
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRouterStages - 1) : "memory");
+        __syncthreads();
+        float xf[WT][8];
+#pragma unroll
+        for (int t = 0; t < WT; ++t)
+            bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][wt * WT + t][lane * 8]), xf[t]);
+#pragma unroll
+        for (int j = 0; j < WE; ++j) {
+            float wf[8];
+            bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][TT + we * WE + j][lane * 8]), wf);
+#pragma unroll
+            for (int t = 0; t < WT; ++t)
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    acc[t][j] = __fmaf_rn(xf[t][cc], wf[cc], acc[t][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int t = 0; t < WT; ++t)
+#pragma unroll
+        for (int j = 0; j < WE; ++j) {
+            float v = butterfly_sum(acc[t][j]);
+            const int tok = t0 + wt * WT + t, e = e0 + we * WE + j;
+            if (lane == 0 && tok < T && e < E) {
+                if (bias)
+                    v = __fadd_rn(v, bias[e]);
+                logits[(size_t)tok * E + e] = v;
+            }
+        }
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                  int32_t *__restrict__ ids, float *__restrict__ wts)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (tok >= T)
+        return;
+    warp_topk_softmax(logits + (size_t)tok * E, E, k, threadIdx.x & 31, ids + (size_t)tok * k, wts + (size_t)tok * k);
+}
+
+bool router_needs_logits(int T, int E) { return (long)T * E > 64L * 64; }
+
+template <int WT, int WE, int NWT, int NWE>
+static cudaError_t launch_router_tiled(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T,
+                                       int H, int E, float *logits, int *status, bool pdl, cudaStream_t st)
+{
+    auto kern = router_tiled_kernel<WT, WE, NWT, NWE>;
+    constexpr size_t smem = router_tiled_smem<WT, WE, NWT, NWE>();
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess)
+        return err;
+    return launch_kernel(pdl, kern, dim3((T + WT * NWT - 1) / (WT * NWT), (E + WE * NWE - 1) / (WE * NWE)),
+                         dim3(256), smem, st, x, Wr, bias, T, H, E, logits, status);
+}
+
+cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
+                          int k, int32_t *ids, float *wts, float *logits, int *status, bool pdl, cudaStream_t st)
 {
     if (T <= 0)
-        return;
-    if ((long)T * E <= 256L * 64) {
-        constexpr int TT = 2;
-        const size_t sm = sizeof(float) * TT * E;
-        router_kernel<TT, 1><<<(T + TT - 1) / TT, 256, sm, st>>>(x, Wr, bias, T, H, E, k, ids, wts, logits);
-    } else {
+        return cudaSuccess;
+    if (!router_needs_logits(T, E) || !logits) {
+        if ((long)T * E <= 64L * 64) {
+            constexpr int TT = 2;
+            return launch_kernel(pdl, router_small_kernel<TT, 1, 8>, dim3((T + TT - 1) / TT), dim3(256),
+                                 sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, ids, wts, logits, status);
+        }
         constexpr int TT = 8;
-        const size_t sm = sizeof(float) * TT * E;
-        router_kernel<TT, 4><<<(T + TT - 1) / TT, 256, sm, st>>>(x, Wr, bias, T, H, E, k, ids, wts, logits);
+        return launch_kernel(pdl, router_small_kernel<TT, 4, 2>, dim3((T + TT - 1) / TT), dim3(256),
+                             sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, ids, wts, logits, status);
     }
+    cudaError_t err;
+    if (E <= 8)
+        err = launch_router_tiled<2, 8, 8, 1>(x, Wr, bias, T, H, E, logits, status, pdl, st);
+    else if (E <= 16)
+        err = launch_router_tiled<2, 16, 8, 1>(x, Wr, bias, T, H, E, logits, status, pdl, st);
+    else
+        err = launch_router_tiled<4, 16, 4, 2>(x, Wr, bias, T, H, E, logits, status, pdl, st);
+    if (err != cudaSuccess)
+        return err;
+    return launch_kernel(pdl_enabled(kPdlTopk), topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T, E, k,
+                         ids, wts);
 }
 
 // ============================================================ align-sort
 //
-// Three launches over chunks of kSortChunk consecutive slots:
+// Small S (<= 1024 slots): one CTA.  Thread e counts expert e's slots, the
+// padded lengths are scanned over the experts, and thread e writes its own
+// segment in ascending slot order followed by its padding.
+//
+// Larger S: three launches over chunks of kSortChunk consecutive slots:
 //  1. count:   per-chunk histogram of expert ids -> cc[chunk][e]; also
 //              pre-fills sorted_ids with the sentinel S and sorted_weights
 //              with 0 (grid-stride over all max_padded entries).
@@ -183,11 +363,89 @@ void launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float 
 //              counts, ascending slot) and writes slot s to
 //              offset[e] + prefix[chunk][e] + rank.
 
+constexpr int kSmallSort = 1024;
+
 size_t sort_scratch_bytes(int T, int k, int E)
 {
     const long S = (long)T * k;
     const long nchunks = (S + kSortChunk - 1) / kSortChunk;
     return (size_t)(nchunks > 0 ? nchunks : 1) * E * sizeof(int32_t);
+}
+
+// Inclusive Hillis-Steele scans of two 1024-entry shared arrays (one per thread).
+__device__ __forceinline__ void scan2_1024(int32_t *a, int32_t *b)
+{
+    const int i = threadIdx.x;
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int x = (i >= off) ? a[i - off] : 0;
+        const int y = (i >= off) ? b[i - off] : 0;
+        __syncthreads();
+        a[i] += x;
+        b[i] += y;
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restrict__ ids,
+                                                         const float *__restrict__ wts, int S, int E, int B,
+                                                         int64_t P_max, int64_t NB_max, SortOut o)
+{
+    __shared__ int32_t s_ids[kSmallSort];
+    __shared__ int32_t s_pad[1024];
+    __shared__ int32_t s_act[1024];
+    pdl_wait();
+    pdl_trigger();
+    const int e = threadIdx.x;
+    if (e < S)
+        s_ids[e] = ids[e];
+    __syncthreads();
+    int cnt = 0;
+    if (e < E)
+        for (int s = 0; s < S; ++s)
+            cnt += (s_ids[s] == e);
+    const int pad = (cnt + B - 1) / B * B;
+    s_pad[e] = (e < E) ? pad : 0;
+    s_act[e] = (e < E && cnt > 0) ? 1 : 0;
+    __syncthreads();
+    scan2_1024(s_pad, s_act);
+    const int off = s_pad[e] - ((e < E) ? pad : 0);
+    const int total = s_pad[1023];
+    if (e < E) {
+        if (o.expert_counts)
+            o.expert_counts[e] = cnt;
+        if (o.expert_offsets)
+            o.expert_offsets[e] = off;
+        if (o.active_experts && cnt > 0)
+            o.active_experts[s_act[e] - 1] = e;
+        int pos = off;
+        for (int s = 0; s < S; ++s)
+            if (s_ids[s] == e) {
+                o.sorted_ids[pos] = s;
+                o.sorted_weights[pos] = wts[s];
+                if (o.slot_pos)
+                    o.slot_pos[s] = pos;
+                ++pos;
+            }
+        for (; pos < off + pad; ++pos) {
+            o.sorted_ids[pos] = S;
+            o.sorted_weights[pos] = 0.0f;
+        }
+        for (int b = off / B; b < (off + pad) / B; ++b)
+            o.sorted_expert_ids[b] = e;
+    }
+    if (e == 0) {
+        *o.num_post_padded = total;
+        if (o.expert_offsets)
+            o.expert_offsets[E] = total;
+        if (o.num_active)
+            *o.num_active = s_act[1023];
+    }
+    for (int64_t i = total + e; i < P_max; i += 1024) {
+        o.sorted_ids[i] = S;
+        o.sorted_weights[i] = 0.0f;
+    }
+    for (int64_t b = total / B + e; b < NB_max; b += 1024)
+        o.sorted_expert_ids[b] = -1;
 }
 
 __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restrict__ ids, int S, int E,
@@ -196,6 +454,8 @@ __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restr
                                                          float *__restrict__ sorted_w, int64_t P_max)
 {
     extern __shared__ int32_t s_hist[];
+    pdl_wait();
+    pdl_trigger();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         s_hist[e] = 0;
     __syncthreads();
@@ -212,15 +472,12 @@ __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restr
 }
 
 __global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ cc, int nchunks, int E, int B,
-                                                        int64_t NB_max, int32_t *__restrict__ counts,
-                                                        int32_t *__restrict__ offsets,
-                                                        int32_t *__restrict__ sorted_eids,
-                                                        int32_t *__restrict__ npp, int32_t *__restrict__ active,
-                                                        int32_t *__restrict__ num_active)
+                                                        int64_t NB_max, SortOut o)
 {
     __shared__ int32_t s_pad[1024];
     __shared__ int32_t s_act[1024];
-    __shared__ int32_t s_cnt[1024];
+    pdl_wait();
+    pdl_trigger();
     const int e = threadIdx.x;
     int cnt = 0;
     if (e < E) {
@@ -230,52 +487,40 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ c
             cnt += v;
         }
     }
-    s_cnt[e] = cnt;
-    s_pad[e] = (e < E) ? (cnt + B - 1) / B * B : 0;
+    const int pad = (e < E) ? (cnt + B - 1) / B * B : 0;
+    s_pad[e] = pad;
     s_act[e] = (e < E && cnt > 0) ? 1 : 0;
     __syncthreads();
-    // inclusive Hillis-Steele scans over the (at most 1024) experts
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int a = (e >= off) ? s_pad[e - off] : 0;
-        const int b = (e >= off) ? s_act[e - off] : 0;
-        __syncthreads();
-        s_pad[e] += a;
-        s_act[e] += b;
-        __syncthreads();
-    }
+    scan2_1024(s_pad, s_act);
     const int pad_incl = s_pad[e];
-    const int pad_excl = pad_incl - ((e < E) ? (s_cnt[e] + B - 1) / B * B : 0);
+    const int pad_excl = pad_incl - pad;
     if (e < E) {
-        if (counts)
-            counts[e] = cnt;
-        if (offsets)
-            offsets[e] = pad_excl;
-        if (active && cnt > 0)
-            active[s_act[e] - 1] = e;
+        if (o.expert_counts)
+            o.expert_counts[e] = cnt;
+        o.expert_offsets[e] = pad_excl;
+        if (o.active_experts && cnt > 0)
+            o.active_experts[s_act[e] - 1] = e;
         for (int b = pad_excl / B; b < pad_incl / B; ++b)
-            sorted_eids[b] = e;
+            o.sorted_expert_ids[b] = e;
     }
     const int total = s_pad[1023];
     if (e == 0) {
-        *npp = total;
-        if (offsets)
-            offsets[E] = total;
-        if (num_active)
-            *num_active = s_act[1023];
+        *o.num_post_padded = total;
+        o.expert_offsets[E] = total;
+        if (o.num_active)
+            *o.num_active = s_act[1023];
     }
     for (int64_t b = total / B + e; b < NB_max; b += blockDim.x)
-        sorted_eids[b] = -1;
+        o.sorted_expert_ids[b] = -1;
 }
 
 __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t *__restrict__ ids,
                                                            const float *__restrict__ wts, int S, int E,
-                                                           const int32_t *__restrict__ cc,
-                                                           const int32_t *__restrict__ offsets_scan, int B,
-                                                           int32_t *__restrict__ sorted_ids,
-                                                           float *__restrict__ sorted_w,
-                                                           int32_t *__restrict__ slot_pos)
+                                                           const int32_t *__restrict__ cc, SortOut o)
 {
     extern __shared__ int32_t s_wc[];  // [32 warps][E] per-warp counts -> exclusive prefixes over warps
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x)
         s_wc[i] = 0;
@@ -298,34 +543,42 @@ __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t *__res
     }
     __syncthreads();
     if (valid) {
-        const int pos = offsets_scan[e] + cc[(size_t)blockIdx.x * E + e] + s_wc[warp * E + e] + rank;
-        sorted_ids[pos] = s;
-        sorted_w[pos] = wts[s];
-        if (slot_pos)
-            slot_pos[s] = pos;
+        const int pos = o.expert_offsets[e] + cc[(size_t)blockIdx.x * E + e] + s_wc[warp * E + e] + rank;
+        o.sorted_ids[pos] = s;
+        o.sorted_weights[pos] = wts[s];
+        if (o.slot_pos)
+            o.slot_pos[s] = pos;
     }
 }
 
-void launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
-                       const SortOut &o, void *scratch, cudaStream_t st)
+// o.expert_offsets must be non-null (the scatter reads it).
+cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
+                              const SortOut &o, void *scratch, bool pdl, cudaStream_t st)
 {
     const int S = T * k;
-    const int nchunks = (S + kSortChunk - 1) / kSortChunk;
     const int64_t P_max = (int64_t)S + (int64_t)E * block_m - k;
     const int64_t NB_max = (P_max + block_m - 1) / block_m;
-    int32_t *cc = static_cast<int32_t *>(scratch);  // o.expert_offsets must be non-null (the scatter reads it)
-    const int count_grid = nchunks > 0 ? nchunks : 1;
-    sort_count_kernel<<<count_grid, 1024, sizeof(int32_t) * E, st>>>(ids, S, E, cc, o.sorted_ids,
-                                                                    o.sorted_weights, P_max);
-    sort_scan_kernel<<<1, 1024, 0, st>>>(cc, nchunks, E, block_m, NB_max, o.expert_counts, o.expert_offsets,
-                                         o.sorted_expert_ids, o.num_post_padded, o.active_experts,
-                                         o.num_active);
-    if (32 * E * sizeof(int32_t) > 48 * 1024)
-        cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(32 * E * sizeof(int32_t)));
-    if (nchunks > 0)
-        sort_scatter_kernel<<<nchunks, 1024, sizeof(int32_t) * 32 * E, st>>>(
-            ids, wts, S, E, cc, o.expert_offsets, block_m, o.sorted_ids, o.sorted_weights, o.slot_pos);
+    if (S <= kSmallSort)
+        return launch_kernel(pdl, sort_small_kernel, dim3(1), dim3(1024), 0, st, ids, wts, S, E, block_m, P_max,
+                             NB_max, o);
+    const int nchunks = (S + kSortChunk - 1) / kSortChunk;
+    int32_t *cc = static_cast<int32_t *>(scratch);
+    cudaError_t err = launch_kernel(pdl, sort_count_kernel, dim3(nchunks), dim3(1024), sizeof(int32_t) * E, st, ids,
+                                    S, E, cc, o.sorted_ids, o.sorted_weights, P_max);
+    if (err != cudaSuccess)
+        return err;
+    err = launch_kernel(pdl_enabled(kPdlSort), sort_scan_kernel, dim3(1), dim3(1024), 0, st, cc, nchunks, E, block_m,
+                        NB_max, o);
+    if (err != cudaSuccess)
+        return err;
+    const size_t smem = sizeof(int32_t) * 32 * E;
+    if (smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(sort_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess)
+            return err;
+    }
+    return launch_kernel(pdl_enabled(kPdlSort), sort_scatter_kernel, dim3(nchunks), dim3(1024), smem, st, ids, wts, S,
+                         E, cc, o);
 }
 
 // ================================================================ gather
@@ -335,6 +588,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
                                                          const int32_t *__restrict__ npp, int S, int k, int H,
                                                          __nv_bfloat16 *__restrict__ xs)
 {
+    pdl_wait();
+    pdl_trigger();
     const int rows = *npp;
     const int nvec = H / 8;
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
@@ -351,13 +606,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
     }
 }
 
-void launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
-                        int H, int64_t P_max, __nv_bfloat16 *xs, cudaStream_t st)
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
+                               int H, int64_t P_max, __nv_bfloat16 *xs, bool pdl, cudaStream_t st)
 {
     int grid = (int)(P_max < 8192 ? P_max : 8192);
     if (grid < 1)
         grid = 1;
-    gather_rows_kernel<<<grid, 256, 0, st>>>(x, sorted_ids, npp, S, k, H, xs);
+    return launch_kernel(pdl, gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, sorted_ids, npp, S, k, H, xs);
 }
 
 // ---------------------------------------------------- FP8 quantisation
@@ -443,6 +698,8 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
                                                           int64_t P_max, uint8_t *__restrict__ q,
                                                           float *__restrict__ sT)
 {
+    pdl_wait();
+    pdl_trigger();
     const int rows = *npp;
     const int nvec = H / 8;
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
@@ -463,13 +720,14 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
     }
 }
 
-void launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
-                              int k, int H, int64_t P_max, uint8_t *q, float *sT, cudaStream_t st)
+cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
+                                     int k, int H, int64_t P_max, uint8_t *q, float *sT, bool pdl, cudaStream_t st)
 {
     int grid = (int)(P_max < 8192 ? P_max : 8192);
     if (grid < 1)
         grid = 1;
-    gather_quant_kernel<<<grid, 256, 0, st>>>(x, sorted_ids, npp, S, k, H, P_max, q, sT);
+    return launch_kernel(pdl, gather_quant_kernel, dim3(grid), dim3(256), 0, st, x, sorted_ids, npp, S, k, H, P_max,
+                         q, sT);
 }
 
 // One CTA per 128x128 block of W [R][C]: amax over the block, then codes.
@@ -480,7 +738,7 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __nv_bfloat16 *
     const int64_t br = blockIdx.y;
     const int bc = blockIdx.x;
     const int GC = C / 128;
-    // thread -> 16 columns-vectors: row r = tid / 2 (0..127), half = tid % 2 (64 columns)
+    // thread -> row r = tid / 2 (0..127), half = tid % 2 (64 columns)
     const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
     const __nv_bfloat16 *row = W + (br * 128 + r) * (int64_t)C + bc * 128 + half * 64;
     float f[8][8];
@@ -519,9 +777,21 @@ void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, 
 
 // =============================================================== combine
 
+__device__ __forceinline__ uint2 pack_bf16x4(const float4 &a)
+{
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    return pk;
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ Y, int T, int k, int H,
                                                      __nv_bfloat16 *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int nv = H / 4;
     const int64_t total = (int64_t)T * nv;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -536,24 +806,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
             a.z += b.z;
             a.w += b.w;
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        reinterpret_cast<uint2 *>(out)[i] = pk;
+        reinterpret_cast<uint2 *>(out)[i] = pack_bf16x4(a);
     }
 }
 
-void launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st)
+cudaError_t launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st)
 {
     const int64_t total = (int64_t)T * (H / 4);
     int64_t grid = (total + 255) / 256;
     if (grid > 152 * 16)
         grid = 152 * 16;
     if (grid < 1)
-        return;
-    combine_kernel<<<(int)grid, 256, 0, st>>>(Y, T, k, H, out);
+        return cudaSuccess;
+    return launch_kernel(pdl, combine_kernel, dim3((unsigned)grid), dim3(256), 0, st, Y, T, k, H, out);
 }
 
 __global__ void __launch_bounds__(256) splitk_combine_kernel(const float *__restrict__ P, int SK, int64_t P_rows,
@@ -561,6 +826,8 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const float *__rest
                                                             const float *__restrict__ wts, int T, int k, int H,
                                                             __nv_bfloat16 *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int nv = H / 4;
     const int64_t total = (int64_t)T * nv;
     const int64_t split_stride = P_rows * nv;
@@ -585,25 +852,21 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const float *__rest
             a.z += w * p.z;
             a.w += w * p.w;
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        reinterpret_cast<uint2 *>(out)[i] = pk;
+        reinterpret_cast<uint2 *>(out)[i] = pack_bf16x4(a);
     }
 }
 
-void launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
-                           int T, int k, int H, __nv_bfloat16 *out, cudaStream_t st)
+cudaError_t launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
+                                  int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st)
 {
     const int64_t total = (int64_t)T * (H / 4);
     int64_t grid = (total + 255) / 256;
     if (grid > 152 * 16)
         grid = 152 * 16;
     if (grid < 1)
-        return;
-    splitk_combine_kernel<<<(int)grid, 256, 0, st>>>(P, SK, P_rows, slot_pos, wts, T, k, H, out);
+        return cudaSuccess;
+    return launch_kernel(pdl, splitk_combine_kernel, dim3((unsigned)grid), dim3(256), 0, st, P, SK, P_rows, slot_pos,
+                         wts, T, k, H, out);
 }
 
 }  // namespace moe

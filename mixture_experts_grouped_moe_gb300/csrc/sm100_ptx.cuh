@@ -59,6 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// try_wait that lets the thread sleep (up to the hint, 0.1 ms) until the phase
+// completes, so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(100000u)
+        : "memory");
+    return done != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording a timeout in *status and raising *abort) if it does not
 // within the limit, or if another role of the CTA has already aborted.
@@ -68,9 +83,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
         return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity))
             return true;
-        if ((it & 255u) == 0) {
+        if ((it & 15u) == 0) {
             if (*abort)
                 return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
