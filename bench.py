@@ -120,6 +120,20 @@ def profiled_traffic(workload: str, kernel: str):
         return None
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings over the process group (the slowest replica sets the time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_throughput(world, tokens_per_rank, ms_max):
+    """Tokens per second over all replicas: every rank processes its own batch (weak scaling)."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
+
+
 def algorithmic_counts(cfg, counts, dtype_bytes):
     """FLOPs and bytes of the layer from the actual routing (counts per expert)."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
@@ -228,10 +242,7 @@ def run_cuda(args, cfg, rank, world, local_rank):
 
     ms = ms_total / K
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
     return dict(ms=ms, e2e_ms=e2e_ms, stage_ms=stage_ms, counts=counts, clocks=clocks, peaks=peaks,
                 peak_kind=peak_kind, plan=layer.plan, K=K, W=W)
 
@@ -336,7 +347,7 @@ def main():
     flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], 1 if cfg.dtype == "fp8" else 2)
     peaks = r["peaks"]
     ms = r["ms"]
-    tokens_s = world * cfg.T / (ms * 1e-3)
+    tokens_s = whole_job_throughput(world, cfg.T, ms)
     tflops = flops / (ms * 1e-3) / 1e12
     gbs = bytes_ / (ms * 1e-3) / 1e9
     peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -381,7 +392,7 @@ def main():
         "stage_ms_note": "per-kernel CUDA-event times from a second pass of the same steps with an event "
                          "between launches; value is timed without them",
         "clocks": r["clocks"],
-        "e2e": {"value": round(world * cfg.T / (r["e2e_ms"] * 1e-3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(whole_job_throughput(world, cfg.T, r["e2e_ms"]), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": round(r["e2e_ms"], 5)},
         "plan": {"mode": "swap" if r["plan"].mode == 1 else "grouped", "block_m": r["plan"].block_m,

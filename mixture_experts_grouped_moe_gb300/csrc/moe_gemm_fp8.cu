@@ -5,7 +5,7 @@
 // Scales are fp32 per 128x128 weight block and per 1x128 activation group,
 // so they are not the power-of-two 32-element scales the tensor core applies
 // in hardware.  Each 128-wide K block is therefore accumulated on its own
-// by tcgen05.mma kind::f8f6f4 into one of two TMEM buffers, and eight
+// by tcgen05.mma kind::f8f6f4 into one of two TMEM buffers, and sixteen
 // promotion warps fold it into fp32 registers:
 //     acc[row][col] += D_kb[row][col] * s_x[row][kb] * s_w[col_block][kb]
 // while the tensor core fills the other buffer with the next K block.
@@ -13,13 +13,15 @@
 // stage 1 computes h = silu(gate) * up and re-quantises each 1x128 group of
 // h (scale = amax / 448); stage 2 scales rows by their top-k weight.
 //
-// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9
-// promotion/epilogue (warp w reads TMEM lanes 32*(w%4)..+31 and one half
-// of the 256 accumulator columns).  Tiles: M = 128 sorted token rows,
-// N = 256 weight rows (stage 1: 128 gate + the matching 128 up rows;
-// stage 2: 256 output features).  Each thread owns two 64-column chunks:
-// stage 1 gate columns [64h, 64h+64) and up columns [128+64h, ...) so the
-// SwiGLU pairs stay inside the thread; stage 2 columns [128h, 128h+128).
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..17
+// promotion/epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its quadrant)
+// and sub = (w-2)/4 picks a quarter of the 256 accumulator columns, so four
+// warps share each quadrant and hide each other's TMEM-load latency.  Tiles:
+// M = 128 sorted token rows, N = 256 weight rows (stage 1: 128 gate + the
+// matching 128 up rows; stage 2: 256 output features).  Each thread owns two
+// 32-column chunks: stage 1 gate columns [32s, 32s+32) and up columns
+// [128+32s, ...) so the SwiGLU pairs stay inside the thread; stage 2 columns
+// [64s, 64s+64).
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -36,9 +38,23 @@ constexpr int kXBytes = 128 * 128;          // 16 KiB
 constexpr int kStageBytes = kWBytes + kXBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kPromoWarps = 8;
+// Register budget: each SM sub-partition holds 16K registers and gets ceil(warps/4) of
+// the CTA's warps, so 2 + 16 warps leave 96 registers a thread (64 accumulators), and
+// 2 + 8 warps leave 168 (128 accumulators).
+#ifndef MOE_FP8_PROMO_WARPS
+#define MOE_FP8_PROMO_WARPS 16
+#endif
+#ifndef MOE_FP8_LD_COLS
+#define MOE_FP8_LD_COLS 8
+#endif
+constexpr int kPromoWarps = MOE_FP8_PROMO_WARPS;
+constexpr int kLdCols = MOE_FP8_LD_COLS;    // TMEM columns per load (8 or 16), two loads per wait
+constexpr int kSubs = kPromoWarps / 4;      // promotion warps per TMEM lane quadrant
+constexpr int kChunk = 256 / (2 * kSubs);   // columns per chunk, two chunks per thread
 constexpr int kThreads = 64 + 32 * kPromoWarps;
+static_assert(kLdCols == 8 || kLdCols == 16, "TMEM load width");
 constexpr int kGroupM = 16;
+static_assert(kChunk * 2 * kSubs == 256, "the quadrant's warps cover the 256 accumulator columns");
 
 struct __align__(1024) Smem {
     uint8_t stage[kStages][kStageBytes];
@@ -49,7 +65,7 @@ struct __align__(1024) Smem {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float amax[2][128];
+    float amax[kSubs][128];
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -213,10 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
     } else {
         // ------------------------------------------- promotion + epilogue
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;      // 0 or 1
+        const int sub = (warp - 2) >> 2;       // 0 .. kSubs-1
         const int row = q * 32 + lane;
-        const int c0 = (STAGE == 1) ? half * 64 : half * 128;          // first chunk
-        const int c1 = (STAGE == 1) ? 128 + half * 64 : half * 128 + 64;  // second chunk
+        const int c0 = (STAGE == 1) ? sub * kChunk : sub * 2 * kChunk;                // first chunk
+        const int c1 = (STAGE == 1) ? 128 + sub * kChunk : sub * 2 * kChunk + kChunk;  // second chunk
         const int KB128 = a.K / 128;
         int buf = 0;
         uint32_t bph = 0;
@@ -224,18 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
             const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
             const int pos = tl.xrow + row;
-            // weight-scale rows of this thread's two column chunks; a stage-2 half past the last
+            // weight-scale rows of this thread's two column chunks; a stage-2 chunk past the last
             // output feature (H % 256 == 128) reads a valid row and is never stored
             const int nrb = a.E * a.rows_per_expert / 128;
-            int rb0 = (tl.wrow0 + (STAGE == 1 ? half * 64 : half * 128)) / 128;
-            int rb1 = (STAGE == 1 ? tl.wrow1 + half * 64 : tl.wrow0 + half * 128 + 64) / 128;
+            int rb0 = (STAGE == 1 ? tl.wrow0 : tl.wrow0 + sub * 64) / 128;
+            int rb1 = (STAGE == 1 ? tl.wrow1 : tl.wrow0 + sub * 64) / 128;
             rb0 = rb0 < nrb ? rb0 : nrb - 1;
             rb1 = rb1 < nrb ? rb1 : nrb - 1;
             const float *sw0 = a.w_scales + (size_t)rb0 * KB128;
             const float *sw1 = a.w_scales + (size_t)rb1 * KB128;
-            float acc0[64], acc1[64];
+            float acc0[kChunk], acc1[kChunk];
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
+            for (int i = 0; i < kChunk; ++i)
                 acc0[i] = 0.0f, acc1[i] = 0.0f;
             // the scales of block kb+1 are fetched while block kb is still on the tensor core
             float sx_n = a.x_scales[pos], s0_n = sw0[0], s1_n = sw1[0];
@@ -256,21 +272,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 const float f0 = sx * s0;
                 const float f1 = sx * s1;
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
+                // two TMEM loads in flight per wait: the promotion latency of a K block is what
+                // paces the tensor core (it may refill this buffer only after the arrive below)
 #pragma unroll
-                for (int c = 0; c < 64; c += 32) {
-                    float v[32];
-                    tmem_ld32(tb + c0 + c, v);
+                for (int c = 0; c < kChunk; c += kLdCols) {
+                    float v[kLdCols], u[kLdCols];
+                    tmem_ld_nowait(tb + c0 + c, v);
+                    tmem_ld_nowait(tb + c1 + c, u);
+                    tmem_wait_ld(v, u);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc0[c + i] = fmaf(v[i], f0, acc0[c + i]);
-                }
-#pragma unroll
-                for (int c = 0; c < 64; c += 32) {
-                    float v[32];
-                    tmem_ld32(tb + c1 + c, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc1[c + i] = fmaf(v[i], f1, acc1[c + i]);
+                    for (int i = 0; i < kLdCols; i += 2) {
+                        ffma2(acc0[c + i], acc0[c + i + 1], v[i], v[i + 1], f0);
+                        ffma2(acc1[c + i], acc1[c + i + 1], u[i], u[i + 1], f1);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -284,21 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
             if (!ok)
                 break;
             if (STAGE == 1) {
-                // h for columns ncol0 + half*64 + i; one 1x128 group spans both halves of the row
+                // h for columns ncol0 + sub*32 + i; one 1x128 group spans the quadrant's 4 warps
                 float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < kChunk; ++i) {
                     acc0[i] = silu(acc0[i]) * acc1[i];
                     amax = fmaxf(amax, fabsf(acc0[i]));
                 }
-                sm.amax[half][row] = amax;
-                named_bar(1 + q, 64);
-                amax = fmaxf(amax, sm.amax[half ^ 1][row]);
-                named_bar(1 + q, 64);
-                const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
-                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)pos * a.N + tl.ncol0 + half * 64;
+                sm.amax[sub][row] = amax;
+                named_bar(1 + q, 32 * kSubs);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
+                for (int s2 = 0; s2 < kSubs; ++s2)
+                    amax = fmaxf(amax, sm.amax[s2][row]);
+                named_bar(1 + q, 32 * kSubs);
+                const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)pos * a.N + tl.ncol0 + sub * kChunk;
+#pragma unroll
+                for (int v = 0; v < kChunk / 16; ++v) {
                     uint32_t w[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -312,22 +328,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                     }
                     reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                if (half == 0)
+                if (sub == 0)
                     a.inter_scales[(size_t)(tl.ncol0 / 128) * a.P_max + pos] = sc;
             } else {
                 const int slot = a.sorted_ids[pos];
                 if (slot < a.S) {
                     const float wgt = a.sorted_weights[pos];
-                    const int n0 = tl.ncol0 + half * 128;
+                    const int n0 = tl.ncol0 + sub * 2 * kChunk;
                     float *dst = a.y + (size_t)slot * a.N + n0;
                     if (n0 < a.N) {
 #pragma unroll
-                        for (int i = 0; i < 64; i += 4)
+                        for (int i = 0; i < kChunk; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
                                 make_float4(wgt * acc0[i], wgt * acc0[i + 1], wgt * acc0[i + 2], wgt * acc0[i + 3]);
 #pragma unroll
-                        for (int i = 0; i < 64; i += 4)
-                            *reinterpret_cast<float4 *>(dst + 64 + i) =
+                        for (int i = 0; i < kChunk; i += 4)
+                            *reinterpret_cast<float4 *>(dst + kChunk + i) =
                                 make_float4(wgt * acc1[i], wgt * acc1[i + 1], wgt * acc1[i + 2], wgt * acc1[i + 3]);
                     }
                 }
