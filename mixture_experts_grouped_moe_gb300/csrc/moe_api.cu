@@ -124,7 +124,7 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
         off = align_up(off + (bytes > 0 ? bytes : 0), kAlign);
         return o;
     };
-    L.status = take(16);
+    L.status = take(kStatusWords * 4);
     L.logits = take((int64_t)T * E * 4);
     L.topk_ids = take(S * 4);
     L.topk_w = take(S * 4);
@@ -305,11 +305,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g.E = E;
     g.P_max = P;
     g.status = status;
+    g.tile_counter = nullptr;
     const uint32_t box_inner = (uint32_t)(128 / eb);  // one 128-byte swizzle row
     const uint32_t box_x_rows = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
 
     // ---------------------------------------------------------- stage 1
     GemmArgs g1 = g;
+    g1.tile_counter = status + 1;
     if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H, (uint64_t)E * 2 * I, box_inner, 128))
         return MOE_ERR_CUDA;
@@ -336,6 +338,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     // ---------------------------------------------------------- stage 2
     GemmArgs g2 = g;
+    g2.tile_counter = status + 2;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g2.tm_w, W_down, eb, I, (uint64_t)E * H, box_inner, 128))
         return MOE_ERR_CUDA;

@@ -59,11 +59,13 @@ struct __align__(1024) Smem {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    TileQueue tq;
     uint32_t tmem_base;
     int abort;
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+constexpr int kEpiWarps = 4;
 
 struct Tile {
     int valid;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(&sm.tempty[i], 4);
         }
         mbar_init(&sm.drain, 1);
+        tq_init(sm.tq, 1 + kEpiWarps);
         sm.abort = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&a.tm_x);
@@ -212,7 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int i = 0; i < kStages; ++i)
                 issued[i] = 0, issued_ph[i] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            int qs = 0;
+            uint32_t qph = 0;
+            int claim = -2;
+            for (;;) {
+                int t;
+                if (!tq_push_next(sm.tq, qs, qph, a.tile_counter, ntiles, claim, t, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (t < 0)
+                    break;
                 const Tile tl = get_tile<MODE, STAGE>(a, t);
                 const uint32_t bytes = kWBytes + tl.nx * 128;
                 for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
@@ -238,6 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         ph ^= 1;
                     }
                 }
+                if (!ok)
+                    break;
             }
             if (!ok) {
                 // let the copies already in flight land before the CTA exits
@@ -258,7 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t aph = 0;
             bool ok = true;
             bool any = false;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            int qs = 0;
+            uint32_t qph = 0;
+            for (;;) {
+                int t;
+                if (!tq_pop(sm.tq, qs, qph, t, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(&sm.tq.empty[qs]);
+                tq_advance(qs, qph);
+                if (t < 0)
+                    break;
                 const Tile tl = get_tile<MODE, STAGE>(a, t);
                 if (!mbar_wait(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
                     ok = false;
@@ -316,7 +342,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int row = q * 32 + lane;    // accumulator row (TMEM lane)
         int acc = 0;
         uint32_t aph = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        int qs = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int t = -1;
+            bool qok = tq_pop(sm.tq, qs, qph, t, a.status, abort_flag);
+            qok = __all_sync(0xffffffffu, qok);
+            if (!qok)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.tq.empty[qs]);
+            tq_advance(qs, qph);
+            if (t < 0)
+                break;
             const Tile tl = get_tile<MODE, STAGE>(a, t);
             bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);

@@ -63,6 +63,7 @@ struct __align__(1024) Smem {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    TileQueue tq;
     uint32_t tmem_base;
     int abort;
     float amax[kSubs][128];
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
             mbar_init(&sm.tempty[i], kPromoWarps);
         }
         mbar_init(&sm.drain, 1);
+        tq_init(sm.tq, 1 + kPromoWarps);
         sm.abort = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&a.tm_x);
@@ -154,7 +156,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
             for (int i = 0; i < kStages; ++i)
                 issued[i] = 0, issued_ph[i] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            int qs = 0;
+            uint32_t qph = 0;
+            int claim = -2;
+            for (;;) {
+                int t;
+                if (!tq_push_next(sm.tq, qs, qph, a.tile_counter, ntiles, claim, t, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (t < 0)
+                    break;
                 const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
@@ -173,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                         ph ^= 1;
                     }
                 }
+                if (!ok)
+                    break;
             }
             if (!ok) {
                 for (int i = 0; i < kStages; ++i)
@@ -191,7 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
             uint32_t bph = 0;
             bool ok = true, any = false;
             const uint32_t idesc = make_idesc(0, 0, 128, 256);
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            int qs = 0;
+            uint32_t qph = 0;
+            for (;;) {
+                int t;
+                if (!tq_pop(sm.tq, qs, qph, t, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(&sm.tq.empty[qs]);
+                tq_advance(qs, qph);
+                if (t < 0)
+                    break;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&sm.tempty[buf], bph ^ 1, a.status, abort_flag) ||
                         !mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
@@ -218,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                         bph ^= 1;
                     }
                 }
+                if (!ok)
+                    break;
             }
             if (!ok && any) {
                 mma_commit(&sm.drain);
@@ -237,7 +264,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
         int buf = 0;
         uint32_t bph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        int qs = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int t = -1;
+            bool qok = tq_pop(sm.tq, qs, qph, t, a.status, abort_flag);
+            qok = __all_sync(0xffffffffu, qok);
+            if (!qok)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.tq.empty[qs]);
+            tq_advance(qs, qph);
+            if (t < 0)
+                break;
             const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
             const int pos = tl.xrow + row;
             // weight-scale rows of this thread's two column chunks; a stage-2 chunk past the last

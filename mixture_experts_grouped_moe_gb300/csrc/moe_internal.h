@@ -66,9 +66,14 @@ inline cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, di
 
 // ------------------------------------------------------ route / sort / aux
 
+// Words at the start of the fused forward's workspace: [0] status, [1] stage-1
+// tile counter, [2] stage-2 tile counter, [3] spare.  The router zeroes them.
+constexpr int kStatusWords = 4;
+
 // Small T*E: one fused launch.  Large T*E: a tiled logit pass into `logits`
 // (fp32 [T][E], required then) followed by a warp-per-token top-k pass.
-// `status` (nullable) is zeroed by the first kernel.  `pdl` applies to the first launch.
+// `status` (nullable) points at kStatusWords words that the first kernel
+// zeroes.  `pdl` applies to the first launch.
 bool router_needs_logits(int T, int E);
 cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
                           int k, int32_t *ids, float *wts, float *logits, int *status, bool pdl, cudaStream_t st);
@@ -137,6 +142,7 @@ struct GemmArgs {
     float *y;                // stage 2: [S][H] fp32 (weighted)
     float *partials;         // stage 2 split-K: [split][P_max][H]
     int *status;
+    int *tile_counter;       // zeroed before the launch; CTAs claim tiles from it
 };
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,

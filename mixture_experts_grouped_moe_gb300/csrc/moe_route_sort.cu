@@ -38,6 +38,20 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float (&f)[8])
 // same bits, so the two kernels below agree with each other and with the
 // CPU oracle.
 
+// (c0, c1) = (a0 * b0 + c0, a1 * b1 + c1) in one paired-fp32 instruction of the
+// sm_100 family; each lane is rounded once, exactly like fmaf.
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%0, %1};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float butterfly_sum(float v)
 {
 #pragma unroll
@@ -107,8 +121,8 @@ __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16 *
     extern __shared__ float s_logit[];  // [TT][E]
     pdl_wait();
     pdl_trigger();
-    if (status && blockIdx.x == 0 && threadIdx.x == 0)
-        *status = 0;
+    if (status && blockIdx.x == 0 && threadIdx.x < kStatusWords)
+        status[threadIdx.x] = 0;  // status word and the GEMMs' tile counters
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TT;
     const int ngroups = (E + EG - 1) / EG;
@@ -209,8 +223,8 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const __nv_bfloat16 *
     auto s_rows = reinterpret_cast<__nv_bfloat16(*)[ROWS][256]>(s_raw);  // [kRouterStages][ROWS][256]
     pdl_wait();
     pdl_trigger();
-    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-        *status = 0;
+    if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kStatusWords)
+        status[threadIdx.x] = 0;  // status word and the GEMMs' tile counters
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TT, e0 = blockIdx.y * EC;
     const int wt = warp / NWE, we = warp % NWE;
@@ -264,15 +278,17 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const __nv_bfloat16 *
 #pragma unroll
         for (int t = 0; t < WT; ++t)
             bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][wt * WT + t][lane * 8]), xf[t]);
+        static_assert(WE % 2 == 0, "experts are processed in pairs");
 #pragma unroll
-        for (int j = 0; j < WE; ++j) {
-            float wf[8];
-            bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][TT + we * WE + j][lane * 8]), wf);
+        for (int j = 0; j < WE; j += 2) {
+            float wf0[8], wf1[8];
+            bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][TT + we * WE + j][lane * 8]), wf0);
+            bf16x8_to_float(*reinterpret_cast<const uint4 *>(&s_rows[b][TT + we * WE + j + 1][lane * 8]), wf1);
 #pragma unroll
             for (int t = 0; t < WT; ++t)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
-                    acc[t][j] = __fmaf_rn(xf[t][cc], wf[cc], acc[t][j]);
+                    fma2(acc[t][j], acc[t][j + 1], xf[t][cc], xf[t][cc], wf0[cc], wf1[cc]);
         }
         __syncthreads();
     }

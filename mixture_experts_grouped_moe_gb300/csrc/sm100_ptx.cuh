@@ -97,6 +97,71 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
     }
 }
 
+// ------------------------------------------------ dynamic tile queue
+//
+// Persistent GEMM CTAs claim tiles from a global counter (atomicAdd), so
+// that tiles of uneven cost (a memory-bound tile of a lightly loaded expert
+// next to a compute-bound one) balance across SMs.  The producer thread
+// claims; the index reaches the MMA thread and the epilogue warps through a
+// ring of kTileQ shared-memory slots guarded by mbarriers (full: 1 producer
+// arrival; empty: one arrival per consumer).  Index -1 means "no more tiles".
+constexpr int kTileQ = 4;
+
+struct TileQueue {
+    int idx[kTileQ];
+    uint64_t full[kTileQ];
+    uint64_t empty[kTileQ];
+};
+
+__device__ __forceinline__ void tq_init(TileQueue &q, uint32_t consumers)
+{
+    for (int i = 0; i < kTileQ; ++i) {
+        mbar_init(&q.full[i], 1);
+        mbar_init(&q.empty[i], consumers);
+    }
+}
+
+// Producer: publish the next tile index t (claimed from *counter, or -1 past ntiles).
+// Consumer (tq_pop): read the next index, then arrive on q.empty[slot] once every
+// thread of the consumer has read it, and tq_advance.
+__device__ __forceinline__ bool tq_push_next(TileQueue &q, int &slot, uint32_t &ph, int *counter, int ntiles,
+                                             int &claim, int &t, int *status, volatile int *abort)
+{
+    // `claim` holds the tile claimed on the previous call (-2 before the first one): the
+    // next claim is issued right after publishing, so its latency overlaps this tile's loads.
+    if (claim == -2)
+        claim = atomicAdd(counter, 1);
+    if (!mbar_wait(&q.empty[slot], ph ^ 1, status, abort))
+        return false;
+    t = (claim < ntiles) ? claim : -1;
+    *reinterpret_cast<volatile int *>(&q.idx[slot]) = t;
+    mbar_arrive(&q.full[slot]);
+    if (++slot == kTileQ) {
+        slot = 0;
+        ph ^= 1;
+    }
+    if (t >= 0)
+        claim = atomicAdd(counter, 1);
+    return true;
+}
+
+__device__ __forceinline__ bool tq_pop(TileQueue &q, int slot, uint32_t ph, int &t, int *status,
+                                       volatile int *abort)
+{
+    if (!mbar_wait(&q.full[slot], ph, status, abort))
+        return false;
+    t = *reinterpret_cast<volatile int *>(&q.idx[slot]);
+    return true;
+}
+
+__device__ __forceinline__ void tq_advance(int &slot, uint32_t &ph)
+{
+    if (++slot == kTileQ) {
+        slot = 0;
+        ph ^= 1;
+    }
+}
+
 // --------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
