@@ -311,7 +311,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     // ---------------------------------------------------------- stage 1
     GemmArgs g1 = g;
-    g1.tile_counter = status + 1;
+    // grouped tiles differ in cost (compute- vs memory-bound experts): claim them dynamically;
+    // swap-mode tiles are uniform: deal them round-robin
+    g1.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 1 : nullptr;
     if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H, (uint64_t)E * 2 * I, box_inner, 128))
         return MOE_ERR_CUDA;
@@ -338,7 +340,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     // ---------------------------------------------------------- stage 2
     GemmArgs g2 = g;
-    g2.tile_counter = status + 2;
+    g2.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g2.tm_w, W_down, eb, I, (uint64_t)E * H, box_inner, 128))
         return MOE_ERR_CUDA;

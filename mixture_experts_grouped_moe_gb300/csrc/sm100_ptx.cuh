@@ -129,8 +129,9 @@ __device__ __forceinline__ bool tq_push_next(TileQueue &q, int &slot, uint32_t &
 {
     // `claim` holds the tile claimed on the previous call (-2 before the first one): the
     // next claim is issued right after publishing, so its latency overlaps this tile's loads.
+    // Without a counter the tiles are dealt round-robin (blockIdx.x, + gridDim.x, ...).
     if (claim == -2)
-        claim = atomicAdd(counter, 1);
+        claim = counter ? atomicAdd(counter, 1) : (int)blockIdx.x;
     if (!mbar_wait(&q.empty[slot], ph ^ 1, status, abort))
         return false;
     t = (claim < ntiles) ? claim : -1;
@@ -141,7 +142,7 @@ __device__ __forceinline__ bool tq_push_next(TileQueue &q, int &slot, uint32_t &
         ph ^= 1;
     }
     if (t >= 0)
-        claim = atomicAdd(counter, 1);
+        claim = counter ? atomicAdd(counter, 1) : claim + (int)gridDim.x;
     return true;
 }
 
