@@ -95,17 +95,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """Digest of the source files a profiled kernel is built from (names under the package's csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_grouped_moe_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources are unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -113,7 +114,7 @@ def profiled_traffic(workload: str, kernel: str):
         with open(p) as f:
             d = json.load(f)
         ent = d.get(workload, {}).get(kernel)
-        if not ent or ent.get("source_hash") != kernel_source_hash():
+        if not ent or ent.get("source_hash") != kernel_source_hash(ent["sources"]):
             return None
         return ent["dram_bytes_per_launch"]
     except (OSError, ValueError, KeyError):

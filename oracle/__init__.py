@@ -56,12 +56,14 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_quant_1x128.argtypes = [P, i, i, P, P]
         lib.oracle_quant_128x128.argtypes = [P, ctypes.c_long, i, P, P]
+        lib.oracle_quant_rows.argtypes = [P, ctypes.c_long, i, P, P]
         lib.oracle_router_logit.restype = ctypes.c_float
         lib.oracle_router_logit.argtypes = [P, P, i, P, i]
         lib.oracle_route.argtypes = [P, P, P, i, i, i, i, P, P, P, i]
         lib.oracle_align_sort.argtypes = [P, i, i, i, i, P, P, P, P]
         lib.oracle_moe_forward_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
+        lib.oracle_moe_forward_fp8_token.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         _lib = lib
         return lib
 
@@ -124,6 +126,17 @@ def quant_128x128(W_bits) -> tuple[np.ndarray, np.ndarray]:
     q = np.empty(W.shape, np.uint8)
     s = np.empty((R // 128, C // 128), np.float32)
     _load().oracle_quant_128x128(_ptr(W), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_rows(X_bits) -> tuple[np.ndarray, np.ndarray]:
+    """One scale per row ("per_Token" on the AITER page): X viewed as [rows, C]; codes, scales [rows]."""
+    X = _u16(X_bits)
+    C = X.shape[-1]
+    R = X.size // C
+    q = np.empty(X.shape, np.uint8)
+    s = np.empty(R, np.float32)
+    _load().oracle_quant_rows(_ptr(X), R, C, _ptr(q), _ptr(s))
     return q, s
 
 
@@ -210,4 +223,24 @@ def moe_forward_fp8(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens
     _load().oracle_moe_forward_fp8(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(_f32(w1s)),
                                    _ptr(Wd_q), _ptr(_f32(w2s)), T, H, I, E, k, _ptr(tok), len(tok),
                                    _ptr(out), nthreads or default_threads())
+    return out
+
+
+def moe_forward_fp8_token(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens=None,
+                          nthreads: int | None = None) -> np.ndarray:
+    """Per-token FP8 fused MoE layer for `tokens`: out [n, H] fp64.
+
+    Wgu_q [E,2I,H] / Wd_q [E,H,I] e4m3 codes with one scale per output channel: w1s [E*2I], w2s [E*H]."""
+    x = _u16(x_bits)
+    Wr = _u16(Wr_bits)
+    Wgu_q = np.ascontiguousarray(Wgu_q, np.uint8)
+    Wd_q = np.ascontiguousarray(Wd_q, np.uint8)
+    T, H = x.shape
+    E, twoI, _ = Wgu_q.shape
+    I = twoI // 2
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    out = np.empty((len(tok), H), np.float64)
+    _load().oracle_moe_forward_fp8_token(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(_f32(w1s)),
+                                         _ptr(Wd_q), _ptr(_f32(w2s)), T, H, I, E, k, _ptr(tok), len(tok),
+                                         _ptr(out), nthreads or default_threads())
     return out

@@ -20,7 +20,9 @@
  *
  * plus the integer reorder ("moe_sorting" in section 3.1: tokens grouped by
  * expert, each expert padded to whole blocks, buffer of T*k + E*B - k
- * entries) and the per-128 block-scaled FP8 quantisation ("per_1x128").
+ * entries) and the two FP8 quantisation types the page names: per-128
+ * block scaling ("per_1x128") and one scale per row ("per_Token": a scale
+ * per token of the activations, per output channel of the weights).
  *
  * Precision: inputs are bf16 (or e4m3 codes with fp32 scales) taken exactly;
  * every dot product of the expert GEMMs accumulates in fp64.  The router
@@ -151,6 +153,27 @@ void oracle_quant_128x128(const uint16_t *W, long R, int C, uint8_t *q, float *s
                 for (int c = bc * 128; c < bc * 128 + 128; ++c)
                     q[r * C + c] = oracle_e4m3_encode(bf16_to_float(W[r * C + c]) / sc);
         }
+    }
+}
+
+/*
+ * "per_Token" quantisation: one scale per row of X [R, C] (a token of the
+ * activations, an output channel of a weight matrix), scale = amax/448 over
+ * the whole row, codes e4m3(x / scale).  q [R, C], s [R].
+ */
+void oracle_quant_rows(const uint16_t *X, long R, int C, uint8_t *q, float *s)
+{
+    for (long r = 0; r < R; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < C; ++c) {
+            float v = fabsf(bf16_to_float(X[r * C + c]));
+            if (v > amax)
+                amax = v;
+        }
+        float sc = group_scale(amax);
+        s[r] = sc;
+        for (int c = 0; c < C; ++c)
+            q[r * C + c] = oracle_e4m3_encode(bf16_to_float(X[r * C + c]) / sc);
     }
 }
 
@@ -313,12 +336,12 @@ int oracle_align_sort(const int32_t *ids, int T, int k, int E, int B, int32_t *s
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 typedef struct {
-    int mode; /* 0 bf16, 1 fp8 */
+    int mode; /* 0 bf16, 1 fp8 per 128x128 / 1x128 blocks, 2 fp8 per row */
     const uint16_t *x, *Wr;
     const float *bias;
     const uint16_t *Wgu, *Wd;                /* bf16 weights */
     const uint8_t *Wgu_q, *Wd_q;             /* e4m3 codes */
-    const float *w1s, *w2s;                  /* 128x128 block scales */
+    const float *w1s, *w2s;                  /* block scales (mode 1) or row scales (mode 2) */
     int T, H, I, E, k;
     const int64_t *tokens;
     int n0, n1;
@@ -346,10 +369,14 @@ static void *fwd_worker(void *arg)
         if (J->mode == 0) {
             for (int h = 0; h < H; ++h)
                 xt[h] = bf16_to_float(xrow[h]);
-        } else {
+        } else if (J->mode == 1) {
             oracle_quant_1x128(xrow, 1, H, xq, xs);
             for (int h = 0; h < H; ++h)
                 xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[h / 128];
+        } else {
+            oracle_quant_rows(xrow, 1, H, xq, xs);
+            for (int h = 0; h < H; ++h)
+                xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[0];
         }
         double *o = J->out + (size_t)n * H;
         for (int h = 0; h < H; ++h)
@@ -364,6 +391,14 @@ static void *fwd_worker(void *arg)
                     for (int h = 0; h < H; ++h) {
                         g += (double)bf16_to_float(J->Wgu[rg + h]) * xt[h];
                         u += (double)bf16_to_float(J->Wgu[ru + h]) * xt[h];
+                    }
+                } else if (J->mode == 2) {
+                    /* one scale per output channel (row of the [E*2I, H] matrix) */
+                    const double sg = J->w1s[(size_t)e * 2 * I + i];
+                    const double su = J->w1s[(size_t)e * 2 * I + I + i];
+                    for (int h = 0; h < H; ++h) {
+                        g += oracle_e4m3_decode(J->Wgu_q[rg + h]) * sg * xt[h];
+                        u += oracle_e4m3_decode(J->Wgu_q[ru + h]) * su * xt[h];
                     }
                 } else {
                     /* block (row/128, col/128) of the [E*2I, H] matrix */
@@ -392,6 +427,17 @@ static void *fwd_worker(void *arg)
                         a[i] = oracle_e4m3_decode(aq[i]) * (double)sc;
                     }
                 }
+            } else if (J->mode == 2) {
+                /* per-token: one scale for the token's whole intermediate row */
+                float amax = 0.0f;
+                for (int i = 0; i < I; ++i) {
+                    float v = fabsf((float)a[i]);
+                    if (v > amax)
+                        amax = v;
+                }
+                float sc = group_scale(amax);
+                for (int i = 0; i < I; ++i)
+                    a[i] = oracle_e4m3_decode(oracle_e4m3_encode((float)a[i] / sc)) * (double)sc;
             }
             for (int h = 0; h < H; ++h) {
                 double y = 0.0;
@@ -399,6 +445,10 @@ static void *fwd_worker(void *arg)
                 if (J->mode == 0) {
                     for (int i = 0; i < I; ++i)
                         y += (double)bf16_to_float(J->Wd[rd + i]) * a[i];
+                } else if (J->mode == 2) {
+                    const double sd = J->w2s[(size_t)e * H + h];
+                    for (int i = 0; i < I; ++i)
+                        y += oracle_e4m3_decode(J->Wd_q[rd + i]) * sd * a[i];
                 } else {
                     const float *sd = J->w2s + ((size_t)e * H + h) / 128 * (I / 128);
                     for (int i = 0; i < I; ++i)
@@ -478,6 +528,38 @@ int oracle_moe_forward_fp8(const uint16_t *x, const uint16_t *Wr, const float *b
     fwd_job J;
     memset(&J, 0, sizeof J);
     J.mode = 1;
+    J.x = x;
+    J.Wr = Wr;
+    J.bias = bias;
+    J.Wgu_q = Wgu_q;
+    J.w1s = w1s;
+    J.Wd_q = Wd_q;
+    J.w2s = w2s;
+    J.T = T;
+    J.H = H;
+    J.I = I;
+    J.E = E;
+    J.k = k;
+    J.tokens = tokens;
+    J.out = out;
+    return run_forward(J, n_tokens, nthreads);
+}
+
+/*
+ * Per-token FP8 layer ("per_Token" with e4m3 weights): the router runs on
+ * the bf16 activations; the expert GEMMs see x quantised with one scale per
+ * token, weights as e4m3 codes with one fp32 scale per output channel
+ * (w1s [E*2I], w2s [E*H]) and the SwiGLU output re-quantised with one scale
+ * per token over its whole intermediate row.  Products are of the
+ * dequantised values, accumulated in fp64.
+ */
+int oracle_moe_forward_fp8_token(const uint16_t *x, const uint16_t *Wr, const float *bias, const uint8_t *Wgu_q,
+                                 const float *w1s, const uint8_t *Wd_q, const float *w2s, int T, int H, int I,
+                                 int E, int k, const int64_t *tokens, int n_tokens, double *out, int nthreads)
+{
+    fwd_job J;
+    memset(&J, 0, sizeof J);
+    J.mode = 2;
     J.x = x;
     J.Wr = Wr;
     J.bias = bias;

@@ -119,6 +119,36 @@ def test_quant_128x128_block_scales():
     assert np.array_equal(q, ref)
 
 
+def test_quant_rows_against_torch_encoder():
+    """Per-row ("per_Token") scales: amax of the whole row / 448, codes from torch's e4m3 cast."""
+    g = torch.Generator().manual_seed(5)
+    X = (torch.randn(9, 640, generator=g) * torch.exp(torch.randn(9, 1, generator=g) * 3)).to(torch.bfloat16)
+    X[4] = 0  # an all-zero row takes scale 1
+    X[6, 17] = -300.0  # one large entry sets the row's scale
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    q, s = oracle.quant_rows(bits)
+    xf = X.float()
+    amax = xf.abs().amax(-1)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert np.array_equal(s, sc.numpy())
+    ref = (xf / sc[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+    tab = oracle.e4m3_table()
+    for r in range(9):
+        assert np.abs(tab[q[r]]).max() == (0.0 if r == 4 else 448.0)
+    assert tab[q[6, 17]] == -448.0
+
+
+def test_quant_rows_is_1x128_on_single_group_rows():
+    """With 128 columns a row is one 1x128 group: both quantisers must agree."""
+    g = torch.Generator().manual_seed(6)
+    X = (torch.randn(33, 128, generator=g) * 7).to(torch.bfloat16)
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    q1, s1 = oracle.quant_rows(bits)
+    q2, s2 = oracle.quant_1x128(bits)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2[:, 0])
+
+
 # ---------------------------------------------------------------- router
 
 def test_router_order_hand_worked_cases():
@@ -357,6 +387,55 @@ def test_forward_fp8_against_dense_dequantised_reference():
             aq = (a / sc).clamp(-448, 448).to(torch.float8_e4m3fn).double() * sc.double()
             ref[t] += w[t, j] * (Wd[e] @ aq.reshape(-1).numpy())
     assert _rel(got, ref) < 1e-12
+
+
+def test_forward_fp8_token_against_dense_dequantised_reference():
+    """Per-token FP8 path vs an independent dense formulation: scales broadcast
+    by row with numpy, torch's e4m3 encoder for the per-token re-quantisation
+    of the SwiGLU output, numpy matmuls."""
+    cfg = synth.CONFIGS["tiny"].with_(T=7, H=256, I=384, E=3, k=2)
+    inp = synth.make_inputs(cfg, seed=8)
+    xb, wrb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    qgu, s1 = oracle.quant_rows(synth.bf16_bits(inp["W_gate_up"]))
+    qd, s2 = oracle.quant_rows(synth.bf16_bits(inp["W_down"]))
+    assert s1.shape == (cfg.E * 2 * cfg.I,) and s2.shape == (cfg.E * cfg.H,)
+    got = oracle.moe_forward_fp8_token(xb, wrb, None, qgu, s1, qd, s2, cfg.k)
+
+    tab = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    Wgu = tab[qgu] * s1.astype(np.float64).reshape(cfg.E, 2 * cfg.I, 1)
+    Wd = tab[qd] * s2.astype(np.float64).reshape(cfg.E, cfg.H, 1)
+    xf = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).float()
+    xs = xf.abs().amax(-1, keepdim=True) / 448.0
+    x = (xf / xs).to(torch.float8_e4m3fn).double().numpy() * xs.double().numpy()
+    ids, w, _ = oracle.route(xb, wrb, None, cfg.k)
+    ref = np.zeros((cfg.T, cfg.H))
+    I = cfg.I
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            e = ids[t, j]
+            g, u = Wgu[e, :I] @ x[t], Wgu[e, I:] @ x[t]
+            a = torch.from_numpy(g / (1 + np.exp(-g)) * u).float()
+            sc = a.abs().amax() / 448.0
+            aq = (a / sc).to(torch.float8_e4m3fn).double() * sc.double()
+            ref[t] += w[t, j] * (Wd[e] @ aq.numpy())
+    assert _rel(got, ref) < 1e-12
+    sub = np.array([6, 0, 3], np.int64)
+    assert np.array_equal(oracle.moe_forward_fp8_token(xb, wrb, None, qgu, s1, qd, s2, cfg.k, tokens=sub), got[sub])
+
+
+def test_forward_fp8_token_close_to_bf16_layer():
+    """Quantisation only perturbs the layer: the per-token FP8 output stays
+    within the e4m3 error budget of the bf16 layer (and is not identical)."""
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_inputs(cfg, seed=9)
+    xb, wrb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    gub, db = synth.bf16_bits(inp["W_gate_up"]), synth.bf16_bits(inp["W_down"])
+    qgu, s1 = oracle.quant_rows(gub)
+    qd, s2 = oracle.quant_rows(db)
+    got = oracle.moe_forward_fp8_token(xb, wrb, None, qgu, s1, qd, s2, cfg.k)
+    ref = oracle.moe_forward_bf16(xb, wrb, None, gub, db, cfg.k)
+    r = _rel(got, ref)
+    assert 1e-3 < r < 0.15, r  # three e4m3 roundings (x, W, h), each about 3 % relative RMS
 
 
 # ------------------------------------------------------------ heuristics
