@@ -142,8 +142,10 @@ def algorithmic_counts(cfg, counts, dtype_bytes):
     flops = 2.0 * S * 3 * H * I + 2.0 * T * H * E
     active = int(sum(1 for c in counts if c > 0))
     scale_bytes = 0
-    if dtype_bytes == 1:
+    if cfg.dtype == "fp8":
         scale_bytes = active * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+    elif cfg.dtype == "fp8_token":
+        scale_bytes = active * (2 * I + H) * 4
     bytes_ = active * 3 * H * I * dtype_bytes + scale_bytes + T * H * 2 + T * H * 2 + E * H * 2
     s1_bytes = active * 2 * I * H * dtype_bytes
     s2_bytes = active * H * I * dtype_bytes
@@ -163,7 +165,7 @@ def run_cuda(args, cfg, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
     fp8 = cfg.dtype == "fp8"
-    dtype = moe.MOE_FP8_BLOCK128 if fp8 else moe.MOE_BF16
+    dtype = {"fp8": moe.MOE_FP8_BLOCK128, "fp8_token": moe.MOE_FP8_TOKEN}.get(cfg.dtype, moe.MOE_BF16)
 
     inp = synth.make_inputs(cfg, seed=0, device=dev)
     w = {"W_router": inp["W_router"], "bias": inp["bias"]}
@@ -175,6 +177,15 @@ def run_cuda(args, cfg, rank, world, local_rank):
         s2 = torch.empty(E * H // 128, I // 128, dtype=torch.float32, device=dev)
         moe.moe_quantize_fp8_weights(inp["W_gate_up"], E * 2 * I, H, q1, s1)
         moe.moe_quantize_fp8_weights(inp["W_down"], E * H, I, q2, s2)
+        w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
+    elif cfg.dtype == "fp8_token":
+        E, I, H = cfg.E, cfg.I, cfg.H
+        q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        s1 = torch.empty(E * 2 * I, dtype=torch.float32, device=dev)
+        q2 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        s2 = torch.empty(E * H, dtype=torch.float32, device=dev)
+        moe.moe_quantize_fp8_rows(inp["W_gate_up"], E * 2 * I, H, q1, s1)
+        moe.moe_quantize_fp8_rows(inp["W_down"], E * H, I, q2, s2)
         w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
     else:
         w.update(W_gate_up=inp["W_gate_up"], W_down=inp["W_down"])
@@ -273,6 +284,9 @@ def run_oracle(cfg, host, toks):
     if cfg.dtype == "fp8":
         return oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
                                       host["q2"], host["s2"], cfg.k, toks)
+    if cfg.dtype == "fp8_token":
+        return oracle.moe_forward_fp8_token(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
+                                            host["q2"], host["s2"], cfg.k, toks)
     return oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
                                    cfg.k, toks)
 
@@ -288,20 +302,24 @@ def host_inputs(cfg, device):
     if cfg.dtype == "fp8":
         host["q1"], host["s1"] = oracle.quant_128x128(host["W_gate_up"])
         host["q2"], host["s2"] = oracle.quant_128x128(host["W_down"])
+    elif cfg.dtype == "fp8_token":
+        host["q1"], host["s1"] = oracle.quant_rows(host["W_gate_up"])
+        host["q2"], host["s2"] = oracle.quant_rows(host["W_down"])
     return host
 
 
 def launches_per_step(cfg):
     """Kernels the library launches per forward: router (+ top-k pass for large T*E), sort
-    (one launch up to 1024 slots, else three), gather, stage 1, stage 2, combine."""
+    (one launch up to 1024 slots, else three), gather, stage 1 (+ the per-token re-quantisation
+    of h), stage 2, combine."""
     router = 2 if cfg.T * cfg.E > 4096 else 1
     sort = 1 if cfg.T * cfg.k <= 1024 else 3
-    return router + sort + 4
+    return router + sort + 4 + (1 if cfg.dtype == "fp8_token" else 0)
 
 
 def workload_desc(cfg):
     d = {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k} SwiGLU"
-                     + (" block-scaled FP8 e4m3" if cfg.dtype == "fp8" else " bf16")
+                     + {"fp8": " block-scaled FP8 e4m3", "fp8_token": " per-token FP8 e4m3"}.get(cfg.dtype, " bf16")
                      + ("" if cfg.bias is None else f" router bias {cfg.bias}({cfg.bias_param})"),
          "tokens_per_step": cfg.T, "seq_len": 1 if cfg.T <= 128 else cfg.T}
     return d
@@ -345,14 +363,15 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], 1 if cfg.dtype == "fp8" else 2)
+    eb = 1 if cfg.dtype in ("fp8", "fp8_token") else 2
+    flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], eb)
     peaks = r["peaks"]
     ms = r["ms"]
     tokens_s = whole_job_throughput(world, cfg.T, ms)
     tflops = flops / (ms * 1e-3) / 1e12
     gbs = bytes_ / (ms * 1e-3) / 1e9
     peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    if cfg.dtype == "fp8":
+    if eb == 1:
         peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)
     t_roof = max(flops / (peak_t * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9))
     memory_bound = bytes_ / (peaks["hbm_gbs"] * 1e9) >= flops / (peak_t * 1e12)
@@ -360,9 +379,12 @@ def main():
     s1_ms = r["stage_ms"]["stage1"]
     T, H, I = cfg.T, cfg.H, cfg.I
     npp_rows = sum(-(-c // r["plan"].block_m) * r["plan"].block_m for c in r["counts"])
-    eb = 1 if cfg.dtype == "fp8" else 2
     if memory_bound:
-        s1_alg = s1_bytes + npp_rows * H * eb + npp_rows * I * eb
+        # weights, the sorted activations read, h written (bf16 except block FP8's e4m3 codes), scales
+        h_bytes = 1 if cfg.dtype == "fp8" else 2
+        s1_alg = s1_bytes + npp_rows * H * eb + npp_rows * I * h_bytes
+        if cfg.dtype == "fp8_token":
+            s1_alg += active * 2 * I * 4 + npp_rows * 4
         achieved = s1_alg / (s1_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": "stage1 gate/up group GEMM (swap-AB)",
@@ -379,7 +401,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(tokens_s, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": r["K"], "warmup": r["W"], "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3/fp32-acc" if cfg.dtype == "fp8" else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3/fp32-acc" if eb == 1 else "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights; random init, no checkpoint)",
         "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}",
                        l2="inputs larger than L2 (expert weights streamed every step)"),

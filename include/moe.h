@@ -56,6 +56,8 @@ extern "C" {
 #define MOE_BF16 0          /* bf16 weights and activations, fp32 accumulation */
 #define MOE_FP8_BLOCK128 1  /* e4m3 weights (fp32 scale per 128x128 block) and
                                activations (fp32 scale per 1x128 group) */
+#define MOE_FP8_TOKEN 2     /* e4m3 weights (fp32 scale per output channel) and
+                               activations (fp32 scale per token) */
 
 #define MOE_MODE_GROUPED 0  /* tokens on the MMA M side, 128-row blocks */
 #define MOE_MODE_SWAP 1     /* weights on the MMA M side, tokens on N (small T) */
@@ -108,7 +110,8 @@ typedef struct moe_plan {
  * Choose mode, block size and K splits for a layer shape.  block_m = 0 and
  * split_k = 0 mean automatic; otherwise they are used as given (block_m
  * must be 128 in grouped mode and a multiple of 16 up to 128 in swap mode;
- * split_k splits stage 2's K = I and must divide I/64).  num_sms = 0 asks
+ * split_k splits stage 2's K = I and must divide I/64, or I/128 for
+ * MOE_FP8_TOKEN).  num_sms = 0 asks
  * the current CUDA device; a positive value plans for that many SMs without
  * touching CUDA.  Returns MOE_OK or a negative status.  Host only.
  */
@@ -135,9 +138,11 @@ typedef struct moe_ws_layout {
     int64_t num_tokens_post_padded; /* int32 [1] */
     int64_t expert_counts;   /* int32 [E] */
     int64_t x_sorted;        /* bf16 [max_padded][H] or e4m3 [max_padded][H] */
-    int64_t x_scales;        /* fp32 [H/128][max_padded] (FP8 only) */
+    int64_t x_scales;        /* fp32 [H/128][max_padded] (FP8 block), [max_padded] (FP8 token) */
     int64_t inter;           /* bf16 [max_padded][I] or e4m3 [max_padded][I] */
-    int64_t inter_scales;    /* fp32 [I/128][max_padded] (FP8 only) */
+    int64_t inter_scales;    /* fp32 [I/128][max_padded] (FP8 block), [max_padded] (FP8 token) */
+    int64_t inter_h;         /* bf16 [max_padded][I]: SwiGLU output before its per-token
+                                quantisation (FP8 token only) */
     int64_t y;               /* fp32 [T*k][H], weighted rows in slot order */
     int64_t total;
 } moe_ws_layout_t;
@@ -207,6 +212,17 @@ int moe_quantize_fp8_act(const void *X, int64_t R, int C, uint8_t *q, float *s, 
 int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float *s, void *stream);
 
 /*
+ * Per-row FP8 quantisation ("per_Token" on the AITER page, section 3.2's
+ * quantisation types): one scale per row -- a token of the activations or
+ * an output channel of a weight stack -- scale = amax of the row / 448 (1
+ * for an all-zero row), codes e4m3(v / scale), rounded to nearest even and
+ * saturated to +-448.
+ *   X (device) bf16 [R][C], C % 16 == 0 -> q (device) e4m3 [R][C],
+ *   s (device) fp32 [R].  An expert stack [E][N][K] is R = E*N, C = K.
+ */
+int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream);
+
+/*
  * The whole layer: route, align-sort, stage 1 (gate/up group GEMM with the
  * SwiGLU epilogue), stage 2 (down group GEMM scaled by the top-k weights),
  * combine.  out (device) bf16 [T][H].
@@ -216,6 +232,11 @@ int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float 
  *     [E*H/128][I/128] (as produced by moe_quantize_fp8_weights); x is
  *     quantised per 1x128 group inside the call, the router runs on bf16 x,
  *     and the SwiGLU output is re-quantised per 1x128 group between stages.
+ *   dtype MOE_FP8_TOKEN: W_gate_up / W_down (device) e4m3 with w1_scale
+ *     (device) fp32 [E*2I] and w2_scale (device) fp32 [E*H], one per output
+ *     channel (as produced by moe_quantize_fp8_rows); x is quantised per
+ *     token inside the call, the router runs on bf16 x, and the SwiGLU
+ *     output (rounded to bf16) is re-quantised per token between stages.
  *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H]; router_bias
  *   (device) fp32 [E] or NULL; block_m / split_k as in moe_plan;
  *   ws (device) of at least moe_fused_workspace_size bytes, 1024-byte aligned.

@@ -1,8 +1,9 @@
 // C ABI of the fused MoE layer (declared in include/moe.h): argument
 // validation, the host planner (mode, block size, K split, workspace
 // carve-up), TMA descriptor encoding, and the launch sequence
-//   route -> align-sort -> gather (FP8: gather + 1x128 quantise) ->
-//   stage-1 group GEMM -> stage-2 group GEMM -> combine
+//   route -> align-sort -> gather (FP8: gather + quantise) ->
+//   stage-1 group GEMM (per-token FP8: + per-row quantisation of h) ->
+//   stage-2 group GEMM -> combine
 // on the caller's stream.  Nothing here allocates device memory or
 // synchronises (except moe_workspace_status, which reads one word back).
 #include <cudaTypedefs.h>
@@ -92,13 +93,13 @@ int num_sms_current_device()
 struct Layout {
     int64_t status, logits, topk_ids, topk_w, sort_scratch, counts, offsets, active, num_active, npp;
     int64_t sorted_ids, sorted_w, sorted_eids, slot_pos;
-    int64_t x_sorted, x_scales, inter, inter_scales, y, partials;
+    int64_t x_sorted, x_scales, inter, inter_scales, inter_h, y, partials;
     int64_t total;
 };
 
 static int validate_shape(int dtype, int T, int H, int I, int E, int k)
 {
-    if (dtype != MOE_BF16 && dtype != MOE_FP8_BLOCK128)
+    if (dtype != MOE_BF16 && dtype != MOE_FP8_BLOCK128 && dtype != MOE_FP8_TOKEN)
         return MOE_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0)
         return MOE_ERR_INVALID_ARG;
@@ -139,9 +140,10 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
     L.sorted_eids = take(NB * 4);
     L.slot_pos = take(S * 4);
     L.x_sorted = take(P * H * eb);
-    L.x_scales = (dtype == MOE_FP8_BLOCK128) ? take((H / 128) * P * 4) : -1;
+    L.x_scales = (dtype == MOE_FP8_BLOCK128) ? take((H / 128) * P * 4) : (dtype == MOE_FP8_TOKEN) ? take(P * 4) : -1;
     L.inter = take(P * I * eb);
-    L.inter_scales = (dtype == MOE_FP8_BLOCK128) ? take((I / 128) * P * 4) : -1;
+    L.inter_scales = (dtype == MOE_FP8_BLOCK128) ? take((I / 128) * P * 4) : (dtype == MOE_FP8_TOKEN) ? take(P * 4) : -1;
+    L.inter_h = (dtype == MOE_FP8_TOKEN) ? take(P * I * 2) : -1;
     if (p.split_k2 > 1) {
         L.y = -1;
         L.partials = take((int64_t)p.split_k2 * P * H * 4);
@@ -169,8 +171,9 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
     moe_plan_t p;
     memset(&p, 0, sizeof p);
     // Swap (weights on the MMA M side) while every expert segment fits one
-    // N <= 128 tile, i.e. T <= 128; FP8 always runs the grouped kernel.
-    p.mode = (dtype == MOE_BF16 && T <= 128) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
+    // N <= 128 tile, i.e. T <= 128; block-scaled FP8 always runs the grouped
+    // kernel.
+    p.mode = (dtype != MOE_FP8_BLOCK128 && T <= 128) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
     if (block_m == 0)
         block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
     if (p.mode == MOE_MODE_GROUPED && block_m != 128)
@@ -179,7 +182,7 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
         return MOE_ERR_UNSUPPORTED;
     p.block_m = block_m;
     p.split_k1 = 1;
-    const int kblocks2 = I / 64;
+    const int kblocks2 = I / (dtype == MOE_BF16 ? 64 : 128);  // 128-byte K blocks of stage 2
     if (p.mode == MOE_MODE_SWAP) {
         if (split_k == 0) {
             // Enough stage-2 tiles for ~4 per SM: the smallest divisor of I/64 that reaches it.
@@ -232,7 +235,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         return rc;
     if (!x || !W_router || !W_gate_up || !W_down || !out || !ws)
         return MOE_ERR_INVALID_ARG;
-    if (dtype == MOE_FP8_BLOCK128 && (!w1_scale || !w2_scale))
+    if (dtype != MOE_BF16 && (!w1_scale || !w2_scale || !aligned(w1_scale, 16) || !aligned(w2_scale, 16)))
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W_router, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) ||
         !aligned(out, 16) || !aligned(ws, 256))
@@ -283,6 +286,10 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     if (dtype == MOE_BF16)
         ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
                                 static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_enabled(kPdlGather), st);
+    else if (dtype == MOE_FP8_TOKEN)
+        ge = launch_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
+                               static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
+                               pdl_enabled(kPdlGather), st);
     else
         ge = launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S,
                                       k, H, P, static_cast<uint8_t *>(at(L.x_sorted)),
@@ -321,24 +328,35 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g1.N = I;
     g1.rows_per_expert = 2 * I;
     g1.split_k = 1;
-    g1.inter = at(L.inter);
+    g1.inter = (dtype == MOE_FP8_TOKEN) ? at(L.inter_h) : at(L.inter);
     g1.x_scales = static_cast<float *>(at(L.x_scales));
     g1.w_scales = w1_scale;
     g1.inter_scales = static_cast<float *>(at(L.inter_scales));
     cudaError_t ce;
     if (p.mode == MOE_MODE_SWAP) {
         const int64_t ub = (int64_t)((S < E) ? S : E) * (I / 128);
-        ce = launch_gemm_swap_bf16(1, g1, (int)(ub < nsm ? ub : nsm), st);
+        const int grid = (int)(ub < nsm ? ub : nsm);
+        ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(1, g1, grid, st) : launch_gemm_swap_fp8_token(1, g1, grid, st);
     } else {
         const int64_t ub = p.max_blocks * (I / 128);
-        ce = (dtype == MOE_BF16) ? launch_gemm_grouped_bf16(1, g1, (int)(ub < nsm ? ub : nsm), st)
-                                 : launch_gemm_grouped_fp8(1, g1, (int)(ub < nsm ? ub : nsm), st);
+        const int grid = (int)(ub < nsm ? ub : nsm);
+        ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(1, g1, grid, st)
+             : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(1, g1, grid, st)
+                                        : launch_gemm_grouped_fp8(1, g1, grid, st);
     }
     if (ce != cudaSuccess)
         return MOE_ERR_CUDA;
     mark(4, st);
 
     // ---------------------------------------------------------- stage 2
+    if (dtype == MOE_FP8_TOKEN) {
+        // h (bf16, sorted order) -> e4m3 codes with one scale per row (stage 2's input)
+        ce = launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr, so.num_post_padded, P, S,
+                               k, I, static_cast<uint8_t *>(at(L.inter)), static_cast<float *>(at(L.inter_scales)),
+                               pdl_enabled(kPdlGather), st);
+        if (ce != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I, P, box_inner, box_x_rows) ||
@@ -355,11 +373,14 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     const int nt2 = (H + 255) / 256;
     if (p.mode == MOE_MODE_SWAP) {
         const int64_t ub = (int64_t)((S < E) ? S : E) * nt2 * p.split_k2;
-        ce = launch_gemm_swap_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st);
+        const int grid = (int)(ub < nsm ? ub : nsm);
+        ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(2, g2, grid, st) : launch_gemm_swap_fp8_token(2, g2, grid, st);
     } else {
         const int64_t ub = p.max_blocks * nt2;
-        ce = (dtype == MOE_BF16) ? launch_gemm_grouped_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st)
-                                 : launch_gemm_grouped_fp8(2, g2, (int)(ub < nsm ? ub : nsm), st);
+        const int grid = (int)(ub < nsm ? ub : nsm);
+        ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(2, g2, grid, st)
+             : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(2, g2, grid, st)
+                                        : launch_gemm_grouped_fp8(2, g2, grid, st);
     }
     if (ce != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -503,6 +524,7 @@ int moe_workspace_layout(int dtype, int T, int H, int I, int E, int k, int block
     out->x_scales = L.x_scales;
     out->inter = L.inter;
     out->inter_scales = L.inter_scales;
+    out->inter_h = L.inter_h;
     out->y = L.y;
     out->total = L.total;
     return MOE_OK;
@@ -587,6 +609,14 @@ int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float 
         return MOE_ERR_INVALID_ARG;
     launch_quant_weights(static_cast<const __nv_bfloat16 *>(W), R, C, q, s, static_cast<cudaStream_t>(stream));
     return cuda_status(cudaGetLastError());
+}
+
+int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream)
+{
+    if (R < 0 || C <= 0 || C % 16 != 0 || !X || !q || !s || !aligned(X, 16) || !aligned(q, 16))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_rows(static_cast<const __nv_bfloat16 *>(X), nullptr, nullptr, R, 0, 1, C, q, s,
+                                         false, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_fused_forward(int dtype, const void *x, const void *W_router, const float *router_bias,

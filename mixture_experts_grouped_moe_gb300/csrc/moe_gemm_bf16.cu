@@ -1,6 +1,16 @@
-// Stage-1 and stage-2 group GEMMs of the fused MoE layer, bf16 inputs with
-// fp32 accumulation in tensor memory, on the sm_100-family tensor core
-// (tcgen05) fed by TMA.
+// Stage-1 and stage-2 group GEMMs of the fused MoE layer on the sm_100-family
+// tensor core (tcgen05) fed by TMA, fp32 accumulation in tensor memory, for
+// two input types:
+//   QT = 0  bf16 activations and weights (kind::f16)
+//   QT = 1  e4m3 activations and weights with one fp32 scale per row of each
+//           ("per_Token" on the AITER page: a scale per token, a scale per
+//           output channel).  Both scales are constant along K, so the whole
+//           K sum runs in the tensor core (kind::f8f6f4) and the epilogue
+//           multiplies accumulator element (token, channel) by
+//           s_token * s_channel -- no per-K-block promotion.
+// Every pipeline stage carries 128 bytes of K per row either way (64 bf16 or
+// 128 e4m3 elements), so the tiles, the 128-byte swizzle and the descriptor
+// steps (32 bytes per MMA: K = 16 bf16 or 32 e4m3) are shared.
 //
 // The two stages are the "2-stage" path of the AITER walk-through
 // (section 3.2: stage 1 = gate/up projection + activation, stage 2 = down
@@ -40,7 +50,8 @@ namespace moe {
 
 namespace bf16gemm {
 
-constexpr int kBK = 64;                     // K elements per stage (128 bytes)
+template <int QT>
+constexpr int kBK = QT ? 128 : 64;          // K elements per stage (128 bytes)
 constexpr int kStages = 4;
 constexpr int kWRows = 256;
 constexpr int kXRows = 128;
@@ -95,12 +106,12 @@ __device__ __forceinline__ int num_tiles(const GemmArgs &a)
     }
 }
 
-template <int MODE, int STAGE>
+template <int MODE, int STAGE, int QT>
 __device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t)
 {
     Tile tl;
     tl.valid = 1;
-    const int nkb = a.K / kBK;
+    const int nkb = a.K / kBK<QT>;
     if (MODE == MOE_MODE_GROUPED) {
         const int nmb = *a.num_post_padded / 128;
         const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
@@ -166,7 +177,20 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
     }
 }
 
-template <int MODE, int STAGE>
+template <int QT>
+__device__ __forceinline__ void mma_kind(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
+{
+    if (QT)
+        mma_fp8(d, ad, bd, idesc, accum);
+    else
+        mma_bf16(d, ad, bd, idesc, accum);
+}
+
+// Per-channel and per-token scales of QT = 1 for 4 consecutive columns
+// (16-byte aligned: channel and token bases are multiples of 16).
+__device__ __forceinline__ float4 ld_scale4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+
+template <int MODE, int STAGE, int QT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -226,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 if (t < 0)
                     break;
-                const Tile tl = get_tile<MODE, STAGE>(a, t);
+                const Tile tl = get_tile<MODE, STAGE, QT>(a, t);
                 const uint32_t bytes = kWBytes + tl.nx * 128;
                 for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
                     if (!mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
@@ -236,13 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t *wdst = sm.stage[s];
                     uint8_t *xdst = sm.stage[s] + kWBytes;
                     mbar_arrive_expect_tx(&sm.full[s], bytes);
-                    tma_load_2d(wdst, &a.tm_w, kb * kBK, tl.wrow0, &sm.full[s], pol_w);
-                    tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * kBK, tl.wrow1, &sm.full[s], pol_w);
+                    tma_load_2d(wdst, &a.tm_w, kb * kBK<QT>, tl.wrow0, &sm.full[s], pol_w);
+                    tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * kBK<QT>, tl.wrow1, &sm.full[s], pol_w);
                     if (MODE == MOE_MODE_GROUPED) {
-                        tma_load_2d(xdst, &a.tm_x, kb * kBK, tl.xrow, &sm.full[s], pol_x);
+                        tma_load_2d(xdst, &a.tm_x, kb * kBK<QT>, tl.xrow, &sm.full[s], pol_x);
                     } else {
                         for (int c = 0; c < tl.nx; c += 16)
-                            tma_load_2d(xdst + c * 128, &a.tm_x, kb * kBK, tl.xrow + c, &sm.full[s], pol_x);
+                            tma_load_2d(xdst + c * 128, &a.tm_x, kb * kBK<QT>, tl.xrow + c, &sm.full[s], pol_x);
                     }
                     issued[s] = 1;
                     issued_ph[s] = ph;
@@ -285,15 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tq_advance(qs, qph);
                 if (t < 0)
                     break;
-                const Tile tl = get_tile<MODE, STAGE>(a, t);
+                const Tile tl = get_tile<MODE, STAGE, QT>(a, t);
                 if (!mbar_wait(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccCols;
-                const uint32_t idesc = (MODE == MOE_MODE_GROUPED) ? make_idesc(1, 1, 128, 256)
-                                                                  : make_idesc(1, 1, 128, (uint32_t)tl.nx);
+                constexpr uint32_t kFmt = QT ? 0u : 1u;  // e4m3 (kind::f8f6f4) or bf16 (kind::f16)
+                const uint32_t idesc = (MODE == MOE_MODE_GROUPED) ? make_idesc(kFmt, kFmt, 128, 256)
+                                                                  : make_idesc(kFmt, kFmt, 128, (uint32_t)tl.nx);
                 for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
                     if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
                         ok = false;
@@ -303,14 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     const uint8_t *w = sm.stage[s];
                     const uint8_t *xs = sm.stage[s] + kWBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                    for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
                         const uint32_t accum = (kb > tl.kb0 || kk > 0) ? 1u : 0u;
                         if (MODE == MOE_MODE_GROUPED) {
-                            mma_bf16(d, smem_desc_sw128(xs + kk * 32), smem_desc_sw128(w + kk * 32), idesc, accum);
+                            mma_kind<QT>(d, smem_desc_sw128(xs + kk * 32), smem_desc_sw128(w + kk * 32), idesc,
+                                         accum);
                         } else {
-                            mma_bf16(d, smem_desc_sw128(w + kk * 32), smem_desc_sw128(xs + kk * 32), idesc, accum);
-                            mma_bf16(d + 128, smem_desc_sw128(w + kWBytes / 2 + kk * 32),
-                                     smem_desc_sw128(xs + kk * 32), idesc, accum);
+                            mma_kind<QT>(d, smem_desc_sw128(w + kk * 32), smem_desc_sw128(xs + kk * 32), idesc,
+                                         accum);
+                            mma_kind<QT>(d + 128, smem_desc_sw128(w + kWBytes / 2 + kk * 32),
+                                         smem_desc_sw128(xs + kk * 32), idesc, accum);
                         }
                     }
                     any = true;
@@ -356,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tq_advance(qs, qph);
             if (t < 0)
                 break;
-            const Tile tl = get_tile<MODE, STAGE>(a, t);
+            const Tile tl = get_tile<MODE, STAGE, QT>(a, t);
             bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
@@ -367,11 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (MODE == MOE_MODE_GROUPED && STAGE == 1) {
                 // row = sorted position; columns j (gate) and 128+j (up) of h column ncol0+j
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)(tl.xrow + row) * a.N + tl.ncol0;
+                const float sx = QT ? a.x_scales[tl.xrow + row] : 1.0f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     float g[32], u[32], h[32];
                     tmem_ld32(tacc + c0, g);
                     tmem_ld32(tacc + 128 + c0, u);
+                    if (QT) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 sg = ld_scale4(a.w_scales + tl.wrow0 + c0 + i);
+                            const float4 su = ld_scale4(a.w_scales + tl.wrow1 + c0 + i);
+                            g[i] *= sx * sg.x, g[i + 1] *= sx * sg.y, g[i + 2] *= sx * sg.z, g[i + 3] *= sx * sg.w;
+                            u[i] *= sx * su.x, u[i + 1] *= sx * su.y, u[i + 2] *= sx * su.z, u[i + 3] *= sx * su.w;
+                        }
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         h[i] = silu(g[i]) * u[i];
@@ -380,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             } else if (MODE == MOE_MODE_GROUPED && STAGE == 2) {
                 const int pos = tl.xrow + row;
                 const int slot = a.sorted_ids[pos];
-                const float wgt = a.sorted_weights[pos];
+                const float wgt = a.sorted_weights[pos] * (QT ? a.x_scales[pos] : 1.0f);
                 const bool live = slot < a.S;
                 float *dst = a.y + (size_t)(live ? slot : 0) * a.N + tl.ncol0;
                 const int ncols = min(256, a.N - tl.ncol0);
@@ -388,6 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int c0 = 0; c0 < ncols; c0 += 32) {
                     float v[32];
                     tmem_ld32(tacc + c0, v);
+                    if (QT) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 sw = ld_scale4(a.w_scales + tl.wrow0 + c0 + i);
+                            v[i] *= sw.x, v[i + 1] *= sw.y, v[i + 2] *= sw.z, v[i + 3] *= sw.w;
+                        }
+                    }
                     if (live) {
                         float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
@@ -399,11 +443,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             } else if (MODE == MOE_MODE_SWAP && STAGE == 1) {
                 // row = h column within the 128-wide tile; TMEM columns = tokens of the segment
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)tl.xrow * a.N + tl.ncol0 + row;
+                const float swg = QT ? a.w_scales[tl.wrow0 + row] : 1.0f;
+                const float swu = QT ? a.w_scales[tl.wrow1 + row] : 1.0f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < tl.nx; c0 += 16) {
                     float g[16], u[16];
                     tmem_ld16(tacc + c0, g);
                     tmem_ld16(tacc + 128 + c0, u);
+                    if (QT) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 sx = ld_scale4(a.x_scales + tl.xrow + c0 + j);
+                            g[j] *= swg * sx.x, g[j + 1] *= swg * sx.y, g[j + 2] *= swg * sx.z, g[j + 3] *= swg * sx.w;
+                            u[j] *= swu * sx.x, u[j + 1] *= swu * sx.y, u[j + 2] *= swu * sx.z, u[j + 3] *= swu * sx.w;
+                        }
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         dst[(size_t)(c0 + j) * a.N] = __float2bfloat16_rn(silu(g[j]) * u[j]);
@@ -414,12 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int half = 0; half < 2; ++half) {
                     const int n = tl.ncol0 + half * 128 + row;
                     const bool nok = n < a.N;
+                    const float sw = (QT && nok) ? a.w_scales[tl.wrow0 + half * 128 + row] : 1.0f;
 #pragma unroll 1
                     for (int c0 = 0; c0 < tl.nx; c0 += 16) {
                         float v[16];
                         tmem_ld16(tacc + half * 128 + c0, v);
                         if (!nok)
                             continue;
+                        if (QT) {
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4) {
+                                const float4 sx = ld_scale4(a.x_scales + tl.xrow + c0 + j);
+                                v[j] *= sw * sx.x, v[j + 1] *= sw * sx.y, v[j + 2] *= sw * sx.z, v[j + 3] *= sw * sx.w;
+                            }
+                        }
                         if (a.split_k > 1) {
                             float *dst = a.partials + ((size_t)tl.ks * a.P_max + tl.xrow + c0) * a.N + n;
 #pragma unroll
@@ -455,10 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int MODE, int STAGE>
+template <int MODE, int STAGE, int QT>
 cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
 {
-    auto kern = gemm_kernel<MODE, STAGE>;
+    auto kern = gemm_kernel<MODE, STAGE, QT>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess)
         return err;
@@ -470,14 +532,26 @@ cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
 
 cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st)
 {
-    return stage == 1 ? bf16gemm::launch<MOE_MODE_GROUPED, 1>(a, grid, st)
-                      : bf16gemm::launch<MOE_MODE_GROUPED, 2>(a, grid, st);
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_GROUPED, 1, 0>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_GROUPED, 2, 0>(a, grid, st);
 }
 
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st)
 {
-    return stage == 1 ? bf16gemm::launch<MOE_MODE_SWAP, 1>(a, grid, st)
-                      : bf16gemm::launch<MOE_MODE_SWAP, 2>(a, grid, st);
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_SWAP, 1, 0>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_SWAP, 2, 0>(a, grid, st);
+}
+
+cudaError_t launch_gemm_grouped_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_GROUPED, 1, 1>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_GROUPED, 2, 1>(a, grid, st);
+}
+
+cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? bf16gemm::launch<MOE_MODE_SWAP, 1, 1>(a, grid, st)
+                      : bf16gemm::launch<MOE_MODE_SWAP, 2, 1>(a, grid, st);
 }
 
 }  // namespace moe

@@ -104,6 +104,11 @@ cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sort
                                      int k, int H, int64_t P_max, uint8_t *q, float *sT, bool pdl, cudaStream_t st);
 
 void launch_quant_act(const __nv_bfloat16 *X, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
+// Per-row e4m3 quantisation (scale = row amax / 448); rows gathered through
+// sorted_ids (token = slot / k, padding -> zero row) when it is non-null;
+// the row count read from nrows (device) when non-null, else R.
+cudaError_t launch_quant_rows(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
+                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st);
 void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
 
 // out[t] = sum_j Y[t*k+j] (j ascending), fp32 -> bf16.
@@ -127,8 +132,8 @@ struct GemmArgs {
     const int32_t *num_active;
     const int32_t *expert_counts;
     // FP8 block scales
-    const float *x_scales;   // [K/128][P_max]
-    const float *w_scales;   // [E*rows_per_expert/128][K/128]
+    const float *x_scales;   // block FP8: [K/128][P_max]; per-token FP8: [P_max]
+    const float *w_scales;   // block FP8: [E*rows_per_expert/128][K/128]; per-token FP8: [E*rows_per_expert]
     int K;                   // reduction length
     int N;                   // output columns per expert (stage 1: I, stage 2: H)
     int rows_per_expert;     // weight rows per expert (stage 1: 2I, stage 2: H)
@@ -154,5 +159,7 @@ int num_sms_current_device();
 cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_gemm_grouped_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 
 }  // namespace moe

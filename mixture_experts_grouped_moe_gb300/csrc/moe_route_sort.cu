@@ -407,13 +407,16 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
                                                          int64_t P_max, int64_t NB_max, SortOut o)
 {
     __shared__ int32_t s_ids[kSmallSort];
+    __shared__ float s_w[kSmallSort];
     __shared__ int32_t s_pad[1024];
     __shared__ int32_t s_act[1024];
     pdl_wait();
     pdl_trigger();
     const int e = threadIdx.x;
-    if (e < S)
+    if (e < S) {
         s_ids[e] = ids[e];
+        s_w[e] = wts[e];  // staged so the per-expert scatter below waits on no global load
+    }
     __syncthreads();
     int cnt = 0;
     if (e < E)
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
         for (int s = 0; s < S; ++s)
             if (s_ids[s] == e) {
                 o.sorted_ids[pos] = s;
-                o.sorted_weights[pos] = wts[s];
+                o.sorted_weights[pos] = s_w[s];
                 if (o.slot_pos)
                     o.slot_pos[s] = pos;
                 ++pos;
@@ -744,6 +747,101 @@ cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sort
         grid = 1;
     return launch_kernel(pdl, gather_quant_kernel, dim3(grid), dim3(256), 0, st, x, sorted_ids, npp, S, k, H, P_max,
                          q, sT);
+}
+
+// One scale per row ("per_Token"): a CTA per row, amax over the whole row,
+// then codes.  With sorted_ids the rows are gathered (row i is token
+// sorted_ids[i] / k, a zero row with scale 1 for padding); with nrows the row
+// count is read on the device (the rows past it are never used).  NV > 0
+// keeps the row in registers between the two passes (C <= 256 * 8 * NV);
+// NV = 0 reads it twice.
+template <int NV>
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16 *__restrict__ X,
+                                                        const int32_t *__restrict__ sorted_ids,
+                                                        const int32_t *__restrict__ nrows, int64_t R, int S,
+                                                        int k, int C, uint8_t *__restrict__ q,
+                                                        float *__restrict__ s)
+{
+    __shared__ float s_red[8];
+    pdl_wait();
+    pdl_trigger();
+    const int64_t rows = nrows ? (int64_t)*nrows : R;
+    const int nvec = C / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        bool zero = false;
+        int64_t src_row = r;
+        if (sorted_ids) {
+            const int sl = sorted_ids[r];
+            zero = sl >= S;
+            src_row = zero ? 0 : sl / k;
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(X + src_row * C);
+        uint2 *dst = reinterpret_cast<uint2 *>(q + r * C);
+        float m = 0.0f;
+        uint4 v[NV > 0 ? NV : 1];
+        if (NV > 0) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * 256;
+                v[i] = (c < nvec && !zero) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                float f[8];
+                bf16x8_to_float(v[i], f);
+                m = fmaxf(m, absmax8(f));
+            }
+        } else if (!zero) {
+            for (int c = threadIdx.x; c < nvec; c += 256) {
+                float f[8];
+                bf16x8_to_float(__ldg(src + c), f);
+                m = fmaxf(m, absmax8(f));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0)
+            s_red[warp] = m;
+        __syncthreads();
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            amax = fmaxf(amax, s_red[i]);
+        const float sc = group_scale(amax);
+        if (NV > 0) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c = threadIdx.x + i * 256;
+                if (c < nvec) {
+                    float f[8];
+                    bf16x8_to_float(v[i], f);
+                    dst[c] = encode8(f, sc);
+                }
+            }
+        } else {
+            for (int c = threadIdx.x; c < nvec; c += 256) {
+                float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (!zero)
+                    bf16x8_to_float(__ldg(src + c), f);
+                dst[c] = encode8(f, sc);
+            }
+        }
+        if (threadIdx.x == 0)
+            s[r] = sc;
+        __syncthreads();  // s_red is rewritten for the next row
+    }
+}
+
+cudaError_t launch_quant_rows(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
+                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st)
+{
+    int64_t grid = R < 16384 ? R : 16384;
+    if (grid < 1)
+        return cudaSuccess;
+    if (C <= 256 * 8 * 8)
+        return launch_kernel(pdl, quant_rows_kernel<8>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows,
+                             R, S, k, C, q, s);
+    return launch_kernel(pdl, quant_rows_kernel<0>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows, R,
+                         S, k, C, q, s);
 }
 
 // One CTA per 128x128 block of W [R][C]: amax over the block, then codes.

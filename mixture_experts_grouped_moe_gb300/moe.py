@@ -23,6 +23,7 @@ MOE_ERR_TIMEOUT = -5
 
 MOE_BF16 = 0
 MOE_FP8_BLOCK128 = 1
+MOE_FP8_TOKEN = 2
 MOE_MODE_GROUPED = 0
 MOE_MODE_SWAP = 1
 
@@ -30,8 +31,8 @@ EXPORTED = [
     "moe_status_string", "moe_version", "moe_align_sort_sizes", "moe_block_size_m_heuristic",
     "moe_ksplit_heuristic", "moe_plan", "moe_fused_workspace_size", "moe_workspace_layout",
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
-    "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_fused_forward", "moe_host_staging_bytes",
-    "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
+    "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
+    "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
 ]
 
 
@@ -50,8 +51,8 @@ class moe_plan_t(ctypes.Structure):
 class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "status", "topk_ids", "topk_weights", "sorted_ids", "sorted_weights", "sorted_expert_ids",
-        "num_tokens_post_padded", "expert_counts", "x_sorted", "x_scales", "inter", "inter_scales", "y",
-        "total")]
+        "num_tokens_post_padded", "expert_counts", "x_sorted", "x_scales", "inter", "inter_scales", "inter_h",
+        "y", "total")]
 
 
 _lock = threading.Lock()
@@ -90,6 +91,7 @@ def load(build_if_missing: bool = False):
             "moe_align_sort": (I, [P, P, I, I, I, I, P, P, P, P, P, P, SZ, P]),
             "moe_quantize_fp8_act": (I, [P, I64, I, P, P, P]),
             "moe_quantize_fp8_weights": (I, [P, I64, I, P, P, P]),
+            "moe_quantize_fp8_rows": (I, [P, I64, I, P, P, P]),
             "moe_fused_forward": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_host_staging_bytes": (SZ, [I, I]),
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
@@ -210,6 +212,10 @@ def moe_quantize_fp8_act(X, R, C, q, s, stream=None):
 def moe_quantize_fp8_weights(W, R, C, q, s, stream=None):
     return _check("moe_quantize_fp8_weights",
                   load().moe_quantize_fp8_weights(_p(W), R, C, _p(q), _p(s), _stream(stream)))
+
+
+def moe_quantize_fp8_rows(X, R, C, q, s, stream=None):
+    return _check("moe_quantize_fp8_rows", load().moe_quantize_fp8_rows(_p(X), R, C, _p(q), _p(s), _stream(stream)))
 
 
 def moe_fused_forward(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,

@@ -11,7 +11,9 @@ DeepSeek-style shapes; tensors are random, there are no trained weights):
   tiny              T=16   H=128  I=256   E=4   k=2
   mixtral_decode    T=32   H=4096 I=14336 E=8   k=2
   mixtral_prefill   T=8192 H=4096 I=14336 E=8   k=2  router bias ~ N(0, var 0.5)
-  mixtral_fp8       T=4096 H=4096 I=14336 E=8   k=2  (quantised by the path)
+  mixtral_fp8       T=4096 H=4096 I=14336 E=8   k=2  (block-scaled FP8, quantised by the path)
+  mixtral_fp8_token T=4096 H=4096 I=14336 E=8   k=2  (per-token FP8)
+  mixtral_fp8_token_decode  T=32, same shapes (per-token FP8)
   finegrained_zipf  T=4096 H=7168 I=2048  E=256 k=8  Zipf(s=1.2) router bias
 
 Distributions: x ~ N(0, 1); W_router, W_gate, W_up ~ N(0, 1/H);
@@ -43,7 +45,7 @@ class MoEConfig:
     bias: str | None = None  # None | "normal" | "zipf"
     bias_param: float = 0.0  # variance for "normal", exponent s for "zipf"
     zipf_beta: float = 1.0
-    dtype: str = "bf16"      # "bf16" | "fp8" (block-scaled e4m3)
+    dtype: str = "bf16"      # "bf16" | "fp8" (block-scaled e4m3) | "fp8_token" (per-token e4m3)
 
     @property
     def S(self) -> int:
@@ -59,6 +61,9 @@ CONFIGS = {
     "mixtral_prefill": MoEConfig("mixtral_prefill", T=8192, H=4096, I=14336, E=8, k=2,
                                  bias="normal", bias_param=0.5),
     "mixtral_fp8": MoEConfig("mixtral_fp8", T=4096, H=4096, I=14336, E=8, k=2, dtype="fp8"),
+    "mixtral_fp8_token": MoEConfig("mixtral_fp8_token", T=4096, H=4096, I=14336, E=8, k=2, dtype="fp8_token"),
+    "mixtral_fp8_token_decode": MoEConfig("mixtral_fp8_token_decode", T=32, H=4096, I=14336, E=8, k=2,
+                                          dtype="fp8_token"),
     "finegrained_zipf": MoEConfig("finegrained_zipf", T=4096, H=7168, I=2048, E=256, k=8,
                                   bias="zipf", bias_param=1.2),
 }
