@@ -296,10 +296,23 @@ int moe_align_sort_noalloc(const int32_t *topk_ids, const float *topk_weights, i
  * events, cudaEvent_t cast to void*, created by the caller) are recorded on
  * the call's stream at [0] entry, [1] after routing, [2] after the sort,
  * [3] after the gather (FP8: gather + quantise), [4] after stage 1, [5]
- * after stage 2, [6] after the combine.  One call consumes the setting;
+ * after stage 2 (per-token FP8: including the re-quantisation of the
+ * intermediate), [6] after the combine.  One call consumes the setting;
  * events = NULL clears it.  Returns MOE_OK or MOE_ERR_INVALID_ARG.
  */
 int moe_set_stage_events(void *const *events, int n);
+
+/*
+ * Choice of the grouped-mode GEMM kernel for MOE_BF16 and MOE_FP8_TOKEN,
+ * process-wide: mode 1 always runs the two-SM (CTA pair) kernels, 0 never,
+ * -1 (the default, or MOE_GEMM_PAIR unset in the environment) lets the
+ * library choose: pairs when the average active expert holds at least 4
+ * token blocks, in both stages for bf16 and in stage 2 for per-token FP8.
+ * Both kernels give results within the same tolerance of the definition.
+ * Returns MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the fused-MoE
+ * pages: a kernel-selection switch of this library.)
+ */
+int moe_set_gemm_pair(int mode);
 
 #ifdef __cplusplus
 }

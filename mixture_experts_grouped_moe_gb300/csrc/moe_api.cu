@@ -10,6 +10,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -72,6 +73,41 @@ bool pdl_enabled(int site, bool grouped)
     if (mask < 0)
         mask = grouped ? 0x3f & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : 0x3f;
     return (mask >> site) & 1;
+}
+
+// Two-SM (CTA pair) grouped GEMMs: -1 automatic, 0 never, 1 whenever supported.
+// Starts from MOE_GEMM_PAIR in the environment; moe_set_gemm_pair overrides it.
+static std::atomic<int> g_pair_mode{-2};
+
+static int pair_mode()
+{
+    int m = g_pair_mode.load(std::memory_order_relaxed);
+    if (m == -2) {
+        const char *v = getenv("MOE_GEMM_PAIR");
+        m = (v && v[0] == '0') ? 0 : (v && v[0] == '1') ? 1 : -1;
+        g_pair_mode.store(m, std::memory_order_relaxed);
+    }
+    return m;
+}
+
+// Automatic rule (same-box measurements on GB300): pairs pay off once the
+// average active expert holds at least 4 token blocks (a half-used pair at an
+// expert's end then wastes at most 1/8 of its tiles); for per-token FP8 only
+// stage 2 gains (Mixtral shapes, T=4096: stage 2 0.49 -> 0.42 ms, stage 1
+// 0.77 -> 0.83 ms), for bf16 both stages (T=8192: 2.45 -> 2.31 and
+// 1.38 -> 1.16 ms).
+static bool use_pair(int dtype, int stage, int T, int k, int E)
+{
+    if (dtype == MOE_FP8_BLOCK128 || !gemm_pair_supported(E))
+        return false;
+    const int m = pair_mode();
+    if (m >= 0)
+        return m == 1;
+    const int64_t S = (int64_t)T * k;
+    const int64_t act = S < E ? S : E;
+    if (S < 4 * 128 * act)
+        return false;
+    return dtype == MOE_BF16 || stage == 2;
 }
 
 int num_sms_current_device()
@@ -337,6 +373,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         const int64_t ub = (int64_t)((S < E) ? S : E) * (I / 128);
         const int grid = (int)(ub < nsm ? ub : nsm);
         ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(1, g1, grid, st) : launch_gemm_swap_fp8_token(1, g1, grid, st);
+    } else if (use_pair(dtype, 1, T, k, E)) {
+        ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
     } else {
         const int64_t ub = p.max_blocks * (I / 128);
         const int grid = (int)(ub < nsm ? ub : nsm);
@@ -375,6 +413,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         const int64_t ub = (int64_t)((S < E) ? S : E) * nt2 * p.split_k2;
         const int grid = (int)(ub < nsm ? ub : nsm);
         ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(2, g2, grid, st) : launch_gemm_swap_fp8_token(2, g2, grid, st);
+    } else if (use_pair(dtype, 2, T, k, E)) {
+        ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
     } else {
         const int64_t ub = p.max_blocks * nt2;
         const int grid = (int)(ub < nsm ? ub : nsm);
@@ -417,6 +457,14 @@ const char *moe_status_string(int status)
 }
 
 int moe_version(void) { return 100; }
+
+int moe_set_gemm_pair(int mode)
+{
+    if (mode < -1 || mode > 1)
+        return MOE_ERR_INVALID_ARG;
+    g_pair_mode.store(mode, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 int moe_set_stage_events(void *const *events, int n)
 {

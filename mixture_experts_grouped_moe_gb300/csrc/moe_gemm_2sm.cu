@@ -1,0 +1,514 @@
+// Grouped-mode (large T) stage-1 and stage-2 group GEMMs on CTA pairs: the
+// two-SM form of the tcgen05 tensor core (.cta_group::2) computes one
+// 256 x 256 tile per pair, bf16 (QT = 0) or per-token e4m3 (QT = 1) inputs,
+// fp32 accumulation in TMEM.
+//
+// Why pairs: a one-SM 128 x 256 tile moves 384 operand rows through shared
+// memory for 128 * 256 products per K step; a pair tile moves 2 x 256 rows
+// for 256 * 256, a third fewer bytes per FLOP through the L2 -> SM path,
+// which is what limits the one-SM kernel at FP8 rates.
+//
+// A pair tile is two consecutive 128-row blocks of one expert's sorted rows
+// (the token sort of the AITER walk-through, section 3.1, pads every expert
+// to whole blocks) against 256 weight rows: stage 1, 128 gate rows and the
+// matching 128 up rows (accumulator columns j and 128 + j pair up for
+// SwiGLU); stage 2, 256 rows of W_down.  CTA r of the pair holds block r of
+// the tokens (A rows) and weight half r (B columns) in its shared memory, and
+// block r's 128 accumulator rows in its TMEM.  An expert with an odd block
+// count ends on a half-used pair: the second CTA repeats the first block's
+// rows and stores nothing.
+//
+// Roles (192 threads per CTA, one CTA per SM):
+//   warp 0      TMA producer in both CTAs: the CTA's own A and B halves; both
+//               CTAs' bytes complete on the leader's stage barrier
+//   warp 1      TMEM allocation of the pair (both CTAs); in the leader, one
+//               thread issues the pair MMAs and commits them to barriers of
+//               both CTAs (stage free, accumulator ready)
+//   warps 2..5  epilogue in both CTAs on the CTA's own accumulator rows;
+//               they release the accumulator on the leader's barrier
+// The leader claims tiles from a global counter and publishes each index to
+// both CTAs through a small shared-memory queue.  Within an expert, groups of
+// up to 8 pairs walk the N tiles together so that one weight tile serves
+// 16 token blocks from L2 and an expert's weights are read from HBM about
+// once.  Every wait is bounded; a CTA that gives up raises the status word
+// and both CTAs still meet at the final cluster barrier.
+#include "gemm_common.cuh"
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace gemm2sm {
+
+constexpr int kStages = 6;
+constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes of K
+constexpr int kStageBytes = 2 * kHalfBytes; // [A: token rows | B: weight rows]
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kMaxE = 1024;
+constexpr int kGroupPairs = 8;
+
+struct __align__(1024) Smem {
+    uint8_t stage[kStages][kStageBytes];
+    uint64_t full[kStages];    // leader: both CTAs' TMA bytes of the stage
+    uint64_t empty[kStages];   // both: the pair MMAs have read the stage
+    uint64_t tfull[2];         // both: accumulator complete
+    uint64_t tempty[2];        // leader: both CTAs' epilogues have drained it
+    uint64_t drain;
+    int qidx[kTileQ];          // tile queue: indices claimed by the leader, published to both CTAs
+    uint64_t qfull[kTileQ];    // both: an index is in this CTA's slot
+    uint64_t qempty[kTileQ];   // leader: every consumer of both CTAs has read the slot
+    uint32_t tmem_base;
+    int abort;
+    int ntiles;
+    int off[kMaxE + 1];        // expert_offsets (sorted rows)
+    int tstart[kMaxE + 1];     // first pair tile of each expert
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct PairTile {
+    int e;
+    int mb0;      // first 128-row block of the pair
+    int second;   // the pair's second block is a real block of expert e
+    int wrow0;    // weight rows of B half 0 / half 1
+    int wrow1;
+    int ncol0;    // output column base
+};
+
+template <int STAGE>
+__device__ __forceinline__ int n_tiles_n(const GemmArgs &a)
+{
+    return (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
+}
+
+template <int STAGE>
+__device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, int t)
+{
+    const int nnt = n_tiles_n<STAGE>(a);
+    // the expert: the last e with tstart[e] <= t (empty experts share their successor's start)
+    int lo = 0, hi = a.E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.tstart[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    PairTile p;
+    p.e = lo;
+    const int local = t - sm.tstart[lo];
+    const int nb = (sm.off[lo + 1] - sm.off[lo]) >> 7;
+    const int np = (nb + 1) >> 1;
+    const int gi = local / (kGroupPairs * nnt);
+    const int gsize = min(kGroupPairs, np - gi * kGroupPairs);
+    const int wi = local - gi * kGroupPairs * nnt;
+    const int nt = wi / gsize;
+    const int pi = gi * kGroupPairs + wi % gsize;
+    p.mb0 = (sm.off[lo] >> 7) + 2 * pi;
+    p.second = (2 * pi + 1 < nb) ? 1 : 0;
+    if (STAGE == 1) {
+        p.wrow0 = lo * a.rows_per_expert + nt * 128;          // gate rows
+        p.wrow1 = lo * a.rows_per_expert + a.N + nt * 128;    // matching up rows
+        p.ncol0 = nt * 128;
+    } else {
+        p.wrow0 = lo * a.rows_per_expert + nt * 256;
+        p.wrow1 = p.wrow0 + 128;
+        p.ncol0 = nt * 256;
+    }
+    return p;
+}
+
+template <int STAGE, int QT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    volatile int *abort_flag = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 2 * kEpiWarps);
+        }
+        mbar_init(&sm.drain, 1);
+        for (int i = 0; i < kTileQ; ++i) {
+            mbar_init(&sm.qfull[i], 1);
+            mbar_init(&sm.qempty[i], 2 * (1 + kEpiWarps));  // producer/MMA + epilogue warps of each CTA
+        }
+        sm.abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&a.tm_x);
+        tma_prefetch_desc(&a.tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    pdl_wait();
+    pdl_trigger();
+
+    // pair-tile table: tstart[e] = sum over experts before e of ceil(blocks/2) * N tiles
+    if (warp == 2) {
+        const int E = a.E;
+        const int nnt = n_tiles_n<STAGE>(a);
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int sum = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int o0 = a.expert_offsets[e], o1 = a.expert_offsets[e + 1];
+            sm.off[e] = o0;
+            sum += (((o1 - o0) >> 7) + 1) / 2 * nnt;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += v;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < e1; ++e) {
+            sm.tstart[e] = run;
+            run += (((a.expert_offsets[e + 1] - a.expert_offsets[e]) >> 7) + 1) / 2 * nnt;
+        }
+        if (lane == 31) {
+            sm.tstart[E] = incl;
+            sm.off[E] = a.expert_offsets[E];
+            sm.ntiles = incl;
+        }
+    }
+    __syncthreads();
+    const int ntiles = sm.ntiles;
+    const int nkb = a.K / kBK<QT>;
+    // consumers of the tile queue: wait for the slot, read it, release it on the leader
+    auto pop = [&](int &qs, uint32_t &qph, int &t) -> bool {
+        if (!mbar_wait_cluster(&sm.qfull[qs], qph, a.status, abort_flag))
+            return false;
+        t = *reinterpret_cast<volatile int *>(&sm.qidx[qs]);
+        return true;
+    };
+    auto release = [&](int qs) { mbar_arrive_cluster(cluster_map(&sm.qempty[qs], 0)); };
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true, any = false;
+            int qs = 0;
+            uint32_t qph = 0;
+            // the leader claims tiles one ahead from the global counter (uneven pair speeds balance out)
+            int claim = leader ? atomicAdd(a.tile_counter, 1) : 0;
+            for (;;) {
+                int t;
+                if (leader) {
+                    if (!mbar_wait_cluster(&sm.qempty[qs], qph ^ 1, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    t = claim < ntiles ? claim : -1;
+                    *reinterpret_cast<volatile int *>(&sm.qidx[qs]) = t;
+                    st_cluster_s32(cluster_map(&sm.qidx[qs], 1), t);
+                    mbar_arrive(&sm.qfull[qs]);
+                    mbar_arrive_cluster(cluster_map(&sm.qfull[qs], 1));
+                    if (t >= 0)
+                        claim = atomicAdd(a.tile_counter, 1);
+                } else {
+                    if (!pop(qs, qph, t)) {
+                        ok = false;
+                        break;
+                    }
+                    release(qs);
+                }
+                if (++qs == kTileQ) {
+                    qs = 0;
+                    qph ^= 1;
+                }
+                if (t < 0)
+                    break;
+                const PairTile p = decode<STAGE>(sm, a, t);
+                const int xrow = (rank == 1 && p.second) ? (p.mb0 + 1) * 128 : p.mb0 * 128;
+                const int wrow = rank == 0 ? p.wrow0 : p.wrow1;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fullc = cluster_map(&sm.full[s], 0);
+                    if (leader)
+                        mbar_arrive_expect_tx(&sm.full[s], 2 * kStageBytes);
+                    tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
+                    tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_w);
+                    any = true;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+            }
+            if (!ok && any) {
+                // copies in flight complete on the leader's barriers: give them a bounded moment to land
+                const unsigned long long t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 20000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (leader && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true, any = false;
+            const uint32_t idesc = make_idesc(QT ? 0u : 1u, QT ? 0u : 1u, 256, 256);
+            int qs = 0;
+            uint32_t qph = 0;
+            for (;;) {
+                int t;
+                if (!pop(qs, qph, t)) {
+                    ok = false;
+                    break;
+                }
+                release(qs);
+                if (++qs == kTileQ) {
+                    qs = 0;
+                    qph ^= 1;
+                }
+                if (t < 0)
+                    break;
+                if (!mbar_wait_cluster(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * kAccCols;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *xa = sm.stage[s];
+                    const uint8_t *wb = sm.stage[s] + kHalfBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_pair<QT>(d, smem_desc_sw128(xa + kk * 32), smem_desc_sw128(wb + kk * 32), idesc,
+                                     (kb > 0 || kk > 0) ? 1u : 0u);
+                    any = true;
+                    mma_commit_pair(&sm.empty[s], 0x3);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit_pair(&sm.tfull[acc], 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok && any) {
+                mma_commit_pair(&sm.drain, 0x1);
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&sm.drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;           // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;    // accumulator row = token row within the CTA's block
+        int acc = 0;
+        uint32_t aph = 0;
+        int qs = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int t = -1;
+            bool qok = pop(qs, qph, t);
+            qok = __all_sync(0xffffffffu, qok);
+            if (!qok)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                release(qs);
+            if (++qs == kTileQ) {
+                qs = 0;
+                qph ^= 1;
+            }
+            if (t < 0)
+                break;
+            const PairTile p = decode<STAGE>(sm, a, t);
+            bool ok = mbar_wait_cluster(&sm.tfull[acc], aph, a.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+            const bool store = rank == 0 || p.second;
+            const int pos = (p.mb0 + (int)rank) * 128 + row;   // sorted row of this thread
+            if (STAGE == 1) {
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)pos * a.N + p.ncol0;
+                const float sx = (QT && store) ? a.x_scales[pos] : 1.0f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    float g[32], u[32], h[32];
+                    tmem_ld32(tacc + c0, g);
+                    tmem_ld32(tacc + 128 + c0, u);
+                    if (!store)
+                        continue;
+                    if (QT) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 sg = ld_scale4(a.w_scales + p.wrow0 + c0 + i);
+                            const float4 su = ld_scale4(a.w_scales + p.wrow1 + c0 + i);
+                            g[i] *= sx * sg.x, g[i + 1] *= sx * sg.y, g[i + 2] *= sx * sg.z, g[i + 3] *= sx * sg.w;
+                            u[i] *= sx * su.x, u[i + 1] *= sx * su.y, u[i + 2] *= sx * su.z, u[i + 3] *= sx * su.w;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        h[i] = silu(g[i]) * u[i];
+                    store_bf16x32(dst + c0, h);
+                }
+            } else {
+                const int slot = store ? a.sorted_ids[pos] : a.S;
+                const bool live = slot < a.S;
+                const float wgt = live ? a.sorted_weights[pos] * (QT ? a.x_scales[pos] : 1.0f) : 0.0f;
+                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + p.ncol0;
+                const int ncols = min(256, a.N - p.ncol0);
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    if (!live)
+                        continue;
+                    if (QT) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 sw = ld_scale4(a.w_scales + p.wrow0 + c0 + i);
+                            v[i] *= sw.x, v[i + 1] *= sw.y, v[i + 2] *= sw.z, v[i + 3] *= sw.w;
+                        }
+                    }
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
+                                            wgt * v[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(cluster_map(&sm.tempty[acc], 0));
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    // both CTAs stay until the pair's last MMA, copy and remote arrive are done
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+template <int STAGE, int QT>
+cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
+{
+    auto kern = gemm_pair_kernel<STAGE, QT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Clusters of two that can be resident at once (one CTA per SM), cached per device.
+template <int STAGE, int QT>
+int max_clusters()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    if (cache[dev] == 0) {
+        auto kern = gemm_pair_kernel<STAGE, QT>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+            return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace gemm2sm
+
+bool gemm_pair_supported(int E) { return E <= gemm2sm::kMaxE; }
+
+cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st)
+{
+    int ncl = 0;
+    if (stage == 1)
+        ncl = qt ? gemm2sm::max_clusters<1, 1>() : gemm2sm::max_clusters<1, 0>();
+    else
+        ncl = qt ? gemm2sm::max_clusters<2, 1>() : gemm2sm::max_clusters<2, 0>();
+    if (ncl <= 0)
+        return cudaErrorInvalidConfiguration;
+    if (max_pair_tiles < ncl)
+        ncl = (int)(max_pair_tiles > 0 ? max_pair_tiles : 1);
+    if (stage == 1)
+        return qt ? gemm2sm::launch<1, 1>(a, ncl, st) : gemm2sm::launch<1, 0>(a, ncl, st);
+    return qt ? gemm2sm::launch<2, 1>(a, ncl, st) : gemm2sm::launch<2, 0>(a, ncl, st);
+}
+
+}  // namespace moe

@@ -43,6 +43,7 @@
 //     every weight byte of an active expert is streamed exactly once.
 //     Stage 2 may split K (= I) across CTAs; the partial sums then go to a
 //     workspace and a separate pass reduces them in a fixed order.
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -50,8 +51,6 @@ namespace moe {
 
 namespace bf16gemm {
 
-template <int QT>
-constexpr int kBK = QT ? 128 : 64;          // K elements per stage (128 bytes)
 constexpr int kStages = 4;
 constexpr int kWRows = 256;
 constexpr int kXRows = 128;
@@ -89,8 +88,6 @@ struct Tile {
     int kb0, kb1;   // K-block range
     int ks;         // K split index (swap stage 2)
 };
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
 template <int MODE, int STAGE>
 __device__ __forceinline__ int num_tiles(const GemmArgs &a)
@@ -161,34 +158,6 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t)
     }
     return tl;
 }
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&h)[32])
-{
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 p = __floats2bfloat162_rn(h[q * 8 + 2 * i], h[q * 8 + 2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t *>(&p);
-        }
-        d[q] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
-template <int QT>
-__device__ __forceinline__ void mma_kind(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
-{
-    if (QT)
-        mma_fp8(d, ad, bd, idesc, accum);
-    else
-        mma_bf16(d, ad, bd, idesc, accum);
-}
-
-// Per-channel and per-token scales of QT = 1 for 4 consecutive columns
-// (16-byte aligned: channel and token bases are multiples of 16).
-__device__ __forceinline__ float4 ld_scale4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
 
 template <int MODE, int STAGE, int QT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a)

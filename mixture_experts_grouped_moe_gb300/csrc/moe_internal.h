@@ -160,6 +160,10 @@ cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cud
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+// Grouped-mode GEMM on CTA pairs (two-SM tensor core), bf16 (qt = 0) or
+// per-token FP8 (qt = 1); max_pair_tiles bounds the useful cluster count.
+bool gemm_pair_supported(int E);
+cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st);
 cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 
 }  // namespace moe

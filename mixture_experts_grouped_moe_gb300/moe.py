@@ -33,6 +33,7 @@ EXPORTED = [
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
     "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
+    "moe_set_gemm_pair",
 ]
 
 
@@ -96,6 +97,7 @@ def load(build_if_missing: bool = False):
             "moe_host_staging_bytes": (SZ, [I, I]),
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_set_stage_events": (I, [P, I]),
+            "moe_set_gemm_pair": (I, [I]),
             "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -234,6 +236,11 @@ def moe_fused_forward_host(dtype, x_host, W_router, router_bias, W_gate_up, w1_s
     return _check("moe_fused_forward_host", load().moe_fused_forward_host(
         dtype, _p(x_host), _p(W_router), _p(router_bias), _p(W_gate_up), _p(w1_scale), _p(W_down), _p(w2_scale),
         T, H, I, E, k, block_m, split_k, _p(out_host), _p(ws), ws_bytes, _stream(stream)))
+
+
+def moe_set_gemm_pair(mode: int):
+    """Grouped-mode GEMM kernel choice: 1 CTA pairs, 0 one-SM, -1 automatic (process-wide)."""
+    return _check("moe_set_gemm_pair", load().moe_set_gemm_pair(mode))
 
 
 def moe_set_stage_events(events):

@@ -1,0 +1,115 @@
+"""Grouped-mode GEMMs on CTA pairs (two-SM tensor core) vs the one-SM kernels.
+
+Each case runs the fused layer with the kernel choice forced both ways
+(moe_set_gemm_pair 1 and 0): both must meet the tolerance against the
+oracle, and the routing / sort outputs stay bit-exact.  The cases cover odd
+block counts per expert (half-used pairs), experts without tokens, a ragged
+last N tile of stage 2 and the Mixtral prefill shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_grouped_moe_gb300 import synth
+from moe_checks import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_grouped_moe_gb300 import build
+    build.build()
+    from mixture_experts_grouped_moe_gb300 import moe as m
+    m.load()
+    yield m
+    m.moe_set_gemm_pair(-1)
+
+
+def _host(inp):
+    return {k: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+            for k, v in inp.items()}
+
+
+def _run(moe, cfg, inp, w, dtype):
+    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    assert layer.plan.mode == moe.MOE_MODE_GROUPED
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    layer(inp["x"], w, out)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    return out.float().cpu().numpy(), layer
+
+
+CASES = [
+    # (name, T, H, I, E, k, bias)
+    ("t129_e4", 129, 256, 256, 4, 2, None),
+    ("t300_ragged", 300, 384, 640, 6, 3, "normal"),
+    ("h_odd", 200, 640, 384, 8, 2, "normal"),
+    ("many_experts", 700, 256, 256, 40, 4, "normal"),   # some experts empty, many with one block
+    ("e1k1", 520, 256, 384, 1, 1, None),                # one expert, odd block count
+]
+
+
+@pytest.mark.parametrize("mode", [1, 0], ids=["pair", "one_sm"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
+def test_bf16_grouped_both_kernels(moe, case, mode):
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5)
+    inp = synth.make_inputs(cfg, seed=11, device="cuda")
+    host = _host(inp)
+    moe.moe_set_gemm_pair(mode)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
+    got, layer = _run(moe, cfg, inp, w, moe.MOE_BF16)
+    r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], k)
+    assert np.array_equal(layer.view("topk_ids", torch.int32, (T, k)).cpu().numpy(), r_ids)
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
+    assert rel_l2(got, ref) <= 5e-3
+
+
+@pytest.mark.parametrize("mode", [1, 0], ids=["pair", "one_sm"])
+@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: c[0])
+def test_fp8_token_grouped_both_kernels(moe, case, mode):
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="fp8_token")
+    inp = synth.make_inputs(cfg, seed=12, device="cuda")
+    host = _host(inp)
+    moe.moe_set_gemm_pair(mode)
+    q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    s1 = torch.empty(E * 2 * I, dtype=torch.float32, device="cuda")
+    q2 = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(E * H, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(inp["W_gate_up"], E * 2 * I, H, q1, s1)
+    moe.moe_quantize_fp8_rows(inp["W_down"], E * H, I, q2, s2)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": q1, "w1_scale": s1, "W_down": q2,
+         "w2_scale": s2}
+    got, _ = _run(moe, cfg, inp, w, moe.MOE_FP8_TOKEN)
+    o1, os1 = oracle.quant_rows(host["W_gate_up"])
+    o2, os2 = oracle.quant_rows(host["W_down"])
+    ref = oracle.moe_forward_fp8_token(host["x"], host["W_router"], host["bias"], o1, os1, o2, os2, k)
+    assert rel_l2(got, ref) <= 3e-2
+
+
+def test_prefill_pair_matches_one_sm(moe):
+    """Mixtral prefill shapes: the two kernels agree closely on a token sample."""
+    cfg = synth.CONFIGS["mixtral_prefill"]
+    inp = synth.make_inputs(cfg, seed=0, device="cuda")
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
+    outs = []
+    for mode in (1, 0):
+        moe.moe_set_gemm_pair(mode)
+        got, _ = _run(moe, cfg, inp, w, moe.MOE_BF16)
+        outs.append(got)
+    moe.moe_set_gemm_pair(-1)
+    toks = synth.token_sample(cfg.T, 64).numpy()
+    host = _host(inp)
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
+                                  cfg.k, toks)
+    assert rel_l2(outs[0][toks], ref) <= 5e-3
+    assert rel_l2(outs[0], outs[1]) <= 5e-3
+
+
+def test_set_gemm_pair_rejects_bad_mode(moe):
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_gemm_pair(2)
