@@ -57,6 +57,13 @@ def _load():
         lib.oracle_quant_1x128.argtypes = [P, i, i, P, P]
         lib.oracle_quant_128x128.argtypes = [P, ctypes.c_long, i, P, P]
         lib.oracle_quant_rows.argtypes = [P, ctypes.c_long, i, P, P]
+        lib.oracle_e2m1_decode.restype = ctypes.c_double
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        lib.oracle_mx_exponent.restype = ctypes.c_int
+        lib.oracle_mx_exponent.argtypes = [ctypes.c_float]
+        lib.oracle_quant_mx4.argtypes = [P, ctypes.c_long, i, P, P]
         lib.oracle_router_logit.restype = ctypes.c_float
         lib.oracle_router_logit.argtypes = [P, P, i, P, i]
         lib.oracle_route.argtypes = [P, P, P, i, i, i, i, P, P, P, i]
@@ -64,6 +71,7 @@ def _load():
         lib.oracle_moe_forward_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8_token.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
+        lib.oracle_moe_forward_mxfp4.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         _lib = lib
         return lib
 
@@ -137,6 +145,38 @@ def quant_rows(X_bits) -> tuple[np.ndarray, np.ndarray]:
     q = np.empty(X.shape, np.uint8)
     s = np.empty(R, np.float32)
     _load().oracle_quant_rows(_ptr(X), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+# ----------------------------------------------------------------- MXFP4
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of each E2M1 code (0..15: sign << 3 | magnitude index), fp64."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_e2m1_decode(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def e2m1_encode(values) -> np.ndarray:
+    """Nearest E2M1 code (ties to the even mantissa), clamped to +-6."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32)
+    return np.array([lib.oracle_e2m1_encode(float(x)) for x in v.ravel()], dtype=np.uint8).reshape(v.shape)
+
+
+def mx_exponent(amax: float) -> int:
+    """Shared (unbiased) exponent of an MX FP4 block: floor(log2 amax) - 2, 0 for amax 0."""
+    return int(_load().oracle_mx_exponent(float(amax)))
+
+
+def quant_mx4(X_bits) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4 ("per_1x32") quantisation of X viewed as [rows, C]: codes (one per byte), E8M0 scales [rows, C/32]."""
+    X = _u16(X_bits)
+    C = X.shape[-1]
+    R = X.size // C
+    q = np.empty(X.shape, np.uint8)
+    s = np.empty((R, C // 32), np.uint8)
+    _load().oracle_quant_mx4(_ptr(X), R, C, _ptr(q), _ptr(s))
     return q, s
 
 
@@ -243,4 +283,26 @@ def moe_forward_fp8_token(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, 
     _load().oracle_moe_forward_fp8_token(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(_f32(w1s)),
                                          _ptr(Wd_q), _ptr(_f32(w2s)), T, H, I, E, k, _ptr(tok), len(tok),
                                          _ptr(out), nthreads or default_threads())
+    return out
+
+
+def moe_forward_mxfp4(x_bits, Wr_bits, bias, Wgu_q, w1x, Wd_q, w2x, k: int, tokens=None,
+                      nthreads: int | None = None) -> np.ndarray:
+    """MXFP4 fused MoE layer for `tokens`: out [n, H] fp64.
+
+    Wgu_q [E,2I,H] / Wd_q [E,H,I] E2M1 codes (one per byte) with E8M0 scales w1x [E*2I, H/32], w2x [E*H, I/32]."""
+    x = _u16(x_bits)
+    Wr = _u16(Wr_bits)
+    Wgu_q = np.ascontiguousarray(Wgu_q, np.uint8)
+    Wd_q = np.ascontiguousarray(Wd_q, np.uint8)
+    w1x = np.ascontiguousarray(w1x, np.uint8)
+    w2x = np.ascontiguousarray(w2x, np.uint8)
+    T, H = x.shape
+    E, twoI, _ = Wgu_q.shape
+    I = twoI // 2
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    out = np.empty((len(tok), H), np.float64)
+    _load().oracle_moe_forward_mxfp4(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(w1x), _ptr(Wd_q),
+                                     _ptr(w2x), T, H, I, E, k, _ptr(tok), len(tok), _ptr(out),
+                                     nthreads or default_threads())
     return out

@@ -22,7 +22,9 @@
  * expert, each expert padded to whole blocks, buffer of T*k + E*B - k
  * entries) and the two FP8 quantisation types the page names: per-128
  * block scaling ("per_1x128") and one scale per row ("per_Token": a scale
- * per token of the activations, per output channel of the weights).
+ * per token of the activations, per output channel of the weights), plus
+ * the microscaling 4-bit format ("per_1x32", MXFP4: OCP Microscaling
+ * Formats -- E2M1 elements sharing one power-of-two E8M0 scale per 32).
  *
  * Precision: inputs are bf16 (or e4m3 codes with fp32 scales) taken exactly;
  * every dot product of the expert GEMMs accumulates in fp64.  The router
@@ -175,6 +177,80 @@ void oracle_quant_rows(const uint16_t *X, long R, int C, uint8_t *q, float *s)
         for (int c = 0; c < C; ++c)
             q[r * C + c] = oracle_e4m3_encode(bf16_to_float(X[r * C + c]) / sc);
     }
+}
+
+/* ------------------------------------------------------- MXFP4 (1x32) */
+/*
+ * OCP Microscaling (MX) FP4: each element is E2M1 (1 sign, 2 exponent bits
+ * with bias 1, 1 mantissa bit; no infinity or NaN): magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6.  Each block of 32 consecutive elements of a row shares
+ * one scale X = 2^e stored as E8M0 (the biased exponent e + 127).  The MX
+ * conversion rule: e = floor(log2(amax)) - 2, where 2 is the exponent of the
+ * largest E2M1 power of two (4); elements are V / X rounded to nearest
+ * (ties to even mantissa) and clamped to +-6.  An all-zero block takes
+ * e = 0.  The codes here are one per byte (sign << 3 | magnitude index).
+ */
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double oracle_e2m1_decode(uint8_t c)
+{
+    double v = kE2M1[c & 7];
+    return (c & 8) ? -v : v;
+}
+
+uint8_t oracle_e2m1_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs((double)v);
+    if (isnan(v) || a >= 6.0)
+        return sign | 7;
+    int best = 0;
+    for (int i = 1; i < 8; ++i) {
+        double d = fabs(a - kE2M1[i]), db = fabs(a - kE2M1[best]);
+        if (d < db || (d == db && (i & 1) == 0))  /* ties: the even mantissa (even index) */
+            best = i;
+    }
+    return sign | (uint8_t)best;
+}
+
+/* Shared exponent of a block with the given amax (unbiased). */
+int oracle_mx_exponent(float amax)
+{
+    if (!(amax > 0.0f))
+        return 0;
+    int e2;
+    frexp((double)amax, &e2); /* amax = m * 2^e2, m in [0.5, 1): floor(log2 amax) = e2 - 1 */
+    int e = (e2 - 1) - 2;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+/* Rows of X [R, C] (C % 32 == 0): codes q [R, C] (one per byte), E8M0 scales s [R, C/32]. */
+void oracle_quant_mx4(const uint16_t *X, long R, int C, uint8_t *q, uint8_t *s)
+{
+    int G = C / 32;
+    for (long r = 0; r < R; ++r) {
+        for (int g = 0; g < G; ++g) {
+            float amax = 0.0f;
+            for (int c = g * 32; c < g * 32 + 32; ++c) {
+                float v = fabsf(bf16_to_float(X[r * C + c]));
+                if (v > amax)
+                    amax = v;
+            }
+            int e = oracle_mx_exponent(amax);
+            s[r * G + g] = (uint8_t)(e + 127);
+            for (int c = g * 32; c < g * 32 + 32; ++c)
+                q[r * C + c] = oracle_e2m1_encode((float)ldexp((double)bf16_to_float(X[r * C + c]), -e));
+        }
+    }
+}
+
+static double mx4_value(const uint8_t *q, const uint8_t *s, long idx, int C)
+{
+    return ldexp(oracle_e2m1_decode(q[idx]), (int)s[(idx / C) * (C / 32) + (idx % C) / 32] - 127);
 }
 
 /* -------------------------------------------------------------- router */
@@ -336,12 +412,13 @@ int oracle_align_sort(const int32_t *ids, int T, int k, int E, int B, int32_t *s
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 typedef struct {
-    int mode; /* 0 bf16, 1 fp8 per 128x128 / 1x128 blocks, 2 fp8 per row */
+    int mode; /* 0 bf16, 1 fp8 per 128x128 / 1x128 blocks, 2 fp8 per row, 3 mxfp4 per 1x32 */
     const uint16_t *x, *Wr;
     const float *bias;
     const uint16_t *Wgu, *Wd;                /* bf16 weights */
     const uint8_t *Wgu_q, *Wd_q;             /* e4m3 codes */
     const float *w1s, *w2s;                  /* block scales (mode 1) or row scales (mode 2) */
+    const uint8_t *w1x, *w2x;                /* E8M0 scales per 1x32 (mode 3) */
     int T, H, I, E, k;
     const int64_t *tokens;
     int n0, n1;
@@ -360,6 +437,7 @@ static void *fwd_worker(void *arg)
     uint8_t *xq = (uint8_t *)malloc(H);
     float *xs = (float *)malloc(sizeof(float) * (H / 128 + 1));
     uint8_t *aq = (uint8_t *)malloc(I);
+    uint8_t *xsx = (uint8_t *)malloc(H / 32 + 1);
     for (int n = J->n0; n < J->n1; ++n) {
         long t = (long)J->tokens[n];
         const uint16_t *xrow = J->x + t * H;
@@ -373,10 +451,14 @@ static void *fwd_worker(void *arg)
             oracle_quant_1x128(xrow, 1, H, xq, xs);
             for (int h = 0; h < H; ++h)
                 xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[h / 128];
-        } else {
+        } else if (J->mode == 2) {
             oracle_quant_rows(xrow, 1, H, xq, xs);
             for (int h = 0; h < H; ++h)
                 xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[0];
+        } else {
+            oracle_quant_mx4(xrow, 1, H, xq, xsx);
+            for (int h = 0; h < H; ++h)
+                xt[h] = mx4_value(xq, xsx, h, H);
         }
         double *o = J->out + (size_t)n * H;
         for (int h = 0; h < H; ++h)
@@ -391,6 +473,11 @@ static void *fwd_worker(void *arg)
                     for (int h = 0; h < H; ++h) {
                         g += (double)bf16_to_float(J->Wgu[rg + h]) * xt[h];
                         u += (double)bf16_to_float(J->Wgu[ru + h]) * xt[h];
+                    }
+                } else if (J->mode == 3) {
+                    for (int h = 0; h < H; ++h) {
+                        g += mx4_value(J->Wgu_q, J->w1x, (long)rg + h, H) * xt[h];
+                        u += mx4_value(J->Wgu_q, J->w1x, (long)ru + h, H) * xt[h];
                     }
                 } else if (J->mode == 2) {
                     /* one scale per output channel (row of the [E*2I, H] matrix) */
@@ -427,6 +514,20 @@ static void *fwd_worker(void *arg)
                         a[i] = oracle_e4m3_decode(aq[i]) * (double)sc;
                     }
                 }
+            } else if (J->mode == 3) {
+                /* MXFP4 between the stages: each 1x32 group of the intermediate row */
+                for (int gi = 0; gi < I / 32; ++gi) {
+                    float amax = 0.0f;
+                    for (int i = gi * 32; i < gi * 32 + 32; ++i) {
+                        float v = fabsf((float)a[i]);
+                        if (v > amax)
+                            amax = v;
+                    }
+                    int ex = oracle_mx_exponent(amax);
+                    for (int i = gi * 32; i < gi * 32 + 32; ++i)
+                        a[i] = ldexp(oracle_e2m1_decode(oracle_e2m1_encode((float)ldexp((double)(float)a[i], -ex))),
+                                     ex);
+                }
             } else if (J->mode == 2) {
                 /* per-token: one scale for the token's whole intermediate row */
                 float amax = 0.0f;
@@ -445,6 +546,9 @@ static void *fwd_worker(void *arg)
                 if (J->mode == 0) {
                     for (int i = 0; i < I; ++i)
                         y += (double)bf16_to_float(J->Wd[rd + i]) * a[i];
+                } else if (J->mode == 3) {
+                    for (int i = 0; i < I; ++i)
+                        y += mx4_value(J->Wd_q, J->w2x, (long)rd + i, I) * a[i];
                 } else if (J->mode == 2) {
                     const double sd = J->w2s[(size_t)e * H + h];
                     for (int i = 0; i < I; ++i)
@@ -466,6 +570,7 @@ static void *fwd_worker(void *arg)
     free(xq);
     free(xs);
     free(aq);
+    free(xsx);
     return NULL;
 }
 
@@ -567,6 +672,38 @@ int oracle_moe_forward_fp8_token(const uint16_t *x, const uint16_t *Wr, const fl
     J.w1s = w1s;
     J.Wd_q = Wd_q;
     J.w2s = w2s;
+    J.T = T;
+    J.H = H;
+    J.I = I;
+    J.E = E;
+    J.k = k;
+    J.tokens = tokens;
+    J.out = out;
+    return run_forward(J, n_tokens, nthreads);
+}
+
+/*
+ * MXFP4 layer ("per_1x32", microscaling FP4): the router runs on the bf16
+ * activations; the expert GEMMs see x quantised per 1x32 group, weights as
+ * E2M1 codes (one per byte here) with an E8M0 scale per 1x32 group along K
+ * (w1x [E*2I, H/32], w2x [E*H, I/32]) and the SwiGLU output re-quantised
+ * per 1x32 group.  Products are of the dequantised values, accumulated in
+ * fp64.
+ */
+int oracle_moe_forward_mxfp4(const uint16_t *x, const uint16_t *Wr, const float *bias, const uint8_t *Wgu_q,
+                             const uint8_t *w1x, const uint8_t *Wd_q, const uint8_t *w2x, int T, int H, int I,
+                             int E, int k, const int64_t *tokens, int n_tokens, double *out, int nthreads)
+{
+    fwd_job J;
+    memset(&J, 0, sizeof J);
+    J.mode = 3;
+    J.x = x;
+    J.Wr = Wr;
+    J.bias = bias;
+    J.Wgu_q = Wgu_q;
+    J.w1x = w1x;
+    J.Wd_q = Wd_q;
+    J.w2x = w2x;
     J.T = T;
     J.H = H;
     J.I = I;

@@ -149,6 +149,92 @@ def test_quant_rows_is_1x128_on_single_group_rows():
     assert np.array_equal(q1, q2) and np.array_equal(s1, s2[:, 0])
 
 
+# ----------------------------------------------------------------- MXFP4
+
+def test_e2m1_codes_golden():
+    tab = oracle.e2m1_decode(np.arange(16))
+    assert list(tab[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(tab[8:]) == [-v for v in tab[:8]]
+    for v, code in _golden_rows("e2m1_codes.txt"):
+        assert int(oracle.e2m1_encode([v])[0]) == int(code), (v, code)
+    # every representable value encodes to itself
+    assert np.array_equal(oracle.e2m1_encode(tab.astype(np.float32)), np.arange(16, dtype=np.uint8))
+
+
+def test_mx_exponent_golden():
+    for amax, e in _golden_rows("mx_exponent.txt"):
+        assert oracle.mx_exponent(amax) == int(e), (amax, e)
+
+
+def _mx4_numpy(xf):
+    """Independent restatement of the MX FP4 rule on a float array [R, C]."""
+    R, C = xf.shape
+    g = xf.astype(np.float64).reshape(R, C // 32, 32)
+    amax = np.abs(g).max(-1)
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0).astype(np.int64)
+    y = g / np.exp2(e)[..., None]
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    a = np.minimum(np.abs(y), 6.0)
+    d = np.abs(a[..., None] - grid)
+    best = d.argmin(-1)
+    # ties: argmin keeps the lower index; move to the upper one when it is the even index
+    upper = np.minimum(best + 1, 7)
+    tie = (np.abs(a - grid[upper]) == d.min(-1)) & (upper != best) & (upper % 2 == 0)
+    idx = np.where(tie, upper, best)
+    code = (idx + np.where(np.signbit(y), 8, 0)).astype(np.uint8)
+    return code.reshape(R, C), (e + 127).astype(np.uint8)
+
+
+def test_quant_mx4_against_numpy_restatement():
+    g = torch.Generator().manual_seed(13)
+    X = (torch.randn(11, 256, generator=g) * torch.exp(torch.randn(11, 8, generator=g).repeat_interleave(32, 1) * 3))
+    X = X.to(torch.bfloat16)
+    X[3, 64:96] = 0  # an all-zero block
+    X[5, 0:32] = torch.tensor([4.0, 2.5, 1.25, 0.75, 0.25, 5.0, 3.5, 1.75] * 4)  # block scale 1: exact ties
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    q, s = oracle.quant_mx4(bits)
+    rq, rs = _mx4_numpy(X.float().numpy())
+    assert np.array_equal(s, rs)
+    assert np.array_equal(q, rq)
+    assert s[3, 2] == 127 and not q[3, 64:96].any()
+    # every non-zero block reaches 4 or 6 in magnitude (amax / X lies in [4, 8))
+    tab = oracle.e2m1_decode(np.arange(16))
+    for r in range(11):
+        for b in range(8):
+            if (r, b) != (3, 2):
+                assert np.abs(tab[q[r, b * 32:(b + 1) * 32]]).max() in (4.0, 6.0)
+
+
+def test_forward_mxfp4_against_dense_dequantised_reference():
+    cfg = synth.CONFIGS["tiny"].with_(T=6, H=256, I=384, E=3, k=2)
+    inp = synth.make_inputs(cfg, seed=14)
+    xb, wrb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    q1, s1 = oracle.quant_mx4(synth.bf16_bits(inp["W_gate_up"]))
+    q2, s2 = oracle.quant_mx4(synth.bf16_bits(inp["W_down"]))
+    assert s1.shape == (cfg.E * 2 * cfg.I, cfg.H // 32) and s2.shape == (cfg.E * cfg.H, cfg.I // 32)
+    got = oracle.moe_forward_mxfp4(xb, wrb, None, q1, s1, q2, s2, cfg.k)
+
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+    deq = lambda q, s: grid[q] * np.repeat(np.exp2(s.astype(np.float64) - 127), 32, -1).reshape(q.shape)
+    Wgu = deq(q1, s1.reshape(cfg.E, 2 * cfg.I, -1))
+    Wd = deq(q2, s2.reshape(cfg.E, cfg.H, -1))
+    xq, xs = _mx4_numpy(inp["x"].float().numpy())
+    x = deq(xq, xs)
+    ids, w, _ = oracle.route(xb, wrb, None, cfg.k)
+    ref = np.zeros((cfg.T, cfg.H))
+    I = cfg.I
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            e = ids[t, j]
+            g, u = Wgu[e, :I] @ x[t], Wgu[e, I:] @ x[t]
+            a = (g / (1 + np.exp(-g)) * u).astype(np.float32)[None]
+            aq, as_ = _mx4_numpy(a)
+            ref[t] += w[t, j] * (Wd[e] @ deq(aq, as_)[0])
+    assert _rel(got, ref) < 1e-12
+    sub = np.array([5, 1], np.int64)
+    assert np.array_equal(oracle.moe_forward_mxfp4(xb, wrb, None, q1, s1, q2, s2, cfg.k, tokens=sub), got[sub])
+
+
 # ---------------------------------------------------------------- router
 
 def test_router_order_hand_worked_cases():
