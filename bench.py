@@ -146,9 +146,11 @@ def algorithmic_counts(cfg, counts, dtype_bytes):
         scale_bytes = active * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
     elif cfg.dtype == "fp8_token":
         scale_bytes = active * (2 * I + H) * 4
-    bytes_ = active * 3 * H * I * dtype_bytes + scale_bytes + T * H * 2 + T * H * 2 + E * H * 2
-    s1_bytes = active * 2 * I * H * dtype_bytes
-    s2_bytes = active * H * I * dtype_bytes
+    elif cfg.dtype == "mxfp4":
+        scale_bytes = active * 3 * H * I // 32
+    bytes_ = int(active * 3 * H * I * dtype_bytes) + scale_bytes + T * H * 2 + T * H * 2 + E * H * 2
+    s1_bytes = int(active * 2 * I * H * dtype_bytes)
+    s2_bytes = int(active * H * I * dtype_bytes)
     return flops, bytes_, active, s1_bytes, s2_bytes
 
 
@@ -165,7 +167,8 @@ def run_cuda(args, cfg, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
     fp8 = cfg.dtype == "fp8"
-    dtype = {"fp8": moe.MOE_FP8_BLOCK128, "fp8_token": moe.MOE_FP8_TOKEN}.get(cfg.dtype, moe.MOE_BF16)
+    dtype = {"fp8": moe.MOE_FP8_BLOCK128, "fp8_token": moe.MOE_FP8_TOKEN, "mxfp4": moe.MOE_MXFP4}.get(
+        cfg.dtype, moe.MOE_BF16)
 
     inp = synth.make_inputs(cfg, seed=0, device=dev)
     w = {"W_router": inp["W_router"], "bias": inp["bias"]}
@@ -186,6 +189,15 @@ def run_cuda(args, cfg, rank, world, local_rank):
         s2 = torch.empty(E * H, dtype=torch.float32, device=dev)
         moe.moe_quantize_fp8_rows(inp["W_gate_up"], E * 2 * I, H, q1, s1)
         moe.moe_quantize_fp8_rows(inp["W_down"], E * H, I, q2, s2)
+        w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
+    elif cfg.dtype == "mxfp4":
+        E, I, H = cfg.E, cfg.I, cfg.H
+        q1 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
+        s1 = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
+        q2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
+        s2 = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
+        moe.moe_quantize_mxfp4(inp["W_gate_up"], E * 2 * I, H, q1, s1, tiled=True)
+        moe.moe_quantize_mxfp4(inp["W_down"], E * H, I, q2, s2, tiled=True)
         w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
     else:
         w.update(W_gate_up=inp["W_gate_up"], W_down=inp["W_down"])
@@ -284,6 +296,9 @@ def run_oracle(cfg, host, toks):
     if cfg.dtype == "fp8":
         return oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
                                       host["q2"], host["s2"], cfg.k, toks)
+    if cfg.dtype == "mxfp4":
+        return oracle.moe_forward_mxfp4(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
+                                        host["q2"], host["s2"], cfg.k, toks)
     if cfg.dtype == "fp8_token":
         return oracle.moe_forward_fp8_token(host["x"], host["W_router"], host["bias"], host["q1"], host["s1"],
                                             host["q2"], host["s2"], cfg.k, toks)
@@ -305,6 +320,9 @@ def host_inputs(cfg, device):
     elif cfg.dtype == "fp8_token":
         host["q1"], host["s1"] = oracle.quant_rows(host["W_gate_up"])
         host["q2"], host["s2"] = oracle.quant_rows(host["W_down"])
+    elif cfg.dtype == "mxfp4":
+        host["q1"], host["s1"] = oracle.quant_mx4(host["W_gate_up"])
+        host["q2"], host["s2"] = oracle.quant_mx4(host["W_down"])
     return host
 
 
@@ -319,7 +337,8 @@ def launches_per_step(cfg):
 
 def workload_desc(cfg):
     d = {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k} SwiGLU"
-                     + {"fp8": " block-scaled FP8 e4m3", "fp8_token": " per-token FP8 e4m3"}.get(cfg.dtype, " bf16")
+                     + {"fp8": " block-scaled FP8 e4m3", "fp8_token": " per-token FP8 e4m3",
+                        "mxfp4": " MXFP4 (E2M1, E8M0 per 1x32)"}.get(cfg.dtype, " bf16")
                      + ("" if cfg.bias is None else f" router bias {cfg.bias}({cfg.bias_param})"),
          "tokens_per_step": cfg.T, "seq_len": 1 if cfg.T <= 128 else cfg.T}
     return d
@@ -363,7 +382,7 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    eb = 1 if cfg.dtype in ("fp8", "fp8_token") else 2
+    eb = {"fp8": 1, "fp8_token": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
     flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], eb)
     peaks = r["peaks"]
     ms = r["ms"]
@@ -373,6 +392,8 @@ def main():
     peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     if eb == 1:
         peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)
+    elif eb == 0.5:
+        peak_t = peaks.get("fp4_tflops", 6.0 * peak_t)  # nominal dense FP4 / bf16 ratio on GB300 (13.5 / 2.25)
     t_roof = max(flops / (peak_t * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9))
     memory_bound = bytes_ / (peaks["hbm_gbs"] * 1e9) >= flops / (peak_t * 1e12)
     # dominant kernel: stage 1 (gate/up group GEMM)
@@ -381,10 +402,12 @@ def main():
     npp_rows = sum(-(-c // r["plan"].block_m) * r["plan"].block_m for c in r["counts"])
     if memory_bound:
         # weights, the sorted activations read, h written (bf16 except block FP8's e4m3 codes), scales
-        h_bytes = 1 if cfg.dtype == "fp8" else 2
-        s1_alg = s1_bytes + npp_rows * H * eb + npp_rows * I * h_bytes
+        h_bytes = {"fp8": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
+        s1_alg = int(s1_bytes + npp_rows * H * eb + npp_rows * I * h_bytes)
         if cfg.dtype == "fp8_token":
             s1_alg += active * 2 * I * 4 + npp_rows * 4
+        elif cfg.dtype == "mxfp4":
+            s1_alg += (active * 2 * I * H + npp_rows * H + npp_rows * I) // 32
         achieved = s1_alg / (s1_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": "stage1 gate/up group GEMM (swap-AB)",
@@ -401,7 +424,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(tokens_s, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": r["K"], "warmup": r["W"], "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3/fp32-acc" if eb == 1 else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": {1: "fp8-e4m3/fp32-acc", 0.5: "mxfp4-e2m1/fp32-acc"}.get(eb, "bf16"),
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights; random init, no checkpoint)",
         "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}",
                        l2="inputs larger than L2 (expert weights streamed every step)"),

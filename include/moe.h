@@ -58,6 +58,8 @@ extern "C" {
                                activations (fp32 scale per 1x128 group) */
 #define MOE_FP8_TOKEN 2     /* e4m3 weights (fp32 scale per output channel) and
                                activations (fp32 scale per token) */
+#define MOE_MXFP4 3         /* E2M1 weights and activations, E8M0 scale per 1x32
+                               group (decode sizes, T <= 64) */
 
 #define MOE_MODE_GROUPED 0  /* tokens on the MMA M side, 128-row blocks */
 #define MOE_MODE_SWAP 1     /* weights on the MMA M side, tokens on N (small T) */
@@ -223,6 +225,22 @@ int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float 
 int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream);
 
 /*
+ * MXFP4 quantisation ("per_1x32" on the AITER page; OCP microscaling FP4):
+ * each group of 32 consecutive elements of a row shares the power-of-two
+ * scale 2^e, e = floor(log2(group amax)) - 2 (0 for an all-zero group),
+ * stored as the E8M0 byte e + 127; elements are v * 2^-e rounded to the
+ * nearest E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives; ties to the
+ * even mantissa), clamped to +-6, as codes sign << 3 | magnitude index.
+ *   X (device) bf16 [R][C], C % 32 == 0 -> q (device) [R][C/2] bytes, two
+ *   codes per byte (element 2j in the low nibble of byte j);
+ *   s (device) E8M0 bytes: tiled = 0 row-major [R][C/32]; tiled = 1 (R and
+ *   C multiples of 128; the weight order moe_fused_forward reads)
+ *   [R/128][C/128][512], group g of row r of a 128 x 128 tile at byte
+ *   (r % 32) * 16 + (r % 128 / 32) * 4 + g % 4.
+ */
+int moe_quantize_mxfp4(const void *X, int64_t R, int C, uint8_t *q, uint8_t *s, int tiled, void *stream);
+
+/*
  * The whole layer: route, align-sort, stage 1 (gate/up group GEMM with the
  * SwiGLU epilogue), stage 2 (down group GEMM scaled by the top-k weights),
  * combine.  out (device) bf16 [T][H].
@@ -237,13 +255,20 @@ int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s,
  *     channel (as produced by moe_quantize_fp8_rows); x is quantised per
  *     token inside the call, the router runs on bf16 x, and the SwiGLU
  *     output (rounded to bf16) is re-quantised per token between stages.
+ *   dtype MOE_MXFP4: W_gate_up / W_down (device) E2M1 codes, two per byte
+ *     ([E][2I][H/2] and [E][H][I/2] bytes), with w1_scale / w2_scale
+ *     (device) the E8M0 scale bytes in the tiled weight order of
+ *     moe_quantize_mxfp4 (tiled = 1); x is quantised per 1x32 group inside
+ *     the call, the router runs on bf16 x, and the SwiGLU output is
+ *     re-quantised per 1x32 group between stages.  H and I multiples of
+ *     256, T <= 64 (MOE_ERR_UNSUPPORTED otherwise).
  *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H]; router_bias
  *   (device) fp32 [E] or NULL; block_m / split_k as in moe_plan;
  *   ws (device) of at least moe_fused_workspace_size bytes, 1024-byte aligned.
  * The result is deterministic: no atomics touch floating-point data.
  */
 int moe_fused_forward(int dtype, const void *x, const void *W_router, const float *router_bias,
-                      const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                      const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
                       int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
                       size_t ws_bytes, void *stream);
 
@@ -257,8 +282,8 @@ int moe_fused_forward(int dtype, const void *x, const void *W_router, const floa
  */
 size_t moe_host_staging_bytes(int T, int H);
 int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, const float *router_bias,
-                           const void *W_gate_up, const float *w1_scale, const void *W_down,
-                           const float *w2_scale, int T, int H, int I, int E, int k, int block_m,
+                           const void *W_gate_up, const void *w1_scale, const void *W_down,
+                           const void *w2_scale, int T, int H, int I, int E, int k, int block_m,
                            int split_k, void *out_host, void *ws, size_t ws_bytes, void *stream);
 
 /*

@@ -135,7 +135,7 @@ struct Layout {
 
 static int validate_shape(int dtype, int T, int H, int I, int E, int k)
 {
-    if (dtype != MOE_BF16 && dtype != MOE_FP8_BLOCK128 && dtype != MOE_FP8_TOKEN)
+    if (dtype != MOE_BF16 && dtype != MOE_FP8_BLOCK128 && dtype != MOE_FP8_TOKEN && dtype != MOE_MXFP4)
         return MOE_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0)
         return MOE_ERR_INVALID_ARG;
@@ -143,6 +143,8 @@ static int validate_shape(int dtype, int T, int H, int I, int E, int k)
         return MOE_ERR_UNSUPPORTED;
     if (H % 128 != 0 || I % 128 != 0)
         return MOE_ERR_UNSUPPORTED;
+    if (dtype == MOE_MXFP4 && (H % 256 != 0 || I % 256 != 0 || T > 64))
+        return MOE_ERR_UNSUPPORTED;  // 256 FP4 elements of K per pipeline stage; decode-size batches only
     if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)E * 2 * I > (int64_t)1 << 30 ||
         (int64_t)E * H > (int64_t)1 << 30 || H > (1 << 20) || I > (1 << 20))
         return MOE_ERR_UNSUPPORTED;
@@ -175,10 +177,21 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
     L.sorted_w = take(P * 4);
     L.sorted_eids = take(NB * 4);
     L.slot_pos = take(S * 4);
-    L.x_sorted = take(P * H * eb);
-    L.x_scales = (dtype == MOE_FP8_BLOCK128) ? take((H / 128) * P * 4) : (dtype == MOE_FP8_TOKEN) ? take(P * 4) : -1;
-    L.inter = take(P * I * eb);
-    L.inter_scales = (dtype == MOE_FP8_BLOCK128) ? take((I / 128) * P * 4) : (dtype == MOE_FP8_TOKEN) ? take(P * 4) : -1;
+    if (dtype == MOE_MXFP4) {
+        L.x_sorted = take(P * H / 2);      // two E2M1 codes per byte
+        L.x_scales = take(P * H / 32);     // E8M0 per 1x32 group
+        L.inter = take(P * I / 2);
+        L.inter_scales = take(P * I / 32);
+    } else {
+        L.x_sorted = take(P * H * eb);
+        L.x_scales = (dtype == MOE_FP8_BLOCK128) ? take((H / 128) * P * 4)
+                     : (dtype == MOE_FP8_TOKEN)  ? take(P * 4)
+                                                 : -1;
+        L.inter = take(P * I * eb);
+        L.inter_scales = (dtype == MOE_FP8_BLOCK128) ? take((I / 128) * P * 4)
+                         : (dtype == MOE_FP8_TOKEN)  ? take(P * 4)
+                                                     : -1;
+    }
     L.inter_h = (dtype == MOE_FP8_TOKEN) ? take(P * I * 2) : -1;
     if (p.split_k2 > 1) {
         L.y = -1;
@@ -214,11 +227,11 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
         block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
     if (p.mode == MOE_MODE_GROUPED && block_m != 128)
         return MOE_ERR_UNSUPPORTED;
-    if (p.mode == MOE_MODE_SWAP && (block_m % 16 != 0 || block_m > 128))
+    if (p.mode == MOE_MODE_SWAP && (block_m % 16 != 0 || block_m > (dtype == MOE_MXFP4 ? 64 : 128)))
         return MOE_ERR_UNSUPPORTED;
     p.block_m = block_m;
     p.split_k1 = 1;
-    const int kblocks2 = I / (dtype == MOE_BF16 ? 64 : 128);  // 128-byte K blocks of stage 2
+    const int kblocks2 = I / (dtype == MOE_BF16 ? 64 : dtype == MOE_MXFP4 ? 256 : 128);  // 128-byte K blocks
     if (p.mode == MOE_MODE_SWAP) {
         if (split_k == 0) {
             // Enough stage-2 tiles for ~4 per SM: the smallest divisor of I/64 that reaches it.
@@ -262,7 +275,7 @@ static void mark(int i, cudaStream_t st)
 }
 
 static int forward_impl(int dtype, const void *x, const void *W_router, const float *router_bias,
-                        const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                        const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
                         int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
                         size_t ws_bytes, cudaStream_t st)
 {
@@ -272,6 +285,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     if (!x || !W_router || !W_gate_up || !W_down || !out || !ws)
         return MOE_ERR_INVALID_ARG;
     if (dtype != MOE_BF16 && (!w1_scale || !w2_scale || !aligned(w1_scale, 16) || !aligned(w2_scale, 16)))
+        return MOE_ERR_INVALID_ARG;
+    if (dtype == MOE_BF16 && (w1_scale || w2_scale))
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W_router, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) ||
         !aligned(out, 16) || !aligned(ws, 256))
@@ -326,6 +341,10 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         ge = launch_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
                                static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
                                pdl_enabled(kPdlGather), st);
+    else if (dtype == MOE_MXFP4)
+        ge = launch_quant_mx4(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
+                              static_cast<uint8_t *>(at(L.x_sorted)), static_cast<uint8_t *>(at(L.x_scales)), false,
+                              pdl_enabled(kPdlGather), st);
     else
         ge = launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S,
                                       k, H, P, static_cast<uint8_t *>(at(L.x_sorted)),
@@ -349,7 +368,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g.P_max = P;
     g.status = status;
     g.tile_counter = nullptr;
-    const uint32_t box_inner = (uint32_t)(128 / eb);  // one 128-byte swizzle row
+    const uint32_t box_inner = (uint32_t)(128 / eb);  // one 128-byte swizzle row (elements; bytes for MXFP4)
+    const uint64_t kdiv = (dtype == MOE_MXFP4) ? 2 : 1;  // packed FP4: K/2 bytes per row
     const uint32_t box_x_rows = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
 
     // ---------------------------------------------------------- stage 1
@@ -357,8 +377,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // grouped tiles differ in cost (compute- vs memory-bound experts): claim them dynamically;
     // swap-mode tiles are uniform: deal them round-robin
     g1.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 1 : nullptr;
-    if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H, P, box_inner, box_x_rows) ||
-        !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H, (uint64_t)E * 2 * I, box_inner, 128))
+    if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H / kdiv, P, box_inner, box_x_rows) ||
+        !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H / kdiv, (uint64_t)E * 2 * I, box_inner, 128))
         return MOE_ERR_CUDA;
     g1.K = H;
     g1.N = I;
@@ -366,13 +386,15 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g1.split_k = 1;
     g1.inter = (dtype == MOE_FP8_TOKEN) ? at(L.inter_h) : at(L.inter);
     g1.x_scales = static_cast<float *>(at(L.x_scales));
-    g1.w_scales = w1_scale;
+    g1.w_scales = static_cast<const float *>(w1_scale);
     g1.inter_scales = static_cast<float *>(at(L.inter_scales));
     cudaError_t ce;
     if (p.mode == MOE_MODE_SWAP) {
         const int64_t ub = (int64_t)((S < E) ? S : E) * (I / 128);
         const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(1, g1, grid, st) : launch_gemm_swap_fp8_token(1, g1, grid, st);
+        ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(1, g1, grid, st)
+             : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(1, g1, grid, st)
+                                    : launch_gemm_swap_fp8_token(1, g1, grid, st);
     } else if (use_pair(dtype, 1, T, k, E)) {
         ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
     } else {
@@ -397,22 +419,24 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     }
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 2 : nullptr;
-    if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I, P, box_inner, box_x_rows) ||
-        !encode_tmap_2d(&g2.tm_w, W_down, eb, I, (uint64_t)E * H, box_inner, 128))
+    if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I / kdiv, P, box_inner, box_x_rows) ||
+        !encode_tmap_2d(&g2.tm_w, W_down, eb, I / kdiv, (uint64_t)E * H, box_inner, 128))
         return MOE_ERR_CUDA;
     g2.K = I;
     g2.N = H;
     g2.rows_per_expert = H;
     g2.split_k = p.split_k2;
     g2.x_scales = static_cast<float *>(at(L.inter_scales));
-    g2.w_scales = w2_scale;
+    g2.w_scales = static_cast<const float *>(w2_scale);
     g2.y = static_cast<float *>(at(L.y));
     g2.partials = static_cast<float *>(at(L.partials));
     const int nt2 = (H + 255) / 256;
     if (p.mode == MOE_MODE_SWAP) {
         const int64_t ub = (int64_t)((S < E) ? S : E) * nt2 * p.split_k2;
         const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16) ? launch_gemm_swap_bf16(2, g2, grid, st) : launch_gemm_swap_fp8_token(2, g2, grid, st);
+        ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(2, g2, grid, st)
+             : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(2, g2, grid, st)
+                                    : launch_gemm_swap_fp8_token(2, g2, grid, st);
     } else if (use_pair(dtype, 2, T, k, E)) {
         ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
     } else {
@@ -659,6 +683,16 @@ int moe_quantize_fp8_weights(const void *W, int64_t R, int C, uint8_t *q, float 
     return cuda_status(cudaGetLastError());
 }
 
+int moe_quantize_mxfp4(const void *X, int64_t R, int C, uint8_t *q, uint8_t *s, int tiled, void *stream)
+{
+    if (R < 0 || C <= 0 || C % 32 != 0 || !X || !q || !s || !aligned(X, 16) || !aligned(q, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (tiled && (R % 128 != 0 || C % 128 != 0))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_mx4(static_cast<const __nv_bfloat16 *>(X), nullptr, nullptr, R, 0, 1, C, q, s,
+                                        tiled != 0, false, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream)
 {
     if (R < 0 || C <= 0 || C % 16 != 0 || !X || !q || !s || !aligned(X, 16) || !aligned(q, 16))
@@ -668,7 +702,7 @@ int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s,
 }
 
 int moe_fused_forward(int dtype, const void *x, const void *W_router, const float *router_bias,
-                      const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale, int T,
+                      const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale, int T,
                       int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws, size_t ws_bytes,
                       void *stream)
 {
@@ -684,7 +718,7 @@ size_t moe_host_staging_bytes(int T, int H)
 }
 
 int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, const float *router_bias,
-                           const void *W_gate_up, const float *w1_scale, const void *W_down, const float *w2_scale,
+                           const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
                            int T, int H, int I, int E, int k, int block_m, int split_k, void *out_host, void *ws,
                            size_t ws_bytes, void *stream)
 {

@@ -160,6 +160,11 @@ cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cud
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+// MXFP4: swap-AB GEMMs with hardware block scaling, and the 1x32 quantiser
+// (row-major or tiled E8M0 scales; optional gather through sorted_ids).
+cudaError_t launch_gemm_swap_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
+                             int S, int k, int C, uint8_t *q, uint8_t *s, bool tiled, bool pdl, cudaStream_t st);
 // Grouped-mode GEMM on CTA pairs (two-SM tensor core), bf16 (qt = 0) or
 // per-token FP8 (qt = 1); max_pair_tiles bounds the useful cluster count.
 bool gemm_pair_supported(int E);

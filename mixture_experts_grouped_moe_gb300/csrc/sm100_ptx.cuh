@@ -196,6 +196,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// Non-tensor bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, size a multiple of 16), completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Orders this thread's ordinary shared-memory writes before later reads of
+// the async proxy (TMA, tcgen05.cp, tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------- clusters (CTA pairs)
 //
 // Two-SM tensor-core operations (tcgen05 .cta_group::2) run on a pair of
@@ -429,6 +446,61 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
            | (b_fmt << 10)      // B format
            | ((N >> 3) << 17)   // N / 8
            | ((M >> 4) << 24);  // M / 16
+}
+
+// ---------------------------------------------- block-scaled FP4 (MXFP4)
+//
+// kind::mxf4 multiplies E2M1 operands (two per byte, K-major, 128-byte
+// swizzle; one MMA covers K = 64 elements = 32 bytes) and applies one
+// UE8M0 scale per 32 elements of K to each row of A and of B
+// (scale_vec::2X: two scales per row per MMA).  The scales sit in TMEM in
+// the 128 x 4 blocked order: for a block of 128 rows and 4 consecutive
+// 32-element groups, row r's four scale bytes are 32-bit word r / 32 of TMEM
+// lane r % 32, replicated in all four lane quadrants (tcgen05.cp
+// .32x128b.warpx4 from 512 contiguous bytes, byte (r % 32) * 16 + (r / 32) * 4
+// + g).  The scale id in the instruction descriptor selects the byte pair
+// of the group pair an MMA uses (0: groups 0-1, 2: groups 2-3).
+
+// Instruction descriptor for kind::mxf4: E2M1 A and B (format 1), K-major,
+// UE8M0 scales, M x N, scale ids of A and B.
+__host__ __device__ constexpr uint32_t make_idesc_mx4(uint32_t M, uint32_t N, uint32_t a_sf_id, uint32_t b_sf_id)
+{
+    return (b_sf_id << 4)         // B scale factor id
+           | (1u << 7)            // A format: E2M1
+           | (1u << 10)           // B format: E2M1
+           | ((N >> 3) << 17)     // N / 8
+           | (1u << 23)           // scale factor type: UE8M0
+           | ((M >> 4) << 24)     // M / 16
+           | (a_sf_id << 29);     // A scale factor id
+}
+
+__device__ __forceinline__ void mma_mx4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of 32 rows x 16 bytes stored contiguously (no
+// swizzle: four 8 x 16-byte core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_rows16(const void *p)
+{
+    const uint64_t addr = smem_addr(p);
+    return ((addr & 0x3FFFFull) >> 4)       // start address
+           | ((uint64_t)(128 >> 4) << 32)   // stride between core matrices along the rows
+           | (1ull << 46);                  // descriptor version (sm_100 family); layout: no swizzle
+}
+
+// Copy 512 bytes of 128 x 4 blocked scale factors from shared memory to the 4
+// TMEM columns at taddr, replicated in the four lane quadrants.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // (acc0, acc1) = (v0, v1) * s + (acc0, acc1): the paired fp32 FMA of the

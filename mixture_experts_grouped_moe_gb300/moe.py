@@ -24,6 +24,7 @@ MOE_ERR_TIMEOUT = -5
 MOE_BF16 = 0
 MOE_FP8_BLOCK128 = 1
 MOE_FP8_TOKEN = 2
+MOE_MXFP4 = 3
 MOE_MODE_GROUPED = 0
 MOE_MODE_SWAP = 1
 
@@ -33,7 +34,7 @@ EXPORTED = [
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
     "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
-    "moe_set_gemm_pair",
+    "moe_set_gemm_pair", "moe_quantize_mxfp4",
 ]
 
 
@@ -98,6 +99,7 @@ def load(build_if_missing: bool = False):
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_set_stage_events": (I, [P, I]),
             "moe_set_gemm_pair": (I, [I]),
+            "moe_quantize_mxfp4": (I, [P, I64, I, P, P, I, P]),
             "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -218,6 +220,11 @@ def moe_quantize_fp8_weights(W, R, C, q, s, stream=None):
 
 def moe_quantize_fp8_rows(X, R, C, q, s, stream=None):
     return _check("moe_quantize_fp8_rows", load().moe_quantize_fp8_rows(_p(X), R, C, _p(q), _p(s), _stream(stream)))
+
+
+def moe_quantize_mxfp4(X, R, C, q, s, tiled=False, stream=None):
+    return _check("moe_quantize_mxfp4",
+                  load().moe_quantize_mxfp4(_p(X), R, C, _p(q), _p(s), 1 if tiled else 0, _stream(stream)))
 
 
 def moe_fused_forward(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,

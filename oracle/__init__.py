@@ -64,6 +64,7 @@ def _load():
         lib.oracle_mx_exponent.restype = ctypes.c_int
         lib.oracle_mx_exponent.argtypes = [ctypes.c_float]
         lib.oracle_quant_mx4.argtypes = [P, ctypes.c_long, i, P, P]
+        lib.oracle_quant_mx4_mt.argtypes = [P, ctypes.c_long, i, P, P, i]
         lib.oracle_router_logit.restype = ctypes.c_float
         lib.oracle_router_logit.argtypes = [P, P, i, P, i]
         lib.oracle_route.argtypes = [P, P, P, i, i, i, i, P, P, P, i]
@@ -176,7 +177,7 @@ def quant_mx4(X_bits) -> tuple[np.ndarray, np.ndarray]:
     R = X.size // C
     q = np.empty(X.shape, np.uint8)
     s = np.empty((R, C // 32), np.uint8)
-    _load().oracle_quant_mx4(_ptr(X), R, C, _ptr(q), _ptr(s))
+    _load().oracle_quant_mx4_mt(_ptr(X), R, C, _ptr(q), _ptr(s), default_threads())
     return q, s
 
 

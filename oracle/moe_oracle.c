@@ -228,24 +228,65 @@ int oracle_mx_exponent(float amax)
     return e;
 }
 
-/* Rows of X [R, C] (C % 32 == 0): codes q [R, C] (one per byte), E8M0 scales s [R, C/32]. */
-void oracle_quant_mx4(const uint16_t *X, long R, int C, uint8_t *q, uint8_t *s)
+typedef struct {
+    const uint16_t *X;
+    long r0, r1;
+    int C;
+    uint8_t *q, *s;
+} mx4_job;
+
+static void *mx4_worker(void *arg)
 {
-    int G = C / 32;
-    for (long r = 0; r < R; ++r) {
+    mx4_job *J = (mx4_job *)arg;
+    int C = J->C, G = C / 32;
+    for (long r = J->r0; r < J->r1; ++r) {
         for (int g = 0; g < G; ++g) {
             float amax = 0.0f;
             for (int c = g * 32; c < g * 32 + 32; ++c) {
-                float v = fabsf(bf16_to_float(X[r * C + c]));
+                float v = fabsf(bf16_to_float(J->X[r * C + c]));
                 if (v > amax)
                     amax = v;
             }
             int e = oracle_mx_exponent(amax);
-            s[r * G + g] = (uint8_t)(e + 127);
+            double inv = ldexp(1.0, -e); /* exact power of two */
+            J->s[r * G + g] = (uint8_t)(e + 127);
             for (int c = g * 32; c < g * 32 + 32; ++c)
-                q[r * C + c] = oracle_e2m1_encode((float)ldexp((double)bf16_to_float(X[r * C + c]), -e));
+                J->q[r * C + c] = oracle_e2m1_encode((float)((double)bf16_to_float(J->X[r * C + c]) * inv));
         }
     }
+    return NULL;
+}
+
+static int clamp_threads(int nthreads, int work);
+
+/*
+ * Rows of X [R, C] (C % 32 == 0): codes q [R, C] (one per byte), E8M0 scales
+ * s [R, C/32].  Rows are independent; they are split across nthreads.
+ */
+void oracle_quant_mx4_mt(const uint16_t *X, long R, int C, uint8_t *q, uint8_t *s, int nthreads)
+{
+    if (R <= 0)
+        return;
+    nthreads = clamp_threads(nthreads, R > 1 << 30 ? 1 << 30 : (int)R);
+    pthread_t th[256];
+    mx4_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].X = X;
+        jobs[i].C = C;
+        jobs[i].q = q;
+        jobs[i].s = s;
+        jobs[i].r0 = R * i / nthreads;
+        jobs[i].r1 = R * (i + 1) / nthreads;
+        pthread_create(&th[i], NULL, mx4_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(th[i], NULL);
+}
+
+void oracle_quant_mx4(const uint16_t *X, long R, int C, uint8_t *q, uint8_t *s)
+{
+    mx4_job J = {X, 0, R, C, q, s};
+    mx4_worker(&J);
 }
 
 static double mx4_value(const uint8_t *q, const uint8_t *s, long idx, int C)
