@@ -375,8 +375,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // ---------------------------------------------------------- stage 1
     GemmArgs g1 = g;
     // grouped tiles differ in cost (compute- vs memory-bound experts): claim them dynamically;
-    // swap-mode tiles are uniform: deal them round-robin
-    g1.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 1 : nullptr;
+    // bf16 / FP8 swap-mode tiles are uniform: deal them round-robin; the short MXFP4 decode
+    // tiles balance better claimed (same-box A/B: 0.1488 -> 0.1478 ms per Mixtral decode step)
+    g1.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 1 : nullptr;
     if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H / kdiv, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H / kdiv, (uint64_t)E * 2 * I, box_inner, 128))
         return MOE_ERR_CUDA;
@@ -418,7 +419,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             return MOE_ERR_CUDA;
     }
     GemmArgs g2 = g;
-    g2.tile_counter = (p.mode == MOE_MODE_GROUPED) ? status + 2 : nullptr;
+    g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I / kdiv, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g2.tm_w, W_down, eb, I / kdiv, (uint64_t)E * H, box_inner, 128))
         return MOE_ERR_CUDA;

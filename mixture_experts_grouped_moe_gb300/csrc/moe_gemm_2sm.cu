@@ -28,9 +28,8 @@
 //               they release the accumulator on the leader's barrier
 // The leader claims tiles from a global counter and publishes each index to
 // both CTAs through a small shared-memory queue.  Within an expert, groups of
-// up to 8 pairs walk the N tiles together so that one weight tile serves
-// 16 token blocks from L2 and an expert's weights are read from HBM about
-// once.  Every wait is bounded; a CTA that gives up raises the status word
+// up to 8 pairs walk the N tiles together so that one weight tile serves 16
+// token blocks from L2.  Every wait is bounded; a CTA that gives up raises the status word
 // and both CTAs still meet at the final cluster barrier.
 #include "gemm_common.cuh"
 #include "moe_internal.h"
@@ -48,6 +47,10 @@ constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kMaxE = 1024;
+// Pairs of one expert that walk the N tiles together (16 token blocks).  A
+// whole-expert group in stage 1 (up to 9 pairs at Mixtral prefill) measured
+// slower: 76 clusters then share a smaller set of L2 lines.
+template <int STAGE>
 constexpr int kGroupPairs = 8;
 
 struct __align__(1024) Smem {
@@ -102,11 +105,11 @@ __device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, in
     const int local = t - sm.tstart[lo];
     const int nb = (sm.off[lo + 1] - sm.off[lo]) >> 7;
     const int np = (nb + 1) >> 1;
-    const int gi = local / (kGroupPairs * nnt);
-    const int gsize = min(kGroupPairs, np - gi * kGroupPairs);
-    const int wi = local - gi * kGroupPairs * nnt;
+    const int gi = local / (kGroupPairs<STAGE> * nnt);
+    const int gsize = min(kGroupPairs<STAGE>, np - gi * kGroupPairs<STAGE>);
+    const int wi = local - gi * kGroupPairs<STAGE> * nnt;
     const int nt = wi / gsize;
-    const int pi = gi * kGroupPairs + wi % gsize;
+    const int pi = gi * kGroupPairs<STAGE> + wi % gsize;
     p.mb0 = (sm.off[lo] >> 7) + 2 * pi;
     p.second = (2 * pi + 1 < nb) ? 1 : 0;
     if (STAGE == 1) {

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
             int t = -1;
             bool qok = true;
             if (lane == 0)
-                qok = tq_push_next(sm.tq, qs, qph, nullptr, ntiles, claim, t, a.status, abort_flag);
+                qok = tq_push_next(sm.tq, qs, qph, a.tile_counter, ntiles, claim, t, a.status, abort_flag);
             qok = __shfl_sync(0xffffffffu, (int)qok, 0) != 0;
             t = __shfl_sync(0xffffffffu, t, 0);
             if (!qok) {
