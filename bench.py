@@ -163,6 +163,7 @@ def run_cuda(args, cfg, rank, world, local_rank):
 
     moe_build.build()
     moe.load()
+    moe.moe_set_one_stage(0 if args.two_launch else 1)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
@@ -326,13 +327,13 @@ def host_inputs(cfg, device):
     return host
 
 
-def launches_per_step(cfg):
+def launches_per_step(cfg, one_stage=False):
     """Kernels the library launches per forward: router (+ top-k pass for large T*E), sort
     (one launch up to 1024 slots, else three), gather, stage 1 (+ the per-token re-quantisation
-    of h), stage 2, combine."""
+    of h), stage 2 (or one launch for both stages), combine."""
     router = 2 if cfg.T * cfg.E > 4096 else 1
     sort = 1 if cfg.T * cfg.k <= 1024 else 3
-    return router + sort + 4 + (1 if cfg.dtype == "fp8_token" else 0)
+    return router + sort + 4 + (1 if cfg.dtype == "fp8_token" else 0) - (1 if one_stage else 0)
 
 
 def workload_desc(cfg):
@@ -352,6 +353,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--workload", default="mixtral_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="bf16 decode: stage 1 and stage 2 as two launches instead of the one-kernel path")
     ap.add_argument("--experts", type=int, default=0, help="profiling aid: override E (not a bench line)")
     ap.add_argument("--tokens", type=int, default=0, help="profiling aid: override T (not a bench line)")
     args = ap.parse_args()
@@ -363,6 +366,8 @@ def main():
         cfg = cfg.with_(name=cfg.name + f"_E{args.experts}", E=args.experts)
     if args.tokens:
         cfg = cfg.with_(name=cfg.name + f"_T{args.tokens}", T=args.tokens)
+    # the library runs bf16 decode-size batches (swap mode, T <= 128) in one kernel unless told otherwise
+    args.one_stage = cfg.dtype == "bf16" and cfg.T <= 128 and not args.two_launch
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -408,10 +413,14 @@ def main():
             s1_alg += active * 2 * I * 4 + npp_rows * 4
         elif cfg.dtype == "mxfp4":
             s1_alg += (active * 2 * I * H + npp_rows * H + npp_rows * I) // 32
+        kname = "stage1 gate/up group GEMM (swap-AB)"
+        if args.one_stage:
+            # one launch runs both stages: its bytes add stage 2's weights, h read back and the partials
+            s1_alg += s2_bytes + npp_rows * I * 2 + r["plan"].split_k2 * npp_rows * H * 4
+            kname = "one-kernel stage 1 + stage 2 (swap-AB)"
         achieved = s1_alg / (s1_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": "stage1 gate/up group GEMM (swap-AB)",
-                "alg_bytes_per_launch": s1_alg}
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": kname, "alg_bytes_per_launch": s1_alg}
     else:
         s1_flops = 2.0 * cfg.S * 2 * H * I
         achieved = s1_flops / (s1_ms * 1e-3) / 1e12
@@ -419,7 +428,7 @@ def main():
                 "frac": round(achieved / peak_t, 4), "kernel": "stage1 gate/up group GEMM",
                 "alg_flops_per_launch": s1_flops}
     roof["peak_source"] = r["peak_kind"]
-    roof["traffic"] = profiled_traffic(cfg.name, "stage1")
+    roof["traffic"] = profiled_traffic(cfg.name, "one_kernel" if args.one_stage else "stage1")
     roof["kernel_ms"] = round(s1_ms, 5)
     line = {
         "metric": METRIC, "value": round(tokens_s, 2), "unit": "tokens/s", "n_gpus": world,
@@ -427,6 +436,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": {1: "fp8-e4m3/fp32-acc", 0.5: "mxfp4-e2m1/fp32-acc"}.get(eb, "bf16"),
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights; random init, no checkpoint)",
         "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}",
+                       **({"one_stage": True} if args.one_stage else {}),
                        l2="inputs larger than L2 (expert weights streamed every step)"),
         "tflops": round(tflops, 2), "hbm_gbs": round(gbs, 1),
         "layer_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof / (ms * 1e-3), 4),
@@ -434,7 +444,7 @@ def main():
                            "active_experts": active},
         "stage_ms": {k: round(v, 5) for k, v in r["stage_ms"].items()},
         "roofline": roof,
-        "gpu_launches": launches_per_step(cfg) * r["K"],
+        "gpu_launches": launches_per_step(cfg, args.one_stage) * r["K"],
         "stage_ms_note": "per-kernel CUDA-event times from a second pass of the same steps with an event "
                          "between launches; value is timed without them",
         "clocks": r["clocks"],

@@ -339,6 +339,20 @@ int moe_set_stage_events(void *const *events, int n);
  */
 int moe_set_gemm_pair(int mode);
 
+/*
+ * One-kernel ("1-stage", AITER page section 3.2) decode path, process-wide:
+ * mode 1 runs stage 1 and stage 2 of MOE_BF16 swap-mode calls (T <= 128) in
+ * one persistent launch -- tiles of both stages claimed from one counter,
+ * stage-1 tiles first; the intermediate stays in L2; the down-projection
+ * weights of a stage-2 tile stream while the last stage-1 tiles finish --
+ * followed by the usual split reduce and combine; the default (1 unless
+ * MOE_ONE_STAGE=0 is in the environment).  0 keeps two launches.  Both give
+ * bit-identical results (same tiles and MMA order); with one launch the
+ * per-stage timing events record stage 2 as empty.
+ * Returns MOE_OK or MOE_ERR_INVALID_ARG.
+ */
+int moe_set_one_stage(int mode);
+
 #ifdef __cplusplus
 }
 #endif

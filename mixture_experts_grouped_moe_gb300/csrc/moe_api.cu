@@ -96,6 +96,22 @@ static int pair_mode()
 // stage 2 gains (Mixtral shapes, T=4096: stage 2 0.49 -> 0.42 ms, stage 1
 // 0.77 -> 0.83 ms), for bf16 both stages (T=8192: 2.45 -> 2.31 and
 // 1.38 -> 1.16 ms).
+// One-kernel decode (bf16 swap mode): 1 on (the default: same-box Mixtral
+// decode 0.4355 -> 0.4307 ms per step), 0 off; MOE_ONE_STAGE=0 in the
+// environment sets the start value, moe_set_one_stage overrides it.
+static std::atomic<int> g_one_stage{-2};
+
+static bool one_stage_enabled()
+{
+    int m = g_one_stage.load(std::memory_order_relaxed);
+    if (m == -2) {
+        const char *v = getenv("MOE_ONE_STAGE");
+        m = (v && v[0] == '0') ? 0 : 1;
+        g_one_stage.store(m, std::memory_order_relaxed);
+    }
+    return m == 1;
+}
+
 static bool use_pair(int dtype, int stage, int T, int k, int E)
 {
     if (dtype == MOE_FP8_BLOCK128 || !gemm_pair_supported(E))
@@ -389,35 +405,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g1.x_scales = static_cast<float *>(at(L.x_scales));
     g1.w_scales = static_cast<const float *>(w1_scale);
     g1.inter_scales = static_cast<float *>(at(L.inter_scales));
-    cudaError_t ce;
-    if (p.mode == MOE_MODE_SWAP) {
-        const int64_t ub = (int64_t)((S < E) ? S : E) * (I / 128);
-        const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(1, g1, grid, st)
-             : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(1, g1, grid, st)
-                                    : launch_gemm_swap_fp8_token(1, g1, grid, st);
-    } else if (use_pair(dtype, 1, T, k, E)) {
-        ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
-    } else {
-        const int64_t ub = p.max_blocks * (I / 128);
-        const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(1, g1, grid, st)
-             : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(1, g1, grid, st)
-                                        : launch_gemm_grouped_fp8(1, g1, grid, st);
-    }
-    if (ce != cudaSuccess)
-        return MOE_ERR_CUDA;
-    mark(4, st);
 
-    // ---------------------------------------------------------- stage 2
-    if (dtype == MOE_FP8_TOKEN) {
-        // h (bf16, sorted order) -> e4m3 codes with one scale per row (stage 2's input)
-        ce = launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr, so.num_post_padded, P, S,
-                               k, I, static_cast<uint8_t *>(at(L.inter)), static_cast<float *>(at(L.inter_scales)),
-                               pdl_enabled(kPdlGather), st);
-        if (ce != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I / kdiv, P, box_inner, box_x_rows) ||
@@ -432,24 +420,70 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g2.y = static_cast<float *>(at(L.y));
     g2.partials = static_cast<float *>(at(L.partials));
     const int nt2 = (H + 255) / 256;
-    if (p.mode == MOE_MODE_SWAP) {
-        const int64_t ub = (int64_t)((S < E) ? S : E) * nt2 * p.split_k2;
-        const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(2, g2, grid, st)
-             : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(2, g2, grid, st)
-                                    : launch_gemm_swap_fp8_token(2, g2, grid, st);
-    } else if (use_pair(dtype, 2, T, k, E)) {
-        ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
+    const int64_t e_act = (S < E) ? S : E;
+    cudaError_t ce;
+
+    if (p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled()) {
+        // both stages in one persistent launch (status[1]: tile claims, status[3]: h written)
+        FusedArgs F;
+        F.s1 = g1;
+        F.s2 = g2;
+        F.tile_counter = status + 1;
+        F.h_done = status + 3;
+        const int64_t ub = e_act * ((I / 128) + nt2 * p.split_k2);
+        ce = launch_fused_decode(F, (int)(ub < nsm ? ub : nsm), st);
+        if (ce != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(4, st);
+        mark(5, st);
     } else {
-        const int64_t ub = p.max_blocks * nt2;
-        const int grid = (int)(ub < nsm ? ub : nsm);
-        ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(2, g2, grid, st)
-             : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(2, g2, grid, st)
-                                        : launch_gemm_grouped_fp8(2, g2, grid, st);
+        if (p.mode == MOE_MODE_SWAP) {
+            const int64_t ub = e_act * (I / 128);
+            const int grid = (int)(ub < nsm ? ub : nsm);
+            ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(1, g1, grid, st)
+                 : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(1, g1, grid, st)
+                                        : launch_gemm_swap_fp8_token(1, g1, grid, st);
+        } else if (use_pair(dtype, 1, T, k, E)) {
+            ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
+        } else {
+            const int64_t ub = p.max_blocks * (I / 128);
+            const int grid = (int)(ub < nsm ? ub : nsm);
+            ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(1, g1, grid, st)
+                 : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(1, g1, grid, st)
+                                            : launch_gemm_grouped_fp8(1, g1, grid, st);
+        }
+        if (ce != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(4, st);
+
+        // ------------------------------------------------------ stage 2
+        if (dtype == MOE_FP8_TOKEN) {
+            // h (bf16, sorted order) -> e4m3 codes with one scale per row (stage 2's input)
+            ce = launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr, so.num_post_padded, P,
+                                   S, k, I, static_cast<uint8_t *>(at(L.inter)),
+                                   static_cast<float *>(at(L.inter_scales)), pdl_enabled(kPdlGather), st);
+            if (ce != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        if (p.mode == MOE_MODE_SWAP) {
+            const int64_t ub = e_act * nt2 * p.split_k2;
+            const int grid = (int)(ub < nsm ? ub : nsm);
+            ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(2, g2, grid, st)
+                 : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(2, g2, grid, st)
+                                        : launch_gemm_swap_fp8_token(2, g2, grid, st);
+        } else if (use_pair(dtype, 2, T, k, E)) {
+            ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
+        } else {
+            const int64_t ub = p.max_blocks * nt2;
+            const int grid = (int)(ub < nsm ? ub : nsm);
+            ce = (dtype == MOE_BF16)        ? launch_gemm_grouped_bf16(2, g2, grid, st)
+                 : (dtype == MOE_FP8_TOKEN) ? launch_gemm_grouped_fp8_token(2, g2, grid, st)
+                                            : launch_gemm_grouped_fp8(2, g2, grid, st);
+        }
+        if (ce != cudaSuccess)
+            return MOE_ERR_CUDA;
+        mark(5, st);
     }
-    if (ce != cudaSuccess)
-        return MOE_ERR_CUDA;
-    mark(5, st);
 
     // ----------------------------------------------------------- combine
     if (p.split_k2 > 1)
@@ -488,6 +522,14 @@ int moe_set_gemm_pair(int mode)
     if (mode < -1 || mode > 1)
         return MOE_ERR_INVALID_ARG;
     g_pair_mode.store(mode, std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+int moe_set_one_stage(int mode)
+{
+    if (mode < 0 || mode > 1)
+        return MOE_ERR_INVALID_ARG;
+    g_one_stage.store(mode, std::memory_order_relaxed);
     return MOE_OK;
 }
 

@@ -160,6 +160,15 @@ cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cud
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+// One-kernel decode (bf16, swap-AB): both stages in one persistent launch;
+// tile_counter claims tiles of both stages, h_done counts finished stage-1
+// epilogue warps (both zeroed by the router).
+struct FusedArgs {
+    GemmArgs s1, s2;
+    int *tile_counter;
+    int *h_done;
+};
+cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st);
 // MXFP4: swap-AB GEMMs with hardware block scaling, and the 1x32 quantiser
 // (row-major or tiled E8M0 scales; optional gather through sorted_ids).
 cudaError_t launch_gemm_swap_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st);

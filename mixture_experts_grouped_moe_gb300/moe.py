@@ -34,7 +34,7 @@ EXPORTED = [
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
     "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
-    "moe_set_gemm_pair", "moe_quantize_mxfp4",
+    "moe_set_gemm_pair", "moe_quantize_mxfp4", "moe_set_one_stage",
 ]
 
 
@@ -99,6 +99,7 @@ def load(build_if_missing: bool = False):
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_set_stage_events": (I, [P, I]),
             "moe_set_gemm_pair": (I, [I]),
+            "moe_set_one_stage": (I, [I]),
             "moe_quantize_mxfp4": (I, [P, I64, I, P, P, I, P]),
             "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
@@ -248,6 +249,11 @@ def moe_fused_forward_host(dtype, x_host, W_router, router_bias, W_gate_up, w1_s
 def moe_set_gemm_pair(mode: int):
     """Grouped-mode GEMM kernel choice: 1 CTA pairs, 0 one-SM, -1 automatic (process-wide)."""
     return _check("moe_set_gemm_pair", load().moe_set_gemm_pair(mode))
+
+
+def moe_set_one_stage(mode: int):
+    """One-kernel bf16 decode path: 1 on, 0 off (process-wide)."""
+    return _check("moe_set_one_stage", load().moe_set_one_stage(mode))
 
 
 def moe_set_stage_events(events):
