@@ -59,7 +59,7 @@ extern "C" {
 #define MOE_FP8_TOKEN 2     /* e4m3 weights (fp32 scale per output channel) and
                                activations (fp32 scale per token) */
 #define MOE_MXFP4 3         /* E2M1 weights and activations, E8M0 scale per 1x32
-                               group (decode sizes, T <= 64) */
+                               group */
 
 #define MOE_MODE_GROUPED 0  /* tokens on the MMA M side, 128-row blocks */
 #define MOE_MODE_SWAP 1     /* weights on the MMA M side, tokens on N (small T) */
@@ -112,8 +112,9 @@ typedef struct moe_plan {
  * Choose mode, block size and K splits for a layer shape.  block_m = 0 and
  * split_k = 0 mean automatic; otherwise they are used as given (block_m
  * must be 128 in grouped mode and a multiple of 16 up to 128 in swap mode;
- * split_k splits stage 2's K = I and must divide I/64, or I/128 for
- * MOE_FP8_TOKEN).  num_sms = 0 asks
+ * split_k splits stage 2's K = I and must divide I/64, I/128 for
+ * MOE_FP8_TOKEN or I/256 for MOE_MXFP4; MXFP4 swap mode (T <= 64) takes
+ * block_m up to 64).  num_sms = 0 asks
  * the current CUDA device; a positive value plans for that many SMs without
  * touching CUDA.  Returns MOE_OK or a negative status.  Host only.
  */
@@ -261,7 +262,7 @@ int moe_quantize_mxfp4(const void *X, int64_t R, int C, uint8_t *q, uint8_t *s, 
  *     moe_quantize_mxfp4 (tiled = 1); x is quantised per 1x32 group inside
  *     the call, the router runs on bf16 x, and the SwiGLU output is
  *     re-quantised per 1x32 group between stages.  H and I multiples of
- *     256, T <= 64 (MOE_ERR_UNSUPPORTED otherwise).
+ *     256 (MOE_ERR_UNSUPPORTED otherwise).
  *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H]; router_bias
  *   (device) fp32 [E] or NULL; block_m / split_k as in moe_plan;
  *   ws (device) of at least moe_fused_workspace_size bytes, 1024-byte aligned.

@@ -114,7 +114,7 @@ static bool one_stage_enabled()
 
 static bool use_pair(int dtype, int stage, int T, int k, int E)
 {
-    if (dtype == MOE_FP8_BLOCK128 || !gemm_pair_supported(E))
+    if (dtype == MOE_FP8_BLOCK128 || dtype == MOE_MXFP4 || !gemm_pair_supported(E))
         return false;
     const int m = pair_mode();
     if (m >= 0)
@@ -159,8 +159,8 @@ static int validate_shape(int dtype, int T, int H, int I, int E, int k)
         return MOE_ERR_UNSUPPORTED;
     if (H % 128 != 0 || I % 128 != 0)
         return MOE_ERR_UNSUPPORTED;
-    if (dtype == MOE_MXFP4 && (H % 256 != 0 || I % 256 != 0 || T > 64))
-        return MOE_ERR_UNSUPPORTED;  // 256 FP4 elements of K per pipeline stage; decode-size batches only
+    if (dtype == MOE_MXFP4 && (H % 256 != 0 || I % 256 != 0))
+        return MOE_ERR_UNSUPPORTED;  // 256 FP4 elements of K per pipeline stage
     if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)E * 2 * I > (int64_t)1 << 30 ||
         (int64_t)E * H > (int64_t)1 << 30 || H > (1 << 20) || I > (1 << 20))
         return MOE_ERR_UNSUPPORTED;
@@ -236,9 +236,10 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
     moe_plan_t p;
     memset(&p, 0, sizeof p);
     // Swap (weights on the MMA M side) while every expert segment fits one
-    // N <= 128 tile, i.e. T <= 128; block-scaled FP8 always runs the grouped
-    // kernel.
-    p.mode = (dtype != MOE_FP8_BLOCK128 && T <= 128) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
+    // N <= 128 tile, i.e. T <= 128 (MXFP4: N <= 64, T <= 64); block-scaled
+    // FP8 always runs the grouped kernel.
+    const int swap_max = (dtype == MOE_MXFP4) ? 64 : 128;
+    p.mode = (dtype != MOE_FP8_BLOCK128 && T <= swap_max) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
     if (block_m == 0)
         block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
     if (p.mode == MOE_MODE_GROUPED && block_m != 128)
@@ -394,8 +395,10 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // bf16 / FP8 swap-mode tiles are uniform: deal them round-robin; the short MXFP4 decode
     // tiles balance better claimed (same-box A/B: 0.1488 -> 0.1478 ms per Mixtral decode step)
     g1.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 1 : nullptr;
+    // grouped MXFP4 tiles take weights in 64-row halves (gate/up pairs of 64 rows)
+    const uint32_t box_w_rows = (dtype == MOE_MXFP4 && p.mode == MOE_MODE_GROUPED) ? 64 : 128;
     if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H / kdiv, P, box_inner, box_x_rows) ||
-        !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H / kdiv, (uint64_t)E * 2 * I, box_inner, 128))
+        !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H / kdiv, (uint64_t)E * 2 * I, box_inner, box_w_rows))
         return MOE_ERR_CUDA;
     g1.K = H;
     g1.N = I;
@@ -409,7 +412,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I / kdiv, P, box_inner, box_x_rows) ||
-        !encode_tmap_2d(&g2.tm_w, W_down, eb, I / kdiv, (uint64_t)E * H, box_inner, 128))
+        !encode_tmap_2d(&g2.tm_w, W_down, eb, I / kdiv, (uint64_t)E * H, box_inner, box_w_rows))
         return MOE_ERR_CUDA;
     g2.K = I;
     g2.N = H;
@@ -443,6 +446,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(1, g1, grid, st)
                  : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(1, g1, grid, st)
                                         : launch_gemm_swap_fp8_token(1, g1, grid, st);
+        } else if (dtype == MOE_MXFP4) {
+            const int64_t ub = p.max_blocks * (I / 64);
+            ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 1, T, k, E)) {
             ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
         } else {
@@ -471,6 +477,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             ce = (dtype == MOE_BF16)    ? launch_gemm_swap_bf16(2, g2, grid, st)
                  : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(2, g2, grid, st)
                                         : launch_gemm_swap_fp8_token(2, g2, grid, st);
+        } else if (dtype == MOE_MXFP4) {
+            const int64_t ub = p.max_blocks * (H / 128);
+            ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 2, T, k, E)) {
             ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
         } else {

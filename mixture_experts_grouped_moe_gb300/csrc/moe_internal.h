@@ -172,6 +172,7 @@ cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st);
 // MXFP4: swap-AB GEMMs with hardware block scaling, and the 1x32 quantiser
 // (row-major or tiled E8M0 scales; optional gather through sorted_ids).
 cudaError_t launch_gemm_swap_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_gemm_grouped_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
                              int S, int k, int C, uint8_t *q, uint8_t *s, bool tiled, bool pdl, cudaStream_t st);
 // Grouped-mode GEMM on CTA pairs (two-SM tensor core), bf16 (qt = 0) or

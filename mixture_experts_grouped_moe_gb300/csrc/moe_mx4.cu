@@ -21,7 +21,8 @@
 // features), the expert's padded token segment (16..64 rows, MMA N = 64) on N.  A
 // pipeline stage carries 256 elements (128 bytes) of K per row plus the
 // scales of both operands; the weight scales arrive by bulk copy in their
-// tiled order, the token scales are re-tiled by the producer warp.  The MMA
+// tiled order, the token scales are re-tiled by the producer warp with
+// asynchronous copies that complete on the stage barrier.  The MMA
 // thread copies each stage's scales into a TMEM ring (tcgen05.cp) ahead of
 // its MMAs (same thread, so they run in issue order).  Stage 1's epilogue
 // computes SwiGLU and re-quantises h per 1x32 group directly: the 32 h
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.full[i], 2);
+            mbar_init(&sm.full[i], 1 + 32);  // TMA bytes + the producer lanes' scale copies
             mbar_init(&sm.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -302,23 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
                     issued[s] = 1;
                     issued_ph[s] = ph;
                 }
-                // token scales: 8 bytes per row for this stage, re-tiled into two 128 x 4 blocks
+                // token scales: 8 bytes per row for this stage, re-tiled into two 128 x 4 blocks by
+                // asynchronous 4-byte copies that complete on the stage barrier
                 uint8_t *xsf = st + kWBytes + kXBytes + kWSf;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int j = lane + 32 * h;
                     if (j < tl.nx) {
-                        const uint2 v =
-                            *reinterpret_cast<const uint2 *>(xsf_g + (size_t)(tl.xrow + j) * kgroups + kb * 8);
+                        const uint8_t *src = xsf_g + (size_t)(tl.xrow + j) * kgroups + kb * 8;
                         const int off = (j & 31) * 16 + (j >> 5) * 4;
-                        *reinterpret_cast<uint32_t *>(xsf + off) = v.x;
-                        *reinterpret_cast<uint32_t *>(xsf + 512 + off) = v.y;
+                        cp_async_4(xsf + off, src);
+                        cp_async_4(xsf + 512 + off, src + 4);
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.full[s]);
+                cp_async_arrive(&sm.full[s]);
                 if (++s == kStages) {
                     s = 0;
                     ph ^= 1;
@@ -327,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
             if (!ok)
                 break;
         }
+        cp_async_wait_all();
         if (!ok && lane == 0) {
             for (int i = 0; i < kStages; ++i)
                 if (issued[i]) {
@@ -372,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
                     const uint8_t *sfw = st + kWBytes + kXBytes;
                     const uint8_t *sfx = sfw + kWSf;
                     const uint32_t sf = tmem_base + kSfBase + s * kSfCols;
+                    fence_proxy_async_smem();  // the scale copies (generic proxy) before tcgen05.cp reads them
 #pragma unroll
                     for (int i = 0; i < 4; ++i)  // weight scales: half i/2, K tile i%2
                         tmem_cp_sf(sf + 4 * i, smem_desc_rows16(sfw + 512 * i));
@@ -513,6 +513,380 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
         tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// ------------------------------------------------- grouped (T > 64)
+//
+// Tokens on the MMA M side (128 sorted rows of one expert), weights on N:
+// 128 rows per tile -- stage 1, 64 gate rows and the matching 64 up rows
+// (accumulator columns j and 64 + j pair up), stage 2, 128 output features.
+// N = 128 keeps two accumulators (2 x 128 columns) and the scale ring within
+// 512 TMEM columns.  The producer warp assembles both operands' 128 x 4
+// scale blocks per K tile: the tokens' from their row-major scales, the
+// weights' from the matching words of their tiled scales (a 64-row half of
+// a 128-row tile occupies words 0-1 or 2-3 of every lane).  Stage 1's
+// epilogue thread holds a whole token row of the tile, so it quantises its
+// 64 h values (two 1x32 groups) by itself.
+namespace grouped {
+
+constexpr int kStages = 6;
+constexpr int kHalf = 128 * kKBytes;                    // 16 KiB: 128 rows x 256 elements
+constexpr int kStageBytes = 2 * kHalf + 2 * 1024;      // [A tokens | B weights | A scales | B scales]
+constexpr int kAccCols = 128;
+constexpr int kSfCols = 16;                            // A: 2 K tiles x 4 columns, B: the same
+constexpr int kSfBase = 2 * kAccCols;
+constexpr int kGroupM = 16;
+static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KiB alignment");
+static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+
+struct __align__(1024) Smem {
+    uint8_t stage[kStages][kStageBytes];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    TileQueue tq;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct GTile {
+    int e, mb, wrow0, wrow1, ncol0;
+};
+
+template <int STAGE>
+__device__ __forceinline__ int nnt_of(const GemmArgs &a)
+{
+    return (STAGE == 1) ? a.N / 64 : (a.N + 127) / 128;
+}
+
+template <int STAGE>
+__device__ __forceinline__ GTile get_gtile(const GemmArgs &a, int t)
+{
+    const int nmb = *a.num_post_padded / 128;
+    const int nnt = nnt_of<STAGE>(a);
+    const int group = t / (kGroupM * nnt);
+    const int within = t - group * kGroupM * nnt;
+    const int gsize = min(kGroupM, nmb - group * kGroupM);
+    const int nt = within / gsize;
+    GTile g;
+    g.mb = group * kGroupM + within % gsize;
+    g.e = a.sorted_expert_ids[g.mb];
+    if (STAGE == 1) {
+        g.wrow0 = g.e * a.rows_per_expert + nt * 64;          // gate rows
+        g.wrow1 = g.e * a.rows_per_expert + a.N + nt * 64;    // matching up rows
+        g.ncol0 = nt * 64;
+    } else {
+        g.wrow0 = g.e * a.rows_per_expert + nt * 128;
+        g.wrow1 = g.wrow0 + 64;
+        g.ncol0 = nt * 128;
+    }
+    return g;
+}
+
+// Address of words w0, w0+1 of lane l of tiled scale tile (row block rb, K tile kt).
+__device__ __forceinline__ const uint8_t *sf_word_ptr(const uint8_t *sf, int64_t rb, int ktiles, int kt, int l,
+                                                      int w0)
+{
+    return sf + ((size_t)rb * ktiles + kt) * 512 + l * 16 + w0 * 4;
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __grid_constant__ GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &sm.abort;
+    const uint8_t *wsf_g = reinterpret_cast<const uint8_t *>(a.w_scales);
+    const uint8_t *xsf_g = reinterpret_cast<const uint8_t *>(a.x_scales);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1 + 32);  // TMA bytes + the producer lanes' scale copies
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], kEpiWarps);
+        }
+        mbar_init(&sm.drain, 1);
+        tq_init(sm.tq, 1 + kEpiWarps);
+        sm.abort = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&a.tm_x);
+        tma_prefetch_desc(&a.tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+    pdl_wait();
+    pdl_trigger();
+    const int ntiles = (*a.num_post_padded / 128) * nnt_of<STAGE>(a);
+    const int nkb = a.K / 256;
+    const int kgroups = a.K / 32;
+    const int ktiles = a.K / 128;
+
+    if (warp == 0) {
+        // ------------------------------------------ producer (whole warp)
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_x = l2_policy_evict_last();
+        int s = 0;
+        uint32_t ph = 0;
+        int issued[kStages];
+        uint32_t issued_ph[kStages];
+        for (int i = 0; i < kStages; ++i)
+            issued[i] = 0, issued_ph[i] = 0;
+        bool ok = true;
+        int qs = 0;
+        uint32_t qph = 0;
+        int claim = -2;
+        for (;;) {
+            int t = -1;
+            bool qok = true;
+            if (lane == 0)
+                qok = tq_push_next(sm.tq, qs, qph, a.tile_counter, ntiles, claim, t, a.status, abort_flag);
+            qok = __shfl_sync(0xffffffffu, (int)qok, 0) != 0;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (!qok) {
+                ok = false;
+                break;
+            }
+            if (t < 0)
+                break;
+            const GTile g = get_gtile<STAGE>(a, t);
+            const int xrow = g.mb * 128;
+            for (int kb = 0; kb < nkb; ++kb) {
+                bool w_ok = mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag);
+                w_ok = __all_sync(0xffffffffu, w_ok);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = sm.stage[s];
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sm.full[s], 2 * kHalf);
+                    tma_load_2d(st, &a.tm_x, kb * kKBytes, xrow, &sm.full[s], pol_x);
+                    tma_load_2d(st + kHalf, &a.tm_w, kb * kKBytes, g.wrow0, &sm.full[s], pol_w);
+                    tma_load_2d(st + kHalf + kHalf / 2, &a.tm_w, kb * kKBytes, g.wrow1, &sm.full[s], pol_w);
+                    issued[s] = 1;
+                    issued_ph[s] = ph;
+                }
+                uint8_t *asf = st + 2 * kHalf;
+                uint8_t *bsf = asf + 1024;
+                // A scales: token rows l + 32 w of the block, 8 bytes each (two K tiles of 4 groups);
+                // B scales: rows 0-63 from wrow0's tile, 64-127 from wrow1's (words of a 64-row half).
+                // Asynchronous copies that complete on the stage barrier.
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint8_t *src = xsf_g + (size_t)(xrow + lane + 32 * w) * kgroups + kb * 8;
+                    cp_async_4(asf + lane * 16 + w * 4, src);
+                    cp_async_4(asf + 512 + lane * 16 + w * 4, src + 4);
+                }
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int k_tile = 2 * kb + kt;
+                    cp_async_8(bsf + kt * 512 + lane * 16,
+                               sf_word_ptr(wsf_g, g.wrow0 >> 7, ktiles, k_tile, lane, (g.wrow0 & 127) >> 5));
+                    cp_async_8(bsf + kt * 512 + lane * 16 + 8,
+                               sf_word_ptr(wsf_g, g.wrow1 >> 7, ktiles, k_tile, lane, (g.wrow1 & 127) >> 5));
+                }
+                cp_async_arrive(&sm.full[s]);
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (!ok)
+                break;
+        }
+        cp_async_wait_all();
+        if (!ok && lane == 0) {
+            for (int i = 0; i < kStages; ++i)
+                if (issued[i]) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait(&sm.full[i], issued_ph[i]) && global_timer_ns() - t0 < 100000000ull) {
+                    }
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true, any = false;
+            int qs = 0;
+            uint32_t qph = 0;
+            for (;;) {
+                int t;
+                if (!tq_pop(sm.tq, qs, qph, t, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(&sm.tq.empty[qs]);
+                tq_advance(qs, qph);
+                if (t < 0)
+                    break;
+                if (!mbar_wait(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * kAccCols;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t *st = sm.stage[s];
+                    const uint32_t sf = tmem_base + kSfBase + s * kSfCols;
+                    fence_proxy_async_smem();  // the scale copies (generic proxy) before tcgen05.cp reads them
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)  // A K tiles 0,1 then B K tiles 0,1
+                        tmem_cp_sf(sf + 4 * i, smem_desc_rows16(st + 2 * kHalf + 512 * i));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t b = kk >> 1, id = (kk & 1) * 2;
+                        mma_mx4(d, smem_desc_sw128(st + kk * 32), smem_desc_sw128(st + kHalf + kk * 32),
+                                make_idesc_mx4(128, 128, id, id), sf + b * 4, sf + 8 + b * 4,
+                                (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    any = true;
+                    mma_commit(&sm.empty[s]);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit(&sm.tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok && any) {
+                mma_commit(&sm.drain);
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&sm.drain, 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;    // token row within the block (TMEM lane)
+        int acc = 0;
+        uint32_t aph = 0;
+        int qs = 0;
+        uint32_t qph = 0;
+        for (;;) {
+            int t = -1;
+            bool qok = tq_pop(sm.tq, qs, qph, t, a.status, abort_flag);
+            qok = __all_sync(0xffffffffu, qok);
+            if (!qok)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.tq.empty[qs]);
+            tq_advance(qs, qph);
+            if (t < 0)
+                break;
+            const GTile g = get_gtile<STAGE>(a, t);
+            bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+            const int pos = g.mb * 128 + row;
+            if (STAGE == 1) {
+                uint8_t *hq = static_cast<uint8_t *>(a.inter) + (size_t)pos * (a.N / 2) + g.ncol0 / 2;
+                uint8_t *hs = reinterpret_cast<uint8_t *>(a.inter_scales) + (size_t)pos * (a.N / 32) + g.ncol0 / 32;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float gv[32], uv[32], h[32];
+                    tmem_ld32(tacc + c0, gv);
+                    tmem_ld32(tacc + 64 + c0, uv);
+                    float m = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        h[i] = silu(gv[i]) * uv[i];
+                        m = fmaxf(m, fabsf(h[i]));
+                    }
+                    const int e = mx_exponent(m);
+                    const float inv = pow2_neg(e);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        w[b] = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[b] |= e2m1_code(h[8 * b + i] * inv) << (4 * i);
+                    }
+                    *reinterpret_cast<uint4 *>(hq + c0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+                    hs[c0 / 32] = (uint8_t)(e + 127);
+                }
+            } else {
+                const int slot = a.sorted_ids[pos];
+                const float wgt = a.sorted_weights[pos];
+                const bool live = slot < a.S;
+                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + g.ncol0;
+                const int ncols = min(128, a.N - g.ncol0);
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    if (!live)
+                        continue;
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
+                                            wgt * v[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int STAGE>
+cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
+{
+    auto kern = gemm_mx4_grouped_kernel<STAGE>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess)
+        return err;
+    return launch_kernel(pdl_enabled(STAGE == 1 ? kPdlStage1 : kPdlStage2, true), kern, dim3(grid),
+                         dim3(kThreads), kSmemBytes, st, a);
+}
+
+}  // namespace grouped
+
 template <int STAGE>
 cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
 {
@@ -542,6 +916,11 @@ cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, 
 cudaError_t launch_gemm_swap_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st)
 {
     return stage == 1 ? mx4::launch<1>(a, grid, st) : mx4::launch<2>(a, grid, st);
+}
+
+cudaError_t launch_gemm_grouped_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    return stage == 1 ? mx4::grouped::launch<1>(a, grid, st) : mx4::grouped::launch<2>(a, grid, st);
 }
 
 }  // namespace moe

@@ -206,6 +206,26 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// 4- / 8-byte asynchronous copies global -> shared (cp.async), and an arrival
+// on an mbarrier once all of this thread's earlier cp.async copies have
+// landed (.noinc: the barrier's expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_8(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Orders this thread's ordinary shared-memory writes before later reads of
 // the async proxy (TMA, tcgen05.cp, tcgen05.mma).
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -15,6 +15,7 @@ DeepSeek-style shapes; tensors are random, there are no trained weights):
   mixtral_fp8_token T=4096 H=4096 I=14336 E=8   k=2  (per-token FP8)
   mixtral_fp8_token_decode  T=32, same shapes (per-token FP8)
   mixtral_mxfp4_decode      T=32, same shapes (MXFP4, per 1x32)
+  mixtral_mxfp4             T=4096, same shapes (MXFP4)
   finegrained_zipf  T=4096 H=7168 I=2048  E=256 k=8  Zipf(s=1.2) router bias
 
 Distributions: x ~ N(0, 1); W_router, W_gate, W_up ~ N(0, 1/H);
@@ -66,6 +67,7 @@ CONFIGS = {
     "mixtral_fp8_token_decode": MoEConfig("mixtral_fp8_token_decode", T=32, H=4096, I=14336, E=8, k=2,
                                           dtype="fp8_token"),
     "mixtral_mxfp4_decode": MoEConfig("mixtral_mxfp4_decode", T=32, H=4096, I=14336, E=8, k=2, dtype="mxfp4"),
+    "mixtral_mxfp4": MoEConfig("mixtral_mxfp4", T=4096, H=4096, I=14336, E=8, k=2, dtype="mxfp4"),
     "finegrained_zipf": MoEConfig("finegrained_zipf", T=4096, H=7168, I=2048, E=256, k=8,
                                   bias="zipf", bias_param=1.2),
 }

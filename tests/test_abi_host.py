@@ -83,6 +83,8 @@ def test_plan_without_gpu(moe):
     assert p.mode == moe.MOE_MODE_SWAP and p.block_m == 16 and (14336 // 256) % p.split_k2 == 0
     with pytest.raises(moe.MoEError):
         moe.moe_plan(moe.MOE_MXFP4, 32, 4096, 14336, 8, 2, block_m=128, num_sms=152)  # segments above 64 rows
+    p = moe.moe_plan(moe.MOE_MXFP4, 65, 4096, 14336, 8, 2, num_sms=152)
+    assert p.mode == moe.MOE_MODE_GROUPED and p.block_m == 128 and p.split_k2 == 1
     p = moe.moe_plan(moe.MOE_FP8_TOKEN, 4096, 4096, 14336, 8, 2, num_sms=152)
     assert p.mode == moe.MOE_MODE_GROUPED and p.block_m == 128
     p = moe.moe_plan(moe.MOE_BF16, 128, 256, 256, 4, 2, block_m=32, split_k=2, num_sms=152)
@@ -99,7 +101,6 @@ def test_plan_without_gpu(moe):
     ((0, 16, 128, 256, 64, 33), -2),    # k > 32
     ((4, 16, 128, 256, 4, 2), -1),      # unknown dtype
     ((3, 16, 128, 256, 4, 2), -2),      # MXFP4: H not a multiple of 256
-    ((3, 65, 256, 256, 4, 2), -2),      # MXFP4: decode sizes only (T <= 64)
     ((0, -1, 128, 256, 4, 2), -1),      # negative T
 ])
 def test_plan_rejects_invalid(moe, args, status):

@@ -171,6 +171,52 @@ def test_fused_mxfp4_edge_cases(moe, case):
     assert err <= TOL_MX4, err
 
 
-def test_fused_mxfp4_rejects_large_batches(moe):
-    with pytest.raises(moe.MoEError):
-        moe.FusedMoE(moe.MOE_MXFP4, 65, 256, 256, 4, 2)
+GROUPED = [
+    # (name, T, H, I, E, k, bias): grouped mode (T > 64), 128-row blocks
+    ("t65", 65, 256, 256, 4, 2, None),
+    ("t300_ragged", 300, 512, 256, 6, 3, "normal"),
+    ("e1k1_t200", 200, 256, 512, 1, 1, None),
+    ("h_odd", 150, 768, 256, 5, 2, "normal"),
+    ("many_experts", 500, 256, 256, 40, 4, "normal"),
+]
+
+
+@pytest.mark.parametrize("case", GROUPED, ids=lambda c: c[0])
+def test_fused_mxfp4_grouped_edge_cases(moe, case):
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="mxfp4")
+    inp = synth.make_inputs(cfg, seed=6, device="cuda")
+    host = _host(inp)
+    w4 = quantize_weights_gpu(moe, inp, cfg)
+    out, layer = run_fused(moe, cfg, inp, w4)
+    assert layer.plan.mode == moe.MOE_MODE_GROUPED
+    _check_workspace(moe, layer, cfg, host)
+    q1, s1 = oracle.quant_mx4(host["W_gate_up"])
+    q2, s2 = oracle.quant_mx4(host["W_down"])
+    ref = oracle.moe_forward_mxfp4(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, k, np.arange(T))
+    err = rel_l2(out.float().cpu().numpy(), ref)
+    assert err <= TOL_MX4, err
+
+
+def test_fused_mxfp4_prefill_parity(moe):
+    cfg = synth.CONFIGS["mixtral_mxfp4"]
+    inp = synth.make_inputs(cfg, seed=0, device="cuda")
+    host = _host(inp)
+    w4 = quantize_weights_gpu(moe, inp, cfg)
+    out, layer = run_fused(moe, cfg, inp, w4)
+    assert layer.plan.mode == moe.MOE_MODE_GROUPED
+    _check_workspace(moe, layer, cfg, host)
+    q1, s1 = oracle.quant_mx4(host["W_gate_up"])
+    q2, s2 = oracle.quant_mx4(host["W_down"])
+    r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], cfg.k)
+    toks = set(synth.token_sample(cfg.T, 48).tolist())
+    counts = np.bincount(r_ids.ravel(), minlength=cfg.E)
+    smallest = np.argsort(counts, kind="stable")[:2]
+    toks.update([t for t in range(cfg.T) if set(r_ids[t].tolist()) & set(smallest.tolist())][:16])
+    toks = np.array(sorted(toks), np.int64)
+    ref = oracle.moe_forward_mxfp4(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks)
+    got = out.float().cpu().numpy()[toks]
+    assert np.isfinite(got).all()
+    err = rel_l2(got, ref)
+    print(f"mxfp4 prefill: relL2 {err:.3e} over {len(toks)} tokens")
+    assert err <= TOL_MX4
