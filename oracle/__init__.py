@@ -73,6 +73,7 @@ def _load():
         lib.oracle_moe_forward_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8_token.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_mxfp4.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
+        lib.oracle_moe_backward_bf16.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, P, P, P, P, i]
         _lib = lib
         return lib
 
@@ -307,3 +308,24 @@ def moe_forward_mxfp4(x_bits, Wr_bits, bias, Wgu_q, w1x, Wd_q, w2x, k: int, toke
                                      _ptr(w2x), T, H, I, E, k, _ptr(tok), len(tok), _ptr(out),
                                      nthreads or default_threads())
     return out
+
+
+def moe_backward_bf16(x_bits, Wr_bits, bias, Wgu_bits, Wd_bits, dout_bits, k: int, nthreads: int | None = None):
+    """Gradients of the bf16 layer for loss = sum(dout * out): dict of fp64 arrays
+    dx [T,H], dW_gate_up [E,2I,H], dW_down [E,H,I], dW_router [E,H], dbias [E]."""
+    x = _u16(x_bits)
+    Wr = _u16(Wr_bits)
+    Wgu = _u16(Wgu_bits)
+    Wd = _u16(Wd_bits)
+    dout = _u16(dout_bits)
+    T, H = x.shape
+    E, twoI, _ = Wgu.shape
+    I = twoI // 2
+    g = {"dx": np.empty((T, H)), "dW_gate_up": np.empty((E, 2 * I, H)), "dW_down": np.empty((E, H, I)),
+         "dW_router": np.empty((E, H)), "dbias": np.empty(E)}
+    rc = _load().oracle_moe_backward_bf16(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu), _ptr(Wd), _ptr(dout),
+                                          T, H, I, E, k, _ptr(g["dx"]), _ptr(g["dW_gate_up"]), _ptr(g["dW_down"]),
+                                          _ptr(g["dW_router"]), _ptr(g["dbias"]), nthreads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle backward scratch")
+    return g

@@ -754,3 +754,253 @@ int oracle_moe_forward_mxfp4(const uint16_t *x, const uint16_t *Wr, const float 
     J.out = out;
     return run_forward(J, n_tokens, nthreads);
 }
+
+/* ------------------------------------------------------------ backward */
+/*
+ * Gradients of the bf16 layer (the training direction of the group GEMMs:
+ * "dgrad" of both stages and "wgrad" of both weight stacks, plus the
+ * router), for loss = sum_t dout_t . out_t.  The top-k choice is a
+ * selection (no gradient); the weights of the chosen experts carry the
+ * gradient to their logits through the softmax over the k:
+ *
+ *   dy_j = w_j dout                      dh_j = W_down[e_j]^T dy_j
+ *   dg = dh * u * silu'(g)               du = dh * silu(g),
+ *        silu'(g) = s (1 + g (1 - s)),   s = 1 / (1 + exp(-g))
+ *   dx  = sum_j (W_gate[e_j]^T dg_j + W_up[e_j]^T du_j) + sum_j dl_j W_router[e_j]
+ *   dw_j = dout . y_j                    dl_j = w_j (dw_j - sum_m w_m dw_m)
+ *   dW_down[e] = sum over e's slots of dy h^T,  dW_gate[e] = sum dg x^T,
+ *   dW_up[e] = sum du x^T,  dW_router[e] = sum_t dl_{t,e} x_t,  dbias_e = sum_t dl_{t,e}
+ *
+ * All in fp64 (the logits and the routing as in the forward).  Phase 1 runs
+ * per token; phase 2 sums the weight gradients over tokens per expert row.
+ */
+typedef struct {
+    const uint16_t *x, *Wr, *Wgu, *Wd, *dout;
+    const float *bias;
+    int T, H, I, E, k;
+    int32_t *ids;    /* [T, k] */
+    double *w;       /* [T, k] */
+    double *dl;      /* [T, E] */
+    double *hbuf;    /* [T*k, I]: h */
+    double *dgbuf;   /* [T*k, I]: dg */
+    double *dubuf;   /* [T*k, I]: du */
+    double *dx;      /* [T, H] */
+    int t0, t1;
+} bwd_job;
+
+static void *bwd_token_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    int H = J->H, I = J->I, E = J->E, k = J->k;
+    float *l = (float *)malloc(sizeof(float) * E);
+    double *xt = (double *)malloc(sizeof(double) * H);
+    double *dout = (double *)malloc(sizeof(double) * H);
+    double *g = (double *)malloc(sizeof(double) * I);
+    double *u = (double *)malloc(sizeof(double) * I);
+    double *y = (double *)malloc(sizeof(double) * H);
+    double *dw = (double *)malloc(sizeof(double) * k);
+    for (int t = J->t0; t < J->t1; ++t) {
+        const uint16_t *xrow = J->x + (size_t)t * H;
+        for (int e = 0; e < E; ++e)
+            l[e] = oracle_router_logit(xrow, J->Wr + (size_t)e * H, H, J->bias, e);
+        int32_t *ids = J->ids + (size_t)t * k;
+        double *w = J->w + (size_t)t * k;
+        route_token(l, E, k, ids, w);
+        for (int h = 0; h < H; ++h) {
+            xt[h] = bf16_to_float(xrow[h]);
+            dout[h] = bf16_to_float(J->dout[(size_t)t * H + h]);
+        }
+        double *dx = J->dx + (size_t)t * H;
+        for (int h = 0; h < H; ++h)
+            dx[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[j];
+            double *hh = J->hbuf + ((size_t)t * k + j) * I;
+            double *dg = J->dgbuf + ((size_t)t * k + j) * I;
+            double *du = J->dubuf + ((size_t)t * k + j) * I;
+            for (int i = 0; i < I; ++i) {
+                const uint16_t *rg = J->Wgu + ((size_t)e * 2 * I + i) * H;
+                const uint16_t *ru = J->Wgu + ((size_t)e * 2 * I + I + i) * H;
+                double gs = 0.0, us = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    gs += (double)bf16_to_float(rg[h]) * xt[h];
+                    us += (double)bf16_to_float(ru[h]) * xt[h];
+                }
+                g[i] = gs;
+                u[i] = us;
+                hh[i] = silu(gs) * us;
+            }
+            /* y_j and dh_j = W_down^T (w_j dout) */
+            for (int i = 0; i < I; ++i)
+                dg[i] = 0.0; /* dh accumulates here first */
+            double dwj = 0.0;
+            for (int h = 0; h < H; ++h) {
+                const uint16_t *rd = J->Wd + ((size_t)e * H + h) * I;
+                double yh = 0.0;
+                for (int i = 0; i < I; ++i)
+                    yh += (double)bf16_to_float(rd[i]) * hh[i];
+                y[h] = yh;
+                dwj += dout[h] * yh;
+                double dyh = w[j] * dout[h];
+                for (int i = 0; i < I; ++i)
+                    dg[i] += (double)bf16_to_float(rd[i]) * dyh;
+            }
+            dw[j] = dwj;
+            for (int i = 0; i < I; ++i) {
+                double dh = dg[i];
+                double sg = 1.0 / (1.0 + exp(-g[i]));
+                dg[i] = dh * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
+                du[i] = dh * g[i] * sg;
+            }
+            for (int i = 0; i < I; ++i) {
+                const uint16_t *rg = J->Wgu + ((size_t)e * 2 * I + i) * H;
+                const uint16_t *ru = J->Wgu + ((size_t)e * 2 * I + I + i) * H;
+                for (int h = 0; h < H; ++h)
+                    dx[h] += dg[i] * (double)bf16_to_float(rg[h]) + du[i] * (double)bf16_to_float(ru[h]);
+            }
+        }
+        /* softmax over the k chosen logits */
+        double sw = 0.0;
+        for (int j = 0; j < k; ++j)
+            sw += w[j] * dw[j];
+        double *dl = J->dl + (size_t)t * E;
+        for (int e = 0; e < E; ++e)
+            dl[e] = 0.0;
+        for (int j = 0; j < k; ++j)
+            dl[ids[j]] = w[j] * (dw[j] - sw);
+        for (int j = 0; j < k; ++j) {
+            const uint16_t *rr = J->Wr + (size_t)ids[j] * H;
+            for (int h = 0; h < H; ++h)
+                dx[h] += dl[ids[j]] * (double)bf16_to_float(rr[h]);
+        }
+    }
+    free(l);
+    free(xt);
+    free(dout);
+    free(g);
+    free(u);
+    free(y);
+    free(dw);
+    return NULL;
+}
+
+typedef struct {
+    const bwd_job *P;
+    double *dWgu, *dWd, *dWr, *dbias;
+    int e0, e1; /* experts of this worker */
+} wgrad_job;
+
+static void *bwd_weight_worker(void *arg)
+{
+    wgrad_job *W = (wgrad_job *)arg;
+    const bwd_job *J = W->P;
+    int T = J->T, H = J->H, I = J->I, E = J->E, k = J->k;
+    for (int e = W->e0; e < W->e1; ++e) {
+        double *dWg = W->dWgu + (size_t)e * 2 * I * H;
+        double *dWu = dWg + (size_t)I * H;
+        double *dWd = W->dWd + (size_t)e * H * I;
+        double *dWr = W->dWr + (size_t)e * H;
+        memset(dWg, 0, sizeof(double) * 2 * I * H);
+        memset(dWd, 0, sizeof(double) * H * I);
+        memset(dWr, 0, sizeof(double) * H);
+        double db = 0.0;
+        for (int t = 0; t < T; ++t) {
+            const uint16_t *xrow = J->x + (size_t)t * H;
+            double dle = J->dl[(size_t)t * E + e];
+            db += dle;
+            for (int h = 0; h < H; ++h)
+                dWr[h] += dle * (double)bf16_to_float(xrow[h]);
+            for (int j = 0; j < k; ++j) {
+                if (J->ids[(size_t)t * k + j] != e)
+                    continue;
+                const double *hh = J->hbuf + ((size_t)t * k + j) * I;
+                const double *dg = J->dgbuf + ((size_t)t * k + j) * I;
+                const double *du = J->dubuf + ((size_t)t * k + j) * I;
+                double wj = J->w[(size_t)t * k + j];
+                for (int h = 0; h < H; ++h) {
+                    double dyh = wj * (double)bf16_to_float(J->dout[(size_t)t * H + h]);
+                    for (int i = 0; i < I; ++i)
+                        dWd[(size_t)h * I + i] += dyh * hh[i];
+                }
+                for (int i = 0; i < I; ++i)
+                    for (int h = 0; h < H; ++h) {
+                        double xv = (double)bf16_to_float(xrow[h]);
+                        dWg[(size_t)i * H + h] += dg[i] * xv;
+                        dWu[(size_t)i * H + h] += du[i] * xv;
+                    }
+            }
+        }
+        W->dbias[e] = db;
+    }
+    return NULL;
+}
+
+/*
+ * Backward of the bf16 layer.  x, W_router, W_gate_up, W_down as in the
+ * forward, dout [T, H] bf16 bits.  Outputs (fp64): dx [T, H],
+ * dW_gate_up [E, 2I, H], dW_down [E, H, I], dW_router [E, H], dbias [E]
+ * (always written; 0 where an expert takes no token).  Returns 0, or -1 if
+ * the per-slot scratch cannot be allocated.
+ */
+int oracle_moe_backward_bf16(const uint16_t *x, const uint16_t *Wr, const float *bias, const uint16_t *Wgu,
+                             const uint16_t *Wd, const uint16_t *dout, int T, int H, int I, int E, int k, double *dx,
+                             double *dWgu, double *dWd, double *dWr, double *dbias, int nthreads)
+{
+    bwd_job P;
+    memset(&P, 0, sizeof P);
+    P.x = x;
+    P.Wr = Wr;
+    P.bias = bias;
+    P.Wgu = Wgu;
+    P.Wd = Wd;
+    P.dout = dout;
+    P.T = T;
+    P.H = H;
+    P.I = I;
+    P.E = E;
+    P.k = k;
+    P.ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)T * k);
+    P.w = (double *)malloc(sizeof(double) * (size_t)T * k);
+    P.dl = (double *)malloc(sizeof(double) * (size_t)T * E);
+    P.hbuf = (double *)malloc(sizeof(double) * (size_t)T * k * I);
+    P.dgbuf = (double *)malloc(sizeof(double) * (size_t)T * k * I);
+    P.dubuf = (double *)malloc(sizeof(double) * (size_t)T * k * I);
+    P.dx = dx;
+    int rc = 0;
+    if (!P.ids || !P.w || !P.dl || !P.hbuf || !P.dgbuf || !P.dubuf) {
+        rc = -1;
+    } else if (T > 0) {
+        int nt = clamp_threads(nthreads, T);
+        pthread_t th[256];
+        bwd_job jobs[256];
+        for (int i = 0; i < nt; ++i) {
+            jobs[i] = P;
+            jobs[i].t0 = (int)((long)T * i / nt);
+            jobs[i].t1 = (int)((long)T * (i + 1) / nt);
+            pthread_create(&th[i], NULL, bwd_token_worker, &jobs[i]);
+        }
+        for (int i = 0; i < nt; ++i)
+            pthread_join(th[i], NULL);
+        int ne = clamp_threads(nthreads, E);
+        wgrad_job wj[256];
+        for (int i = 0; i < ne; ++i) {
+            wj[i].P = &P;
+            wj[i].dWgu = dWgu;
+            wj[i].dWd = dWd;
+            wj[i].dWr = dWr;
+            wj[i].dbias = dbias;
+            wj[i].e0 = (int)((long)E * i / ne);
+            wj[i].e1 = (int)((long)E * (i + 1) / ne);
+            pthread_create(&th[i], NULL, bwd_weight_worker, &wj[i]);
+        }
+        for (int i = 0; i < ne; ++i)
+            pthread_join(th[i], NULL);
+    }
+    free(P.ids);
+    free(P.w);
+    free(P.dl);
+    free(P.hbuf);
+    free(P.dgbuf);
+    free(P.dubuf);
+    return rc;
+}

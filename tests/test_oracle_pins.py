@@ -524,6 +524,58 @@ def test_forward_fp8_token_close_to_bf16_layer():
     assert 1e-3 < r < 0.15, r  # three e4m3 roundings (x, W, h), each about 3 % relative RMS
 
 
+def _autograd_reference(inp, ids, dout, k):
+    """Plain fp64 torch model of the layer with the routing choice fixed to `ids`."""
+    X = inp["x"].double().clone().requires_grad_()
+    Wr = inp["W_router"].double().clone().requires_grad_()
+    b = (inp["bias"].double() if inp["bias"] is not None else torch.zeros(Wr.shape[0], dtype=torch.float64))
+    b = b.clone().requires_grad_()
+    Wgu = inp["W_gate_up"].double().clone().requires_grad_()
+    Wd = inp["W_down"].double().clone().requires_grad_()
+    I = Wgu.shape[1] // 2
+    L = X @ Wr.T + b
+    ids_t = torch.from_numpy(ids.astype(np.int64))
+    w = torch.softmax(L.gather(1, ids_t), dim=1)
+    out = []
+    for t in range(X.shape[0]):
+        acc = torch.zeros(X.shape[1], dtype=torch.float64)
+        for j in range(k):
+            e = int(ids[t, j])
+            h = torch.nn.functional.silu(Wgu[e, :I] @ X[t]) * (Wgu[e, I:] @ X[t])
+            acc = acc + w[t, j] * (Wd[e] @ h)
+        out.append(acc)
+    out = torch.stack(out)
+    (out * dout.double()).sum().backward()
+    return {"dx": X.grad, "dW_gate_up": Wgu.grad, "dW_down": Wd.grad, "dW_router": Wr.grad, "dbias": b.grad}
+
+
+@pytest.mark.parametrize("shape", [(9, 96, 80, 4, 2, "normal"), (5, 64, 48, 7, 3, None), (6, 32, 32, 1, 1, None)],
+                         ids=["t9_e4_k2_bias", "t5_e7_k3", "e1_k1"])
+def test_backward_against_torch_autograd(shape):
+    T, H, I, E, k, bias = shape
+    cfg = synth.CONFIGS["tiny"].with_(T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5)
+    inp = synth.make_inputs(cfg, seed=15)
+    dout = (torch.randn(T, H, generator=torch.Generator().manual_seed(16))).to(torch.bfloat16)
+    xb, wrb = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"])
+    b = None if inp["bias"] is None else inp["bias"].numpy()
+    got = oracle.moe_backward_bf16(xb, wrb, b, synth.bf16_bits(inp["W_gate_up"]), synth.bf16_bits(inp["W_down"]),
+                                   synth.bf16_bits(dout), k)
+    ids, _, _ = oracle.route(xb, wrb, b, k)
+    ref = _autograd_reference(inp, ids, dout, k)
+    for name in ("dx", "dW_gate_up", "dW_down", "dW_router", "dbias"):
+        r = ref[name].numpy()
+        if not np.abs(r).max() > 1e-30:  # k = 1: the softmax over one logit passes no gradient
+            assert np.abs(got[name]).max() < 1e-30, name
+            continue
+        # the oracle's softmax weights come from the fp32 logits that decide the routing: ~1e-7 relative
+        assert _rel(got[name], r) < 1e-5, (name, _rel(got[name], r))
+    # experts without tokens get exactly zero weight gradients
+    used = set(ids.ravel().tolist())
+    for e in range(E):
+        if e not in used:
+            assert not got["dW_gate_up"][e].any() and not got["dW_down"][e].any()
+
+
 # ------------------------------------------------------------ heuristics
 
 def test_heuristics_golden():
