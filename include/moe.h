@@ -274,6 +274,38 @@ int moe_fused_forward(int dtype, const void *x, const void *W_router, const floa
                       size_t ws_bytes, void *stream);
 
 /*
+ * Training (bf16; the pages' stated future work for the group-GEMM MoE
+ * kernels: backward "dgrad" and "wgrad" passes).
+ *
+ * moe_train_workspace_size: bytes of the workspace shared by one training
+ * forward and its backward (0 on invalid input; I must be a multiple of 256).
+ *
+ * moe_fused_forward_train: moe_fused_forward for MOE_BF16 that always runs
+ * the grouped (128-row block) path and keeps in ws what the backward needs:
+ * the routing and sort, the sorted x rows, the pre-activations g | u, the
+ * SwiGLU output h and the weighted stage-2 rows.  Same arguments as
+ * moe_fused_forward without dtype, scales, block_m and split_k.
+ *
+ * moe_fused_backward: gradients for loss = sum(dout * out) of the forward
+ * that last ran on ws (same x, weights and shape):
+ *   dout (device) bf16 [T][H]  ->  dx (device) bf16 [T][H];
+ *   dW_gate_up (device) fp32 [E][2I][H], dW_down (device) fp32 [E][H][I],
+ *   dW_router (device) fp32 [E][H], dbias (device) fp32 [E] or NULL.
+ * The top-k choice is a selection: the gradient reaches the router through
+ * the softmax over the chosen k logits.  Experts without tokens get zero
+ * weight gradients.  Every sum runs in a fixed order (no atomics), so the
+ * gradients are bitwise reproducible.  Returns MOE_OK or a negative status.
+ */
+size_t moe_train_workspace_size(int T, int H, int I, int E, int k);
+int moe_fused_forward_train(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
+                            const void *W_down, int T, int H, int I, int E, int k, void *out, void *ws,
+                            size_t ws_bytes, void *stream);
+int moe_fused_backward(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
+                       const void *W_down, const void *dout, int T, int H, int I, int E, int k, void *dx,
+                       float *dW_gate_up, float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/*
  * moe_fused_forward with the activations in host memory: x_host (host) bf16
  * [T][H] is copied to the device inside the call and the result is copied
  * back to out_host (host) bf16 [T][H], all on `stream` (pinned host memory

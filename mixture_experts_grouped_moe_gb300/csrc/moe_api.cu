@@ -221,7 +221,7 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
 }
 
 static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k, int num_sms,
-                     moe_plan_t *plan)
+                     moe_plan_t *plan, bool grouped_only = false)
 {
     int st = validate_shape(dtype, T, H, I, E, k);
     if (st != MOE_OK)
@@ -239,7 +239,7 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
     // N <= 128 tile, i.e. T <= 128 (MXFP4: N <= 64, T <= 64); block-scaled
     // FP8 always runs the grouped kernel.
     const int swap_max = (dtype == MOE_MXFP4) ? 64 : 128;
-    p.mode = (dtype != MOE_FP8_BLOCK128 && T <= swap_max) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
+    p.mode = (dtype != MOE_FP8_BLOCK128 && T <= swap_max && !grouped_only) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
     if (block_m == 0)
         block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
     if (p.mode == MOE_MODE_GROUPED && block_m != 128)
@@ -291,10 +291,12 @@ static void mark(int i, cudaStream_t st)
         cudaEventRecord(t_stage_events[i], st);
 }
 
+// gu (training): when set, the grouped path is forced and stage 1 also keeps
+// the pre-activations g | u there for the backward.
 static int forward_impl(int dtype, const void *x, const void *W_router, const float *router_bias,
                         const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
                         int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
-                        size_t ws_bytes, cudaStream_t st)
+                        size_t ws_bytes, cudaStream_t st, __nv_bfloat16 *gu = nullptr)
 {
     int rc = validate_shape(dtype, T, H, I, E, k);
     if (rc != MOE_OK)
@@ -311,11 +313,12 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     if (T == 0)
         return MOE_OK;
     moe_plan_t p;
-    rc = plan_impl(dtype, T, H, I, E, k, block_m, split_k, 0, &p);
+    rc = plan_impl(dtype, T, H, I, E, k, block_m, split_k, 0, &p, gu != nullptr);
     if (rc != MOE_OK)
         return rc;
     if (ws_bytes < p.workspace_bytes)
         return MOE_ERR_WORKSPACE;
+    const bool train = gu != nullptr;
     const Layout L = make_layout(dtype, T, H, I, E, k, p);
     uint8_t *w = static_cast<uint8_t *>(ws);
     auto at = [&](int64_t off) -> void * { return off < 0 ? nullptr : (void *)(w + off); };
@@ -408,6 +411,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g1.x_scales = static_cast<float *>(at(L.x_scales));
     g1.w_scales = static_cast<const float *>(w1_scale);
     g1.inter_scales = static_cast<float *>(at(L.inter_scales));
+    g1.gu = gu;
 
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
@@ -426,7 +430,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     const int64_t e_act = (S < E) ? S : E;
     cudaError_t ce;
 
-    if (p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled()) {
+    if (p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled() && !train) {
         // both stages in one persistent launch (status[1]: tile claims, status[3]: h written)
         FusedArgs F;
         F.s1 = g1;
@@ -449,7 +453,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (I / 64);
             ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
-        } else if (use_pair(dtype, 1, T, k, E)) {
+        } else if (!train && use_pair(dtype, 1, T, k, E)) {
             ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
         } else {
             const int64_t ub = p.max_blocks * (I / 128);
@@ -480,7 +484,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
-        } else if (use_pair(dtype, 2, T, k, E)) {
+        } else if (!train && use_pair(dtype, 2, T, k, E)) {
             ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
         } else {
             const int64_t ub = p.max_blocks * nt2;
@@ -503,6 +507,187 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     mark(6, st);
     t_stage_armed = false;
     return cuda_status(ce);
+}
+
+// ------------------------------------------------------------ training
+//
+// Workspace of a training forward + backward: the forward's (grouped plan)
+// followed by the saved pre-activations and the backward's buffers.
+struct TrainLayout {
+    moe_plan_t plan;
+    Layout L;
+    int64_t gu, dys, dgu, dxs, dlogit, wdT, wguT, dysT, hT, dguT, xsT, total;
+    int64_t Pp;  // row length of the transposed activations (>= max_padded, multiple of 64)
+};
+
+static int train_layout(int T, int H, int I, int E, int k, TrainLayout &TL)
+{
+    int rc = validate_shape(MOE_BF16, T, H, I, E, k);
+    if (rc != MOE_OK)
+        return rc;
+    if (I % 256 != 0)
+        return MOE_ERR_UNSUPPORTED;  // the backward of stage 2 works in 256-column tiles of I
+    rc = plan_impl(MOE_BF16, T, H, I, E, k, 128, 0, 0, &TL.plan, true);
+    if (rc != MOE_OK)
+        return rc;
+    TL.L = make_layout(MOE_BF16, T, H, I, E, k, TL.plan);
+    const int64_t P = TL.plan.max_padded, S = (int64_t)T * k;
+    TL.Pp = align_up(P, 64);
+    int64_t off = align_up((int64_t)TL.plan.workspace_bytes, kAlign);
+    auto take = [&](int64_t bytes) {
+        const int64_t o = off;
+        off = align_up(off + bytes, kAlign);
+        return o;
+    };
+    TL.gu = take(P * 2 * I * 2);
+    TL.dys = take(P * H * 2);
+    TL.dgu = take(P * 2 * I * 2);
+    TL.dxs = take(S * H * 4);
+    TL.dlogit = take((int64_t)T * E * 4);
+    TL.wdT = take((int64_t)E * I * H * 2);
+    TL.wguT = take((int64_t)E * H * 2 * I * 2);
+    TL.dysT = take(H * TL.Pp * 2);
+    TL.hT = take(I * TL.Pp * 2);
+    TL.dguT = take(2 * I * TL.Pp * 2);
+    TL.xsT = take(H * TL.Pp * 2);
+    TL.total = off;
+    return MOE_OK;
+}
+
+static int backward_impl(const void *x, const void *W_router, const void *W_gate_up, const void *W_down,
+                         const void *dout, int T, int H, int I, int E, int k, void *dx, float *dW_gate_up,
+                         float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes, cudaStream_t st)
+{
+    TrainLayout TL;
+    int rc = train_layout(T, H, I, E, k, TL);
+    if (rc != MOE_OK)
+        return rc;
+    if (!x || !W_router || !W_gate_up || !W_down || !dout || !dx || !dW_gate_up || !dW_down || !dW_router || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(dout, 16) || !aligned(dx, 16) || !aligned(W_gate_up, 16) ||
+        !aligned(W_down, 16) || !aligned(dW_gate_up, 16) || !aligned(dW_down, 16) || !aligned(ws, 256))
+        return MOE_ERR_INVALID_ARG;
+    if ((size_t)TL.total > ws_bytes)
+        return MOE_ERR_WORKSPACE;
+    const Layout &L = TL.L;
+    const moe_plan_t &p = TL.plan;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    auto at = [&](int64_t off) -> void * { return off < 0 ? nullptr : (void *)(w + off); };
+    auto bf = [&](int64_t off) { return static_cast<__nv_bfloat16 *>(at(off)); };
+    const int S = T * k;
+    const int64_t P = p.max_padded;
+    const int nsm = num_sms_current_device();
+    int *status = static_cast<int *>(at(L.status));
+
+    BackwardAux b;
+    memset(&b, 0, sizeof b);
+    b.dout = static_cast<const __nv_bfloat16 *>(dout);
+    b.x = static_cast<const __nv_bfloat16 *>(x);
+    b.Wr = static_cast<const __nv_bfloat16 *>(W_router);
+    b.sorted_ids = static_cast<const int32_t *>(at(L.sorted_ids));
+    b.sorted_w = static_cast<const float *>(at(L.sorted_w));
+    b.npp = static_cast<const int32_t *>(at(L.npp));
+    b.Y = static_cast<const float *>(at(L.y));
+    b.topk_ids = static_cast<const int32_t *>(at(L.topk_ids));
+    b.topk_w = static_cast<const float *>(at(L.topk_w));
+    b.T = T;
+    b.k = k;
+    b.E = E;
+    b.H = H;
+    b.P_max = P;
+    b.dys = bf(TL.dys);
+    b.dlogit = static_cast<float *>(at(TL.dlogit));
+    b.dxs = static_cast<const float *>(at(TL.dxs));
+    b.dx = static_cast<__nv_bfloat16 *>(dx);
+    b.dWr = dW_router;
+    b.dbias = dbias;
+    if (launch_backward_aux(0, b, st) != cudaSuccess || launch_backward_aux(1, b, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    // weights transposed so that both backward GEMMs read K-major rows
+    if (launch_transpose(static_cast<const __nv_bfloat16 *>(W_down), bf(TL.wdT), E, H, I, H, st) != cudaSuccess ||
+        launch_transpose(static_cast<const __nv_bfloat16 *>(W_gate_up), bf(TL.wguT), E, 2 * I, H, 2 * I, st) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    g.sorted_ids = b.sorted_ids;
+    g.sorted_expert_ids = static_cast<const int32_t *>(at(L.sorted_eids));
+    g.num_post_padded = b.npp;
+    g.expert_offsets = static_cast<const int32_t *>(at(L.offsets));
+    g.active_experts = static_cast<const int32_t *>(at(L.active));
+    g.num_active = static_cast<const int32_t *>(at(L.num_active));
+    g.expert_counts = static_cast<const int32_t *>(at(L.counts));
+    g.S = S;
+    g.E = E;
+    g.P_max = P;
+    g.split_k = 1;
+    g.status = status;
+
+    // dh = dY W_down, with SwiGLU's backward in the epilogue -> dg | du
+    GemmArgs g3 = g;
+    if (!encode_tmap_2d(&g3.tm_x, at(TL.dys), 2, H, P, 64, 128) ||
+        !encode_tmap_2d(&g3.tm_w, at(TL.wdT), 2, H, (uint64_t)E * I, 64, 128))
+        return MOE_ERR_CUDA;
+    g3.K = H;
+    g3.N = I;
+    g3.rows_per_expert = I;
+    g3.gu_in = bf(TL.gu);
+    g3.dgu = bf(TL.dgu);
+    g3.tile_counter = status + 1;
+    if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    int64_t ub = p.max_blocks * (I / 256);
+    if (launch_gemm_backward_bf16(3, g3, (int)(ub < nsm ? ub : nsm), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    // dx per slot = dg W_gate + du W_up (stage 2's tile shape, unit weights)
+    GemmArgs g2 = g;
+    if (!encode_tmap_2d(&g2.tm_x, at(TL.dgu), 2, 2 * I, P, 64, 128) ||
+        !encode_tmap_2d(&g2.tm_w, at(TL.wguT), 2, 2 * I, (uint64_t)E * H, 64, 128))
+        return MOE_ERR_CUDA;
+    g2.K = 2 * I;
+    g2.N = H;
+    g2.rows_per_expert = H;
+    g2.sorted_weights = nullptr;
+    g2.y = static_cast<float *>(at(TL.dxs));
+    g2.tile_counter = status + 1;
+    if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    ub = p.max_blocks * ((H + 255) / 256);
+    if (launch_gemm_backward_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_backward_aux(2, b, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    // weight gradients: activations transposed to [rows][P] so K runs over each expert's positions
+    const int64_t Pp = TL.Pp;
+    if (launch_transpose(bf(TL.dys), bf(TL.dysT), 1, P, H, Pp, st) != cudaSuccess ||
+        launch_transpose(bf(L.inter), bf(TL.hT), 1, P, I, Pp, st) != cudaSuccess ||
+        launch_transpose(bf(TL.dgu), bf(TL.dguT), 1, P, 2 * I, Pp, st) != cudaSuccess ||
+        launch_transpose(bf(L.x_sorted), bf(TL.xsT), 1, P, H, Pp, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    struct WG {
+        int64_t a_off, b_off;
+        int M, N;
+        float *out;
+    } wg[2] = {{TL.dysT, TL.hT, H, I, dW_down}, {TL.dguT, TL.xsT, 2 * I, H, dW_gate_up}};
+    for (const WG &q : wg) {
+        GemmArgs g5 = g;
+        if (!encode_tmap_2d(&g5.tm_x, at(q.a_off), 2, Pp, q.M, 64, 128) ||
+            !encode_tmap_2d(&g5.tm_w, at(q.b_off), 2, Pp, q.N, 64, 128))
+            return MOE_ERR_CUDA;
+        g5.K = (int)Pp;
+        g5.M = q.M;
+        g5.N = q.N;
+        g5.dw_out = q.out;
+        const int64_t tiles = (int64_t)E * (q.M / 128) * ((q.N + 255) / 256);
+        if (launch_gemm_backward_bf16(5, g5, (int)(tiles < nsm ? tiles : nsm), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    if (launch_backward_aux(3, b, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // namespace moe
@@ -760,6 +945,41 @@ int moe_fused_forward(int dtype, const void *x, const void *W_router, const floa
 {
     return forward_impl(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
                         block_m, split_k, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_train_workspace_size(int T, int H, int I, int E, int k)
+{
+    TrainLayout TL;
+    if (train_layout(T, H, I, E, k, TL) != MOE_OK)
+        return 0;
+    return (size_t)TL.total;
+}
+
+int moe_fused_forward_train(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
+                            const void *W_down, int T, int H, int I, int E, int k, void *out, void *ws,
+                            size_t ws_bytes, void *stream)
+{
+    TrainLayout TL;
+    int rc = train_layout(T, H, I, E, k, TL);
+    if (rc != MOE_OK)
+        return rc;
+    if (!ws || (size_t)TL.total > ws_bytes)
+        return !ws ? MOE_ERR_INVALID_ARG : MOE_ERR_WORKSPACE;
+    return forward_impl(MOE_BF16, x, W_router, router_bias, W_gate_up, nullptr, W_down, nullptr, T, H, I, E, k, 128,
+                        0, out, ws, TL.plan.workspace_bytes, static_cast<cudaStream_t>(stream),
+                        reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) + TL.gu));
+}
+
+int moe_fused_backward(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
+                       const void *W_down, const void *dout, int T, int H, int I, int E, int k, void *dx,
+                       float *dW_gate_up, float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes,
+                       void *stream)
+{
+    (void)router_bias;  // enters the backward only through the routing kept by the training forward
+    if (T == 0)
+        return MOE_OK;
+    return backward_impl(x, W_router, W_gate_up, W_down, dout, T, H, I, E, k, dx, dW_gate_up, dW_down, dW_router,
+                         dbias, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_host_staging_bytes(int T, int H)

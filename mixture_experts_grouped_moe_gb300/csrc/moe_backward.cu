@@ -1,0 +1,216 @@
+// Backward of the bf16 fused MoE layer (training): the "dgrad" of both
+// group GEMMs, the "wgrad" of both weight stacks, and the router, for
+// loss = sum(dout * out) -- the pages' stated future work for the group-GEMM
+// MoE kernels (FlyDSL-JAX talk, outlook; Jaxator talk, weight-gradient pass).
+//
+// A training forward (moe_fused_forward_train) runs the grouped path and
+// keeps, in its workspace, the routing, the sorted activations x_s, the
+// pre-activations g | u, h and the weighted stage-2 rows Y.  The backward:
+//   dY_p = w_p dout_t (sorted order)          D_s = dout_t . Y_s
+//   dl   = softmax backward over the chosen k from the D_s (dlogit, zero elsewhere)
+//   dh   = dY W_down            -> SwiGLU backward in the GEMM epilogue -> dg | du
+//   dx_s = dg W_gate + du W_up  (stage 2's tile shape, unit weights)
+//   dx_t = sum_j dx_{t,j} + sum_j dl_j W_router[e_j]
+//   dW_down[e] = dY_e^T h_e, dW_gate_up[e] = (dg|du)_e^T x_e  (K over e's tokens)
+//   dW_router = dlogit^T x, dbias = column sums of dlogit
+// Every GEMM keeps both operands K-major, the form the tcgen05 kernels take:
+// the weights are transposed once per call ([E][I][H] and [E][H][2I]) and
+// the activations of the weight gradients are transposed into [rows][P].
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// dY rows in sorted order: dY_p = w_p * dout[t_p] (bf16), zero for padding.
+__global__ void __launch_bounds__(256) dy_gather_kernel(const __nv_bfloat16 *__restrict__ dout,
+                                                       const int32_t *__restrict__ sorted_ids,
+                                                       const float *__restrict__ sorted_w,
+                                                       const int32_t *__restrict__ npp, int S, int k, int H,
+                                                       __nv_bfloat16 *__restrict__ dys)
+{
+    const int rows = *npp;
+    const int nvec = H / 8;
+    for (int p = blockIdx.x; p < rows; p += gridDim.x) {
+        const int s = sorted_ids[p];
+        uint4 *dst = reinterpret_cast<uint4 *>(dys + (size_t)p * H);
+        if (s >= S) {
+            for (int c = threadIdx.x; c < nvec; c += blockDim.x)
+                dst[c] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const float w = sorted_w[p];
+        const uint4 *src = reinterpret_cast<const uint4 *>(dout + (size_t)(s / k) * H);
+        for (int c = threadIdx.x; c < nvec; c += blockDim.x) {
+            uint4 v = src[c];
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h2[i]);
+                h2[i] = __floats2bfloat162_rn(w * f.x, w * f.y);
+            }
+            dst[c] = v;
+        }
+    }
+}
+
+// One warp per token.  With D_j = dout_t . Y_{t,j} (Y holds the weighted rows
+// w_j y_j), the softmax backward dl_j = w_j (dw_j - sum_m w_m dw_m), dw_j =
+// dout_t . y_j, is dl_j = D_j - w_j sum_m D_m; written to dlogit[t][e_j].
+__global__ void __launch_bounds__(256) router_grad_kernel(const __nv_bfloat16 *__restrict__ dout,
+                                                         const float *__restrict__ Y,
+                                                         const int32_t *__restrict__ ids,
+                                                         const float *__restrict__ wts, int T, int k, int E, int H,
+                                                         float *__restrict__ dlogit)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T)
+        return;
+    const int t = warp;
+    float D = 0.0f;    // lane j < k keeps D_j
+    float sum = 0.0f;  // sum_m D_m
+    for (int j = 0; j < k; ++j) {
+        const float *yr = Y + ((size_t)t * k + j) * H;
+        const __nv_bfloat16 *dr = dout + (size_t)t * H;
+        float acc = 0.0f;
+        for (int h = lane; h < H; h += 32)
+            acc = fmaf(bf2f(dr[h]), yr[h], acc);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == j)
+            D = acc;
+        sum += acc;
+    }
+    for (int e = lane; e < E; e += 32)
+        dlogit[(size_t)t * E + e] = 0.0f;
+    __syncwarp();
+    if (lane < k)
+        dlogit[(size_t)t * E + ids[(size_t)t * k + lane]] = D - wts[(size_t)t * k + lane] * sum;
+}
+
+// out[b][c][r] = in[b][r][c] for r < R (rows), c < C; out rows have ld_out elements.
+__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *__restrict__ in,
+                                                       __nv_bfloat16 *__restrict__ out, int64_t R, int64_t C,
+                                                       int64_t ld_out)
+{
+    __shared__ __nv_bfloat16 tile[32][33];
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+    const __nv_bfloat16 *src = in + b * R * C;
+    __nv_bfloat16 *dst = out + b * C * ld_out;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const int64_t r = r0 + ty + i, c = c0 + tx;
+        if (r < R && c < C)
+            tile[ty + i][tx] = src[r * C + c];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const int64_t c = c0 + ty + i, r = r0 + tx;
+        if (r < R && c < C)
+            dst[c * ld_out + r] = tile[tx][ty + i];
+    }
+}
+
+// dx[t] = sum_j dxs[t*k + j] (j ascending) + sum_j dlogit[t][e_j] W_router[e_j]  -> bf16
+__global__ void __launch_bounds__(256) dx_kernel(const float *__restrict__ dxs, const float *__restrict__ dlogit,
+                                                const int32_t *__restrict__ ids,
+                                                const __nv_bfloat16 *__restrict__ Wr, int T, int k, int E, int H,
+                                                __nv_bfloat16 *__restrict__ dx)
+{
+    const int64_t total = (int64_t)T * H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / H;
+        const int h = (int)(i - t * H);
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j)
+            acc += dxs[(t * k + j) * H + h];
+        for (int j = 0; j < k; ++j) {
+            const int e = ids[t * k + j];
+            acc = fmaf(dlogit[t * E + e], bf2f(Wr[(size_t)e * H + h]), acc);
+        }
+        dx[i] = __float2bfloat16_rn(acc);
+    }
+}
+
+// dW_router[e][h] = sum_t dlogit[t][e] x[t][h] (t ascending); dbias[e] = sum_t dlogit[t][e].
+__global__ void __launch_bounds__(256) router_wgrad_kernel(const float *__restrict__ dlogit,
+                                                          const __nv_bfloat16 *__restrict__ x, int T, int E, int H,
+                                                          float *__restrict__ dWr, float *__restrict__ dbias)
+{
+    const int e = blockIdx.y;
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h < H) {
+        float acc = 0.0f;
+        for (int t = 0; t < T; ++t)
+            acc = fmaf(dlogit[(size_t)t * E + e], bf2f(x[(size_t)t * H + h]), acc);
+        dWr[(size_t)e * H + h] = acc;
+    }
+    if (dbias && blockIdx.x == 0 && threadIdx.x == 0) {
+        float acc = 0.0f;
+        for (int t = 0; t < T; ++t)
+            acc += dlogit[(size_t)t * E + e];
+        dbias[e] = acc;
+    }
+}
+
+cudaError_t transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batches, int64_t R, int64_t C,
+                      int64_t ld_out, cudaStream_t st)
+{
+    if (batches <= 0 || R <= 0 || C <= 0)
+        return cudaSuccess;
+    dim3 grid((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)batches);
+    transpose_kernel<<<grid, 256, 0, st>>>(in, out, R, C, ld_out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_aux(int which, const BackwardAux &b, cudaStream_t st)
+{
+    switch (which) {
+    case 0: {  // dY gather
+        const int grid = (int)(b.P_max < 8192 ? b.P_max : 8192);
+        dy_gather_kernel<<<grid > 0 ? grid : 1, 256, 0, st>>>(b.dout, b.sorted_ids, b.sorted_w, b.npp, b.T * b.k,
+                                                              b.k, b.H, b.dys);
+        return cudaGetLastError();
+    }
+    case 1: {  // routing gradient
+        const int grid = (b.T * 32 + 255) / 256;
+        router_grad_kernel<<<grid > 0 ? grid : 1, 256, 0, st>>>(b.dout, b.Y, b.topk_ids, b.topk_w, b.T, b.k, b.E,
+                                                                b.H, b.dlogit);
+        return cudaGetLastError();
+    }
+    case 2: {  // dx
+        int64_t grid = ((int64_t)b.T * b.H + 255) / 256;
+        if (grid > 65535)
+            grid = 65535;
+        dx_kernel<<<(int)(grid > 0 ? grid : 1), 256, 0, st>>>(b.dxs, b.dlogit, b.topk_ids, b.Wr, b.T, b.k, b.E, b.H,
+                                                            b.dx);
+        return cudaGetLastError();
+    }
+    case 3: {  // router weight gradient
+        dim3 grid((unsigned)((b.H + 255) / 256), (unsigned)b.E);
+        router_wgrad_kernel<<<grid, 256, 0, st>>>(b.dlogit, b.x, b.T, b.E, b.H, b.dWr, b.dbias);
+        return cudaGetLastError();
+    }
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batches, int64_t R, int64_t C,
+                             int64_t ld_out, cudaStream_t st)
+{
+    return transpose(in, out, batches, R, C, ld_out, st);
+}
+
+}  // namespace moe

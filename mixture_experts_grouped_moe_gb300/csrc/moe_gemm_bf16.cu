@@ -89,9 +89,17 @@ struct Tile {
     int ks;         // K split index (swap stage 2)
 };
 
+// Internal tile shape of the weight-gradient GEMMs (STAGE 5): per expert e,
+// D[e] (M x N) = A_e B_e^T with K running over e's sorted token positions;
+// A and B are row arrays whose K dimension is the position (transposed
+// activations), tiles 128 rows of A x 256 rows of B.
+constexpr int kModeSegment = 2;
+
 template <int MODE, int STAGE>
 __device__ __forceinline__ int num_tiles(const GemmArgs &a)
 {
+    if (MODE == kModeSegment)
+        return a.E * (a.M / 128) * ((a.N + 255) / 256);
     if (MODE == MOE_MODE_GROUPED) {
         const int nmb = *a.num_post_padded / 128;
         const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
@@ -109,6 +117,21 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t)
     Tile tl;
     tl.valid = 1;
     const int nkb = a.K / kBK<QT>;
+    if (MODE == kModeSegment) {
+        const int nmt = a.M / 128, nnt = (a.N + 255) / 256;
+        tl.e = t / (nmt * nnt);
+        const int rem = t - tl.e * nmt * nnt;
+        const int nt = rem / nmt, mt = rem % nmt;
+        tl.xrow = mt * 128;            // A rows (output rows)
+        tl.nx = 128;
+        tl.wrow0 = nt * 256;           // B rows (output columns)
+        tl.wrow1 = tl.wrow0 + 128;
+        tl.ncol0 = nt * 256;
+        tl.kb0 = a.expert_offsets[tl.e] / kBK<QT>;   // segments are whole 128-row blocks
+        tl.kb1 = a.expert_offsets[tl.e + 1] / kBK<QT>;
+        tl.ks = 0;
+        return tl;
+    }
     if (MODE == MOE_MODE_GROUPED) {
         const int nmb = *a.num_post_padded / 128;
         const int nnt = (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
@@ -231,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     mbar_arrive_expect_tx(&sm.full[s], bytes);
                     tma_load_2d(wdst, &a.tm_w, kb * kBK<QT>, tl.wrow0, &sm.full[s], pol_w);
                     tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * kBK<QT>, tl.wrow1, &sm.full[s], pol_w);
-                    if (MODE == MOE_MODE_GROUPED) {
+                    if (MODE != MOE_MODE_SWAP) {
                         tma_load_2d(xdst, &a.tm_x, kb * kBK<QT>, tl.xrow, &sm.full[s], pol_x);
                     } else {
                         for (int c = 0; c < tl.nx; c += 16)
@@ -286,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccCols;
                 constexpr uint32_t kFmt = QT ? 0u : 1u;  // e4m3 (kind::f8f6f4) or bf16 (kind::f16)
-                const uint32_t idesc = (MODE == MOE_MODE_GROUPED) ? make_idesc(kFmt, kFmt, 128, 256)
-                                                                  : make_idesc(kFmt, kFmt, 128, (uint32_t)tl.nx);
+                const uint32_t idesc = (MODE != MOE_MODE_SWAP) ? make_idesc(kFmt, kFmt, 128, 256)
+                                                               : make_idesc(kFmt, kFmt, 128, (uint32_t)tl.nx);
                 for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
                     if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
                         ok = false;
@@ -299,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {  // 4 MMAs of 32 bytes of K each
                         const uint32_t accum = (kb > tl.kb0 || kk > 0) ? 1u : 0u;
-                        if (MODE == MOE_MODE_GROUPED) {
+                        if (MODE != MOE_MODE_SWAP) {
                             mma_kind<QT>(d, smem_desc_sw128(xs + kk * 32), smem_desc_sw128(w + kk * 32), idesc,
                                          accum);
                         } else {
@@ -382,11 +405,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     for (int i = 0; i < 32; ++i)
                         h[i] = silu(g[i]) * u[i];
                     store_bf16x32(dst + c0, h);
+                    if (a.gu) {  // training: keep the pre-activations for the backward
+                        __nv_bfloat16 *gr = a.gu + (size_t)(tl.xrow + row) * (2 * a.N) + tl.ncol0 + c0;
+                        store_bf16x32(gr, g);
+                        store_bf16x32(gr + a.N, u);
+                    }
+                }
+            } else if (MODE == MOE_MODE_GROUPED && STAGE == 3) {
+                // backward of stage 2 (dh = dY W_down): SwiGLU's backward with the saved g | u,
+                // dg = dh u silu'(g), du = dh silu(g), into dgu (g part at column c, u part at I + c)
+                const size_t p = (size_t)(tl.xrow + row);
+                const __nv_bfloat16 *gr = a.gu_in + p * (2 * a.N) + tl.ncol0;
+                __nv_bfloat16 *dr = a.dgu + p * (2 * a.N) + tl.ncol0;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    float dh[32], dg[32], du[32];
+                    tmem_ld32(tacc + c0, dh);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(gr + c0 + i);
+                        const uint4 uv = *reinterpret_cast<const uint4 *>(gr + a.N + c0 + i);
+                        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+                        const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const float2 gf = __bfloat1622float2(g2[q2]);
+                            const float2 uf = __bfloat1622float2(u2[q2]);
+                            const float gg[2] = {gf.x, gf.y}, uu[2] = {uf.x, uf.y};
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int ii = i + 2 * q2 + r;
+                                const float sg = 1.0f / (1.0f + __expf(-gg[r]));
+                                dg[ii] = dh[ii] * uu[r] * sg * (1.0f + gg[r] * (1.0f - sg));
+                                du[ii] = dh[ii] * gg[r] * sg;
+                            }
+                        }
+                    }
+                    store_bf16x32(dr + c0, dg);
+                    store_bf16x32(dr + a.N + c0, du);
+                }
+            } else if (MODE == kModeSegment) {
+                // weight gradient: output row tl.xrow + row of expert e, columns ncol0 .. +256
+                float *dst = a.dw_out + ((size_t)tl.e * a.M + tl.xrow + row) * a.N + tl.ncol0;
+                const int ncols = min(256, a.N - tl.ncol0);
+                const bool empty = tl.kb0 == tl.kb1;  // an expert without tokens: zero gradient
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = empty ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             } else if (MODE == MOE_MODE_GROUPED && STAGE == 2) {
                 const int pos = tl.xrow + row;
                 const int slot = a.sorted_ids[pos];
-                const float wgt = a.sorted_weights[pos] * (QT ? a.x_scales[pos] : 1.0f);
+                // no weights: the unweighted rows (the backward's dx per slot)
+                const float wgt = (a.sorted_weights ? a.sorted_weights[pos] : 1.0f) * (QT ? a.x_scales[pos] : 1.0f);
                 const bool live = slot < a.S;
                 float *dst = a.y + (size_t)(live ? slot : 0) * a.N + tl.ncol0;
                 const int ncols = min(256, a.N - tl.ncol0);
@@ -503,6 +580,17 @@ cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cud
 {
     return stage == 1 ? bf16gemm::launch<MOE_MODE_GROUPED, 1, 0>(a, grid, st)
                       : bf16gemm::launch<MOE_MODE_GROUPED, 2, 0>(a, grid, st);
+}
+
+cudaError_t launch_gemm_backward_bf16(int which, const GemmArgs &a, int grid, cudaStream_t st)
+{
+    // 3: backward of stage 2 with SwiGLU's backward; 2: backward of stage 1 (stage 2's
+    // tile shape, unit weights); 5: weight gradients over token segments
+    if (which == 3)
+        return bf16gemm::launch<MOE_MODE_GROUPED, 3, 0>(a, grid, st);
+    if (which == 5)
+        return bf16gemm::launch<bf16gemm::kModeSegment, 5, 0>(a, grid, st);
+    return bf16gemm::launch<MOE_MODE_GROUPED, 2, 0>(a, grid, st);
 }
 
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st)

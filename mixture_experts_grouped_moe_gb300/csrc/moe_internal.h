@@ -148,6 +148,12 @@ struct GemmArgs {
     float *partials;         // stage 2 split-K: [split][P_max][H]
     int *status;
     int *tile_counter;       // zeroed before the launch; CTAs claim tiles from it
+    // training (bf16, grouped mode)
+    __nv_bfloat16 *gu;       // stage 1: when set, also the pre-activations [P_max][2I] (g | u)
+    const __nv_bfloat16 *gu_in;  // backward of stage 2 (STAGE 3): saved g | u
+    __nv_bfloat16 *dgu;      // backward of stage 2: dg | du [P_max][2I]
+    float *dw_out;           // weight gradient (STAGE 5, segment mode): [E][M][N] fp32
+    int M;                   // segment mode: rows of the A operand (output rows)
 };
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
@@ -169,6 +175,32 @@ struct FusedArgs {
     int *h_done;
 };
 cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st);
+// Training (bf16): backward GEMMs -- which = 3: dh = dY W_down with
+// SwiGLU's backward epilogue (into dgu); 2: dx per slot = dgu W_gate_up
+// (stage 2's tile shape, sorted_weights null = unit weights); 5: weight
+// gradients over token segments (A, B transposed activations [rows][P]).
+cudaError_t launch_gemm_backward_bf16(int which, const GemmArgs &a, int grid, cudaStream_t st);
+struct BackwardAux {
+    const __nv_bfloat16 *dout, *x, *Wr;
+    const int32_t *sorted_ids;
+    const float *sorted_w;
+    const int32_t *npp;
+    const float *Y;            // forward's weighted stage-2 rows [S][H]
+    const int32_t *topk_ids;
+    const float *topk_w;
+    int T, k, E, H;
+    int64_t P_max;
+    __nv_bfloat16 *dys;        // [P_max][H]
+    float *dlogit;             // [T][E]
+    const float *dxs;          // [S][H]
+    __nv_bfloat16 *dx;         // [T][H]
+    float *dWr, *dbias;        // [E][H], [E] (dbias nullable)
+};
+// which: 0 dY gather, 1 routing gradient, 2 dx, 3 router weight gradient
+cudaError_t launch_backward_aux(int which, const BackwardAux &b, cudaStream_t st);
+// out[b][c][r] = in[b][r][c] (bf16), out rows of ld_out elements
+cudaError_t launch_transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batches, int64_t R, int64_t C,
+                             int64_t ld_out, cudaStream_t st);
 // MXFP4: swap-AB GEMMs with hardware block scaling, and the 1x32 quantiser
 // (row-major or tiled E8M0 scales; optional gather through sorted_ids).
 cudaError_t launch_gemm_swap_mx4(int stage, const GemmArgs &a, int grid, cudaStream_t st);

@@ -34,7 +34,8 @@ EXPORTED = [
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
     "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
-    "moe_set_gemm_pair", "moe_quantize_mxfp4", "moe_set_one_stage",
+    "moe_set_gemm_pair", "moe_quantize_mxfp4", "moe_set_one_stage", "moe_train_workspace_size",
+    "moe_fused_forward_train", "moe_fused_backward",
 ]
 
 
@@ -100,6 +101,9 @@ def load(build_if_missing: bool = False):
             "moe_set_stage_events": (I, [P, I]),
             "moe_set_gemm_pair": (I, [I]),
             "moe_set_one_stage": (I, [I]),
+            "moe_train_workspace_size": (SZ, [I, I, I, I, I]),
+            "moe_fused_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]),
+            "moe_fused_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, SZ, P]),
             "moe_quantize_mxfp4": (I, [P, I64, I, P, P, I, P]),
             "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
@@ -254,6 +258,58 @@ def moe_set_gemm_pair(mode: int):
 def moe_set_one_stage(mode: int):
     """One-kernel bf16 decode path: 1 on, 0 off (process-wide)."""
     return _check("moe_set_one_stage", load().moe_set_one_stage(mode))
+
+
+def moe_train_workspace_size(T, H, I, E, k) -> int:
+    return load().moe_train_workspace_size(T, H, I, E, k)
+
+
+def moe_fused_forward_train(x, W_router, router_bias, W_gate_up, W_down, T, H, I, E, k, out, ws, ws_bytes,
+                            stream=None):
+    return _check("moe_fused_forward_train", load().moe_fused_forward_train(
+        _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(W_down), T, H, I, E, k, _p(out), _p(ws), ws_bytes,
+        _stream(stream)))
+
+
+def moe_fused_backward(x, W_router, router_bias, W_gate_up, W_down, dout, T, H, I, E, k, dx, dW_gate_up, dW_down,
+                       dW_router, dbias, ws, ws_bytes, stream=None):
+    return _check("moe_fused_backward", load().moe_fused_backward(
+        _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(W_down), _p(dout), T, H, I, E, k, _p(dx),
+        _p(dW_gate_up), _p(dW_down), _p(dW_router), _p(dbias), _p(ws), ws_bytes, _stream(stream)))
+
+
+class MoETrain:
+    """Owns the training workspace of one bf16 layer shape: forward(), then backward()."""
+
+    def __init__(self, T, H, I, E, k, device="cuda"):
+        import torch
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.ws_bytes = moe_train_workspace_size(T, H, I, E, k)
+        if self.ws_bytes == 0:
+            raise MoEError("moe_train_workspace_size", MOE_ERR_INVALID_ARG)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def forward(self, x, w, out, stream=None):
+        moe_fused_forward_train(x, w["W_router"], w.get("bias"), w["W_gate_up"], w["W_down"], self.T, self.H, self.I,
+                                self.E, self.k, out, self.ws, self.ws_bytes, stream)
+        return out
+
+    def backward(self, x, w, dout, stream=None):
+        """Returns dict dx (bf16), dW_gate_up, dW_down, dW_router, dbias (fp32)."""
+        import torch
+        dev = x.device
+        g = {"dx": torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev),
+             "dW_gate_up": torch.empty(self.E, 2 * self.I, self.H, dtype=torch.float32, device=dev),
+             "dW_down": torch.empty(self.E, self.H, self.I, dtype=torch.float32, device=dev),
+             "dW_router": torch.empty(self.E, self.H, dtype=torch.float32, device=dev),
+             "dbias": torch.empty(self.E, dtype=torch.float32, device=dev)}
+        moe_fused_backward(x, w["W_router"], w.get("bias"), w["W_gate_up"], w["W_down"], dout, self.T, self.H, self.I,
+                           self.E, self.k, g["dx"], g["dW_gate_up"], g["dW_down"], g["dW_router"], g["dbias"], self.ws,
+                           self.ws_bytes, stream)
+        return g
+
+    def status(self, stream=None) -> int:
+        return moe_workspace_status(self.ws, stream)
 
 
 def moe_set_stage_events(events):
