@@ -353,6 +353,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--workload", default="mixtral_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="bf16 training step: training forward + backward (dx and all weight gradients)")
     ap.add_argument("--two-launch", action="store_true",
                     help="bf16 decode: stage 1 and stage 2 as two launches instead of the one-kernel path")
     ap.add_argument("--experts", type=int, default=0, help="profiling aid: override E (not a bench line)")
@@ -381,6 +383,8 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
+    if args.train:
+        return run_train(args, cfg, rank, world, local_rank)
     r = run_cuda(args, cfg, rank, world, local_rank)
     if rank != 0:
         if world > 1:
@@ -462,6 +466,91 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def run_train(args, cfg, rank, world, local_rank):
+    """One training step = moe_fused_forward_train + moe_fused_backward on device-resident inputs."""
+    import torch
+
+    from mixture_experts_grouped_moe_gb300 import build as moe_build
+    from mixture_experts_grouped_moe_gb300 import moe, synth
+
+    if cfg.dtype != "bf16":
+        raise SystemExit("--train runs the bf16 layer")
+    moe_build.build()
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_kind = load_peaks()
+    inp = synth.make_inputs(cfg, seed=0, device=dev)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
+    dout = torch.randn(cfg.T, cfg.H, generator=torch.Generator(device=dev).manual_seed(1), device=dev).to(
+        torch.bfloat16)
+    tr = moe.MoETrain(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, device=dev)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        tr.forward(inp["x"], w, out)
+        g = tr.backward(inp["x"], w, dout)
+    torch.cuda.synchronize()
+    if tr.status() != moe.MOE_OK:
+        raise RuntimeError("device wait timed out during warm-up")
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    fw = bw = 0.0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.15)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        tr.forward(inp["x"], w, out)
+        g = tr.backward(inp["x"], w, dout)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = start.elapsed_time(stop) / K
+    for _ in range(K):  # split of the step (events between the two calls)
+        ev[0].record(stream)
+        tr.forward(inp["x"], w, out)
+        ev[1].record(stream)
+        g = tr.backward(inp["x"], w, dout)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        fw += ev[0].elapsed_time(ev[1])
+        bw += ev[1].elapsed_time(ev[2])
+    fw, bw = fw / K, bw / K
+    assert all(torch.isfinite(v.float()).all() for v in g.values())
+    if world > 1:
+        ms, = max_over_ranks([ms], dev)
+    if rank != 0:
+        return 0
+    S, H, I = cfg.S, cfg.H, cfg.I
+    fwd_flops = 2.0 * S * 3 * H * I
+    flops = 3 * fwd_flops  # forward, input gradient, weight gradients
+    peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    bwd_tflops = 2 * fwd_flops / (bw * 1e-3) / 1e12
+    line = {
+        "metric": METRIC + " (training step)", "value": round(whole_job_throughput(world, cfg.T, ms), 2),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations and output gradient, N(0,1/fan_in) weights)",
+        "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}", step="forward + backward"),
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "stage_ms": {"forward_train": round(fw, 5), "backward": round(bw, 5)},
+        "roofline": {"bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": round(bwd_tflops / peak_t, 4), "kernel": "backward (its GEMMs, transposes and aux)",
+                     "alg_flops_per_launch": 2 * fwd_flops, "peak_source": peak_kind, "traffic": None},
+        "clocks": clocks,
+        "e2e": None,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
