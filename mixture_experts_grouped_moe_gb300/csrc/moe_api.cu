@@ -516,7 +516,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 struct TrainLayout {
     moe_plan_t plan;
     Layout L;
-    int64_t gu, dys, dgu, dxs, dlogit, wdT, wguT, dysT, hT, dguT, xsT, total;
+    int64_t gu, dys, dgu, dxs, dlogit, wdT, wguT, dysT, hT, dguT, xsT, rg_part, total;
     int64_t Pp;  // row length of the transposed activations (>= max_padded, multiple of 64)
 };
 
@@ -550,6 +550,7 @@ static int train_layout(int T, int H, int I, int E, int k, TrainLayout &TL)
     TL.hT = take(I * TL.Pp * 2);
     TL.dguT = take(2 * I * TL.Pp * 2);
     TL.xsT = take(H * TL.Pp * 2);
+    TL.rg_part = take(router_wgrad_scratch(T, E, H) * 4);
     TL.total = off;
     return MOE_OK;
 }
@@ -601,6 +602,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     b.dx = static_cast<__nv_bfloat16 *>(dx);
     b.dWr = dW_router;
     b.dbias = dbias;
+    b.rg_part = static_cast<float *>(at(TL.rg_part));
     if (launch_backward_aux(0, b, st) != cudaSuccess || launch_backward_aux(1, b, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     // weights transposed so that both backward GEMMs read K-major rows
@@ -681,6 +683,9 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
         g5.M = q.M;
         g5.N = q.N;
         g5.dw_out = q.out;
+        g5.tile_counter = status + 1;  // tiles of unequal K (segment lengths): claimed dynamically
+        if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
         const int64_t tiles = (int64_t)E * (q.M / 128) * ((q.N + 255) / 256);
         if (launch_gemm_backward_bf16(5, g5, (int)(tiles < nsm ? tiles : nsm), st) != cudaSuccess)
             return MOE_ERR_CUDA;

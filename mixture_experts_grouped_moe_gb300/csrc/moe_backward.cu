@@ -94,29 +94,40 @@ __global__ void __launch_bounds__(256) router_grad_kernel(const __nv_bfloat16 *_
         dlogit[(size_t)t * E + ids[(size_t)t * k + lane]] = D - wts[(size_t)t * k + lane] * sum;
 }
 
-// out[b][c][r] = in[b][r][c] for r < R (rows), c < C; out rows have ld_out elements.
+// out[b][c][r] = in[b][r][c] for r < R (rows), c < C (C % 64 == 0); out rows
+// have ld_out >= round_up(R, 64) elements (columns R..ld_out-1 of a tile are
+// written as 0).  64 x 64 tiles, 16-byte loads and stores.
 __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *__restrict__ in,
                                                        __nv_bfloat16 *__restrict__ out, int64_t R, int64_t C,
                                                        int64_t ld_out)
 {
-    __shared__ __nv_bfloat16 tile[32][33];
+    __shared__ uint16_t tile[64][66];
     const int64_t b = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
-    const __nv_bfloat16 *src = in + b * R * C;
-    __nv_bfloat16 *dst = out + b * C * ld_out;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(in) + b * R * C;
+    uint16_t *dst = reinterpret_cast<uint16_t *>(out) + b * C * ld_out;
+    const int t = threadIdx.x;
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-        const int64_t r = r0 + ty + i, c = c0 + tx;
-        if (r < R && c < C)
-            tile[ty + i][tx] = src[r * C + c];
+    for (int i = 0; i < 2; ++i) {
+        const int rr = t / 8 + 32 * i, cc = (t % 8) * 8;
+        const int64_t r = r0 + rr;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < R)
+            v = *reinterpret_cast<const uint4 *>(src + r * C + c0 + cc);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint32_t *>(&tile[rr][cc + 2 * q]) = w[q];
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-        const int64_t c = c0 + ty + i, r = r0 + tx;
-        if (r < R && c < C)
-            dst[c * ld_out + r] = tile[tx][ty + i];
+    for (int i = 0; i < 2; ++i) {
+        const int cc = t / 8 + 32 * i, rr = (t % 8) * 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = (uint32_t)tile[rr + 2 * q][cc] | ((uint32_t)tile[rr + 2 * q + 1][cc] << 16);
+        *reinterpret_cast<uint4 *>(dst + (c0 + cc) * ld_out + r0 + rr) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -141,25 +152,71 @@ __global__ void __launch_bounds__(256) dx_kernel(const float *__restrict__ dxs, 
     }
 }
 
-// dW_router[e][h] = sum_t dlogit[t][e] x[t][h] (t ascending); dbias[e] = sum_t dlogit[t][e].
-__global__ void __launch_bounds__(256) router_wgrad_kernel(const float *__restrict__ dlogit,
-                                                          const __nv_bfloat16 *__restrict__ x, int T, int E, int H,
-                                                          float *__restrict__ dWr, float *__restrict__ dbias)
+// dW_router[e][h] = sum_t dlogit[t][e] x[t][h], dbias[e] = sum_t dlogit[t][e]:
+// partial sums over chunks of 128 tokens (t ascending within a chunk; 8
+// experts per block, each x element read once; the bias sums alongside),
+// then a fixed-order sum of the chunks.
+constexpr int kRgChunk = 128;
+constexpr int kRgE = 8;
+
+__global__ void __launch_bounds__(256) router_wgrad_partial_kernel(const float *__restrict__ dlogit,
+                                                                  const __nv_bfloat16 *__restrict__ x, int T, int E,
+                                                                  int H, float *__restrict__ part,
+                                                                  float *__restrict__ bpart)
 {
-    const int e = blockIdx.y;
+    __shared__ float s_dl[kRgChunk][kRgE];
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h < H) {
-        float acc = 0.0f;
-        for (int t = 0; t < T; ++t)
-            acc = fmaf(dlogit[(size_t)t * E + e], bf2f(x[(size_t)t * H + h]), acc);
-        dWr[(size_t)e * H + h] = acc;
+    const int e0 = blockIdx.y * kRgE;
+    const int t0 = blockIdx.z * kRgChunk;
+    for (int i = threadIdx.x; i < kRgChunk * kRgE; i += blockDim.x) {
+        const int tt = i / kRgE, ee = i % kRgE;
+        s_dl[tt][ee] = (t0 + tt < T && e0 + ee < E) ? dlogit[(size_t)(t0 + tt) * E + e0 + ee] : 0.0f;
     }
-    if (dbias && blockIdx.x == 0 && threadIdx.x == 0) {
-        float acc = 0.0f;
-        for (int t = 0; t < T; ++t)
-            acc += dlogit[(size_t)t * E + e];
-        dbias[e] = acc;
+    __syncthreads();
+    const int tn = min(kRgChunk, T - t0);
+    if (blockIdx.x == 0 && threadIdx.x < kRgE && e0 + threadIdx.x < E) {  // the chunk's bias-gradient sums
+        float bsum = 0.0f;
+        for (int tt = 0; tt < tn; ++tt)
+            bsum += s_dl[tt][threadIdx.x];
+        bpart[(size_t)blockIdx.z * E + e0 + threadIdx.x] = bsum;
     }
+    if (h >= H)
+        return;
+    float acc[kRgE];
+#pragma unroll
+    for (int j = 0; j < kRgE; ++j)
+        acc[j] = 0.0f;
+    for (int tt = 0; tt < tn; ++tt) {
+        const float xv = bf2f(x[(size_t)(t0 + tt) * H + h]);
+#pragma unroll
+        for (int j = 0; j < kRgE; ++j)
+            acc[j] = fmaf(s_dl[tt][j], xv, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kRgE; ++j)
+        if (e0 + j < E)
+            part[((size_t)blockIdx.z * E + e0 + j) * H + h] = acc[j];
+}
+
+__global__ void __launch_bounds__(256) router_wgrad_reduce_kernel(const float *__restrict__ part,
+                                                                 const float *__restrict__ bpart, int E, int H,
+                                                                 int nchunks, float *__restrict__ dWr,
+                                                                 float *__restrict__ dbias)
+{
+    const int64_t total = (int64_t)E * H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = 0.0f;
+        for (int c = 0; c < nchunks; ++c)
+            acc += part[(size_t)c * total + i];
+        dWr[i] = acc;
+    }
+    if (dbias && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            float acc = 0.0f;
+            for (int c = 0; c < nchunks; ++c)
+                acc += bpart[(size_t)c * E + e];
+            dbias[e] = acc;
+        }
 }
 
 cudaError_t transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batches, int64_t R, int64_t C,
@@ -167,7 +224,7 @@ cudaError_t transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batch
 {
     if (batches <= 0 || R <= 0 || C <= 0)
         return cudaSuccess;
-    dim3 grid((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)batches);
+    dim3 grid((unsigned)((C + 63) / 64), (unsigned)((R + 63) / 64), (unsigned)batches);
     transpose_kernel<<<grid, 256, 0, st>>>(in, out, R, C, ld_out);
     return cudaGetLastError();
 }
@@ -198,8 +255,14 @@ cudaError_t launch_backward_aux(int which, const BackwardAux &b, cudaStream_t st
         return cudaGetLastError();
     }
     case 3: {  // router weight gradient
-        dim3 grid((unsigned)((b.H + 255) / 256), (unsigned)b.E);
-        router_wgrad_kernel<<<grid, 256, 0, st>>>(b.dlogit, b.x, b.T, b.E, b.H, b.dWr, b.dbias);
+        const int nchunks = (b.T + kRgChunk - 1) / kRgChunk;
+        dim3 grid((unsigned)((b.H + 255) / 256), (unsigned)((b.E + kRgE - 1) / kRgE), (unsigned)nchunks);
+        float *bpart = b.rg_part + (int64_t)nchunks * b.E * b.H;
+        router_wgrad_partial_kernel<<<grid, 256, 0, st>>>(b.dlogit, b.x, b.T, b.E, b.H, b.rg_part, bpart);
+        int64_t g2 = ((int64_t)b.E * b.H + 255) / 256;
+        if (g2 > 4096)
+            g2 = 4096;
+        router_wgrad_reduce_kernel<<<(int)g2, 256, 0, st>>>(b.rg_part, bpart, b.E, b.H, nchunks, b.dWr, b.dbias);
         return cudaGetLastError();
     }
     default:

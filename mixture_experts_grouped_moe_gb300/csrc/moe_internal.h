@@ -195,10 +195,13 @@ struct BackwardAux {
     const float *dxs;          // [S][H]
     __nv_bfloat16 *dx;         // [T][H]
     float *dWr, *dbias;        // [E][H], [E] (dbias nullable)
+    float *rg_part;            // [ceil(T/128)][E][H] + [ceil(T/128)][E] partial router / bias gradients
 };
+// Scratch floats of the router weight and bias gradients' partial sums.
+inline int64_t router_wgrad_scratch(int T, int E, int H) { return (int64_t)((T + 127) / 128) * E * (H + 1); }
 // which: 0 dY gather, 1 routing gradient, 2 dx, 3 router weight gradient
 cudaError_t launch_backward_aux(int which, const BackwardAux &b, cudaStream_t st);
-// out[b][c][r] = in[b][r][c] (bf16), out rows of ld_out elements
+// out[b][c][r] = in[b][r][c] (bf16); C % 64 == 0; out rows of ld_out >= round_up(R, 64) elements
 cudaError_t launch_transpose(const __nv_bfloat16 *in, __nv_bfloat16 *out, int64_t batches, int64_t R, int64_t C,
                              int64_t ld_out, cudaStream_t st);
 // MXFP4: swap-AB GEMMs with hardware block scaling, and the 1x32 quantiser
