@@ -453,7 +453,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (I / 64);
             ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
-        } else if (!train && use_pair(dtype, 1, T, k, E)) {
+        } else if (use_pair(dtype, 1, T, k, E)) {
             ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
         } else {
             const int64_t ub = p.max_blocks * (I / 128);
@@ -484,7 +484,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
-        } else if (!train && use_pair(dtype, 2, T, k, E)) {
+        } else if (use_pair(dtype, 2, T, k, E)) {
             ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
         } else {
             const int64_t ub = p.max_blocks * nt2;
@@ -639,8 +639,11 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     g3.tile_counter = status + 1;
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    // CTA pairs under the same rule as the forward's GEMMs
+    const bool pairs = use_pair(MOE_BF16, 1, T, k, E);
     int64_t ub = p.max_blocks * (I / 256);
-    if (launch_gemm_backward_bf16(3, g3, (int)(ub < nsm ? ub : nsm), st) != cudaSuccess)
+    if ((pairs ? launch_gemm_pair(3, 0, g3, (p.max_blocks / 2 + E) * (I / 256), st)
+               : launch_gemm_backward_bf16(3, g3, (int)(ub < nsm ? ub : nsm), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     // dx per slot = dg W_gate + du W_up (stage 2's tile shape, unit weights)
@@ -657,7 +660,8 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     ub = p.max_blocks * ((H + 255) / 256);
-    if (launch_gemm_backward_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st) != cudaSuccess)
+    if ((pairs ? launch_gemm_pair(2, 0, g2, (p.max_blocks / 2 + E) * ((H + 255) / 256), st)
+               : launch_gemm_backward_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_backward_aux(2, b, st) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -687,7 +691,9 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
         if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         const int64_t tiles = (int64_t)E * (q.M / 128) * ((q.N + 255) / 256);
-        if (launch_gemm_backward_bf16(5, g5, (int)(tiles < nsm ? tiles : nsm), st) != cudaSuccess)
+        const bool pair5 = pairs && q.M % 256 == 0;  // pair tiles span 256 gradient rows
+        if ((pair5 ? launch_gemm_pair(5, 0, g5, tiles / 2, st)
+                   : launch_gemm_backward_bf16(5, g5, (int)(tiles < nsm ? tiles : nsm), st)) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     if (launch_backward_aux(3, b, st) != cudaSuccess)

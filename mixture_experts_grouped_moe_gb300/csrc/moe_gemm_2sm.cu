@@ -79,7 +79,12 @@ struct PairTile {
     int wrow0;    // weight rows of B half 0 / half 1
     int wrow1;
     int ncol0;    // output column base
+    int kb0, kb1; // K blocks (weight gradients: the expert's token positions)
 };
+
+// STAGE 5 (weight gradients): D[e] (M x N) = A_e B_e^T with K over expert e's
+// sorted token positions; A and B are transposed activations [rows][P]; a
+// pair tile is 256 rows of A (128 per CTA) x 256 rows of B.
 
 template <int STAGE>
 __device__ __forceinline__ int n_tiles_n(const GemmArgs &a)
@@ -91,6 +96,21 @@ template <int STAGE>
 __device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, int t)
 {
     const int nnt = n_tiles_n<STAGE>(a);
+    if (STAGE == 5) {
+        const int nmp = a.M / 256;
+        PairTile p;
+        p.e = t / (nmp * nnt);
+        const int rem = t - p.e * nmp * nnt;
+        const int nt = rem / nmp;
+        p.mb0 = 2 * (rem % nmp);
+        p.second = 1;
+        p.wrow0 = nt * 256;
+        p.wrow1 = p.wrow0 + 128;
+        p.ncol0 = nt * 256;
+        p.kb0 = sm.off[p.e] / 64;
+        p.kb1 = sm.off[p.e + 1] / 64;
+        return p;
+    }
     // the expert: the last e with tstart[e] <= t (empty experts share their successor's start)
     int lo = 0, hi = a.E;
     while (hi - lo > 1) {
@@ -121,6 +141,7 @@ __device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, in
         p.wrow1 = p.wrow0 + 128;
         p.ncol0 = nt * 256;
     }
+    p.kb0 = p.kb1 = 0;  // the whole K (set by the kernel, which knows the element size)
     return p;
 }
 
@@ -166,7 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
     pdl_trigger();
 
     // pair-tile table: tstart[e] = sum over experts before e of ceil(blocks/2) * N tiles
-    if (warp == 2) {
+    if (STAGE == 5 && warp == 2) {
+        for (int e = lane; e <= a.E; e += 32)
+            sm.off[e] = a.expert_offsets[e];
+        if (lane == 0)
+            sm.ntiles = a.E * (a.M / 256) * n_tiles_n<STAGE>(a);
+    } else if (warp == 2) {
         const int E = a.E;
         const int nnt = n_tiles_n<STAGE>(a);
         const int per = (E + 31) / 32;
@@ -249,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 const PairTile p = decode<STAGE>(sm, a, t);
                 const int xrow = (rank == 1 && p.second) ? (p.mb0 + 1) * 128 : p.mb0 * 128;
                 const int wrow = rank == 0 ? p.wrow0 : p.wrow1;
-                for (int kb = 0; kb < nkb; ++kb) {
+                const int kb0 = STAGE == 5 ? p.kb0 : 0, kb1 = STAGE == 5 ? p.kb1 : nkb;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
                         ok = false;
                         break;
@@ -305,7 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccCols;
-                for (int kb = 0; kb < nkb; ++kb) {
+                int kb0 = 0, kb1 = nkb;
+                if (STAGE == 5) {
+                    const PairTile p = decode<STAGE>(sm, a, t);
+                    kb0 = p.kb0;
+                    kb1 = p.kb1;
+                }
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
                         ok = false;
                         break;
@@ -316,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_pair<QT>(d, smem_desc_sw128(xa + kk * 32), smem_desc_sw128(wb + kk * 32), idesc,
-                                     (kb > 0 || kk > 0) ? 1u : 0u);
+                                     (kb > kb0 || kk > 0) ? 1u : 0u);
                     any = true;
                     mma_commit_pair(&sm.empty[s], 0x3);
                     if (++s == kStages) {
@@ -394,11 +427,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     for (int i = 0; i < 32; ++i)
                         h[i] = silu(g[i]) * u[i];
                     store_bf16x32(dst + c0, h);
+                    if (a.gu) {  // training: keep the pre-activations for the backward
+                        __nv_bfloat16 *gr = a.gu + (size_t)pos * (2 * a.N) + p.ncol0 + c0;
+                        store_bf16x32(gr, g);
+                        store_bf16x32(gr + a.N, u);
+                    }
+                }
+            } else if (STAGE == 3) {
+                // backward of stage 2: dh in the accumulator; SwiGLU's backward with the saved g | u
+                const __nv_bfloat16 *gr = a.gu_in + (size_t)pos * (2 * a.N) + p.ncol0;
+                __nv_bfloat16 *dr = a.dgu + (size_t)pos * (2 * a.N) + p.ncol0;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    float dh[32], dg[32], du[32];
+                    tmem_ld32(tacc + c0, dh);
+                    if (!store)
+                        continue;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(gr + c0 + i);
+                        const uint4 uv = *reinterpret_cast<const uint4 *>(gr + a.N + c0 + i);
+                        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+                        const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const float2 gf = __bfloat1622float2(g2[q2]);
+                            const float2 uf = __bfloat1622float2(u2[q2]);
+                            const float gg[2] = {gf.x, gf.y}, uu[2] = {uf.x, uf.y};
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int ii = i + 2 * q2 + r;
+                                const float sg = 1.0f / (1.0f + __expf(-gg[r]));
+                                dg[ii] = dh[ii] * uu[r] * sg * (1.0f + gg[r] * (1.0f - sg));
+                                du[ii] = dh[ii] * gg[r] * sg;
+                            }
+                        }
+                    }
+                    store_bf16x32(dr + c0, dg);
+                    store_bf16x32(dr + a.N + c0, du);
+                }
+            } else if (STAGE == 5) {
+                // weight gradient: rows (mb0 + rank) * 128 + row of expert e's gradient
+                float *dst = a.dw_out + ((size_t)p.e * a.M + pos) * a.N + p.ncol0;
+                const int ncols = min(256, a.N - p.ncol0);
+                const bool empty = p.kb0 == p.kb1;  // an expert without tokens: zero gradient
+#pragma unroll 1
+                for (int c0 = 0; c0 < ncols; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = empty ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             } else {
                 const int slot = store ? a.sorted_ids[pos] : a.S;
                 const bool live = slot < a.S;
-                const float wgt = live ? a.sorted_weights[pos] * (QT ? a.x_scales[pos] : 1.0f) : 0.0f;
+                // no weights: the unweighted rows (the backward's dx per slot)
+                const float wgt =
+                    live ? (a.sorted_weights ? a.sorted_weights[pos] : 1.0f) * (QT ? a.x_scales[pos] : 1.0f) : 0.0f;
                 float *dst = a.y + (size_t)(live ? slot : 0) * a.N + p.ncol0;
                 const int ncols = min(256, a.N - p.ncol0);
 #pragma unroll 1
@@ -500,18 +588,30 @@ bool gemm_pair_supported(int E) { return E <= gemm2sm::kMaxE; }
 
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st)
 {
+    // stages 1, 2 (bf16 or per-token FP8); 3 and 5 (training, bf16): the backward of stage 2
+    // and the weight gradients
     int ncl = 0;
-    if (stage == 1)
-        ncl = qt ? gemm2sm::max_clusters<1, 1>() : gemm2sm::max_clusters<1, 0>();
-    else
-        ncl = qt ? gemm2sm::max_clusters<2, 1>() : gemm2sm::max_clusters<2, 0>();
+    switch (stage * 2 + (qt ? 1 : 0)) {
+    case 2: ncl = gemm2sm::max_clusters<1, 0>(); break;
+    case 3: ncl = gemm2sm::max_clusters<1, 1>(); break;
+    case 4: ncl = gemm2sm::max_clusters<2, 0>(); break;
+    case 5: ncl = gemm2sm::max_clusters<2, 1>(); break;
+    case 6: ncl = gemm2sm::max_clusters<3, 0>(); break;
+    case 10: ncl = gemm2sm::max_clusters<5, 0>(); break;
+    default: return cudaErrorInvalidValue;
+    }
     if (ncl <= 0)
         return cudaErrorInvalidConfiguration;
     if (max_pair_tiles < ncl)
         ncl = (int)(max_pair_tiles > 0 ? max_pair_tiles : 1);
-    if (stage == 1)
-        return qt ? gemm2sm::launch<1, 1>(a, ncl, st) : gemm2sm::launch<1, 0>(a, ncl, st);
-    return qt ? gemm2sm::launch<2, 1>(a, ncl, st) : gemm2sm::launch<2, 0>(a, ncl, st);
+    switch (stage * 2 + (qt ? 1 : 0)) {
+    case 2: return gemm2sm::launch<1, 0>(a, ncl, st);
+    case 3: return gemm2sm::launch<1, 1>(a, ncl, st);
+    case 4: return gemm2sm::launch<2, 0>(a, ncl, st);
+    case 5: return gemm2sm::launch<2, 1>(a, ncl, st);
+    case 6: return gemm2sm::launch<3, 0>(a, ncl, st);
+    default: return gemm2sm::launch<5, 0>(a, ncl, st);
+    }
 }
 
 }  // namespace moe

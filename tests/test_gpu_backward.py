@@ -93,3 +93,14 @@ def test_backward_reproducible(moe):
 def test_train_workspace_rejects_unsupported(moe):
     assert moe.moe_train_workspace_size(16, 256, 384, 4, 2) == 0   # I not a multiple of 256
     assert moe.moe_train_workspace_size(16, 256, 256, 4, 2) > 0
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[4]], ids=lambda c: c[0] + "_pairs")
+def test_backward_parity_cta_pairs(moe, case):
+    """The same gradients with the CTA-pair GEMMs forced (training forward, both backward GEMMs, and
+    the weight gradients whose row count is a multiple of 256)."""
+    moe.moe_set_gemm_pair(1)
+    try:
+        test_backward_parity(moe, case)
+    finally:
+        moe.moe_set_gemm_pair(-1)
