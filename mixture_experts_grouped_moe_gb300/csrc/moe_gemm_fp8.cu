@@ -5,7 +5,7 @@
 // Scales are fp32 per 128x128 weight block and per 1x128 activation group,
 // so they are not the power-of-two 32-element scales the tensor core applies
 // in hardware.  Each 128-wide K block is therefore accumulated on its own
-// by tcgen05.mma kind::f8f6f4 into one of two TMEM buffers, and sixteen
+// by tcgen05.mma kind::f8f6f4 into one of two TMEM buffers, and eight
 // promotion warps fold it into fp32 registers:
 //     acc[row][col] += D_kb[row][col] * s_x[row][kb] * s_w[col_block][kb]
 // while the tensor core fills the other buffer with the next K block.
@@ -13,15 +13,19 @@
 // stage 1 computes h = silu(gate) * up and re-quantises each 1x128 group of
 // h (scale = amax / 448); stage 2 scales rows by their top-k weight.
 //
-// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..17
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9
 // promotion/epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its quadrant)
-// and sub = (w-2)/4 picks a quarter of the 256 accumulator columns, so four
-// warps share each quadrant and hide each other's TMEM-load latency.  Tiles:
-// M = 128 sorted token rows, N = 256 weight rows (stage 1: 128 gate + the
-// matching 128 up rows; stage 2: 256 output features).  Each thread owns two
-// 32-column chunks: stage 1 gate columns [32s, 32s+32) and up columns
-// [128+32s, ...) so the SwiGLU pairs stay inside the thread; stage 2 columns
-// [64s, 64s+64).
+// and sub = (w-2)/4 picks half of the 256 accumulator columns, so two warps
+// share each quadrant.  Tiles: M = 128 sorted token rows, N = 256 weight rows
+// (stage 1: 128 gate + the matching 128 up rows; stage 2: 256 output
+// features).  Each thread owns two 64-column chunks: stage 1 gate columns
+// [64s, 64s+64) and up columns [128+64s, ...) so the SwiGLU pairs stay
+// inside the thread; stage 2 columns [128s, 128s+128).
+//
+// Eight warps with 16-column TMEM loads measured faster than sixteen warps
+// with 8-column loads (stage 1 of the Mixtral shapes at T=4096: 0.836 vs
+// 0.889 ms): sixteen warps leave 96 registers a thread, too few for wider
+// loads in flight next to 64 accumulators.
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -42,10 +46,10 @@ constexpr int kTmemCols = 2 * kAccCols;
 // the CTA's warps, so 2 + 16 warps leave 96 registers a thread (64 accumulators), and
 // 2 + 8 warps leave 168 (128 accumulators).
 #ifndef MOE_FP8_PROMO_WARPS
-#define MOE_FP8_PROMO_WARPS 16
+#define MOE_FP8_PROMO_WARPS 8
 #endif
 #ifndef MOE_FP8_LD_COLS
-#define MOE_FP8_LD_COLS 8
+#define MOE_FP8_LD_COLS 16
 #endif
 constexpr int kPromoWarps = MOE_FP8_PROMO_WARPS;
 constexpr int kLdCols = MOE_FP8_LD_COLS;    // TMEM columns per load (8 or 16), two loads per wait
@@ -66,7 +70,8 @@ struct __align__(1024) Smem {
     TileQueue tq;
     uint32_t tmem_base;
     int abort;
-    float amax[kSubs][128];
+    float amax[2][kSubs][128];  // per tile parity: row amax of each promotion warp's h chunk
+    uint64_t ep_bar[4];         // per lane quadrant: one phase per tile once every warp wrote its amax
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -75,11 +80,6 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 // tile, so it uses the fast reciprocal-based division (at most 2 ulp from the rounded
 // quotient; h is re-quantised to 3 mantissa bits right after).
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
-__device__ __forceinline__ void named_bar(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 struct Tile {
     int e, xrow, wrow0, wrow1, ncol0;
@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
         mbar_init(&sm.drain, 1);
         tq_init(sm.tq, 1 + kPromoWarps);
         sm.abort = 0;
+        for (int i = 0; i < 4; ++i)
+            mbar_init(&sm.ep_bar[i], 32 * kSubs);
         fence_mbarrier_init();
         tma_prefetch_desc(&a.tm_x);
         tma_prefetch_desc(&a.tm_w);
@@ -221,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 if (t < 0)
                     break;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&sm.tempty[buf], bph ^ 1, a.status, abort_flag) ||
-                        !mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
+                    // the stage is normally loaded long before its TMEM buffer is released, so
+                    // waiting on it first leaves only the MMA issue after the release
+                    if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag) ||
+                        !mbar_wait(&sm.tempty[buf], bph ^ 1, a.status, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -269,35 +273,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
         bool ok = true;
         int qs = 0;
         uint32_t qph = 0;
-        for (;;) {
-            int t = -1;
+        const int nrb = a.E * a.rows_per_expert / 128;
+        // Next tile and the first scales of its K loop.  The next tile is taken from the queue
+        // right after the last K block of the current one, before its epilogue, so the
+        // dependent global loads (expert id, then scales) overlap the epilogue.
+        int t = -1;
+        Tile tl{};
+        int pos = 0;
+        const float *sw0 = nullptr, *sw1 = nullptr;
+        float sx_n = 0.0f, s0_n = 0.0f, s1_n = 0.0f;
+        auto next_tile = [&]() -> bool {
             bool qok = tq_pop(sm.tq, qs, qph, t, a.status, abort_flag);
             qok = __all_sync(0xffffffffu, qok);
             if (!qok)
-                break;
+                return false;
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.tq.empty[qs]);
             tq_advance(qs, qph);
-            if (t < 0)
-                break;
-            const Tile tl = get_tile<STAGE>(a, t, nmb, nnt);
-            const int pos = tl.xrow + row;
-            // weight-scale rows of this thread's two column chunks; a stage-2 chunk past the last
-            // output feature (H % 256 == 128) reads a valid row and is never stored
-            const int nrb = a.E * a.rows_per_expert / 128;
-            int rb0 = (STAGE == 1 ? tl.wrow0 : tl.wrow0 + sub * 64) / 128;
-            int rb1 = (STAGE == 1 ? tl.wrow1 : tl.wrow0 + sub * 64) / 128;
-            rb0 = rb0 < nrb ? rb0 : nrb - 1;
-            rb1 = rb1 < nrb ? rb1 : nrb - 1;
-            const float *sw0 = a.w_scales + (size_t)rb0 * KB128;
-            const float *sw1 = a.w_scales + (size_t)rb1 * KB128;
+            if (t >= 0) {
+                tl = get_tile<STAGE>(a, t, nmb, nnt);
+                pos = tl.xrow + row;
+                // weight-scale rows of this thread's two column chunks; a stage-2 chunk past the
+                // last output feature (H % 256 == 128) reads a valid row and is never stored
+                int rb0 = (STAGE == 1 ? tl.wrow0 : tl.wrow0 + sub * 2 * kChunk) / 128;
+                int rb1 = (STAGE == 1 ? tl.wrow1 : tl.wrow0 + sub * 2 * kChunk) / 128;
+                rb0 = rb0 < nrb ? rb0 : nrb - 1;
+                rb1 = rb1 < nrb ? rb1 : nrb - 1;
+                sw0 = a.w_scales + (size_t)rb0 * KB128;
+                sw1 = a.w_scales + (size_t)rb1 * KB128;
+                sx_n = a.x_scales[pos];
+                s0_n = sw0[0];
+                s1_n = sw1[0];
+            }
+            return true;
+        };
+        int gen = 0;  // epilogues done by this warp
+        if (!next_tile())
+            t = -1;
+        while (t >= 0) {
             float acc0[kChunk], acc1[kChunk];
 #pragma unroll
             for (int i = 0; i < kChunk; ++i)
                 acc0[i] = 0.0f, acc1[i] = 0.0f;
             // the scales of block kb+1 are fetched while block kb is still on the tensor core
-            float sx_n = a.x_scales[pos], s0_n = sw0[0], s1_n = sw1[0];
             for (int kb = 0; kb < nkb; ++kb) {
                 const float sx = sx_n, s0 = s0_n, s1 = s1_n;
                 if (kb + 1 < nkb) {
@@ -340,26 +359,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
             }
             if (!ok)
                 break;
+            const Tile ctl = tl;
+            const int cpos = pos;
+            // stage 1 takes the next tile now, so that its expert id and first scales load during
+            // the long SwiGLU epilogue; stage 2 (short epilogue) takes it afterwards
+            if (STAGE == 1 && !next_tile()) {
+                ok = false;
+                t = -1;
+            }
+            ++gen;
             if (STAGE == 1) {
-                // h for columns ncol0 + sub*32 + i; one 1x128 group spans the quadrant's 4 warps
+                // h for columns ncol0 + sub*kChunk + i; one 1x128 group spans the quadrant's
+                // kSubs warps, which exchange their row amax through shared memory and a bounded
+                // mbarrier wait (a named barrier would hang a warp whose partner left on an
+                // abort).  The slot alternates with the tile: a warp can be at most one tile
+                // ahead of its partners.
                 float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
                     acc0[i] = silu(acc0[i]) * acc1[i];
                     amax = fmaxf(amax, fabsf(acc0[i]));
                 }
-                sm.amax[sub][row] = amax;
-                named_bar(1 + q, 32 * kSubs);
+                sm.amax[gen & 1][sub][row] = amax;
+                mbar_arrive(&sm.ep_bar[q]);
+                bool x_ok = mbar_wait(&sm.ep_bar[q], (uint32_t)(gen - 1) & 1u, a.status, abort_flag);
+                x_ok = __all_sync(0xffffffffu, x_ok);
+                if (!x_ok)
+                    break;
 #pragma unroll
                 for (int s2 = 0; s2 < kSubs; ++s2)
-                    amax = fmaxf(amax, sm.amax[s2][row]);
-                named_bar(1 + q, 32 * kSubs);
+                    amax = fmaxf(amax, sm.amax[gen & 1][s2][row]);
                 const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
                 // codes = RNE(h * (1/sc)) two at a time; the product can differ from h / sc in the
                 // last fp32 bit, which moves a code only for a quotient within that bit of an e4m3
                 // rounding midpoint
                 const float isc = 1.0f / sc;
-                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)pos * a.N + tl.ncol0 + sub * kChunk;
+                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)cpos * a.N + ctl.ncol0 + sub * kChunk;
 #pragma unroll
                 for (int v = 0; v < kChunk / 16; ++v) {
                     uint32_t w[4];
@@ -375,12 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                     reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 if (sub == 0)
-                    a.inter_scales[(size_t)(tl.ncol0 / 128) * a.P_max + pos] = sc;
+                    a.inter_scales[(size_t)(ctl.ncol0 / 128) * a.P_max + cpos] = sc;
             } else {
-                const int slot = a.sorted_ids[pos];
+                const int slot = a.sorted_ids[cpos];
                 if (slot < a.S) {
-                    const float wgt = a.sorted_weights[pos];
-                    const int n0 = tl.ncol0 + sub * 2 * kChunk;
+                    const float wgt = a.sorted_weights[cpos];
+                    const int n0 = ctl.ncol0 + sub * 2 * kChunk;
                     float *dst = a.y + (size_t)slot * a.N + n0;
                     if (n0 < a.N) {
 #pragma unroll
@@ -393,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                                 make_float4(wgt * acc1[i], wgt * acc1[i + 1], wgt * acc1[i + 2], wgt * acc1[i + 3]);
                     }
                 }
+                if (!next_tile())
+                    t = -1;
             }
         }
     }
