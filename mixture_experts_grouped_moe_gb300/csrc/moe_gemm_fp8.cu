@@ -72,6 +72,7 @@ struct __align__(1024) Smem {
     int abort;
     float amax[2][kSubs][128];  // per tile parity: row amax of each promotion warp's h chunk
     uint64_t ep_bar[4];         // per lane quadrant: one phase per tile once every warp wrote its amax
+    float4 ep_out[kPromoWarps][32][4];  // stage 2: a warp's 32 rows x 16 columns on their way to y
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -420,20 +421,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 if (sub == 0)
                     a.inter_scales[(size_t)(ctl.ncol0 / 128) * a.P_max + cpos] = sc;
             } else {
+                // Each lane holds one row; stored straight from registers, every store instruction
+                // would touch 32 rows of y (32 cache lines).  Blocks of 16 columns go through a
+                // per-warp shared buffer instead (float4 slot j of row r at j ^ ((r >> 1) & 3), free
+                // of bank conflicts both ways) and leave as 8 rows x 64 contiguous bytes.
                 const int slot = a.sorted_ids[cpos];
-                if (slot < a.S) {
-                    const float wgt = a.sorted_weights[cpos];
-                    const int n0 = ctl.ncol0 + sub * 2 * kChunk;
-                    float *dst = a.y + (size_t)slot * a.N + n0;
-                    if (n0 < a.N) {
+                const float wgt = slot < a.S ? a.sorted_weights[cpos] : 0.0f;
+                const int n0 = ctl.ncol0 + sub * 2 * kChunk;
+                float4(*buf)[4] = sm.ep_out[warp - 2];
+                const int rr = lane >> 2, cq = lane & 3;  // read side: row within 8, float4 column
+                if (n0 < a.N) {
 #pragma unroll
-                        for (int i = 0; i < kChunk; i += 4)
-                            *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(wgt * acc0[i], wgt * acc0[i + 1], wgt * acc0[i + 2], wgt * acc0[i + 3]);
+                    for (int blk = 0; blk < 2 * kChunk / 16; ++blk) {
+                        const float *v = blk < kChunk / 16 ? &acc0[blk * 16] : &acc1[blk * 16 - kChunk];
 #pragma unroll
-                        for (int i = 0; i < kChunk; i += 4)
-                            *reinterpret_cast<float4 *>(dst + kChunk + i) =
-                                make_float4(wgt * acc1[i], wgt * acc1[i + 1], wgt * acc1[i + 2], wgt * acc1[i + 3]);
+                        for (int j = 0; j < 4; ++j)
+                            buf[lane][j ^ ((lane >> 1) & 3)] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1],
+                                                                           wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int r = 8 * it + rr;
+                            const int rslot = __shfl_sync(0xffffffffu, slot, r);
+                            const float4 o = buf[r][cq ^ ((r >> 1) & 3)];
+                            if (rslot < a.S)
+                                *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 16 + 4 * cq) = o;
+                        }
+                        __syncwarp();
                     }
                 }
                 if (!next_tile())
