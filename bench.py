@@ -330,10 +330,13 @@ def host_inputs(cfg, device):
 def launches_per_step(cfg, one_stage=False):
     """Kernels the library launches per forward: router (+ top-k pass for large T*E), sort
     (one launch up to 1024 slots, else three), gather, stage 1 (+ the per-token re-quantisation
-    of h), stage 2 (or one launch for both stages), combine."""
+    of h), stage 2, combine; the one-kernel decode path replaces gather, stage 1 and stage 2 by
+    one launch that fetches the token rows itself."""
     router = 2 if cfg.T * cfg.E > 4096 else 1
     sort = 1 if cfg.T * cfg.k <= 1024 else 3
-    return router + sort + 4 + (1 if cfg.dtype == "fp8_token" else 0) - (1 if one_stage else 0)
+    if one_stage:
+        return router + sort + 2
+    return router + sort + 4 + (1 if cfg.dtype == "fp8_token" else 0)
 
 
 def workload_desc(cfg):

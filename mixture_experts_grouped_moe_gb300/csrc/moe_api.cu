@@ -353,8 +353,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     const int64_t P = p.max_padded;
     const int eb = (dtype == MOE_BF16) ? 2 : 1;
-    cudaError_t ge;
-    if (dtype == MOE_BF16)
+    // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
+    // itself (no gather pass)
+    const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled() && !train;
+    cudaError_t ge = cudaSuccess;
+    if (fused) {
+        // nothing to gather
+    } else if (dtype == MOE_BF16)
         ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
                                 static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_enabled(kPdlGather), st);
     else if (dtype == MOE_FP8_TOKEN)
@@ -430,13 +435,15 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     const int64_t e_act = (S < E) ? S : E;
     cudaError_t ce;
 
-    if (p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled() && !train) {
+    if (fused) {
         // both stages in one persistent launch (status[1]: tile claims, status[3]: h written)
         FusedArgs F;
         F.s1 = g1;
         F.s2 = g2;
         F.tile_counter = status + 1;
         F.h_done = status + 3;
+        F.x = static_cast<const __nv_bfloat16 *>(x);
+        F.k = k;
         const int64_t ub = e_act * ((I / 128) + nt2 * p.split_k2);
         ce = launch_fused_decode(F, (int)(ub < nsm ? ub : nsm), st);
         if (ce != cudaSuccess)

@@ -42,6 +42,7 @@ struct __align__(1024) Smem {
     TileQueue tq;
     uint32_t tmem_base;
     int abort;
+    int xtok[kXRows];  // stage-1 tile: token of each sorted row, -1 for padding
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.full[i], 1 + 32);  // TMA bytes + the producer lanes' token-row copies
             mbar_init(&sm.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -157,70 +158,111 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
     const int h_target = n1 * kEpiWarps;  // epilogue warps of all stage-1 tiles
 
     if (warp == 0) {
-        // ---------------------------------------------------- TMA producer
-        if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
-            int s = 0;
-            uint32_t ph = 0;
-            int issued[kStages];
-            uint32_t issued_ph[kStages];
-            for (int i = 0; i < kStages; ++i)
-                issued[i] = 0, issued_ph[i] = 0;
-            bool ok = true, h_ready = false;
-            int qs = 0;
-            uint32_t qph = 0;
-            int claim = -2;
-            for (;;) {
-                int t;
-                if (!tq_push_next(sm.tq, qs, qph, F.tile_counter, ntiles, claim, t, status, abort_flag)) {
+        // ------------------------------------------------- producer (whole warp)
+        // Lane 0 claims tiles and issues the weight loads (and stage 2's h rows) by TMA.  The
+        // token rows of a stage-1 tile come straight from x: the 32 lanes copy them in 16-byte
+        // pieces (cp.async) into the 128-byte-swizzled layout a TMA load would have produced
+        // (16-byte chunk c of row r at chunk c ^ (r % 8)), zero-filled for padding rows, so no
+        // gather pass runs before this kernel.  Each lane's copies complete on the stage
+        // barrier (1 + 32 arrivals per phase).
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_x = l2_policy_evict_last();
+        int s = 0;
+        uint32_t ph = 0;
+        int issued[kStages];
+        uint32_t issued_ph[kStages];
+        for (int i = 0; i < kStages; ++i)
+            issued[i] = 0, issued_ph[i] = 0;
+        bool ok = true, h_ready = false;
+        int qs = 0;
+        uint32_t qph = 0;
+        int claim = -2;
+        const int H = F.s1.K;
+        for (;;) {
+            int t = -1;
+            bool qok = true;
+            if (lane == 0)
+                qok = tq_push_next(sm.tq, qs, qph, F.tile_counter, ntiles, claim, t, status, abort_flag);
+            qok = __shfl_sync(0xffffffffu, (int)qok, 0) != 0;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (!qok) {
+                ok = false;
+                break;
+            }
+            if (t < 0)
+                break;
+            const Tile tl = get_tile(F, t, n1);
+            const GemmArgs &a = tl.stage == 1 ? F.s1 : F.s2;
+            if (tl.stage == 1) {
+                __syncwarp();  // the previous tile's copies have all been issued
+                for (int r = lane; r < tl.nx; r += 32) {
+                    const int slot = a.sorted_ids[tl.xrow + r];
+                    sm.xtok[r] = slot < a.S ? slot / F.k : -1;
+                }
+                __syncwarp();
+            }
+            const uint32_t bytes = tl.stage == 1 ? kWBytes : kWBytes + tl.nx * 128;
+            for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+                bool w_ok = mbar_wait(&sm.empty[s], ph ^ 1, status, abort_flag);
+                w_ok = __all_sync(0xffffffffu, w_ok);
+                if (!w_ok) {
                     ok = false;
                     break;
                 }
-                if (t < 0)
-                    break;
-                const Tile tl = get_tile(F, t, n1);
-                const GemmArgs &a = tl.stage == 1 ? F.s1 : F.s2;
-                const uint32_t bytes = kWBytes + tl.nx * 128;
-                for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-                    if (!mbar_wait(&sm.empty[s], ph ^ 1, status, abort_flag)) {
-                        ok = false;
-                        break;
+                uint8_t *wdst = sm.stage[s];
+                uint8_t *xdst = sm.stage[s] + kWBytes;
+                if (tl.stage == 1) {
+                    for (int j = lane; j < tl.nx * 8; j += 32) {
+                        const int r = j >> 3, c = j & 7;
+                        const int tok = sm.xtok[r];
+                        const __nv_bfloat16 *src = F.x + (size_t)(tok < 0 ? 0 : tok) * H + kb * 64 + c * 8;
+                        cp_async_16_zfill(xdst + r * 128 + ((c ^ (r & 7)) << 4), src, tok >= 0);
                     }
-                    uint8_t *wdst = sm.stage[s];
-                    uint8_t *xdst = sm.stage[s] + kWBytes;
+                }
+                if (lane == 0) {
                     mbar_arrive_expect_tx(&sm.full[s], bytes);
                     tma_load_2d(wdst, &a.tm_w, kb * 64, tl.wrow0, &sm.full[s], pol_w);
                     tma_load_2d(wdst + kWBytes / 2, &a.tm_w, kb * 64, tl.wrow1, &sm.full[s], pol_w);
                     issued[s] = 1;
                     issued_ph[s] = ph;
-                    if (tl.stage == 2 && !h_ready) {
+                }
+                if (tl.stage == 2) {
+                    if (!h_ready) {
                         // h is written by every stage-1 epilogue: wait for all of them once
-                        if (!wait_count(F.h_done, h_target, status, abort_flag)) {
+                        bool h_ok = true;
+                        if (lane == 0) {
+                            h_ok = wait_count(F.h_done, h_target, status, abort_flag);
+                            if (h_ok)
+                                asm volatile("fence.proxy.async.global;" ::: "memory");
+                        }
+                        h_ok = __shfl_sync(0xffffffffu, (int)h_ok, 0) != 0;
+                        if (!h_ok) {
                             ok = false;
                             break;
                         }
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
                         h_ready = true;
                     }
-                    for (int c = 0; c < tl.nx; c += 16)
-                        tma_load_2d(xdst + c * 128, &a.tm_x, kb * 64, tl.xrow + c, &sm.full[s], pol_x);
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1;
+                    if (lane == 0)
+                        for (int c = 0; c < tl.nx; c += 16)
+                            tma_load_2d(xdst + c * 128, &a.tm_x, kb * 64, tl.xrow + c, &sm.full[s], pol_x);
+                }
+                cp_async_arrive(&sm.full[s]);
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (!ok)
+                break;
+        }
+        cp_async_wait_all();
+        if (!ok && lane == 0) {
+            for (int i = 0; i < kStages; ++i)
+                if (issued[i]) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait(&sm.full[i], issued_ph[i]) && global_timer_ns() - t0 < 100000000ull) {
                     }
                 }
-                if (!ok)
-                    break;
-            }
-            if (!ok) {
-                for (int i = 0; i < kStages; ++i)
-                    if (issued[i]) {
-                        const unsigned long long t0 = global_timer_ns();
-                        while (!mbar_try_wait(&sm.full[i], issued_ph[i]) && global_timer_ns() - t0 < 100000000ull) {
-                        }
-                    }
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -256,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
                         break;
                     }
                     tc_fence_after();
+                    fence_proxy_async_smem();  // the token-row copies (generic proxy) before the MMAs read them
                     const uint8_t *w = sm.stage[s];
                     const uint8_t *xs = sm.stage[s] + kWBytes;
 #pragma unroll

@@ -173,6 +173,8 @@ struct FusedArgs {
     GemmArgs s1, s2;
     int *tile_counter;
     int *h_done;
+    const __nv_bfloat16 *x;  // the layer input [T][H]: stage-1 token rows are fetched from it directly
+    int k;                   // top-k (slot s belongs to token s / k)
 };
 cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st);
 // Training (bf16): backward GEMMs -- which = 3: dh = dY W_down with

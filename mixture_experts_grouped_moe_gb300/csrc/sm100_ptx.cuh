@@ -219,6 +219,15 @@ __device__ __forceinline__ void cp_async_8(void *dst, const void *src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared; with valid == false the 16 bytes are zero-filled
+// and nothing is read.
+__device__ __forceinline__ void cp_async_16_zfill(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
