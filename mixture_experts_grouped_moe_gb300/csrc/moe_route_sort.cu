@@ -467,6 +467,86 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
         o.sorted_expert_ids[b] = -1;
 }
 
+// Few experts (E <= 32) and small S: the same outputs as sort_small_kernel, with the
+// per-expert counts scanned by one warp's shuffles instead of a 1024-thread block scan
+// (twenty block barriers), so the CTA is 256 threads.  Every decode step runs it.
+__global__ void __launch_bounds__(256) sort_few_kernel(const int32_t *__restrict__ ids,
+                                                       const float *__restrict__ wts, int S, int E, int B,
+                                                       int64_t P_max, int64_t NB_max, SortOut o)
+{
+    __shared__ int32_t s_ids[kSmallSort];
+    __shared__ float s_w[kSmallSort];
+    __shared__ int s_total;
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        s_ids[i] = ids[i];
+        s_w[i] = wts[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int e = threadIdx.x;
+        int cnt = 0;
+        if (e < E)
+            for (int s = 0; s < S; ++s)
+                cnt += (s_ids[s] == e);
+        const int pad = (e < E) ? (cnt + B - 1) / B * B : 0;
+        const int act = (e < E && cnt > 0) ? 1 : 0;
+        int ipad = pad, iact = act;  // inclusive scans over the experts
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int vp = __shfl_up_sync(0xffffffffu, ipad, d);
+            const int va = __shfl_up_sync(0xffffffffu, iact, d);
+            if (e >= d) {
+                ipad += vp;
+                iact += va;
+            }
+        }
+        const int off = ipad - pad;
+        const int total = __shfl_sync(0xffffffffu, ipad, 31);
+        const int nact = __shfl_sync(0xffffffffu, iact, 31);
+        if (e < E) {
+            if (o.expert_counts)
+                o.expert_counts[e] = cnt;
+            if (o.expert_offsets)
+                o.expert_offsets[e] = off;
+            if (o.active_experts && cnt > 0)
+                o.active_experts[iact - 1] = e;
+            int pos = off;
+            for (int s = 0; s < S; ++s)
+                if (s_ids[s] == e) {
+                    o.sorted_ids[pos] = s;
+                    o.sorted_weights[pos] = s_w[s];
+                    if (o.slot_pos)
+                        o.slot_pos[s] = pos;
+                    ++pos;
+                }
+            for (; pos < off + pad; ++pos) {
+                o.sorted_ids[pos] = S;
+                o.sorted_weights[pos] = 0.0f;
+            }
+            for (int b = off / B; b < (off + pad) / B; ++b)
+                o.sorted_expert_ids[b] = e;
+        }
+        if (e == 0) {
+            *o.num_post_padded = total;
+            if (o.expert_offsets)
+                o.expert_offsets[E] = total;
+            if (o.num_active)
+                *o.num_active = nact;
+            s_total = total;
+        }
+    }
+    __syncthreads();
+    const int total = s_total;
+    for (int64_t i = total + threadIdx.x; i < P_max; i += blockDim.x) {
+        o.sorted_ids[i] = S;
+        o.sorted_weights[i] = 0.0f;
+    }
+    for (int64_t b = total / B + threadIdx.x; b < NB_max; b += blockDim.x)
+        o.sorted_expert_ids[b] = -1;
+}
+
 __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restrict__ ids, int S, int E,
                                                          int32_t *__restrict__ cc,
                                                          int32_t *__restrict__ sorted_ids,
@@ -577,6 +657,9 @@ cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k
     const int S = T * k;
     const int64_t P_max = (int64_t)S + (int64_t)E * block_m - k;
     const int64_t NB_max = (P_max + block_m - 1) / block_m;
+    if (S <= kSmallSort && E <= 32)
+        return launch_kernel(pdl, sort_few_kernel, dim3(1), dim3(256), 0, st, ids, wts, S, E, block_m, P_max,
+                             NB_max, o);
     if (S <= kSmallSort)
         return launch_kernel(pdl, sort_small_kernel, dim3(1), dim3(1024), 0, st, ids, wts, S, E, block_m, P_max,
                              NB_max, o);

@@ -132,8 +132,11 @@ def test_router_parity(moe, cfg):
 
 # ------------------------------------------------------------ align-sort
 
+# single-CTA sorts: S <= 1024 with E <= 32 (one-warp scan) and with E > 32 (block scan), each at
+# its limits; then the three-launch sort
 SORT_CASES = [(16, 2, 4, 16), (32, 2, 8, 16), (8192, 2, 8, 128), (4096, 8, 256, 128), (1, 1, 1, 1),
-              (3, 2, 3, 4), (700, 3, 1000, 32), (5000, 1, 7, 64), (2049, 4, 16, 128)]
+              (3, 2, 3, 4), (700, 3, 1000, 32), (5000, 1, 7, 64), (2049, 4, 16, 128),
+              (512, 2, 32, 16), (100, 4, 64, 16), (128, 8, 256, 32)]
 
 
 @pytest.mark.parametrize("T,k,E,B", SORT_CASES)
