@@ -71,7 +71,7 @@ bool pdl_enabled(int site, bool grouped)
     }();
     int mask = env_mask;
     if (mask < 0)
-        mask = grouped ? 0x3f & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : 0x3f;
+        mask = grouped ? 0x7f & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : 0x7f;
     return (mask >> site) & 1;
 }
 
@@ -329,10 +329,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     mark(0, st);
     int32_t *topk_ids = static_cast<int32_t *>(at(L.topk_ids));
     float *topk_w = static_cast<float *>(at(L.topk_w));
-    // the first kernel follows arbitrary caller work: a normal launch; it also zeroes the status word
+    // The first kernel follows arbitrary caller work.  With programmatic dependent launch it
+    // still waits (griddepcontrol.wait) for the preceding kernel to complete before it reads x or
+    // zeroes the status words; it only starts early after a kernel that triggers its dependents,
+    // such as the previous call's combine.
     if (launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
-                      router_bias, T, H, E, k, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status, false,
-                      st) != cudaSuccess)
+                      router_bias, T, H, E, k, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status,
+                      pdl_enabled(kPdlRouter), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     mark(1, st);
 

@@ -39,6 +39,9 @@ enum PdlSite {
     kPdlStage2 = 3,   // stage 1 -> stage 2
     kPdlCombine = 4,  // stage 2 -> combine
     kPdlTopk = 5,     // logit pass -> top-k pass
+    kPdlRouter = 6,   // whatever precedes the layer -> router (the router waits for its completion
+                      // before reading anything; it starts early only after a kernel that
+                      // triggers, such as the previous layer call's combine)
 };
 // Whether launches at this site use programmatic serialisation: environment
 // MOE_PDL=0 turns it off everywhere, MOE_PDL_MASK (hex) selects sites.
