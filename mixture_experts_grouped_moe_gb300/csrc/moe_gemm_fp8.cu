@@ -59,6 +59,7 @@ constexpr int kThreads = 64 + 32 * kPromoWarps;
 static_assert(kLdCols == 8 || kLdCols == 16, "TMEM load width");
 constexpr int kGroupM = 16;
 static_assert(kChunk * 2 * kSubs == 256, "the quadrant's warps cover the 256 accumulator columns");
+static_assert(kChunk == 64, "the epilogue stores move 64-byte (stage 1) and 16-column (stage 2) row pieces");
 
 struct __align__(1024) Smem {
     uint8_t stage[kStages][kStageBytes];
@@ -403,7 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 // last fp32 bit, which moves a code only for a quotient within that bit of an e4m3
                 // rounding midpoint
                 const float isc = 1.0f / sc;
-                uint8_t *dst = static_cast<uint8_t *>(a.inter) + (size_t)cpos * a.N + ctl.ncol0 + sub * kChunk;
+                // 64 code bytes per row: through the warp's shared block (same swizzle as stage 2)
+                // so that each store writes 8 rows x 64 contiguous bytes instead of 32 rows
+                float4(*buf)[4] = sm.ep_out[warp - 2];
 #pragma unroll
                 for (int v = 0; v < kChunk / 16; ++v) {
                     uint32_t w[4];
@@ -416,8 +419,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                             __nv_cvt_float2_to_fp8x2(make_float2(e[2] * isc, e[3] * isc), __NV_SATFINITE, __NV_E4M3);
                         w[j] = lo | (hi << 16);
                     }
-                    reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    buf[lane][v ^ ((lane >> 1) & 3)] = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]),
+                                                                   __uint_as_float(w[2]), __uint_as_float(w[3]));
                 }
+                __syncwarp();
+                {
+                    const int rr = lane >> 2, cq = lane & 3;
+                    const int row0 = ctl.xrow + q * 32;  // sorted row of the warp's lane 0
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int r = 8 * it + rr;
+                        const float4 o = buf[r][cq ^ ((r >> 1) & 3)];
+                        *reinterpret_cast<float4 *>(static_cast<uint8_t *>(a.inter) + (size_t)(row0 + r) * a.N +
+                                                    ctl.ncol0 + sub * kChunk + 16 * cq) = o;
+                    }
+                }
+                __syncwarp();
                 if (sub == 0)
                     a.inter_scales[(size_t)(ctl.ncol0 / 128) * a.P_max + cpos] = sc;
             } else {
