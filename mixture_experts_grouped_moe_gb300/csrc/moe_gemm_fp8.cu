@@ -43,20 +43,13 @@ constexpr int kStageBytes = kWBytes + kXBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 2 * kAccCols;
 // Register budget: each SM sub-partition holds 16K registers and gets ceil(warps/4) of
-// the CTA's warps, so 2 + 16 warps leave 96 registers a thread (64 accumulators), and
-// 2 + 8 warps leave 168 (128 accumulators).
-#ifndef MOE_FP8_PROMO_WARPS
-#define MOE_FP8_PROMO_WARPS 8
-#endif
-#ifndef MOE_FP8_LD_COLS
-#define MOE_FP8_LD_COLS 16
-#endif
-constexpr int kPromoWarps = MOE_FP8_PROMO_WARPS;
-constexpr int kLdCols = MOE_FP8_LD_COLS;    // TMEM columns per load (8 or 16), two loads per wait
+// the CTA's warps, so 2 + 8 warps leave 168 registers a thread: 128 accumulators and two
+// 16-column TMEM loads in flight (2 + 16 warps would leave 96).
+constexpr int kPromoWarps = 8;
+constexpr int kLdCols = 16;                 // TMEM columns per load, two loads per wait
 constexpr int kSubs = kPromoWarps / 4;      // promotion warps per TMEM lane quadrant
 constexpr int kChunk = 256 / (2 * kSubs);   // columns per chunk, two chunks per thread
 constexpr int kThreads = 64 + 32 * kPromoWarps;
-static_assert(kLdCols == 8 || kLdCols == 16, "TMEM load width");
 constexpr int kGroupM = 16;
 static_assert(kChunk * 2 * kSubs == 256, "the quadrant's warps cover the 256 accumulator columns");
 static_assert(kChunk == 64, "the epilogue stores move 64-byte (stage 1) and 16-column (stage 2) row pieces");
