@@ -694,16 +694,24 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
     pdl_trigger();
     const int rows = *npp;
     const int nvec = H / 8;
+    constexpr int U = 4;  // 16-byte pieces a thread requests before storing any (H <= 8192 in one round)
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
         const int s = sorted_ids[i];
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)i * H);
-        if (s < S) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s / k) * H);
-            for (int c = threadIdx.x; c < nvec; c += blockDim.x)
-                dst[c] = __ldg(src + c);
-        } else {
-            for (int c = threadIdx.x; c < nvec; c += blockDim.x)
-                dst[c] = make_uint4(0, 0, 0, 0);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s < S ? s / k : 0) * H);
+        for (int c0 = threadIdx.x; c0 < nvec; c0 += U * blockDim.x) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x;
+                v[u] = (s < S && c < nvec) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x;
+                if (c < nvec)
+                    dst[c] = v[u];
+            }
         }
     }
 }
@@ -804,19 +812,28 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
     pdl_trigger();
     const int rows = *npp;
     const int nvec = H / 8;
+    constexpr int U = 2;  // 16-byte pieces a thread requests before encoding any (H <= 4096 in one round)
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
         const int s = sorted_ids[i];
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s < S ? s / k : 0) * H);
-        for (int c0 = 0; c0 < nvec; c0 += blockDim.x) {
-            const int c = c0 + threadIdx.x;
-            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (c < nvec && s < S)
-                bf16x8_to_float(__ldg(src + c), f);
-            const float sc = group_scale(seg16_max(absmax8(f)));
-            if (c < nvec) {
-                reinterpret_cast<uint2 *>(q + (size_t)i * H)[c] = encode8(f, sc);
-                if ((c & 15) == 0)
-                    sT[(size_t)(c / 16) * P_max + i] = sc;
+        for (int c0 = 0; c0 < nvec; c0 += U * blockDim.x) {
+            uint4 raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                raw[u] = (c < nvec && s < S) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * blockDim.x + threadIdx.x;
+                float f[8];
+                bf16x8_to_float(raw[u], f);  // zero pieces past the row or for padding convert to 0
+                const float sc = group_scale(seg16_max(absmax8(f)));
+                if (c < nvec) {
+                    reinterpret_cast<uint2 *>(q + (size_t)i * H)[c] = encode8(f, sc);
+                    if ((c & 15) == 0)
+                        sT[(size_t)(c / 16) * P_max + i] = sc;
+                }
             }
         }
     }
