@@ -91,11 +91,13 @@ static int pair_mode()
 }
 
 // Automatic rule (same-box measurements on GB300): pairs pay off once the
-// average active expert holds at least 4 token blocks (a half-used pair at an
-// expert's end then wastes at most 1/8 of its tiles); for per-token FP8 only
-// stage 2 gains (Mixtral shapes, T=4096: stage 2 0.49 -> 0.42 ms, stage 1
-// 0.77 -> 0.83 ms), for bf16 both stages (T=8192: 2.45 -> 2.31 and
-// 1.38 -> 1.16 ms).
+// average active expert holds one token block (S >= 128 per expert, E standing
+// in for the active count): bf16 Mixtral shapes, one-SM vs pairs, T=512
+// 0.656 -> 0.637 ms, T=1024 0.815 -> 0.744, T=2048 1.222 -> 1.186, T=8192
+// stage 1 2.45 -> 2.31 and stage 2 1.38 -> 1.16 ms; the fine-grained E=256
+// workload (2.4 blocks per active expert) is even (4.110 vs 4.123 ms).  For
+// per-token FP8 only stage 2 gains (Mixtral shapes, T=4096: stage 2
+// 0.49 -> 0.42 ms, stage 1 0.77 -> 0.83 ms).
 // One-kernel decode (bf16 swap mode): 1 on (the default: same-box Mixtral
 // decode 0.4355 -> 0.4307 ms per step), 0 off; MOE_ONE_STAGE=0 in the
 // environment sets the start value, moe_set_one_stage overrides it.
@@ -121,7 +123,7 @@ static bool use_pair(int dtype, int stage, int T, int k, int E)
         return m == 1;
     const int64_t S = (int64_t)T * k;
     const int64_t act = S < E ? S : E;
-    if (S < 4 * 128 * act)
+    if (S < 128 * act)
         return false;
     return dtype == MOE_BF16 || stage == 2;
 }
