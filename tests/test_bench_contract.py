@@ -1,0 +1,70 @@
+"""bench.py's output contract and host-side accounting (CPU only).
+
+The reference arm (the CPU oracle timed on the host cores) prints the same
+JSON line as the CUDA arm; its keys and types are checked here.  The helper
+that counts the library's launches per forward and the rule that reports ncu
+traffic only for unchanged kernel sources are checked on their own.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from mixture_experts_grouped_moe_gb300 import synth  # noqa: E402
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.strip().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC
+    for key, typ in (("value", float), ("ms_per_step", float), ("n_gpus", int), ("steps", int), ("warmup", int)):
+        assert isinstance(d[key], typ), key
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["steps"] == 1 and d["warmup"] >= 3
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["config"]["workload"].startswith("mixtral_decode")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_launches_per_step():
+    # decode, one-kernel path: router, sort, both GEMM stages with the token-row fetch, combine
+    assert bench.launches_per_step(synth.CONFIGS["mixtral_decode"], one_stage=True) == 4
+    # two launches for the stages: + gather, stage 1, stage 2
+    assert bench.launches_per_step(synth.CONFIGS["mixtral_decode"], one_stage=False) == 6
+    # large T*E: logit pass + top-k pass; more than 1024 slots: three-launch sort
+    assert bench.launches_per_step(synth.CONFIGS["finegrained_zipf"]) == 2 + 3 + 4
+    # per-token FP8: + the row re-quantisation of h
+    cfg = synth.CONFIGS["mixtral_fp8_token"]
+    assert bench.launches_per_step(cfg) == 2 + 3 + 5
+
+
+def test_traffic_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
+    csrc = tmp_path / "mixture_experts_grouped_moe_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1")
+    (csrc / "h.cuh").write_text("header v1")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.kernel_source_hash(["k.cu", "h.cuh"])
+    assert digest == bench.kernel_source_hash(["h.cuh", "k.cu"])  # order of the list does not matter
+    (tmp_path / "profiles").mkdir()
+    entry = {"w": {"stage1": {"dram_bytes_per_launch": 1234, "sources": ["k.cu", "h.cuh"], "source_hash": digest}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(entry))
+    assert bench.profiled_traffic("w", "stage1") == 1234
+    assert bench.profiled_traffic("w", "one_kernel") is None
+    assert bench.profiled_traffic("other", "stage1") is None
+    (csrc / "h.cuh").write_text("header v2")  # any source change voids the recorded traffic
+    assert bench.profiled_traffic("w", "stage1") is None
