@@ -12,7 +12,8 @@
 // wait on a global counter that the epilogues release after their stores),
 // so W_down streams from HBM while the last stage-1 tiles finish.  Stage 2
 // splits K = I as the two-launch path does; the fixed-order split reduce and
-// top-k combine remain a separate pass.
+// top-k combine remain a separate pass.  No gather pass precedes the launch:
+// the producer warp fetches each stage-1 tile's token rows from x itself.
 #include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
