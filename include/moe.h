@@ -364,8 +364,9 @@ int moe_set_stage_events(void *const *events, int n);
  * Choice of the grouped-mode GEMM kernel for MOE_BF16 and MOE_FP8_TOKEN,
  * process-wide: mode 1 always runs the two-SM (CTA pair) kernels, 0 never,
  * -1 (the default, or MOE_GEMM_PAIR unset in the environment) lets the
- * library choose: pairs when the average active expert holds at least 4
- * token blocks, in both stages for bf16 and in stage 2 for per-token FP8.
+ * library choose: pairs when the average expert holds at least one 128-row
+ * token block (T*k >= 128 * min(E, T*k)), in both stages for bf16 and in
+ * stage 2 for per-token FP8.
  * Both kernels give results within the same tolerance of the definition.
  * Returns MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the fused-MoE
  * pages: a kernel-selection switch of this library.)
@@ -378,10 +379,11 @@ int moe_set_gemm_pair(int mode);
  * one persistent launch -- tiles of both stages claimed from one counter,
  * stage-1 tiles first; the intermediate stays in L2; the down-projection
  * weights of a stage-2 tile stream while the last stage-1 tiles finish --
- * followed by the usual split reduce and combine; the default (1 unless
+ * followed by the usual split reduce and combine; the launch fetches the
+ * token rows from x itself, so no gather pass runs; the default (1 unless
  * MOE_ONE_STAGE=0 is in the environment).  0 keeps two launches.  Both give
  * bit-identical results (same tiles and MMA order); with one launch the
- * per-stage timing events record stage 2 as empty.
+ * per-stage timing events record the gather and stage 2 as empty.
  * Returns MOE_OK or MOE_ERR_INVALID_ARG.
  */
 int moe_set_one_stage(int mode);
