@@ -256,20 +256,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_id_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t nclusters_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
 // The shared::cluster address of the same variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank)
 {
