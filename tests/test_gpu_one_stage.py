@@ -50,6 +50,7 @@ CASES = [
     ("b128_sk1", 20, 256, 512, 4, 2, None, 128, 1),
     ("sk8", 8, 512, 1024, 8, 2, None, 0, 8),
     ("h_odd", 50, 640, 256, 8, 2, "normal", 0, 0),
+    ("t128_e1k1", 128, 256, 256, 1, 1, None, 0, 0),   # one 128-row tile of real token rows
 ]
 
 
