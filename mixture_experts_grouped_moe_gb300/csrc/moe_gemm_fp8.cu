@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 const float isc = 1.0f / sc;
                 // 64 code bytes per row: through the warp's shared block (same swizzle as stage 2)
                 // so that each store writes 8 rows x 64 contiguous bytes instead of 32 rows
-                float4(*buf)[4] = sm.ep_out[warp - 2];
+                float4(*ep_rows)[4] = sm.ep_out[warp - 2];
 #pragma unroll
                 for (int v = 0; v < kChunk / 16; ++v) {
                     uint32_t w[4];
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                             __nv_cvt_float2_to_fp8x2(make_float2(e[2] * isc, e[3] * isc), __NV_SATFINITE, __NV_E4M3);
                         w[j] = lo | (hi << 16);
                     }
-                    buf[lane][v ^ ((lane >> 1) & 3)] = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]),
+                    ep_rows[lane][v ^ ((lane >> 1) & 3)] = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]),
                                                                    __uint_as_float(w[2]), __uint_as_float(w[3]));
                 }
                 __syncwarp();
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
 #pragma unroll
                     for (int it = 0; it < 4; ++it) {
                         const int r = 8 * it + rr;
-                        const float4 o = buf[r][cq ^ ((r >> 1) & 3)];
+                        const float4 o = ep_rows[r][cq ^ ((r >> 1) & 3)];
                         *reinterpret_cast<float4 *>(static_cast<uint8_t *>(a.inter) + (size_t)(row0 + r) * a.N +
                                                     ctl.ncol0 + sub * kChunk + 16 * cq) = o;
                     }
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 const int slot = a.sorted_ids[cpos];
                 const float wgt = slot < a.S ? a.sorted_weights[cpos] : 0.0f;
                 const int n0 = ctl.ncol0 + sub * 2 * kChunk;
-                float4(*buf)[4] = sm.ep_out[warp - 2];
+                float4(*ep_rows)[4] = sm.ep_out[warp - 2];
                 const int rr = lane >> 2, cq = lane & 3;  // read side: row within 8, float4 column
                 if (n0 < a.N) {
 #pragma unroll
@@ -446,14 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                         const float *v = blk < kChunk / 16 ? &acc0[blk * 16] : &acc1[blk * 16 - kChunk];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            buf[lane][j ^ ((lane >> 1) & 3)] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1],
+                            ep_rows[lane][j ^ ((lane >> 1) & 3)] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1],
                                                                            wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
                         __syncwarp();
 #pragma unroll
                         for (int it = 0; it < 4; ++it) {
                             const int r = 8 * it + rr;
                             const int rslot = __shfl_sync(0xffffffffu, slot, r);
-                            const float4 o = buf[r][cq ^ ((r >> 1) & 3)];
+                            const float4 o = ep_rows[r][cq ^ ((r >> 1) & 3)];
                             if (rslot < a.S)
                                 *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 16 + 4 * cq) = o;
                         }
