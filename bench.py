@@ -1,11 +1,15 @@
 """Benchmark of the fused MoE layer on GB300 (one JSON line on stdout).
 
-Default workload: Mixtral-8x7B MoE decode (T=32 tokens, H=4096, I=14336,
+Headline workload: Mixtral-8x7B MoE decode (T=32 tokens, H=4096, I=14336,
 E=8 experts, top-2, bf16 weights/activations, fp32 accumulation).  A step is
 one whole forward of the layer (route, sort, gather, stage-1 and stage-2
-group GEMMs, combine) through the C ABI on device-resident inputs.
+group GEMMs, combine) through the C ABI on device-resident inputs.  The
+default run also times, one after another, the tiny layer, Mixtral prefill
+(T=8192 with uneven expert loads), the block-scaled FP8 layer (T=4096) and
+the fine-grained skewed layer (T=4096, E=256, top-8), each with its own
+clocks and rooflines under "per_config".
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-per-config]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 
 Under torchrun (N > 1) each rank runs an independent replica on its own GPU
@@ -136,45 +140,33 @@ def whole_job_throughput(world, tokens_per_rank, ms_max):
 
 
 def algorithmic_counts(cfg, counts, dtype_bytes):
-    """FLOPs and bytes of the layer from the actual routing (counts per expert)."""
+    """FLOPs and bytes of the layer from the actual routing (counts per expert), as the roofline
+    definition states them: routed FLOPs 2*S*3*H*I + 2*T*H*E; bytes = weights (+ scales) of the
+    experts that received a slot, x and out once (bf16), the router weights."""
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
     S = T * k
     flops = 2.0 * S * 3 * H * I + 2.0 * T * H * E
     active = int(sum(1 for c in counts if c > 0))
-    scale_bytes = 0
+    s1_scale = s2_scale = 0
     if cfg.dtype == "fp8":
-        scale_bytes = active * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+        s1_scale = active * (2 * I // 128) * (H // 128) * 4
+        s2_scale = active * (H // 128) * (I // 128) * 4
     elif cfg.dtype == "fp8_token":
-        scale_bytes = active * (2 * I + H) * 4
+        s1_scale, s2_scale = active * 2 * I * 4, active * H * 4
     elif cfg.dtype == "mxfp4":
-        scale_bytes = active * 3 * H * I // 32
-    bytes_ = int(active * 3 * H * I * dtype_bytes) + scale_bytes + T * H * 2 + T * H * 2 + E * H * 2
-    s1_bytes = int(active * 2 * I * H * dtype_bytes)
-    s2_bytes = int(active * H * I * dtype_bytes)
+        s1_scale, s2_scale = active * 2 * I * H // 32, active * H * I // 32
+    s1_bytes = int(active * 2 * I * H * dtype_bytes) + s1_scale
+    s2_bytes = int(active * H * I * dtype_bytes) + s2_scale
+    bytes_ = s1_bytes + s2_bytes + T * H * 2 + T * H * 2 + E * H * 2
     return flops, bytes_, active, s1_bytes, s2_bytes
 
 
-def run_cuda(args, cfg, rank, world, local_rank):
-    import numpy as np
+def make_weights(moe, cfg, inp, dev):
+    """The layer's weights in the workload's format (quantised on the GPU by the library)."""
     import torch
-
-    from mixture_experts_grouped_moe_gb300 import build as moe_build
-    from mixture_experts_grouped_moe_gb300 import moe, synth
-
-    moe_build.build()
-    moe.load()
-    moe.moe_set_one_stage(0 if args.two_launch else 1)
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    peaks, peak_kind = load_peaks()
-    fp8 = cfg.dtype == "fp8"
-    dtype = {"fp8": moe.MOE_FP8_BLOCK128, "fp8_token": moe.MOE_FP8_TOKEN, "mxfp4": moe.MOE_MXFP4}.get(
-        cfg.dtype, moe.MOE_BF16)
-
-    inp = synth.make_inputs(cfg, seed=0, device=dev)
     w = {"W_router": inp["W_router"], "bias": inp["bias"]}
-    if fp8:
-        E, I, H = cfg.E, cfg.I, cfg.H
+    E, I, H = cfg.E, cfg.I, cfg.H
+    if cfg.dtype == "fp8":
         q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
         s1 = torch.empty(E * 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
         q2 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
@@ -183,7 +175,6 @@ def run_cuda(args, cfg, rank, world, local_rank):
         moe.moe_quantize_fp8_weights(inp["W_down"], E * H, I, q2, s2)
         w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
     elif cfg.dtype == "fp8_token":
-        E, I, H = cfg.E, cfg.I, cfg.H
         q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
         s1 = torch.empty(E * 2 * I, dtype=torch.float32, device=dev)
         q2 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
@@ -192,7 +183,6 @@ def run_cuda(args, cfg, rank, world, local_rank):
         moe.moe_quantize_fp8_rows(inp["W_down"], E * H, I, q2, s2)
         w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
     elif cfg.dtype == "mxfp4":
-        E, I, H = cfg.E, cfg.I, cfg.H
         q1 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
         s1 = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
         q2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
@@ -202,21 +192,52 @@ def run_cuda(args, cfg, rank, world, local_rank):
         w.update(W_gate_up=q1, w1_scale=s1, W_down=q2, w2_scale=s2)
     else:
         w.update(W_gate_up=inp["W_gate_up"], W_down=inp["W_down"])
-    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, host_staging=True)
+    return w
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def layer_bytes_exceed_l2(cfg):
+    eb = {"fp8": 1, "fp8_token": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
+    return cfg.E * 3 * cfg.H * cfg.I * eb > 2 * L2_BYTES
+
+
+def measure(args, cfg, rank, world, local_rank, e2e=False):
+    """Time K whole-layer steps of one workload on this rank's GPU (after W warm-ups): the
+    device-resident step, the per-stage split (a second pass with events between launches), and
+    optionally the end-to-end step through the host-buffer entry."""
+    import numpy as np
+    import torch
+
+    from mixture_experts_grouped_moe_gb300 import moe, synth
+
+    dev = torch.device("cuda", local_rank)
+    dtype = {"fp8": moe.MOE_FP8_BLOCK128, "fp8_token": moe.MOE_FP8_TOKEN, "mxfp4": moe.MOE_MXFP4}.get(
+        cfg.dtype, moe.MOE_BF16)
+    inp = synth.make_inputs(cfg, seed=0, device=dev)
+    w = make_weights(moe, cfg, inp, dev)
+    if cfg.dtype != "bf16":
+        del inp["W_gate_up"], inp["W_down"]  # only the quantised stacks are used
+    one_stage = cfg.dtype == "bf16" and cfg.T <= 128 and not args.two_launch
+    opts = moe.Options(one_stage=1 if one_stage else 0)
+    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, host_staging=e2e, options=opts)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-    # per-step events: 7 stage marks per step
     K, W = args.steps, args.warmup
+    # inputs smaller than L2 (the tiny workload): a buffer larger than L2 is written between steps
+    flush = None if layer_bytes_exceed_l2(cfg) else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     for _ in range(W):
         layer(inp["x"], w, out)
     torch.cuda.synchronize()
     if layer.status() != moe.MOE_OK:
-        raise RuntimeError("device wait timed out during warm-up")
+        raise RuntimeError(f"{cfg.name}: device wait timed out during warm-up")
     counts = layer.view("expert_counts", torch.int32, (cfg.E,)).cpu().numpy().tolist()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
     for row in ev:  # torch creates the CUDA event on first record; the handles must exist before use
         for e in row:
             e.record(stream)
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
 
@@ -228,48 +249,123 @@ def run_cuda(args, cfg, rank, world, local_rank):
     if sampler:
         sampler.start()
         time.sleep(0.15)
-    # timed region: K whole-layer steps, nothing between the library's launches
-    start.record(stream)
-    for i in range(K):
-        layer(inp["x"], w, out)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    if flush is None:
+        # timed region: K whole-layer steps back to back, nothing between the library's launches
+        start.record(stream)
+        for _ in range(K):
+            layer(inp["x"], w, out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        ms_total = start.elapsed_time(stop)
+    else:
+        for i in range(K):
+            flush.fill_(float(i))
+            steps_ev[i][0].record(stream)
+            layer(inp["x"], w, out)
+            steps_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms_total = sum(a.elapsed_time(b) for a, b in steps_ev)
     clocks = sampler.stop() if sampler else None
-    ms_total = start.elapsed_time(stop)
     # per-kernel timing: the same steps again with the library recording an event between its
     # launches (events between kernels stop the launch overlap, so this pass does not set `value`)
     for i in range(K):
-        moe.moe_set_stage_events(ev[i])
-        layer(inp["x"], w, out)
+        if flush is not None:
+            flush.fill_(float(i))
+        layer(inp["x"], w, out, options=moe.Options(one_stage=opts.one_stage, stage_events=ev[i]))
     torch.cuda.synchronize()
-    stage_ms = {s: 0.0 for s in STAGES}
+    stage_ms = {st: 0.0 for st in STAGES}
     for i in range(K):
-        for j, s in enumerate(STAGES):
-            stage_ms[s] += ev[i][j].elapsed_time(ev[i][j + 1])
-    stage_ms = {s: v / K for s, v in stage_ms.items()}
+        for j, st in enumerate(STAGES):
+            stage_ms[st] += ev[i][j].elapsed_time(ev[i][j + 1])
+    stage_ms = {st: v / K for st, v in stage_ms.items()}
 
-    # end to end: host (pinned) x in, host out back, through the C-ABI host entry
-    x_host = inp["x"].cpu().pin_memory()
-    out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
-    for _ in range(max(3, W // 4)):
-        layer.forward_host(x_host, w, out_host)
-    torch.cuda.synchronize()
-    K2 = max(1, K // 2)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K2):
-        layer.forward_host(x_host, w, out_host)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K2
-    assert np.isfinite(out_host.float().numpy()).all()
+    e2e_ms = None
+    if e2e:
+        # end to end: host (pinned) x in, host out back, through the C-ABI host entry
+        x_host = inp["x"].cpu().pin_memory()
+        out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+        for _ in range(max(3, W // 4)):
+            layer.forward_host(x_host, w, out_host)
+        torch.cuda.synchronize()
+        K2 = max(1, K // 2)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K2):
+            layer.forward_host(x_host, w, out_host)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / K2
+        assert np.isfinite(out_host.float().numpy()).all()
+    assert torch.isfinite(out.float()).all()
 
     ms = ms_total / K
     if world > 1:
-        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
-    return dict(ms=ms, e2e_ms=e2e_ms, stage_ms=stage_ms, counts=counts, clocks=clocks, peaks=peaks,
-                peak_kind=peak_kind, plan=layer.plan, K=K, W=W)
+        ms, e2e_max = max_over_ranks([ms, e2e_ms or 0.0], dev)
+        e2e_ms = e2e_max if e2e else None
+    plan = layer.plan
+    r = dict(ms=ms, e2e_ms=e2e_ms, stage_ms=stage_ms, counts=counts, clocks=clocks, plan=plan, K=K, W=W,
+             one_stage=one_stage, l2="L2 flushed between steps (256 MiB written)" if flush is not None
+             else "inputs larger than L2 (expert weights streamed every step)")
+    del layer, w, inp, out, flush
+    torch.cuda.empty_cache()
+    return r
+
+
+def summarize(cfg, r, peaks, peak_kind, world):
+    """Throughput, the layer roofline and the dominant kernel's roofline of one measured workload."""
+    eb = {"fp8": 1, "fp8_token": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
+    flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], eb)
+    ms = r["ms"]
+    peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    if eb == 1:
+        peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)  # nominal dense FP8 / bf16 ratio
+    elif eb == 0.5:
+        peak_t = peaks.get("fp4_tflops", 6.0 * peak_t)  # nominal dense FP4 / bf16 ratio on GB300 (13.5 / 2.25)
+    hbm = peaks["hbm_gbs"]
+    t_roof = max(flops / (peak_t * 1e12), bytes_ / (hbm * 1e9))
+    T, H, I, S = cfg.T, cfg.H, cfg.I, cfg.S
+    plan = r["plan"]
+    npp_rows = sum(-(-c // plan.block_m) * plan.block_m for c in r["counts"])
+    h_bytes = {"fp8": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
+    x_bytes = T * H * 2
+    if r["one_stage"]:
+        # one launch runs both stages and reads x itself
+        kname, kms = "one-kernel stage 1 + stage 2 (swap-AB)", r["stage_ms"]["stage1"]
+        k_flops = 2.0 * S * 3 * H * I
+        k_bytes = s1_bytes + s2_bytes + x_bytes
+        impl = int(k_bytes + 2 * npp_rows * I * 2 + plan.split_k2 * npp_rows * H * 4)  # h out and back, partials
+    else:
+        kname, kms = "stage 1 gate/up group GEMM" + (" (swap-AB)" if plan.mode == 1 else ""), r["stage_ms"]["stage1"]
+        k_flops = 2.0 * S * 2 * I * H
+        k_bytes = s1_bytes + x_bytes
+        impl = int(s1_bytes + npp_rows * H * eb + npp_rows * I * h_bytes)  # gathered x rows in, h out
+    mem_bound = k_bytes / (hbm * 1e9) >= k_flops / (peak_t * 1e12)
+    if mem_bound:
+        achieved = k_bytes / (kms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "alg_bytes_per_launch": int(k_bytes)}
+    else:
+        achieved = k_flops / (kms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak_t, 4), "alg_flops_per_launch": k_flops}
+    roof.update(kernel=kname, impl_bytes_per_launch=impl, peak_source=peak_kind, kernel_ms=round(kms, 5),
+                traffic=profiled_traffic(cfg.name, "one_kernel" if r["one_stage"] else "stage1"))
+    return {
+        "value": round(whole_job_throughput(world, T, ms), 2), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "steps": r["K"], "warmup": r["W"],
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "hbm_gbs": round(bytes_ / (ms * 1e-3) / 1e9, 1),
+        "layer_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof / (ms * 1e-3), 4),
+                           "bound": "hbm" if bytes_ / (hbm * 1e9) >= flops / (peak_t * 1e12) else "tensor",
+                           "alg_bytes": bytes_, "alg_flops": flops, "active_experts": active},
+        "stage_ms": {k2: round(v, 5) for k2, v in r["stage_ms"].items()},
+        "roofline": roof,
+        "gpu_launches": launches_per_step(cfg, r["one_stage"]) * r["K"],
+        "clocks": r["clocks"],
+        "plan": {"mode": "swap" if plan.mode == 1 else "grouped", "block_m": plan.block_m,
+                 "split_k2": plan.split_k2},
+        "l2": r["l2"],
+    }
 
 
 def cpu_baseline(cfg, host, budget_s=20.0):
@@ -348,13 +444,22 @@ def workload_desc(cfg):
     return d
 
 
+# The workloads timed beside the headline in the default run (one after another on the same GPU,
+# each allocated, timed and freed in turn): the small case, Mixtral prefill with uneven loads, the
+# block-scaled FP8 layer and the fine-grained skewed layer.
+PER_CONFIG = ["tiny", "mixtral_prefill", "mixtral_fp8", "finegrained_zipf"]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="mixtral_decode")
+    ap.add_argument("--workload", default=None,
+                    help="time only this workload (default: Mixtral decode as the headline, plus the other "
+                         "workloads under per_config)")
+    ap.add_argument("--no-per-config", action="store_true", help="the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="bf16 training step: training forward + backward (dx and all weight gradients)")
@@ -366,13 +471,12 @@ def main():
     args.warmup = max(3, args.warmup)
 
     from mixture_experts_grouped_moe_gb300 import synth
-    cfg = synth.CONFIGS[args.workload]
+    explicit = args.workload is not None
+    cfg = synth.CONFIGS[args.workload or "mixtral_decode"]
     if args.experts:
         cfg = cfg.with_(name=cfg.name + f"_E{args.experts}", E=args.experts)
     if args.tokens:
         cfg = cfg.with_(name=cfg.name + f"_T{args.tokens}", T=args.tokens)
-    # the library runs bf16 decode-size batches (swap mode, T <= 128) in one kernel unless told otherwise
-    args.one_stage = cfg.dtype == "bf16" and cfg.T <= 128 and not args.two_launch
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -383,86 +487,60 @@ def main():
             return 0
         return run_reference(args, cfg)
 
+    import torch
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
+    from mixture_experts_grouped_moe_gb300 import build as moe_build
+    from mixture_experts_grouped_moe_gb300 import moe
+    moe_build.build()
+    moe.load()
+    torch.cuda.set_device(local_rank)
     if args.train:
         return run_train(args, cfg, rank, world, local_rank)
-    r = run_cuda(args, cfg, rank, world, local_rank)
+    peaks, peak_kind = load_peaks()
+    r = measure(args, cfg, rank, world, local_rank, e2e=True)
+    others = []
+    if not explicit and not args.no_per_config:
+        for name in PER_CONFIG:
+            c = synth.CONFIGS[name]
+            others.append((c, measure(args, c, rank, world, local_rank)))
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
+    head = summarize(cfg, r, peaks, peak_kind, world)
     eb = {"fp8": 1, "fp8_token": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
-    flops, bytes_, active, s1_bytes, s2_bytes = algorithmic_counts(cfg, r["counts"], eb)
-    peaks = r["peaks"]
-    ms = r["ms"]
-    tokens_s = whole_job_throughput(world, cfg.T, ms)
-    tflops = flops / (ms * 1e-3) / 1e12
-    gbs = bytes_ / (ms * 1e-3) / 1e9
-    peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    if eb == 1:
-        peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)
-    elif eb == 0.5:
-        peak_t = peaks.get("fp4_tflops", 6.0 * peak_t)  # nominal dense FP4 / bf16 ratio on GB300 (13.5 / 2.25)
-    t_roof = max(flops / (peak_t * 1e12), bytes_ / (peaks["hbm_gbs"] * 1e9))
-    memory_bound = bytes_ / (peaks["hbm_gbs"] * 1e9) >= flops / (peak_t * 1e12)
-    # dominant kernel: stage 1 (gate/up group GEMM)
-    s1_ms = r["stage_ms"]["stage1"]
-    T, H, I = cfg.T, cfg.H, cfg.I
-    npp_rows = sum(-(-c // r["plan"].block_m) * r["plan"].block_m for c in r["counts"])
-    if memory_bound:
-        # weights, the sorted activations read, h written (bf16 except block FP8's e4m3 codes), scales
-        h_bytes = {"fp8": 1, "mxfp4": 0.5}.get(cfg.dtype, 2)
-        s1_alg = int(s1_bytes + npp_rows * H * eb + npp_rows * I * h_bytes)
-        if cfg.dtype == "fp8_token":
-            s1_alg += active * 2 * I * 4 + npp_rows * 4
-        elif cfg.dtype == "mxfp4":
-            s1_alg += (active * 2 * I * H + npp_rows * H + npp_rows * I) // 32
-        kname = "stage1 gate/up group GEMM (swap-AB)"
-        if args.one_stage:
-            # one launch runs both stages: its bytes add stage 2's weights, h read back and the partials
-            s1_alg += s2_bytes + npp_rows * I * 2 + r["plan"].split_k2 * npp_rows * H * 4
-            kname = "one-kernel stage 1 + stage 2 (swap-AB)"
-        achieved = s1_alg / (s1_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "kernel": kname, "alg_bytes_per_launch": s1_alg}
-    else:
-        s1_flops = 2.0 * cfg.S * 2 * H * I
-        achieved = s1_flops / (s1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_t, "unit": "TFLOP/s",
-                "frac": round(achieved / peak_t, 4), "kernel": "stage1 gate/up group GEMM",
-                "alg_flops_per_launch": s1_flops}
-    roof["peak_source"] = r["peak_kind"]
-    roof["traffic"] = profiled_traffic(cfg.name, "one_kernel" if args.one_stage else "stage1")
-    roof["kernel_ms"] = round(s1_ms, 5)
+    T, H = cfg.T, cfg.H
     line = {
-        "metric": METRIC, "value": round(tokens_s, 2), "unit": "tokens/s", "n_gpus": world,
-        "steps": r["K"], "warmup": r["W"], "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": {1: "fp8-e4m3/fp32-acc", 0.5: "mxfp4-e2m1/fp32-acc"}.get(eb, "bf16"),
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": r["K"], "warmup": r["W"], "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {1: "fp8-e4m3/fp32-acc", 0.5: "mxfp4-e2m1/fp32-acc"}.get(eb, "bf16"),
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights; random init, no checkpoint)",
         "config": dict(workload_desc(cfg), parallelism=f"replicas x{world}",
-                       **({"one_stage": True} if args.one_stage else {}),
-                       l2="inputs larger than L2 (expert weights streamed every step)"),
-        "tflops": round(tflops, 2), "hbm_gbs": round(gbs, 1),
-        "layer_roofline": {"t_roof_ms": round(t_roof * 1e3, 4), "frac": round(t_roof / (ms * 1e-3), 4),
-                           "bound": "hbm" if memory_bound else "tensor", "alg_bytes": bytes_, "alg_flops": flops,
-                           "active_experts": active},
-        "stage_ms": {k: round(v, 5) for k, v in r["stage_ms"].items()},
-        "roofline": roof,
-        "gpu_launches": launches_per_step(cfg, args.one_stage) * r["K"],
+                       **({"one_stage": True} if r["one_stage"] else {}), l2=head["l2"]),
+        "tflops": head["tflops"], "hbm_gbs": head["hbm_gbs"],
+        "layer_roofline": head["layer_roofline"],
+        "stage_ms": head["stage_ms"],
+        "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"],
         "stage_ms_note": "per-kernel CUDA-event times from a second pass of the same steps with an event "
                          "between launches; value is timed without them",
-        "clocks": r["clocks"],
-        "e2e": {"value": round(whole_job_throughput(world, cfg.T, r["e2e_ms"]), 2), "unit": "tokens/s",
+        "clocks": head["clocks"],
+        "e2e": {"value": round(whole_job_throughput(world, T, r["e2e_ms"]), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": round(r["e2e_ms"], 5)},
-        "plan": {"mode": "swap" if r["plan"].mode == 1 else "grouped", "block_m": r["plan"].block_m,
-                 "split_k2": r["plan"].split_k2},
+        "plan": head["plan"],
     }
+    if others:
+        line["per_config"] = {}
+        for c, rc in others:
+            ent = summarize(c, rc, peaks, peak_kind, world)
+            ent["workload"] = workload_desc(c)["workload"]
+            line["per_config"][c.name] = ent
     if not args.no_cpu_baseline:
-        import torch
         host = host_inputs(cfg, torch.device("cuda", local_rank))
         line["cpu_baseline"] = cpu_baseline(cfg, host)
     print(json.dumps(line), flush=True)

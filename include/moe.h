@@ -25,16 +25,22 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous on it: no host synchronisation, no
  *    allocation, no exceptions; results are ready when the stream is.
- *  - The caller owns every buffer.  The library keeps only per-device
- *    constants (SM count, kernel attributes).
+ *  - The caller owns every buffer.  The library keeps no mutable state
+ *    that changes what a call computes or launches: only per-device
+ *    constants (SM count, the no-allocation sort's scratch address).  Every
+ *    choice a caller can make travels in the call's own arguments
+ *    (block_m, split_k, and moe_options_t for moe_fused_forward_ex); the
+ *    library reads no environment variables.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns a negative status and launches nothing.  A CUDA
  *    launch error returns MOE_ERR_CUDA.  Kernels that wait on barriers give
  *    up after a bounded time and record MOE_ERR_TIMEOUT in the workspace
  *    status word (read it with moe_workspace_status).
  *
- * Limits: 1 <= k <= min(E, 32); E <= 1024; H and I multiples of 128;
- * T >= 0 (T = 0 is a no-op that returns MOE_OK).
+ * Limits: 1 <= k <= min(E, 32); E <= 1024; H and I multiples of 128 (the
+ * tile granule of every GEMM kernel here, and the granule the AITER page's
+ * stage rules test, inter_dim % 128); T >= 0 (T = 0 is a no-op that
+ * returns MOE_OK).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -167,16 +173,20 @@ int moe_workspace_status(const void *ws, int *status, void *stream);
  * adds in ascending h, then the partials are combined by a butterfly with
  * strides 16, 8, 4, 2, 1 -- so the ids are a deterministic function of the
  * bytes.  topk_ids[t] = the k largest logits, largest first, an equal logit
- * going to the lower expert; topk_weights[t][j] = exp(l_j - l_0) / sum.
+ * going to the lower expert.  topk_weights[t][j]:
+ *   renormalize = 1: exp(l_j - l_0) / sum over the k selected (they sum to 1;
+ *                    what moe_fused_forward uses);
+ *   renormalize = 0: exp(l_j - l_0) / sum over all E experts (the softmax
+ *                    over all experts, evaluated at the selected ones).
  *   x (device) bf16 [T][H]; W_router (device) bf16 [E][H];
  *   bias (device) fp32 [E] or NULL; topk_ids (device) int32 [T][k];
  *   topk_weights (device) fp32 [T][k]; logits (device) fp32 [T][E] or NULL.
  * With logits given and T*E > 4096 the logits are computed by a tiled pass
  * and the top-k by a second pass (faster for large T*E); otherwise one fused
- * launch.  Both give the same bits.
+ * launch.  Both give the same bits.  H % 8 == 0.
  */
 int moe_route_topk(const void *x, const void *W_router, const float *bias, int T, int H, int E, int k,
-                   int32_t *topk_ids, float *topk_weights, float *logits, void *stream);
+                   int renormalize, int32_t *topk_ids, float *topk_weights, float *logits, void *stream);
 
 /* Scratch bytes moe_align_sort needs (device memory passed as ws). */
 size_t moe_align_sort_workspace_size(int T, int k, int E);
@@ -193,7 +203,11 @@ size_t moe_align_sort_workspace_size(int T, int k, int E);
  *   num_tokens_post_padded (device) int32 [1]: sum of the padded segment lengths;
  *   expert_counts (device) int32 [E] or NULL: slots per expert;
  *   ws (device) scratch of moe_align_sort_workspace_size bytes.
- * Ids outside [0, E) are a caller error and are not checked on the device.
+ * An id outside [0, E) is a caller error.  The kernels check every id: a
+ * slot with a bad id is left out of every segment (nothing outside the
+ * output buffers is written) and num_tokens_post_padded is set to
+ * MOE_ERR_INVALID_ARG (-1), which no valid result can be; check it when the
+ * ids come from untrusted code.
  */
 int moe_align_sort(const int32_t *topk_ids, const float *topk_weights, int T, int k, int E, int block_m,
                    int32_t *sorted_ids, float *sorted_weights, int32_t *sorted_expert_ids,
@@ -240,6 +254,72 @@ int moe_quantize_fp8_rows(const void *X, int64_t R, int C, uint8_t *q, float *s,
  *   (r % 32) * 16 + (r % 128 / 32) * 4 + g % 4.
  */
 int moe_quantize_mxfp4(const void *X, int64_t R, int C, uint8_t *q, uint8_t *s, int tiled, void *stream);
+
+/*
+ * Per-call choices of moe_fused_forward_ex and the training entries.  Fill
+ * one with moe_options_init (the library's defaults) and change the fields
+ * you need; a NULL options pointer means the defaults.  These select among
+ * kernels that compute the same layer (each within the same tolerance of
+ * the definition) or add instrumentation; none changes the workspace size.
+ * (No counterpart on the fused-MoE pages: launch choices of this library.)
+ */
+typedef struct moe_options {
+    /* Grouped-mode GEMM kernel for MOE_BF16 and MOE_FP8_TOKEN: -1 automatic
+     * (CTA pairs when the average expert holds at least one 128-row token
+     * block, T*k >= 128 * min(E, T*k): in both stages for bf16, in stage 2
+     * for per-token FP8), 0 always the one-SM kernels, 1 CTA pairs (the
+     * two-SM tensor core) wherever supported. */
+    int gemm_pair;
+    /* bf16 swap mode (T <= 128): 1 runs both GEMM stages in one persistent
+     * launch ("1-stage", AITER page section 3.2: tiles of both stages claimed
+     * from one counter, stage-1 tiles first, the intermediate kept in L2,
+     * the token rows fetched from x by the launch itself), 0 two launches
+     * with a gather pass before them.  Both give bit-identical results.
+     * Default 1. */
+    int one_stage;
+    /* Programmatic dependent launch: -1 the library's default set of launch
+     * boundaries, otherwise a mask of them (bit 0 router -> sort and inside
+     * the sort, 1 sort -> gather, 2 -> stage 1, 3 stage 1 -> stage 2, 4 ->
+     * combine, 5 logit pass -> top-k pass, 6 preceding work -> router);
+     * 0 turns it off.  Default -1 (all, except bits 2 and 3 in grouped mode,
+     * where an early-resident persistent GEMM measured slower). */
+    int pdl_mask;
+    /* NULL, or 7 CUDA events (cudaEvent_t cast to void*, created by the
+     * caller) recorded on the call's stream at [0] entry, [1] after routing,
+     * [2] after the sort, [3] after the gather (FP8: gather + quantise),
+     * [4] after stage 1, [5] after stage 2 (per-token FP8: including the
+     * re-quantisation of the intermediate), [6] after the combine.  With the
+     * one-launch decode path [3] follows [2] and [5] follows [4] directly.
+     * Events between launches stop their overlap: time whole calls without. */
+    void *const *stage_events;
+    /* Limit, in microseconds, of the one-launch decode path's wait for the
+     * intermediate (stage-2 tiles wait for every stage-1 epilogue); 0 = the
+     * default of 2 s.  Every other device wait keeps its 2 s limit. */
+    unsigned int h_wait_limit_us;
+    /* Test of the timeout path only (0 otherwise): 1 makes the one-launch
+     * decode path's stage-2 tiles wait for one more stage-1 epilogue than
+     * exists, so that wait runs out after h_wait_limit_us; the call then
+     * records MOE_ERR_TIMEOUT in the workspace status word and every CTA
+     * returns after its copies and MMAs in flight have completed.  The
+     * output of such a call is undefined; the next call on the workspace
+     * starts clean. */
+    int unsatisfiable_h_wait;
+} moe_options_t;
+
+/* Set *options to the defaults (gemm_pair -1, one_stage 1, pdl_mask -1, no
+ * events, default wait limit, no test switch).  Returns MOE_OK or
+ * MOE_ERR_INVALID_ARG (NULL). */
+int moe_options_init(moe_options_t *options);
+
+/*
+ * moe_fused_forward with per-call options (NULL = defaults).  Everything else
+ * as moe_fused_forward.  Returns MOE_ERR_INVALID_ARG for an option outside
+ * its range.
+ */
+int moe_fused_forward_ex(int dtype, const void *x, const void *W_router, const float *router_bias,
+                         const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
+                         int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
+                         size_t ws_bytes, const moe_options_t *options, void *stream);
 
 /*
  * The whole layer: route, align-sort, stage 1 (gate/up group GEMM with the
@@ -299,11 +379,11 @@ int moe_fused_forward(int dtype, const void *x, const void *W_router, const floa
 size_t moe_train_workspace_size(int T, int H, int I, int E, int k);
 int moe_fused_forward_train(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
                             const void *W_down, int T, int H, int I, int E, int k, void *out, void *ws,
-                            size_t ws_bytes, void *stream);
+                            size_t ws_bytes, const moe_options_t *options, void *stream);
 int moe_fused_backward(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
                        const void *W_down, const void *dout, int T, int H, int I, int E, int k, void *dx,
                        float *dW_gate_up, float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes,
-                       void *stream);
+                       const moe_options_t *options, void *stream);
 
 /*
  * moe_fused_forward with the activations in host memory: x_host (host) bf16
@@ -331,15 +411,17 @@ int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, 
  *
  * The scratch is a fixed array of MOE_NOALLOC_SORT_SCRATCH_BYTES in the
  * library's own device memory; every GPU that loads the library holds it
- * until the process exits.  The first call on each device looks up the
- * array's device address (with that device current), so make that first
- * call before any stream capture.  Nothing is allocated, by this library or
- * any library it calls.  Shapes whose scratch (one int32 per expert per
- * 1024 slots, plus E+1 offsets) does not fit return MOE_ERR_UNSUPPORTED;
- * use moe_align_sort with a workspace for those.  All calls share the one
- * array and it keeps the last call's contents: calls that overlap on the GPU
- * (on different streams, or from different host threads without ordering)
- * race on it and must be serialised by the caller.
+ * until the process exits.  Every call looks up the array's address on the
+ * current device (cudaGetSymbolAddress, which allocates nothing; it stays
+ * right after a cudaDeviceReset).  The first call on a device may load the
+ * library's device code there, so make that first call before any stream
+ * capture.  Nothing is allocated, by this library or any library it calls.
+ * Shapes whose scratch (one int32 per expert per 1024 slots, plus E+1
+ * offsets) does not fit return MOE_ERR_UNSUPPORTED; use moe_align_sort with
+ * a workspace for those.  All calls share the one array and it keeps the
+ * last call's contents: calls that overlap on the GPU (on different streams,
+ * or from different host threads without ordering) race on it and must be
+ * serialised by the caller.  Ids are checked as in moe_align_sort.
  */
 #define MOE_NOALLOC_SORT_SCRATCH_BYTES (1 << 20)
 
@@ -347,46 +429,6 @@ int moe_align_sort_noalloc(const int32_t *topk_ids, const float *topk_weights, i
                            int block_m, int32_t *sorted_ids, float *sorted_weights,
                            int32_t *sorted_expert_ids, int32_t *num_tokens_post_padded,
                            int32_t *expert_counts, void *stream);
-
-/*
- * Optional per-stage timing for the next moe_fused_forward (or _host) call
- * made by the calling host thread: `events` (host array of n >= 7 CUDA
- * events, cudaEvent_t cast to void*, created by the caller) are recorded on
- * the call's stream at [0] entry, [1] after routing, [2] after the sort,
- * [3] after the gather (FP8: gather + quantise), [4] after stage 1, [5]
- * after stage 2 (per-token FP8: including the re-quantisation of the
- * intermediate), [6] after the combine.  One call consumes the setting;
- * events = NULL clears it.  Returns MOE_OK or MOE_ERR_INVALID_ARG.
- */
-int moe_set_stage_events(void *const *events, int n);
-
-/*
- * Choice of the grouped-mode GEMM kernel for MOE_BF16 and MOE_FP8_TOKEN,
- * process-wide: mode 1 always runs the two-SM (CTA pair) kernels, 0 never,
- * -1 (the default, or MOE_GEMM_PAIR unset in the environment) lets the
- * library choose: pairs when the average expert holds at least one 128-row
- * token block (T*k >= 128 * min(E, T*k)), in both stages for bf16 and in
- * stage 2 for per-token FP8.
- * Both kernels give results within the same tolerance of the definition.
- * Returns MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the fused-MoE
- * pages: a kernel-selection switch of this library.)
- */
-int moe_set_gemm_pair(int mode);
-
-/*
- * One-kernel ("1-stage", AITER page section 3.2) decode path, process-wide:
- * mode 1 runs stage 1 and stage 2 of MOE_BF16 swap-mode calls (T <= 128) in
- * one persistent launch -- tiles of both stages claimed from one counter,
- * stage-1 tiles first; the intermediate stays in L2; the down-projection
- * weights of a stage-2 tile stream while the last stage-1 tiles finish --
- * followed by the usual split reduce and combine; the launch fetches the
- * token rows from x itself, so no gather pass runs; the default (1 unless
- * MOE_ONE_STAGE=0 is in the environment).  0 keeps two launches.  Both give
- * bit-identical results (same tiles and MMA order); with one launch the
- * per-stage timing events record the gather and stage 2 as empty.
- * Returns MOE_OK or MOE_ERR_INVALID_ARG.
- */
-int moe_set_one_stage(int mode);
 
 #ifdef __cplusplus
 }

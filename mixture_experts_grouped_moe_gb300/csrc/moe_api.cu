@@ -10,7 +10,6 @@
 
 #include <cstdio>
 #include <cstdlib>
-#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -60,67 +59,21 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-bool pdl_enabled(int site, bool grouped)
-{
-    static const int env_mask = [] {
-        const char *off = getenv("MOE_PDL");
-        if (off && off[0] == '0')
-            return 0;
-        const char *m = getenv("MOE_PDL_MASK");
-        return m ? (int)strtol(m, nullptr, 16) : -1;
-    }();
-    int mask = env_mask;
-    if (mask < 0)
-        mask = grouped ? 0x7f & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : 0x7f;
-    return (mask >> site) & 1;
-}
-
-// Two-SM (CTA pair) grouped GEMMs: -1 automatic, 0 never, 1 whenever supported.
-// Starts from MOE_GEMM_PAIR in the environment; moe_set_gemm_pair overrides it.
-static std::atomic<int> g_pair_mode{-2};
-
-static int pair_mode()
-{
-    int m = g_pair_mode.load(std::memory_order_relaxed);
-    if (m == -2) {
-        const char *v = getenv("MOE_GEMM_PAIR");
-        m = (v && v[0] == '0') ? 0 : (v && v[0] == '1') ? 1 : -1;
-        g_pair_mode.store(m, std::memory_order_relaxed);
-    }
-    return m;
-}
-
-// Automatic rule (same-box measurements on GB300): pairs pay off once the
-// average active expert holds one token block (S >= 128 per expert, E standing
-// in for the active count): bf16 Mixtral shapes, one-SM vs pairs, T=512
-// 0.656 -> 0.637 ms, T=1024 0.815 -> 0.744, T=2048 1.222 -> 1.186, T=8192
-// stage 1 2.45 -> 2.31 and stage 2 1.38 -> 1.16 ms; the fine-grained E=256
-// workload (2.4 blocks per active expert) is even (4.110 vs 4.123 ms).  For
-// per-token FP8 only stage 2 gains (Mixtral shapes, T=4096: stage 2
-// 0.49 -> 0.42 ms, stage 1 0.77 -> 0.83 ms).
-// One-kernel decode (bf16 swap mode): 1 on (the default: same-box Mixtral
-// decode 0.4355 -> 0.4307 ms per step), 0 off; MOE_ONE_STAGE=0 in the
-// environment sets the start value, moe_set_one_stage overrides it.
-static std::atomic<int> g_one_stage{-2};
-
-static bool one_stage_enabled()
-{
-    int m = g_one_stage.load(std::memory_order_relaxed);
-    if (m == -2) {
-        const char *v = getenv("MOE_ONE_STAGE");
-        m = (v && v[0] == '0') ? 0 : 1;
-        g_one_stage.store(m, std::memory_order_relaxed);
-    }
-    return m == 1;
-}
-
-static bool use_pair(int dtype, int stage, int T, int k, int E)
+// Automatic CTA-pair rule (same-box measurements on GB300): pairs pay off once
+// the average active expert holds one token block (S >= 128 per expert, E
+// standing in for the active count): bf16 Mixtral shapes, one-SM vs pairs,
+// T=512 0.656 -> 0.637 ms, T=1024 0.815 -> 0.744, T=2048 1.222 -> 1.186,
+// T=8192 stage 1 2.45 -> 2.31 and stage 2 1.38 -> 1.16 ms; the fine-grained
+// E=256 workload (2.4 blocks per active expert) is even (4.110 vs 4.123 ms).
+// For per-token FP8 only stage 2 gains (Mixtral shapes, T=4096: stage 2
+// 0.49 -> 0.42 ms, stage 1 0.77 -> 0.83 ms).  gemm_pair: the caller's
+// choice (-1 automatic, 0 never, 1 whenever supported).
+static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
 {
     if (dtype == MOE_FP8_BLOCK128 || dtype == MOE_MXFP4 || !gemm_pair_supported(E))
         return false;
-    const int m = pair_mode();
-    if (m >= 0)
-        return m == 1;
+    if (gemm_pair >= 0)
+        return gemm_pair == 1;
     const int64_t S = (int64_t)T * k;
     const int64_t act = S < E ? S : E;
     if (S < 128 * act)
@@ -283,14 +236,33 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Per-stage timing events of the next forward call on this host thread.
-static thread_local cudaEvent_t t_stage_events[7];
-static thread_local bool t_stage_armed = false;
-
-static void mark(int i, cudaStream_t st)
+static moe_options_t default_options()
 {
-    if (t_stage_armed)
-        cudaEventRecord(t_stage_events[i], st);
+    moe_options_t o;
+    memset(&o, 0, sizeof o);
+    o.gemm_pair = -1;
+    o.one_stage = 1;
+    o.pdl_mask = -1;
+    return o;
+}
+
+static int check_options(const moe_options_t &o)
+{
+    if (o.gemm_pair < -1 || o.gemm_pair > 1 || o.one_stage < 0 || o.one_stage > 1 || o.pdl_mask < -1 ||
+        o.pdl_mask > kPdlAll || o.unsatisfiable_h_wait < 0 || o.unsatisfiable_h_wait > 1)
+        return MOE_ERR_INVALID_ARG;
+    if (o.stage_events)
+        for (int i = 0; i < 7; ++i)
+            if (!o.stage_events[i])
+                return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// Records stage mark i on the call's stream when the caller asked for stage events.
+static void mark(const moe_options_t &o, int i, cudaStream_t st)
+{
+    if (o.stage_events)
+        cudaEventRecord(static_cast<cudaEvent_t>(o.stage_events[i]), st);
 }
 
 // gu (training): when set, the grouped path is forced and stage 1 also keeps
@@ -298,9 +270,12 @@ static void mark(int i, cudaStream_t st)
 static int forward_impl(int dtype, const void *x, const void *W_router, const float *router_bias,
                         const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale,
                         int T, int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws,
-                        size_t ws_bytes, cudaStream_t st, __nv_bfloat16 *gu = nullptr)
+                        size_t ws_bytes, const moe_options_t &o, cudaStream_t st, __nv_bfloat16 *gu = nullptr)
 {
     int rc = validate_shape(dtype, T, H, I, E, k);
+    if (rc != MOE_OK)
+        return rc;
+    rc = check_options(o);
     if (rc != MOE_OK)
         return rc;
     if (!x || !W_router || !W_gate_up || !W_down || !out || !ws)
@@ -328,7 +303,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     const int nsm = num_sms_current_device();
 
     int *status = static_cast<int *>(at(L.status));
-    mark(0, st);
+    const int pdl = o.pdl_mask >= 0 ? o.pdl_mask : pdl_default_mask(p.mode == MOE_MODE_GROUPED);
+    mark(o, 0, st);
     int32_t *topk_ids = static_cast<int32_t *>(at(L.topk_ids));
     float *topk_w = static_cast<float *>(at(L.topk_w));
     // The first kernel follows arbitrary caller work.  With programmatic dependent launch it
@@ -336,10 +312,10 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // zeroes the status words; it only starts early after a kernel that triggers its dependents,
     // such as the previous call's combine.
     if (launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
-                      router_bias, T, H, E, k, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status,
-                      pdl_enabled(kPdlRouter), st) != cudaSuccess)
+                      router_bias, T, H, E, k, 1, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status, pdl,
+                      st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    mark(1, st);
+    mark(o, 1, st);
 
     SortOut so;
     so.sorted_ids = static_cast<int32_t *>(at(L.sorted_ids));
@@ -351,37 +327,37 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     so.active_experts = static_cast<int32_t *>(at(L.active));
     so.num_active = static_cast<int32_t *>(at(L.num_active));
     so.slot_pos = static_cast<int32_t *>(at(L.slot_pos));
-    if (launch_align_sort(topk_ids, topk_w, T, k, E, p.block_m, so, at(L.sort_scratch), pdl_enabled(kPdlSort),
-                          st) != cudaSuccess)
+    if (launch_align_sort(topk_ids, topk_w, T, k, E, p.block_m, so, at(L.sort_scratch), pdl_site(pdl, kPdlSort),
+                          pdl_site(pdl, kPdlSort), st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    mark(2, st);
+    mark(o, 2, st);
 
     const int64_t P = p.max_padded;
     const int eb = (dtype == MOE_BF16) ? 2 : 1;
     // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
     // itself (no gather pass)
-    const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && one_stage_enabled() && !train;
+    const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && o.one_stage == 1 && !train;
     cudaError_t ge = cudaSuccess;
     if (fused) {
         // nothing to gather
     } else if (dtype == MOE_BF16)
         ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
-                                static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_enabled(kPdlGather), st);
+                                static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_site(pdl, kPdlGather), st);
     else if (dtype == MOE_FP8_TOKEN)
         ge = launch_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
                                static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
-                               pdl_enabled(kPdlGather), st);
+                               pdl_site(pdl, kPdlGather), st);
     else if (dtype == MOE_MXFP4)
         ge = launch_quant_mx4(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
                               static_cast<uint8_t *>(at(L.x_sorted)), static_cast<uint8_t *>(at(L.x_scales)), false,
-                              pdl_enabled(kPdlGather), st);
+                              pdl_site(pdl, kPdlGather), st);
     else
         ge = launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S,
                                       k, H, P, static_cast<uint8_t *>(at(L.x_sorted)),
-                                      static_cast<float *>(at(L.x_scales)), pdl_enabled(kPdlGather), st);
+                                      static_cast<float *>(at(L.x_scales)), pdl_site(pdl, kPdlGather), st);
     if (ge != cudaSuccess)
         return MOE_ERR_CUDA;
-    mark(3, st);
+    mark(o, 3, st);
 
     GemmArgs g;
     memset(&g, 0, sizeof g);
@@ -398,6 +374,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g.P_max = P;
     g.status = status;
     g.tile_counter = nullptr;
+    g.pdl_mask = pdl;
     const uint32_t box_inner = (uint32_t)(128 / eb);  // one 128-byte swizzle row (elements; bytes for MXFP4)
     const uint64_t kdiv = (dtype == MOE_MXFP4) ? 2 : 1;  // packed FP4: K/2 bytes per row
     const uint32_t box_x_rows = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
@@ -449,12 +426,14 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         F.h_done = status + 3;
         F.x = static_cast<const __nv_bfloat16 *>(x);
         F.k = k;
+        F.h_wait_ns = o.h_wait_limit_us ? (unsigned long long)o.h_wait_limit_us * 1000ull : 2000000000ull;
+        F.h_extra = o.unsatisfiable_h_wait;
         const int64_t ub = e_act * ((I / 128) + nt2 * p.split_k2);
         ce = launch_fused_decode(F, (int)(ub < nsm ? ub : nsm), st);
         if (ce != cudaSuccess)
             return MOE_ERR_CUDA;
-        mark(4, st);
-        mark(5, st);
+        mark(o, 4, st);
+        mark(o, 5, st);
     } else {
         if (p.mode == MOE_MODE_SWAP) {
             const int64_t ub = e_act * (I / 128);
@@ -465,7 +444,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (I / 64);
             ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
-        } else if (use_pair(dtype, 1, T, k, E)) {
+        } else if (use_pair(dtype, 1, T, k, E, o.gemm_pair)) {
             ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
         } else {
             const int64_t ub = p.max_blocks * (I / 128);
@@ -476,14 +455,14 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         }
         if (ce != cudaSuccess)
             return MOE_ERR_CUDA;
-        mark(4, st);
+        mark(o, 4, st);
 
         // ------------------------------------------------------ stage 2
         if (dtype == MOE_FP8_TOKEN) {
             // h (bf16, sorted order) -> e4m3 codes with one scale per row (stage 2's input)
             ce = launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr, so.num_post_padded, P,
                                    S, k, I, static_cast<uint8_t *>(at(L.inter)),
-                                   static_cast<float *>(at(L.inter_scales)), pdl_enabled(kPdlGather), st);
+                                   static_cast<float *>(at(L.inter_scales)), pdl_site(pdl, kPdlGather), st);
             if (ce != cudaSuccess)
                 return MOE_ERR_CUDA;
         }
@@ -496,7 +475,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         } else if (dtype == MOE_MXFP4) {
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
-        } else if (use_pair(dtype, 2, T, k, E)) {
+        } else if (use_pair(dtype, 2, T, k, E, o.gemm_pair)) {
             ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
         } else {
             const int64_t ub = p.max_blocks * nt2;
@@ -507,17 +486,16 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         }
         if (ce != cudaSuccess)
             return MOE_ERR_CUDA;
-        mark(5, st);
+        mark(o, 5, st);
     }
 
     // ----------------------------------------------------------- combine
     if (p.split_k2 > 1)
         ce = launch_splitk_combine(g2.partials, p.split_k2, P, so.slot_pos, topk_w, T, k, H,
-                                   static_cast<__nv_bfloat16 *>(out), pdl_enabled(kPdlCombine), st);
+                                   static_cast<__nv_bfloat16 *>(out), pdl_site(pdl, kPdlCombine), st);
     else
-        ce = launch_combine(g2.y, T, k, H, static_cast<__nv_bfloat16 *>(out), pdl_enabled(kPdlCombine), st);
-    mark(6, st);
-    t_stage_armed = false;
+        ce = launch_combine(g2.y, T, k, H, static_cast<__nv_bfloat16 *>(out), pdl_site(pdl, kPdlCombine), st);
+    mark(o, 6, st);
     return cuda_status(ce);
 }
 
@@ -569,8 +547,11 @@ static int train_layout(int T, int H, int I, int E, int k, TrainLayout &TL)
 
 static int backward_impl(const void *x, const void *W_router, const void *W_gate_up, const void *W_down,
                          const void *dout, int T, int H, int I, int E, int k, void *dx, float *dW_gate_up,
-                         float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes, cudaStream_t st)
+                         float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes,
+                         const moe_options_t &o, cudaStream_t st)
 {
+    if (check_options(o) != MOE_OK)
+        return MOE_ERR_INVALID_ARG;
     TrainLayout TL;
     int rc = train_layout(T, H, I, E, k, TL);
     if (rc != MOE_OK)
@@ -652,7 +633,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     // CTA pairs under the same rule as the forward's GEMMs
-    const bool pairs = use_pair(MOE_BF16, 1, T, k, E);
+    const bool pairs = use_pair(MOE_BF16, 1, T, k, E, o.gemm_pair);
     int64_t ub = p.max_blocks * (I / 256);
     if ((pairs ? launch_gemm_pair(3, 0, g3, (p.max_blocks / 2 + E) * (I / 256), st)
                : launch_gemm_backward_bf16(3, g3, (int)(ub < nsm ? ub : nsm), st)) != cudaSuccess)
@@ -734,36 +715,11 @@ const char *moe_status_string(int status)
 
 int moe_version(void) { return 100; }
 
-int moe_set_gemm_pair(int mode)
+int moe_options_init(moe_options_t *options)
 {
-    if (mode < -1 || mode > 1)
+    if (!options)
         return MOE_ERR_INVALID_ARG;
-    g_pair_mode.store(mode, std::memory_order_relaxed);
-    return MOE_OK;
-}
-
-int moe_set_one_stage(int mode)
-{
-    if (mode < 0 || mode > 1)
-        return MOE_ERR_INVALID_ARG;
-    g_one_stage.store(mode, std::memory_order_relaxed);
-    return MOE_OK;
-}
-
-int moe_set_stage_events(void *const *events, int n)
-{
-    if (!events) {
-        t_stage_armed = false;
-        return MOE_OK;
-    }
-    if (n < 7)
-        return MOE_ERR_INVALID_ARG;
-    for (int i = 0; i < 7; ++i) {
-        if (!events[i])
-            return MOE_ERR_INVALID_ARG;
-        t_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
-    }
-    t_stage_armed = true;
+    *options = default_options();
     return MOE_OK;
 }
 
@@ -876,9 +832,9 @@ int moe_workspace_status(const void *ws, int *status, void *stream)
 }
 
 int moe_route_topk(const void *x, const void *W_router, const float *bias, int T, int H, int E, int k,
-                   int32_t *topk_ids, float *topk_weights, float *logits, void *stream)
+                   int renormalize, int32_t *topk_ids, float *topk_weights, float *logits, void *stream)
 {
-    if (T < 0 || H <= 0 || H % 8 != 0 || E <= 0 || k <= 0)
+    if (T < 0 || H <= 0 || H % 8 != 0 || E <= 0 || k <= 0 || renormalize < 0 || renormalize > 1)
         return MOE_ERR_INVALID_ARG;
     if (E > 1024 || k > E || k > 32)
         return MOE_ERR_UNSUPPORTED;
@@ -887,8 +843,9 @@ int moe_route_topk(const void *x, const void *W_router, const float *bias, int T
     if (!x || !W_router || !topk_ids || !topk_weights || !aligned(x, 16) || !aligned(W_router, 16))
         return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_router(static_cast<const __nv_bfloat16 *>(x),
-                                     static_cast<const __nv_bfloat16 *>(W_router), bias, T, H, E, k, topk_ids,
-                                     topk_weights, logits, nullptr, false, static_cast<cudaStream_t>(stream)));
+                                     static_cast<const __nv_bfloat16 *>(W_router), bias, T, H, E, k, renormalize,
+                                     topk_ids, topk_weights, logits, nullptr, 1 << kPdlTopk,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_align_sort_workspace_size(int T, int k, int E)
@@ -922,8 +879,8 @@ int moe_align_sort(const int32_t *topk_ids, const float *topk_weights, int T, in
     so.expert_counts = expert_counts;
     so.expert_offsets = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) +
                                                     align_up((int64_t)sort_scratch_bytes(T, k, E), kAlign));
-    return cuda_status(
-        launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, ws, false, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, ws, false, true,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int moe_quantize_fp8_act(const void *X, int64_t R, int C, uint8_t *q, float *s, void *stream)
@@ -967,7 +924,17 @@ int moe_fused_forward(int dtype, const void *x, const void *W_router, const floa
                       void *stream)
 {
     return forward_impl(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
-                        block_m, split_k, out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+                        block_m, split_k, out, ws, ws_bytes, default_options(), static_cast<cudaStream_t>(stream));
+}
+
+int moe_fused_forward_ex(int dtype, const void *x, const void *W_router, const float *router_bias,
+                         const void *W_gate_up, const void *w1_scale, const void *W_down, const void *w2_scale, int T,
+                         int H, int I, int E, int k, int block_m, int split_k, void *out, void *ws, size_t ws_bytes,
+                         const moe_options_t *options, void *stream)
+{
+    return forward_impl(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
+                        block_m, split_k, out, ws, ws_bytes, options ? *options : default_options(),
+                        static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_train_workspace_size(int T, int H, int I, int E, int k)
@@ -980,8 +947,10 @@ size_t moe_train_workspace_size(int T, int H, int I, int E, int k)
 
 int moe_fused_forward_train(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
                             const void *W_down, int T, int H, int I, int E, int k, void *out, void *ws,
-                            size_t ws_bytes, void *stream)
+                            size_t ws_bytes, const moe_options_t *options, void *stream)
 {
+    if (options && check_options(*options) != MOE_OK)
+        return MOE_ERR_INVALID_ARG;
     TrainLayout TL;
     int rc = train_layout(T, H, I, E, k, TL);
     if (rc != MOE_OK)
@@ -989,20 +958,24 @@ int moe_fused_forward_train(const void *x, const void *W_router, const float *ro
     if (!ws || (size_t)TL.total > ws_bytes)
         return !ws ? MOE_ERR_INVALID_ARG : MOE_ERR_WORKSPACE;
     return forward_impl(MOE_BF16, x, W_router, router_bias, W_gate_up, nullptr, W_down, nullptr, T, H, I, E, k, 128,
-                        0, out, ws, TL.plan.workspace_bytes, static_cast<cudaStream_t>(stream),
+                        0, out, ws, TL.plan.workspace_bytes, options ? *options : default_options(),
+                        static_cast<cudaStream_t>(stream),
                         reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) + TL.gu));
 }
 
 int moe_fused_backward(const void *x, const void *W_router, const float *router_bias, const void *W_gate_up,
                        const void *W_down, const void *dout, int T, int H, int I, int E, int k, void *dx,
                        float *dW_gate_up, float *dW_down, float *dW_router, float *dbias, void *ws, size_t ws_bytes,
-                       void *stream)
+                       const moe_options_t *options, void *stream)
 {
+    if (options && check_options(*options) != MOE_OK)
+        return MOE_ERR_INVALID_ARG;
     (void)router_bias;  // enters the backward only through the routing kept by the training forward
     if (T == 0)
         return MOE_OK;
     return backward_impl(x, W_router, W_gate_up, W_down, dout, T, H, I, E, k, dx, dW_gate_up, dW_down, dW_router,
-                         dbias, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+                         dbias, ws, ws_bytes, options ? *options : default_options(),
+                         static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_host_staging_bytes(int T, int H)
@@ -1038,7 +1011,7 @@ int moe_fused_forward_host(int dtype, const void *x_host, const void *W_router, 
     if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     rc = forward_impl(dtype, x_dev, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
-                      block_m, split_k, out_dev, ws, need, st);
+                      block_m, split_k, out_dev, ws, need, default_options(), st);
     if (rc != MOE_OK)
         return rc;
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)

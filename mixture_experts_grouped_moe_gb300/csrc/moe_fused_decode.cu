@@ -98,8 +98,9 @@ __device__ __forceinline__ int ld_acquire(const int *p)
     return v;
 }
 
-// Wait (bounded) until *p >= target; false (status raised) on timeout or abort.
-__device__ __forceinline__ bool wait_count(const int *p, int target, int *status, volatile int *abort)
+// Wait (bounded by limit_ns) until *p >= target; false (status raised) on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int *p, int target, unsigned long long limit_ns, int *status,
+                                           volatile int *abort)
 {
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
@@ -109,7 +110,7 @@ __device__ __forceinline__ bool wait_count(const int *p, int target, int *status
         if ((it & 63u) == 63u) {
             if (*abort)
                 return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicExch(status, -5 /* MOE_ERR_TIMEOUT */);
                 *abort = 1;
                 return false;
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
     pdl_trigger();
     const int n1 = tiles_of(F.s1, 1);
     const int ntiles = n1 + tiles_of(F.s2, 2);
-    const int h_target = n1 * kEpiWarps;  // epilogue warps of all stage-1 tiles
+    const int h_target = n1 * kEpiWarps + F.h_extra;  // epilogue warps of all stage-1 tiles
 
     if (warp == 0) {
         // ------------------------------------------------- producer (whole warp)
@@ -232,12 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
                         // h is written by every stage-1 epilogue: wait for all of them once
                         bool h_ok = true;
                         if (lane == 0) {
-                            h_ok = wait_count(F.h_done, h_target, status, abort_flag);
+                            h_ok = wait_count(F.h_done, h_target, F.h_wait_ns, status, abort_flag);
                             if (h_ok)
                                 asm volatile("fence.proxy.async.global;" ::: "memory");
                         }
                         h_ok = __shfl_sync(0xffffffffu, (int)h_ok, 0) != 0;
                         if (!h_ok) {
+                            // This stage's phase expects the h rows' bytes and the lanes' copy
+                            // arrivals, which will not come now: retire both, so that the phase
+                            // completes exactly when its weight copies have landed (the drain
+                            // below waits for that before the CTA exits).
+                            if (lane == 0)
+                                mbar_complete_tx(&sm.full[s], (uint32_t)tl.nx * 128);
+                            cp_async_arrive(&sm.full[s]);
                             ok = false;
                             break;
                         }
@@ -432,7 +440,7 @@ cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused::kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    return launch_kernel(pdl_enabled(kPdlStage1, false), kern, dim3(grid), dim3(fused::kThreads), fused::kSmemBytes,
+    return launch_kernel(pdl_site(F.s1.pdl_mask, kPdlStage1), kern, dim3(grid), dim3(fused::kThreads), fused::kSmemBytes,
                          st, F);
 }
 

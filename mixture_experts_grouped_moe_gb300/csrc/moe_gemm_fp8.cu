@@ -480,7 +480,7 @@ cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err != cudaSuccess)
         return err;
-    return launch_kernel(pdl_enabled(STAGE == 1 ? kPdlStage1 : kPdlStage2, true), kern, dim3(grid),
+    return launch_kernel(pdl_site(a.pdl_mask, STAGE == 1 ? kPdlStage1 : kPdlStage2), kern, dim3(grid),
                          dim3(kThreads), kSmemBytes, st, a);
 }
 

@@ -31,7 +31,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #endif
 
-// Launch boundaries that may overlap (bit i of MOE_PDL_MASK, default all):
+// Launch boundaries that may overlap (bit i of moe_options_t::pdl_mask):
 enum PdlSite {
     kPdlSort = 0,     // router/top-k -> sort, and inside the sort
     kPdlGather = 1,   // sort -> gather
@@ -43,12 +43,15 @@ enum PdlSite {
                       // before reading anything; it starts early only after a kernel that
                       // triggers, such as the previous layer call's combine)
 };
-// Whether launches at this site use programmatic serialisation: environment
-// MOE_PDL=0 turns it off everywhere, MOE_PDL_MASK (hex) selects sites.
-// Default: every site, except the two GEMM boundaries in grouped mode, where
-// an early-resident persistent GEMM measured slower (Mixtral prefill 3.94 ms
-// without vs 4.38 ms with) while swap mode gains from it.
-bool pdl_enabled(int site, bool grouped = false);
+constexpr int kPdlAll = 0x7f;
+// The default set: every boundary, except the two GEMM boundaries in grouped
+// mode, where an early-resident persistent GEMM measured slower (Mixtral
+// prefill 3.94 ms without vs 4.38 ms with) while swap mode gains from it.
+inline int pdl_default_mask(bool grouped)
+{
+    return grouped ? kPdlAll & ~((1 << kPdlStage1) | (1 << kPdlStage2)) : kPdlAll;
+}
+inline bool pdl_site(int mask, int site) { return (mask >> site) & 1; }
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -78,8 +81,11 @@ constexpr int kStatusWords = 4;
 // `status` (nullable) points at kStatusWords words that the first kernel
 // zeroes.  `pdl` applies to the first launch.
 bool router_needs_logits(int T, int E);
+// renorm: 1 softmax over the k selected, 0 softmax over all E evaluated at the selected.
+// pdl_mask: sites kPdlRouter (the first launch) and kPdlTopk (the top-k pass).
 cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
-                          int k, int32_t *ids, float *wts, float *logits, int *status, bool pdl, cudaStream_t st);
+                          int k, int renorm, int32_t *ids, float *wts, float *logits, int *status, int pdl_mask,
+                          cudaStream_t st);
 
 // Chunked stable counting sort; ws holds nchunks*E int32 chunk counters.
 constexpr int kSortChunk = 1024;
@@ -96,8 +102,11 @@ struct SortOut {
     int32_t *num_active;      // [1] (may be null)
     int32_t *slot_pos;        // [S] sorted position of each slot (may be null)
 };
+// pdl_first: the first launch follows another kernel of this library; pdl_inner: the
+// chunked sort's second and third launches.  An id outside [0, E) is left out of every
+// segment and sets *num_post_padded to -1.
 cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
-                              const SortOut &o, void *scratch, bool pdl, cudaStream_t st);
+                              const SortOut &o, void *scratch, bool pdl_first, bool pdl_inner, cudaStream_t st);
 
 // x rows gathered into sorted order (zero rows for padding), up to *npp rows.
 cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
@@ -157,6 +166,7 @@ struct GemmArgs {
     __nv_bfloat16 *dgu;      // backward of stage 2: dg | du [P_max][2I]
     float *dw_out;           // weight gradient (STAGE 5, segment mode): [E][M][N] fp32
     int M;                   // segment mode: rows of the A operand (output rows)
+    int pdl_mask;            // launch boundaries with programmatic serialisation (PdlSite bits)
 };
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
@@ -164,7 +174,7 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
 
 int num_sms_current_device();
 
-// The GEMMs are always launched with programmatic serialisation (they follow another kernel).
+// The GEMM launchers take their programmatic-serialisation choice from a.pdl_mask.
 cudaError_t launch_gemm_grouped_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_swap_bf16(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_gemm_grouped_fp8(int stage, const GemmArgs &a, int grid, cudaStream_t st);
@@ -178,6 +188,8 @@ struct FusedArgs {
     int *h_done;
     const __nv_bfloat16 *x;  // the layer input [T][H]: stage-1 token rows are fetched from it directly
     int k;                   // top-k (slot s belongs to token s / k)
+    unsigned long long h_wait_ns;  // limit of the stage-2 tiles' wait for the intermediate
+    int h_extra;             // added to that wait's target (1 only to test the timeout path)
 };
 cudaError_t launch_fused_decode(const FusedArgs &F, int grid, cudaStream_t st);
 // Training (bf16): backward GEMMs -- which = 3: dh = dY W_down with

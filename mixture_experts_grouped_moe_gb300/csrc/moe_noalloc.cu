@@ -4,11 +4,9 @@
 // library's own device memory instead of a caller-provided workspace.
 //
 // The array's name in host code is only a host-side stand-in for the device
-// symbol, never a device address, so its address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and that
-// pointer is what the kernels receive.
-#include <mutex>
-
+// symbol, never a device address, so its address on the current device is
+// looked up with cudaGetSymbolAddress and that pointer is what the kernels
+// receive.
 #include "moe_internal.h"
 
 namespace moe {
@@ -20,24 +18,17 @@ constexpr int64_t kScratchInts = MOE_NOALLOC_SORT_SCRATCH_BYTES / 4;
 // Every GPU that loads the library holds this array until the process exits.
 static __device__ __align__(256) int32_t g_sort_scratch[kScratchInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int32_t *g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_sort_scratch on the current device (looked up once per device).
+// Device address of g_sort_scratch on the current device, looked up on every call: the
+// lookup allocates nothing and costs far less than the sort, and a cached address would go
+// stale after cudaDeviceReset, when the module (and this array) is loaded again in a new
+// primary context, possibly elsewhere.  The first lookup on a device may load the library's
+// device code there.
 int scratch_on_current_device(int32_t **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sort_scratch) != cudaSuccess || !p)
         return MOE_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_sort_scratch) != cudaSuccess || !p)
-            return MOE_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<int32_t *>(p);
-    }
-    *out = g_scratch_ptr[dev];
+    *out = static_cast<int32_t *>(p);
     return MOE_OK;
 }
 
@@ -77,6 +68,7 @@ extern "C" int moe_align_sort_noalloc(const int32_t *topk_ids, const float *topk
     so.expert_counts = expert_counts;
     so.expert_offsets = scratch + off_at;
     const cudaError_t err =
-        launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, scratch, false, static_cast<cudaStream_t>(stream));
+        launch_align_sort(topk_ids, topk_weights, T, k, E, block_m, so, scratch, false, true,
+                          static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -61,9 +61,10 @@ __device__ __forceinline__ float butterfly_sum(float v)
 }
 
 // Top k of one token's E logits by one warp (larger logit first, the lower
-// expert on ties), then the softmax over the k selected.  k <= 32, E <= 1024.
-__device__ __forceinline__ void warp_topk_softmax(const float *lg, int E, int k, int lane, int32_t *ids_out,
-                                                  float *w_out)
+// expert on ties), then the softmax over the k selected (renorm = 1) or over
+// all E, evaluated at the selected (renorm = 0).  k <= 32, E <= 1024.
+__device__ __forceinline__ void warp_topk_softmax(const float *lg, int E, int k, int renorm, int lane,
+                                                  int32_t *ids_out, float *w_out)
 {
     uint32_t taken = 0;  // bit m: expert lane + 32m already selected
     float my_v = 0.0f;
@@ -99,8 +100,16 @@ __device__ __forceinline__ void warp_topk_softmax(const float *lg, int E, int k,
     const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
     float sum = 0.0f;
-    for (int j = 0; j < k; ++j)
-        sum += __shfl_sync(0xffffffffu, ex, j);
+    if (renorm) {
+        for (int j = 0; j < k; ++j)
+            sum += __shfl_sync(0xffffffffu, ex, j);
+    } else {
+        for (int e = lane; e < E; e += 32)
+            sum += expf(lg[e] - vmax);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    }
     if (lane < k) {
         ids_out[lane] = my_e;
         w_out[lane] = ex / sum;
@@ -114,7 +123,7 @@ template <int TT, int EG, int UNR>
 __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16 *__restrict__ x,
                                                            const __nv_bfloat16 *__restrict__ Wr,
                                                            const float *__restrict__ bias, int T, int H, int E,
-                                                           int k, int32_t *__restrict__ ids,
+                                                           int k, int renorm, int32_t *__restrict__ ids,
                                                            float *__restrict__ wts, float *__restrict__ logits_out,
                                                            int *status)
 {
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(const __nv_bfloat16 *
         if (logits_out)
             for (int e = lane; e < E; e += 32)
                 logits_out[(size_t)tok * E + e] = lg[e];
-        warp_topk_softmax(lg, E, k, lane, ids + (size_t)tok * k, wts + (size_t)tok * k);
+        warp_topk_softmax(lg, E, k, renorm, lane, ids + (size_t)tok * k, wts + (size_t)tok * k);
     }
 }
 
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const __nv_bfloat16 *
         }
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E, int k,
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm,
                                                   int32_t *__restrict__ ids, float *__restrict__ wts)
 {
     pdl_wait();
@@ -314,7 +323,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (tok >= T)
         return;
-    warp_topk_softmax(logits + (size_t)tok * E, E, k, threadIdx.x & 31, ids + (size_t)tok * k, wts + (size_t)tok * k);
+    warp_topk_softmax(logits + (size_t)tok * E, E, k, renorm, threadIdx.x & 31, ids + (size_t)tok * k,
+                      wts + (size_t)tok * k);
 }
 
 bool router_needs_logits(int T, int E) { return (long)T * E > 64L * 64; }
@@ -333,19 +343,22 @@ static cudaError_t launch_router_tiled(const __nv_bfloat16 *x, const __nv_bfloat
 }
 
 cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
-                          int k, int32_t *ids, float *wts, float *logits, int *status, bool pdl, cudaStream_t st)
+                          int k, int renorm, int32_t *ids, float *wts, float *logits, int *status, int pdl_mask,
+                          cudaStream_t st)
 {
     if (T <= 0)
         return cudaSuccess;
+    const bool pdl = pdl_site(pdl_mask, kPdlRouter);
     if (!router_needs_logits(T, E) || !logits) {
         if ((long)T * E <= 64L * 64) {
             constexpr int TT = 2;
             return launch_kernel(pdl, router_small_kernel<TT, 1, 8>, dim3((T + TT - 1) / TT), dim3(256),
-                                 sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, ids, wts, logits, status);
+                                 sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, renorm, ids, wts, logits,
+                                 status);
         }
         constexpr int TT = 8;
         return launch_kernel(pdl, router_small_kernel<TT, 4, 2>, dim3((T + TT - 1) / TT), dim3(256),
-                             sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, ids, wts, logits, status);
+                             sizeof(float) * TT * E, st, x, Wr, bias, T, H, E, k, renorm, ids, wts, logits, status);
     }
     cudaError_t err;
     if (E <= 8)
@@ -356,8 +369,8 @@ cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const
         err = launch_router_tiled<4, 16, 4, 2>(x, Wr, bias, T, H, E, logits, status, pdl, st);
     if (err != cudaSuccess)
         return err;
-    return launch_kernel(pdl_enabled(kPdlTopk), topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T, E, k,
-                         ids, wts);
+    return launch_kernel(pdl_site(pdl_mask, kPdlTopk), topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T,
+                         E, k, renorm, ids, wts);
 }
 
 // ============================================================ align-sort
@@ -413,11 +426,15 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
     pdl_wait();
     pdl_trigger();
     const int e = threadIdx.x;
+    bool bad_id = false;
     if (e < S) {
         s_ids[e] = ids[e];
         s_w[e] = wts[e];  // staged so the per-expert scatter below waits on no global load
+        bad_id = (unsigned)s_ids[e] >= (unsigned)E;
     }
-    __syncthreads();
+    // an id outside [0, E) matches no expert below, so its slot is left out; it is reported
+    // through num_post_padded = -1
+    const bool any_bad = __syncthreads_or(bad_id);
     int cnt = 0;
     if (e < E)
         for (int s = 0; s < S; ++s)
@@ -453,7 +470,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t *__restr
             o.sorted_expert_ids[b] = e;
     }
     if (e == 0) {
-        *o.num_post_padded = total;
+        *o.num_post_padded = any_bad ? -1 : total;
         if (o.expert_offsets)
             o.expert_offsets[E] = total;
         if (o.num_active)
@@ -479,11 +496,13 @@ __global__ void __launch_bounds__(256) sort_few_kernel(const int32_t *__restrict
     __shared__ int s_total;
     pdl_wait();
     pdl_trigger();
+    bool bad_id = false;
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         s_ids[i] = ids[i];
         s_w[i] = wts[i];
+        bad_id |= (unsigned)s_ids[i] >= (unsigned)E;  // matches no expert below: left out, reported
     }
-    __syncthreads();
+    const bool any_bad = __syncthreads_or(bad_id);
     if (threadIdx.x < 32) {
         const int e = threadIdx.x;
         int cnt = 0;
@@ -529,7 +548,7 @@ __global__ void __launch_bounds__(256) sort_few_kernel(const int32_t *__restrict
                 o.sorted_expert_ids[b] = e;
         }
         if (e == 0) {
-            *o.num_post_padded = total;
+            *o.num_post_padded = any_bad ? -1 : total;
             if (o.expert_offsets)
                 o.expert_offsets[E] = total;
             if (o.num_active)
@@ -559,8 +578,11 @@ __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restr
         s_hist[e] = 0;
     __syncthreads();
     const int s = blockIdx.x * kSortChunk + threadIdx.x;
-    if (s < S)
-        atomicAdd(&s_hist[ids[s]], 1);
+    if (s < S) {
+        const int e = ids[s];
+        if ((unsigned)e < (unsigned)E)  // a bad id is not counted; the scan sees the shortfall
+            atomicAdd(&s_hist[e], 1);
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         cc[(size_t)blockIdx.x * E + e] = s_hist[e];
@@ -570,14 +592,17 @@ __global__ void __launch_bounds__(1024) sort_count_kernel(const int32_t *__restr
     }
 }
 
-__global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ cc, int nchunks, int E, int B,
-                                                        int64_t NB_max, SortOut o)
+__global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ cc, int nchunks, int S, int E,
+                                                        int B, int64_t NB_max, SortOut o)
 {
     __shared__ int32_t s_pad[1024];
     __shared__ int32_t s_act[1024];
+    __shared__ int s_counted;
     pdl_wait();
     pdl_trigger();
     const int e = threadIdx.x;
+    if (e == 0)
+        s_counted = 0;
     int cnt = 0;
     if (e < E) {
         for (int c = 0; c < nchunks; ++c) {
@@ -590,6 +615,8 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ c
     s_pad[e] = pad;
     s_act[e] = (e < E && cnt > 0) ? 1 : 0;
     __syncthreads();
+    if (cnt)
+        atomicAdd(&s_counted, cnt);  // fewer than S counted slots: some id was outside [0, E)
     scan2_1024(s_pad, s_act);
     const int pad_incl = s_pad[e];
     const int pad_excl = pad_incl - pad;
@@ -604,7 +631,7 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ c
     }
     const int total = s_pad[1023];
     if (e == 0) {
-        *o.num_post_padded = total;
+        *o.num_post_padded = (s_counted == S) ? total : -1;
         o.expert_offsets[E] = total;
         if (o.num_active)
             *o.num_active = s_act[1023];
@@ -625,8 +652,9 @@ __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t *__res
         s_wc[i] = 0;
     __syncthreads();
     const int s = blockIdx.x * kSortChunk + threadIdx.x;
-    const bool valid = s < S;
-    const int e = valid ? ids[s] : -1;
+    const int e_in = s < S ? ids[s] : -1;
+    const bool valid = (unsigned)e_in < (unsigned)E;  // past S or a bad id: not placed
+    const int e = valid ? e_in : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (valid && rank == 0)
@@ -652,7 +680,7 @@ __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t *__res
 
 // o.expert_offsets must be non-null (the scatter reads it).
 cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
-                              const SortOut &o, void *scratch, bool pdl, cudaStream_t st)
+                              const SortOut &o, void *scratch, bool pdl, bool pdl_inner, cudaStream_t st)
 {
     const int S = T * k;
     const int64_t P_max = (int64_t)S + (int64_t)E * block_m - k;
@@ -669,8 +697,8 @@ cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k
                                     S, E, cc, o.sorted_ids, o.sorted_weights, P_max);
     if (err != cudaSuccess)
         return err;
-    err = launch_kernel(pdl_enabled(kPdlSort), sort_scan_kernel, dim3(1), dim3(1024), 0, st, cc, nchunks, E, block_m,
-                        NB_max, o);
+    err = launch_kernel(pdl_inner, sort_scan_kernel, dim3(1), dim3(1024), 0, st, cc, nchunks, S, E, block_m, NB_max,
+                        o);
     if (err != cudaSuccess)
         return err;
     const size_t smem = sizeof(int32_t) * 32 * E;
@@ -679,8 +707,7 @@ cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k
         if (err != cudaSuccess)
             return err;
     }
-    return launch_kernel(pdl_enabled(kPdlSort), sort_scatter_kernel, dim3(nchunks), dim3(1024), smem, st, ids, wts, S,
-                         E, cc, o);
+    return launch_kernel(pdl_inner, sort_scatter_kernel, dim3(nchunks), dim3(1024), smem, st, ids, wts, S, E, cc, o);
 }
 
 // ================================================================ gather

@@ -74,6 +74,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return done != 0;
 }
 
+// Retire `bytes` of the current phase's expected transaction count without a
+// copy (for bytes announced with expect_tx whose copies will not be issued),
+// so that the phase completes once the copies that were issued have landed.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (after recording a timeout in *status and raising *abort) if it does not
 // within the limit, or if another role of the CTA has already aborted.

@@ -33,9 +33,9 @@ EXPORTED = [
     "moe_ksplit_heuristic", "moe_plan", "moe_fused_workspace_size", "moe_workspace_layout",
     "moe_workspace_status", "moe_route_topk", "moe_align_sort_workspace_size", "moe_align_sort",
     "moe_quantize_fp8_act", "moe_quantize_fp8_weights", "moe_quantize_fp8_rows", "moe_fused_forward",
-    "moe_host_staging_bytes", "moe_fused_forward_host", "moe_set_stage_events", "moe_align_sort_noalloc",
-    "moe_set_gemm_pair", "moe_quantize_mxfp4", "moe_set_one_stage", "moe_train_workspace_size",
-    "moe_fused_forward_train", "moe_fused_backward",
+    "moe_host_staging_bytes", "moe_fused_forward_host", "moe_align_sort_noalloc", "moe_quantize_mxfp4",
+    "moe_train_workspace_size", "moe_fused_forward_train", "moe_fused_backward", "moe_options_init",
+    "moe_fused_forward_ex",
 ]
 
 
@@ -49,6 +49,12 @@ class moe_plan_t(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("block_m", ctypes.c_int), ("split_k1", ctypes.c_int),
                 ("split_k2", ctypes.c_int), ("max_padded", ctypes.c_int64), ("max_blocks", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t)]
+
+
+class moe_options_t(ctypes.Structure):
+    _fields_ = [("gemm_pair", ctypes.c_int), ("one_stage", ctypes.c_int), ("pdl_mask", ctypes.c_int),
+                ("stage_events", ctypes.c_void_p), ("h_wait_limit_us", ctypes.c_uint),
+                ("unsatisfiable_h_wait", ctypes.c_int)]
 
 
 class moe_ws_layout_t(ctypes.Structure):
@@ -89,7 +95,7 @@ def load(build_if_missing: bool = False):
             "moe_fused_workspace_size": (SZ, [I, I, I, I, I, I, I, I]),
             "moe_workspace_layout": (I, [I, I, I, I, I, I, I, I, P]),
             "moe_workspace_status": (I, [P, P, P]),
-            "moe_route_topk": (I, [P, P, P, I, I, I, I, P, P, P, P]),
+            "moe_route_topk": (I, [P, P, P, I, I, I, I, I, P, P, P, P]),
             "moe_align_sort_workspace_size": (SZ, [I, I, I]),
             "moe_align_sort": (I, [P, P, I, I, I, I, P, P, P, P, P, P, SZ, P]),
             "moe_quantize_fp8_act": (I, [P, I64, I, P, P, P]),
@@ -98,12 +104,11 @@ def load(build_if_missing: bool = False):
             "moe_fused_forward": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
             "moe_host_staging_bytes": (SZ, [I, I]),
             "moe_fused_forward_host": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P]),
-            "moe_set_stage_events": (I, [P, I]),
-            "moe_set_gemm_pair": (I, [I]),
-            "moe_set_one_stage": (I, [I]),
+            "moe_options_init": (I, [P]),
+            "moe_fused_forward_ex": (I, [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, SZ, P, P]),
             "moe_train_workspace_size": (SZ, [I, I, I, I, I]),
-            "moe_fused_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]),
-            "moe_fused_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, SZ, P]),
+            "moe_fused_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, SZ, P, P]),
+            "moe_fused_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, SZ, P, P]),
             "moe_quantize_mxfp4": (I, [P, I64, I, P, P, I, P]),
             "moe_align_sort_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         }
@@ -189,9 +194,11 @@ def moe_workspace_status(ws, stream=None) -> int:
     return v.value
 
 
-def moe_route_topk(x, W_router, bias, T, H, E, k, topk_ids, topk_weights, logits=None, stream=None):
+def moe_route_topk(x, W_router, bias, T, H, E, k, topk_ids, topk_weights, logits=None, stream=None,
+                   renormalize=True):
     return _check("moe_route_topk", load().moe_route_topk(
-        _p(x), _p(W_router), _p(bias), T, H, E, k, _p(topk_ids), _p(topk_weights), _p(logits), _stream(stream)))
+        _p(x), _p(W_router), _p(bias), T, H, E, k, 1 if renormalize else 0, _p(topk_ids), _p(topk_weights),
+        _p(logits), _stream(stream)))
 
 
 def moe_align_sort_workspace_size(T, k, E) -> int:
@@ -250,14 +257,53 @@ def moe_fused_forward_host(dtype, x_host, W_router, router_bias, W_gate_up, w1_s
         T, H, I, E, k, block_m, split_k, _p(out_host), _p(ws), ws_bytes, _stream(stream)))
 
 
-def moe_set_gemm_pair(mode: int):
-    """Grouped-mode GEMM kernel choice: 1 CTA pairs, 0 one-SM, -1 automatic (process-wide)."""
-    return _check("moe_set_gemm_pair", load().moe_set_gemm_pair(mode))
+class Options:
+    """Per-call choices of moe_fused_forward_ex (see moe_options_t in include/moe.h).
+
+    Keyword arguments override the library's defaults: gemm_pair (-1/0/1), one_stage (0/1),
+    pdl_mask (-1 or a mask), stage_events (7 torch.cuda.Event or None), h_wait_limit_us,
+    unsatisfiable_h_wait (0/1, for the timeout test only)."""
+
+    def __init__(self, **kw):
+        self.c = moe_options_t()
+        _check("moe_options_init", load().moe_options_init(ctypes.byref(self.c)))
+        self._events = None
+        for key, val in kw.items():
+            setattr(self, key, val)
+
+    def __setattr__(self, key, val):
+        if key in ("c", "_events"):
+            object.__setattr__(self, key, val)
+        elif key == "stage_events":
+            if val is None:
+                self._events = None
+                self.c.stage_events = None
+            else:
+                arr = (ctypes.c_void_p * len(val))(*[e.cuda_event for e in val])
+                self._events = (arr, list(val))  # keep both alive while the options are in use
+                self.c.stage_events = ctypes.cast(arr, ctypes.c_void_p)
+        elif key in dict(moe_options_t._fields_):
+            setattr(self.c, key, val)
+        else:
+            raise AttributeError(key)
+
+    def __getattr__(self, key):
+        if key in dict(moe_options_t._fields_):
+            return getattr(self.c, key)
+        raise AttributeError(key)
 
 
-def moe_set_one_stage(mode: int):
-    """One-kernel bf16 decode path: 1 on, 0 off (process-wide)."""
-    return _check("moe_set_one_stage", load().moe_set_one_stage(mode))
+def _opt(options):
+    if options is None:
+        return None
+    return ctypes.byref(options.c if isinstance(options, Options) else options)
+
+
+def moe_fused_forward_ex(dtype, x, W_router, router_bias, W_gate_up, w1_scale, W_down, w2_scale, T, H, I, E, k,
+                         block_m, split_k, out, ws, ws_bytes, options=None, stream=None):
+    return _check("moe_fused_forward_ex", load().moe_fused_forward_ex(
+        dtype, _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(w1_scale), _p(W_down), _p(w2_scale),
+        T, H, I, E, k, block_m, split_k, _p(out), _p(ws), ws_bytes, _opt(options), _stream(stream)))
 
 
 def moe_train_workspace_size(T, H, I, E, k) -> int:
@@ -265,25 +311,26 @@ def moe_train_workspace_size(T, H, I, E, k) -> int:
 
 
 def moe_fused_forward_train(x, W_router, router_bias, W_gate_up, W_down, T, H, I, E, k, out, ws, ws_bytes,
-                            stream=None):
+                            options=None, stream=None):
     return _check("moe_fused_forward_train", load().moe_fused_forward_train(
         _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(W_down), T, H, I, E, k, _p(out), _p(ws), ws_bytes,
-        _stream(stream)))
+        _opt(options), _stream(stream)))
 
 
 def moe_fused_backward(x, W_router, router_bias, W_gate_up, W_down, dout, T, H, I, E, k, dx, dW_gate_up, dW_down,
-                       dW_router, dbias, ws, ws_bytes, stream=None):
+                       dW_router, dbias, ws, ws_bytes, options=None, stream=None):
     return _check("moe_fused_backward", load().moe_fused_backward(
         _p(x), _p(W_router), _p(router_bias), _p(W_gate_up), _p(W_down), _p(dout), T, H, I, E, k, _p(dx),
-        _p(dW_gate_up), _p(dW_down), _p(dW_router), _p(dbias), _p(ws), ws_bytes, _stream(stream)))
+        _p(dW_gate_up), _p(dW_down), _p(dW_router), _p(dbias), _p(ws), ws_bytes, _opt(options), _stream(stream)))
 
 
 class MoETrain:
     """Owns the training workspace of one bf16 layer shape: forward(), then backward()."""
 
-    def __init__(self, T, H, I, E, k, device="cuda"):
+    def __init__(self, T, H, I, E, k, device="cuda", options=None):
         import torch
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.options = options
         self.ws_bytes = moe_train_workspace_size(T, H, I, E, k)
         if self.ws_bytes == 0:
             raise MoEError("moe_train_workspace_size", MOE_ERR_INVALID_ARG)
@@ -291,7 +338,7 @@ class MoETrain:
 
     def forward(self, x, w, out, stream=None):
         moe_fused_forward_train(x, w["W_router"], w.get("bias"), w["W_gate_up"], w["W_down"], self.T, self.H, self.I,
-                                self.E, self.k, out, self.ws, self.ws_bytes, stream)
+                                self.E, self.k, out, self.ws, self.ws_bytes, self.options, stream)
         return out
 
     def backward(self, x, w, dout, stream=None):
@@ -305,19 +352,11 @@ class MoETrain:
              "dbias": torch.empty(self.E, dtype=torch.float32, device=dev)}
         moe_fused_backward(x, w["W_router"], w.get("bias"), w["W_gate_up"], w["W_down"], dout, self.T, self.H, self.I,
                            self.E, self.k, g["dx"], g["dW_gate_up"], g["dW_down"], g["dW_router"], g["dbias"], self.ws,
-                           self.ws_bytes, stream)
+                           self.ws_bytes, self.options, stream)
         return g
 
     def status(self, stream=None) -> int:
         return moe_workspace_status(self.ws, stream)
-
-
-def moe_set_stage_events(events):
-    """Arm per-stage timing events (7 torch.cuda.Event(enable_timing=True)) for the next forward call."""
-    if events is None:
-        return _check("moe_set_stage_events", load().moe_set_stage_events(None, 0))
-    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
-    return _check("moe_set_stage_events", load().moe_set_stage_events(arr, len(events)))
 
 
 # ------------------------------------------------------------- conveniences
@@ -329,9 +368,10 @@ class FusedMoE:
     tensors); for FP8 also w1_scale, w2_scale and e4m3 (uint8) weight stacks.
     """
 
-    def __init__(self, dtype, T, H, I, E, k, block_m=0, split_k=0, device="cuda", host_staging=False):
+    def __init__(self, dtype, T, H, I, E, k, block_m=0, split_k=0, device="cuda", host_staging=False, options=None):
         import torch
         self.dtype, self.T, self.H, self.I, self.E, self.k = dtype, T, H, I, E, k
+        self.options = options  # None (library defaults) or an Options
         self.block_m, self.split_k = block_m, split_k
         self.plan = moe_plan(dtype, T, H, I, E, k, block_m, split_k)
         self.ws_bytes = moe_fused_workspace_size(dtype, T, H, I, E, k, block_m, split_k)
@@ -341,10 +381,17 @@ class FusedMoE:
         self.ws = torch.empty(self.ws_bytes + extra, dtype=torch.uint8, device=device)
         self.layout = moe_workspace_layout(dtype, T, H, I, E, k, block_m, split_k)
 
-    def __call__(self, x, w, out, stream=None):
-        moe_fused_forward(self.dtype, x, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
-                          w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k, self.block_m,
-                          self.split_k, out, self.ws, self.ws_bytes, stream)
+    def __call__(self, x, w, out, stream=None, options=None):
+        """One forward; `options` (an Options) overrides the layer's own for this call."""
+        opts = options if options is not None else self.options
+        if opts is None:
+            moe_fused_forward(self.dtype, x, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
+                              w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k, self.block_m,
+                              self.split_k, out, self.ws, self.ws_bytes, stream)
+        else:
+            moe_fused_forward_ex(self.dtype, x, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
+                                 w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k, self.block_m,
+                                 self.split_k, out, self.ws, self.ws_bytes, opts, stream)
         return out
 
     def forward_host(self, x_host, w, out_host, stream=None):

@@ -67,12 +67,13 @@ def _load():
         lib.oracle_quant_mx4_mt.argtypes = [P, ctypes.c_long, i, P, P, i]
         lib.oracle_router_logit.restype = ctypes.c_float
         lib.oracle_router_logit.argtypes = [P, P, i, P, i]
-        lib.oracle_route.argtypes = [P, P, P, i, i, i, i, P, P, P, i]
+        lib.oracle_route.argtypes = [P, P, P, i, i, i, i, i, P, P, P, i]
         lib.oracle_align_sort.argtypes = [P, i, i, i, i, P, P, P, P]
         lib.oracle_moe_forward_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_fp8_token.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_forward_mxfp4.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
+        lib.oracle_moe_forward_expert_major.argtypes = [i, P, P, P, P, P, P, P, i, i, i, i, i, P, i, P, i]
         lib.oracle_moe_backward_bf16.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, P, P, P, P, i]
         _lib = lib
         return lib
@@ -192,8 +193,11 @@ def router_logit(x_row_bits, w_row_bits, bias=None, e: int = 0) -> np.float32:
     return np.float32(_load().oracle_router_logit(_ptr(x), _ptr(w), x.shape[-1], _ptr(b), e))
 
 
-def route(x_bits, Wr_bits, bias, k: int, nthreads: int | None = None):
-    """Gating + top-k (AITER page, section 3): ids [T,k] int32, weights [T,k] fp64, logits [T,E] fp32."""
+def route(x_bits, Wr_bits, bias, k: int, nthreads: int | None = None, renormalize: bool = True):
+    """Gating + top-k (AITER page, section 3): ids [T,k] int32, weights [T,k] fp64, logits [T,E] fp32.
+
+    renormalize=True: softmax over the k selected (the layer's weights); False: softmax over all E
+    evaluated at the selected experts."""
     x = _u16(x_bits)
     Wr = _u16(Wr_bits)
     T, H = x.shape
@@ -202,7 +206,8 @@ def route(x_bits, Wr_bits, bias, k: int, nthreads: int | None = None):
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     logits = np.empty((T, E), np.float32)
-    _load().oracle_route(_ptr(x), _ptr(Wr), _ptr(b), T, H, E, k, _ptr(ids), _ptr(w), _ptr(logits),
+    _load().oracle_route(_ptr(x), _ptr(Wr), _ptr(b), T, H, E, k, 1 if renormalize else 0, _ptr(ids), _ptr(w),
+                         _ptr(logits),
                          nthreads or default_threads())
     return ids, w, logits
 
@@ -231,9 +236,26 @@ def align_sort(ids, E: int, B: int):
 
 # --------------------------------------------------------------- forward
 
+def _expert_major(mode, x, Wr, bias, Wgu, s1, Wd, s2, k, tok, nthreads):
+    """The same layer evaluated expert by expert (bit-identical to the per-token loop)."""
+    T, H = x.shape
+    E, twoI, _ = Wgu.shape
+    I = twoI // 2
+    out = np.empty((len(tok), H), np.float64)
+    rc = _load().oracle_moe_forward_expert_major(mode, _ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu), _ptr(s1),
+                                                 _ptr(Wd), _ptr(s2), T, H, I, E, k, _ptr(tok), len(tok), _ptr(out),
+                                                 nthreads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle expert-major scratch")
+    return out
+
+
 def moe_forward_bf16(x_bits, Wr_bits, bias, Wgu_bits, Wd_bits, k: int, tokens=None,
-                     nthreads: int | None = None) -> np.ndarray:
-    """bf16 fused MoE layer (fp64 accumulation) for `tokens` (all if None): out [n, H] fp64."""
+                     nthreads: int | None = None, expert_major: bool = False) -> np.ndarray:
+    """bf16 fused MoE layer (fp64 accumulation) for `tokens` (all if None): out [n, H] fp64.
+
+    expert_major=True evaluates the same sums in the same order expert by expert (faster for many
+    tokens; bit-identical results)."""
     x = _u16(x_bits)
     Wr = _u16(Wr_bits)
     Wgu = _u16(Wgu_bits)
@@ -242,6 +264,8 @@ def moe_forward_bf16(x_bits, Wr_bits, bias, Wgu_bits, Wd_bits, k: int, tokens=No
     E, twoI, _ = Wgu.shape
     I = twoI // 2
     tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    if expert_major:
+        return _expert_major(0, x, Wr, bias, Wgu, None, Wd, None, k, tok, nthreads)
     out = np.empty((len(tok), H), np.float64)
     _load().oracle_moe_forward_bf16(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu), _ptr(Wd), T, H, I, E, k,
                                     _ptr(tok), len(tok), _ptr(out), nthreads or default_threads())
@@ -249,7 +273,7 @@ def moe_forward_bf16(x_bits, Wr_bits, bias, Wgu_bits, Wd_bits, k: int, tokens=No
 
 
 def moe_forward_fp8(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens=None,
-                    nthreads: int | None = None) -> np.ndarray:
+                    nthreads: int | None = None, expert_major: bool = False) -> np.ndarray:
     """Block-scaled FP8 fused MoE layer for `tokens`: out [n, H] fp64.
 
     Wgu_q [E,2I,H] / Wd_q [E,H,I] e4m3 codes with scales w1s [E*2I/128, H/128], w2s [E*H/128, I/128]."""
@@ -261,6 +285,8 @@ def moe_forward_fp8(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens
     E, twoI, _ = Wgu_q.shape
     I = twoI // 2
     tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    if expert_major:
+        return _expert_major(1, x, Wr, bias, Wgu_q, _f32(w1s), Wd_q, _f32(w2s), k, tok, nthreads)
     out = np.empty((len(tok), H), np.float64)
     _load().oracle_moe_forward_fp8(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(_f32(w1s)),
                                    _ptr(Wd_q), _ptr(_f32(w2s)), T, H, I, E, k, _ptr(tok), len(tok),
@@ -269,7 +295,7 @@ def moe_forward_fp8(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens
 
 
 def moe_forward_fp8_token(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, tokens=None,
-                          nthreads: int | None = None) -> np.ndarray:
+                          nthreads: int | None = None, expert_major: bool = False) -> np.ndarray:
     """Per-token FP8 fused MoE layer for `tokens`: out [n, H] fp64.
 
     Wgu_q [E,2I,H] / Wd_q [E,H,I] e4m3 codes with one scale per output channel: w1s [E*2I], w2s [E*H]."""
@@ -281,6 +307,8 @@ def moe_forward_fp8_token(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, 
     E, twoI, _ = Wgu_q.shape
     I = twoI // 2
     tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    if expert_major:
+        return _expert_major(2, x, Wr, bias, Wgu_q, _f32(w1s), Wd_q, _f32(w2s), k, tok, nthreads)
     out = np.empty((len(tok), H), np.float64)
     _load().oracle_moe_forward_fp8_token(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(_f32(w1s)),
                                          _ptr(Wd_q), _ptr(_f32(w2s)), T, H, I, E, k, _ptr(tok), len(tok),
@@ -289,7 +317,7 @@ def moe_forward_fp8_token(x_bits, Wr_bits, bias, Wgu_q, w1s, Wd_q, w2s, k: int, 
 
 
 def moe_forward_mxfp4(x_bits, Wr_bits, bias, Wgu_q, w1x, Wd_q, w2x, k: int, tokens=None,
-                      nthreads: int | None = None) -> np.ndarray:
+                      nthreads: int | None = None, expert_major: bool = False) -> np.ndarray:
     """MXFP4 fused MoE layer for `tokens`: out [n, H] fp64.
 
     Wgu_q [E,2I,H] / Wd_q [E,H,I] E2M1 codes (one per byte) with E8M0 scales w1x [E*2I, H/32], w2x [E*H, I/32]."""
@@ -303,6 +331,8 @@ def moe_forward_mxfp4(x_bits, Wr_bits, bias, Wgu_q, w1x, Wd_q, w2x, k: int, toke
     E, twoI, _ = Wgu_q.shape
     I = twoI // 2
     tok = np.arange(T, dtype=np.int64) if tokens is None else np.ascontiguousarray(tokens, np.int64)
+    if expert_major:
+        return _expert_major(3, x, Wr, bias, Wgu_q, w1x, Wd_q, w2x, k, tok, nthreads)
     out = np.empty((len(tok), H), np.float64)
     _load().oracle_moe_forward_mxfp4(_ptr(x), _ptr(Wr), _ptr(_f32(bias)), _ptr(Wgu_q), _ptr(w1x), _ptr(Wd_q),
                                      _ptr(w2x), T, H, I, E, k, _ptr(tok), len(tok), _ptr(out),

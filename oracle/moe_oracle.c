@@ -329,9 +329,11 @@ float oracle_router_logit(const uint16_t *x, const uint16_t *w, int H, const flo
 /*
  * Top-k on the logits (largest first; an equal logit goes to the lower
  * expert index), then softmax over the k selected logits, which is the same
- * as softmax over all E followed by top-k and renormalisation.
+ * as softmax over all E followed by top-k and renormalisation (renorm = 1);
+ * with renorm = 0 the weights are the softmax over all E experts evaluated
+ * at the selected ones (they need not sum to 1).
  */
-static void route_token(const float *logit, int E, int k, int32_t *ids, double *w)
+static void route_token_r(const float *logit, int E, int k, int renorm, int32_t *ids, double *w)
 {
     for (int j = 0; j < k; ++j) {
         int best = -1;
@@ -353,14 +355,25 @@ static void route_token(const float *logit, int E, int k, int32_t *ids, double *
         w[j] = exp((double)logit[ids[j]] - lmax);
         sum += w[j];
     }
+    if (!renorm) {
+        sum = 0.0;
+        for (int e = 0; e < E; ++e)
+            sum += exp((double)logit[e] - lmax);
+    }
     for (int j = 0; j < k; ++j)
         w[j] /= sum;
+}
+
+/* The layer's routing: renormalised over the k selected. */
+static void route_token(const float *logit, int E, int k, int32_t *ids, double *w)
+{
+    route_token_r(logit, E, k, 1, ids, w);
 }
 
 typedef struct {
     const uint16_t *x, *Wr;
     const float *bias;
-    int T, H, E, k;
+    int T, H, E, k, renorm;
     int32_t *ids;
     double *w;
     float *logits;
@@ -376,7 +389,7 @@ static void *route_worker(void *arg)
             l[e] = oracle_router_logit(J->x + (size_t)t * J->H, J->Wr + (size_t)e * J->H, J->H, J->bias, e);
         if (J->logits)
             memcpy(J->logits + (size_t)t * J->E, l, sizeof(float) * J->E);
-        route_token(l, J->E, J->k, J->ids + (size_t)t * J->k, J->w + (size_t)t * J->k);
+        route_token_r(l, J->E, J->k, J->renorm, J->ids + (size_t)t * J->k, J->w + (size_t)t * J->k);
     }
     free(l);
     return NULL;
@@ -393,8 +406,8 @@ static int clamp_threads(int nthreads, int work)
     return nthreads < 1 ? 1 : nthreads;
 }
 
-/* ids [T,k] int32, w [T,k] fp64, logits [T,E] fp32 (nullable). */
-int oracle_route(const uint16_t *x, const uint16_t *Wr, const float *bias, int T, int H, int E, int k,
+/* ids [T,k] int32, w [T,k] fp64, logits [T,E] fp32 (nullable); renorm as in route_token_r. */
+int oracle_route(const uint16_t *x, const uint16_t *Wr, const float *bias, int T, int H, int E, int k, int renorm,
                  int32_t *ids, double *w, float *logits, int nthreads)
 {
     if (T <= 0)
@@ -403,7 +416,7 @@ int oracle_route(const uint16_t *x, const uint16_t *Wr, const float *bias, int T
     pthread_t th[256];
     route_job jobs[256];
     for (int i = 0; i < nthreads; ++i) {
-        route_job J = {x, Wr, bias, T, H, E, k, ids, w, logits,
+        route_job J = {x, Wr, bias, T, H, E, k, renorm, ids, w, logits,
                        (int)((long)T * i / nthreads), (int)((long)T * (i + 1) / nthreads)};
         jobs[i] = J;
         pthread_create(&th[i], NULL, route_worker, &jobs[i]);
@@ -452,6 +465,52 @@ int oracle_align_sort(const int32_t *ids, int T, int k, int E, int B, int32_t *s
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
+/*
+ * Quantisation of the SwiGLU output a[0..I) between the two stages, as the
+ * two-stage path does it (the intermediate is quantised before the down
+ * projection): mode 1 per 1x128 group (e4m3, scale amax/448), mode 2 one
+ * scale for the whole row (per token), mode 3 MXFP4 per 1x32 group; mode 0
+ * keeps the value.  a is replaced by the dequantised value.
+ */
+static void requant_inter(int mode, double *a, int I)
+{
+    if (mode == 1) {
+        for (int gi = 0; gi < I / 128; ++gi) {
+            float amax = 0.0f;
+            for (int i = gi * 128; i < gi * 128 + 128; ++i) {
+                float v = fabsf((float)a[i]);
+                if (v > amax)
+                    amax = v;
+            }
+            float sc = group_scale(amax);
+            for (int i = gi * 128; i < gi * 128 + 128; ++i)
+                a[i] = oracle_e4m3_decode(oracle_e4m3_encode((float)a[i] / sc)) * (double)sc;
+        }
+    } else if (mode == 3) {
+        for (int gi = 0; gi < I / 32; ++gi) {
+            float amax = 0.0f;
+            for (int i = gi * 32; i < gi * 32 + 32; ++i) {
+                float v = fabsf((float)a[i]);
+                if (v > amax)
+                    amax = v;
+            }
+            int ex = oracle_mx_exponent(amax);
+            for (int i = gi * 32; i < gi * 32 + 32; ++i)
+                a[i] = ldexp(oracle_e2m1_decode(oracle_e2m1_encode((float)ldexp((double)(float)a[i], -ex))), ex);
+        }
+    } else if (mode == 2) {
+        float amax = 0.0f;
+        for (int i = 0; i < I; ++i) {
+            float v = fabsf((float)a[i]);
+            if (v > amax)
+                amax = v;
+        }
+        float sc = group_scale(amax);
+        for (int i = 0; i < I; ++i)
+            a[i] = oracle_e4m3_decode(oracle_e4m3_encode((float)a[i] / sc)) * (double)sc;
+    }
+}
+
 typedef struct {
     int mode; /* 0 bf16, 1 fp8 per 128x128 / 1x128 blocks, 2 fp8 per row, 3 mxfp4 per 1x32 */
     const uint16_t *x, *Wr;
@@ -466,6 +525,8 @@ typedef struct {
     double *out; /* [n, H] */
 } fwd_job;
 
+static void token_input(int mode, const uint16_t *xrow, int H, double *xt, uint8_t *xq, float *xs, uint8_t *xsx);
+
 static void *fwd_worker(void *arg)
 {
     fwd_job *J = (fwd_job *)arg;
@@ -477,7 +538,6 @@ static void *fwd_worker(void *arg)
     double *a = (double *)malloc(sizeof(double) * I);
     uint8_t *xq = (uint8_t *)malloc(H);
     float *xs = (float *)malloc(sizeof(float) * (H / 128 + 1));
-    uint8_t *aq = (uint8_t *)malloc(I);
     uint8_t *xsx = (uint8_t *)malloc(H / 32 + 1);
     for (int n = J->n0; n < J->n1; ++n) {
         long t = (long)J->tokens[n];
@@ -485,22 +545,7 @@ static void *fwd_worker(void *arg)
         for (int e = 0; e < E; ++e)
             l[e] = oracle_router_logit(xrow, J->Wr + (size_t)e * H, H, J->bias, e);
         route_token(l, E, k, ids, w);
-        if (J->mode == 0) {
-            for (int h = 0; h < H; ++h)
-                xt[h] = bf16_to_float(xrow[h]);
-        } else if (J->mode == 1) {
-            oracle_quant_1x128(xrow, 1, H, xq, xs);
-            for (int h = 0; h < H; ++h)
-                xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[h / 128];
-        } else if (J->mode == 2) {
-            oracle_quant_rows(xrow, 1, H, xq, xs);
-            for (int h = 0; h < H; ++h)
-                xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[0];
-        } else {
-            oracle_quant_mx4(xrow, 1, H, xq, xsx);
-            for (int h = 0; h < H; ++h)
-                xt[h] = mx4_value(xq, xsx, h, H);
-        }
+        token_input(J->mode, xrow, H, xt, xq, xs, xsx);
         double *o = J->out + (size_t)n * H;
         for (int h = 0; h < H; ++h)
             o[h] = 0.0;
@@ -539,48 +584,7 @@ static void *fwd_worker(void *arg)
                 }
                 a[i] = silu(g) * u;
             }
-            if (J->mode == 1) {
-                /* the intermediate is re-quantised per 1x128 group before the
-                 * down projection (two-stage path, quantised between stages) */
-                for (int gi = 0; gi < I / 128; ++gi) {
-                    float amax = 0.0f;
-                    for (int i = gi * 128; i < gi * 128 + 128; ++i) {
-                        float v = fabsf((float)a[i]);
-                        if (v > amax)
-                            amax = v;
-                    }
-                    float sc = group_scale(amax);
-                    for (int i = gi * 128; i < gi * 128 + 128; ++i) {
-                        aq[i] = oracle_e4m3_encode((float)a[i] / sc);
-                        a[i] = oracle_e4m3_decode(aq[i]) * (double)sc;
-                    }
-                }
-            } else if (J->mode == 3) {
-                /* MXFP4 between the stages: each 1x32 group of the intermediate row */
-                for (int gi = 0; gi < I / 32; ++gi) {
-                    float amax = 0.0f;
-                    for (int i = gi * 32; i < gi * 32 + 32; ++i) {
-                        float v = fabsf((float)a[i]);
-                        if (v > amax)
-                            amax = v;
-                    }
-                    int ex = oracle_mx_exponent(amax);
-                    for (int i = gi * 32; i < gi * 32 + 32; ++i)
-                        a[i] = ldexp(oracle_e2m1_decode(oracle_e2m1_encode((float)ldexp((double)(float)a[i], -ex))),
-                                     ex);
-                }
-            } else if (J->mode == 2) {
-                /* per-token: one scale for the token's whole intermediate row */
-                float amax = 0.0f;
-                for (int i = 0; i < I; ++i) {
-                    float v = fabsf((float)a[i]);
-                    if (v > amax)
-                        amax = v;
-                }
-                float sc = group_scale(amax);
-                for (int i = 0; i < I; ++i)
-                    a[i] = oracle_e4m3_decode(oracle_e4m3_encode((float)a[i] / sc)) * (double)sc;
-            }
+            requant_inter(J->mode, a, I);
             for (int h = 0; h < H; ++h) {
                 double y = 0.0;
                 size_t rd = ((size_t)e * H + h) * I;
@@ -610,7 +614,6 @@ static void *fwd_worker(void *arg)
     free(a);
     free(xq);
     free(xs);
-    free(aq);
     free(xsx);
     return NULL;
 }
@@ -753,6 +756,331 @@ int oracle_moe_forward_mxfp4(const uint16_t *x, const uint16_t *Wr, const float 
     J.tokens = tokens;
     J.out = out;
     return run_forward(J, n_tokens, nthreads);
+}
+
+/* ------------------------------------------- forward, expert by expert */
+/*
+ * The same layer as the per-token loop above, evaluated expert by expert so
+ * that each weight row, once dequantised, serves up to EM_SLOTS slots of the
+ * expert (the route-then-group view of the fused-MoE pages: tokens reordered
+ * by expert, each expert's rows multiplied by its weights).  Every output
+ * value is the same sum in the same order as in the per-token loop:
+ *   g, u  = sum over h ascending of (dequantised weight * x), from 0.0
+ *   y     = sum over i ascending of (dequantised down weight * a), from 0.0
+ *   out_t = sum over j ascending of w_j * y_j, from 0.0
+ * so the results are bit-identical to it; only the loop nest is reordered
+ * (the slot index innermost), which is what makes full-size comparisons of
+ * thousands of tokens affordable.  Tokens are taken in waves that bound the
+ * per-slot buffer of y.
+ */
+#define EM_SLOTS 16
+
+static double g_e4m3_tab[256];
+static double g_e2m1_tab[16];
+static double g_pow2_tab[256]; /* 2^(b - 127): the value of E8M0 byte b */
+static pthread_once_t g_tab_once = PTHREAD_ONCE_INIT;
+
+static void init_tables(void)
+{
+    for (int c = 0; c < 256; ++c)
+        g_e4m3_tab[c] = oracle_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 16; ++c)
+        g_e2m1_tab[c] = oracle_e2m1_decode((uint8_t)c);
+    for (int b = 0; b < 256; ++b)
+        g_pow2_tab[b] = ldexp(1.0, b - 127); /* exact: 2^-127 .. 2^128 are normal doubles */
+}
+
+/*
+ * Row `row` of a weight stack viewed as [rows][len] (len = the reduction
+ * length), dequantised to fp64 exactly as the per-token loop does it: bf16
+ * value; e4m3 code * scale of its 128x128 block; e4m3 code * scale of the
+ * row; E2M1 code * 2^(E8M0 - 127) of its 1x32 group (the power of two is
+ * exact, so this equals ldexp).
+ */
+static void dequant_row(int mode, const uint16_t *Wb, const uint8_t *Wq, const float *ws, const uint8_t *wx,
+                        size_t row, int len, double *out)
+{
+    if (mode == 0) {
+        const uint16_t *r = Wb + row * (size_t)len;
+        for (int h = 0; h < len; ++h)
+            out[h] = (double)bf16_to_float(r[h]);
+    } else if (mode == 1) {
+        const uint8_t *r = Wq + row * (size_t)len;
+        const float *sb = ws + row / 128 * (size_t)(len / 128);
+        for (int h = 0; h < len; ++h)
+            out[h] = g_e4m3_tab[r[h]] * (double)sb[h / 128];
+    } else if (mode == 2) {
+        const uint8_t *r = Wq + row * (size_t)len;
+        const double sr = ws[row];
+        for (int h = 0; h < len; ++h)
+            out[h] = g_e4m3_tab[r[h]] * sr;
+    } else {
+        const uint8_t *r = Wq + row * (size_t)len;
+        const uint8_t *sx = wx + row * (size_t)(len / 32);
+        for (int h = 0; h < len; ++h)
+            out[h] = g_e2m1_tab[r[h] & 15] * g_pow2_tab[sx[h / 32]];
+    }
+}
+
+/* The token row x_t as the expert GEMMs see it (bf16, or dequantised codes). */
+static void token_input(int mode, const uint16_t *xrow, int H, double *xt, uint8_t *xq, float *xs, uint8_t *xsx)
+{
+    if (mode == 0) {
+        for (int h = 0; h < H; ++h)
+            xt[h] = bf16_to_float(xrow[h]);
+    } else if (mode == 1) {
+        oracle_quant_1x128(xrow, 1, H, xq, xs);
+        for (int h = 0; h < H; ++h)
+            xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[h / 128];
+    } else if (mode == 2) {
+        oracle_quant_rows(xrow, 1, H, xq, xs);
+        for (int h = 0; h < H; ++h)
+            xt[h] = oracle_e4m3_decode(xq[h]) * (double)xs[0];
+    } else {
+        oracle_quant_mx4(xrow, 1, H, xq, xsx);
+        for (int h = 0; h < H; ++h)
+            xt[h] = mx4_value(xq, xsx, h, H);
+    }
+}
+
+typedef struct {
+    fwd_job f;          /* weights, shape, mode */
+    const int64_t *tok; /* tokens of this wave */
+    int nw;
+    double *xt;         /* [nw][H] */
+    int32_t *ids;       /* [nw][k] */
+    double *w;          /* [nw][k] */
+    double *Y;          /* [nw][k][H] */
+    double *out;        /* [nw][H] */
+    int32_t *slots;     /* wave slots n*k + j grouped by expert, ascending within an expert */
+    int32_t *item_e, *item_first, *item_len;
+    int n_items;
+    int next;           /* next unclaimed unit of the current phase */
+    int phase;          /* 0 route + inputs, 1 expert items, 2 combine */
+    pthread_mutex_t mu;
+} em_state;
+
+static int em_claim(em_state *S, int limit)
+{
+    pthread_mutex_lock(&S->mu);
+    int i = S->next < limit ? S->next++ : -1;
+    pthread_mutex_unlock(&S->mu);
+    return i;
+}
+
+/* acc[s] = sum over h ascending of w[h] * X[h][s], from 0.0, for the EM_SLOTS columns of X [n][EM_SLOTS]. */
+__attribute__((noinline)) static void em_dot(const double *w, const double *X, int n, double *acc)
+{
+    double a[EM_SLOTS];
+    for (int s = 0; s < EM_SLOTS; ++s)
+        a[s] = 0.0;
+    for (int h = 0; h < n; ++h) {
+        const double wh = w[h];
+        const double *xr = X + (size_t)h * EM_SLOTS;
+        for (int s = 0; s < EM_SLOTS; ++s)
+            a[s] += wh * xr[s];
+    }
+    for (int s = 0; s < EM_SLOTS; ++s)
+        acc[s] = a[s];
+}
+
+static void em_item(em_state *S, int it, double *Xt, double *wg, double *wu, double *At, double *acol)
+{
+    const fwd_job *J = &S->f;
+    const int H = J->H, I = J->I, k = J->k, mode = J->mode;
+    const int e = S->item_e[it], nb = S->item_len[it];
+    const int32_t *sl = S->slots + S->item_first[it];
+    for (int h = 0; h < H; ++h)
+        for (int s = 0; s < EM_SLOTS; ++s)
+            Xt[(size_t)h * EM_SLOTS + s] = s < nb ? S->xt[(size_t)(sl[s] / k) * H + h] : 0.0;
+    for (int i = 0; i < I; ++i) {
+        dequant_row(mode, J->Wgu, J->Wgu_q, J->w1s, J->w1x, (size_t)e * 2 * I + i, H, wg);
+        dequant_row(mode, J->Wgu, J->Wgu_q, J->w1s, J->w1x, (size_t)e * 2 * I + I + i, H, wu);
+        double g[EM_SLOTS], u[EM_SLOTS];
+        em_dot(wg, Xt, H, g);
+        em_dot(wu, Xt, H, u);
+        for (int s = 0; s < EM_SLOTS; ++s)
+            At[(size_t)i * EM_SLOTS + s] = silu(g[s]) * u[s];
+    }
+    if (mode != 0) {
+        for (int s = 0; s < nb; ++s) {
+            for (int i = 0; i < I; ++i)
+                acol[i] = At[(size_t)i * EM_SLOTS + s];
+            requant_inter(mode, acol, I);
+            for (int i = 0; i < I; ++i)
+                At[(size_t)i * EM_SLOTS + s] = acol[i];
+        }
+    }
+    for (int h = 0; h < H; ++h) {
+        dequant_row(mode, J->Wd, J->Wd_q, J->w2s, J->w2x, (size_t)e * H + h, I, wg);
+        double y[EM_SLOTS];
+        em_dot(wg, At, I, y);
+        for (int s = 0; s < nb; ++s)
+            S->Y[(size_t)sl[s] * H + h] = y[s];
+    }
+}
+
+static void *em_worker(void *arg)
+{
+    em_state *S = (em_state *)arg;
+    const fwd_job *J = &S->f;
+    const int H = J->H, I = J->I, E = J->E, k = J->k;
+    if (S->phase == 0) {
+        float *l = (float *)malloc(sizeof(float) * E);
+        uint8_t *xq = (uint8_t *)malloc(H);
+        float *xs = (float *)malloc(sizeof(float) * (H / 128 + 1));
+        uint8_t *xsx = (uint8_t *)malloc(H / 32 + 1);
+        for (int n; (n = em_claim(S, S->nw)) >= 0;) {
+            const uint16_t *xrow = J->x + (size_t)S->tok[n] * H;
+            for (int e = 0; e < E; ++e)
+                l[e] = oracle_router_logit(xrow, J->Wr + (size_t)e * H, H, J->bias, e);
+            route_token(l, E, k, S->ids + (size_t)n * k, S->w + (size_t)n * k);
+            token_input(J->mode, xrow, H, S->xt + (size_t)n * H, xq, xs, xsx);
+        }
+        free(l);
+        free(xq);
+        free(xs);
+        free(xsx);
+    } else if (S->phase == 1) {
+        const int L = H > I ? H : I;
+        double *Xt = (double *)malloc(sizeof(double) * (size_t)H * EM_SLOTS);
+        double *At = (double *)malloc(sizeof(double) * (size_t)I * EM_SLOTS);
+        double *wg = (double *)malloc(sizeof(double) * L);
+        double *wu = (double *)malloc(sizeof(double) * L);
+        double *acol = (double *)malloc(sizeof(double) * I);
+        for (int it; (it = em_claim(S, S->n_items)) >= 0;)
+            em_item(S, it, Xt, wg, wu, At, acol);
+        free(Xt);
+        free(At);
+        free(wg);
+        free(wu);
+        free(acol);
+    } else {
+        for (int n; (n = em_claim(S, S->nw)) >= 0;) {
+            double *o = S->out + (size_t)n * H;
+            for (int h = 0; h < H; ++h)
+                o[h] = 0.0;
+            for (int j = 0; j < k; ++j) {
+                const double wj = S->w[(size_t)n * k + j];
+                const double *y = S->Y + ((size_t)n * k + j) * H;
+                for (int h = 0; h < H; ++h)
+                    o[h] += wj * y[h];
+            }
+        }
+    }
+    return NULL;
+}
+
+static void em_run_phase(em_state *S, int phase, int nthreads, int work)
+{
+    S->phase = phase;
+    S->next = 0;
+    int nt = clamp_threads(nthreads, work > 0 ? work : 1);
+    pthread_t th[256];
+    for (int i = 0; i < nt; ++i)
+        pthread_create(&th[i], NULL, em_worker, S);
+    for (int i = 0; i < nt; ++i)
+        pthread_join(th[i], NULL);
+}
+
+/*
+ * mode as in the per-token entries (0 bf16, 1 block FP8, 2 per-token FP8,
+ * 3 MXFP4) with the same weight and scale arguments (unused ones NULL).
+ * Returns 0, or -1 if scratch cannot be allocated.
+ */
+int oracle_moe_forward_expert_major(int mode, const uint16_t *x, const uint16_t *Wr, const float *bias,
+                                    const void *Wgu, const void *w1scale, const void *Wd, const void *w2scale,
+                                    int T, int H, int I, int E, int k, const int64_t *tokens, int n_tokens,
+                                    double *out, int nthreads)
+{
+    pthread_once(&g_tab_once, init_tables);
+    em_state S;
+    memset(&S, 0, sizeof S);
+    fwd_job *J = &S.f;
+    J->mode = mode;
+    J->x = x;
+    J->Wr = Wr;
+    J->bias = bias;
+    if (mode == 0) {
+        J->Wgu = (const uint16_t *)Wgu;
+        J->Wd = (const uint16_t *)Wd;
+    } else {
+        J->Wgu_q = (const uint8_t *)Wgu;
+        J->Wd_q = (const uint8_t *)Wd;
+    }
+    if (mode == 1 || mode == 2) {
+        J->w1s = (const float *)w1scale;
+        J->w2s = (const float *)w2scale;
+    } else if (mode == 3) {
+        J->w1x = (const uint8_t *)w1scale;
+        J->w2x = (const uint8_t *)w2scale;
+    }
+    J->T = T;
+    J->H = H;
+    J->I = I;
+    J->E = E;
+    J->k = k;
+    if (n_tokens <= 0)
+        return 0;
+    /* a wave keeps y of all its slots: at most ~512 MB */
+    long wave = (512L << 20) / ((long)k * H * (long)sizeof(double));
+    if (wave < 1)
+        wave = 1;
+    if (wave > n_tokens)
+        wave = n_tokens;
+    S.xt = (double *)malloc(sizeof(double) * (size_t)wave * H);
+    S.ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)wave * k);
+    S.w = (double *)malloc(sizeof(double) * (size_t)wave * k);
+    S.Y = (double *)malloc(sizeof(double) * (size_t)wave * k * H);
+    S.slots = (int32_t *)malloc(sizeof(int32_t) * (size_t)wave * k);
+    long max_items = (long)wave * k / EM_SLOTS + E + 1;
+    S.item_e = (int32_t *)malloc(sizeof(int32_t) * max_items);
+    S.item_first = (int32_t *)malloc(sizeof(int32_t) * max_items);
+    S.item_len = (int32_t *)malloc(sizeof(int32_t) * max_items);
+    int32_t *cnt = (int32_t *)calloc((size_t)E + 1, sizeof(int32_t));
+    int rc = 0;
+    if (!S.xt || !S.ids || !S.w || !S.Y || !S.slots || !S.item_e || !S.item_first || !S.item_len || !cnt)
+        rc = -1;
+    pthread_mutex_init(&S.mu, NULL);
+    for (long n0 = 0; rc == 0 && n0 < n_tokens; n0 += wave) {
+        S.tok = tokens + n0;
+        S.nw = (int)((n_tokens - n0) < wave ? (n_tokens - n0) : wave);
+        S.out = out + (size_t)n0 * H;
+        em_run_phase(&S, 0, nthreads, S.nw);
+        /* group the wave's slots by expert (ascending slot within an expert) */
+        for (int e = 0; e <= E; ++e)
+            cnt[e] = 0;
+        for (long s = 0; s < (long)S.nw * k; ++s)
+            cnt[S.ids[s] + 1]++;
+        for (int e = 0; e < E; ++e)
+            cnt[e + 1] += cnt[e];
+        S.n_items = 0;
+        for (int e = 0; e < E; ++e) {
+            int pos = cnt[e];
+            for (long s = 0; s < (long)S.nw * k; ++s)
+                if (S.ids[s] == e)
+                    S.slots[pos++] = (int32_t)s;
+            for (int f = cnt[e]; f < cnt[e + 1]; f += EM_SLOTS) {
+                S.item_e[S.n_items] = e;
+                S.item_first[S.n_items] = f;
+                S.item_len[S.n_items] = cnt[e + 1] - f < EM_SLOTS ? cnt[e + 1] - f : EM_SLOTS;
+                S.n_items++;
+            }
+        }
+        em_run_phase(&S, 1, nthreads, S.n_items);
+        em_run_phase(&S, 2, nthreads, S.nw);
+    }
+    pthread_mutex_destroy(&S.mu);
+    free(S.xt);
+    free(S.ids);
+    free(S.w);
+    free(S.Y);
+    free(S.slots);
+    free(S.item_e);
+    free(S.item_first);
+    free(S.item_len);
+    free(cnt);
+    return rc;
 }
 
 /* ------------------------------------------------------------ backward */

@@ -125,8 +125,9 @@ def test_entry_points_reject_null_before_cuda(moe):
                                  None, None, 0, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_fused_forward(1, 16, 16, None, 16, None, 16, None, 16, 128, 256, 4, 2, 0, 0,
                                  16, 256, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG  # FP8 needs scales
-    assert lib.moe_route_topk(None, None, None, 4, 128, 4, 2, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
-    assert lib.moe_route_topk(16, 16, None, 4, 12, 4, 2, 16, 16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_topk(None, None, None, 4, 128, 4, 2, 1, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_topk(16, 16, None, 4, 12, 4, 2, 1, 16, 16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_topk(16, 16, None, 4, 128, 4, 2, 2, 16, 16, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_align_sort(None, None, 4, 2, 4, 16, None, None, None, None, None, None, 0, None) == \
         moe.MOE_ERR_INVALID_ARG
     assert lib.moe_quantize_fp8_act(None, 4, 128, None, None, None) == moe.MOE_ERR_INVALID_ARG
@@ -137,6 +138,32 @@ def test_entry_points_reject_null_before_cuda(moe):
     # misaligned workspace
     assert lib.moe_fused_forward(0, 16, 16, None, 16, None, 16, None, 4, 128, 256, 4, 2, 0, 0,
                                  16, 264, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_options_defaults_and_validation(moe):
+    """Per-call options: the defaults, and out-of-range values rejected on the host before any CUDA call."""
+    o = moe.Options()
+    assert (o.gemm_pair, o.one_stage, o.pdl_mask, o.h_wait_limit_us, o.unsatisfiable_h_wait) == (-1, 1, -1, 0, 0)
+    assert o.c.stage_events is None
+    lib = moe.load()
+    assert lib.moe_options_init(None) == moe.MOE_ERR_INVALID_ARG
+    args = (0, 16, 16, None, 16, None, 16, None, 4, 128, 256, 4, 2, 0, 0, 16, 256, 1 << 30)
+    for bad in (dict(gemm_pair=2), dict(gemm_pair=-2), dict(one_stage=2), dict(pdl_mask=0x80), dict(pdl_mask=-2),
+                dict(unsatisfiable_h_wait=2)):
+        opt = moe.Options(**bad)
+        assert lib.moe_fused_forward_ex(*args, moe._opt(opt), None) == moe.MOE_ERR_INVALID_ARG, bad
+        assert lib.moe_fused_forward_train(16, 16, None, 16, 16, 4, 128, 256, 4, 2, 16, 256, 1 << 30,
+                                           moe._opt(opt), None) == moe.MOE_ERR_INVALID_ARG, bad
+
+
+def test_no_environment_knobs_or_process_switches(moe):
+    """The library reads no environment variables and exports no process-wide switches."""
+    import subprocess
+    lib_path = moe.library_path()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True).stdout
+    assert "moe_set_gemm_pair" not in out and "moe_set_one_stage" not in out and "moe_set_stage_events" not in out
+    und = subprocess.run(["nm", "-D", "--undefined-only", lib_path], capture_output=True, text=True).stdout
+    assert "getenv" not in und
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -68,3 +68,35 @@ def test_traffic_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("other", "stage1") is None
     (csrc / "h.cuh").write_text("header v2")  # any source change voids the recorded traffic
     assert bench.profiled_traffic("w", "stage1") is None
+
+
+class _Plan:
+    mode, block_m, split_k2 = 1, 16, 7
+
+
+def test_summarize_reports_algorithmic_counts():
+    """The dominant kernel's roofline uses the layer definition's algorithmic bytes (weights of the
+    active experts and x once); implementation bytes (h round trip, split partials) are separate."""
+    cfg = synth.CONFIGS["mixtral_decode"]
+    stage_ms = {s: 0.01 for s in bench.STAGES}
+    stage_ms["stage1"] = 0.42
+    r = dict(ms=0.44, stage_ms=stage_ms, counts=[8] * 8, clocks=None, plan=_Plan, K=20, W=5, one_stage=True,
+             l2="inputs larger than L2")
+    peaks = {"hbm_gbs": 6700.0, "bf16_tflops": 1900.0}
+    d = bench.summarize(cfg, r, peaks, "measured", 1)
+    H, I, T = cfg.H, cfg.I, cfg.T
+    alg = 8 * 3 * H * I * 2 + T * H * 2
+    roof = d["roofline"]
+    assert roof["bound"] == "hbm" and roof["alg_bytes_per_launch"] == alg
+    assert abs(roof["achieved"] - alg / 0.42e-3 / 1e9) < 0.1
+    assert abs(roof["frac"] - roof["achieved"] / 6700.0) < 1e-4
+    assert roof["impl_bytes_per_launch"] > alg
+    assert d["layer_roofline"]["alg_bytes"] == alg + T * H * 2 + cfg.E * H * 2
+    assert d["gpu_launches"] == 4 * 20 and d["value"] == round(T / 0.44e-3, 2)
+    # a compute-bound workload reports tensor FLOPs of stage 1
+    cfg2 = synth.CONFIGS["mixtral_prefill"]
+    r2 = dict(r, one_stage=False, plan=type("P", (), {"mode": 0, "block_m": 128, "split_k2": 1}),
+              counts=[2048] * 8, ms=3.5)
+    d2 = bench.summarize(cfg2, r2, peaks, "measured", 1)
+    assert d2["roofline"]["bound"] == "tensor"
+    assert d2["roofline"]["alg_flops_per_launch"] == 2.0 * cfg2.S * 2 * cfg2.I * cfg2.H

@@ -28,8 +28,8 @@ def moe():
     return m
 
 
-def _run(moe, cfg, inp, dout):
-    tr = moe.MoETrain(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+def _run(moe, cfg, inp, dout, options=None):
+    tr = moe.MoETrain(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, options=options)
     w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
     tr.forward(inp["x"], w, out)
@@ -51,13 +51,13 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
-def test_backward_parity(moe, case):
+def test_backward_parity(moe, case, options=None):
     name, T, H, I, E, k, bias = case
     cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5)
     inp = synth.make_inputs(cfg, seed=17, device="cuda")
     dout = torch.randn(T, H, generator=torch.Generator(device="cuda").manual_seed(18), device="cuda").to(
         torch.bfloat16)
-    out, g = _run(moe, cfg, inp, dout)
+    out, g = _run(moe, cfg, inp, dout, options)
     host = {kk: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
             for kk, v in inp.items()}
     ref_out = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
@@ -99,8 +99,4 @@ def test_train_workspace_rejects_unsupported(moe):
 def test_backward_parity_cta_pairs(moe, case):
     """The same gradients with the CTA-pair GEMMs forced (training forward, both backward GEMMs, and
     the weight gradients whose row count is a multiple of 256)."""
-    moe.moe_set_gemm_pair(1)
-    try:
-        test_backward_parity(moe, case)
-    finally:
-        moe.moe_set_gemm_pair(-1)
+    test_backward_parity(moe, case, options=moe.Options(gemm_pair=1))

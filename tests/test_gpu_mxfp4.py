@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from mixture_experts_grouped_moe_gb300 import synth
-from moe_checks import rel_l2
+from moe_checks import check_rows, parity_tokens, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -209,14 +209,7 @@ def test_fused_mxfp4_prefill_parity(moe):
     q1, s1 = oracle.quant_mx4(host["W_gate_up"])
     q2, s2 = oracle.quant_mx4(host["W_down"])
     r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], cfg.k)
-    toks = set(synth.token_sample(cfg.T, 48).tolist())
-    counts = np.bincount(r_ids.ravel(), minlength=cfg.E)
-    smallest = np.argsort(counts, kind="stable")[:2]
-    toks.update([t for t in range(cfg.T) if set(r_ids[t].tolist()) & set(smallest.tolist())][:16])
-    toks = np.array(sorted(toks), np.int64)
-    ref = oracle.moe_forward_mxfp4(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks)
-    got = out.float().cpu().numpy()[toks]
-    assert np.isfinite(got).all()
-    err = rel_l2(got, ref)
-    print(f"mxfp4 prefill: relL2 {err:.3e} over {len(toks)} tokens")
-    assert err <= TOL_MX4
+    toks = parity_tokens(r_ids, cfg.E, layer.plan.block_m)
+    ref = oracle.moe_forward_mxfp4(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks,
+                                   expert_major=True)
+    check_rows(out.float().cpu().numpy()[toks], ref, TOL_MX4, label="mxfp4 T=4096")

@@ -1,7 +1,7 @@
 """Grouped-mode GEMMs on CTA pairs (two-SM tensor core) vs the one-SM kernels.
 
 Each case runs the fused layer with the kernel choice forced both ways
-(moe_set_gemm_pair 1 and 0): both must meet the tolerance against the
+(per-call option gemm_pair 1 and 0): both must meet the tolerance against the
 oracle, and the routing / sort outputs stay bit-exact.  The cases cover odd
 block counts per expert (half-used pairs), experts without tokens, a ragged
 last N tile of stage 2 and the Mixtral prefill shapes.
@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from mixture_experts_grouped_moe_gb300 import synth
-from moe_checks import rel_l2
+from moe_checks import check_rows, parity_tokens, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +23,7 @@ def moe():
     build.build()
     from mixture_experts_grouped_moe_gb300 import moe as m
     m.load()
-    yield m
-    m.moe_set_gemm_pair(-1)
+    return m
 
 
 def _host(inp):
@@ -32,8 +31,8 @@ def _host(inp):
             for k, v in inp.items()}
 
 
-def _run(moe, cfg, inp, w, dtype):
-    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+def _run(moe, cfg, inp, w, dtype, pair_mode):
+    layer = moe.FusedMoE(dtype, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, options=moe.Options(gemm_pair=pair_mode))
     assert layer.plan.mode == moe.MOE_MODE_GROUPED
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
     layer(inp["x"], w, out)
@@ -59,9 +58,8 @@ def test_bf16_grouped_both_kernels(moe, case, mode):
     cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5)
     inp = synth.make_inputs(cfg, seed=11, device="cuda")
     host = _host(inp)
-    moe.moe_set_gemm_pair(mode)
     w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
-    got, layer = _run(moe, cfg, inp, w, moe.MOE_BF16)
+    got, layer = _run(moe, cfg, inp, w, moe.MOE_BF16, mode)
     r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], k)
     assert np.array_equal(layer.view("topk_ids", torch.int32, (T, k)).cpu().numpy(), r_ids)
     ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
@@ -75,7 +73,6 @@ def test_fp8_token_grouped_both_kernels(moe, case, mode):
     cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="fp8_token")
     inp = synth.make_inputs(cfg, seed=12, device="cuda")
     host = _host(inp)
-    moe.moe_set_gemm_pair(mode)
     q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
     s1 = torch.empty(E * 2 * I, dtype=torch.float32, device="cuda")
     q2 = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
@@ -84,7 +81,7 @@ def test_fp8_token_grouped_both_kernels(moe, case, mode):
     moe.moe_quantize_fp8_rows(inp["W_down"], E * H, I, q2, s2)
     w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": q1, "w1_scale": s1, "W_down": q2,
          "w2_scale": s2}
-    got, _ = _run(moe, cfg, inp, w, moe.MOE_FP8_TOKEN)
+    got, _ = _run(moe, cfg, inp, w, moe.MOE_FP8_TOKEN, mode)
     o1, os1 = oracle.quant_rows(host["W_gate_up"])
     o2, os2 = oracle.quant_rows(host["W_down"])
     ref = oracle.moe_forward_fp8_token(host["x"], host["W_router"], host["bias"], o1, os1, o2, os2, k)
@@ -92,24 +89,27 @@ def test_fp8_token_grouped_both_kernels(moe, case, mode):
 
 
 def test_prefill_pair_matches_one_sm(moe):
-    """Mixtral prefill shapes: the two kernels agree closely on a token sample."""
+    """Mixtral prefill shapes: both kernels against the oracle on the full-size parity sample (every
+    M-block, the least-loaded experts, each expert's last row), and against each other on every token."""
     cfg = synth.CONFIGS["mixtral_prefill"]
     inp = synth.make_inputs(cfg, seed=0, device="cuda")
     w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
-    outs = []
-    for mode in (1, 0):
-        moe.moe_set_gemm_pair(mode)
-        got, _ = _run(moe, cfg, inp, w, moe.MOE_BF16)
-        outs.append(got)
-    moe.moe_set_gemm_pair(-1)
-    toks = synth.token_sample(cfg.T, 64).numpy()
+    outs = [_run(moe, cfg, inp, w, moe.MOE_BF16, mode)[0] for mode in (1, 0)]
     host = _host(inp)
+    r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], cfg.k)
+    toks = parity_tokens(r_ids, cfg.E, 128)
     ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
-                                  cfg.k, toks)
-    assert rel_l2(outs[0][toks], ref) <= 5e-3
+                                  cfg.k, toks, expert_major=True)
+    check_rows(outs[0][toks], ref, 5e-3, label="prefill pairs")
+    check_rows(outs[1][toks], ref, 5e-3, label="prefill one-SM")
     assert rel_l2(outs[0], outs[1]) <= 5e-3
 
 
-def test_set_gemm_pair_rejects_bad_mode(moe):
-    with pytest.raises(moe.MoEError):
-        moe.moe_set_gemm_pair(2)
+def test_gemm_pair_option_rejects_bad_value(moe):
+    cfg = synth.MoEConfig("bad", T=200, H=256, I=256, E=4, k=2)
+    inp = synth.make_inputs(cfg, seed=1, device="cuda")
+    layer = moe.FusedMoE(moe.MOE_BF16, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, options=moe.Options(gemm_pair=2))
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        layer(inp["x"], inp, out)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG

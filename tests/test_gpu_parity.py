@@ -3,9 +3,11 @@
 Integer outputs (expert ids, sort order, padding, FP8 codes) must match
 bit for bit; floating-point outputs must meet relative L2 error <= 5e-3
 (bf16) and <= 3e-2 (block-scaled FP8) against the oracle fed the same
-inputs; top-k weights within 1e-5 relative.  Large workloads compare every
-routing/sort output in full and the layer output on a seeded token sample
-plus the tokens of the least-loaded experts.
+inputs, and every compared token row within 4x that; top-k weights within
+1e-5 relative.  Large workloads compare every routing/sort output in full
+and the layer output on the full-size parity sample of moe_checks
+(512 seeded tokens, a row of every sorted M-block, the last row of every
+expert, the tokens of the least-loaded experts).
 """
 import math
 
@@ -15,7 +17,7 @@ import torch
 
 import oracle
 from mixture_experts_grouped_moe_gb300 import synth
-from moe_checks import check_sort_invariants, rel_l2
+from moe_checks import check_rows, check_sort_invariants, parity_tokens, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -77,15 +79,6 @@ def quantize_weights_gpu(moe, inp, cfg):
     return {"W_gate_up": q1, "w1_scale": s1, "W_down": q2, "w2_scale": s2}
 
 
-def sample_tokens(cfg, ids, n=64):
-    toks = set(synth.token_sample(cfg.T, n).tolist())
-    counts = np.bincount(ids.ravel(), minlength=cfg.E)
-    nonempty = [e for e in np.argsort(counts, kind="stable") if counts[e] > 0][:4]
-    extra = [t for t in range(cfg.T) if set(ids[t].tolist()) & set(nonempty)]
-    toks.update(extra[:32])
-    return np.array(sorted(toks), np.int64)
-
-
 # ---------------------------------------------------------------- router
 
 ROUTER_CASES = [
@@ -121,6 +114,14 @@ def test_router_parity(moe, cfg):
         counts = np.bincount(r_ids.ravel(), minlength=E)
         assert (counts == 0).sum() >= 1
         assert (counts > 0.05 * cfg.S).sum() >= 2
+    # the softmax over all E at the selected experts (renormalize = 0): same ids
+    ids3 = torch.empty_like(ids)
+    w3 = torch.empty_like(w)
+    moe.moe_route_topk(inp["x"], inp["W_router"], inp["bias"], T, cfg.H, E, k, ids3, w3, logits, renormalize=False)
+    torch.cuda.synchronize()
+    _, r_w3, _ = oracle.route(xb, wb, b, k, renormalize=False)
+    assert torch.equal(ids3, ids)
+    np.testing.assert_allclose(w3.cpu().numpy(), r_w3, rtol=1e-5, atol=1e-7)
     if T * E > 4096 and T <= 2048:
         # without a logits buffer the fused one-launch router runs instead: same bits
         ids2 = torch.empty_like(ids)
@@ -169,6 +170,41 @@ def test_align_sort_parity(moe, T, k, E, B):
     ref_w = np.where(r_ids < S, wts.ravel()[np.minimum(r_ids, S - 1)], 0.0).astype(np.float32)
     assert np.array_equal(s_w.cpu().numpy(), ref_w)
     check_sort_invariants(ids, E, B, g_ids, s_e.cpu().numpy(), int(npp.item()), cnt.cpu().numpy())
+
+
+@pytest.mark.parametrize("T,k,E,B", [(16, 2, 4, 16), (100, 4, 64, 16), (2049, 4, 16, 128)],
+                         ids=["one_warp", "one_cta", "chunked"])
+def test_align_sort_reports_bad_ids(moe, T, k, E, B):
+    """An id outside [0, E) from the caller is never used as an index: its slot is left out and
+    num_tokens_post_padded reports -1 (all three sort kernels).  The GPU must stay usable."""
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids[T // 2, 0] = E + 3
+    ids[T - 1, k - 1] = -2
+    wts = rng.random((T, k)).astype(np.float32)
+    P, NB = oracle.align_sort_sizes(T, k, E, B)
+    d_ids = torch.from_numpy(ids).cuda()
+    d_w = torch.from_numpy(wts).cuda()
+    s_ids = torch.full((P,), -7, dtype=torch.int32, device="cuda")
+    s_w = torch.zeros(P, dtype=torch.float32, device="cuda")
+    s_e = torch.zeros(NB, dtype=torch.int32, device="cuda")
+    npp = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsb = moe.moe_align_sort_workspace_size(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    moe.moe_align_sort(d_ids, d_w, T, k, E, B, s_ids, s_w, s_e, npp, None, ws, wsb)
+    torch.cuda.synchronize()
+    assert int(npp.item()) == moe.MOE_ERR_INVALID_ARG
+    got = s_ids.cpu().numpy()
+    assert not np.isin([(T // 2) * k, T * k - 1], got).any()   # the two bad slots are placed nowhere
+    # the same call with valid ids still sorts correctly afterwards
+    ids[T // 2, 0] = 0
+    ids[T - 1, k - 1] = E - 1
+    d_ids.copy_(torch.from_numpy(ids))
+    moe.moe_align_sort(d_ids, d_w, T, k, E, B, s_ids, s_w, s_e, npp, None, ws, wsb)
+    torch.cuda.synchronize()
+    r_ids, r_e, r_npp, _ = oracle.align_sort(ids, E, B)
+    assert int(npp.item()) == r_npp
+    assert np.array_equal(s_ids.cpu().numpy(), r_ids)
 
 
 # ------------------------------------------------------------ FP8 codes
@@ -232,13 +268,28 @@ def test_fused_bf16_parity(moe, name):
     inp, host = gpu_inputs(cfg)
     out, layer = run_fused(moe, cfg, inp)
     r_ids = _check_intermediates(moe, layer, cfg, host)
-    toks = np.arange(cfg.T) if cfg.T <= 64 else sample_tokens(cfg, r_ids)
-    ref = _oracle_bf16(host, cfg, toks)
-    got = out.float().cpu().numpy()[toks]
-    assert np.isfinite(got).all()
-    err = rel_l2(got, ref)
-    print(f"{name}: relL2 {err:.3e} over {len(toks)} tokens")
-    assert err <= TOL_BF16
+    toks = np.arange(cfg.T) if cfg.T <= 128 else parity_tokens(r_ids, cfg.E, layer.plan.block_m)
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
+                                  cfg.k, toks, expert_major=True)
+    check_rows(out.float().cpu().numpy()[toks], ref, TOL_BF16, label=name)
+
+
+def _check_fp8_block_gathered_codes(layer, cfg, host):
+    """The block-FP8 call's own gather + quantise: the e4m3 codes of x in sorted order and their
+    1x128 scales (stored transposed, [H/128][max_padded]) equal the oracle's quantiser applied to
+    the gathered rows, bit for bit; padding rows are zero rows (codes 0, scale 1)."""
+    T, H, k = cfg.T, cfg.H, cfg.k
+    P = layer.plan.max_padded
+    npp = int(layer.view("num_tokens_post_padded", torch.int32, (1,)).item())
+    s_ids = layer.view("sorted_ids", torch.int32, (P,)).cpu().numpy()[:npp]
+    rows = np.zeros((npp, H), np.uint16)
+    real = s_ids < T * k
+    rows[real] = host["x"][s_ids[real] // k]
+    rq, rs = oracle.quant_1x128(rows)
+    gq = layer.view("x_sorted", torch.uint8, (P, H)).cpu().numpy()[:npp]
+    gs = layer.view("x_scales", torch.float32, (H // 128, P)).cpu().numpy()[:, :npp].T
+    assert np.array_equal(gq, rq)
+    assert np.array_equal(np.ascontiguousarray(gs).view(np.uint32), rs.view(np.uint32))
 
 
 def test_fused_fp8_parity(moe):
@@ -247,16 +298,17 @@ def test_fused_fp8_parity(moe):
     fp8w = quantize_weights_gpu(moe, inp, cfg)
     out, layer = run_fused(moe, cfg, inp, dtype=moe.MOE_FP8_BLOCK128, fp8w=fp8w)
     r_ids = _check_intermediates(moe, layer, cfg, host)
-    # the oracle quantises the weights itself; its codes equal the GPU's (checked on a slice)
+    # the oracle quantises the weights itself; its codes and scales equal the GPU's, in full
     q1, s1 = oracle.quant_128x128(host["W_gate_up"])
     q2, s2 = oracle.quant_128x128(host["W_down"])
-    assert np.array_equal(fp8w["W_gate_up"][0, :256].cpu().numpy(), q1[0, :256])
-    toks = sample_tokens(cfg, r_ids, n=48)
-    ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks)
-    got = out.float().cpu().numpy()[toks]
-    err = rel_l2(got, ref)
-    print(f"fp8: relL2 {err:.3e} over {len(toks)} tokens")
-    assert err <= TOL_FP8
+    for name, ref_q, sname, ref_s in (("W_gate_up", q1, "w1_scale", s1), ("W_down", q2, "w2_scale", s2)):
+        assert np.array_equal(fp8w[name].cpu().numpy(), ref_q), name
+        assert np.array_equal(fp8w[sname].cpu().numpy().view(np.uint32), ref_s.view(np.uint32)), sname
+    _check_fp8_block_gathered_codes(layer, cfg, host)
+    toks = parity_tokens(r_ids, cfg.E, layer.plan.block_m)
+    ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, cfg.k, toks,
+                                 expert_major=True)
+    check_rows(out.float().cpu().numpy()[toks], ref, TOL_FP8, label="fp8 block")
 
 
 EDGE_CASES = [
@@ -301,6 +353,7 @@ def test_fused_fp8_edge_cases(moe, case):
     fp8w = quantize_weights_gpu(moe, inp, cfg)
     out, layer = run_fused(moe, cfg, inp, dtype=moe.MOE_FP8_BLOCK128, fp8w=fp8w)
     _check_intermediates(moe, layer, cfg, host)
+    _check_fp8_block_gathered_codes(layer, cfg, host)
     q1, s1 = oracle.quant_128x128(host["W_gate_up"])
     q2, s2 = oracle.quant_128x128(host["W_down"])
     ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, k, np.arange(T))

@@ -289,6 +289,15 @@ def test_route_topk_against_fp64_softmax_topk_renorm():
     for t in (0, 7):
         for e in range(cfg.E):
             assert logits[t, e] == oracle.router_logit(xb[t], wb[e])
+    # without renormalisation: the same ids, weights = the softmax over all E at those ids
+    ids2, w2, _ = oracle.route(xb, wb, None, cfg.k, renormalize=False)
+    assert np.array_equal(ids2, ids)
+    for t in range(cfg.T):
+        gaps = np.abs(np.diff(np.sort(L[t])[::-1][:cfg.k + 1]))
+        if gaps.min() < 1e-5:
+            continue
+        np.testing.assert_allclose(w2[t], P[t, ids[t]], rtol=1e-6)
+        assert w2[t].sum() < 1.0
 
 
 def test_route_ties_go_to_lower_expert():
@@ -443,6 +452,35 @@ def test_forward_token_permutation_and_subset():
     assert np.array_equal(_oracle_bf16(inp2, 2), full[perm.numpy()])
     sub = np.array([0, 5, 15], np.int64)
     assert np.array_equal(_oracle_bf16(inp, 2, sub), full[sub])
+
+
+@pytest.mark.parametrize("T,H,I,E,k,bias", [(37, 256, 384, 6, 3, "normal"), (20, 128, 256, 4, 2, None),
+                                            (50, 256, 256, 16, 4, "zipf"), (5, 128, 128, 1, 1, None),
+                                            (40, 128, 256, 3, 3, None)])
+def test_forward_expert_major_bit_identical_to_per_token(T, H, I, E, k, bias):
+    """The expert-by-expert evaluation computes the same fp64 sums in the same order as the
+    per-token loop, in all four number formats: equal bit for bit (token lists with repeats,
+    any order, experts with one slot and with more than one 16-slot group)."""
+    cfg = synth.MoEConfig("em", T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5 if bias == "normal" else 1.2)
+    inp = synth.make_inputs(cfg, seed=7)
+    h = {n: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.numpy()))
+         for n, v in inp.items()}
+    toks = np.array([T - 1, 0, 3 % T, 3 % T] + list(range(T)), np.int64)
+    args = (h["x"], h["W_router"], h["bias"])
+    runs = [(oracle.moe_forward_bf16, (h["W_gate_up"], h["W_down"]))]
+    q1, s1 = oracle.quant_128x128(h["W_gate_up"])
+    q2, s2 = oracle.quant_128x128(h["W_down"])
+    runs.append((oracle.moe_forward_fp8, (q1, s1, q2, s2)))
+    q1, s1 = oracle.quant_rows(h["W_gate_up"])
+    q2, s2 = oracle.quant_rows(h["W_down"])
+    runs.append((oracle.moe_forward_fp8_token, (q1, s1, q2, s2)))
+    q1, s1 = oracle.quant_mx4(h["W_gate_up"])
+    q2, s2 = oracle.quant_mx4(h["W_down"])
+    runs.append((oracle.moe_forward_mxfp4, (q1, s1, q2, s2)))
+    for fn, w in runs:
+        a = fn(*args, *w, k, toks)
+        b = fn(*args, *w, k, toks, expert_major=True)
+        assert np.array_equal(a.view(np.uint64), b.view(np.uint64)), fn.__name__
 
 
 def test_forward_fp8_against_dense_dequantised_reference():

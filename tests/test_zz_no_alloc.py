@@ -25,7 +25,10 @@ def moe():
 def _routing(T, k, E, seed):
     rng = np.random.default_rng(seed)
     p = rng.dirichlet(np.full(E, 0.3))
-    ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    if k == 1:
+        ids = rng.choice(E, size=(T, 1), p=p).astype(np.int32)
+    else:
+        ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
     return ids, rng.random((T, k)).astype(np.float32)
 
 
@@ -37,10 +40,20 @@ def _outputs(P, NB, E, fill):
             torch.full((E,), fill, dtype=torch.int32, device="cuda"))
 
 
+# the largest shape whose scratch fits: E = 1024 experts and 254 chunks of 1024 slots
+# (254 * 1024 histogram words, then 1025 offsets: 261,121 of the 262,144 words)
+LIMIT_T = 254 * 1024
+
+
 @pytest.mark.gpu
 def test_noalloc_sort_matches_workspace_sort_twice(moe):
-    # a large sort first, then a small one: the second must not see the first's leftovers
-    for (T, k, E, B, seed) in [(4096, 8, 256, 128, 1), (100, 2, 8, 16, 2)]:
+    # Calls in a row that all use the shared scratch (the chunked three-launch sort): a large
+    # sort, then one with another chunk count and expert count, so the offsets sit elsewhere in
+    # the array and the second must not read the first's leftovers; then the largest shape that
+    # fits; then the first shape again.
+    for (T, k, E, B, seed) in [(4096, 8, 256, 128, 1), (700, 2, 64, 64, 2), (LIMIT_T, 1, 1024, 128, 3),
+                               (4096, 8, 256, 128, 4)]:
+        assert T * k > 1024   # more than one CTA's worth of slots: the path that uses the scratch
         ids, w = _routing(T, k, E, seed)
         d_ids, d_w = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
         P, NB = moe.moe_align_sort_sizes(T, k, E, B)
@@ -53,10 +66,14 @@ def test_noalloc_sort_matches_workspace_sort_twice(moe):
         torch.cuda.synchronize()
         for a, b in zip(got, ref):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert int(got[3].item()) > 0
 
 
 def test_noalloc_sort_rejects_oversize(moe):
-    # 1 MiB of scratch: 1024 experts x 1024 chunks of slots cannot fit; rejected before any launch
+    # rejected on the host before any launch (the pointers are never touched)
     lib = moe.load()
     rc = lib.moe_align_sort_noalloc(16, 16, 1 << 20, 1, 1024, 128, 16, 16, 16, 16, None, None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    # one chunk more than the largest shape that fits
+    rc = lib.moe_align_sort_noalloc(16, 16, LIMIT_T + 1, 1, 1024, 128, 16, 16, 16, 16, None, None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
