@@ -87,9 +87,12 @@ int moe_align_sort_sizes(int T, int k, int E, int block_m, int64_t *max_padded, 
 /*
  * The block-size rule of the AITER page (section 3.3, get_block_size_M):
  * among `candidates` (n entries), the block size with the fewest rounds of
- * ceil(inter_dim/128) * ceil(max_padded/BM) tiles over `units` compute
- * units, then the fewest idle units in the last round.  Host only; returns
- * the chosen block size or a negative status.
+ * tiles over `units` compute units, then the fewest idle units in the last
+ * round (a full tie keeps the earlier candidate), where the tile count is
+ * the page's tgN * (max_padded + BM - 1) // BM evaluated left to right,
+ * (tgN * (max_padded + BM - 1)) / BM, with tgN = ceil(inter_dim/128) and
+ * max_padded = token*topk + expert*BM - topk.  Host only; returns the chosen
+ * block size or a negative status.
  */
 int moe_block_size_m_heuristic(int token, int topk, int expert, int inter_dim, int units,
                                const int *candidates, int n);
@@ -304,6 +307,15 @@ typedef struct moe_options {
      * output of such a call is undefined; the next call on the workspace
      * starts clean. */
     int unsatisfiable_h_wait;
+    /* MOE_BF16 on CTA pairs: experts whose tokens fit one 128-row block take
+     * swap-AB pair tiles (the weights on the pair's 256-row MMA side, the
+     * expert's tokens, rounded up to 32, on N) instead of a mostly padded
+     * 256 x 256 tile; light and 256 x 256 tiles are interleaved so that
+     * weight streaming and tensor work overlap.  -1 automatic (default: on
+     * when I is a multiple of 256 and the average expert that can hold a slot
+     * has fewer than 4 blocks of 128 rows), 0 off, 1 on (needs I % 256 == 0,
+     * else MOE_ERR_UNSUPPORTED).  Not used by the training forward. */
+    int light_tiles;
 } moe_options_t;
 
 /* Set *options to the defaults (gemm_pair -1, one_stage 1, pdl_mask -1, no

@@ -175,6 +175,59 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
     return L;
 }
 
+// GB300 analogue of the AITER page's get_block_size_M (section 3.3) for the swap-AB (decode)
+// kernels: the same choice -- fewest rounds of tiles over the compute units, then fewest idle
+// units in the last round, a full tie keeping the earlier candidate -- over the swap kernels'
+// block sizes {16, 32, 64, 128} (MXFP4: up to 64), with the SM count as the units and the
+// tiles those kernels actually run: one stage-1 tile per 128 rows of W_gate_up's gate half for
+// every expert that can hold a slot, whatever the block size (the expert's whole padded
+// segment is the MMA's N side).  The rounds therefore tie and the first candidate, 16, is
+// kept, which is also the measured best: Mixtral decode shapes on GB300 (same box, 400 steps)
+// T=1 137 / 149 / 184 / 282 us, T=32 436 / 448 / 525 / 785 us, T=128 476 / 512 / 534 / 794 us
+// for block sizes 16 / 32 / 64 / 128 (larger blocks only add padded rows to every tile).
+static int swap_block_m(int dtype, int64_t e_act, int I, int units)
+{
+    const int cands[4] = {16, 32, 64, 128};
+    const int n = dtype == MOE_MXFP4 ? 3 : 4;
+    int best = cands[0];
+    int64_t best_r = 0, best_idle = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t tiles = e_act * (I / 128);  // independent of the block size in swap mode
+        const int64_t rounds = (tiles + units - 1) / units;
+        const int64_t idle = units - tiles % units;
+        if (i == 0 || rounds < best_r || (rounds == best_r && idle < best_idle)) {
+            best = cands[i];
+            best_r = rounds;
+            best_idle = idle;
+        }
+    }
+    return best;
+}
+
+// GB300 analogue of the page's get_ksplit (section 3.4) for the swap-AB kernels' stage 2
+// (K = I): when its tiles (experts that can hold a slot x 256-feature tiles of H) leave SMs
+// idle, split K so that every SM gets work: split_max = ceil(units / tiles) as on the page,
+// but the smallest divisor of K's 128-byte blocks that reaches it (the page takes the
+// largest one below it, leaving a partial wave).  The page's first test (no split when
+// token * topk > expert) is not kept: it concerns its stage-1 split.  Measured (Mixtral decode
+// shapes, same box): T >= 8 (128 tiles) split 2 436 us / 4 440 / 7 436 / 14 441 / none 453
+// at T=32, and 467 / 474 / 476 / 492 / 500 us at T=128; T=1 (32 tiles) split 4 151 us,
+// 7 135 us, 14 135 us, none 190 us.
+static int swap_split_k(int64_t tiles, int kblocks, int units)
+{
+    if (tiles >= units || tiles <= 0)
+        return 1;
+    const int64_t need = (units + tiles - 1) / tiles;
+    int split = 1;
+    for (int d = 2; d <= 16 && d <= kblocks; ++d)
+        if (kblocks % d == 0) {
+            split = d;
+            if (d >= need)
+                break;
+        }
+    return split;
+}
+
 static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, int split_k, int num_sms,
                      moe_plan_t *plan, bool grouped_only = false)
 {
@@ -195,8 +248,10 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
     // FP8 always runs the grouped kernel.
     const int swap_max = (dtype == MOE_MXFP4) ? 64 : 128;
     p.mode = (dtype != MOE_FP8_BLOCK128 && T <= swap_max && !grouped_only) ? MOE_MODE_SWAP : MOE_MODE_GROUPED;
+    // Experts that can hold a slot (the tile counts below are upper bounds for them).
+    const int64_t e_act = ((int64_t)T * k < E) ? (int64_t)T * k : E;
     if (block_m == 0)
-        block_m = (p.mode == MOE_MODE_SWAP) ? 16 : 128;
+        block_m = (p.mode == MOE_MODE_SWAP) ? swap_block_m(dtype, e_act, I, num_sms) : 128;
     if (p.mode == MOE_MODE_GROUPED && block_m != 128)
         return MOE_ERR_UNSUPPORTED;
     if (p.mode == MOE_MODE_SWAP && (block_m % 16 != 0 || block_m > (dtype == MOE_MXFP4 ? 64 : 128)))
@@ -205,22 +260,10 @@ static int plan_impl(int dtype, int T, int H, int I, int E, int k, int block_m, 
     p.split_k1 = 1;
     const int kblocks2 = I / (dtype == MOE_BF16 ? 64 : dtype == MOE_MXFP4 ? 256 : 128);  // 128-byte K blocks
     if (p.mode == MOE_MODE_SWAP) {
-        if (split_k == 0) {
-            // Enough stage-2 tiles for ~4 per SM: the smallest divisor of I/64 that reaches it.
-            const int64_t e_act = (int64_t)((T * k < E) ? T * k : E);
-            const int64_t tiles = e_act * ((H + 255) / 256);
-            split_k = 1;
-            if (tiles < 4LL * num_sms) {
-                for (int d = 2; d <= 16 && d <= kblocks2; ++d)
-                    if (kblocks2 % d == 0) {
-                        split_k = d;
-                        if (tiles * d >= 4LL * num_sms)
-                            break;
-                    }
-            }
-        } else if (kblocks2 % split_k != 0) {
+        if (split_k == 0)
+            split_k = swap_split_k(e_act * ((H + 255) / 256), kblocks2, num_sms);
+        else if (kblocks2 % split_k != 0)
             return MOE_ERR_UNSUPPORTED;
-        }
         p.split_k2 = split_k;
     } else {
         if (split_k > 1)
@@ -243,13 +286,15 @@ static moe_options_t default_options()
     o.gemm_pair = -1;
     o.one_stage = 1;
     o.pdl_mask = -1;
+    o.light_tiles = -1;
     return o;
 }
 
 static int check_options(const moe_options_t &o)
 {
     if (o.gemm_pair < -1 || o.gemm_pair > 1 || o.one_stage < 0 || o.one_stage > 1 || o.pdl_mask < -1 ||
-        o.pdl_mask > kPdlAll || o.unsatisfiable_h_wait < 0 || o.unsatisfiable_h_wait > 1)
+        o.pdl_mask > kPdlAll || o.unsatisfiable_h_wait < 0 || o.unsatisfiable_h_wait > 1 || o.light_tiles < -1 ||
+        o.light_tiles > 1)
         return MOE_ERR_INVALID_ARG;
     if (o.stage_events)
         for (int i = 0; i < 7; ++i)
@@ -334,6 +379,15 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
 
     const int64_t P = p.max_padded;
     const int eb = (dtype == MOE_BF16) ? 2 : 1;
+    // Light-expert (swap-AB) pair tiles: bf16 grouped mode on CTA pairs, I a multiple of 256.
+    // Automatic when the average expert that can hold a slot has fewer than 4 token blocks
+    // (fine-grained routing): their kernel keeps one pipeline stage fewer in stage 1, which
+    // measured 2-4 % slower on Mixtral prefill, where no expert is light.
+    if (o.light_tiles == 1 && (dtype != MOE_BF16 || I % 256 != 0))
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t e_can = ((int64_t)S < E) ? S : E;
+    const bool light = dtype == MOE_BF16 && !train && I % 256 == 0 &&
+                       (o.light_tiles == 1 || (o.light_tiles == -1 && (int64_t)S < 4LL * 128 * e_can));
     // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
     // itself (no gather pass)
     const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && o.one_stage == 1 && !train;
@@ -390,6 +444,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     if (!encode_tmap_2d(&g1.tm_x, at(L.x_sorted), eb, H / kdiv, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g1.tm_w, W_gate_up, eb, H / kdiv, (uint64_t)E * 2 * I, box_inner, box_w_rows))
         return MOE_ERR_CUDA;
+    if (light && !encode_tmap_2d(&g1.tm_x16, at(L.x_sorted), eb, H, P, box_inner, 16))
+        return MOE_ERR_CUDA;
     g1.K = H;
     g1.N = I;
     g1.rows_per_expert = 2 * I;
@@ -404,6 +460,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
     if (!encode_tmap_2d(&g2.tm_x, at(L.inter), eb, I / kdiv, P, box_inner, box_x_rows) ||
         !encode_tmap_2d(&g2.tm_w, W_down, eb, I / kdiv, (uint64_t)E * H, box_inner, box_w_rows))
+        return MOE_ERR_CUDA;
+    if (light && !encode_tmap_2d(&g2.tm_x16, at(L.inter), eb, I, P, box_inner, 16))
         return MOE_ERR_CUDA;
     g2.K = I;
     g2.N = H;
@@ -445,7 +503,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             const int64_t ub = p.max_blocks * (I / 64);
             ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 1, T, k, E, o.gemm_pair)) {
-            ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st);
+            ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st, light);
         } else {
             const int64_t ub = p.max_blocks * (I / 128);
             const int grid = (int)(ub < nsm ? ub : nsm);
@@ -476,7 +534,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 2, T, k, E, o.gemm_pair)) {
-            ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st);
+            ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st, light);
         } else {
             const int64_t ub = p.max_blocks * nt2;
             const int grid = (int)(ub < nsm ? ub : nsm);
@@ -746,11 +804,12 @@ int moe_block_size_m_heuristic(int token, int topk, int expert, int inter_dim, i
         if (bm <= 0)
             return MOE_ERR_INVALID_ARG;
         const int64_t padded = (int64_t)token * topk + (int64_t)expert * bm - topk;
-        const int64_t tiles = tgN * ((padded + bm - 1) / bm);
+        // the page's tgN * (max + bm - 1) // bm, grouped as Python groups it (left to right)
+        const int64_t tiles = tgN * (padded + bm - 1) / bm;
         const int64_t rounds = (tiles + units - 1) / units;
         const int64_t idle = units - tiles % units;
-        if (best < 0 || rounds < best_r || (rounds == best_r && idle < best_idle) ||
-            (rounds == best_r && idle == best_idle && bm < best)) {
+        // fewest rounds, then fewest idle units; a full tie keeps the earlier candidate
+        if (best < 0 || rounds < best_r || (rounds == best_r && idle < best_idle)) {
             best = bm;
             best_r = rounds;
             best_idle = idle;

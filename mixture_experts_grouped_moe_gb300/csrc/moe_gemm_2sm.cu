@@ -31,6 +31,19 @@
 // up to 8 pairs walk the N tiles together so that one weight tile serves 16
 // token blocks from L2.  Every wait is bounded; a CTA that gives up raises the status word
 // and both CTAs still meet at the final cluster barrier.
+//
+// Light experts (LT = 1, stages 1 and 2, bf16): an expert whose sorted rows
+// fit one 128-row block would waste most of a 256-row pair tile on padding
+// (fine-grained routing leaves most experts with a few tokens).  Its tiles
+// swap the operands instead: the pair's 256-row MMA side holds weight rows
+// (128 per CTA) and the N side its np = ceil32(count) token rows (np / 2 per
+// CTA, loaded in 16-row boxes).  Stage 1 issues two MMAs per K step, gate
+// rows and the matching up rows, into two accumulators of the same TMEM
+// lanes, so SwiGLU still pairs within a thread; a tile covers 256
+// intermediate columns.  Stage 2 covers 256 output features per tile.  The
+// epilogue then holds one feature per thread and a token per accumulator
+// column.  Heavy and light experts' tiles are claimed from the same counter,
+// so tensor-bound and weight-streaming tiles run side by side.
 #include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
@@ -39,9 +52,14 @@ namespace moe {
 
 namespace gemm2sm {
 
-constexpr int kStages = 6;
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes of K
-constexpr int kStageBytes = 2 * kHalfBytes; // [A: token rows | B: weight rows]
+constexpr int kSwapRowsPerLoad = 16;        // token rows per TMA box of a light expert's tile
+// Pipeline stage: [A: token rows | B: weight rows]; with light-expert tiles in stage 1 a stage
+// also holds [gate rows | up rows | up to 64 token rows], 40 KB, so one fewer stage fits.
+template <int STAGE, int LT>
+constexpr int kStageBytesT = (STAGE == 1 && LT) ? 2 * kHalfBytes + 64 * 128 : 2 * kHalfBytes;
+template <int STAGE, int LT>
+constexpr int kStagesT = (STAGE == 1 && LT) ? 5 : 6;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;
@@ -53,7 +71,10 @@ constexpr int kMaxE = 1024;
 template <int STAGE>
 constexpr int kGroupPairs = 8;
 
+template <int STAGE, int LT>
 struct __align__(1024) Smem {
+    static constexpr int kStages = kStagesT<STAGE, LT>;
+    static constexpr int kStageBytes = kStageBytesT<STAGE, LT>;
     uint8_t stage[kStages][kStageBytes];
     uint64_t full[kStages];    // leader: both CTAs' TMA bytes of the stage
     uint64_t empty[kStages];   // both: the pair MMAs have read the stage
@@ -67,20 +88,57 @@ struct __align__(1024) Smem {
     int abort;
     int ntiles;
     int off[kMaxE + 1];        // expert_offsets (sorted rows)
-    int tstart[kMaxE + 1];     // first pair tile of each expert
+    int tstart[kMaxE + 1];     // first pair tile of each expert (with LT: among the 256 x 256 tiles)
+    int lstart[LT ? kMaxE + 1 : 1];  // LT: first light-expert tile of each expert
+    int nheavy, nlight;        // LT: tiles of each kind
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+template <int STAGE, int LT>
+constexpr size_t kSmemBytesT = sizeof(Smem<STAGE, LT>) + 1024;
 
 struct PairTile {
     int e;
     int mb0;      // first 128-row block of the pair
     int second;   // the pair's second block is a real block of expert e
-    int wrow0;    // weight rows of B half 0 / half 1
+    int wrow0;    // weight rows of B half 0 / half 1 (light tile: gate / up rows, or W_down rows, of CTA 0)
     int wrow1;
     int ncol0;    // output column base
     int kb0, kb1; // K blocks (weight gradients: the expert's token positions)
+    int swap;     // light-expert tile: weights on the MMA's 256-row side, tokens on N
+    int cnt;      // light tile: the expert's token rows
+    int np;       // light tile: MMA N = cnt rounded up to 32 (np / 2 rows per CTA)
 };
+
+// A light expert: all its sorted rows fit one 128-row block.
+__device__ __forceinline__ bool light_expert(int nb) { return nb == 1; }
+
+// Tiles of one expert: ceil(blocks / 2) pairs per N tile; with LT, a light expert has none of
+// those and one light tile per 256 output columns instead.
+template <int STAGE, int LT>
+__device__ __forceinline__ int heavy_tiles(int nb, int nnt)
+{
+    return (LT && light_expert(nb)) ? 0 : (nb + 1) / 2 * nnt;
+}
+
+template <int LT>
+__device__ __forceinline__ int light_tiles(const GemmArgs &a, int nb)
+{
+    return (LT && light_expert(nb)) ? (a.N + 255) / 256 : 0;
+}
+
+// The last e in [0, E) with start[e] <= t (experts without tiles share their successor's start).
+__device__ __forceinline__ int find_expert(const int *start, int E, int t)
+{
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
 
 // STAGE 5 (weight gradients): D[e] (M x N) = A_e B_e^T with K over expert e's
 // sorted token positions; A and B are transposed activations [rows][P]; a
@@ -92,13 +150,14 @@ __device__ __forceinline__ int n_tiles_n(const GemmArgs &a)
     return (STAGE == 1) ? a.N / 128 : (a.N + 255) / 256;
 }
 
-template <int STAGE>
-__device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, int t)
+template <int STAGE, int LT, class SM>
+__device__ __forceinline__ PairTile decode(const SM &sm, const GemmArgs &a, int t)
 {
     const int nnt = n_tiles_n<STAGE>(a);
     if (STAGE == 5) {
         const int nmp = a.M / 256;
         PairTile p;
+        p.swap = p.cnt = p.np = 0;
         p.e = t / (nmp * nnt);
         const int rem = t - p.e * nmp * nnt;
         const int nt = rem / nmp;
@@ -111,16 +170,34 @@ __device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, in
         p.kb1 = sm.off[p.e + 1] / 64;
         return p;
     }
-    // the expert: the last e with tstart[e] <= t (empty experts share their successor's start)
-    int lo = 0, hi = a.E;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (sm.tstart[mid] <= t)
-            lo = mid;
-        else
-            hi = mid;
-    }
     PairTile p;
+    p.swap = p.cnt = p.np = 0;
+    if (LT) {
+        // The two kinds of tile are interleaved in proportion to their counts, so that
+        // weight-streaming (light) and tensor-bound (256 x 256) tiles run side by side: tile t is
+        // the light tile floor(t * L / (L + H)) when that count steps at t, else heavy tile
+        // t - floor(t * L / (L + H)).
+        const int L = sm.nlight, tot = sm.nlight + sm.nheavy;
+        const int lb = (int)((int64_t)t * L / tot);
+        if ((int)((int64_t)(t + 1) * L / tot) > lb) {
+            const int lo = find_expert(sm.lstart, a.E, lb);
+            p.e = lo;
+            // local = the 256-column slice of the output
+            const int local = lb - sm.lstart[lo];
+            p.swap = 1;
+            p.mb0 = sm.off[lo] >> 7;
+            p.second = 1;
+            p.cnt = __ldg(a.expert_counts + lo);
+            p.np = (p.cnt + 31) & ~31;
+            p.ncol0 = local * 256;
+            p.wrow0 = lo * a.rows_per_expert + p.ncol0;        // gate rows (stage 1) / W_down rows
+            p.wrow1 = lo * a.rows_per_expert + a.N + p.ncol0;  // up rows (stage 1)
+            p.kb0 = p.kb1 = 0;
+            return p;
+        }
+        t -= lb;
+    }
+    const int lo = find_expert(sm.tstart, a.E, t);
     p.e = lo;
     const int local = t - sm.tstart[lo];
     const int nb = (sm.off[lo + 1] - sm.off[lo]) >> 7;
@@ -145,11 +222,14 @@ __device__ __forceinline__ PairTile decode(const Smem &sm, const GemmArgs &a, in
     return p;
 }
 
-template <int STAGE, int QT>
+template <int STAGE, int QT, int LT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmArgs a)
 {
+    static_assert(!LT || ((STAGE == 1 || STAGE == 2) && QT == 0), "light-expert tiles: bf16 stages 1 and 2");
+    using SmemT = Smem<STAGE, LT>;
+    constexpr int kStages = SmemT::kStages;
     extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemT &sm = *reinterpret_cast<SmemT *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
@@ -173,6 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         fence_mbarrier_init();
         tma_prefetch_desc(&a.tm_x);
         tma_prefetch_desc(&a.tm_w);
+        if (LT)
+            tma_prefetch_desc(&a.tm_x16);
     }
     if (warp == 1) {
         tmem_alloc_pair(&sm.tmem_base, kTmemCols);
@@ -193,32 +275,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         if (lane == 0)
             sm.ntiles = a.E * (a.M / 256) * n_tiles_n<STAGE>(a);
     } else if (warp == 2) {
+        // per-expert tile starts: a warp scan over the experts (light tiles separately with LT)
         const int E = a.E;
         const int nnt = n_tiles_n<STAGE>(a);
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-        int sum = 0;
+        int hsum = 0, lsum = 0;
         for (int e = e0; e < e1; ++e) {
             const int o0 = a.expert_offsets[e], o1 = a.expert_offsets[e + 1];
             sm.off[e] = o0;
-            sum += (((o1 - o0) >> 7) + 1) / 2 * nnt;
+            hsum += heavy_tiles<STAGE, LT>((o1 - o0) >> 7, nnt);
+            lsum += light_tiles<LT>(a, (o1 - o0) >> 7);
         }
-        int incl = sum;
+        int hincl = hsum, lincl = lsum;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d)
-                incl += v;
+            const int hv = __shfl_up_sync(0xffffffffu, hincl, d);
+            const int lv = __shfl_up_sync(0xffffffffu, lincl, d);
+            if (lane >= d) {
+                hincl += hv;
+                lincl += lv;
+            }
         }
-        int run = incl - sum;
+        int hrun = hincl - hsum, lrun = lincl - lsum;
         for (int e = e0; e < e1; ++e) {
-            sm.tstart[e] = run;
-            run += (((a.expert_offsets[e + 1] - a.expert_offsets[e]) >> 7) + 1) / 2 * nnt;
+            const int nb = (a.expert_offsets[e + 1] - a.expert_offsets[e]) >> 7;
+            sm.tstart[e] = hrun;
+            hrun += heavy_tiles<STAGE, LT>(nb, nnt);
+            if (LT) {
+                sm.lstart[e] = lrun;
+                lrun += light_tiles<LT>(a, nb);
+            }
         }
         if (lane == 31) {
-            sm.tstart[E] = incl;
+            sm.tstart[E] = hincl;
+            if (LT)
+                sm.lstart[E] = lincl;
             sm.off[E] = a.expert_offsets[E];
-            sm.ntiles = incl;
+            sm.nheavy = hincl;
+            sm.nlight = lincl;
+            sm.ntiles = hincl + lincl;
         }
     }
     __syncthreads();
@@ -272,20 +368,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 }
                 if (t < 0)
                     break;
-                const PairTile p = decode<STAGE>(sm, a, t);
+                const PairTile p = decode<STAGE, LT>(sm, a, t);
                 const int xrow = (rank == 1 && p.second) ? (p.mb0 + 1) * 128 : p.mb0 * 128;
                 const int wrow = rank == 0 ? p.wrow0 : p.wrow1;
                 const int kb0 = STAGE == 5 ? p.kb0 : 0, kb1 = STAGE == 5 ? p.kb1 : nkb;
+                // light tile: this CTA's half of the token rows, and the bytes of both CTAs per stage
+                const int half = p.swap ? p.np / 2 : 0;
+                const uint32_t swap_bytes = 2u * ((STAGE == 1 ? 2 : 1) * kHalfBytes + half * 128);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fullc = cluster_map(&sm.full[s], 0);
-                    if (leader)
-                        mbar_arrive_expect_tx(&sm.full[s], 2 * kStageBytes);
-                    tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
-                    tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_w);
+                    if (LT && p.swap) {
+                        if (leader)
+                            mbar_arrive_expect_tx(&sm.full[s], swap_bytes);
+                        // weights: rows r*128.. of the tile's 256 (stage 1: gate, then up), tokens after them
+                        tma_load_2d_pair(sm.stage[s], &a.tm_w, kb * kBK<QT>, p.wrow0 + (int)rank * 128, fullc,
+                                         pol_w);
+                        if (STAGE == 1)
+                            tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>,
+                                             p.wrow1 + (int)rank * 128, fullc, pol_w);
+                        uint8_t *tok = sm.stage[s] + (STAGE == 1 ? 2 : 1) * kHalfBytes;
+                        const int trow = p.mb0 * 128 + (int)rank * half;
+                        for (int c = 0; c < half; c += kSwapRowsPerLoad)
+                            tma_load_2d_pair(tok + c * 128, &a.tm_x16, kb * kBK<QT>, trow + c, fullc, pol_x);
+                    } else {
+                        if (leader)
+                            mbar_arrive_expect_tx(&sm.full[s], 2 * 2 * kHalfBytes);
+                        tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
+                        tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_w);
+                    }
                     any = true;
                     if (++s == kStages) {
                         s = 0;
@@ -333,10 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccCols;
                 int kb0 = 0, kb1 = nkb;
-                if (STAGE == 5) {
-                    const PairTile p = decode<STAGE>(sm, a, t);
-                    kb0 = p.kb0;
-                    kb1 = p.kb1;
+                bool swap = false;
+                uint32_t idesc_swap = 0;
+                if (STAGE == 5 || LT) {
+                    const PairTile p = decode<STAGE, LT>(sm, a, t);
+                    kb0 = STAGE == 5 ? p.kb0 : 0;
+                    kb1 = STAGE == 5 ? p.kb1 : nkb;
+                    swap = p.swap != 0;
+                    if (swap)
+                        idesc_swap = make_idesc(1, 1, 256, (uint32_t)p.np);
                 }
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&sm.full[s], ph, a.status, abort_flag)) {
@@ -344,12 +463,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t *xa = sm.stage[s];
-                    const uint8_t *wb = sm.stage[s] + kHalfBytes;
+                    const uint32_t accum0 = kb > kb0 ? 1u : 0u;
+                    if (LT && swap) {
+                        // A = weight rows (this CTA's 128 of 256), B = the expert's token rows
+                        const uint8_t *w0 = sm.stage[s];
+                        const uint8_t *tok = sm.stage[s] + (STAGE == 1 ? 2 : 1) * kHalfBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_pair<QT>(d, smem_desc_sw128(xa + kk * 32), smem_desc_sw128(wb + kk * 32), idesc,
-                                     (kb > kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t accum = (kk > 0) ? 1u : accum0;
+                            mma_pair<QT>(d, smem_desc_sw128(w0 + kk * 32), smem_desc_sw128(tok + kk * 32),
+                                         idesc_swap, accum);
+                            if (STAGE == 1)  // the up rows into the second accumulator half
+                                mma_pair<QT>(d + 128, smem_desc_sw128(w0 + kHalfBytes + kk * 32),
+                                             smem_desc_sw128(tok + kk * 32), idesc_swap, accum);
+                        }
+                    } else {
+                        const uint8_t *xa = sm.stage[s];
+                        const uint8_t *wb = sm.stage[s] + kHalfBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_pair<QT>(d, smem_desc_sw128(xa + kk * 32), smem_desc_sw128(wb + kk * 32), idesc,
+                                         (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
                     any = true;
                     mma_commit_pair(&sm.empty[s], 0x3);
                     if (++s == kStages) {
@@ -395,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             }
             if (t < 0)
                 break;
-            const PairTile p = decode<STAGE>(sm, a, t);
+            const PairTile p = decode<STAGE, LT>(sm, a, t);
             bool ok = mbar_wait_cluster(&sm.tfull[acc], aph, a.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
@@ -404,7 +539,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
             const bool store = rank == 0 || p.second;
             const int pos = (p.mb0 + (int)rank) * 128 + row;   // sorted row of this thread
-            if (STAGE == 1) {
+            if (LT && p.swap) {
+                // one output feature per thread, one token per accumulator column
+                const int f = p.ncol0 + (int)rank * 128 + row;
+                const int row0 = p.mb0 * 128;  // the expert's first sorted row
+#pragma unroll 1
+                for (int c0 = 0; c0 < p.np; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tacc + c0, v);
+                    if (STAGE == 1) {
+                        float u[32];
+                        tmem_ld32(tacc + 128 + c0, u);
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)(row0 + c0) * a.N + f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            dst[(size_t)j * a.N] = __float2bfloat16_rn(silu(v[j]) * u[j]);
+                    } else if (f < a.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int c = c0 + j;
+                            if (c < p.cnt) {
+                                const int slot = a.sorted_ids[row0 + c];
+                                a.y[(size_t)slot * a.N + f] = a.sorted_weights[row0 + c] * v[j];
+                            }
+                        }
+                    }
+                }
+            } else if (STAGE == 1) {
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)pos * a.N + p.ncol0;
                 const float sx = (QT && store) ? a.x_scales[pos] : 1.0f;
 #pragma unroll 1
@@ -529,17 +690,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-template <int STAGE, int QT>
+template <int STAGE, int QT, int LT>
 cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 {
-    auto kern = gemm_pair_kernel<STAGE, QT>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kern = gemm_pair_kernel<STAGE, QT, LT>;
+    constexpr size_t smem = kSmemBytesT<STAGE, LT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -552,7 +714,7 @@ cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 }
 
 // Clusters of two that can be resident at once (one CTA per SM), cached per device.
-template <int STAGE, int QT>
+template <int STAGE, int QT, int LT>
 int max_clusters()
 {
     static int cache[64] = {0};
@@ -560,13 +722,14 @@ int max_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 0;
     if (cache[dev] == 0) {
-        auto kern = gemm_pair_kernel<STAGE, QT>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+        auto kern = gemm_pair_kernel<STAGE, QT, LT>;
+        constexpr size_t smem = kSmemBytesT<STAGE, LT>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -586,31 +749,39 @@ int max_clusters()
 
 bool gemm_pair_supported(int E) { return E <= gemm2sm::kMaxE; }
 
-cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st)
+cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
+                             bool light)
 {
-    // stages 1, 2 (bf16 or per-token FP8); 3 and 5 (training, bf16): the backward of stage 2
-    // and the weight gradients
+    // stages 1, 2 (bf16 or per-token FP8; bf16 optionally with light-expert tiles); 3 and 5
+    // (training, bf16): the backward of stage 2 and the weight gradients
+    if (light && (qt || (stage != 1 && stage != 2)))
+        return cudaErrorInvalidValue;
+    const int key = stage * 4 + (qt ? 1 : 0) + (light ? 2 : 0);
     int ncl = 0;
-    switch (stage * 2 + (qt ? 1 : 0)) {
-    case 2: ncl = gemm2sm::max_clusters<1, 0>(); break;
-    case 3: ncl = gemm2sm::max_clusters<1, 1>(); break;
-    case 4: ncl = gemm2sm::max_clusters<2, 0>(); break;
-    case 5: ncl = gemm2sm::max_clusters<2, 1>(); break;
-    case 6: ncl = gemm2sm::max_clusters<3, 0>(); break;
-    case 10: ncl = gemm2sm::max_clusters<5, 0>(); break;
+    switch (key) {
+    case 4: ncl = gemm2sm::max_clusters<1, 0, 0>(); break;
+    case 5: ncl = gemm2sm::max_clusters<1, 1, 0>(); break;
+    case 6: ncl = gemm2sm::max_clusters<1, 0, 1>(); break;
+    case 8: ncl = gemm2sm::max_clusters<2, 0, 0>(); break;
+    case 9: ncl = gemm2sm::max_clusters<2, 1, 0>(); break;
+    case 10: ncl = gemm2sm::max_clusters<2, 0, 1>(); break;
+    case 12: ncl = gemm2sm::max_clusters<3, 0, 0>(); break;
+    case 20: ncl = gemm2sm::max_clusters<5, 0, 0>(); break;
     default: return cudaErrorInvalidValue;
     }
     if (ncl <= 0)
         return cudaErrorInvalidConfiguration;
     if (max_pair_tiles < ncl)
         ncl = (int)(max_pair_tiles > 0 ? max_pair_tiles : 1);
-    switch (stage * 2 + (qt ? 1 : 0)) {
-    case 2: return gemm2sm::launch<1, 0>(a, ncl, st);
-    case 3: return gemm2sm::launch<1, 1>(a, ncl, st);
-    case 4: return gemm2sm::launch<2, 0>(a, ncl, st);
-    case 5: return gemm2sm::launch<2, 1>(a, ncl, st);
-    case 6: return gemm2sm::launch<3, 0>(a, ncl, st);
-    default: return gemm2sm::launch<5, 0>(a, ncl, st);
+    switch (key) {
+    case 4: return gemm2sm::launch<1, 0, 0>(a, ncl, st);
+    case 5: return gemm2sm::launch<1, 1, 0>(a, ncl, st);
+    case 6: return gemm2sm::launch<1, 0, 1>(a, ncl, st);
+    case 8: return gemm2sm::launch<2, 0, 0>(a, ncl, st);
+    case 9: return gemm2sm::launch<2, 1, 0>(a, ncl, st);
+    case 10: return gemm2sm::launch<2, 0, 1>(a, ncl, st);
+    case 12: return gemm2sm::launch<3, 0, 0>(a, ncl, st);
+    default: return gemm2sm::launch<5, 0, 0>(a, ncl, st);
     }
 }
 

@@ -135,6 +135,7 @@ struct GemmArgs {
     // tensor maps (host-encoded; passed by value as __grid_constant__)
     CUtensorMap tm_x;     // token operand rows [P_max][K]
     CUtensorMap tm_w;     // weight operand rows [E*rows_per_expert][K]
+    CUtensorMap tm_x16;   // the token operand in 16-row boxes (light-expert pair tiles)
     const int32_t *sorted_ids;
     const float *sorted_weights;
     const int32_t *sorted_expert_ids;
@@ -229,8 +230,12 @@ cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, 
                              int S, int k, int C, uint8_t *q, uint8_t *s, bool tiled, bool pdl, cudaStream_t st);
 // Grouped-mode GEMM on CTA pairs (two-SM tensor core), bf16 (qt = 0) or
 // per-token FP8 (qt = 1); max_pair_tiles bounds the useful cluster count.
+// light (bf16 stages 1 and 2; stage 1 needs N % 256 == 0): experts whose rows fit
+// one 128-row block take swap-AB pair tiles (a.tm_x16: the token operand in
+// 16-row boxes; a.expert_counts required).
 bool gemm_pair_supported(int E);
-cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st);
+cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
+                             bool light = false);
 cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 
 }  // namespace moe

@@ -109,6 +109,26 @@ def test_plan_rejects_invalid(moe, args, status):
     assert ei.value.status == status
 
 
+@pytest.mark.parametrize("units", [80, 148, 152, 304])
+def test_swap_planner_follows_the_gb300_rules(moe, units):
+    """moe_plan's automatic block size and stage-2 split in swap mode equal the restated GB300
+    analogues of the page's get_block_size_M and get_ksplit (oracle/heuristics.py)."""
+    for dtype, kgran, tmax in ((moe.MOE_BF16, 64, 128), (moe.MOE_FP8_TOKEN, 128, 128), (moe.MOE_MXFP4, 256, 64)):
+        for T in (1, 2, 3, 8, 17, 32, 64, tmax):
+            for (H, I, E, k) in ((4096, 14336, 8, 2), (7168, 2048, 256, 8), (1024, 768, 16, 4), (512, 256, 3, 3)):
+                if dtype == moe.MOE_MXFP4 and (H % 256 or I % 256):
+                    continue
+                p = moe.moe_plan(dtype, T, H, I, E, k, num_sms=units)
+                assert p.mode == moe.MOE_MODE_SWAP
+                assert p.block_m == heuristics.swap_block_m(T, k, E, I, units, dtype == moe.MOE_MXFP4)
+                assert p.split_k2 == heuristics.swap_split_k(T, k, E, H, I // kgran, units), (dtype, T, H, I, E, k)
+    # the measured choices for the Mixtral decode shapes on 152 SMs
+    if units == 152:
+        assert moe.moe_plan(moe.MOE_BF16, 32, 4096, 14336, 8, 2, num_sms=152).split_k2 == 2
+        assert moe.moe_plan(moe.MOE_BF16, 1, 4096, 14336, 8, 2, num_sms=152).split_k2 == 7
+        assert moe.moe_plan(moe.MOE_BF16, 32, 4096, 14336, 8, 2, num_sms=152).block_m == 16
+
+
 def test_plan_rejects_bad_options(moe):
     with pytest.raises(moe.MoEError):   # grouped mode supports block 128 only
         moe.moe_plan(moe.MOE_BF16, 512, 256, 256, 4, 2, block_m=64, num_sms=152)

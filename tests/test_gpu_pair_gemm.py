@@ -113,3 +113,77 @@ def test_gemm_pair_option_rejects_bad_value(moe):
     with pytest.raises(moe.MoEError) as ei:
         layer(inp["x"], inp, out)
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+# Light experts (all rows in one 128-row block) on swap-AB pair tiles: routings with empty,
+# single-token, one-block and multi-block experts; I a multiple of 256 (the light stage-1 tile
+# covers 256 intermediate columns); a ragged last tile of H in stage 2.
+LIGHT_CASES = [
+    # (name, T, H, I, E, k, bias)
+    ("all_light", 200, 256, 256, 64, 2, None),
+    ("zipf_mix", 1000, 512, 512, 64, 4, "zipf"),
+    ("ragged_h", 300, 640, 256, 32, 3, "normal"),
+    ("few_experts", 260, 256, 768, 4, 1, "normal"),
+]
+
+
+@pytest.mark.parametrize("light", [1, 0], ids=["light", "pairs_only"])
+@pytest.mark.parametrize("case", LIGHT_CASES, ids=lambda c: c[0])
+def test_light_expert_tiles(moe, case, light):
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=1.2 if bias == "zipf" else 0.5)
+    inp = synth.make_inputs(cfg, seed=13, device="cuda")
+    host = _host(inp)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
+    layer = moe.FusedMoE(moe.MOE_BF16, T, H, I, E, k, options=moe.Options(gemm_pair=1, light_tiles=light))
+    assert layer.plan.mode == moe.MOE_MODE_GROUPED
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    layer(inp["x"], w, out)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    counts = layer.view("expert_counts", torch.int32, (E,)).cpu().numpy()
+    print(name, "counts", sorted(counts.tolist()))
+    assert ((counts > 0) & (counts <= 128)).any()   # some light experts in every case
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
+    check_rows(out.float().cpu().numpy(), ref, 5e-3, label=f"{name} light={light}")
+    # bitwise reproducible
+    out2 = torch.empty_like(out)
+    layer(inp["x"], w, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_light_tiles_need_i_multiple_of_256(moe):
+    cfg = synth.MoEConfig("bad_light", T=200, H=256, I=384, E=8, k=2)
+    inp = synth.make_inputs(cfg, seed=1, device="cuda")
+    layer = moe.FusedMoE(moe.MOE_BF16, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k,
+                         options=moe.Options(gemm_pair=1, light_tiles=1))
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        layer(inp["x"], inp, out)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_finegrained_light_tiles_on_and_off(moe):
+    """The fine-grained workload (most experts hold a few tokens): both tile choices against the oracle
+    on the full-size parity sample."""
+    cfg = synth.CONFIGS["finegrained_zipf"]
+    inp = synth.make_inputs(cfg, seed=0, device="cuda")
+    host = _host(inp)
+    w = {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": inp["W_gate_up"], "W_down": inp["W_down"]}
+    outs = []
+    for light in (1, 0):
+        layer = moe.FusedMoE(moe.MOE_BF16, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k,
+                             options=moe.Options(gemm_pair=1, light_tiles=light))
+        out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+        layer(inp["x"], w, out)
+        torch.cuda.synchronize()
+        assert layer.status() == moe.MOE_OK
+        outs.append(out.float().cpu().numpy())
+        del layer
+    r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], cfg.k)
+    toks = parity_tokens(r_ids, cfg.E, 128)
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"],
+                                  cfg.k, toks, expert_major=True)
+    check_rows(outs[0][toks], ref, 5e-3, label="fine-grained light tiles")
+    check_rows(outs[1][toks], ref, 5e-3, label="fine-grained pair tiles only")
