@@ -141,7 +141,9 @@ size_t moe_fused_workspace_size(int dtype, int T, int H, int I, int E, int k, in
  * moe_fused_forward (for inspection and tests; -1 = not present).
  */
 typedef struct moe_ws_layout {
-    int64_t status;          /* int32 status word (MOE_OK or MOE_ERR_TIMEOUT) */
+    int64_t status;          /* int32 status word (MOE_OK or MOE_ERR_TIMEOUT); word 4 after it:
+                                tokens whose tensor-core routing fell back to all
+                                fixed-order logits */
     int64_t topk_ids;        /* int32 [T][k] */
     int64_t topk_weights;    /* fp32 [T][k] */
     int64_t sorted_ids;      /* int32 [max_padded] */
@@ -156,6 +158,9 @@ typedef struct moe_ws_layout {
     int64_t inter_h;         /* bf16 [max_padded][I]: SwiGLU output before its per-token
                                 quantisation (FP8 token only) */
     int64_t y;               /* fp32 [T*k][H], weighted rows in slot order */
+    int64_t router_logits;   /* fp32 router logits: [T][E] from the CUDA-core router, or the
+                                tensor-core router's per-slice partial sums
+                                [splits][ceil(T/128)*128][E] */
     int64_t total;
 } moe_ws_layout_t;
 
@@ -316,6 +321,14 @@ typedef struct moe_options {
      * has fewer than 4 blocks of 128 rows), 0 off, 1 on (needs I % 256 == 0,
      * else MOE_ERR_UNSUPPORTED).  Not used by the training forward. */
     int light_tiles;
+    /* Router for many experts (E >= 64, E % 32 == 0, T >= 64, k <= 28):
+     * -1 automatic / 1: logits on the tensor core, then the k + 4 leading
+     * candidates recomputed in the fixed order and the remaining experts
+     * checked against a bound on the difference of the two sums (a near tie
+     * recomputes all E logits in the fixed order), so the ids and weights are
+     * those of the fixed-order router bit for bit; 0: the fixed-order router
+     * on CUDA cores for every logit. */
+    int tc_router;
 } moe_options_t;
 
 /* Set *options to the defaults (gemm_pair -1, one_stage 1, pdl_mask -1, no

@@ -8,6 +8,7 @@
 // synchronises (except moe_workspace_status, which reads one word back).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -135,7 +136,12 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
         return o;
     };
     L.status = take(kStatusWords * 4);
-    L.logits = take((int64_t)T * E * 4);
+    {
+        int64_t lf = (int64_t)T * E;
+        if (router_tc_eligible(T, H, E, k))
+            lf = std::max<int64_t>(lf, (int64_t)router_tc_scratch_floats_max(T, E));
+        L.logits = take(lf * 4);
+    }
     L.topk_ids = take(S * 4);
     L.topk_w = take(S * 4);
     L.sort_scratch = take((int64_t)sort_scratch_bytes(T, k, E));
@@ -287,6 +293,7 @@ static moe_options_t default_options()
     o.one_stage = 1;
     o.pdl_mask = -1;
     o.light_tiles = -1;
+    o.tc_router = -1;
     return o;
 }
 
@@ -294,7 +301,7 @@ static int check_options(const moe_options_t &o)
 {
     if (o.gemm_pair < -1 || o.gemm_pair > 1 || o.one_stage < 0 || o.one_stage > 1 || o.pdl_mask < -1 ||
         o.pdl_mask > kPdlAll || o.unsatisfiable_h_wait < 0 || o.unsatisfiable_h_wait > 1 || o.light_tiles < -1 ||
-        o.light_tiles > 1)
+        o.light_tiles > 1 || o.tc_router < -1 || o.tc_router > 1)
         return MOE_ERR_INVALID_ARG;
     if (o.stage_events)
         for (int i = 0; i < 7; ++i)
@@ -356,10 +363,17 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // still waits (griddepcontrol.wait) for the preceding kernel to complete before it reads x or
     // zeroes the status words; it only starts early after a kernel that triggers its dependents,
     // such as the previous call's combine.
-    if (launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
-                      router_bias, T, H, E, k, 1, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status, pdl,
-                      st) != cudaSuccess)
+    const bool tc_router = o.tc_router != 0 && router_tc_eligible(T, H, E, k);
+    if (tc_router) {
+        if (launch_router_tc(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
+                             router_bias, T, H, E, k, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status,
+                             pdl, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else if (launch_router(static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(W_router),
+                             router_bias, T, H, E, k, 1, topk_ids, topk_w, static_cast<float *>(at(L.logits)), status,
+                             pdl, st) != cudaSuccess) {
         return MOE_ERR_CUDA;
+    }
     mark(o, 1, st);
 
     SortOut so;
@@ -873,6 +887,7 @@ int moe_workspace_layout(int dtype, int T, int H, int I, int E, int k, int block
     out->inter_scales = L.inter_scales;
     out->inter_h = L.inter_h;
     out->y = L.y;
+    out->router_logits = L.logits;
     out->total = L.total;
     return MOE_OK;
 }

@@ -92,7 +92,9 @@ struct Tile {
 // Internal tile shape of the weight-gradient GEMMs (STAGE 5): per expert e,
 // D[e] (M x N) = A_e B_e^T with K running over e's sorted token positions;
 // A and B are row arrays whose K dimension is the position (transposed
-// activations), tiles 128 rows of A x 256 rows of B.
+// activations), tiles 128 rows of A x 256 rows of B.  With no
+// expert_offsets the a.E "segments" are equal slices of K instead (the
+// router's tensor-core logits: D[s] = partial x W_router^T over slice s).
 constexpr int kModeSegment = 2;
 
 template <int MODE, int STAGE>
@@ -127,8 +129,15 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs &a, int t)
         tl.wrow0 = nt * 256;           // B rows (output columns)
         tl.wrow1 = tl.wrow0 + 128;
         tl.ncol0 = nt * 256;
-        tl.kb0 = a.expert_offsets[tl.e] / kBK<QT>;   // segments are whole 128-row blocks
-        tl.kb1 = a.expert_offsets[tl.e + 1] / kBK<QT>;
+        if (a.expert_offsets) {
+            tl.kb0 = a.expert_offsets[tl.e] / kBK<QT>;   // segments are whole 128-row blocks
+            tl.kb1 = a.expert_offsets[tl.e + 1] / kBK<QT>;
+        } else {
+            // dense: K = a.K split evenly over the a.E "segments" (the router's logits)
+            const int per = nkb / a.E;
+            tl.kb0 = tl.e * per;
+            tl.kb1 = tl.kb0 + per;
+        }
         tl.ks = 0;
         return tl;
     }

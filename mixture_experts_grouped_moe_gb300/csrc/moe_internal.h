@@ -73,8 +73,10 @@ inline cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, di
 // ------------------------------------------------------ route / sort / aux
 
 // Words at the start of the fused forward's workspace: [0] status, [1] stage-1
-// tile counter, [2] stage-2 tile counter, [3] spare.  The router zeroes them.
-constexpr int kStatusWords = 4;
+// tile counter, [2] stage-2 tile counter, [3] the one-launch decode's count of
+// finished stage-1 epilogue warps, [4] tokens whose tensor-core routing fell
+// back to all fixed-order logits, [5..7] spare.  The router zeroes them.
+constexpr int kStatusWords = 8;
 
 // Small T*E: one fused launch.  Large T*E: a tiled logit pass into `logits`
 // (fp32 [T][E], required then) followed by a warp-per-token top-k pass.
@@ -86,6 +88,20 @@ bool router_needs_logits(int T, int E);
 cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
                           int k, int renorm, int32_t *ids, float *wts, float *logits, int *status, int pdl_mask,
                           cudaStream_t st);
+
+// Router on the tensor core for many experts (ids and weights identical to
+// launch_router's with renorm = 1): per-expert norms (+ zeroing the status
+// words), logits on the tensor core in K slices, then a warp per token that
+// recomputes the leading candidates in the fixed order and checks the rest
+// against a bound.  scratch: router_tc_scratch_floats floats.
+bool router_tc_eligible(int T, int H, int E, int k);
+int router_tc_splits(int T, int H, int E, int num_sms);
+size_t router_tc_scratch_floats(int T, int H, int E, int num_sms);
+// An upper bound of router_tc_scratch_floats for any SM count (at most 8 K slices).
+inline size_t router_tc_scratch_floats_max(int T, int E) { return (size_t)8 * ((T + 127) / 128 * 128) * E + E; }
+cudaError_t launch_router_tc(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
+                             int k, int32_t *ids, float *wts, float *scratch, int *status, int pdl_mask,
+                             cudaStream_t st);
 
 // Chunked stable counting sort; ws holds nchunks*E int32 chunk counters.
 constexpr int kSortChunk = 1024;

@@ -12,6 +12,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <cstring>
 
 #include "moe_internal.h"
 
@@ -60,6 +61,9 @@ __device__ __forceinline__ float butterfly_sum(float v)
     return v;
 }
 
+__device__ __forceinline__ void warp_softmax_k(const float *lg, int E, int k, int renorm, int lane, float my_v,
+                                               int my_e, int32_t *ids_out, float *w_out);
+
 // Top k of one token's E logits by one warp (larger logit first, the lower
 // expert on ties), then the softmax over the k selected (renorm = 1) or over
 // all E, evaluated at the selected (renorm = 0).  k <= 32, E <= 1024.
@@ -97,6 +101,14 @@ __device__ __forceinline__ void warp_topk_softmax(const float *lg, int E, int k,
             my_e = be;
         }
     }
+    warp_softmax_k(lg, E, k, renorm, lane, my_v, my_e, ids_out, w_out);
+}
+
+// Lanes j < k hold the j-th selected logit and expert (largest first): the weights, softmax over
+// the k (renorm = 1) or over all E logits lg (renorm = 0), and the outputs.
+__device__ __forceinline__ void warp_softmax_k(const float *lg, int E, int k, int renorm, int lane, float my_v,
+                                               int my_e, int32_t *ids_out, float *w_out)
+{
     const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
     float sum = 0.0f;
@@ -371,6 +383,286 @@ cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const
         return err;
     return launch_kernel(pdl_site(pdl_mask, kPdlTopk), topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, logits, T,
                          E, k, renorm, ids, wts);
+}
+
+// ============================================== router on the tensor core
+//
+// With many experts (fine-grained routing: E = 256, H = 7168) the fixed-order
+// fp32 logits cost E*H FMAs per token on CUDA cores.  Here the tensor core
+// computes all logits (bf16 products, fp32 accumulation in an unspecified
+// order, K split into slices whose partial logits are added after), and the
+// fixed order is spent only where it decides something:
+//   1. the k + kTcExtra experts with the largest tensor-core logits are the
+//      candidates; their logits are recomputed in the fixed order (exactly
+//      the values the other router kernels produce);
+//   2. the k largest candidates by those exact values (ties to the lower
+//      expert) are the selection, if every other expert's tensor-core logit
+//      plus a bound on the two computations' difference stays below the
+//      k-th exact value: then no other expert's exact logit can reach it;
+//   3. otherwise (a near tie) all E logits are recomputed in the fixed order
+//      and selected as the other kernels do.
+// So the ids and weights are the fixed-order ones bit for bit.  The bound:
+// both sums consist of the same exact products p_h = x_h * w_h (a bf16 x
+// bf16 product fits fp32); the fixed order adds at most H/32 + 5 of them in
+// a chain (error <= 2^-16 sum|p| for H <= 2^20 ... far below the next
+// term); the tensor core's accumulation is taken to lose at most 2^-12
+// sum|p| (an fp32 accumulator, even truncating, loses about 2^-22 per
+// addition; a test measures the actual difference); the slice additions and
+// the bias add a few fp32 roundings.  Together <= 2^-11 sum|p| + 2^-22 |bias|,
+// with sum|p| <= ||x_t|| ||w_e|| (Cauchy-Schwarz; both norms rounded up).
+constexpr int kTcExtra = 4;
+
+bool router_tc_eligible(int T, int H, int E, int k)
+{
+    return E >= 64 && E % 32 == 0 && E <= 1024 && k + kTcExtra <= 32 && T >= 64 && H % 64 == 0;
+}
+
+int router_tc_splits(int T, int H, int E, int num_sms)
+{
+    const int nkb = H / 64;
+    const int64_t tiles1 = (int64_t)((T + 127) / 128) * ((E + 255) / 256);
+    int s = 1;
+    while (s < 8 && tiles1 * s < num_sms / 2 && nkb % (2 * s) == 0)
+        s *= 2;
+    return s;
+}
+
+size_t router_tc_scratch_floats(int T, int H, int E, int num_sms)
+{
+    return (size_t)router_tc_splits(T, H, E, num_sms) * ((T + 127) / 128 * 128) * E + E;
+}
+
+// Upper bound of ||W_router[e]||_2 per expert (one warp per expert); also zeroes the status words.
+__global__ void __launch_bounds__(256) router_wnorm_kernel(const __nv_bfloat16 *__restrict__ Wr, int H, int E,
+                                                          float *__restrict__ wnorm, int *status)
+{
+    pdl_wait();
+    pdl_trigger();
+    if (status && blockIdx.x == 0 && threadIdx.x < kStatusWords)
+        status[threadIdx.x] = 0;  // status word, tile counters, router fall-back count
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    if (e >= E)
+        return;
+    float ss = 0.0f;
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+        float f[8];
+        bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0)), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            ss = fmaf(f[c], f[c], ss);
+    }
+    ss = butterfly_sum(ss);
+    // the fp32 sum of squares is within (H/32 + 6) * 2^-24 of the exact one (H <= 2^20)
+    if (lane == 0)
+        wnorm[e] = sqrtf(ss) * (1.0f + 0x1p-8f);
+}
+
+// Fixed-order logits (the order of the other router kernels: lane L adds the elements h with
+// (h / 8) mod 32 == L in ascending h, then the butterfly, then the bias) of n <= 4 experts of
+// one token, by one warp; every lane returns the values.
+__device__ __forceinline__ void exact_logits4(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
+                                              int H, const int (&es)[4], int n, int lane, float (&out)[4])
+{
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+        float xf[8];
+        bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(xrow + h0)), xf);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < n) {
+                float wf[8];
+                bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)es[j] * H + h0)), wf);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    acc[j] = __fmaf_rn(xf[c], wf[c], acc[j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float v = butterfly_sum(acc[j]);
+        if (j < n && bias)
+            v = __fadd_rn(v, bias[es[j]]);
+        out[j] = v;
+    }
+}
+
+// One warp per token: tensor-core logits -> candidates -> exact values -> checked selection.
+__global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                           const __nv_bfloat16 *__restrict__ Wr,
+                                                           const float *__restrict__ bias, int T, int H, int E,
+                                                           int k, const float *__restrict__ part, int nsplit,
+                                                           int64_t part_rows, const float *__restrict__ wnorm,
+                                                           int32_t *__restrict__ ids, float *__restrict__ wts,
+                                                           int *fallbacks)
+{
+    extern __shared__ float s_lg[];  // [8 warps][E]
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T)
+        return;
+    float *lg = s_lg + warp * E;
+    const __nv_bfloat16 *xrow = x + (size_t)t * H;
+    for (int e = lane; e < E; e += 32) {
+        float v = 0.0f;
+        for (int sl = 0; sl < nsplit; ++sl)
+            v += part[((size_t)sl * part_rows + t) * E + e];
+        if (bias)
+            v += bias[e];
+        lg[e] = v;
+    }
+    float ss = 0.0f;
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+        float f[8];
+        bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(xrow + h0)), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            ss = fmaf(f[c], f[c], ss);
+    }
+    const float xnorm = sqrtf(butterfly_sum(ss)) * (1.0f + 0x1p-8f);
+    __syncwarp();
+
+    // 1. candidates: the nc largest tensor-core logits (ties to the lower expert); lane c keeps one
+    const int nc = min(E, k + kTcExtra);
+    uint32_t taken = 0;  // bit m: expert lane + 32m is a candidate
+    int my_c = 0;
+    for (int c = 0; c < nc; ++c) {
+        float bv = -FLT_MAX;
+        int be = INT_MAX;
+        for (int m = 0, e = lane; e < E; ++m, e += 32) {
+            if (taken & (1u << m))
+                continue;
+            if (be == INT_MAX || lg[e] > bv) {
+                bv = lg[e];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane)
+            taken |= 1u << (be >> 5);
+        if (lane == c)
+            my_c = be;
+    }
+    // 2. their fixed-order logits, four experts per pass over the token's row
+    float my_x = 0.0f;
+    for (int c0 = 0; c0 < nc; c0 += 4) {
+        int es[4];
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            es[j] = __shfl_sync(0xffffffffu, my_c, min(c0 + j, nc - 1));
+        exact_logits4(xrow, Wr, bias, H, es, min(4, nc - c0), lane, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (lane == c0 + j)
+                my_x = v[j];
+    }
+    // 3. the k largest candidates by exact value (ties to the lower expert), in lanes 0..k-1
+    uint32_t sel = 0;  // bit c: candidate c selected
+    float my_v = 0.0f;
+    int my_e = 0;
+    float vk = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -FLT_MAX;
+        int be = INT_MAX, bc = -1;
+        if (lane < nc && !(sel & (1u << lane))) {
+            bv = my_x;
+            be = my_c;
+            bc = lane;
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+                bc = oc;
+            }
+        }
+        sel |= 1u << bc;
+        if (lane == j) {
+            my_v = bv;
+            my_e = be;
+        }
+        vk = bv;
+    }
+    // 4. no other expert may reach the k-th exact value
+    bool near = false;
+    if (nc < E) {
+        for (int m = 0, e = lane; e < E; ++m, e += 32) {
+            if (taken & (1u << m))
+                continue;
+            const float margin = 0x1p-11f * xnorm * wnorm[e] + (bias ? 0x1p-22f * fabsf(bias[e]) : 0.0f);
+            if (lg[e] + margin * (1.0f + 0x1p-20f) >= vk)
+                near = true;
+        }
+    }
+    if (__any_sync(0xffffffffu, near)) {
+        // a near tie: every logit in the fixed order, selected as the other router kernels do
+        for (int e0 = 0; e0 < E; e0 += 4) {
+            const int es[4] = {e0, min(e0 + 1, E - 1), min(e0 + 2, E - 1), min(e0 + 3, E - 1)};
+            float v[4];
+            exact_logits4(xrow, Wr, bias, H, es, min(4, E - e0), lane, v);
+            if (lane == 0)
+                for (int j = 0; j < 4 && e0 + j < E; ++j)
+                    lg[e0 + j] = v[j];
+        }
+        __syncwarp();
+        if (lane == 0 && fallbacks)
+            atomicAdd(fallbacks, 1);
+        warp_topk_softmax(lg, E, k, 1, lane, ids + (size_t)t * k, wts + (size_t)t * k);
+        return;
+    }
+    warp_softmax_k(lg, E, k, 1, lane, my_v, my_e, ids + (size_t)t * k, wts + (size_t)t * k);
+}
+
+cudaError_t launch_router_tc(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const float *bias, int T, int H, int E,
+                             int k, int32_t *ids, float *wts, float *scratch, int *status, int pdl_mask,
+                             cudaStream_t st)
+{
+    const int nsm = num_sms_current_device();
+    if (nsm <= 0)
+        return cudaErrorInvalidDevice;
+    const int nsplit = router_tc_splits(T, H, E, nsm);
+    const int64_t rows = (T + 127) / 128 * 128;
+    float *part = scratch;
+    float *wnorm = scratch + (size_t)nsplit * rows * E;
+    cudaError_t err = launch_kernel(pdl_site(pdl_mask, kPdlRouter), router_wnorm_kernel, dim3((E + 7) / 8),
+                                    dim3(256), 0, st, Wr, H, E, wnorm, status);
+    if (err != cudaSuccess)
+        return err;
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    if (!encode_tmap_2d(&g.tm_x, x, 2, H, T, 64, 128) || !encode_tmap_2d(&g.tm_w, Wr, 2, H, E, 64, 128))
+        return cudaErrorInvalidValue;
+    g.K = H;
+    g.M = (int)rows;
+    g.N = E;
+    g.E = nsplit;            // K slices
+    g.expert_offsets = nullptr;
+    g.dw_out = part;
+    g.status = status;
+    g.tile_counter = nullptr;
+    const int64_t tiles = (int64_t)nsplit * (rows / 128) * ((E + 255) / 256);
+    err = launch_gemm_backward_bf16(5, g, (int)(tiles < nsm ? tiles : nsm), st);
+    if (err != cudaSuccess)
+        return err;
+    return launch_kernel(pdl_site(pdl_mask, kPdlTopk), router_select_kernel, dim3((T + 7) / 8), dim3(256),
+                         sizeof(float) * 8 * E, st, x, Wr, bias, T, H, E, k, part, nsplit, rows, wnorm, ids, wts,
+                         status ? status + 4 : nullptr);
 }
 
 // ============================================================ align-sort

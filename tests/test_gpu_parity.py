@@ -399,3 +399,80 @@ def test_fused_host_entry_matches_device_entry(moe):
                                 "W_down": inp["W_down"]}, out_host)
     torch.cuda.synchronize()
     assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+
+
+# ------------------------------------------------ tensor-core router
+
+def _route_in_layer(moe, cfg, inp, tc):
+    """Run the layer with the tensor-core router on or off; return its workspace's ids, weights, layer."""
+    layer = moe.FusedMoE(moe.MOE_BF16, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, options=moe.Options(tc_router=tc))
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    layer(inp["x"], inp, out)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    ids = layer.view("topk_ids", torch.int32, (cfg.T, cfg.k)).cpu().numpy()
+    w = layer.view("topk_weights", torch.float32, (cfg.T, cfg.k)).cpu().numpy()
+    return ids, w, layer
+
+
+TC_ROUTER_CASES = [
+    synth.CONFIGS["finegrained_zipf"],
+    synth.MoEConfig("e64_k2", T=300, H=512, I=256, E=64, k=2),
+    synth.MoEConfig("e128_k8_bias", T=1000, H=1024, I=256, E=128, k=8, bias="normal", bias_param=0.5),
+    synth.MoEConfig("e1024_k28", T=70, H=256, I=256, E=1024, k=28, bias="zipf", bias_param=1.2),
+]
+
+
+@pytest.mark.parametrize("cfg", TC_ROUTER_CASES, ids=lambda c: c.name)
+def test_tc_router_bit_identical_to_fixed_order(moe, cfg):
+    """Ids and weights of the tensor-core router equal the fixed-order router's and the oracle's ids
+    bit for bit; few tokens need the all-exact fall-back."""
+    if cfg.name == "finegrained_zipf":
+        inp, host = gpu_inputs(cfg)
+    else:
+        inp = synth.make_inputs(cfg, seed=4, device="cuda")
+        host = {kk: (None if v is None else (synth.bf16_bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()))
+                for kk, v in inp.items()}
+    ids1, w1, layer = _route_in_layer(moe, cfg, inp, 1)
+    ids0, w0, _ = _route_in_layer(moe, cfg, inp, 0)
+    assert np.array_equal(ids1, ids0)
+    assert np.array_equal(w1.view(np.uint32), w0.view(np.uint32))
+    r_ids, _, r_logits = oracle.route(host["x"], host["W_router"], host["bias"], cfg.k)
+    assert np.array_equal(ids1, r_ids)
+    st = layer.ws[layer.layout.status:layer.layout.status + 32].view(torch.int32).cpu().numpy()
+    fallbacks = int(st[4])
+    print(f"{cfg.name}: {fallbacks} of {cfg.T} tokens fell back to all fixed-order logits")
+    assert fallbacks <= max(2, cfg.T // 10)
+    # the tensor-core logits against the fixed-order ones: far inside the bound the check assumes
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = (cfg.T + 127) // 128 * 128
+    s, nkb, tiles1 = 1, cfg.H // 64, (rows // 128) * ((cfg.E + 255) // 256)
+    while s < 8 and tiles1 * s < nsm // 2 and nkb % (2 * s) == 0:
+        s *= 2
+    part = layer.view("router_logits", torch.float32, (s, rows, cfg.E)).double().sum(0)[:cfg.T].cpu().numpy()
+    if host["bias"] is not None:
+        part = part + host["bias"][None, :].astype(np.float64)
+    xf = host["x"].astype(np.uint32) << 16
+    wf = host["W_router"].astype(np.uint32) << 16
+    xn = np.linalg.norm(xf.view(np.float32).astype(np.float64), axis=1)
+    wn = np.linalg.norm(wf.view(np.float32).astype(np.float64), axis=1)
+    rel = np.abs(part - r_logits.astype(np.float64)) / (xn[:, None] * wn[None, :])
+    print(f"{cfg.name}: max |tensor-core - fixed-order| / (||x|| ||w||) = {rel.max():.3e}")
+    assert rel.max() < 2.0 ** -16
+
+
+def test_tc_router_exact_ties_fall_back(moe):
+    """Experts with identical router rows tie exactly: the check must fall back to the fixed order
+    and give the tie to the lower expert, as the fixed-order router does."""
+    cfg = synth.MoEConfig("ties", T=256, H=512, I=256, E=64, k=4)
+    inp = synth.make_inputs(cfg, seed=6, device="cuda")
+    for e in range(64):  # four groups of 16 identical rows: the leading group ties well past k + 4
+        inp["W_router"][e] = inp["W_router"][e - e % 16]
+    ids1, w1, layer = _route_in_layer(moe, cfg, inp, 1)
+    ids0, w0, _ = _route_in_layer(moe, cfg, inp, 0)
+    assert np.array_equal(ids1, ids0)
+    assert np.array_equal(w1.view(np.uint32), w0.view(np.uint32))
+    r_ids, _, _ = oracle.route(synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"]), None, cfg.k)
+    assert np.array_equal(ids1, r_ids)
+    st = layer.ws[layer.layout.status:layer.layout.status + 32].view(torch.int32).cpu().numpy()
+    assert st[4] == cfg.T   # every token's leading group ties beyond its candidates: all fell back
