@@ -37,12 +37,15 @@
 // (fine-grained routing leaves most experts with a few tokens).  Its tiles
 // swap the operands instead: the pair's 256-row MMA side holds weight rows
 // (128 per CTA) and the N side its np = ceil32(count) token rows (np / 2 per
-// CTA, loaded in 16-row boxes).  Stage 1 issues two MMAs per K step, gate
-// rows and the matching up rows, into two accumulators of the same TMEM
-// lanes, so SwiGLU still pairs within a thread; a tile covers 256
-// intermediate columns.  Stage 2 covers 256 output features per tile.  The
-// epilogue then holds one feature per thread and a token per accumulator
-// column.  Heavy and light experts' tiles are claimed from the same counter,
+// CTA, loaded in 16-row boxes).  Each K step issues two MMAs into two
+// accumulators of the same TMEM lanes: stage 1 gate rows and the matching
+// up rows (SwiGLU still pairs within a thread; a tile covers 256
+// intermediate columns), stage 2 two consecutive 256-row ranges of W_down (a
+// tile covers 512 output features).  So a light tile streams 32 KB of
+// weights per CTA per K step and five 40 KB stages keep 160 KB in flight: a
+// light tile is bound by the bytes in flight per SM at the loaded memory
+// latency, not by the tensor core.  The epilogue holds one feature per
+// thread and a token per accumulator column.  Heavy and light experts' tiles are claimed from the same counter,
 // so tensor-bound and weight-streaming tiles run side by side.
 #include "gemm_common.cuh"
 #include "moe_internal.h"
@@ -54,12 +57,13 @@ namespace gemm2sm {
 
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes of K
 constexpr int kSwapRowsPerLoad = 16;        // token rows per TMA box of a light expert's tile
-// Pipeline stage: [A: token rows | B: weight rows]; with light-expert tiles in stage 1 a stage
-// also holds [gate rows | up rows | up to 64 token rows], 40 KB, so one fewer stage fits.
+// Pipeline stage: [A: token rows | B: weight rows]; with light-expert tiles a stage also holds
+// [weight rows 0-127 | weight rows 128-255 of the second range | up to 64 token rows], 40 KB, so
+// one fewer stage fits.
 template <int STAGE, int LT>
-constexpr int kStageBytesT = (STAGE == 1 && LT) ? 2 * kHalfBytes + 64 * 128 : 2 * kHalfBytes;
+constexpr int kStageBytesT = LT ? 2 * kHalfBytes + 64 * 128 : 2 * kHalfBytes;
 template <int STAGE, int LT>
-constexpr int kStagesT = (STAGE == 1 && LT) ? 5 : 6;
+constexpr int kStagesT = LT ? 5 : 6;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;
@@ -113,17 +117,20 @@ struct PairTile {
 __device__ __forceinline__ bool light_expert(int nb) { return nb == 1; }
 
 // Tiles of one expert: ceil(blocks / 2) pairs per N tile; with LT, a light expert has none of
-// those and one light tile per 256 output columns instead.
+// those and one light tile per 256 (stage 1) or 512 (stage 2) output columns instead.
 template <int STAGE, int LT>
 __device__ __forceinline__ int heavy_tiles(int nb, int nnt)
 {
     return (LT && light_expert(nb)) ? 0 : (nb + 1) / 2 * nnt;
 }
 
-template <int LT>
+template <int STAGE>
+constexpr int kLightCols = STAGE == 1 ? 256 : 512;
+
+template <int STAGE, int LT>
 __device__ __forceinline__ int light_tiles(const GemmArgs &a, int nb)
 {
-    return (LT && light_expert(nb)) ? (a.N + 255) / 256 : 0;
+    return (LT && light_expert(nb)) ? (a.N + kLightCols<STAGE> - 1) / kLightCols<STAGE> : 0;
 }
 
 // The last e in [0, E) with start[e] <= t (experts without tiles share their successor's start).
@@ -182,16 +189,17 @@ __device__ __forceinline__ PairTile decode(const SM &sm, const GemmArgs &a, int 
         if ((int)((int64_t)(t + 1) * L / tot) > lb) {
             const int lo = find_expert(sm.lstart, a.E, lb);
             p.e = lo;
-            // local = the 256-column slice of the output
+            // local = the slice of kLightCols output columns
             const int local = lb - sm.lstart[lo];
             p.swap = 1;
             p.mb0 = sm.off[lo] >> 7;
             p.second = 1;
             p.cnt = __ldg(a.expert_counts + lo);
             p.np = (p.cnt + 31) & ~31;
-            p.ncol0 = local * 256;
-            p.wrow0 = lo * a.rows_per_expert + p.ncol0;        // gate rows (stage 1) / W_down rows
-            p.wrow1 = lo * a.rows_per_expert + a.N + p.ncol0;  // up rows (stage 1)
+            p.ncol0 = local * kLightCols<STAGE>;
+            p.wrow0 = lo * a.rows_per_expert + p.ncol0;  // gate rows (stage 1) / W_down rows ncol0..
+            // stage 1: the matching up rows; stage 2: the next 256 rows of W_down
+            p.wrow1 = STAGE == 1 ? lo * a.rows_per_expert + a.N + p.ncol0 : p.wrow0 + 256;
             p.kb0 = p.kb1 = 0;
             return p;
         }
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             const int o0 = a.expert_offsets[e], o1 = a.expert_offsets[e + 1];
             sm.off[e] = o0;
             hsum += heavy_tiles<STAGE, LT>((o1 - o0) >> 7, nnt);
-            lsum += light_tiles<LT>(a, (o1 - o0) >> 7);
+            lsum += light_tiles<STAGE, LT>(a, (o1 - o0) >> 7);
         }
         int hincl = hsum, lincl = lsum;
 #pragma unroll
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             hrun += heavy_tiles<STAGE, LT>(nb, nnt);
             if (LT) {
                 sm.lstart[e] = lrun;
-                lrun += light_tiles<LT>(a, nb);
+                lrun += light_tiles<STAGE, LT>(a, nb);
             }
         }
         if (lane == 31) {
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 const int kb0 = STAGE == 5 ? p.kb0 : 0, kb1 = STAGE == 5 ? p.kb1 : nkb;
                 // light tile: this CTA's half of the token rows, and the bytes of both CTAs per stage
                 const int half = p.swap ? p.np / 2 : 0;
-                const uint32_t swap_bytes = 2u * ((STAGE == 1 ? 2 : 1) * kHalfBytes + half * 128);
+                const uint32_t swap_bytes = 2u * (2 * kHalfBytes + half * 128);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
                         ok = false;
@@ -384,13 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     if (LT && p.swap) {
                         if (leader)
                             mbar_arrive_expect_tx(&sm.full[s], swap_bytes);
-                        // weights: rows r*128.. of the tile's 256 (stage 1: gate, then up), tokens after them
+                        // weights: rows r*128.. of each of the tile's two 256-row ranges, tokens after them
                         tma_load_2d_pair(sm.stage[s], &a.tm_w, kb * kBK<QT>, p.wrow0 + (int)rank * 128, fullc,
                                          pol_w);
-                        if (STAGE == 1)
-                            tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>,
-                                             p.wrow1 + (int)rank * 128, fullc, pol_w);
-                        uint8_t *tok = sm.stage[s] + (STAGE == 1 ? 2 : 1) * kHalfBytes;
+                        tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, p.wrow1 + (int)rank * 128,
+                                         fullc, pol_w);
+                        uint8_t *tok = sm.stage[s] + 2 * kHalfBytes;
                         const int trow = p.mb0 * 128 + (int)rank * half;
                         for (int c = 0; c < half; c += kSwapRowsPerLoad)
                             tma_load_2d_pair(tok + c * 128, &a.tm_x16, kb * kBK<QT>, trow + c, fullc, pol_x);
@@ -465,17 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     tc_fence_after();
                     const uint32_t accum0 = kb > kb0 ? 1u : 0u;
                     if (LT && swap) {
-                        // A = weight rows (this CTA's 128 of 256), B = the expert's token rows
+                        // A = weight rows (this CTA's 128 of each 256-row range), B = the expert's token
+                        // rows; the second range into the second accumulator half
                         const uint8_t *w0 = sm.stage[s];
-                        const uint8_t *tok = sm.stage[s] + (STAGE == 1 ? 2 : 1) * kHalfBytes;
+                        const uint8_t *tok = sm.stage[s] + 2 * kHalfBytes;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t accum = (kk > 0) ? 1u : accum0;
                             mma_pair<QT>(d, smem_desc_sw128(w0 + kk * 32), smem_desc_sw128(tok + kk * 32),
                                          idesc_swap, accum);
-                            if (STAGE == 1)  // the up rows into the second accumulator half
-                                mma_pair<QT>(d + 128, smem_desc_sw128(w0 + kHalfBytes + kk * 32),
-                                             smem_desc_sw128(tok + kk * 32), idesc_swap, accum);
+                            mma_pair<QT>(d + 128, smem_desc_sw128(w0 + kHalfBytes + kk * 32),
+                                         smem_desc_sw128(tok + kk * 32), idesc_swap, accum);
                         }
                     } else {
                         const uint8_t *xa = sm.stage[s];
@@ -554,13 +561,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             dst[(size_t)j * a.N] = __float2bfloat16_rn(silu(v[j]) * u[j]);
-                    } else if (f < a.N) {
+                    } else {
+                        // features f (first accumulator half) and f + 256 (second half)
+                        float v2[32];
+                        tmem_ld32(tacc + 128 + c0, v2);
+                        const bool ok0 = f < a.N, ok1 = f + 256 < a.N;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int c = c0 + j;
                             if (c < p.cnt) {
                                 const int slot = a.sorted_ids[row0 + c];
-                                a.y[(size_t)slot * a.N + f] = a.sorted_weights[row0 + c] * v[j];
+                                const float wgt = a.sorted_weights[row0 + c];
+                                if (ok0)
+                                    a.y[(size_t)slot * a.N + f] = wgt * v[j];
+                                if (ok1)
+                                    a.y[(size_t)slot * a.N + f + 256] = wgt * v2[j];
                             }
                         }
                     }

@@ -124,9 +124,13 @@ struct SortOut {
 cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k, int E, int block_m,
                               const SortOut &o, void *scratch, bool pdl_first, bool pdl_inner, cudaStream_t st);
 
-// x rows gathered into sorted order (zero rows for padding), up to *npp rows.
+// x rows gathered into sorted order, up to *npp rows.  Padding rows are written as zeros when
+// zero_padding is set (the training forward: the weight gradients sum over every position);
+// otherwise they are left as they are -- a GEMM output row depends only on its own input row,
+// and the results of padding rows are never stored.
 cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
-                               int H, int64_t P_max, __nv_bfloat16 *xs, bool pdl, cudaStream_t st);
+                               int H, int64_t P_max, __nv_bfloat16 *xs, bool zero_padding, bool pdl,
+                               cudaStream_t st);
 // Same, quantised per 1x128 group: codes [P_max][H], scales transposed [H/128][P_max].
 cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
                                      int k, int H, int64_t P_max, uint8_t *q, float *sT, bool pdl, cudaStream_t st);

@@ -459,28 +459,56 @@ __global__ void __launch_bounds__(256) router_wnorm_kernel(const __nv_bfloat16 *
 }
 
 // Fixed-order logits (the order of the other router kernels: lane L adds the elements h with
-// (h / 8) mod 32 == L in ascending h, then the butterfly, then the bias) of n <= 4 experts of
-// one token, by one warp; every lane returns the values.
-__device__ __forceinline__ void exact_logits4(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
-                                              int H, const int (&es)[4], int n, int lane, float (&out)[4])
+// (h / 8) mod 32 == L in ascending h, then the butterfly, then the bias) of n <= 8 experts of
+// one token, by one warp; every lane returns the values.  Two 256-element rounds are loaded
+// before either is added, so more loads are in flight; each lane's chain still adds its
+// elements in ascending h (round r before round r + 1).
+__device__ __forceinline__ void exact_logits8(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
+                                              int H, const int (&es)[8], int n, int lane, float (&out)[8])
 {
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
-        float xf[8];
-        bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(xrow + h0)), xf);
+    float acc[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j)
+        acc[j] = 0.0f;
+    for (int h0 = lane * 8; h0 < H; h0 += 512) {
+        const bool two = h0 + 256 < H;
+        const uint4 xv0 = __ldg(reinterpret_cast<const uint4 *>(xrow + h0));
+        const uint4 xv1 = two ? __ldg(reinterpret_cast<const uint4 *>(xrow + h0 + 256)) : make_uint4(0, 0, 0, 0);
+        uint4 wv0[8], wv1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < n) {
+                const __nv_bfloat16 *wr = Wr + (size_t)es[j] * H + h0;
+                wv0[j] = __ldg(reinterpret_cast<const uint4 *>(wr));
+                wv1[j] = two ? __ldg(reinterpret_cast<const uint4 *>(wr + 256)) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        float xf[8];
+        bf16x8_to_float(xv0, xf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
             if (j < n) {
                 float wf[8];
-                bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)es[j] * H + h0)), wf);
+                bf16x8_to_float(wv0[j], wf);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     acc[j] = __fmaf_rn(xf[c], wf[c], acc[j]);
             }
+        if (two) {
+            bf16x8_to_float(xv1, xf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < n) {
+                    float wf[8];
+                    bf16x8_to_float(wv1[j], wf);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        acc[j] = __fmaf_rn(xf[c], wf[c], acc[j]);
+                }
         }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
         float v = butterfly_sum(acc[j]);
         if (j < n && bias)
             v = __fadd_rn(v, bias[es[j]]);
@@ -554,17 +582,17 @@ __global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 
         if (lane == c)
             my_c = be;
     }
-    // 2. their fixed-order logits, four experts per pass over the token's row
+    // 2. their fixed-order logits, up to eight experts per pass over the token's row
     float my_x = 0.0f;
-    for (int c0 = 0; c0 < nc; c0 += 4) {
-        int es[4];
-        float v[4];
+    for (int c0 = 0; c0 < nc; c0 += 8) {
+        int es[8];
+        float v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 8; ++j)
             es[j] = __shfl_sync(0xffffffffu, my_c, min(c0 + j, nc - 1));
-        exact_logits4(xrow, Wr, bias, H, es, min(4, nc - c0), lane, v);
+        exact_logits8(xrow, Wr, bias, H, es, min(8, nc - c0), lane, v);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 8; ++j)
             if (lane == c0 + j)
                 my_x = v[j];
     }
@@ -612,12 +640,15 @@ __global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 
     }
     if (__any_sync(0xffffffffu, near)) {
         // a near tie: every logit in the fixed order, selected as the other router kernels do
-        for (int e0 = 0; e0 < E; e0 += 4) {
-            const int es[4] = {e0, min(e0 + 1, E - 1), min(e0 + 2, E - 1), min(e0 + 3, E - 1)};
-            float v[4];
-            exact_logits4(xrow, Wr, bias, H, es, min(4, E - e0), lane, v);
+        for (int e0 = 0; e0 < E; e0 += 8) {
+            int es[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                es[j] = min(e0 + j, E - 1);
+            float v[8];
+            exact_logits8(xrow, Wr, bias, H, es, min(8, E - e0), lane, v);
             if (lane == 0)
-                for (int j = 0; j < 4 && e0 + j < E; ++j)
+                for (int j = 0; j < 8 && e0 + j < E; ++j)
                     lg[e0 + j] = v[j];
         }
         __syncwarp();
@@ -1007,7 +1038,7 @@ cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x,
                                                          const int32_t *__restrict__ sorted_ids,
                                                          const int32_t *__restrict__ npp, int S, int k, int H,
-                                                         __nv_bfloat16 *__restrict__ xs)
+                                                         __nv_bfloat16 *__restrict__ xs, int zero_padding)
 {
     pdl_wait();
     pdl_trigger();
@@ -1016,6 +1047,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
     constexpr int U = 4;  // 16-byte pieces a thread requests before storing any (H <= 8192 in one round)
     for (int i = blockIdx.x; i < rows; i += gridDim.x) {
         const int s = sorted_ids[i];
+        if (s >= S && !zero_padding)
+            continue;  // a padding row: its GEMM results are discarded, so its contents do not matter
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)i * H);
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(s < S ? s / k : 0) * H);
         for (int c0 = threadIdx.x; c0 < nvec; c0 += U * blockDim.x) {
@@ -1036,12 +1069,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
-                               int H, int64_t P_max, __nv_bfloat16 *xs, bool pdl, cudaStream_t st)
+                               int H, int64_t P_max, __nv_bfloat16 *xs, bool zero_padding, bool pdl, cudaStream_t st)
 {
     int grid = (int)(P_max < 8192 ? P_max : 8192);
     if (grid < 1)
         grid = 1;
-    return launch_kernel(pdl, gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, sorted_ids, npp, S, k, H, xs);
+    return launch_kernel(pdl, gather_rows_kernel, dim3(grid), dim3(256), 0, st, x, sorted_ids, npp, S, k, H, xs,
+                         zero_padding ? 1 : 0);
 }
 
 // ---------------------------------------------------- FP8 quantisation
