@@ -312,14 +312,15 @@ typedef struct moe_options {
      * output of such a call is undefined; the next call on the workspace
      * starts clean. */
     int unsatisfiable_h_wait;
-    /* MOE_BF16 on CTA pairs: experts whose tokens fit one 128-row block take
-     * swap-AB pair tiles (the weights on the pair's 256-row MMA side, the
-     * expert's tokens, rounded up to 32, on N) instead of a mostly padded
-     * 256 x 256 tile; light and 256 x 256 tiles are interleaved so that
-     * weight streaming and tensor work overlap.  -1 automatic (default: on
-     * when I is a multiple of 256 and the average expert that can hold a slot
-     * has fewer than 4 blocks of 128 rows), 0 off, 1 on (needs I % 256 == 0,
-     * else MOE_ERR_UNSUPPORTED).  Not used by the training forward. */
+    /* MOE_BF16 on CTA pairs: experts with at most 64 tokens take swap-AB
+     * pair tiles (the weights on the pair's 256-row MMA side, the expert's
+     * tokens, rounded up to 32, on N) instead of a mostly padded 256 x 256
+     * tile; light and 256 x 256 tiles are interleaved so that weight
+     * streaming and tensor work overlap.  -1 automatic (default: on when I is
+     * a multiple of 256, E <= 512 and the average expert that can hold a slot
+     * has fewer than 4 blocks of 128 rows), 0 off, 1 on (needs I % 256 == 0
+     * and E <= 512, else MOE_ERR_UNSUPPORTED).  Not used by the training
+     * forward. */
     int light_tiles;
     /* Router for many experts (E >= 64, E % 32 == 0, T >= 64, k <= 28):
      * -1 automatic / 1: logits on the tensor core, then the k + 4 leading

@@ -397,10 +397,10 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // Automatic when the average expert that can hold a slot has fewer than 4 token blocks
     // (fine-grained routing): their kernel keeps one pipeline stage fewer in stage 1, which
     // measured 2-4 % slower on Mixtral prefill, where no expert is light.
-    if (o.light_tiles == 1 && (dtype != MOE_BF16 || I % 256 != 0))
+    if (o.light_tiles == 1 && (dtype != MOE_BF16 || I % 256 != 0 || !gemm_pair_light_supported(E)))
         return MOE_ERR_UNSUPPORTED;
     const int64_t e_can = ((int64_t)S < E) ? S : E;
-    const bool light = dtype == MOE_BF16 && !train && I % 256 == 0 &&
+    const bool light = dtype == MOE_BF16 && !train && I % 256 == 0 && gemm_pair_light_supported(E) &&
                        (o.light_tiles == 1 || (o.light_tiles == -1 && (int64_t)S < 4LL * 128 * e_can));
     // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
     // itself (no gather pass)

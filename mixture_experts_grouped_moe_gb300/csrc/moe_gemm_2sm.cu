@@ -32,19 +32,20 @@
 // token blocks from L2.  Every wait is bounded; a CTA that gives up raises the status word
 // and both CTAs still meet at the final cluster barrier.
 //
-// Light experts (LT = 1, stages 1 and 2, bf16): an expert whose sorted rows
-// fit one 128-row block would waste most of a 256-row pair tile on padding
-// (fine-grained routing leaves most experts with a few tokens).  Its tiles
-// swap the operands instead: the pair's 256-row MMA side holds weight rows
-// (128 per CTA) and the N side its np = ceil32(count) token rows (np / 2 per
+// Light experts (LT = 1, stages 1 and 2, bf16): an expert with at most 64
+// tokens would waste most of a 256-row pair tile on padding (fine-grained
+// routing leaves most experts with a few tokens).  Its tiles swap the
+// operands instead: the pair's 256-row MMA side holds weight rows (128 per
+// CTA) and the N side its np = ceil32(count) token rows (np / 2 <= 32 per
 // CTA, loaded in 16-row boxes).  Each K step issues two MMAs into two
 // accumulators of the same TMEM lanes: stage 1 gate rows and the matching
 // up rows (SwiGLU still pairs within a thread; a tile covers 256
 // intermediate columns), stage 2 two consecutive 256-row ranges of W_down (a
 // tile covers 512 output features).  So a light tile streams 32 KB of
-// weights per CTA per K step and five 40 KB stages keep 160 KB in flight: a
+// weights per CTA per K step and six 36 KB stages keep 192 KB in flight: a
 // light tile is bound by the bytes in flight per SM at the loaded memory
-// latency, not by the tensor core.  The epilogue holds one feature per
+// latency, not by the tensor core (hence the 64-token limit: a 128-token
+// light tile would need 40 KB stages, of which only five fit).  The epilogue holds one feature per
 // thread and a token per accumulator column.  Heavy and light experts' tiles are claimed from the same counter,
 // so tensor-bound and weight-streaming tiles run side by side.
 #include "gemm_common.cuh"
@@ -58,12 +59,14 @@ namespace gemm2sm {
 constexpr int kHalfBytes = 128 * 128;       // 128 rows x 128 bytes of K
 constexpr int kSwapRowsPerLoad = 16;        // token rows per TMA box of a light expert's tile
 // Pipeline stage: [A: token rows | B: weight rows]; with light-expert tiles a stage also holds
-// [weight rows 0-127 | weight rows 128-255 of the second range | up to 64 token rows], 40 KB, so
-// one fewer stage fits.
+// [weight rows 0-127 | weight rows 128-255 of the second range | up to 32 token rows], 36 KB.
+constexpr int kMaxLightTokens = 64;
 template <int STAGE, int LT>
-constexpr int kStageBytesT = LT ? 2 * kHalfBytes + 64 * 128 : 2 * kHalfBytes;
+constexpr int kStageBytesT = LT ? 2 * kHalfBytes + kMaxLightTokens / 2 * 128 : 2 * kHalfBytes;
 template <int STAGE, int LT>
-constexpr int kStagesT = LT ? 5 : 6;
+constexpr int kStagesT = 6;
+// Per-expert tables in shared memory: with light tiles the six 36 KB stages leave room for 512.
+constexpr int kMaxELight = 512;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;
@@ -91,14 +94,16 @@ struct __align__(1024) Smem {
     uint32_t tmem_base;
     int abort;
     int ntiles;
-    int off[kMaxE + 1];        // expert_offsets (sorted rows)
-    int tstart[kMaxE + 1];     // first pair tile of each expert (with LT: among the 256 x 256 tiles)
-    int lstart[LT ? kMaxE + 1 : 1];  // LT: first light-expert tile of each expert
+    int off[(LT ? kMaxELight : kMaxE) + 1];     // expert_offsets (sorted rows)
+    int tstart[(LT ? kMaxELight : kMaxE) + 1];  // first pair tile of each expert (LT: among the 256 x 256 tiles)
+    int lstart[LT ? kMaxELight + 1 : 1];        // LT: first light-expert tile of each expert
     int nheavy, nlight;        // LT: tiles of each kind
 };
 
 template <int STAGE, int LT>
 constexpr size_t kSmemBytesT = sizeof(Smem<STAGE, LT>) + 1024;
+static_assert(kSmemBytesT<1, 1> <= 227 * 1024 && kSmemBytesT<2, 1> <= 227 * 1024 && kSmemBytesT<1, 0> <= 227 * 1024,
+              "a CTA has at most 227 KB of shared memory");
 
 struct PairTile {
     int e;
@@ -113,24 +118,24 @@ struct PairTile {
     int np;       // light tile: MMA N = cnt rounded up to 32 (np / 2 rows per CTA)
 };
 
-// A light expert: all its sorted rows fit one 128-row block.
-__device__ __forceinline__ bool light_expert(int nb) { return nb == 1; }
+// A light expert: at most kMaxLightTokens tokens (one 128-row block, mostly padding).
+__device__ __forceinline__ bool light_expert(int nb, int cnt) { return nb == 1 && cnt <= kMaxLightTokens; }
 
 // Tiles of one expert: ceil(blocks / 2) pairs per N tile; with LT, a light expert has none of
 // those and one light tile per 256 (stage 1) or 512 (stage 2) output columns instead.
 template <int STAGE, int LT>
-__device__ __forceinline__ int heavy_tiles(int nb, int nnt)
+__device__ __forceinline__ int heavy_tiles(int nb, int cnt, int nnt)
 {
-    return (LT && light_expert(nb)) ? 0 : (nb + 1) / 2 * nnt;
+    return (LT && light_expert(nb, cnt)) ? 0 : (nb + 1) / 2 * nnt;
 }
 
 template <int STAGE>
 constexpr int kLightCols = STAGE == 1 ? 256 : 512;
 
 template <int STAGE, int LT>
-__device__ __forceinline__ int light_tiles(const GemmArgs &a, int nb)
+__device__ __forceinline__ int light_tiles(const GemmArgs &a, int nb, int cnt)
 {
-    return (LT && light_expert(nb)) ? (a.N + kLightCols<STAGE> - 1) / kLightCols<STAGE> : 0;
+    return (LT && light_expert(nb, cnt)) ? (a.N + kLightCols<STAGE> - 1) / kLightCols<STAGE> : 0;
 }
 
 // The last e in [0, E) with start[e] <= t (experts without tiles share their successor's start).
@@ -291,9 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         int hsum = 0, lsum = 0;
         for (int e = e0; e < e1; ++e) {
             const int o0 = a.expert_offsets[e], o1 = a.expert_offsets[e + 1];
+            const int cnt = LT ? a.expert_counts[e] : 0;
             sm.off[e] = o0;
-            hsum += heavy_tiles<STAGE, LT>((o1 - o0) >> 7, nnt);
-            lsum += light_tiles<STAGE, LT>(a, (o1 - o0) >> 7);
+            hsum += heavy_tiles<STAGE, LT>((o1 - o0) >> 7, cnt, nnt);
+            lsum += light_tiles<STAGE, LT>(a, (o1 - o0) >> 7, cnt);
         }
         int hincl = hsum, lincl = lsum;
 #pragma unroll
@@ -308,11 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         int hrun = hincl - hsum, lrun = lincl - lsum;
         for (int e = e0; e < e1; ++e) {
             const int nb = (a.expert_offsets[e + 1] - a.expert_offsets[e]) >> 7;
+            const int cnt = LT ? a.expert_counts[e] : 0;
             sm.tstart[e] = hrun;
-            hrun += heavy_tiles<STAGE, LT>(nb, nnt);
+            hrun += heavy_tiles<STAGE, LT>(nb, cnt, nnt);
             if (LT) {
                 sm.lstart[e] = lrun;
-                lrun += light_tiles<STAGE, LT>(a, nb);
+                lrun += light_tiles<STAGE, LT>(a, nb, cnt);
             }
         }
         if (lane == 31) {
@@ -763,6 +770,7 @@ int max_clusters()
 }  // namespace gemm2sm
 
 bool gemm_pair_supported(int E) { return E <= gemm2sm::kMaxE; }
+bool gemm_pair_light_supported(int E) { return E <= gemm2sm::kMaxELight; }
 
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
                              bool light)

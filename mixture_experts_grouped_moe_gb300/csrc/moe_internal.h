@@ -250,10 +250,11 @@ cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, 
                              int S, int k, int C, uint8_t *q, uint8_t *s, bool tiled, bool pdl, cudaStream_t st);
 // Grouped-mode GEMM on CTA pairs (two-SM tensor core), bf16 (qt = 0) or
 // per-token FP8 (qt = 1); max_pair_tiles bounds the useful cluster count.
-// light (bf16 stages 1 and 2; stage 1 needs N % 256 == 0): experts whose rows fit
-// one 128-row block take swap-AB pair tiles (a.tm_x16: the token operand in
+// light (bf16 stages 1 and 2; stage 1 needs N % 256 == 0; E <= 512): experts with
+// at most 64 tokens take swap-AB pair tiles (a.tm_x16: the token operand in
 // 16-row boxes; a.expert_counts required).
 bool gemm_pair_supported(int E);
+bool gemm_pair_light_supported(int E);  // light-expert tiles: E <= 512
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
                              bool light = false);
 cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
