@@ -156,6 +156,7 @@ struct GemmArgs {
     CUtensorMap tm_x;     // token operand rows [P_max][K]
     CUtensorMap tm_w;     // weight operand rows [E*rows_per_expert][K]
     CUtensorMap tm_x16;   // the token operand in 16-row boxes (light-expert pair tiles)
+    CUtensorMap tm_xg;    // the layer input x [T][K], one-row boxes: rows gathered by token (gather_x)
     const int32_t *sorted_ids;
     const float *sorted_weights;
     const int32_t *sorted_expert_ids;
@@ -188,6 +189,8 @@ struct GemmArgs {
     float *dw_out;           // weight gradient (STAGE 5, segment mode): [E][M][N] fp32
     int M;                   // segment mode: rows of the A operand (output rows)
     int pdl_mask;            // launch boundaries with programmatic serialisation (PdlSite bits)
+    int gather_x;            // pair kernel stage 1: token rows gathered from x (tm_xg) by sorted slot
+    int topk;                // k: slot s belongs to token s / k (gather_x)
 };
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,

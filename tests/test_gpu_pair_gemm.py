@@ -187,3 +187,29 @@ def test_finegrained_light_tiles_on_and_off(moe):
                                   cfg.k, toks, expert_major=True)
     check_rows(outs[0][toks], ref, 5e-3, label="fine-grained light tiles")
     check_rows(outs[1][toks], ref, 5e-3, label="fine-grained pair tiles only")
+
+
+@pytest.mark.parametrize("case", [("prefill_like", 1024, 512, 512, 8, 2, "normal"),
+                                  ("light_mix", 1000, 512, 512, 64, 4, "zipf"),
+                                  ("odd_blocks", 700, 384, 256, 6, 3, None)], ids=lambda c: c[0])
+def test_gather_in_gemm_bit_identical(moe, case):
+    """Stage 1 fetching its token rows from x by TMA gather gives exactly the bytes the gather pass
+    would have written, so the layer's output is bit-identical either way (light tiles on and off)."""
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=1.2 if bias == "zipf" else 0.5)
+    inp = synth.make_inputs(cfg, seed=23, device="cuda")
+    outs = {}
+    for light in (0, -1):
+        for gx in (1, 0):
+            layer = moe.FusedMoE(moe.MOE_BF16, T, H, I, E, k,
+                                 options=moe.Options(gemm_pair=1, gather_x=gx, light_tiles=light))
+            out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+            layer(inp["x"], inp, out)
+            torch.cuda.synchronize()
+            assert layer.status() == moe.MOE_OK
+            outs[(light, gx)] = out
+    for light in (0, -1):
+        assert torch.equal(outs[(light, 1)].view(torch.int16), outs[(light, 0)].view(torch.int16)), light
+    host = _host(inp)
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
+    check_rows(outs[(-1, 1)].float().cpu().numpy(), ref, 5e-3, label=f"{name} gathered in the GEMM")
