@@ -330,17 +330,6 @@ typedef struct moe_options {
      * those of the fixed-order router bit for bit; 0: the fixed-order router
      * on CUDA cores for every logit. */
     int tc_router;
-    /* MOE_BF16 grouped mode on CTA pairs (not the training forward): 1:
-     * stage 1 fetches each block's token rows straight from x (TMA
-     * tile::gather4, four rows per copy, row = slot / k), so no gather pass
-     * writes a sorted copy of x; -1 automatic / 0: the gather pass runs
-     * first and stage 1 reads whole 128-row boxes of the sorted copy.  The
-     * two give identical bytes; the automatic choice is the gather pass
-     * because 32 four-row copies per K step issue far slower than one box
-     * (GB300, Mixtral prefill T=4096: stage 1 2.5 ms with the gather pass,
-     * 8.2 ms with gather4).  No effect where the CTA-pair kernel is not
-     * used. */
-    int gather_x;
 } moe_options_t;
 
 /* Set *options to the defaults (gemm_pair -1, one_stage 1, pdl_mask -1, no

@@ -71,7 +71,7 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
 // choice (-1 automatic, 0 never, 1 whenever supported).
 static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
 {
-    if (dtype == MOE_FP8_BLOCK128 || dtype == MOE_MXFP4 || !gemm_pair_supported(E))
+    if (dtype == MOE_MXFP4 || !(dtype == MOE_FP8_BLOCK128 ? gemm_pair_fp8_supported(E) : gemm_pair_supported(E)))
         return false;
     if (gemm_pair >= 0)
         return gemm_pair == 1;
@@ -79,7 +79,7 @@ static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
     const int64_t act = S < E ? S : E;
     if (S < 128 * act)
         return false;
-    return dtype == MOE_BF16 || stage == 2;
+    return dtype == MOE_BF16 || dtype == MOE_FP8_BLOCK128 || stage == 2;
 }
 
 int num_sms_current_device()
@@ -294,7 +294,6 @@ static moe_options_t default_options()
     o.pdl_mask = -1;
     o.light_tiles = -1;
     o.tc_router = -1;
-    o.gather_x = -1;
     return o;
 }
 
@@ -302,7 +301,7 @@ static int check_options(const moe_options_t &o)
 {
     if (o.gemm_pair < -1 || o.gemm_pair > 1 || o.one_stage < 0 || o.one_stage > 1 || o.pdl_mask < -1 ||
         o.pdl_mask > kPdlAll || o.unsatisfiable_h_wait < 0 || o.unsatisfiable_h_wait > 1 || o.light_tiles < -1 ||
-        o.light_tiles > 1 || o.tc_router < -1 || o.tc_router > 1 || o.gather_x < -1 || o.gather_x > 1)
+        o.light_tiles > 1 || o.tc_router < -1 || o.tc_router > 1)
         return MOE_ERR_INVALID_ARG;
     if (o.stage_events)
         for (int i = 0; i < 7; ++i)
@@ -406,15 +405,8 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
     // itself (no gather pass)
     const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && o.one_stage == 1 && !train;
-    // bf16 grouped mode on CTA pairs, on request: stage 1 fetches its token rows from x by TMA
-    // gather4 (no gather pass; the training forward keeps the sorted copy for the weight
-    // gradients).  Not automatic: the 32 four-row copies per K step issue far slower than the one
-    // 128-row box they replace (Mixtral prefill T=4096, stage 1: 2.5 ms -> 8.2 ms; fine-grained
-    // Zipf: 1.85 -> 4.87 ms, against 0.04-0.10 ms for the whole gather pass).
-    const bool pair1 = p.mode == MOE_MODE_GROUPED && dtype == MOE_BF16 && use_pair(dtype, 1, T, k, E, o.gemm_pair);
-    const bool gather_in_gemm = pair1 && !train && o.gather_x == 1;
     cudaError_t ge = cudaSuccess;
-    if (fused || gather_in_gemm) {
+    if (fused) {
         // nothing to gather
     } else if (dtype == MOE_BF16)
         ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
@@ -468,12 +460,6 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         return MOE_ERR_CUDA;
     if (light && !encode_tmap_2d(&g1.tm_x16, at(L.x_sorted), eb, H, P, box_inner, 16))
         return MOE_ERR_CUDA;
-    if (gather_in_gemm) {
-        if (!encode_tmap_2d(&g1.tm_xg, x, eb, H, T, box_inner, 1))  // one-row boxes for tile::gather4
-            return MOE_ERR_CUDA;
-        g1.gather_x = 1;
-        g1.topk = k;
-    }
     g1.K = H;
     g1.N = I;
     g1.rows_per_expert = 2 * I;
@@ -531,7 +517,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             const int64_t ub = p.max_blocks * (I / 64);
             ce = launch_gemm_grouped_mx4(1, g1, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 1, T, k, E, o.gemm_pair)) {
-            ce = launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, (p.max_blocks / 2 + E) * (I / 128), st, light);
+            const int64_t ub = (p.max_blocks / 2 + E) * (I / 128);
+            ce = (dtype == MOE_FP8_BLOCK128) ? launch_gemm_pair_fp8(1, g1, ub, st)
+                                             : launch_gemm_pair(1, dtype == MOE_FP8_TOKEN, g1, ub, st, light);
         } else {
             const int64_t ub = p.max_blocks * (I / 128);
             const int grid = (int)(ub < nsm ? ub : nsm);
@@ -562,7 +550,9 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 2, T, k, E, o.gemm_pair)) {
-            ce = launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, (p.max_blocks / 2 + E) * nt2, st, light);
+            const int64_t ub = (p.max_blocks / 2 + E) * nt2;
+            ce = (dtype == MOE_FP8_BLOCK128) ? launch_gemm_pair_fp8(2, g2, ub, st)
+                                             : launch_gemm_pair(2, dtype == MOE_FP8_TOKEN, g2, ub, st, light);
         } else {
             const int64_t ub = p.max_blocks * nt2;
             const int grid = (int)(ub < nsm ? ub : nsm);

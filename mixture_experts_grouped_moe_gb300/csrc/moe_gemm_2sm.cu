@@ -345,88 +345,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
     auto release = [&](int qs) { mbar_arrive_cluster(cluster_map(&sm.qempty[qs], 0)); };
 
     if (warp == 0) {
-        // ---------------------------------------------------- TMA producer (whole warp)
-        // Lane 0 runs the tile queue and the weight loads.  Token rows come from the sorted
-        // copy of x (tm_x, one box per 128-row block) or, with a.gather_x (stage 1), straight
-        // from x: lane l gathers rows 4l..4l+3 of this CTA's block with one tile::gather4 per K
-        // step (the token of a sorted row is its slot / k; padding rows read token 0 -- a GEMM
-        // output row depends only on its own input row, and padding rows' results are never
-        // stored), so the K step's 32 row quads go out in one warp instruction.
-        const uint64_t pol_w = l2_policy_evict_first();
-        const uint64_t pol_x = l2_policy_evict_last();
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true, any = false;
-        int qs = 0;
-        uint32_t qph = 0;
-        // the leader claims tiles one ahead from the global counter (uneven pair speeds balance out)
-        int claim = (leader && lane == 0) ? atomicAdd(a.tile_counter, 1) : 0;
-        const bool gx = STAGE == 1 && a.gather_x;
-        for (;;) {
-            int t = -1;
-            bool qok = true;
-            if (lane == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true, any = false;
+            int qs = 0;
+            uint32_t qph = 0;
+            // the leader claims tiles one ahead from the global counter (uneven pair speeds balance out)
+            int claim = leader ? atomicAdd(a.tile_counter, 1) : 0;
+            for (;;) {
+                int t;
                 if (leader) {
                     if (!mbar_wait_cluster(&sm.qempty[qs], qph ^ 1, a.status, abort_flag)) {
-                        qok = false;
-                    } else {
-                        t = claim < ntiles ? claim : -1;
-                        *reinterpret_cast<volatile int *>(&sm.qidx[qs]) = t;
-                        st_cluster_s32(cluster_map(&sm.qidx[qs], 1), t);
-                        mbar_arrive(&sm.qfull[qs]);
-                        mbar_arrive_cluster(cluster_map(&sm.qfull[qs], 1));
-                        if (t >= 0)
-                            claim = atomicAdd(a.tile_counter, 1);
+                        ok = false;
+                        break;
                     }
+                    t = claim < ntiles ? claim : -1;
+                    *reinterpret_cast<volatile int *>(&sm.qidx[qs]) = t;
+                    st_cluster_s32(cluster_map(&sm.qidx[qs], 1), t);
+                    mbar_arrive(&sm.qfull[qs]);
+                    mbar_arrive_cluster(cluster_map(&sm.qfull[qs], 1));
+                    if (t >= 0)
+                        claim = atomicAdd(a.tile_counter, 1);
                 } else {
-                    if (!pop(qs, qph, t))
-                        qok = false;
-                    else
-                        release(qs);
+                    if (!pop(qs, qph, t)) {
+                        ok = false;
+                        break;
+                    }
+                    release(qs);
                 }
-            }
-            if (!__shfl_sync(0xffffffffu, (int)qok, 0)) {
-                ok = false;
-                break;
-            }
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (++qs == kTileQ) {
-                qs = 0;
-                qph ^= 1;
-            }
-            if (t < 0)
-                break;
-            const PairTile p = decode<STAGE, LT>(sm, a, t);
-            const int xrow = (rank == 1 && p.second) ? (p.mb0 + 1) * 128 : p.mb0 * 128;
-            const int wrow = rank == 0 ? p.wrow0 : p.wrow1;
-            const int kb0 = STAGE == 5 ? p.kb0 : 0, kb1 = STAGE == 5 ? p.kb1 : nkb;
-            // light tile: this CTA's half of the token rows, and the bytes of both CTAs per stage
-            const int half = p.swap ? p.np / 2 : 0;
-            const int trow = p.mb0 * 128 + (int)rank * half;
-            const uint32_t swap_bytes = 2u * (2 * kHalfBytes + half * 128);
-            // gathered rows of this lane: 4 consecutive sorted rows of this CTA's part of the tile
-            int tok[4] = {0, 0, 0, 0};
-            const int grow = (LT && p.swap ? trow : xrow) + 4 * lane;
-            const bool glane = gx && (LT && p.swap ? 4 * lane < half : true);
-            if (glane) {
-                const int4 sl = *reinterpret_cast<const int4 *>(a.sorted_ids + grow);
-                const int sv[4] = {sl.x, sl.y, sl.z, sl.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tok[q] = sv[q] < a.S ? sv[q] / a.topk : 0;
-            }
-            for (int kb = kb0; kb < kb1; ++kb) {
-                bool wok = true;
-                if (lane == 0)
-                    wok = mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag);
-                if (!__shfl_sync(0xffffffffu, (int)wok, 0)) {
-                    ok = false;
+                if (++qs == kTileQ) {
+                    qs = 0;
+                    qph ^= 1;
+                }
+                if (t < 0)
                     break;
-                }
-                const uint32_t fullc = cluster_map(&sm.full[s], 0);
-                if (LT && p.swap) {
-                    uint8_t *tokp = sm.stage[s] + 2 * kHalfBytes;
-                    if (lane == 0) {
+                const PairTile p = decode<STAGE, LT>(sm, a, t);
+                const int xrow = (rank == 1 && p.second) ? (p.mb0 + 1) * 128 : p.mb0 * 128;
+                const int wrow = rank == 0 ? p.wrow0 : p.wrow1;
+                const int kb0 = STAGE == 5 ? p.kb0 : 0, kb1 = STAGE == 5 ? p.kb1 : nkb;
+                // light tile: this CTA's half of the token rows, and the bytes of both CTAs per stage
+                const int half = p.swap ? p.np / 2 : 0;
+                const uint32_t swap_bytes = 2u * (2 * kHalfBytes + half * 128);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fullc = cluster_map(&sm.full[s], 0);
+                    if (LT && p.swap) {
                         if (leader)
                             mbar_arrive_expect_tx(&sm.full[s], swap_bytes);
                         // weights: rows r*128.. of each of the tile's two 256-row ranges, tokens after them
@@ -434,38 +404,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                                          pol_w);
                         tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, p.wrow1 + (int)rank * 128,
                                          fullc, pol_w);
-                        if (!gx)
-                            for (int c = 0; c < half; c += kSwapRowsPerLoad)
-                                tma_load_2d_pair(tokp + c * 128, &a.tm_x16, kb * kBK<QT>, trow + c, fullc, pol_x);
-                    }
-                    if (glane)
-                        tma_gather4_pair(tokp + 4 * lane * 128, &a.tm_xg, kb * kBK<QT>, tok[0], tok[1], tok[2], tok[3],
-                                         fullc, pol_x);
-                } else {
-                    if (lane == 0) {
+                        uint8_t *tok = sm.stage[s] + 2 * kHalfBytes;
+                        const int trow = p.mb0 * 128 + (int)rank * half;
+                        for (int c = 0; c < half; c += kSwapRowsPerLoad)
+                            tma_load_2d_pair(tok + c * 128, &a.tm_x16, kb * kBK<QT>, trow + c, fullc, pol_x);
+                    } else {
                         if (leader)
                             mbar_arrive_expect_tx(&sm.full[s], 2 * 2 * kHalfBytes);
-                        if (!gx)
-                            tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
+                        tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
                         tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_w);
                     }
-                    if (glane)
-                        tma_gather4_pair(sm.stage[s] + 4 * lane * 128, &a.tm_xg, kb * kBK<QT>, tok[0], tok[1],
-                                         tok[2], tok[3], fullc, pol_x);
+                    any = true;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
-                any = true;
-                if (++s == kStages) {
-                    s = 0;
-                    ph ^= 1;
-                }
+                if (!ok)
+                    break;
             }
-            if (!ok)
-                break;
-        }
-        if (!ok && any && lane == 0) {
-            // copies in flight complete on the leader's barriers: give them a bounded moment to land
-            const unsigned long long t0 = global_timer_ns();
-            while (global_timer_ns() - t0 < 20000000ull) {
+            if (!ok && any) {
+                // copies in flight complete on the leader's barriers: give them a bounded moment to land
+                const unsigned long long t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 20000000ull) {
+                }
             }
         }
     } else if (warp == 1) {

@@ -156,7 +156,6 @@ struct GemmArgs {
     CUtensorMap tm_x;     // token operand rows [P_max][K]
     CUtensorMap tm_w;     // weight operand rows [E*rows_per_expert][K]
     CUtensorMap tm_x16;   // the token operand in 16-row boxes (light-expert pair tiles)
-    CUtensorMap tm_xg;    // the layer input x [T][K], one-row boxes: rows gathered by token (gather_x)
     const int32_t *sorted_ids;
     const float *sorted_weights;
     const int32_t *sorted_expert_ids;
@@ -189,8 +188,6 @@ struct GemmArgs {
     float *dw_out;           // weight gradient (STAGE 5, segment mode): [E][M][N] fp32
     int M;                   // segment mode: rows of the A operand (output rows)
     int pdl_mask;            // launch boundaries with programmatic serialisation (PdlSite bits)
-    int gather_x;            // pair kernel stage 1: token rows gathered from x (tm_xg) by sorted slot
-    int topk;                // k: slot s belongs to token s / k (gather_x)
 };
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
@@ -257,6 +254,9 @@ cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, 
 // at most 64 tokens take swap-AB pair tiles (a.tm_x16: the token operand in
 // 16-row boxes; a.expert_counts required).
 bool gemm_pair_supported(int E);
+// Block-scaled FP8 group GEMM on CTA pairs (grouped mode, stages 1 and 2).
+bool gemm_pair_fp8_supported(int E);
+cudaError_t launch_gemm_pair_fp8(int stage, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st);
 bool gemm_pair_light_supported(int E);  // light-expert tiles: E <= 512
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
                              bool light = false);

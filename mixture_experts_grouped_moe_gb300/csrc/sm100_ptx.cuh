@@ -336,20 +336,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, in
         : "memory");
 }
 
-// TMA gather of four arbitrary rows (r0..r3) of a 2-D tensor map whose box is one row high,
-// starting at inner coordinate x, into this CTA's shared memory as four consecutive 128-byte
-// rows; the bytes complete on an mbarrier of either CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void tma_gather4_pair(void *dst, const void *tmap, int x, int r0, int r1, int r2, int r3,
-                                                 uint32_t bar_cluster, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.cta_group::2"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar_cluster),
-        "l"(policy)
-        : "memory");
-}
-
 // TMEM allocation of the CTA pair (one warp of each CTA, together).
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols)
 {

@@ -54,8 +54,7 @@ class moe_plan_t(ctypes.Structure):
 class moe_options_t(ctypes.Structure):
     _fields_ = [("gemm_pair", ctypes.c_int), ("one_stage", ctypes.c_int), ("pdl_mask", ctypes.c_int),
                 ("stage_events", ctypes.c_void_p), ("h_wait_limit_us", ctypes.c_uint),
-                ("unsatisfiable_h_wait", ctypes.c_int), ("light_tiles", ctypes.c_int), ("tc_router", ctypes.c_int),
-                ("gather_x", ctypes.c_int)]
+                ("unsatisfiable_h_wait", ctypes.c_int), ("light_tiles", ctypes.c_int), ("tc_router", ctypes.c_int)]
 
 
 class moe_ws_layout_t(ctypes.Structure):
@@ -263,8 +262,7 @@ class Options:
 
     Keyword arguments override the library's defaults: gemm_pair (-1/0/1), one_stage (0/1),
     pdl_mask (-1 or a mask), stage_events (7 torch.cuda.Event or None), h_wait_limit_us,
-    unsatisfiable_h_wait (0/1, for the timeout test only), light_tiles (-1/0/1), tc_router (-1/0/1),
-    gather_x (-1/0/1)."""
+    unsatisfiable_h_wait (0/1, for the timeout test only), light_tiles (-1/0/1), tc_router (-1/0/1)."""
 
     def __init__(self, **kw):
         self.c = moe_options_t()

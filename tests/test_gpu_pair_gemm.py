@@ -88,6 +88,67 @@ def test_fp8_token_grouped_both_kernels(moe, case, mode):
     assert rel_l2(got, ref) <= 3e-2
 
 
+def _fp8_block_weights(moe, inp, cfg):
+    E, I, H = cfg.E, cfg.I, cfg.H
+    q1 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    s1 = torch.empty(E * 2 * I // 128, H // 128, dtype=torch.float32, device="cuda")
+    q2 = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(E * H // 128, I // 128, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_weights(inp["W_gate_up"], E * 2 * I, H, q1, s1)
+    moe.moe_quantize_fp8_weights(inp["W_down"], E * H, I, q2, s2)
+    return {"W_router": inp["W_router"], "bias": inp["bias"], "W_gate_up": q1, "w1_scale": s1, "W_down": q2,
+            "w2_scale": s2}
+
+
+def _fp8_block_both(moe, cfg, inp, w):
+    """The block-FP8 layer with the pair kernels and with the one-SM kernels: outputs, the stage-1
+    h codes and their 1x128 scales of the real sorted rows."""
+    res = []
+    for mode in (1, 0):
+        out, layer = _run(moe, cfg, inp, w, moe.MOE_FP8_BLOCK128, mode)
+        P = layer.plan.max_padded
+        npp = int(layer.view("num_tokens_post_padded", torch.int32, (1,)).item())
+        ids = layer.view("sorted_ids", torch.int32, (P,))[:npp]
+        real = (ids < cfg.T * cfg.k).cpu()
+        h = layer.view("inter", torch.uint8, (P, cfg.I))[:npp].cpu()[real]
+        hs = layer.view("inter_scales", torch.float32, (cfg.I // 128, P))[:, :npp].cpu()[:, real]
+        res.append((out, h, hs))
+    return res
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
+def test_fp8_block_pair_bit_identical(moe, case):
+    """Block-FP8 on CTA pairs: each CTA promotes the same per-128 products in the same order as the
+    one-SM kernel, so the h codes, their scales and the output are bit-identical to it (half-used
+    pairs, empty experts, a ragged last stage-2 tile included), and within the FP8 tolerance of the
+    oracle."""
+    name, T, H, I, E, k, bias = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="fp8")
+    inp = synth.make_inputs(cfg, seed=13, device="cuda")
+    w = _fp8_block_weights(moe, inp, cfg)
+    (o_p, h_p, s_p), (o_1, h_1, s_1) = _fp8_block_both(moe, cfg, inp, w)
+    assert torch.equal(h_p, h_1)
+    assert torch.equal(s_p.view(torch.int32), s_1.view(torch.int32))
+    assert np.array_equal(o_p.view(np.uint32), o_1.view(np.uint32))
+    host = _host(inp)
+    q1, s1 = oracle.quant_128x128(host["W_gate_up"])
+    q2, s2 = oracle.quant_128x128(host["W_down"])
+    ref = oracle.moe_forward_fp8(host["x"], host["W_router"], host["bias"], q1, s1, q2, s2, k)
+    assert rel_l2(o_p, ref) <= 3e-2
+
+
+def test_fp8_block_pair_full_size_bit_identical(moe):
+    """Mixtral shapes at T=4096 (block FP8): the pair kernels reproduce the one-SM kernels' h codes,
+    scales and outputs bit for bit on every token."""
+    cfg = synth.CONFIGS["mixtral_fp8"]
+    inp = synth.make_inputs(cfg, seed=0, device="cuda")
+    w = _fp8_block_weights(moe, inp, cfg)
+    (o_p, h_p, s_p), (o_1, h_1, s_1) = _fp8_block_both(moe, cfg, inp, w)
+    assert torch.equal(h_p, h_1)
+    assert torch.equal(s_p.view(torch.int32), s_1.view(torch.int32))
+    assert np.array_equal(o_p.view(np.uint32), o_1.view(np.uint32))
+
+
 def test_prefill_pair_matches_one_sm(moe):
     """Mixtral prefill shapes: both kernels against the oracle on the full-size parity sample (every
     M-block, the least-loaded experts, each expert's last row), and against each other on every token."""
@@ -187,29 +248,3 @@ def test_finegrained_light_tiles_on_and_off(moe):
                                   cfg.k, toks, expert_major=True)
     check_rows(outs[0][toks], ref, 5e-3, label="fine-grained light tiles")
     check_rows(outs[1][toks], ref, 5e-3, label="fine-grained pair tiles only")
-
-
-@pytest.mark.parametrize("case", [("prefill_like", 1024, 512, 512, 8, 2, "normal"),
-                                  ("light_mix", 1000, 512, 512, 64, 4, "zipf"),
-                                  ("odd_blocks", 700, 384, 256, 6, 3, None)], ids=lambda c: c[0])
-def test_gather_in_gemm_bit_identical(moe, case):
-    """Stage 1 fetching its token rows from x by TMA gather gives exactly the bytes the gather pass
-    would have written, so the layer's output is bit-identical either way (light tiles on and off)."""
-    name, T, H, I, E, k, bias = case
-    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=1.2 if bias == "zipf" else 0.5)
-    inp = synth.make_inputs(cfg, seed=23, device="cuda")
-    outs = {}
-    for light in (0, -1):
-        for gx in (1, 0):
-            layer = moe.FusedMoE(moe.MOE_BF16, T, H, I, E, k,
-                                 options=moe.Options(gemm_pair=1, gather_x=gx, light_tiles=light))
-            out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
-            layer(inp["x"], inp, out)
-            torch.cuda.synchronize()
-            assert layer.status() == moe.MOE_OK
-            outs[(light, gx)] = out
-    for light in (0, -1):
-        assert torch.equal(outs[(light, 1)].view(torch.int16), outs[(light, 0)].view(torch.int16)), light
-    host = _host(inp)
-    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k)
-    check_rows(outs[(-1, 1)].float().cpu().numpy(), ref, 5e-3, label=f"{name} gathered in the GEMM")
