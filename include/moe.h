@@ -272,10 +272,12 @@ int moe_quantize_mxfp4(const void *X, int64_t R, int C, uint8_t *q, uint8_t *s, 
  * (No counterpart on the fused-MoE pages: launch choices of this library.)
  */
 typedef struct moe_options {
-    /* Grouped-mode GEMM kernel for MOE_BF16 and MOE_FP8_TOKEN: -1 automatic
-     * (CTA pairs when the average expert holds at least one 128-row token
-     * block, T*k >= 128 * min(E, T*k): in both stages for bf16, in stage 2
-     * for per-token FP8), 0 always the one-SM kernels, 1 CTA pairs (the
+    /* Grouped-mode GEMM kernel for MOE_BF16, MOE_FP8_TOKEN and
+     * MOE_FP8_BLOCK128: -1 automatic (CTA pairs when the average expert
+     * holds at least one 128-row token block, T*k >= 128 * min(E, T*k): in
+     * both stages for bf16, in stage 2 for per-token FP8, never for block
+     * FP8, whose pair kernels are bit-identical to its one-SM kernels but
+     * slower in stage 1), 0 always the one-SM kernels, 1 CTA pairs (the
      * two-SM tensor core) wherever supported. */
     int gemm_pair;
     /* bf16 swap mode (T <= 128): 1 runs both GEMM stages in one persistent

@@ -67,8 +67,11 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
 // T=8192 stage 1 2.45 -> 2.31 and stage 2 1.38 -> 1.16 ms; the fine-grained
 // E=256 workload (2.4 blocks per active expert) is even (4.110 vs 4.123 ms).
 // For per-token FP8 only stage 2 gains (Mixtral shapes, T=4096: stage 2
-// 0.49 -> 0.42 ms, stage 1 0.77 -> 0.83 ms).  gemm_pair: the caller's
-// choice (-1 automatic, 0 never, 1 whenever supported).
+// 0.49 -> 0.42 ms, stage 1 0.77 -> 0.83 ms).  Block-scaled FP8 stays on the
+// one-SM kernels: its pair kernels are bit-identical but their per-K-block
+// promotion round trip crosses the pair (same shapes: stage 1 0.82 -> 1.14
+// ms, stage 2 0.48 -> 0.48 ms).  gemm_pair: the caller's choice (-1
+// automatic, 0 never, 1 whenever supported).
 static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
 {
     if (dtype == MOE_MXFP4 || !(dtype == MOE_FP8_BLOCK128 ? gemm_pair_fp8_supported(E) : gemm_pair_supported(E)))
@@ -77,9 +80,9 @@ static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
         return gemm_pair == 1;
     const int64_t S = (int64_t)T * k;
     const int64_t act = S < E ? S : E;
-    if (S < 128 * act)
+    if (S < 128 * act || dtype == MOE_FP8_BLOCK128)
         return false;
-    return dtype == MOE_BF16 || dtype == MOE_FP8_BLOCK128 || stage == 2;
+    return dtype == MOE_BF16 || stage == 2;
 }
 
 int num_sms_current_device()

@@ -291,6 +291,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier of either CTA of the cluster with the default semantics (release at CTA
+// scope), for a signal that publishes no data the other CTA reads -- "this CTA has finished
+// reading its TMEM buffer" -- and so needs no cluster-scope release, whose fence would first wait
+// for the thread's global loads in flight.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // try_wait with acquire at cluster scope: sees the peer CTA's writes released by its arrive.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
 {
