@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 const int half = p.swap ? p.np / 2 : 0;
                 const uint32_t swap_bytes = 2u * (2 * kHalfBytes + half * 128);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
+                    if (!mbar_wait(&sm.empty[s], ph ^ 1, a.status, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 }
                 if (t < 0)
                     break;
-                if (!mbar_wait_cluster(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
+                if (!mbar_wait(&sm.tempty[acc], aph ^ 1, a.status, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             if (t < 0)
                 break;
             const PairTile p = decode<STAGE, LT>(sm, a, t);
-            bool ok = mbar_wait_cluster(&sm.tfull[acc], aph, a.status, abort_flag);
+            bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive_cluster(cluster_map(&sm.tempty[acc], 0));
+                mbar_arrive_remote(cluster_map(&sm.tempty[acc], 0));
             if (++acc == 2) {
                 acc = 0;
                 aph ^= 1;
