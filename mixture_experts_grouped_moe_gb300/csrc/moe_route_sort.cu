@@ -459,60 +459,86 @@ __global__ void __launch_bounds__(256) router_wnorm_kernel(const __nv_bfloat16 *
 }
 
 // Fixed-order logits (the order of the other router kernels: lane L adds the elements h with
-// (h / 8) mod 32 == L in ascending h, then the butterfly, then the bias) of n <= 8 experts of
+// (h / 8) mod 32 == L in ascending h, then the butterfly, then the bias) of N <= 8 experts of
 // one token, by one warp; every lane returns the values.  Two 256-element rounds are loaded
 // before either is added, so more loads are in flight; each lane's chain still adds its
-// elements in ascending h (round r before round r + 1).
-__device__ __forceinline__ void exact_logits8(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
-                                              int H, const int (&es)[8], int n, int lane, float (&out)[8])
+// elements in ascending h (round r before round r + 1).  The products take the bf16 operands
+// straight from the loaded words (mixed-precision fma: exact product, one rounding, as fmaf on
+// the widened values), so no conversion instructions are spent.
+__device__ __forceinline__ void fma_bf16x2_chain(float &acc, uint32_t xw, uint32_t ww)
 {
-    float acc[8];
+    // elements 2i (low half) then 2i + 1 (high half)
+    asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(xw), "r"(ww));
+}
+
+template <int N>
+__device__ __forceinline__ void exact_logits_acc(const uint4 &xv, const uint4 (&wv)[N], float (&acc)[N])
+{
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < N; ++j) {
+        fma_bf16x2_chain(acc[j], xv.x, wv[j].x);
+        fma_bf16x2_chain(acc[j], xv.y, wv[j].y);
+        fma_bf16x2_chain(acc[j], xv.z, wv[j].z);
+        fma_bf16x2_chain(acc[j], xv.w, wv[j].w);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void exact_logits_n(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
+                                               int H, const int (&es)[8], int lane, float (&out)[8])
+{
+    float acc[N];
+    const __nv_bfloat16 *wp[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
         acc[j] = 0.0f;
+        wp[j] = Wr + (size_t)es[j] * H;
+    }
     for (int h0 = lane * 8; h0 < H; h0 += 512) {
         const bool two = h0 + 256 < H;
         const uint4 xv0 = __ldg(reinterpret_cast<const uint4 *>(xrow + h0));
         const uint4 xv1 = two ? __ldg(reinterpret_cast<const uint4 *>(xrow + h0 + 256)) : make_uint4(0, 0, 0, 0);
-        uint4 wv0[8], wv1[8];
+        uint4 wv0[N], wv1[N];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < n) {
-                const __nv_bfloat16 *wr = Wr + (size_t)es[j] * H + h0;
-                wv0[j] = __ldg(reinterpret_cast<const uint4 *>(wr));
-                wv1[j] = two ? __ldg(reinterpret_cast<const uint4 *>(wr + 256)) : make_uint4(0, 0, 0, 0);
-            }
+        for (int j = 0; j < N; ++j) {
+            wv0[j] = __ldg(reinterpret_cast<const uint4 *>(wp[j] + h0));
+            wv1[j] = two ? __ldg(reinterpret_cast<const uint4 *>(wp[j] + h0 + 256)) : make_uint4(0, 0, 0, 0);
         }
-        float xf[8];
-        bf16x8_to_float(xv0, xf);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < n) {
-                float wf[8];
-                bf16x8_to_float(wv0[j], wf);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    acc[j] = __fmaf_rn(xf[c], wf[c], acc[j]);
-            }
-        if (two) {
-            bf16x8_to_float(xv1, xf);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < n) {
-                    float wf[8];
-                    bf16x8_to_float(wv1[j], wf);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        acc[j] = __fmaf_rn(xf[c], wf[c], acc[j]);
-                }
-        }
+        exact_logits_acc<N>(xv0, wv0, acc);
+        if (two)
+            exact_logits_acc<N>(xv1, wv1, acc);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < N; ++j) {
         float v = butterfly_sum(acc[j]);
-        if (j < n && bias)
+        if (bias)
             v = __fadd_rn(v, bias[es[j]]);
         out[j] = v;
+    }
+#pragma unroll
+    for (int j = N; j < 8; ++j)
+        out[j] = 0.0f;
+}
+
+// exact_logits_n for a run-time count n in 1..8 (out[j] for j >= n is unspecified).
+__device__ __forceinline__ void exact_logits8(const __nv_bfloat16 *xrow, const __nv_bfloat16 *Wr, const float *bias,
+                                              int H, const int (&es)[8], int n, int lane, float (&out)[8])
+{
+    switch (n) {
+    case 1: exact_logits_n<1>(xrow, Wr, bias, H, es, lane, out); break;
+    case 2: exact_logits_n<2>(xrow, Wr, bias, H, es, lane, out); break;
+    case 3: exact_logits_n<3>(xrow, Wr, bias, H, es, lane, out); break;
+    case 4: exact_logits_n<4>(xrow, Wr, bias, H, es, lane, out); break;
+    case 5: exact_logits_n<5>(xrow, Wr, bias, H, es, lane, out); break;
+    case 6: exact_logits_n<6>(xrow, Wr, bias, H, es, lane, out); break;
+    case 7: exact_logits_n<7>(xrow, Wr, bias, H, es, lane, out); break;
+    default: exact_logits_n<8>(xrow, Wr, bias, H, es, lane, out); break;
     }
 }
 
