@@ -394,6 +394,22 @@ class FusedMoE:
                                  self.split_k, out, self.ws, self.ws_bytes, opts, stream)
         return out
 
+    def capture(self, x, w, out, options=None):
+        """A CUDA graph of one forward on these buffers (x, the weights, out and the workspace stay
+        bound to it): graph.replay() reruns the whole layer, every kernel of the call, with one
+        launch from the host -- for shapes where the host's per-call work would outlast the GPU's.
+        The library allocates nothing and never synchronises, so a call is capturable as it is."""
+        import torch
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self(x, w, out, options=options)  # outside the capture: the per-device launch limits are read here
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(graph):
+            self(x, w, out, options=options)
+        return graph
+
     def forward_host(self, x_host, w, out_host, stream=None):
         moe_fused_forward_host(self.dtype, x_host, w["W_router"], w.get("bias"), w["W_gate_up"], w.get("w1_scale"),
                                w["W_down"], w.get("w2_scale"), self.T, self.H, self.I, self.E, self.k,

@@ -100,3 +100,8 @@ def test_summarize_reports_algorithmic_counts():
     d2 = bench.summarize(cfg2, r2, peaks, "measured", 1)
     assert d2["roofline"]["bound"] == "tensor"
     assert d2["roofline"]["alg_flops_per_launch"] == 2.0 * cfg2.S * 2 * cfg2.I * cfg2.H
+    assert d2["roofline"]["peak"] == 1900.0 and d2["roofline"]["peak_source"] == "measured, burst"
+    # a timed region of a second or more is measured against the sustained GEMM peak
+    d3 = bench.summarize(cfg2, dict(r2, timed_ms=1750.0), dict(peaks, bf16_tflops_sustained=1700.0), "measured", 1)
+    assert d3["roofline"]["peak"] == 1700.0 and d3["roofline"]["peak_source"] == "measured, sustained"
+    assert abs(d3["roofline"]["frac"] - d2["roofline"]["frac"] * 1900.0 / 1700.0) < 1e-3
