@@ -347,7 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
+            // Weight tiles of 256 x 256 tiles are read by up to 8 pairs of a group within a few
+            // microseconds; streamed as evict-first they were dropped between those reads while
+            // light tiles streamed their weights through L2 (fine-grained stage 1: 10.97 GB of
+            // DRAM reads per launch against 7.99 GB algorithmic; Mixtral prefill 4.33 GB against
+            // 2.5).  Kept as evict-last they are read about once (9.5 and 2.96 GB; fine-grained
+            // 3.39 -> 3.24 ms, prefill stage 1 2.48 -> 2.42 ms, same box).  Light tiles read their
+            // weights once: evict-first.
             const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_wh = l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
             int s = 0;
             uint32_t ph = 0;
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                         if (leader)
                             mbar_arrive_expect_tx(&sm.full[s], 2 * 2 * kHalfBytes);
                         tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
-                        tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_w);
+                        tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_wh);
                     }
                     any = true;
                     if (++s == kStages) {

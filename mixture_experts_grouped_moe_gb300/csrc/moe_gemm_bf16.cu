@@ -231,7 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
+            // grouped mode reuses a weight tile across a raster group of blocks: evict-normal;
+            // swap mode reads every weight byte once: evict-first
+            const uint64_t pol_w = MODE == MOE_MODE_GROUPED ? l2_policy_evict_normal() : l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             int s = 0;
             uint32_t ph = 0;

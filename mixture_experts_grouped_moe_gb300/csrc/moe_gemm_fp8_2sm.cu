@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_pair_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_w = l2_policy_evict_last();  // reused by the group's pairs
             const uint64_t pol_x = l2_policy_evict_last();
             int s = 0;
             uint32_t ph = 0;

@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
 
     if (warp == 0) {
         // ------------------------------------------ producer (whole warp)
-        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_w = l2_policy_evict_normal();  // reused across a raster group of blocks
         const uint64_t pol_x = l2_policy_evict_last();
         int s = 0;
         uint32_t ph = 0;
