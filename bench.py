@@ -333,7 +333,7 @@ def summarize(cfg, r, peaks, peak_kind, world):
     sustained = r.get("timed_ms", 0.0) >= 1000.0
     peak_t = (peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) if sustained
               else peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    peak_kind = f"{peak_kind}, {'sustained' if sustained else 'burst'}"
+    tensor_kind = f"{peak_kind}, {'sustained' if sustained else 'burst'}"
     if eb == 1:
         peak_t = peaks.get("fp8_tflops", 2.0 * peak_t)  # nominal dense FP8 / bf16 ratio
     elif eb == 0.5:
@@ -365,7 +365,8 @@ def summarize(cfg, r, peaks, peak_kind, world):
         achieved = k_flops / (kms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak_t, 4), "alg_flops_per_launch": k_flops}
-    roof.update(kernel=kname, impl_bytes_per_launch=impl, peak_source=peak_kind, kernel_ms=round(kms, 5),
+    roof.update(kernel=kname, impl_bytes_per_launch=impl, peak_source=peak_kind if mem_bound else tensor_kind,
+                kernel_ms=round(kms, 5),
                 traffic=profiled_traffic(cfg.name, "one_kernel" if r["one_stage"] else "stage1"))
     return {
         "value": round(whole_job_throughput(world, T, ms), 2), "unit": "tokens/s", "ms_per_step": round(ms, 5),
