@@ -27,7 +27,7 @@
  *    allocation, no exceptions; results are ready when the stream is.
  *  - The caller owns every buffer.  The library keeps no mutable state
  *    that changes what a call computes or launches: only per-device
- *    constants (SM count, the no-allocation sort's scratch address).  Every
+ *    constants (SM count, how many CTA-pair clusters fit).  Every
  *    choice a caller can make travels in the call's own arguments
  *    (block_m, split_k, and moe_options_t for moe_fused_forward_ex); the
  *    library reads no environment variables.

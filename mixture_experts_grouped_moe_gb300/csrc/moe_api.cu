@@ -6,6 +6,7 @@
 //   stage-2 group GEMM -> combine
 // on the caller's stream.  Nothing here allocates device memory or
 // synchronises (except moe_workspace_status, which reads one word back).
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -87,17 +88,17 @@ static bool use_pair(int dtype, int stage, int T, int k, int E, int gemm_pair)
 
 int num_sms_current_device()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // per device, zero until first computed
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 0;
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 // Workspace carve-up (byte offsets from ws).

@@ -48,6 +48,7 @@
 // light tile would need 40 KB stages, of which only five fit).  The epilogue holds one feature per
 // thread and a token per accumulator column.  Heavy and light experts' tiles are claimed from the same counter,
 // so tensor-bound and weight-streaming tiles run side by side.
+#include <atomic>
 #include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
@@ -747,11 +748,11 @@ cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 template <int STAGE, int QT, int LT>
 int max_clusters()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // per device, zero until first computed
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 0;
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         auto kern = gemm_pair_kernel<STAGE, QT, LT>;
         constexpr size_t smem = kSmemBytesT<STAGE, LT>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -770,9 +771,9 @@ int max_clusters()
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
             return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 }  // namespace gemm2sm

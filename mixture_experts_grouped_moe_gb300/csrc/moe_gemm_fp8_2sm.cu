@@ -49,6 +49,7 @@
 //               256 columns; they release a TMEM buffer on the leader's barrier
 // Every wait is bounded; a CTA that gives up raises the status word, and both
 // CTAs still meet at the final cluster barrier.
+#include <atomic>
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -615,11 +616,11 @@ cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 template <int STAGE>
 int max_clusters()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // per device, zero until first computed
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 0;
-    if (cache[dev] == 0) {
+    if (cache[dev].load(std::memory_order_relaxed) == 0) {
         auto kern = gemm_fp8_pair_kernel<STAGE>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
             return 0;
@@ -637,9 +638,9 @@ int max_clusters()
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
             return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cache[dev].load(std::memory_order_relaxed);
 }
 
 }  // namespace fp8pair
