@@ -420,9 +420,12 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
                                static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
                                pdl_site(pdl, kPdlGather), st);
     else if (dtype == MOE_MXFP4)
+        // grouped mode keeps the token scales in the tensor core's 128 x 4 blocked order (two 16-byte
+        // copies per lane and K step in the GEMM's producer instead of eight 4-byte ones: Mixtral
+        // shapes at T=4096, stage 1 0.921 -> 0.852 ms); swap mode re-tiles its few rows itself
         ge = launch_quant_mx4(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
-                              static_cast<uint8_t *>(at(L.x_sorted)), static_cast<uint8_t *>(at(L.x_scales)), false,
-                              pdl_site(pdl, kPdlGather), st);
+                              static_cast<uint8_t *>(at(L.x_sorted)), static_cast<uint8_t *>(at(L.x_scales)),
+                              p.mode == MOE_MODE_GROUPED, pdl_site(pdl, kPdlGather), st);
     else
         ge = launch_gather_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S,
                                       k, H, P, static_cast<uint8_t *>(at(L.x_sorted)),

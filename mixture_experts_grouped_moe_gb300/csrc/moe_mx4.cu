@@ -630,7 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
     pdl_trigger();
     const int ntiles = (*a.num_post_padded / 128) * nnt_of<STAGE>(a);
     const int nkb = a.K / 256;
-    const int kgroups = a.K / 32;
     const int ktiles = a.K / 128;
 
     if (warp == 0) {
@@ -683,11 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                 // A scales: token rows l + 32 w of the block, 8 bytes each (two K tiles of 4 groups);
                 // B scales: rows 0-63 from wrow0's tile, 64-127 from wrow1's (words of a 64-row half).
                 // Asynchronous copies that complete on the stage barrier.
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint8_t *src = xsf_g + (size_t)(xrow + lane + 32 * w) * kgroups + kb * 8;
-                    cp_async_4(asf + lane * 16 + w * 4, src);
-                    cp_async_4(asf + 512 + lane * 16 + w * 4, src + 4);
+                {
+                    // the block's scales of K tiles 2kb and 2kb + 1 are two consecutive 512-byte tiles
+                    // of the blocked order: two 16-byte copies per lane
+                    const uint8_t *src = xsf_g + ((size_t)(xrow >> 7) * ktiles + 2 * kb) * 512 + lane * 32;
+                    cp_async_16_zfill(asf + lane * 32, src, true);
+                    cp_async_16_zfill(asf + lane * 32 + 16, src + 16, true);
                 }
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
@@ -812,7 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
             const int pos = g.mb * 128 + row;
             if (STAGE == 1) {
                 uint8_t *hq = static_cast<uint8_t *>(a.inter) + (size_t)pos * (a.N / 2) + g.ncol0 / 2;
-                uint8_t *hs = reinterpret_cast<uint8_t *>(a.inter_scales) + (size_t)pos * (a.N / 32) + g.ncol0 / 32;
+                // h's scales in the tensor core's 128 x 4 blocked order, as stage 2's producer copies them
+                uint8_t *hs = reinterpret_cast<uint8_t *>(a.inter_scales);
 #pragma unroll 1
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float gv[32], uv[32], h[32];
@@ -835,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                             w[b] |= e2m1_code(h[8 * b + i] * inv) << (4 * i);
                     }
                     *reinterpret_cast<uint4 *>(hq + c0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
-                    hs[c0 / 32] = (uint8_t)(e + 127);
+                    hs[tiled_sf_offset(pos, (g.ncol0 + c0) / 32, a.N)] = (uint8_t)(e + 127);
                 }
             } else {
                 const int slot = a.sorted_ids[pos];

@@ -105,6 +105,15 @@ def run_fused(moe, cfg, inp, w4, block_m=0, split_k=0):
     return out, layer
 
 
+def untile_scales(tiled, R, C):
+    """Row-major [R][C/32] E8M0 bytes from the 128 x 4 blocked order of 128-row x 128-column tiles
+    ([R/128][C/128][512]; row r, group g at byte (r % 32) * 16 + (r % 128 // 32) * 4 + g % 4)."""
+    r = np.arange(R)[:, None]
+    g = np.arange(C // 32)[None, :]
+    off = ((r // 128) * (C // 128) + g // 4) * 512 + (r % 32) * 16 + (r % 128 // 32) * 4 + g % 4
+    return np.asarray(tiled)[off]
+
+
 def _check_workspace(moe, layer, cfg, host):
     T, k, E = cfg.T, cfg.k, cfg.E
     r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], k)
@@ -118,7 +127,13 @@ def _check_workspace(moe, layer, cfg, host):
     xrows = np.where((s_ids < S)[:, None], host["x"][np.minimum(s_ids, S - 1) // k], np.uint16(0))
     rq, rs = oracle.quant_mx4(xrows)
     xq = layer.view("x_sorted", torch.uint8, (P, cfg.H // 2)).cpu().numpy()[:npp]
-    xs = layer.view("x_scales", torch.uint8, (P, cfg.H // 32)).cpu().numpy()[:npp]
+    xs = layer.view("x_scales", torch.uint8, (P * cfg.H // 32,)).cpu().numpy()
+    if layer.plan.mode == moe.MOE_MODE_GROUPED:
+        # grouped mode keeps them in the tensor core's blocked order (npp: whole 128-row blocks)
+        assert npp % 128 == 0
+        xs = untile_scales(xs, npp, cfg.H)
+    else:
+        xs = xs.reshape(P, cfg.H // 32)[:npp]
     assert np.array_equal(unpack(xq), rq) and np.array_equal(xs, rs)
 
 
