@@ -248,3 +248,30 @@ def test_finegrained_light_tiles_on_and_off(moe):
                                   cfg.k, toks, expert_major=True)
     check_rows(outs[0][toks], ref, 5e-3, label="fine-grained light tiles")
     check_rows(outs[1][toks], ref, 5e-3, label="fine-grained pair tiles only")
+
+
+@pytest.mark.parametrize("case", [("e512_light_limit", 2048, 256, 256, 512, 8, "zipf", 1),
+                                  ("e1024_pair_limit", 2048, 256, 256, 1024, 8, "zipf", -1)],
+                         ids=lambda c: c[0])
+def test_many_experts_at_the_table_limits(moe, case):
+    """The largest expert counts of the per-expert tables: 512 with light-expert tiles (their limit),
+    1024 on plain pair tiles (the pair kernel's and the router's limit; light tiles are not
+    supported there, so the automatic choice leaves them off).  The tensor-core router, the
+    chunked sort and the pair kernels' tile tables at full size, against the oracle."""
+    name, T, H, I, E, k, bias, light = case
+    cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=1.2)
+    inp = synth.make_inputs(cfg, seed=31, device="cuda")
+    host = _host(inp)
+    layer = moe.FusedMoE(moe.MOE_BF16, T, H, I, E, k, options=moe.Options(gemm_pair=1, light_tiles=light))
+    assert layer.plan.mode == moe.MOE_MODE_GROUPED
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    layer(inp["x"], inp, out)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.MOE_OK
+    r_ids, _, _ = oracle.route(host["x"], host["W_router"], host["bias"], k)
+    assert np.array_equal(layer.view("topk_ids", torch.int32, (T, k)).cpu().numpy(), r_ids)
+    counts = layer.view("expert_counts", torch.int32, (E,)).cpu().numpy()
+    assert (counts == 0).any() and (counts > 128).any()   # empty, light and multi-block experts
+    ref = oracle.moe_forward_bf16(host["x"], host["W_router"], host["bias"], host["W_gate_up"], host["W_down"], k,
+                                  expert_major=True)
+    check_rows(out.float().cpu().numpy(), ref, 5e-3, label=name)
