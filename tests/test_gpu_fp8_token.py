@@ -130,6 +130,7 @@ EDGE = [
     ("grouped_t129", 129, 256, 256, 4, 2, None, 0, 0),
     ("grouped_ragged", 257, 384, 256, 6, 3, "normal", 0, 0),
     ("grouped_h_odd", 200, 640, 384, 8, 2, "normal", 0, 0),
+    ("grouped_many_experts", 1024, 256, 256, 128, 4, "zipf", 0, 0),
 ]
 
 

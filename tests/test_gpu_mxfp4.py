@@ -193,6 +193,7 @@ GROUPED = [
     ("e1k1_t200", 200, 256, 512, 1, 1, None),
     ("h_odd", 150, 768, 256, 5, 2, "normal"),
     ("many_experts", 500, 256, 256, 40, 4, "normal"),
+    ("e128_zipf", 1024, 256, 256, 128, 4, "zipf"),
 ]
 
 

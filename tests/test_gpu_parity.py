@@ -343,7 +343,8 @@ def test_fused_bf16_edge_cases(moe, case):
 
 
 @pytest.mark.parametrize("case", [("fp8_small", 40, 256, 384, 4, 2, None), ("fp8_ragged", 257, 384, 256, 6, 3, "normal"),
-                                  ("fp8_t1", 1, 128, 256, 4, 2, None)], ids=lambda c: c[0])
+                                  ("fp8_t1", 1, 128, 256, 4, 2, None),
+                                  ("fp8_many_experts", 1024, 256, 256, 128, 4, "zipf")], ids=lambda c: c[0])
 def test_fused_fp8_edge_cases(moe, case):
     name, T, H, I, E, k, bias = case
     cfg = synth.MoEConfig(name, T=T, H=H, I=I, E=E, k=k, bias=bias, bias_param=0.5, dtype="fp8")
