@@ -681,10 +681,14 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     b.rg_part = static_cast<float *>(at(TL.rg_part));
     if (launch_backward_aux(0, b, st) != cudaSuccess || launch_backward_aux(1, b, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    // weights transposed so that both backward GEMMs read K-major rows
-    if (launch_transpose(static_cast<const __nv_bfloat16 *>(W_down), bf(TL.wdT), E, H, I, H, st) != cudaSuccess ||
-        launch_transpose(static_cast<const __nv_bfloat16 *>(W_gate_up), bf(TL.wguT), E, 2 * I, H, 2 * I, st) !=
-            cudaSuccess)
+    // CTA pairs under the same rule as the forward's GEMMs.  The pair kernels read the weights of
+    // both backward GEMMs in their stored layout as MN-major operands; the one-SM kernels read
+    // K-major rows, from transposed copies.
+    const bool pairs = use_pair(MOE_BF16, 1, T, k, E, o.gemm_pair);
+    if (!pairs &&
+        (launch_transpose(static_cast<const __nv_bfloat16 *>(W_down), bf(TL.wdT), E, H, I, H, st) != cudaSuccess ||
+         launch_transpose(static_cast<const __nv_bfloat16 *>(W_gate_up), bf(TL.wguT), E, 2 * I, H, 2 * I, st) !=
+             cudaSuccess))
         return MOE_ERR_CUDA;
 
     GemmArgs g;
@@ -705,7 +709,8 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     // dh = dY W_down, with SwiGLU's backward in the epilogue -> dg | du
     GemmArgs g3 = g;
     if (!encode_tmap_2d(&g3.tm_x, at(TL.dys), 2, H, P, 64, 128) ||
-        !encode_tmap_2d(&g3.tm_w, at(TL.wdT), 2, H, (uint64_t)E * I, 64, 128))
+        !(pairs ? encode_tmap_2d(&g3.tm_w, W_down, 2, I, (uint64_t)E * H, 64, 64)  // [E*H][I]: K rows, N columns
+                : encode_tmap_2d(&g3.tm_w, at(TL.wdT), 2, H, (uint64_t)E * I, 64, 128)))
         return MOE_ERR_CUDA;
     g3.K = H;
     g3.N = I;
@@ -715,17 +720,16 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     g3.tile_counter = status + 1;
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    // CTA pairs under the same rule as the forward's GEMMs
-    const bool pairs = use_pair(MOE_BF16, 1, T, k, E, o.gemm_pair);
     int64_t ub = p.max_blocks * (I / 256);
-    if ((pairs ? launch_gemm_pair(3, 0, g3, (p.max_blocks / 2 + E) * (I / 256), st)
+    if ((pairs ? launch_gemm_pair(3, 0, g3, (p.max_blocks / 2 + E) * (I / 256), st, false, true)
                : launch_gemm_backward_bf16(3, g3, (int)(ub < nsm ? ub : nsm), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     // dx per slot = dg W_gate + du W_up (stage 2's tile shape, unit weights)
     GemmArgs g2 = g;
     if (!encode_tmap_2d(&g2.tm_x, at(TL.dgu), 2, 2 * I, P, 64, 128) ||
-        !encode_tmap_2d(&g2.tm_w, at(TL.wguT), 2, 2 * I, (uint64_t)E * H, 64, 128))
+        !(pairs ? encode_tmap_2d(&g2.tm_w, W_gate_up, 2, H, (uint64_t)E * 2 * I, 64, 64)  // [E*2I][H]
+                : encode_tmap_2d(&g2.tm_w, at(TL.wguT), 2, 2 * I, (uint64_t)E * H, 64, 128)))
         return MOE_ERR_CUDA;
     g2.K = 2 * I;
     g2.N = H;
@@ -736,30 +740,38 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     ub = p.max_blocks * ((H + 255) / 256);
-    if ((pairs ? launch_gemm_pair(2, 0, g2, (p.max_blocks / 2 + E) * ((H + 255) / 256), st)
+    if ((pairs ? launch_gemm_pair(2, 0, g2, (p.max_blocks / 2 + E) * ((H + 255) / 256), st, false, true)
                : launch_gemm_backward_bf16(2, g2, (int)(ub < nsm ? ub : nsm), st)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_backward_aux(2, b, st) != cudaSuccess)
         return MOE_ERR_CUDA;
 
-    // weight gradients: activations transposed to [rows][P] so K runs over each expert's positions
+    // weight gradients, K over each expert's token positions: on CTA pairs (gradient rows a multiple
+    // of 256) both activations are read as stored, [P][rows], as MN-major operands; the one-SM
+    // kernel reads K-major rows of transposed copies [rows][P]
     const int64_t Pp = TL.Pp;
-    if (launch_transpose(bf(TL.dys), bf(TL.dysT), 1, P, H, Pp, st) != cudaSuccess ||
-        launch_transpose(bf(L.inter), bf(TL.hT), 1, P, I, Pp, st) != cudaSuccess ||
-        launch_transpose(bf(TL.dgu), bf(TL.dguT), 1, P, 2 * I, Pp, st) != cudaSuccess ||
-        launch_transpose(bf(L.x_sorted), bf(TL.xsT), 1, P, H, Pp, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
     struct WG {
-        int64_t a_off, b_off;
+        int64_t a_src, b_src, a_off, b_off;
         int M, N;
         float *out;
-    } wg[2] = {{TL.dysT, TL.hT, H, I, dW_down}, {TL.dguT, TL.xsT, 2 * I, H, dW_gate_up}};
+    } wg[2] = {{TL.dys, L.inter, TL.dysT, TL.hT, H, I, dW_down}, {TL.dgu, L.x_sorted, TL.dguT, TL.xsT, 2 * I, H, dW_gate_up}};
     for (const WG &q : wg) {
+        const bool pair5 = pairs && q.M % 256 == 0;  // pair tiles span 256 gradient rows
         GemmArgs g5 = g;
-        if (!encode_tmap_2d(&g5.tm_x, at(q.a_off), 2, Pp, q.M, 64, 128) ||
-            !encode_tmap_2d(&g5.tm_w, at(q.b_off), 2, Pp, q.N, 64, 128))
-            return MOE_ERR_CUDA;
-        g5.K = (int)Pp;
+        if (pair5) {
+            if (!encode_tmap_2d(&g5.tm_x, at(q.a_src), 2, q.M, P, 64, 64) ||
+                !encode_tmap_2d(&g5.tm_w, at(q.b_src), 2, q.N, P, 64, 64))
+                return MOE_ERR_CUDA;
+            g5.K = (int)P;
+        } else {
+            if (launch_transpose(bf(q.a_src), bf(q.a_off), 1, P, q.M, Pp, st) != cudaSuccess ||
+                launch_transpose(bf(q.b_src), bf(q.b_off), 1, P, q.N, Pp, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            if (!encode_tmap_2d(&g5.tm_x, at(q.a_off), 2, Pp, q.M, 64, 128) ||
+                !encode_tmap_2d(&g5.tm_w, at(q.b_off), 2, Pp, q.N, 64, 128))
+                return MOE_ERR_CUDA;
+            g5.K = (int)Pp;
+        }
         g5.M = q.M;
         g5.N = q.N;
         g5.dw_out = q.out;
@@ -767,8 +779,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
         if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
             return MOE_ERR_CUDA;
         const int64_t tiles = (int64_t)E * (q.M / 128) * ((q.N + 255) / 256);
-        const bool pair5 = pairs && q.M % 256 == 0;  // pair tiles span 256 gradient rows
-        if ((pair5 ? launch_gemm_pair(5, 0, g5, tiles / 2, st)
+        if ((pair5 ? launch_gemm_pair(5, 0, g5, tiles / 2, st, false, true)
                    : launch_gemm_backward_bf16(5, g5, (int)(tiles < nsm ? tiles : nsm), st)) != cudaSuccess)
             return MOE_ERR_CUDA;
     }

@@ -236,10 +236,15 @@ __device__ __forceinline__ PairTile decode(const SM &sm, const GemmArgs &a, int 
     return p;
 }
 
-template <int STAGE, int QT, int LT>
+// BT = 1 (the backward, bf16): operands read in their stored [K][N] layout (64 x 64 boxes) as
+// MN-major operands, so nothing needs a transposed copy -- stages 2 and 3 (dgrad): the weights
+// (a.tm_w over [E*K][N]); stage 5 (weight gradients, K = an expert's token positions): both
+// activations (a.tm_x over [P][M], a.tm_w over [P][N]).
+template <int STAGE, int QT, int LT, int BT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmArgs a)
 {
     static_assert(!LT || ((STAGE == 1 || STAGE == 2) && QT == 0), "light-expert tiles: bf16 stages 1 and 2");
+    static_assert(!BT || ((STAGE == 2 || STAGE == 3 || STAGE == 5) && QT == 0 && !LT), "MN-major: backward stages");
     using SmemT = Smem<STAGE, LT>;
     constexpr int kStages = SmemT::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -420,8 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                     } else {
                         if (leader)
                             mbar_arrive_expect_tx(&sm.full[s], 2 * 2 * kHalfBytes);
-                        tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
-                        tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_wh);
+                        if (BT && STAGE == 5) {
+                            // A: this CTA's 128 gradient rows (columns of [P][M]) at token rows kb*64..
+                            tma_load_2d_pair(sm.stage[s], &a.tm_x, xrow, kb * 64, fullc, pol_x);
+                            tma_load_2d_pair(sm.stage[s] + kHalfBytes / 2, &a.tm_x, xrow + 64, kb * 64, fullc,
+                                             pol_x);
+                        } else {
+                            tma_load_2d_pair(sm.stage[s], &a.tm_x, kb * kBK<QT>, xrow, fullc, pol_x);
+                        }
+                        if (BT) {
+                            // this CTA's 128 of the tile's 256 N columns at K rows kb*64..: two 64 x 64
+                            // boxes, 8 KB apart (weights: expert e's rows of [E*K][N])
+                            const int n0 = STAGE == 5 ? wrow : p.ncol0 + (int)rank * 128;
+                            const int k0 = (STAGE == 5 ? 0 : p.e * a.K) + kb * 64;
+                            tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, n0, k0, fullc, pol_wh);
+                            tma_load_2d_pair(sm.stage[s] + kHalfBytes + kHalfBytes / 2, &a.tm_w, n0 + 64, k0, fullc,
+                                             pol_wh);
+                        } else {
+                            tma_load_2d_pair(sm.stage[s] + kHalfBytes, &a.tm_w, kb * kBK<QT>, wrow, fullc, pol_wh);
+                        }
                     }
                     any = true;
                     if (++s == kStages) {
@@ -447,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true, any = false;
-            const uint32_t idesc = make_idesc(QT ? 0u : 1u, QT ? 0u : 1u, 256, 256);
+            const uint32_t idesc = BT ? (make_idesc_bmn(1, 1, 256, 256) | (STAGE == 5 ? 1u << 15 : 0u))  // A MN-major too
+                                      : make_idesc(QT ? 0u : 1u, QT ? 0u : 1u, 256, 256);
             int qs = 0;
             uint32_t qph = 0;
             for (;;) {
@@ -504,9 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                         const uint8_t *xa = sm.stage[s];
                         const uint8_t *wb = sm.stage[s] + kHalfBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_pair<QT>(d, smem_desc_sw128(xa + kk * 32), smem_desc_sw128(wb + kk * 32), idesc,
-                                         (kb > kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // B: K-major 32 bytes further per 16 K, or MN-major 16 rows (2 KB) further
+                            const uint64_t bdesc = BT ? smem_desc_sw128_mn(wb + kk * 2048, kHalfBytes / 2)
+                                                      : smem_desc_sw128(wb + kk * 32);
+                            const uint64_t adesc = (BT && STAGE == 5) ? smem_desc_sw128_mn(xa + kk * 2048, kHalfBytes / 2)
+                                                                      : smem_desc_sw128(xa + kk * 32);
+                            mma_pair<QT>(d, adesc, bdesc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     any = true;
                     mma_commit_pair(&sm.empty[s], 0x3);
@@ -721,10 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
         tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-template <int STAGE, int QT, int LT>
+template <int STAGE, int QT, int LT, int BT = 0>
 cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 {
-    auto kern = gemm_pair_kernel<STAGE, QT, LT>;
+    auto kern = gemm_pair_kernel<STAGE, QT, LT, BT>;
     constexpr size_t smem = kSmemBytesT<STAGE, LT>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
@@ -745,7 +773,7 @@ cudaError_t launch(const GemmArgs &a, int clusters, cudaStream_t st)
 }
 
 // Clusters of two that can be resident at once (one CTA per SM), cached per device.
-template <int STAGE, int QT, int LT>
+template <int STAGE, int QT, int LT, int BT = 0>
 int max_clusters()
 {
     static std::atomic<int> cache[64];  // per device, zero until first computed
@@ -753,7 +781,7 @@ int max_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 0;
     if (cache[dev].load(std::memory_order_relaxed) == 0) {
-        auto kern = gemm_pair_kernel<STAGE, QT, LT>;
+        auto kern = gemm_pair_kernel<STAGE, QT, LT, BT>;
         constexpr size_t smem = kSmemBytesT<STAGE, LT>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return 0;
@@ -782,13 +810,15 @@ bool gemm_pair_supported(int E) { return E <= gemm2sm::kMaxE; }
 bool gemm_pair_light_supported(int E) { return E <= gemm2sm::kMaxELight; }
 
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
-                             bool light)
+                             bool light, bool w_mn_major)
 {
     // stages 1, 2 (bf16 or per-token FP8; bf16 optionally with light-expert tiles); 3 and 5
     // (training, bf16): the backward of stage 2 and the weight gradients
     if (light && (qt || (stage != 1 && stage != 2)))
         return cudaErrorInvalidValue;
-    const int key = stage * 4 + (qt ? 1 : 0) + (light ? 2 : 0);
+    if (w_mn_major && (qt || light || (stage != 2 && stage != 3 && stage != 5)))
+        return cudaErrorInvalidValue;
+    const int key = stage * 4 + (qt ? 1 : 0) + (light ? 2 : 0) + (w_mn_major ? 64 : 0);
     int ncl = 0;
     switch (key) {
     case 4: ncl = gemm2sm::max_clusters<1, 0, 0>(); break;
@@ -798,6 +828,9 @@ cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_p
     case 9: ncl = gemm2sm::max_clusters<2, 1, 0>(); break;
     case 10: ncl = gemm2sm::max_clusters<2, 0, 1>(); break;
     case 12: ncl = gemm2sm::max_clusters<3, 0, 0>(); break;
+    case 72: ncl = gemm2sm::max_clusters<2, 0, 0, 1>(); break;
+    case 76: ncl = gemm2sm::max_clusters<3, 0, 0, 1>(); break;
+    case 84: ncl = gemm2sm::max_clusters<5, 0, 0, 1>(); break;
     case 20: ncl = gemm2sm::max_clusters<5, 0, 0>(); break;
     default: return cudaErrorInvalidValue;
     }
@@ -813,6 +846,9 @@ cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_p
     case 9: return gemm2sm::launch<2, 1, 0>(a, ncl, st);
     case 10: return gemm2sm::launch<2, 0, 1>(a, ncl, st);
     case 12: return gemm2sm::launch<3, 0, 0>(a, ncl, st);
+    case 72: return gemm2sm::launch<2, 0, 0, 1>(a, ncl, st);
+    case 76: return gemm2sm::launch<3, 0, 0, 1>(a, ncl, st);
+    case 84: return gemm2sm::launch<5, 0, 0, 1>(a, ncl, st);
     default: return gemm2sm::launch<5, 0, 0>(a, ncl, st);
     }
 }

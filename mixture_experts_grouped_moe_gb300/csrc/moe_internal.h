@@ -258,8 +258,10 @@ bool gemm_pair_supported(int E);
 bool gemm_pair_fp8_supported(int E);
 cudaError_t launch_gemm_pair_fp8(int stage, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st);
 bool gemm_pair_light_supported(int E);  // light-expert tiles: E <= 512
+// w_mn_major (bf16 stages 2 and 3, the backward's dgrad GEMMs): a.tm_w covers the weights in their
+// stored [E*K][N] layout with 64 x 64 boxes, read as an MN-major operand (no transposed copy).
 cudaError_t launch_gemm_pair(int stage, int qt, const GemmArgs &a, int64_t max_pair_tiles, cudaStream_t st,
-                             bool light = false);
+                             bool light = false, bool w_mn_major = false);
 cudaError_t launch_gemm_swap_fp8_token(int stage, const GemmArgs &a, int grid, cudaStream_t st);
 
 }  // namespace moe

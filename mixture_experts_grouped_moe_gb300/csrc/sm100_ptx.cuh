@@ -477,6 +477,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void *base)
     return d;
 }
 
+// Shared-memory descriptor of an MN-major operand in 128-byte swizzle: 64 consecutive N (or M)
+// elements of one K index per 128-byte row, 8 K rows per 1024-byte atom (stride byte offset
+// between the K groups of 8), atoms of 64 N elements `lbo` bytes apart (leading byte offset) --
+// the layout of 64 x 64 TMA boxes loaded from a [K][N] row-major matrix, one box per 64 N.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(const void *base, uint32_t lbo)
+{
+    uint64_t addr = smem_addr(base);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;               // start address (16-byte units)
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;  // leading byte offset: next 64 elements of N
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8 rows of K
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor: dense, fp32 accumulator, both operands K-major.
 // a_fmt / b_fmt: kind::f16 -> 1 = bf16; kind::f8f6f4 -> 0 = e4m3.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N)
@@ -486,6 +502,12 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
            | (b_fmt << 10)      // B format
            | ((N >> 3) << 17)   // N / 8
            | ((M >> 4) << 24);  // M / 16
+}
+
+// The same with B MN-major (bit 16: B is read as [K][N], N contiguous).
+__host__ __device__ constexpr uint32_t make_idesc_bmn(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N)
+{
+    return make_idesc(a_fmt, b_fmt, M, N) | (1u << 16);
 }
 
 // ---------------------------------------------- block-scaled FP4 (MXFP4)
