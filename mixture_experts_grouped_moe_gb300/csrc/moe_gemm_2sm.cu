@@ -173,8 +173,12 @@ __device__ __forceinline__ PairTile decode(const SM &sm, const GemmArgs &a, int 
         p.swap = p.cnt = p.np = 0;
         p.e = t / (nmp * nnt);
         const int rem = t - p.e * nmp * nnt;
-        const int nt = rem / nmp;
-        p.mb0 = 2 * (rem % nmp);
+        // consecutive tiles share the larger operand's rows, so that the smaller one is what each
+        // tile re-reads (from L2): the W_gate_up gradient (M = 2I rows of dg | du against N = H
+        // of x) walked its 112 row pairs per N tile and read 13.5 GB of DRAM per launch
+        const bool m_outer = a.M > a.N;
+        const int nt = m_outer ? rem % nnt : rem / nmp;
+        p.mb0 = 2 * (m_outer ? rem / nnt : rem % nmp);
         p.second = 1;
         p.wrow0 = nt * 256;
         p.wrow1 = p.wrow0 + 128;
