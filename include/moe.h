@@ -157,7 +157,8 @@ typedef struct moe_ws_layout {
     int64_t inter_scales;    /* fp32 [I/128][max_padded] (FP8 block), [max_padded] (FP8 token) */
     int64_t inter_h;         /* bf16 [max_padded][I]: SwiGLU output before its per-token
                                 quantisation (FP8 token only) */
-    int64_t y;               /* fp32 [T*k][H], weighted rows in slot order */
+    int64_t y;               /* bf16 [T*k][H], weighted rows in slot order (each rounded once
+                                from its fp32 value) */
     int64_t router_logits;   /* fp32 router logits: [T][E] from the CUDA-core router, or the
                                 tensor-core router's per-slice partial sums
                                 [splits][ceil(T/128)*128][E] */

@@ -1,6 +1,6 @@
-// Pieces shared by the bf16 / per-token FP8 group-GEMM kernels (one-SM and
-// two-SM forms): the K step of a pipeline stage, the MMA of each input type,
-// and the epilogue helpers.
+// Pieces shared by the group-GEMM kernels (one-SM and two-SM forms): the K
+// step of a pipeline stage, the MMA of each input type (bf16 / per-token
+// FP8), and the epilogue helpers.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,6 +42,19 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
         }
         d[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+// s * v[0..7] -> 8 bf16 (round to nearest even), returned as the bits of a float4 (one
+// 16-byte store or shared-memory slot).
+__device__ __forceinline__ float4 pack_bf16x8(const float *v, float s)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 p = __floats2bfloat162_rn(s * v[2 * i], s * v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&p);
+    }
+    return make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]), __uint_as_float(w[3]));
 }
 
 // Per-channel or per-token scales (per-token FP8) of 4 consecutive columns;

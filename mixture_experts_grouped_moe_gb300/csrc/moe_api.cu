@@ -178,7 +178,7 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
         L.y = -1;
         L.partials = take((int64_t)p.split_k2 * P * H * 4);
     } else {
-        L.y = take(S * H * 4);
+        L.y = take(S * H * 2);
         L.partials = -1;
     }
     L.total = off;
@@ -490,7 +490,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g2.split_k = p.split_k2;
     g2.x_scales = static_cast<float *>(at(L.inter_scales));
     g2.w_scales = static_cast<const float *>(w2_scale);
-    g2.y = static_cast<float *>(at(L.y));
+    g2.y = static_cast<__nv_bfloat16 *>(at(L.y));
     g2.partials = static_cast<float *>(at(L.partials));
     const int nt2 = (H + 255) / 256;
     const int64_t e_act = (S < E) ? S : E;
@@ -615,7 +615,7 @@ static int train_layout(int T, int H, int I, int E, int k, TrainLayout &TL)
     TL.gu = take(P * 2 * I * 2);
     TL.dys = take(P * H * 2);
     TL.dgu = take(P * 2 * I * 2);
-    TL.dxs = take(S * H * 4);
+    TL.dxs = take(S * H * 2);
     TL.dlogit = take((int64_t)T * E * 4);
     TL.wdT = take((int64_t)E * I * H * 2);
     TL.wguT = take((int64_t)E * H * 2 * I * 2);
@@ -664,7 +664,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     b.sorted_ids = static_cast<const int32_t *>(at(L.sorted_ids));
     b.sorted_w = static_cast<const float *>(at(L.sorted_w));
     b.npp = static_cast<const int32_t *>(at(L.npp));
-    b.Y = static_cast<const float *>(at(L.y));
+    b.Y = static_cast<const __nv_bfloat16 *>(at(L.y));
     b.topk_ids = static_cast<const int32_t *>(at(L.topk_ids));
     b.topk_w = static_cast<const float *>(at(L.topk_w));
     b.T = T;
@@ -674,7 +674,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     b.P_max = P;
     b.dys = bf(TL.dys);
     b.dlogit = static_cast<float *>(at(TL.dlogit));
-    b.dxs = static_cast<const float *>(at(TL.dxs));
+    b.dxs = static_cast<const __nv_bfloat16 *>(at(TL.dxs));
     b.dx = static_cast<__nv_bfloat16 *>(dx);
     b.dWr = dW_router;
     b.dbias = dbias;
@@ -735,7 +735,7 @@ static int backward_impl(const void *x, const void *W_router, const void *W_gate
     g2.N = H;
     g2.rows_per_expert = H;
     g2.sorted_weights = nullptr;
-    g2.y = static_cast<float *>(at(TL.dxs));
+    g2.y = static_cast<__nv_bfloat16 *>(at(TL.dxs));
     g2.tile_counter = status + 1;
     if (cudaMemsetAsync(status + 1, 0, sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256) dy_gather_kernel(const __nv_bfloat16 *__r
 // w_j y_j), the softmax backward dl_j = w_j (dw_j - sum_m w_m dw_m), dw_j =
 // dout_t . y_j, is dl_j = D_j - w_j sum_m D_m; written to dlogit[t][e_j].
 __global__ void __launch_bounds__(256) router_grad_kernel(const __nv_bfloat16 *__restrict__ dout,
-                                                         const float *__restrict__ Y,
+                                                         const __nv_bfloat16 *__restrict__ Y,
                                                          const int32_t *__restrict__ ids,
                                                          const float *__restrict__ wts, int T, int k, int E, int H,
                                                          float *__restrict__ dlogit)
@@ -75,11 +75,18 @@ __global__ void __launch_bounds__(256) router_grad_kernel(const __nv_bfloat16 *_
     float D = 0.0f;    // lane j < k keeps D_j
     float sum = 0.0f;  // sum_m D_m
     for (int j = 0; j < k; ++j) {
-        const float *yr = Y + ((size_t)t * k + j) * H;
+        const __nv_bfloat16 *yr = Y + ((size_t)t * k + j) * H;
         const __nv_bfloat16 *dr = dout + (size_t)t * H;
         float acc = 0.0f;
-        for (int h = lane; h < H; h += 32)
-            acc = fmaf(bf2f(dr[h]), yr[h], acc);
+        for (int h0 = lane * 8; h0 < H; h0 += 256) {  // eight columns per lane (H % 8 == 0)
+            const uint4 dv = __ldg(reinterpret_cast<const uint4 *>(dr + h0));
+            const uint4 yv = __ldg(reinterpret_cast<const uint4 *>(yr + h0));
+            const __nv_bfloat16 *d8 = reinterpret_cast<const __nv_bfloat16 *>(&dv);
+            const __nv_bfloat16 *y8 = reinterpret_cast<const __nv_bfloat16 *>(&yv);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                acc = fmaf(bf2f(d8[c]), bf2f(y8[c]), acc);
+        }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -131,24 +138,45 @@ __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16 *__r
     }
 }
 
-// dx[t] = sum_j dxs[t*k + j] (j ascending) + sum_j dlogit[t][e_j] W_router[e_j]  -> bf16
-__global__ void __launch_bounds__(256) dx_kernel(const float *__restrict__ dxs, const float *__restrict__ dlogit,
-                                                const int32_t *__restrict__ ids,
+// dx[t] = sum_j dxs[t*k + j] (j ascending) + sum_j dlogit[t][e_j] W_router[e_j]  -> bf16;
+// eight consecutive columns per thread (16-byte loads of the bf16 slot rows and router rows)
+__global__ void __launch_bounds__(256) dx_kernel(const __nv_bfloat16 *__restrict__ dxs,
+                                                const float *__restrict__ dlogit, const int32_t *__restrict__ ids,
                                                 const __nv_bfloat16 *__restrict__ Wr, int T, int k, int E, int H,
                                                 __nv_bfloat16 *__restrict__ dx)
 {
-    const int64_t total = (int64_t)T * H;
+    const int nv = H / 8;
+    const int64_t total = (int64_t)T * nv;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / H;
-        const int h = (int)(i - t * H);
-        float acc = 0.0f;
-        for (int j = 0; j < k; ++j)
-            acc += dxs[(t * k + j) * H + h];
+        const int64_t t = i / nv;
+        const int h0 = (int)(i - t * nv) * 8;
+        float acc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            acc[c] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(dxs + (t * k + j) * H + h0));
+            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                acc[c] += bf2f(b[c]);
+        }
         for (int j = 0; j < k; ++j) {
             const int e = ids[t * k + j];
-            acc = fmaf(dlogit[t * E + e], bf2f(Wr[(size_t)e * H + h]), acc);
+            const float d = dlogit[t * E + e];
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0));
+            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                acc[c] = fmaf(d, bf2f(b[c]), acc[c]);
         }
-        dx[i] = __float2bfloat16_rn(acc);
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[2 * c], acc[2 * c + 1]);
+            w[c] = *reinterpret_cast<uint32_t *>(&p2);
+        }
+        *reinterpret_cast<uint4 *>(dx + t * H + h0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -247,7 +275,7 @@ cudaError_t launch_backward_aux(int which, const BackwardAux &b, cudaStream_t st
         return cudaGetLastError();
     }
     case 2: {  // dx
-        int64_t grid = ((int64_t)b.T * b.H + 255) / 256;
+        int64_t grid = ((int64_t)b.T * (b.H / 8) + 255) / 256;
         if (grid > 65535)
             grid = 65535;
         dx_kernel<<<(int)(grid > 0 ? grid : 1), 256, 0, st>>>(b.dxs, b.dlogit, b.topk_ids, b.Wr, b.T, b.k, b.E, b.H,

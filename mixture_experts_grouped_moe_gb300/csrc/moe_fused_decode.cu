@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_swap_kernel(const __grid_co
                                 const int pos = tl.xrow + c0 + j;
                                 const int slot = a.sorted_ids[pos];
                                 if (slot < a.S)
-                                    a.y[(size_t)slot * a.N + n] = a.sorted_weights[pos] * v[j];
+                                    a.y[(size_t)slot * a.N + n] = __float2bfloat16_rn(a.sorted_weights[pos] * v[j]);
                             }
                         }
                     }

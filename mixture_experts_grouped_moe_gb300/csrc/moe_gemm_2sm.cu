@@ -621,9 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                                 const int slot = a.sorted_ids[row0 + c];
                                 const float wgt = a.sorted_weights[row0 + c];
                                 if (ok0)
-                                    a.y[(size_t)slot * a.N + f] = wgt * v[j];
+                                    a.y[(size_t)slot * a.N + f] = __float2bfloat16_rn(wgt * v[j]);
                                 if (ok1)
-                                    a.y[(size_t)slot * a.N + f + 256] = wgt * v2[j];
+                                    a.y[(size_t)slot * a.N + f + 256] = __float2bfloat16_rn(wgt * v2[j]);
                             }
                         }
                     }
@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                 // no weights: the unweighted rows (the backward's dx per slot)
                 const float wgt =
                     live ? (a.sorted_weights ? a.sorted_weights[pos] : 1.0f) * (QT ? a.x_scales[pos] : 1.0f) : 0.0f;
-                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + p.ncol0;
+                __nv_bfloat16 *dst = a.y + (size_t)(live ? slot : 0) * a.N + p.ncol0;
                 const int ncols = min(256, a.N - p.ncol0);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -726,11 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
                             v[i] *= sw.x, v[i + 1] *= sw.y, v[i + 2] *= sw.z, v[i + 3] *= sw.w;
                         }
                     }
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
-                                            wgt * v[4 * i + 3]);
+                    for (int i = 0; i < 32; ++i)
+                        v[i] *= wgt;
+                    store_bf16x32(dst + c0, v);
                 }
             }
             tc_fence_before();

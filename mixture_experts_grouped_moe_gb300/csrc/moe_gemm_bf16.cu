@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 // no weights: the unweighted rows (the backward's dx per slot)
                 const float wgt = (a.sorted_weights ? a.sorted_weights[pos] : 1.0f) * (QT ? a.x_scales[pos] : 1.0f);
                 const bool live = slot < a.S;
-                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + tl.ncol0;
+                __nv_bfloat16 *dst = a.y + (size_t)(live ? slot : 0) * a.N + tl.ncol0;
                 const int ncols = min(256, a.N - tl.ncol0);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -490,11 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                     }
                     if (live) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
-                                                wgt * v[4 * i + 3]);
+                        for (int i = 0; i < 32; ++i)
+                            v[i] *= wgt;
+                        store_bf16x32(dst + c0, v);
                     }
                 }
             } else if (MODE == MOE_MODE_SWAP && STAGE == 1) {
@@ -550,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                 const int pos = tl.xrow + c0 + j;
                                 const int slot = a.sorted_ids[pos];
                                 if (slot < a.S)
-                                    a.y[(size_t)slot * a.N + n] = a.sorted_weights[pos] * v[j];
+                                    a.y[(size_t)slot * a.N + n] = __float2bfloat16_rn(a.sorted_weights[pos] * v[j]);
                             }
                         }
                     }

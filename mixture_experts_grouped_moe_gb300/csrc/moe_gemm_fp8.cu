@@ -28,6 +28,7 @@
 // loads in flight next to 64 accumulators.
 #include <cuda_fp8.h>
 
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -66,7 +67,7 @@ struct __align__(1024) Smem {
     int abort;
     float amax[2][kSubs][128];  // per tile parity: row amax of each promotion warp's h chunk
     uint64_t ep_bar[4];         // per lane quadrant: one phase per tile once every warp wrote its amax
-    float4 ep_out[kPromoWarps][32][4];  // stage 2: a warp's 32 rows x 16 columns on their way to y
+    float4 ep_out[kPromoWarps][32][4];  // a warp's 32 rows x 64 bytes on their way to global memory
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -435,9 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                     a.inter_scales[(size_t)(ctl.ncol0 / 128) * a.P_max + cpos] = sc;
             } else {
                 // Each lane holds one row; stored straight from registers, every store instruction
-                // would touch 32 rows of y (32 cache lines).  Blocks of 16 columns go through a
-                // per-warp shared buffer instead (float4 slot j of row r at j ^ ((r >> 1) & 3), free
-                // of bank conflicts both ways) and leave as 8 rows x 64 contiguous bytes.
+                // would touch 32 rows of y (32 cache lines).  Blocks of 32 columns (64 bytes of bf16)
+                // go through a per-warp shared buffer instead (16-byte slot j of row r at
+                // j ^ ((r >> 1) & 3), free of bank conflicts both ways) and leave as 8 rows x 64
+                // contiguous bytes.
                 const int slot = a.sorted_ids[cpos];
                 const float wgt = slot < a.S ? a.sorted_weights[cpos] : 0.0f;
                 const int n0 = ctl.ncol0 + sub * 2 * kChunk;
@@ -445,12 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                 const int rr = lane >> 2, cq = lane & 3;  // read side: row within 8, float4 column
                 if (n0 < a.N) {
 #pragma unroll
-                    for (int blk = 0; blk < 2 * kChunk / 16; ++blk) {
-                        const float *v = blk < kChunk / 16 ? &acc0[blk * 16] : &acc1[blk * 16 - kChunk];
+                    for (int blk = 0; blk < 2 * kChunk / 32; ++blk) {
+                        const float *v = blk < kChunk / 32 ? &acc0[blk * 32] : &acc1[blk * 32 - kChunk];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            ep_rows[lane][j ^ ((lane >> 1) & 3)] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1],
-                                                                           wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
+                            ep_rows[lane][j ^ ((lane >> 1) & 3)] = pack_bf16x8(v + 8 * j, wgt);
                         __syncwarp();
 #pragma unroll
                         for (int it = 0; it < 4; ++it) {
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_kernel(const __grid_cons
                             const int rslot = __shfl_sync(0xffffffffu, slot, r);
                             const float4 o = ep_rows[r][cq ^ ((r >> 1) & 3)];
                             if (rslot < a.S)
-                                *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 16 + 4 * cq) = o;
+                                *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 32 + 8 * cq) = o;
                         }
                         __syncwarp();
                     }

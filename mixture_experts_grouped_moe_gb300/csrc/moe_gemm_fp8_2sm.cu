@@ -52,6 +52,7 @@
 #include <atomic>
 #include <cuda_fp8.h>
 
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -546,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_pair_kernel(const __grid
                 }
                 __syncwarp();
             } else {
-                // rows of y through a per-warp shared buffer (float4 slot j of row r at
-                // j ^ ((r >> 1) & 3)), leaving as 8 rows x 64 contiguous bytes per store
+                // rows of y, 32 bf16 columns at a time, through a per-warp shared buffer (16-byte
+                // slot j of row r at j ^ ((r >> 1) & 3)), leaving as 8 rows x 64 contiguous bytes
+                // per store
                 const int slot = cstore ? a.sorted_ids[cpos] : a.S;
                 const float wgt = slot < a.S ? a.sorted_weights[cpos] : 0.0f;
                 const int n0 = ctl.ncol0 + sub * 2 * kChunk;
@@ -555,12 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_pair_kernel(const __grid
                 const int rr = lane >> 2, cq = lane & 3;
                 if (cstore && n0 < a.N) {
 #pragma unroll
-                    for (int blk = 0; blk < 2 * kChunk / 16; ++blk) {
-                        const float *v = blk < kChunk / 16 ? &acc0[blk * 16] : &acc1[blk * 16 - kChunk];
+                    for (int blk = 0; blk < 2 * kChunk / 32; ++blk) {
+                        const float *v = blk < kChunk / 32 ? &acc0[blk * 32] : &acc1[blk * 32 - kChunk];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            ep_rows[lane][j ^ ((lane >> 1) & 3)] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1],
-                                                                           wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
+                            ep_rows[lane][j ^ ((lane >> 1) & 3)] = pack_bf16x8(v + 8 * j, wgt);
                         __syncwarp();
 #pragma unroll
                         for (int it = 0; it < 4; ++it) {
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_pair_kernel(const __grid
                             const int rslot = __shfl_sync(0xffffffffu, slot, r);
                             const float4 o = ep_rows[r][cq ^ ((r >> 1) & 3)];
                             if (rslot < a.S)
-                                *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 16 + 4 * cq) = o;
+                                *reinterpret_cast<float4 *>(a.y + (size_t)rslot * a.N + n0 + blk * 32 + 8 * cq) = o;
                         }
                         __syncwarp();
                     }

@@ -144,7 +144,8 @@ cudaError_t launch_quant_rows(const __nv_bfloat16 *X, const int32_t *sorted_ids,
 void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
 
 // out[t] = sum_j Y[t*k+j] (j ascending), fp32 -> bf16.
-cudaError_t launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st);
+cudaError_t launch_combine(const __nv_bfloat16 *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl,
+                           cudaStream_t st);
 // out[t] = sum_j w[t*k+j] * sum_ks P[ks][slot_pos[t*k+j]]  (split-K stage-2 partials).
 cudaError_t launch_splitk_combine(const float *P, int SK, int64_t P_rows, const int32_t *slot_pos, const float *wts,
                                   int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st);
@@ -177,7 +178,7 @@ struct GemmArgs {
     // outputs
     void *inter;             // stage 1: [P_max][I] bf16 or e4m3
     float *inter_scales;     // stage 1 FP8: [I/128][P_max]
-    float *y;                // stage 2: [S][H] fp32 (weighted)
+    __nv_bfloat16 *y;        // stage 2: [S][H] bf16, each row its weighted fp32 result rounded once
     float *partials;         // stage 2 split-K: [split][P_max][H]
     int *status;
     int *tile_counter;       // zeroed before the launch; CTAs claim tiles from it
@@ -223,14 +224,14 @@ struct BackwardAux {
     const int32_t *sorted_ids;
     const float *sorted_w;
     const int32_t *npp;
-    const float *Y;            // forward's weighted stage-2 rows [S][H]
+    const __nv_bfloat16 *Y;    // forward's weighted stage-2 rows [S][H] bf16
     const int32_t *topk_ids;
     const float *topk_w;
     int T, k, E, H;
     int64_t P_max;
     __nv_bfloat16 *dys;        // [P_max][H]
     float *dlogit;             // [T][E]
-    const float *dxs;          // [S][H]
+    const __nv_bfloat16 *dxs;  // [S][H] bf16
     __nv_bfloat16 *dx;         // [T][H]
     float *dWr, *dbias;        // [E][H], [E] (dbias nullable)
     float *rg_part;            // [ceil(T/128)][E][H] + [ceil(T/128)][E] partial router / bias gradients

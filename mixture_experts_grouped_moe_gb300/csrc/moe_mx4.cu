@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_kernel(const __grid_cons
                                 const int pos = tl.xrow + c0 + j;
                                 const int slot = a.sorted_ids[pos];
                                 if (slot < a.S)
-                                    a.y[(size_t)slot * a.N + n] = a.sorted_weights[pos] * v[j];
+                                    a.y[(size_t)slot * a.N + n] = __float2bfloat16_rn(a.sorted_weights[pos] * v[j]);
                             }
                         }
                     }
@@ -842,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                 const int slot = a.sorted_ids[pos];
                 const float wgt = a.sorted_weights[pos];
                 const bool live = slot < a.S;
-                float *dst = a.y + (size_t)(live ? slot : 0) * a.N + g.ncol0;
+                __nv_bfloat16 *dst = a.y + (size_t)(live ? slot : 0) * a.N + g.ncol0;
                 const int ncols = min(128, a.N - g.ncol0);
 #pragma unroll 1
                 for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -850,11 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                     tmem_ld32(tacc + c0, v);
                     if (!live)
                         continue;
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(wgt * v[4 * i], wgt * v[4 * i + 1], wgt * v[4 * i + 2],
-                                            wgt * v[4 * i + 3]);
+                    for (int i = 0; i < 32; ++i)
+                        v[i] *= wgt;
+                    store_bf16x32(dst + c0, v);
                 }
             }
             tc_fence_before();

@@ -1385,32 +1385,44 @@ __device__ __forceinline__ uint2 pack_bf16x4(const float4 &a)
     return pk;
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ Y, int T, int k, int H,
+// out[t] = sum_j Y[t*k + j] (j ascending, fp32) -> bf16; eight columns per thread (16-byte
+// loads of the bf16 slot rows, one 16-byte store)
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16 *__restrict__ Y, int T, int k, int H,
                                                      __nv_bfloat16 *__restrict__ out)
 {
     pdl_wait();
     pdl_trigger();
-    const int nv = H / 4;
+    const int nv = H / 8;
     const int64_t total = (int64_t)T * nv;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / nv;
         const int c = (int)(i % nv);
-        const float4 *src = reinterpret_cast<const float4 *>(Y) + (t * k) * nv + c;
-        float4 a = __ldg(src);
-        for (int j = 1; j < k; ++j) {
-            const float4 b = __ldg(src + (int64_t)j * nv);
-            a.x += b.x;
-            a.y += b.y;
-            a.z += b.z;
-            a.w += b.w;
+        const uint4 *src = reinterpret_cast<const uint4 *>(Y) + (t * k) * nv + c;
+        float a[8];
+        {
+            const uint4 v = __ldg(src);
+            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                a[q] = __bfloat162float(b[q]);
         }
-        reinterpret_cast<uint2 *>(out)[i] = pack_bf16x4(a);
+        for (int j = 1; j < k; ++j) {
+            const uint4 v = __ldg(src + (int64_t)j * nv);
+            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                a[q] += __bfloat162float(b[q]);
+        }
+        const uint2 lo = pack_bf16x4(make_float4(a[0], a[1], a[2], a[3]));
+        const uint2 hi = pack_bf16x4(make_float4(a[4], a[5], a[6], a[7]));
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
 }
 
-cudaError_t launch_combine(const float *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl, cudaStream_t st)
+cudaError_t launch_combine(const __nv_bfloat16 *Y, int T, int k, int H, __nv_bfloat16 *out, bool pdl,
+                           cudaStream_t st)
 {
-    const int64_t total = (int64_t)T * (H / 4);
+    const int64_t total = (int64_t)T * (H / 8);
     int64_t grid = (total + 255) / 256;
     if (grid > 152 * 16)
         grid = 152 * 16;
