@@ -477,3 +477,27 @@ def test_tc_router_exact_ties_fall_back(moe):
     assert np.array_equal(ids1, r_ids)
     st = layer.ws[layer.layout.status:layer.layout.status + 32].view(torch.int32).cpu().numpy()
     assert st[4] == cfg.T   # every token's leading group ties beyond its candidates: all fell back
+
+
+def test_tc_router_near_ties_settled_by_candidates(moe):
+    """Experts in pairs whose router rows differ in one element by one bf16 step: their fixed-order
+    logits differ, by far less than the tensor core's error bound.  The two of a pair rank next to
+    each other, so with an odd k the k-th and (k+1)-th candidates are a pair for every token and
+    only their fixed-order logits can order them.  The result must still be the fixed-order
+    router's and the oracle's, bit for bit, and the pairs inside the candidate set must not force
+    the all-expert fall-back."""
+    cfg = synth.MoEConfig("twins", T=512, H=512, I=256, E=64, k=3)
+    inp = synth.make_inputs(cfg, seed=8, device="cuda")
+    bits = inp["W_router"].view(torch.int16)
+    for e in range(1, 64, 2):
+        bits[e] = bits[e - 1]
+        bits[e, 5 + e] += 1   # one bf16 step in one element (nonzero rows: no sign or zero crossing)
+    ids1, w1, layer = _route_in_layer(moe, cfg, inp, 1)
+    ids0, w0, _ = _route_in_layer(moe, cfg, inp, 0)
+    assert np.array_equal(ids1, ids0)
+    assert np.array_equal(w1.view(np.uint32), w0.view(np.uint32))
+    r_ids, _, _ = oracle.route(synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["W_router"]), None, cfg.k)
+    assert np.array_equal(ids1, r_ids)
+    st = layer.ws[layer.layout.status:layer.layout.status + 32].view(torch.int32).cpu().numpy()
+    print(f"twins: {st[4]} of {cfg.T} tokens fell back to all fixed-order logits")
+    assert st[4] < cfg.T // 4
