@@ -412,9 +412,12 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     cudaError_t ge = cudaSuccess;
     if (fused) {
         // nothing to gather
-    } else if (dtype == MOE_BF16)
+    } else if (dtype == MOE_BF16 && train)
         ge = launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, S, k, H, P,
-                                static_cast<__nv_bfloat16 *>(at(L.x_sorted)), train, pdl_site(pdl, kPdlGather), st);
+                                static_cast<__nv_bfloat16 *>(at(L.x_sorted)), true, pdl_site(pdl, kPdlGather), st);
+    else if (dtype == MOE_BF16)
+        ge = launch_gather_by_token(static_cast<const __nv_bfloat16 *>(x), so.slot_pos, T, k, H, P,
+                                    static_cast<__nv_bfloat16 *>(at(L.x_sorted)), pdl_site(pdl, kPdlGather), st);
     else if (dtype == MOE_FP8_TOKEN)
         ge = launch_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
                                static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),

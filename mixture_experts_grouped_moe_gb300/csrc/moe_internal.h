@@ -131,6 +131,11 @@ cudaError_t launch_align_sort(const int32_t *ids, const float *wts, int T, int k
 cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S, int k,
                                int H, int64_t P_max, __nv_bfloat16 *xs, bool zero_padding, bool pdl,
                                cudaStream_t st);
+// The same rows (inference: padding rows untouched) walked token by token: x[t] is read once and
+// written to sorted positions slot_pos[t*k + j], j < k (k <= 32; positions outside [0, P_max)
+// are skipped).
+cudaError_t launch_gather_by_token(const __nv_bfloat16 *x, const int32_t *slot_pos, int T, int k, int H,
+                                   int64_t P_max, __nv_bfloat16 *xs, bool pdl, cudaStream_t st);
 // Same, quantised per 1x128 group: codes [P_max][H], scales transposed [H/128][P_max].
 cudaError_t launch_gather_quant_rows(const __nv_bfloat16 *x, const int32_t *sorted_ids, const int32_t *npp, int S,
                                      int k, int H, int64_t P_max, uint8_t *q, float *sT, bool pdl, cudaStream_t st);
