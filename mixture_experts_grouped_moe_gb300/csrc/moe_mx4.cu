@@ -81,23 +81,23 @@ __global__ void __launch_bounds__(256) quant_mx4_kernel(const __nv_bfloat16 *__r
     pdl_trigger();
     const int64_t rows = nrows ? (int64_t)*nrows : R;
     const int nvec = C / 8;
-    const int64_t total = rows * nvec;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v - threadIdx.x < total;
-         v += (int64_t)gridDim.x * blockDim.x) {
-        const bool ok = v < total;
-        const int64_t r = ok ? v / nvec : 0;
-        const int c8 = ok ? (int)(v - r * nvec) : 0;
-        float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (ok) {
-            int64_t src = r;
-            bool zero = false;
-            if (sorted_ids) {
-                const int sl = sorted_ids[r];
-                zero = sl >= S;
-                src = zero ? 0 : sl / k;
-            }
-            if (!zero) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(X + src * C) + c8);
+    // one row per block and pass (no per-thread index division); every thread of a warp takes part
+    // in the group shuffles, past the row's end with zeros
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        int64_t src = r;
+        bool zero = false;
+        if (sorted_ids) {
+            const int sl = sorted_ids[r];
+            zero = sl >= S;
+            src = zero ? 0 : sl / k;
+        }
+        const uint4 *xr = reinterpret_cast<const uint4 *>(X + src * C);
+        for (int c0 = 0; c0 < nvec; c0 += blockDim.x) {
+            const int c8 = c0 + threadIdx.x;
+            const bool ok = c8 < nvec;
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (ok && !zero) {
+                const uint4 raw = __ldg(xr + c8);
                 const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -106,28 +106,28 @@ __global__ void __launch_bounds__(256) quant_mx4_kernel(const __nv_bfloat16 *__r
                     f[2 * i + 1] = t.y;
                 }
             }
-        }
-        float m = 0.0f;
+            float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            m = fmaxf(m, fabsf(f[i]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const int e = mx_exponent(m);
-        const float inv = pow2_neg(e);
-        uint32_t packed = 0;
+            for (int i = 0; i < 8; ++i)
+                m = fmaxf(m, fabsf(f[i]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const int e = mx_exponent(m);
+            const float inv = pow2_neg(e);
+            uint32_t packed = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            packed |= e2m1_code(f[i] * inv) << (4 * i);
-        if (ok) {
-            reinterpret_cast<uint32_t *>(q + r * (C / 2))[c8] = packed;
-            if ((c8 & 3) == 0) {
-                const int g = c8 >> 2;
-                const uint8_t sb = (uint8_t)(e + 127);
-                if (tiled)
-                    s[tiled_sf_offset(r, g, C)] = sb;
-                else
-                    s[r * (C / 32) + g] = sb;
+            for (int i = 0; i < 8; ++i)
+                packed |= e2m1_code(f[i] * inv) << (4 * i);
+            if (ok) {
+                reinterpret_cast<uint32_t *>(q + r * (C / 2))[c8] = packed;
+                if ((c8 & 3) == 0) {
+                    const int g = c8 >> 2;
+                    const uint8_t sb = (uint8_t)(e + 127);
+                    if (tiled)
+                        s[tiled_sf_offset(r, g, C)] = sb;
+                    else
+                        s[r * (C / 32) + g] = sb;
+                }
             }
         }
     }
@@ -684,18 +684,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                 // Asynchronous copies that complete on the stage barrier.
                 {
                     // the block's scales of K tiles 2kb and 2kb + 1 are two consecutive 512-byte tiles
-                    // of the blocked order: two 16-byte copies per lane
-                    const uint8_t *src = xsf_g + ((size_t)(xrow >> 7) * ktiles + 2 * kb) * 512 + lane * 32;
-                    cp_async_16_zfill(asf + lane * 32, src, true);
-                    cp_async_16_zfill(asf + lane * 32 + 16, src + 16, true);
+                    // of the blocked order: one 16-byte copy per lane from each (a warp's copy covers
+                    // 512 contiguous bytes, free of shared-memory bank conflicts)
+                    const uint8_t *src = xsf_g + ((size_t)(xrow >> 7) * ktiles + 2 * kb) * 512 + lane * 16;
+                    cp_async_16_zfill(asf + lane * 16, src, true);
+                    cp_async_16_zfill(asf + 512 + lane * 16, src + 512, true);
                 }
+                // B: blocked row m takes words 0-1 from wrow0's tile and words 2-3 from wrow1's; lanes
+                // 2m and 2m + 1 copy the two halves of row m, so each 16-lane phase of a copy writes
+                // 128 contiguous bytes (no bank conflicts)
+                {
+                    const int part = lane & 1;
+                    const int wrow = part ? g.wrow1 : g.wrow0;
 #pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
-                    const int k_tile = 2 * kb + kt;
-                    cp_async_8(bsf + kt * 512 + lane * 16,
-                               sf_word_ptr(wsf_g, g.wrow0 >> 7, ktiles, k_tile, lane, (g.wrow0 & 127) >> 5));
-                    cp_async_8(bsf + kt * 512 + lane * 16 + 8,
-                               sf_word_ptr(wsf_g, g.wrow1 >> 7, ktiles, k_tile, lane, (g.wrow1 & 127) >> 5));
+                    for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int m = h * 16 + (lane >> 1);
+                            cp_async_8(bsf + kt * 512 + m * 16 + part * 8,
+                                       sf_word_ptr(wsf_g, wrow >> 7, ktiles, 2 * kb + kt, m, (wrow & 127) >> 5));
+                        }
+                    }
                 }
                 cp_async_arrive(&sm.full[s]);
                 if (++s == kStages) {
@@ -903,10 +912,7 @@ cudaError_t launch(const GemmArgs &a, int grid, cudaStream_t st)
 cudaError_t launch_quant_mx4(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
                              int S, int k, int C, uint8_t *q, uint8_t *s, bool tiled, bool pdl, cudaStream_t st)
 {
-    const int64_t total = R * (C / 8);
-    int64_t grid = (total + 255) / 256;
-    if (grid > 65535)
-        grid = 65535;
+    int64_t grid = R < 152 * 32 ? R : 152 * 32;  // rows per pass (the row count may be read on the device)
     if (grid < 1)
         return cudaSuccess;
     return launch_kernel(pdl, mx4::quant_mx4_kernel, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows,
