@@ -462,7 +462,8 @@ __global__ void __launch_bounds__(256) router_wnorm_kernel(const __nv_bfloat16 *
     if (e >= E)
         return;
     float ss = 0.0f;
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+#pragma unroll 4
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {  // (unrolled: several row loads in flight)
         float f[8];
         bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(Wr + (size_t)e * H + h0)), f);
 #pragma unroll
@@ -959,10 +960,18 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int32_t *__restrict__ c
         s_counted = 0;
     int cnt = 0;
     if (e < E) {
-        for (int c = 0; c < nchunks; ++c) {
-            const int v = cc[(size_t)c * E + e];
-            cc[(size_t)c * E + e] = cnt;
-            cnt += v;
+        // eight chunk counts in flight per round (each round one L2 round trip, not eight)
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = c0 + j < nchunks ? cc[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (c0 + j < nchunks) {
+                    cc[(size_t)(c0 + j) * E + e] = cnt;
+                    cnt += v[j];
+                }
         }
     }
     const int pad = (e < E) ? (cnt + B - 1) / B * B : 0;
