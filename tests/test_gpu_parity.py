@@ -325,6 +325,7 @@ EDGE_CASES = [
     ("swap_b128_sk1", 20, 256, 512, 4, 2, None, 128, 1),
     ("swap_sk8", 8, 512, 1024, 8, 2, None, 0, 8),
     ("grouped_h_odd", 200, 640, 256, 8, 2, "normal", 0, 0),
+    ("grouped_k32", 200, 128, 256, 64, 32, "normal", 0, 0),   # the token-major gather at its k limit
 ]
 
 
