@@ -428,6 +428,7 @@ cudaError_t launch_router(const __nv_bfloat16 *x, const __nv_bfloat16 *Wr, const
 // the bias add a few fp32 roundings.  Together <= 2^-11 sum|p| + 2^-22 |bias|,
 // with sum|p| <= ||x_t|| ||w_e|| (Cauchy-Schwarz; both norms rounded up).
 constexpr int kTcExtra = 4;
+constexpr int kTcMaxSplits = 8;  // K slices of the tensor-core logits (router_tc_splits)
 
 bool router_tc_eligible(int T, int H, int E, int k)
 {
@@ -566,13 +567,31 @@ __global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 
         return;
     float *lg = s_lg + warp * E;
     const __nv_bfloat16 *xrow = x + (size_t)t * H;
-    for (int e = lane; e < E; e += 32) {
-        float v = 0.0f;
-        for (int sl = 0; sl < nsplit; ++sl)
-            v += part[((size_t)sl * part_rows + t) * E + e];
-        if (bias)
-            v += bias[e];
-        lg[e] = v;
+    // the slices' partial logits, summed in slice order; the loads of four experts' slices are
+    // issued before any sum (one L2 round trip per four experts, not one per slice)
+    for (int e0 = lane; e0 < E; e0 += 4 * 32) {
+        float pv[4][kTcMaxSplits];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int sl = 0; sl < kTcMaxSplits; ++sl)
+                pv[j][sl] = (e0 + 32 * j < E && sl < nsplit)
+                                ? __ldg(part + ((size_t)sl * part_rows + t) * E + e0 + 32 * j)
+                                : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + 32 * j;
+            if (e >= E)
+                break;
+            float v = 0.0f;
+#pragma unroll
+            for (int sl = 0; sl < kTcMaxSplits; ++sl)
+                if (sl < nsplit)
+                    v += pv[j][sl];
+            if (bias)
+                v += bias[e];
+            lg[e] = v;
+        }
     }
     float ss = 0.0f;
     for (int h0 = lane * 8; h0 < H; h0 += 256) {
@@ -589,15 +608,38 @@ __global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 
     const int nc = min(E, k + kTcExtra);
     uint32_t taken = 0;  // bit m: expert lane + 32m is a candidate
     int my_c = 0;
+    // up to 256 experts: the lane's eight logits stay in registers across the rounds
+    const bool in_regs = E <= 256;
+    float lv[8];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int e = lane + 32 * m;
+        lv[m] = (in_regs && e < E) ? lg[e] : 0.0f;
+        if (e < E)
+            valid |= 1u << m;
+    }
     for (int c = 0; c < nc; ++c) {
         float bv = -FLT_MAX;
         int be = INT_MAX;
-        for (int m = 0, e = lane; e < E; ++m, e += 32) {
-            if (taken & (1u << m))
-                continue;
-            if (be == INT_MAX || lg[e] > bv) {
-                bv = lg[e];
-                be = e;
+        if (in_regs) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if (!(valid & (1u << m)) || (taken & (1u << m)))
+                    continue;
+                if (be == INT_MAX || lv[m] > bv) {
+                    bv = lv[m];
+                    be = lane + 32 * m;
+                }
+            }
+        } else {
+            for (int m = 0, e = lane; e < E; ++m, e += 32) {
+                if (taken & (1u << m))
+                    continue;
+                if (be == INT_MAX || lg[e] > bv) {
+                    bv = lg[e];
+                    be = e;
+                }
             }
         }
 #pragma unroll
