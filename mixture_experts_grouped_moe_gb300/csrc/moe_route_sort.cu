@@ -594,7 +594,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const __nv_bfloat16 
         }
     }
     float ss = 0.0f;
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+#pragma unroll 4
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {  // (unrolled: several row loads in flight)
         float f[8];
         bf16x8_to_float(__ldg(reinterpret_cast<const uint4 *>(xrow + h0)), f);
 #pragma unroll
