@@ -61,6 +61,21 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_rows16(CUtensorMap *map, const void *base, uint64_t nbytes, uint32_t box_rows)
+{
+    auto fn = get_encode_fn();
+    if (!fn || nbytes % 16 != 0)
+        return false;
+    cuuint64_t dims[2] = {16, nbytes / 16};
+    cuuint64_t strides[1] = {16};
+    cuuint32_t box[2] = {16, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Automatic CTA-pair rule (same-box measurements on GB300): pairs pay off once
 // the average active expert holds one token block (S >= 128 per expert, E
 // standing in for the active count): bf16 Mixtral shapes, one-SM vs pairs,
@@ -557,6 +572,11 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
                  : (dtype == MOE_MXFP4) ? launch_gemm_swap_mx4(2, g2, grid, st)
                                         : launch_gemm_swap_fp8_token(2, g2, grid, st);
         } else if (dtype == MOE_MXFP4) {
+            // the scale blocks of h and W_down (blocked order, whole 512-byte tiles per K tile) as TMA
+            // rows of 16 bytes; the sorted rows fill whole 128-row blocks, at most P / 128 of them
+            if (!encode_tmap_rows16(&g2.tm_sfa, at(L.inter_scales), (uint64_t)(P / 128) * 128 * I / 32, 64) ||
+                !encode_tmap_rows16(&g2.tm_sfb, w2_scale, (uint64_t)E * H * I / 32, 64))
+                return MOE_ERR_CUDA;
             const int64_t ub = p.max_blocks * (H / 128);
             ce = launch_gemm_grouped_mx4(2, g2, (int)(ub < nsm ? ub : nsm), st);
         } else if (use_pair(dtype, 2, T, k, E, o.gemm_pair)) {

@@ -162,6 +162,8 @@ struct GemmArgs {
     CUtensorMap tm_x;     // token operand rows [P_max][K]
     CUtensorMap tm_w;     // weight operand rows [E*rows_per_expert][K]
     CUtensorMap tm_x16;   // the token operand in 16-row boxes (light-expert pair tiles)
+    CUtensorMap tm_sfa;   // grouped MXFP4 stage 2: h's blocked scales as 16-byte rows, 64-row boxes
+    CUtensorMap tm_sfb;   // grouped MXFP4 stage 2: W_down's blocked scales, the same
     const int32_t *sorted_ids;
     const float *sorted_weights;
     const int32_t *sorted_expert_ids;
@@ -198,6 +200,8 @@ struct GemmArgs {
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows);
+// A byte buffer of nbytes (a multiple of 16) as rows of 16 bytes, unswizzled, box_rows rows per box.
+bool encode_tmap_rows16(CUtensorMap *map, const void *base, uint64_t nbytes, uint32_t box_rows);
 
 int num_sms_current_device();
 

@@ -604,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.full[i], 1 + 32);  // TMA bytes + the producer lanes' scale copies
+            // TMA bytes (+ the producer lanes' scale copies in stage 1)
+            mbar_init(&sm.full[i], STAGE == 2 ? 1 : 1 + 32);
             mbar_init(&sm.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -617,6 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
         fence_mbarrier_init();
         tma_prefetch_desc(&a.tm_x);
         tma_prefetch_desc(&a.tm_w);
+        if (STAGE == 2) {
+            tma_prefetch_desc(&a.tm_sfa);
+            tma_prefetch_desc(&a.tm_sfb);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -669,16 +674,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                     break;
                 }
                 uint8_t *st = sm.stage[s];
+                uint8_t *asf = st + 2 * kHalf;
+                uint8_t *bsf = asf + 1024;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&sm.full[s], 2 * kHalf);
+                    mbar_arrive_expect_tx(&sm.full[s], 2 * kHalf + (STAGE == 2 ? 2048 : 0));
                     tma_load_2d(st, &a.tm_x, kb * kKBytes, xrow, &sm.full[s], pol_x);
                     tma_load_2d(st + kHalf, &a.tm_w, kb * kKBytes, g.wrow0, &sm.full[s], pol_w);
                     tma_load_2d(st + kHalf + kHalf / 2, &a.tm_w, kb * kKBytes, g.wrow1, &sm.full[s], pol_w);
+                    if (STAGE == 2) {
+                        // stage 2's 128 weight rows are one 128-row tile: both scale blocks are whole
+                        // 512-byte tiles of the blocked order (two K tiles, 64 rows of 16 bytes each),
+                        // so they come by TMA too and need no proxy fence before tcgen05.cp
+                        tma_load_2d(asf, &a.tm_sfa, 0, ((xrow >> 7) * ktiles + 2 * kb) * 32, &sm.full[s], pol_x);
+                        tma_load_2d(bsf, &a.tm_sfb, 0, ((g.wrow0 >> 7) * ktiles + 2 * kb) * 32, &sm.full[s], pol_w);
+                    }
                     issued[s] = 1;
                     issued_ph[s] = ph;
                 }
-                uint8_t *asf = st + 2 * kHalf;
-                uint8_t *bsf = asf + 1024;
+                if (STAGE == 2) {
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    continue;
+                }
                 // A scales: token rows l + 32 w of the block, 8 bytes each (two K tiles of 4 groups);
                 // B scales: rows 0-63 from wrow0's tile, 64-127 from wrow1's (words of a 64-row half).
                 // Asynchronous copies that complete on the stage barrier.
@@ -758,7 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                     tc_fence_after();
                     const uint8_t *st = sm.stage[s];
                     const uint32_t sf = tmem_base + kSfBase + s * kSfCols;
-                    fence_proxy_async_smem();  // the scale copies (generic proxy) before tcgen05.cp reads them
+                    if (STAGE == 1)
+                        fence_proxy_async_smem();  // the scale copies (generic proxy) before tcgen05.cp reads them
 #pragma unroll
                     for (int i = 0; i < 4; ++i)  // A K tiles 0,1 then B K tiles 0,1
                         tmem_cp_sf(sf + 4 * i, smem_desc_rows16(st + 2 * kHalf + 512 * i));
