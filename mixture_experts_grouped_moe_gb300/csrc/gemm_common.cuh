@@ -28,6 +28,15 @@ __device__ __forceinline__ void mma_kind(uint32_t d, uint64_t ad, uint64_t bd, u
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// sigmoid(g) = 0.5 + 0.5 tanh(g / 2) on one special-function instruction (tanh.approx, relative
+// error near 2^-11), for epilogues bound by that unit whose results are rounded to bf16 next.
+__device__ __forceinline__ float sigmoid_fast(float g)
+{
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
+    return fmaf(0.5f, t, 0.5f);
+}
+
 // 32 fp32 values -> 32 bf16 (round to nearest even) at a 16-byte aligned address.
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&h)[32])
 {

@@ -586,14 +586,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
             if (t < 0)
                 break;
             const PairTile p = decode<STAGE, LT>(sm, a, t);
+            const bool store = rank == 0 || p.second;
+            const int pos = (p.mb0 + (int)rank) * 128 + row;   // sorted row of this thread
+            if (STAGE == 3 && store) {
+                // the saved g | u this thread's epilogue reads (2 x 512 bytes of its row, from DRAM):
+                // into L2 while the tile's MMAs run, so that the epilogue's loads wait on L2 only
+                const __nv_bfloat16 *gr = a.gu_in + (size_t)pos * (2 * a.N) + p.ncol0;
+#pragma unroll
+                for (int c = 0; c < 256; c += 64) {
+                    prefetch_l2(gr + c);
+                    prefetch_l2(gr + a.N + c);
+                }
+            }
             bool ok = mbar_wait(&sm.tfull[acc], aph, a.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-            const bool store = rank == 0 || p.second;
-            const int pos = (p.mb0 + (int)rank) * 128 + row;   // sorted row of this thread
             if (LT && p.swap) {
                 // one output feature per thread, one token per accumulator column
                 const int f = p.ncol0 + (int)rank * 128 + row;
@@ -681,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const __grid_con
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int ii = i + 2 * q2 + r;
-                                const float sg = 1.0f / (1.0f + __expf(-gg[r]));
+                                const float sg = sigmoid_fast(gg[r]);
                                 dg[ii] = dh[ii] * uu[r] * sg * (1.0f + gg[r] * (1.0f - sg));
                                 du[ii] = dh[ii] * gg[r] * sg;
                             }

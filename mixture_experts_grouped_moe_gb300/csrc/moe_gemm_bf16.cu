@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                             for (int r = 0; r < 2; ++r) {
                                 const int ii = i + 2 * q2 + r;
-                                const float sg = 1.0f / (1.0f + __expf(-gg[r]));
+                                const float sg = sigmoid_fast(gg[r]);
                                 dg[ii] = dh[ii] * uu[r] * sg * (1.0f + gg[r] * (1.0f - sg));
                                 du[ii] = dh[ii] * gg[r] * sg;
                             }

@@ -23,6 +23,12 @@ __device__ __forceinline__ unsigned long long global_timer_ns()
     return t;
 }
 
+// Bring the 128-byte line holding p into L2 (no register written, nothing waited for).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
