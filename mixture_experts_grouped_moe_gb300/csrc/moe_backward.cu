@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(256) router_wgrad_partial_kernel(const float *
 #pragma unroll
     for (int j = 0; j < kRgE; ++j)
         acc[j] = 0.0f;
-    for (int tt = 0; tt < tn; ++tt) {
+#pragma unroll 8
+    for (int tt = 0; tt < tn; ++tt) {  // (unrolled: several tokens' loads in flight; t ascending)
         const float xv = bf2f(x[(size_t)(t0 + tt) * H + h]);
 #pragma unroll
         for (int j = 0; j < kRgE; ++j)
