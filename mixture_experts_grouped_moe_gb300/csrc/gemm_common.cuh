@@ -26,8 +26,6 @@ __device__ __forceinline__ void mma_kind(uint32_t d, uint64_t ad, uint64_t bd, u
         mma_bf16(d, ad, bd, idesc, accum);
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
-
 // sigmoid(g) = 0.5 + 0.5 tanh(g / 2) on one special-function instruction (tanh.approx, relative
 // error near 2^-11), for epilogues bound by that unit whose results are rounded to bf16 next.
 __device__ __forceinline__ float sigmoid_fast(float g)
@@ -36,6 +34,10 @@ __device__ __forceinline__ float sigmoid_fast(float g)
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
     return fmaf(0.5f, t, 0.5f);
 }
+
+// silu(g) = g sigmoid(g), the sigmoid as above: every SwiGLU epilogue rounds h to bf16 (or
+// quantises it) right after, a relative step of 2^-9 or more against the sigmoid's 2^-11.
+__device__ __forceinline__ float silu(float g) { return g * sigmoid_fast(g); }
 
 // 32 fp32 values -> 32 bf16 (round to nearest even) at a 16-byte aligned address.
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&h)[32])

@@ -412,11 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             u[i] *= sx * su.x, u[i + 1] *= sx * su.y, u[i + 2] *= sx * su.z, u[i + 3] *= sx * su.w;
                         }
                     }
-                    // per-token FP8: h is re-quantised to e4m3 next, so silu takes the one-instruction
-                    // sigmoid (relative error near 2^-11, as the block-FP8 epilogue)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        h[i] = (QT ? g[i] * sigmoid_fast(g[i]) : silu(g[i])) * u[i];
+                        h[i] = silu(g[i]) * u[i];
                     store_bf16x32(dst + c0, h);
                     if (a.gu) {  // training: keep the pre-activations for the backward
                         __nv_bfloat16 *gr = a.gu + (size_t)(tl.xrow + row) * (2 * a.N) + tl.ncol0 + c0;

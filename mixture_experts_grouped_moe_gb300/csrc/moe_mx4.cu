@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                     float m = 0.0f;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        h[i] = gv[i] * sigmoid_fast(gv[i]) * uv[i];  // (re-quantised to E2M1 next)
+                        h[i] = silu(gv[i]) * uv[i];
                         m = fmaxf(m, fabsf(h[i]));
                     }
                     const int e = mx_exponent(m);
