@@ -47,6 +47,24 @@ __device__ __forceinline__ uint32_t e2m1_code(float y)
     return sign | i;
 }
 
+// Eight floats -> eight E2M1 codes in one word, element i in bits 4i..4i+3, by the tensor-format
+// conversion instruction (two elements each; round to nearest even, saturating to +-6): the same
+// rule as e2m1_code in a sixteenth of the instructions.  The quantiser's codes are compared bit for
+// bit with the oracle's on every finite bf16 value of six binades around a group's scale.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
 // Shared exponent floor(log2(amax)) - 2, clamped to [-127, 127]; 0 for amax = 0.
 __device__ __forceinline__ int mx_exponent(float amax)
 {
@@ -114,10 +132,10 @@ __global__ void __launch_bounds__(256) quant_mx4_kernel(const __nv_bfloat16 *__r
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             const int e = mx_exponent(m);
             const float inv = pow2_neg(e);
-            uint32_t packed = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                packed |= e2m1_code(f[i] * inv) << (4 * i);
+                f[i] *= inv;
+            const uint32_t packed = e2m1x8(f);
             if (ok) {
                 reinterpret_cast<uint32_t *>(q + r * (C / 2))[c8] = packed;
                 if ((c8 & 3) == 0) {
@@ -859,10 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx4_grouped_kernel(const __g
                     uint32_t w[4];
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
-                        w[b] = 0;
+                        float y[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            w[b] |= e2m1_code(h[8 * b + i] * inv) << (4 * i);
+                            y[i] = h[8 * b + i] * inv;
+                        w[b] = e2m1x8(y);
                     }
                     *reinterpret_cast<uint4 *>(hq + c0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
                     hs[tiled_sf_offset(pos, (g.ncol0 + c0) / 32, a.N)] = (uint8_t)(e + 127);

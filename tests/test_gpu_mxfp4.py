@@ -82,6 +82,39 @@ def test_quant_mxfp4_bit_exact(moe, tiled):
     assert np.array_equal(unpack(q.cpu().numpy()), rq)
 
 
+def _every_rounding_boundary(R, C):
+    """Groups of 32 bf16 values: a leader 7.875 * 2^j that fixes the group's scale at 2^j (2^-127,
+    the clamp, for the subnormal j), then every finite bf16 value v with 2^(j-3) <= |v| <= leader,
+    both signs, 31 to a group -- each scaled value from 1/8 up into the saturation range meets the
+    rounding rule.  Padded with zero groups to R x C."""
+    vals = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    groups = []
+    for j in (-130, -127, -3, 0, 9, 125):
+        lead = 7.875 * 2.0 ** j
+        v = vals[torch.isfinite(vals) & (vals.abs() <= lead) & (vals.abs() >= 2.0 ** (j - 3))]
+        v = torch.cat([v, torch.zeros((-len(v)) % 31)]).view(-1, 31)
+        groups.append(torch.cat([torch.full((v.shape[0], 1), lead), v], 1))
+    g = torch.cat(groups).reshape(-1)
+    X = torch.zeros(R * C)
+    X[: g.numel()] = g
+    return X.view(R, C).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("tiled", [False, True], ids=["row_major", "tiled"])
+def test_quant_mxfp4_every_rounding_boundary(moe, tiled):
+    R, C = 128, 384
+    X = _every_rounding_boundary(R, C).cuda()
+    q = torch.empty(R, C // 2, dtype=torch.uint8, device="cuda")
+    s = torch.empty(R * C // 32, dtype=torch.uint8, device="cuda")
+    moe.moe_quantize_mxfp4(X, R, C, q, s, tiled=tiled)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_mx4(synth.bf16_bits(X))
+    gs = s.cpu().numpy()
+    gs = untile(gs, R, C) if tiled else gs.reshape(R, C // 32)
+    assert np.array_equal(gs, rs)
+    assert np.array_equal(unpack(q.cpu().numpy()), rq)
+
+
 def test_quant_mxfp4_rejects_bad_shapes(moe):
     X = torch.zeros(4, 48, dtype=torch.bfloat16, device="cuda")
     q = torch.empty(4, 24, dtype=torch.uint8, device="cuda")
