@@ -72,19 +72,6 @@ struct __align__(1024) Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
-// The epilogue runs while the tensor core can only fill the two TMEM buffers of the next
-// tile and is bound by the special-function unit, so silu takes one approximate tanh:
-// silu(g) = g * sigmoid(g) = g * (0.5 + 0.5 * tanh(g / 2)); tanh.approx has a relative error
-// near 2^-11, and h is re-quantised to 3 mantissa bits right after.
-__device__ __forceinline__ float tanh_approx(float x)
-{
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float silu(float g) { return g * fmaf(0.5f, tanh_approx(0.5f * g), 0.5f); }
-
 struct Tile {
     int e, xrow, wrow0, wrow1, ncol0;
 };

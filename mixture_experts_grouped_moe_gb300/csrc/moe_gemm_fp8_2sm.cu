@@ -98,17 +98,6 @@ struct __align__(1024) Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "a CTA has at most 227 KB of shared memory");
 
-// silu(g) = g * sigmoid(g) = g * (0.5 + 0.5 * tanh(g / 2)) with one approximate tanh (relative
-// error near 2^-11; h is re-quantised to 3 mantissa bits right after) -- the one-SM kernel's form.
-__device__ __forceinline__ float tanh_approx(float x)
-{
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float silu_t(float g) { return g * fmaf(0.5f, tanh_approx(0.5f * g), 0.5f); }
-
 struct PairTile {
     int mb0;      // first 128-row block of the pair
     int second;   // the pair's second block is a real block of the expert
@@ -499,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_fp8_pair_kernel(const __grid
                 float amax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
-                    acc0[i] = silu_t(acc0[i]) * acc1[i];
+                    acc0[i] = silu(acc0[i]) * acc1[i];
                     amax = fmaxf(amax, fabsf(acc0[i]));
                 }
                 sm.amax[gen & 1][sub][row] = amax;
