@@ -89,3 +89,24 @@ def check_rows(got, ref, tol, row_factor=4.0, label=""):
     assert err <= tol, f"{label}: relL2 {err:.3e} > {tol}"
     assert rows[worst] <= row_factor * tol, f"{label}: row {worst} relL2 {rows[worst]:.3e} > {row_factor * tol}"
     return err, float(rows[worst]), worst
+
+
+E4M3_LEADERS = (1.3 * 2.0 ** -126, 1e-30, 0.7, 3.1, 57.0, 672.0, 2e30, 1.3 * 2.0 ** 120)
+
+
+def every_bf16_below(leaders, C, group):
+    """bf16 rows for exhaustive quantiser checks: per group of `group` columns a leader (the group's
+    largest magnitude, so it fixes the group's scale), then every finite bf16 value v with
+    leader * 2^-21 <= |v| <= leader, both signs, spread over the row's groups in ascending bit
+    order, the rest zero.  One row per leader; group = C gives one scale per row."""
+    import torch
+    vals = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    rows = []
+    for lead in leaders:
+        lead = torch.tensor(lead).to(torch.bfloat16).float().item()
+        v = vals[torch.isfinite(vals) & (vals.abs() <= lead) & (vals.abs() >= lead * 2.0 ** -21)]
+        ng, per = C // group, group - 1
+        assert len(v) <= ng * per
+        v = torch.cat([v, torch.zeros(ng * per - len(v))]).view(ng, per)
+        rows.append(torch.cat([torch.full((ng, 1), lead), v], 1).reshape(-1))
+    return torch.stack(rows).to(torch.bfloat16)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from mixture_experts_grouped_moe_gb300 import synth
-from moe_checks import check_rows, parity_tokens, rel_l2
+from moe_checks import E4M3_LEADERS, check_rows, every_bf16_below, parity_tokens, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,20 @@ def test_quant_rows_bit_exact(moe, R, C):
     X = (torch.randn(R, C, generator=g, device="cuda") *
          torch.exp(torch.randn(R, 1, generator=g, device="cuda") * 3)).to(torch.bfloat16)
     X[1] = 0
+    q = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+    s = torch.empty(R, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(X, R, C, q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_rows(synth.bf16_bits(X))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_rows_every_bf16_value(moe):
+    # every bf16 value within 21 binades below a row's largest, for eight row scales (one whose
+    # reciprocal is not a normal float): each code must be e4m3 of the IEEE quotient v / scale
+    X = every_bf16_below(E4M3_LEADERS, 5504, 5504).cuda()
+    R, C = X.shape
     q = torch.empty(R, C, dtype=torch.uint8, device="cuda")
     s = torch.empty(R, dtype=torch.float32, device="cuda")
     moe.moe_quantize_fp8_rows(X, R, C, q, s)

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from mixture_experts_grouped_moe_gb300 import synth
-from moe_checks import check_rows, check_sort_invariants, parity_tokens, rel_l2
+from moe_checks import E4M3_LEADERS, check_rows, check_sort_invariants, every_bf16_below, parity_tokens, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -217,6 +217,19 @@ def test_quant_act_bit_exact(moe):
     q = torch.empty(300, 1024, dtype=torch.uint8, device="cuda")
     s = torch.empty(300, 8, dtype=torch.float32, device="cuda")
     moe.moe_quantize_fp8_act(X, 300, 1024, q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_1x128(synth.bf16_bits(X))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_act_every_bf16_value(moe):
+    # every bf16 value within 21 binades below a group's largest, for eight group scales
+    X = every_bf16_below(E4M3_LEADERS, 5504, 128).cuda()
+    R, C = X.shape
+    q = torch.empty(R, C, dtype=torch.uint8, device="cuda")
+    s = torch.empty(R, C // 128, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_act(X, R, C, q, s)
     torch.cuda.synchronize()
     rq, rs = oracle.quant_1x128(synth.bf16_bits(X))
     assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
