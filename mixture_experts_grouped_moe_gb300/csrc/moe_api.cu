@@ -120,7 +120,7 @@ int num_sms_current_device()
 struct Layout {
     int64_t status, logits, topk_ids, topk_w, sort_scratch, counts, offsets, active, num_active, npp;
     int64_t sorted_ids, sorted_w, sorted_eids, slot_pos;
-    int64_t x_sorted, x_scales, inter, inter_scales, inter_h, y, partials;
+    int64_t x_sorted, x_scales, inter, inter_scales, inter_h, h_amax, y, partials;
     int64_t total;
 };
 
@@ -189,6 +189,7 @@ static Layout make_layout(int dtype, int T, int H, int I, int E, int k, const mo
                                                      : -1;
     }
     L.inter_h = (dtype == MOE_FP8_TOKEN) ? take(P * I * 2) : -1;
+    L.h_amax = (dtype == MOE_FP8_TOKEN) ? take(P * 4) : -1;
     if (p.split_k2 > 1) {
         L.y = -1;
         L.partials = take((int64_t)p.split_k2 * P * H * 4);
@@ -424,6 +425,11 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     // bf16 decode: both GEMM stages in one persistent launch that also fetches the token rows
     // itself (no gather pass)
     const bool fused = p.mode == MOE_MODE_SWAP && dtype == MOE_BF16 && o.one_stage == 1 && !train;
+    // per-token FP8 on the one-SM grouped stage 1: its epilogue takes each row's max |h| (into
+    // h_amax, zeroed by the activation quantiser), so h's quantiser needs no reduction pass
+    float *h_amax = (dtype == MOE_FP8_TOKEN && p.mode == MOE_MODE_GROUPED && !use_pair(dtype, 1, T, k, E, o.gemm_pair))
+                        ? static_cast<float *>(at(L.h_amax))
+                        : nullptr;
     cudaError_t ge = cudaSuccess;
     if (fused) {
         // nothing to gather
@@ -436,7 +442,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     else if (dtype == MOE_FP8_TOKEN)
         ge = launch_quant_rows(static_cast<const __nv_bfloat16 *>(x), so.sorted_ids, so.num_post_padded, P, S, k, H,
                                static_cast<uint8_t *>(at(L.x_sorted)), static_cast<float *>(at(L.x_scales)),
-                               pdl_site(pdl, kPdlGather), st);
+                               pdl_site(pdl, kPdlGather), st, h_amax);
     else if (dtype == MOE_MXFP4)
         // grouped mode keeps the token scales in the tensor core's 128 x 4 blocked order (two 16-byte
         // copies per lane and K step in the GEMM's producer instead of eight 4-byte ones: Mixtral
@@ -494,6 +500,7 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
     g1.w_scales = static_cast<const float *>(w1_scale);
     g1.inter_scales = static_cast<float *>(at(L.inter_scales));
     g1.gu = gu;
+    g1.row_amax = h_amax;
 
     GemmArgs g2 = g;
     g2.tile_counter = (p.mode == MOE_MODE_GROUPED || dtype == MOE_MXFP4) ? status + 2 : nullptr;
@@ -559,9 +566,13 @@ static int forward_impl(int dtype, const void *x, const void *W_router, const fl
         // ------------------------------------------------------ stage 2
         if (dtype == MOE_FP8_TOKEN) {
             // h (bf16, sorted order) -> e4m3 codes with one scale per row (stage 2's input)
-            ce = launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr, so.num_post_padded, P,
-                                   S, k, I, static_cast<uint8_t *>(at(L.inter)),
-                                   static_cast<float *>(at(L.inter_scales)), pdl_site(pdl, kPdlGather), st);
+            ce = h_amax ? launch_quant_rows_amax(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), h_amax,
+                                                 so.num_post_padded, P, I, static_cast<uint8_t *>(at(L.inter)),
+                                                 static_cast<float *>(at(L.inter_scales)), pdl_site(pdl, kPdlGather),
+                                                 st)
+                        : launch_quant_rows(static_cast<const __nv_bfloat16 *>(at(L.inter_h)), nullptr,
+                                            so.num_post_padded, P, S, k, I, static_cast<uint8_t *>(at(L.inter)),
+                                            static_cast<float *>(at(L.inter_scales)), pdl_site(pdl, kPdlGather), st);
             if (ce != cudaSuccess)
                 return MOE_ERR_CUDA;
         }

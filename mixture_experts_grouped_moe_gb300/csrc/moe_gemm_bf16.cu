@@ -398,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 // row = sorted position; columns j (gate) and 128+j (up) of h column ncol0+j
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.inter) + (size_t)(tl.xrow + row) * a.N + tl.ncol0;
                 const float sx = QT ? a.x_scales[tl.xrow + row] : 1.0f;
+                float hmax = 0.0f;  // per-token FP8: max |h| of the row's 128 columns here
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     float g[32], u[32], h[32];
@@ -415,6 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         h[i] = silu(g[i]) * u[i];
+                    if (QT)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            hmax = fmaxf(hmax, fabsf(h[i]));
                     store_bf16x32(dst + c0, h);
                     if (a.gu) {  // training: keep the pre-activations for the backward
                         __nv_bfloat16 *gr = a.gu + (size_t)(tl.xrow + row) * (2 * a.N) + tl.ncol0 + c0;
@@ -422,6 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         store_bf16x32(gr + a.N, u);
                     }
                 }
+                // the row's max |h| as the quantiser will see it (bf16 rounding is monotonic, so the
+                // rounded maximum is the maximum of the rounded values); non-negative floats order
+                // as their bits
+                if (QT && a.row_amax)
+                    atomicMax(reinterpret_cast<int *>(a.row_amax) + tl.xrow + row,
+                              __float_as_int(__bfloat162float(__float2bfloat16_rn(hmax))));
             } else if (MODE == MOE_MODE_GROUPED && STAGE == 3) {
                 // backward of stage 2 (dh = dY W_down): SwiGLU's backward with the saved g | u,
                 // dg = dh u silu'(g), du = dh silu(g), into dgu (g part at column c, u part at I + c)

@@ -145,7 +145,12 @@ void launch_quant_act(const __nv_bfloat16 *X, int64_t R, int C, uint8_t *q, floa
 // sorted_ids (token = slot / k, padding -> zero row) when it is non-null;
 // the row count read from nrows (device) when non-null, else R.
 cudaError_t launch_quant_rows(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
-                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st);
+                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st,
+                              float *zero_rows = nullptr);
+// Rows [nrows][C] whose max |v| is known (row_amax, e.g. from the GEMM that wrote them): codes and
+// scales as launch_quant_rows gives for the same rows, in one pass.
+cudaError_t launch_quant_rows_amax(const __nv_bfloat16 *X, const float *row_amax, const int32_t *nrows, int64_t R,
+                                   int C, uint8_t *q, float *s, bool pdl, cudaStream_t st);
 void launch_quant_weights(const __nv_bfloat16 *W, int64_t R, int C, uint8_t *q, float *s, cudaStream_t st);
 
 // out[t] = sum_j Y[t*k+j] (j ascending), fp32 -> bf16.
@@ -185,6 +190,8 @@ struct GemmArgs {
     // outputs
     void *inter;             // stage 1: [P_max][I] bf16 or e4m3
     float *inter_scales;     // stage 1 FP8: [I/128][P_max]
+    float *row_amax;         // per-token FP8 stage 1 (one-SM grouped): max |h| of each row (bf16-rounded),
+                             // by atomicMax on the bits; zeroed by the activation quantiser before
     __nv_bfloat16 *y;        // stage 2: [S][H] bf16, each row its weighted fp32 result rounded once
     float *partials;         // stage 2 split-K: [split][P_max][H]
     int *status;

@@ -1298,12 +1298,15 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16 *__
                                                         const int32_t *__restrict__ sorted_ids,
                                                         const int32_t *__restrict__ nrows, int64_t R, int S,
                                                         int k, int C, uint8_t *__restrict__ q,
-                                                        float *__restrict__ s)
+                                                        float *__restrict__ s, float *__restrict__ zero_rows)
 {
     __shared__ float s_red[8];
     pdl_wait();
     pdl_trigger();
     const int64_t rows = nrows ? (int64_t)*nrows : R;
+    if (zero_rows && threadIdx.x == 0)
+        for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
+            zero_rows[r] = 0.0f;
     const int nvec = C / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -1372,22 +1375,59 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16 *__
 }
 
 cudaError_t launch_quant_rows(const __nv_bfloat16 *X, const int32_t *sorted_ids, const int32_t *nrows, int64_t R,
-                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st)
+                              int S, int k, int C, uint8_t *q, float *s, bool pdl, cudaStream_t st, float *zero_rows)
 {
     int64_t grid = R < 16384 ? R : 16384;
     if (grid < 1)
         return cudaSuccess;
     if (C <= 256 * 8 * 2)
         return launch_kernel(pdl, quant_rows_kernel<2>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows,
-                             R, S, k, C, q, s);
+                             R, S, k, C, q, s, zero_rows);
     if (C <= 256 * 8 * 4)
         return launch_kernel(pdl, quant_rows_kernel<4>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows,
-                             R, S, k, C, q, s);
+                             R, S, k, C, q, s, zero_rows);
     if (C <= 256 * 8 * 8)
         return launch_kernel(pdl, quant_rows_kernel<8>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows,
-                             R, S, k, C, q, s);
+                             R, S, k, C, q, s, zero_rows);
     return launch_kernel(pdl, quant_rows_kernel<0>, dim3((unsigned)grid), dim3(256), 0, st, X, sorted_ids, nrows, R,
-                         S, k, C, q, s);
+                         S, k, C, q, s, zero_rows);
+}
+
+// Rows whose max |v| is already known (the per-token FP8 intermediate: the stage-1 epilogue takes
+// each row's max |h| by atomicMax): no reduction, so no barrier between a row's loads and its
+// codes; a CTA streams whole rows, several 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256) quant_rows_amax_kernel(const __nv_bfloat16 *__restrict__ X,
+                                                             const float *__restrict__ row_amax,
+                                                             const int32_t *__restrict__ nrows, int C,
+                                                             uint8_t *__restrict__ q, float *__restrict__ s)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t rows = *nrows;
+    const int nvec = C / 8;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float sc = group_scale(row_amax[r]);
+        const uint4 *src = reinterpret_cast<const uint4 *>(X + r * C);
+        uint2 *dst = reinterpret_cast<uint2 *>(q + r * C);
+#pragma unroll 4
+        for (int c = threadIdx.x; c < nvec; c += 256) {
+            float f[8];
+            bf16x8_to_float(__ldg(src + c), f);
+            dst[c] = encode8(f, sc);
+        }
+        if (threadIdx.x == 0)
+            s[r] = sc;
+    }
+}
+
+cudaError_t launch_quant_rows_amax(const __nv_bfloat16 *X, const float *row_amax, const int32_t *nrows, int64_t R,
+                                   int C, uint8_t *q, float *s, bool pdl, cudaStream_t st)
+{
+    const int64_t grid = R < 16384 ? R : 16384;
+    if (grid < 1)
+        return cudaSuccess;
+    return launch_kernel(pdl, quant_rows_amax_kernel, dim3((unsigned)grid), dim3(256), 0, st, X, row_amax, nrows, C,
+                         q, s);
 }
 
 // One CTA per 128x128 block of W [R][C]: amax over the block, then codes.
